@@ -1,0 +1,23 @@
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (runs the CUDA path through the C-ABI)")
+    config.addinivalue_line("markers", "slow: long CPU-only check, skipped unless selected with -m slow")
+
+
+def pytest_collection_modifyitems(config, items):
+    markexpr = config.getoption("-m") or ""
+    if "slow" in markexpr:
+        return
+    skip = pytest.mark.skip(reason="slow: select with -m slow")
+    for item in items:
+        if "slow" in item.keywords:
+            item.add_marker(skip)
