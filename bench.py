@@ -1,0 +1,438 @@
+"""Benchmark of the sharded optimizer step on the Llama-style 7B rank view.
+
+Workload: one rank's shard of a Llama-7B-shaped model wrapped as 33 FSDP units
+(32 layers + embedding unit), Psi = 6,738,415,616, N_d = 8 emulated ranks, so
+the rank's shard holds S = 842,301,952 fp32 master weights + both moments and
+receives 8 bf16 gradient contributions.  One step = one fused
+reduce-scatter-average + AdamW + bf16 cast launch over the whole shard, then
+the all-gather of one 202,383,360-parameter layer unit.  Inputs are seeded
+synthetic values generated on the device before timing (no data set, no
+weights); every step consumes the resident gradients with the step count
+advancing.  The step moves ~36 GB, far more than the 129 MB L2, so no L2
+flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle on a
+bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused shard-step HBM GB/s (% of GB300 peak), params/s at Psi=7B, N_d=8"
+KERNEL_SOURCES = ["sharded_optimizer_step_gb300/csrc/step.cu",
+                  "sharded_optimizer_step_gb300/csrc/common.cuh"]
+FUSED_PROFILE = os.path.join(ROOT, "profiles", "fused_step_llama7b_rank_view.md")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=60)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------ environment
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world):
+    if world > 1:
+        import torch.distributed as dist
+        # timing control plane only (barrier + max over ranks); the data path
+        # has no collective: each GPU runs its own rank view
+        dist.init_process_group("gloo")
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def allreduce_max(world, x: float) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def allreduce_sum(world, x: float) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per fused-kernel launch recorded from an ncu capture, if the
+    capture was taken on the current kernel source (else None)."""
+    try:
+        text = open(FUSED_PROFILE).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_element:\s*([0-9.]+)", text)
+    h = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", text)
+    if not m or not h or h.group(1) != kernel_source_hash():
+        return None
+    return float(m.group(1))
+
+
+def smi_index(local: int) -> str:
+    """nvidia-smi id of this process's GPU (CUDA_VISIBLE_DEVICES may remap)."""
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    items = [x.strip() for x in vis.split(",") if x.strip()]
+    return items[local] if local < len(items) else str(local)
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons while the GPU is busy."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: str):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------ our arm
+
+def run_ours(args):
+    import torch
+    world, rank, local = dist_env()
+    init_dist(world)
+    torch.cuda.set_device(local)
+    import __graft_entry__
+    __graft_entry__.build()
+    import numpy as np
+    import sharded_optimizer_step_gb300 as ss
+    import synth
+    from sharded_optimizer_step_gb300.engine import RankShardOptimizer
+    from synth import workloads as W
+
+    w = W.llama_7b_rank_view()
+    nd = w.nd
+    r = rank % nd                       # GPU k holds rank k's view of its own replica
+    dev = torch.device("cuda", local)
+    hp = ss.AdamW(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
+    opt = RankShardOptimizer(w.units, nd, r, hp, device=dev)
+    S = opt.shard_total
+    W.dev_fill_rank_master(w, r, opt.master)
+    for q in range(nd):
+        W.dev_fill_rank_grad(w, 1, r, q, 0, opt.grad_in[q])
+    u = w.extra["ag_unit"]
+    Su, Pu = w.unit_shard(u), w.unit_padded(u)
+    peers = [torch.empty(Su, dtype=torch.bfloat16, device=dev) for _ in range(nd)]
+    for q in range(nd):
+        if q != r:
+            synth.dev_fill(w.peer_shard_stream(1, q, u), peers[q])
+    full = torch.empty(Pu, dtype=torch.bfloat16, device=dev)
+    torch.cuda.synchronize()
+
+    fused_bytes = (2 * nd + 26) * S
+    ag_bytes = 4 * Pu                     # read + write every bf16 element of the unit
+    step_bytes = fused_bytes + ag_bytes
+    stream = torch.cuda.current_stream(dev)
+
+    def one_step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        opt.step()
+        if ev is not None:
+            ev[1].record(stream)
+        opt.gather_unit(u, peers, full)
+        if ev is not None:
+            ev[2].record(stream)
+
+    clocks = ClockSampler(smi_index(local))
+    clocks.start()
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize()
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    launches0 = ss.launch_count()
+    t_start.record(stream)
+    for k in range(args.steps):
+        one_step(events[k])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    launches = ss.launch_count() - launches0
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    fused_ms = [e[0].elapsed_time(e[1]) for e in events]
+    ag_ms = [e[1].elapsed_time(e[2]) for e in events]
+    total_ms_max = allreduce_max(world, total_ms)
+    all_bytes = allreduce_sum(world, step_bytes * args.steps)
+    value = all_bytes / (total_ms_max / 1e3) / 1e9
+    ms_per_step = total_ms_max / args.steps
+    fused_avg = sum(fused_ms) / len(fused_ms)
+    peak, peak_kind = measured_peak()
+    achieved = fused_bytes / (fused_avg / 1e3) / 1e9
+    traffic_per_elem = profiled_traffic()
+
+    # end to end through the public API: pinned host inputs copied in every
+    # step, the gathered unit read back every step
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, torch, opt, peers, full, u, r, nd, stream, step_bytes)
+        e2e["value"] = allreduce_sum(world, e2e.pop("bytes")) / allreduce_max(world, e2e.pop("seconds")) / 1e9
+
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        cpu = cpu_baseline(w, r, budget_s=args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded counter-based generator on the device; no data set or weights)",
+            "config": {"workload": w.name, "model_shape": "Llama-style 7B, 32 layer units + embedding unit",
+                       "psi": w.psi, "nd": nd, "rank": r, "shard_elements": S,
+                       "grad_dtype": "bf16", "state_dtype": "f32",
+                       "ag_unit_params": Pu, "step": "fused rs_avg+AdamW+bf16 cast over the shard, then all-gather of one layer unit",
+                       "bytes_per_step": step_bytes,
+                       "l2": "no flush: each step streams ~36 GB, >> 129 MB L2"},
+            "params_per_s": round(S * world / (ms_per_step / 1e3), 1),
+            "fused_ms": round(fused_avg, 4), "ag_ms": round(sum(ag_ms) / len(ag_ms), 4),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4),
+                         "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback 6800 GB/s",
+                         "kernel": "rs_adamw_cast_vec8<8,bf16>",
+                         "algorithmic_bytes_per_launch": fused_bytes,
+                         "traffic": None if traffic_per_elem is None else round(traffic_per_elem * S)},
+            "e2e": e2e,
+            "gpu_launches": launches,
+            "clocks": clk,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_e2e(args, torch, opt, peers, full, u, r, nd, stream, step_bytes):
+    S = opt.shard_total
+    host_g = [torch.empty(S, dtype=torch.bfloat16, pin_memory=True) for _ in range(nd)]
+    for q in range(nd):
+        host_g[q].copy_(opt.grad_in[q])
+    host_p = [torch.empty(peers[0].numel(), dtype=torch.bfloat16, pin_memory=True)
+              for _ in range(nd)]
+    for q in range(nd):
+        host_p[q].copy_(peers[q])
+    host_out = torch.empty(full.numel(), dtype=torch.bfloat16, pin_memory=True)
+    torch.cuda.synchronize()
+    h2d = sum(x.numel() * 2 for x in host_g) + sum(x.numel() * 2 for q, x in enumerate(host_p)
+                                                   if q != r)
+    d2h = host_out.numel() * 2
+
+    def e2e_step():
+        for q in range(nd):
+            opt.grad_in[q].copy_(host_g[q], non_blocking=True)
+        for q in range(nd):
+            if q != r:
+                peers[q].copy_(host_p[q], non_blocking=True)
+        opt.step()
+        opt.gather_unit(u, peers, full)
+        host_out.copy_(full, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    sec = a.elapsed_time(b) / 1e3
+    return {"unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": args.e2e_steps, "ms_per_step": round(sec * 1e3 / args.e2e_steps, 3),
+            "bytes": step_bytes * args.e2e_steps, "seconds": sec,
+            "path": "torch pinned-host copies + C-ABI calls on one stream"}
+
+
+# ------------------------------------------------------- CPU baseline / reference
+
+def _oracle_sample(w, r, n, step, rng_seed=0):
+    """Inputs of a contiguous sample of n shard elements (plus the matching
+    sample of the all-gather), generated on the host."""
+    import numpy as np
+    from synth import workloads as W
+    import synth
+    start = (rng_seed * 7919 * n) % max(1, 842_301_952 - n)
+    idx = np.arange(start, start + n, dtype=np.int64)
+    contribs = [W.host_gather_rank_grad(w, step, r, q, 0, idx) for q in range(w.nd)]
+    p = W.host_gather_rank_master(w, r, idx)
+    u = w.extra["ag_unit"]
+    n_ag = max(1, n // (w.nd * 4))
+    shards = [synth.host_fill(w.peer_shard_stream(step, q, u), 0, n_ag, "bf16") for q in range(w.nd)]
+    return contribs, p, shards
+
+
+def _time_oracle(w, contribs, p, shards, t):
+    import numpy as np
+    import oracle
+    from oracle.numerics import AdamWConfig
+    hp = AdamWConfig(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
+    n = p.size
+    m = np.zeros(n, np.float32)
+    v = np.zeros(n, np.float32)
+    lay = oracle.layout([w.nd * shards[0].size], w.nd)
+    t0 = time.perf_counter()
+    oracle.fsdp_shard_step(contribs, 0, n, p, m, v, hp, t)
+    oracle.ag_unpack(shards, lay)
+    dt = time.perf_counter() - t0
+    bytes_ = (2 * w.nd + 26) * n + 4 * w.nd * shards[0].size
+    return dt, bytes_
+
+
+def cpu_baseline(w, r, budget_s=10.0, n=4_000_000):
+    contribs, p, shards = _oracle_sample(w, r, n, 1)
+    total_t, total_b, reps = 0.0, 0, 0
+    while total_t < budget_s and reps < 50:
+        dt, b = _time_oracle(w, contribs, p, shards, reps + 1)
+        total_t += dt
+        total_b += b
+        reps += 1
+    return {"value": round(total_b / total_t / 1e9, 4), "unit": "GB/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"{reps} x (fused step on {n} contiguous shard elements of the 7B rank view "
+                      f"+ all-gather of {shards[0].size * w.nd} bf16), numpy single-threaded"}
+
+
+def run_reference(args):
+    world, rank, local = dist_env()
+    if rank != 0:
+        return
+    from synth import workloads as W
+    w = W.llama_7b_rank_view()
+    r = 0
+    n = 2_000_000
+    contribs, p, shards = _oracle_sample(w, r, n, 1)
+    for k in range(args.warmup):
+        _time_oracle(w, contribs, p, shards, k + 1)
+    ts, bs = [], []
+    for k in range(args.steps):
+        dt, b = _time_oracle(w, contribs, p, shards, args.warmup + k + 1)
+        ts.append(dt)
+        bs.append(b)
+    value = sum(bs) / sum(ts) / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * sum(ts) / len(ts), 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "psi": w.psi, "nd": w.nd, "rank": r,
+                   "sample_elements_per_step": n},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"each step: fused step on {n} shard elements + all-gather of "
+                                   f"{shards[0].size * w.nd} bf16"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

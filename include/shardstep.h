@@ -1,0 +1,266 @@
+/*
+ * shardstep.h -- C ABI of libshardstep.so: the data-parallel hot path of a
+ * ZeRO / FSDP sharded optimizer step over a FlatParameter, on one GPU.
+ *
+ * N_d data-parallel ranks are emulated as N_d buffers in one GPU's memory.
+ * The reduce-scatter average, the AdamW update and the bf16 cast run as one
+ * kernel pass; the all-gather is one copy kernel; packing and the DDP-style
+ * bucketed all-reduce average are kernels of their own.
+ *
+ * Sources for what each call computes (page title, section / figure):
+ *   [P1] "Infra: Data Parallel" (pufanyi.com blog)
+ *   [P2] "PyTorch FSDP: 大模型分布式训练的工业级分片并行方案" (2048ai.net)
+ *   [P3] "4.1 数据并行详解" (AIInfraGuide)
+ *
+ * Conventions shared by every entry point
+ *   - Pointers named "device" are CUDA device addresses of the current device;
+ *     "host" pointers are ordinary host memory.  Arrays *of* device pointers
+ *     (src, grad_slices, shards, rank_grads) live in host memory.
+ *   - The caller owns every buffer.  No entry point allocates or frees device
+ *     memory, and none keeps a pointer after it returns.
+ *   - Device work is enqueued on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream) and is asynchronous: a zero return means the launch was
+ *     accepted, not that the kernel has finished.  Kernel faults surface at
+ *     the caller's next synchronisation, as usual in CUDA.
+ *   - Arguments are validated on the host before anything is launched.  On
+ *     error nothing is launched, a negative SHARDSTEP_ERR_* code is returned
+ *     and shardstep_last_error() describes it (per calling thread).  Nothing is
+ *     thrown across the ABI.
+ *   - bf16 data is passed as uint16_t bit patterns.  fp32 arithmetic is IEEE
+ *     single precision, round to nearest, with no contraction into fused
+ *     multiply-adds, in the operation order each call states.
+ *   - Every call is stateless and re-entrant; calls on different streams may
+ *     run concurrently if their buffers do not overlap.
+ */
+#ifndef SHARDSTEP_H
+#define SHARDSTEP_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------ codes */
+#define SHARDSTEP_OK 0
+#define SHARDSTEP_ERR_INVALID (-1)  /* bad pointer, size, dtype, rank or overlap */
+#define SHARDSTEP_ERR_CUDA (-3)     /* the CUDA runtime refused a launch or query */
+#define SHARDSTEP_ERR_TIMEOUT (-4)  /* a host-side wait ran past its limit */
+#define SHARDSTEP_ERR_CAPACITY (-5) /* more ranks than SHARDSTEP_MAX_ND */
+
+#define SHARDSTEP_DTYPE_BF16 0
+#define SHARDSTEP_DTYPE_F32 1
+
+#define SHARDSTEP_MAX_ND 64 /* largest N_d a kernel accepts */
+
+/* ------------------------------------------------------------ types */
+
+/* AdamW hyper-parameters and the 1-based step count t.  The per-step fp32
+ * scalars are derived on the host in double and rounded once to fp32:
+ *   lr*wd, beta1, 1-beta1, beta2, 1-beta2, lr/bc1, sqrt(bc2), eps
+ * with bc_i = 1 - beta_i^t, beta_i^t a left-to-right product of t factors. */
+typedef struct {
+    double lr;
+    double beta1;
+    double beta2;
+    double eps;
+    double weight_decay;
+    int64_t step;
+} shardstep_adamw_t;
+
+/* Sizes of a FlatParameter layout (see fsdp_layout). */
+typedef struct {
+    int64_t total;  /* T = sum of the tensors' numels             */
+    int64_t padded; /* P = ceil(T / N_d) * N_d                     */
+    int64_t shard;  /* S = P / N_d, elements per rank              */
+    int32_t n_tensors;
+    int32_t nd;
+} shardstep_layout_info_t;
+
+/* ------------------------------------------------------ FlatParameter */
+
+/* fsdp_layout -- host only.
+ * [P1] section "FSDP1：先打包，再切分" and its figure (FlatParameter of three
+ * (4,2) weights on two ranks): the tensors of one FSDP unit are flattened and
+ * concatenated in registration order, zero-padded at the tail to a multiple
+ * of N_d, and split into N_d equal contiguous shards; a shard may cut a
+ * tensor, and with use_orig_params a rank's view of a tensor it holds
+ * nothing of is empty.
+ *   numels[n]   host: elements of each tensor (>= 0), registration order.
+ *   nd          N_d >= 1.
+ *   info        host, required: T, P, S.
+ *   offsets[n]  host or NULL: element offset of each tensor in the flat buffer.
+ *   lo, hi      host or NULL, [nd * n], row r = rank: the piece of tensor t
+ *               held by rank r is shard_r[lo[r*n+t], hi[r*n+t]) (shard
+ *               coordinates, the tensor's overlap with [r*S, (r+1)*S) clamped
+ *               to [0, S]); lo == hi when the rank holds nothing of it.
+ * Errors: INVALID for n < 0, nd < 1, a negative numel, or a NULL array with
+ * n > 0. */
+int fsdp_layout(const int64_t* numels, int32_t n, int32_t nd, shardstep_layout_info_t* info,
+                int64_t* offsets, int64_t* lo, int64_t* hi);
+
+/* fsdp_flat_pack -- device.
+ * Same source as fsdp_layout.  Writes flat[off_t + k] = src[t][k] for every
+ * tensor t (a bit copy of contiguous row-major data) and flat[T..P) = 0.
+ *   src[n]      host array of device pointers, one contiguous tensor each
+ *               (may be NULL when numels[t] == 0).
+ *   numels[n]   host, as in fsdp_layout.
+ *   dtype       SHARDSTEP_DTYPE_BF16 (2-byte elements) or _F32 (4-byte).
+ *   flat        device, P elements, must not overlap any source.
+ * Any alignment is accepted; 16-byte-congruent source/destination pairs use
+ * 16-byte accesses. */
+int fsdp_flat_pack(const void* const* src, const int64_t* numels, int32_t n, int32_t nd,
+                   int32_t dtype, void* flat, void* stream);
+
+/* fsdp_views -- host only.
+ * The use_orig_params views of [P1] section "FSDP1：先打包，再切分": per tensor,
+ * the address and element count of its piece inside a buffer laid out by
+ * fsdp_layout.  rank < 0: `base` is the full flat buffer of P elements (after
+ * fsdp_ag_unpack), every tensor's view is whole and the padding is in none.
+ * rank r >= 0: `base` is rank r's shard of S elements and each view is the
+ * (possibly empty) piece the rank holds; an empty view has count 0 and the
+ * address of shard position lo.
+ *   elem_size   bytes per element (2 or 4).
+ *   ptrs[n], counts[n]  host outputs. */
+int fsdp_views(const int64_t* numels, int32_t n, int32_t nd, int32_t rank, void* base,
+               int32_t elem_size, void** ptrs, int64_t* counts);
+
+/* ----------------------------------------------------- accumulation */
+
+/* fsdp_grad_accumulate -- device.
+ * [P1] section "Naïve Data Parallelism": with gradient accumulation over M
+ * micro-batches the gradients are summed locally and only the last
+ * micro-batch synchronises; each micro-batch loss is divided by M, which
+ * scales its gradient by 1/M.  Per element, in fp32:
+ *     first != 0:  acc[i] = g[i] * scale
+ *     first == 0:  acc[i] = acc[i] + g[i] * scale
+ * where g is upcast from bf16 exactly and `scale` is the fp32 value of 1/M.
+ *   g     device, n bf16.      acc  device, n fp32 (read unless first).
+ * g and acc must not overlap. */
+int fsdp_grad_accumulate(const uint16_t* g, float* acc, int64_t n, float scale, int32_t first,
+                         void* stream);
+
+/* ------------------------------------------------- the fused step */
+
+/* fsdp_rs_avg_adamw_cast -- device, one kernel pass.
+ * Rank r's part of a ZeRO / FSDP optimizer step: [P1] ZeRO section (reduce-
+ * scatter with averaging hands each rank its part of the averaged gradient;
+ * AdamW is elementwise so the rank updates only its shard and its moments);
+ * [P3] section 2 (the mean of the N_d local-mean gradients is the global
+ * gradient); [P2] section 3.5 (one high-to-low cast; communication in low
+ * precision, so the cast precedes the all-gather).  Per shard element i:
+ *     g  = (((G_0[i] + G_1[i]) + G_2[i]) + ... + G_{N_d-1}[i]) / N_d
+ *          (fp32, rank order; G_q upcast exactly from bf16, or fp32 when
+ *           micro-batches were accumulated; a power-of-two N_d multiplies by
+ *           the exact reciprocal, which gives the same result)
+ *     p  = p - (lr*wd) * p
+ *     m  = beta1 * m + (1-beta1) * g
+ *     v  = beta2 * v + ((1-beta2) * g) * g
+ *     p  = p - ((lr/bc1) * m) / (sqrt(v) / sqrt(bc2) + eps)
+ *     out[i] = bf16(p), round to nearest even
+ *   grad_slices[nd]  host array of device pointers: grad_slices[q] is rank
+ *                    q's contribution to this rank's shard, S elements of
+ *                    grad_dtype (i.e. rank q's flat gradient + r*S).
+ *   grad_dtype       SHARDSTEP_DTYPE_BF16 or _F32.
+ *   nd               1 <= N_d <= SHARDSTEP_MAX_ND (N_d = 1 is a plain,
+ *                    unsharded AdamW + cast over S elements).
+ *   master, m, v     device, S fp32 each, updated in place.
+ *   out_bf16         device, S bf16; may be the rank's slot of the full flat
+ *                    parameter buffer (full + r*S).
+ * The gradient inputs must not overlap any output; master, m, v and out_bf16
+ * must not overlap one another.  Any alignment is accepted; when every
+ * pointer is 16-byte aligned the kernel moves 16 bytes per access.
+ * Errors: INVALID (null pointer, S < 0, step < 1, bad dtype, overlap),
+ * CAPACITY (nd > SHARDSTEP_MAX_ND), CUDA (launch refused). */
+int fsdp_rs_avg_adamw_cast(const void* const* grad_slices, int32_t grad_dtype, int32_t nd,
+                           int64_t S, float* master, float* m, float* v, uint16_t* out_bf16,
+                           const shardstep_adamw_t* hp, void* stream);
+
+/* ------------------------------------------------------ all-gather */
+
+/* fsdp_ag_unpack -- device, one kernel.
+ * [P1] ZeRO section and [P2] section 3.1: after the update each rank's bf16
+ * shard is all-gathered so every rank holds the whole unit again; [P3]
+ * section 5.1: all-gather concatenates the per-rank pieces.
+ *     full[q*S + i] = shards[q][i]     for q < N_d, i < S
+ * Use fsdp_views(rank = -1) for the per-tensor views of `full`.
+ *   shards[nd]  host array of device pointers, S bf16 each.  shards[q] may
+ *               equal full + q*S (that copy is skipped); otherwise no shard
+ *               may overlap `full`.
+ *   full        device, nd*S bf16. */
+int fsdp_ag_unpack(const uint16_t* const* shards, int32_t nd, int64_t S, uint16_t* full,
+                   void* stream);
+
+/* ---------------------------------------------------- DDP buckets */
+
+/* ddp_bucket_plan -- host only.
+ * [P3] section 4.2: gradients are grouped into buckets in the order backward
+ * produces them (reverse registration order), capped at bucket_cap_mb
+ * (~25 MB by default).  Rule used: walk the parameters in reverse order; close
+ * the open bucket before a parameter that would take it past cap_bytes; a
+ * parameter larger than the cap gets a bucket of its own; parameters are never
+ * split; zero-size parameters join the open bucket.
+ *   numels[n]          host, registration order.
+ *   elem_size          bytes per gradient element (> 0).
+ *   cap_bytes          > 0.
+ *   param_offset[n]    host out: element offset of each parameter in the
+ *                      bucketed flat buffer (buckets back to back).
+ *   bucket_of_param[n] host out.
+ *   bucket_offsets     host out, n + 1 entries available; the first
+ *                      n_buckets + 1 are the buckets' element offsets.
+ *   n_buckets          host out. */
+int ddp_bucket_plan(const int64_t* numels, int32_t n, int32_t elem_size, int64_t cap_bytes,
+                    int64_t* param_offset, int32_t* bucket_of_param, int64_t* bucket_offsets,
+                    int32_t* n_buckets);
+
+/* ddp_bucket_allreduce_avg -- device, one launch per bucket.
+ * [P1] section "Naïve Data Parallelism" and [P3] section 4.2: each bucket's
+ * gradients are all-reduce-averaged over the N_d ranks; the all-reduce keeps
+ * the bf16 dtype, so for every element k of buckets first..first+count-1:
+ *     out[k] = bf16((((G_0[k] + G_1[k]) + ...) + G_{N_d-1}[k]) / N_d)
+ * with the sum in fp32, rank order.  Follow with fsdp_rs_avg_adamw_cast at
+ * nd = 1 on the averaged gradient for the replicated (unsharded) update.
+ *   rank_grads[nd]     host array of device pointers, bucketed flat gradient
+ *                      of each rank (bf16).
+ *   bucket_offsets     host, element offsets from ddp_bucket_plan.
+ *   first, count       the buckets to reduce (a bucket is reduced as soon as
+ *                      it is ready, so callers may go bucket by bucket).
+ *   out                device bf16, same indexing as the rank buffers; must
+ *                      not overlap them. */
+int ddp_bucket_allreduce_avg(const uint16_t* const* rank_grads, int32_t nd,
+                             const int64_t* bucket_offsets, int32_t first, int32_t count,
+                             uint16_t* out, void* stream);
+
+/* --------------------------------------------------------- ledger */
+
+/* Model-state bytes per GPU ([P1] ZeRO figure; [P3] section 7), 16-bit
+ * parameters and gradients, k bytes of optimizer state per parameter:
+ *   stage 0: 2Ψ + 2Ψ + kΨ          stage 1: 2Ψ + 2Ψ + kΨ/N_d
+ *   stage 2: 2Ψ + (2Ψ + kΨ)/N_d    stage 3: (2Ψ + 2Ψ + kΨ)/N_d
+ * Returns a negative value for a bad stage or nd < 1. */
+double shardstep_state_bytes(double psi, int32_t nd, int32_t stage, double k);
+
+/* Bytes sent per GPU for one step's communication ([P1] ZeRO section; [P3]
+ * sections 5 and 8), ring model, 16-bit elements; `exact` keeps the
+ * (N_d-1)/N_d factor the pages drop. */
+#define SHARDSTEP_COMM_REDUCE_SCATTER 0 /* 2Ψ                  */
+#define SHARDSTEP_COMM_ALL_GATHER 1     /* 2Ψ                  */
+#define SHARDSTEP_COMM_ALL_REDUCE 2     /* 4Ψ (naive DP / DDP) */
+#define SHARDSTEP_COMM_ZERO1 3          /* 4Ψ                  */
+#define SHARDSTEP_COMM_ZERO2 4          /* 4Ψ                  */
+#define SHARDSTEP_COMM_ZERO3 5          /* 6Ψ                  */
+double shardstep_comm_bytes(double psi, int32_t nd, int32_t kind, int32_t exact);
+
+/* ------------------------------------------------------------ misc */
+
+/* Description of the last error on the calling thread ("" if none). */
+const char* shardstep_last_error(void);
+
+/* Kernels this library has launched in this process (all threads). */
+uint64_t shardstep_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SHARDSTEP_H */

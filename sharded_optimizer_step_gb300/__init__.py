@@ -1,0 +1,265 @@
+"""sharded_optimizer_step_gb300 -- the data-parallel hot path of a ZeRO / FSDP
+sharded optimizer step over a FlatParameter, as hand-written sm_103a CUDA
+kernels behind the C ABI of include/shardstep.h.
+
+This module is argument marshalling only: every step of the path runs in
+libshardstep.so.  PyTorch supplies device memory and streams.  Each function
+enqueues work on torch's current CUDA stream (or ``stream=``) and returns
+without synchronising.
+
+N_d data-parallel ranks are emulated as N_d buffers in one GPU's memory.
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+
+from . import _capi
+from ._capi import ShardstepError, AdamWHP, MAX_ND
+from .build import build
+
+__all__ = [
+    "build", "ShardstepError", "AdamW", "Layout", "fsdp_layout", "fsdp_flat_pack", "fsdp_views",
+    "fsdp_grad_accumulate", "fsdp_rs_avg_adamw_cast", "fsdp_ag_unpack", "ddp_bucket_plan",
+    "ddp_bucket_allreduce_avg", "state_bytes", "comm_bytes", "launch_count", "MAX_ND",
+]
+
+
+@dataclass
+class AdamW:
+    """AdamW hyper-parameters (decoupled weight decay, bias-corrected moments)."""
+    lr: float = 1e-3
+    beta1: float = 0.9
+    beta2: float = 0.999
+    eps: float = 1e-8
+    weight_decay: float = 0.01
+
+    def at_step(self, step: int) -> AdamWHP:
+        return AdamWHP(self.lr, self.beta1, self.beta2, self.eps, self.weight_decay, int(step))
+
+
+@dataclass
+class Layout:
+    numels: list
+    nd: int
+    total: int
+    padded: int
+    shard: int
+    offsets: list
+    lo: list   # lo[r][t]
+    hi: list   # hi[r][t]
+
+
+def _stream(stream, device=None):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _dtype_code(t):
+    import torch
+    if t.dtype == torch.bfloat16:
+        return _capi.DTYPE_BF16
+    if t.dtype == torch.float32:
+        return _capi.DTYPE_F32
+    raise TypeError(f"unsupported dtype {t.dtype} (bf16 or fp32)")
+
+
+def _need_cuda(*tensors):
+    for t in tensors:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError("expected CUDA tensors")
+        if not t.is_contiguous():
+            raise ValueError("expected contiguous tensors")
+
+
+# ---------------------------------------------------------------- layout
+
+def fsdp_layout(numels, nd: int) -> Layout:
+    """FlatParameter layout of one FSDP unit (host only)."""
+    L = _capi.lib()
+    n = len(numels)
+    info = _capi.LayoutInfo()
+    off = (_capi.c_i64 * max(1, n))()
+    lo = (_capi.c_i64 * max(1, n * max(nd, 1)))()
+    hi = (_capi.c_i64 * max(1, n * max(nd, 1)))()
+    _capi.check("fsdp_layout", L.fsdp_layout(_capi.i64_array(numels), n, nd, ctypes.byref(info),
+                                             off, lo, hi))
+    return Layout(list(int(x) for x in numels), nd, info.total, info.padded, info.shard,
+                  list(off[:n]), [list(lo[r * n:(r + 1) * n]) for r in range(nd)],
+                  [list(hi[r * n:(r + 1) * n]) for r in range(nd)])
+
+
+def fsdp_flat_pack(tensors, nd: int, flat=None, stream=None):
+    """Flatten + concatenate + zero-pad one unit's tensors (all bf16 or all
+    fp32) into ``flat`` (allocated with torch if None).  Returns flat."""
+    import torch
+    if not tensors:
+        raise ValueError("empty unit")
+    dt = tensors[0].dtype
+    if any(t.dtype != dt for t in tensors):
+        raise TypeError("one dtype per unit")
+    _need_cuda(*tensors)
+    numels = [t.numel() for t in tensors]
+    lay = fsdp_layout(numels, nd)
+    if flat is None:
+        flat = torch.empty(lay.padded, dtype=dt, device=tensors[0].device)
+    _need_cuda(flat)
+    if flat.dtype != dt or flat.numel() != lay.padded:
+        raise ValueError(f"flat must be {dt} with {lay.padded} elements")
+    L = _capi.lib()
+    _capi.check("fsdp_flat_pack", L.fsdp_flat_pack(
+        _capi.ptr_array([t.data_ptr() for t in tensors]), _capi.i64_array(numels), len(tensors),
+        nd, _dtype_code(flat), ctypes.c_void_p(flat.data_ptr()), _stream(stream, flat.device)))
+    return flat
+
+
+def fsdp_views(buf, shapes, nd: int, rank: int = -1):
+    """Per-tensor views into ``buf``: the full flat buffer (rank < 0, views
+    reshaped to ``shapes``) or rank ``rank``'s shard (1-D pieces, possibly
+    empty), as use_orig_params exposes them."""
+    L = _capi.lib()
+    numels = []
+    for s in shapes:
+        n = 1
+        for d in s:
+            n *= int(d)
+        numels.append(n)
+    n = len(numels)
+    ptrs = (_capi.c_vp * max(1, n))()
+    counts = (_capi.c_i64 * max(1, n))()
+    es = buf.element_size()
+    _capi.check("fsdp_views", L.fsdp_views(_capi.i64_array(numels), n, nd, rank,
+                                           ctypes.c_void_p(buf.data_ptr()), es, ptrs, counts))
+    views = []
+    base = buf.data_ptr()
+    for t in range(n):
+        off = ((ptrs[t] or 0) - base) // es
+        v = buf[off:off + counts[t]]
+        views.append(v.view(tuple(shapes[t])) if rank < 0 else v)
+    return views
+
+
+# ---------------------------------------------------------- accumulation
+
+def fsdp_grad_accumulate(g, acc, scale: float, first: bool, stream=None):
+    """acc = g*scale (first) or acc + g*scale; g bf16, acc fp32, same numel."""
+    import torch
+    _need_cuda(g, acc)
+    if g.dtype != torch.bfloat16 or acc.dtype != torch.float32 or g.numel() != acc.numel():
+        raise ValueError("g must be bf16 and acc fp32 with the same numel")
+    _capi.check("fsdp_grad_accumulate", _capi.lib().fsdp_grad_accumulate(
+        ctypes.c_void_p(g.data_ptr()), ctypes.c_void_p(acc.data_ptr()), g.numel(),
+        ctypes.c_float(scale), int(bool(first)), _stream(stream, g.device)))
+
+
+# --------------------------------------------------------- the fused step
+
+def fsdp_rs_avg_adamw_cast(grad_slices, master, m, v, out_bf16, hp: AdamW, step: int,
+                           stream=None):
+    """Reduce-scatter average of the N_d gradient slices, AdamW on the fp32
+    shard (in place) and the bf16 cast into ``out_bf16``, in one kernel pass.
+    ``grad_slices[q]`` is rank q's contribution to this shard (S elements,
+    all bf16 or all fp32)."""
+    import torch
+    if not grad_slices:
+        raise ValueError("need at least one gradient slice")
+    _need_cuda(*grad_slices, master, m, v, out_bf16)
+    S = master.numel()
+    gd = grad_slices[0].dtype
+    for g in grad_slices:
+        if g.dtype != gd or g.numel() != S:
+            raise ValueError("gradient slices must share dtype and have S elements")
+    for t in (m, v):
+        if t.dtype != torch.float32 or t.numel() != S:
+            raise ValueError("master / m / v must be fp32 with S elements")
+    if master.dtype != torch.float32 or out_bf16.dtype != torch.bfloat16 or out_bf16.numel() != S:
+        raise ValueError("master fp32 and out bf16 with S elements")
+    hpc = hp.at_step(step)
+    _capi.check("fsdp_rs_avg_adamw_cast", _capi.lib().fsdp_rs_avg_adamw_cast(
+        _capi.ptr_array([g.data_ptr() for g in grad_slices]), _dtype_code(grad_slices[0]),
+        len(grad_slices), S, ctypes.c_void_p(master.data_ptr()), ctypes.c_void_p(m.data_ptr()),
+        ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(out_bf16.data_ptr()), ctypes.byref(hpc),
+        _stream(stream, master.device)))
+
+
+# ------------------------------------------------------------- all-gather
+
+def fsdp_ag_unpack(shards, full, stream=None):
+    """full[q*S:(q+1)*S] = shards[q] for every rank q (bf16).  A shard that
+    already is its slot of ``full`` is not copied."""
+    import torch
+    _need_cuda(*shards, full)
+    nd = len(shards)
+    S = shards[0].numel()
+    if any(s.numel() != S or s.dtype != torch.bfloat16 for s in shards):
+        raise ValueError("shards must be bf16 with equal numel")
+    if full.dtype != torch.bfloat16 or full.numel() != nd * S:
+        raise ValueError("full must be bf16 with nd*S elements")
+    _capi.check("fsdp_ag_unpack", _capi.lib().fsdp_ag_unpack(
+        _capi.ptr_array([s.data_ptr() for s in shards]), nd, S, ctypes.c_void_p(full.data_ptr()),
+        _stream(stream, full.device)))
+    return full
+
+
+# ----------------------------------------------------------- DDP buckets
+
+def ddp_bucket_plan(numels, elem_size: int, cap_bytes: int):
+    """Greedy reverse-order buckets.  Returns (param_offset, bucket_of_param,
+    bucket_offsets) as lists; bucket_offsets has n_buckets + 1 entries."""
+    L = _capi.lib()
+    n = len(numels)
+    off = (_capi.c_i64 * max(1, n))()
+    of = (_capi.c_i32 * max(1, n))()
+    boff = (_capi.c_i64 * (n + 1))()
+    nb = _capi.c_i32(0)
+    _capi.check("ddp_bucket_plan", L.ddp_bucket_plan(_capi.i64_array(numels), n, elem_size,
+                                                     cap_bytes, off, of, boff, ctypes.byref(nb)))
+    return list(off[:n]), list(of[:n]), list(boff[:nb.value + 1])
+
+
+def ddp_bucket_allreduce_avg(rank_grads, bucket_offsets, out, first: int = 0,
+                             count: int | None = None, stream=None):
+    """Bucket-by-bucket all-reduce average of the ranks' bf16 gradients into
+    ``out`` (one kernel launch per non-empty bucket)."""
+    import torch
+    _need_cuda(*rank_grads, out)
+    if any(g.dtype != torch.bfloat16 for g in rank_grads) or out.dtype != torch.bfloat16:
+        raise ValueError("bf16 gradients")
+    nb = len(bucket_offsets) - 1
+    if count is None:
+        count = nb - first
+    if first < 0 or count < 0 or first + count > nb:
+        raise ValueError("bucket range out of bounds")
+    total = bucket_offsets[first + count] if nb >= 0 else 0
+    if out.numel() < total or any(g.numel() < total for g in rank_grads):
+        raise ValueError("buffers shorter than the bucketed range")
+    _capi.check("ddp_bucket_allreduce_avg", _capi.lib().ddp_bucket_allreduce_avg(
+        _capi.ptr_array([g.data_ptr() for g in rank_grads]), len(rank_grads),
+        _capi.i64_array(bucket_offsets), first, count, ctypes.c_void_p(out.data_ptr()),
+        _stream(stream, out.device)))
+    return out
+
+
+# ---------------------------------------------------------------- ledger
+
+def state_bytes(psi: float, nd: int, stage: int, k: float = 12.0) -> float:
+    r = _capi.lib().shardstep_state_bytes(psi, nd, stage, k)
+    if r < 0:
+        raise ValueError("bad stage or nd")
+    return r
+
+
+def comm_bytes(psi: float, nd: int, kind: str, exact: bool = False) -> float:
+    r = _capi.lib().shardstep_comm_bytes(psi, nd, _capi.COMM_KINDS[kind], int(exact))
+    if r < 0:
+        raise ValueError("bad kind or nd")
+    return r
+
+
+def launch_count() -> int:
+    """Kernels libshardstep has launched in this process."""
+    return int(_capi.lib().shardstep_launch_count())

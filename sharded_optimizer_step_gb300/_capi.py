@@ -1,0 +1,100 @@
+"""ctypes declarations of libshardstep.so (include/shardstep.h).
+
+Loading fails loudly when the library has not been built: there is no
+fallback implementation of any entry point."""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+c_i32, c_i64, c_u64, c_f32, c_f64, c_vp = (ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64,
+                                           ctypes.c_float, ctypes.c_double, ctypes.c_void_p)
+P_i64 = ctypes.POINTER(ctypes.c_int64)
+P_i32 = ctypes.POINTER(ctypes.c_int32)
+P_vp = ctypes.POINTER(ctypes.c_void_p)
+
+OK = 0
+ERR_INVALID = -1
+ERR_CUDA = -3
+ERR_TIMEOUT = -4
+ERR_CAPACITY = -5
+DTYPE_BF16 = 0
+DTYPE_F32 = 1
+MAX_ND = 64
+COMM_KINDS = {"reduce_scatter": 0, "all_gather": 1, "all_reduce": 2, "ddp": 2,
+              "zero1": 3, "zero2": 4, "zero3": 5}
+
+
+class AdamWHP(ctypes.Structure):
+    _fields_ = [("lr", c_f64), ("beta1", c_f64), ("beta2", c_f64), ("eps", c_f64),
+                ("weight_decay", c_f64), ("step", c_i64)]
+
+
+class LayoutInfo(ctypes.Structure):
+    _fields_ = [("total", c_i64), ("padded", c_i64), ("shard", c_i64), ("n_tensors", c_i32),
+                ("nd", c_i32)]
+
+
+# name -> (restype, argtypes), exactly the declarations of include/shardstep.h
+SIGNATURES = {
+    "fsdp_layout": (c_i32, [P_i64, c_i32, c_i32, ctypes.POINTER(LayoutInfo), P_i64, P_i64, P_i64]),
+    "fsdp_flat_pack": (c_i32, [P_vp, P_i64, c_i32, c_i32, c_i32, c_vp, c_vp]),
+    "fsdp_views": (c_i32, [P_i64, c_i32, c_i32, c_i32, c_vp, c_i32, P_vp, P_i64]),
+    "fsdp_grad_accumulate": (c_i32, [c_vp, c_vp, c_i64, c_f32, c_i32, c_vp]),
+    "fsdp_rs_avg_adamw_cast": (c_i32, [P_vp, c_i32, c_i32, c_i64, c_vp, c_vp, c_vp, c_vp,
+                                       ctypes.POINTER(AdamWHP), c_vp]),
+    "fsdp_ag_unpack": (c_i32, [P_vp, c_i32, c_i64, c_vp, c_vp]),
+    "ddp_bucket_plan": (c_i32, [P_i64, c_i32, c_i32, c_i64, P_i64, P_i32, P_i64, P_i32]),
+    "ddp_bucket_allreduce_avg": (c_i32, [P_vp, c_i32, P_i64, c_i32, c_i32, c_vp, c_vp]),
+    "shardstep_state_bytes": (c_f64, [c_f64, c_i32, c_i32, c_f64]),
+    "shardstep_comm_bytes": (c_f64, [c_f64, c_i32, c_i32, c_i32]),
+    "shardstep_last_error": (ctypes.c_char_p, []),
+    "shardstep_launch_count": (c_u64, []),
+}
+
+_lib = None
+
+
+class ShardstepError(RuntimeError):
+    def __init__(self, name, code, msg):
+        super().__init__(f"{name} failed ({code}): {msg}")
+        self.code = code
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """The loaded library.  Raises if it was not built (call ``build()``)."""
+    global _lib
+    if _lib is None:
+        path = lib_path()
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: the CUDA library has not been built "
+                "(run sharded_optimizer_step_gb300.build()); there is no fallback")
+        L = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def check(name: str, rc: int) -> None:
+    if rc != OK:
+        raise ShardstepError(name, rc, lib().shardstep_last_error().decode())
+
+
+def i64_array(values):
+    values = [int(x) for x in values]
+    return (c_i64 * max(1, len(values)))(*values)
+
+
+def ptr_array(ptrs):
+    ptrs = [int(p) if p is not None else 0 for p in ptrs]
+    return (c_vp * max(1, len(ptrs)))(*ptrs)

@@ -1,0 +1,474 @@
+// Host side of the C ABI declared in include/shardstep.h: argument checks,
+// FlatParameter layout and bucket planning, the AdamW scalar derivation, and
+// dispatch to the kernels.  Nothing here allocates device memory.
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "internal.h"
+#include "shardstep.h"
+
+namespace shardstep {
+namespace {
+
+thread_local std::string g_error;
+std::atomic<uint64_t> g_launches{0};
+
+int fail(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_error = buf;
+    return code;
+}
+
+int ok() {
+    g_error.clear();
+    return SHARDSTEP_OK;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+    return fail(SHARDSTEP_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+struct Span {
+    uintptr_t lo, hi;  // [lo, hi); empty spans never overlap anything
+};
+Span span(const void* p, int64_t bytes) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    return Span{a, a + static_cast<uintptr_t>(bytes > 0 ? bytes : 0)};
+}
+bool overlap(Span a, Span b) {
+    return a.lo < a.hi && b.lo < b.hi && a.lo < b.hi && b.lo < a.hi;
+}
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int elem_size_of(int32_t dtype) {
+    return dtype == SHARDSTEP_DTYPE_BF16 ? 2 : dtype == SHARDSTEP_DTYPE_F32 ? 4 : 0;
+}
+
+MeanOp mean_op(int nd) {
+    MeanOp mo;
+    mo.nd = static_cast<float>(nd);
+    mo.pow2 = (nd & (nd - 1)) == 0;
+    mo.inv_nd = 1.0f / static_cast<float>(nd);  // exact when nd is a power of two
+    return mo;
+}
+
+// Per-step scalars: double arithmetic, one rounding to fp32 each.  beta^t is
+// the left-to-right product of t factors; once both products reach zero they
+// stay zero, so the loop stops there.
+AdamScalars adam_scalars(const shardstep_adamw_t& hp) {
+    double b1t = 1.0, b2t = 1.0;
+    for (int64_t k = 0; k < hp.step; ++k) {
+        b1t *= hp.beta1;
+        b2t *= hp.beta2;
+        if (b1t == 0.0 && b2t == 0.0) break;
+    }
+    const double bc1 = 1.0 - b1t;
+    const double bc2 = 1.0 - b2t;
+    AdamScalars c;
+    c.lr_wd = static_cast<float>(hp.lr * hp.weight_decay);
+    c.beta1 = static_cast<float>(hp.beta1);
+    c.omb1 = static_cast<float>(1.0 - hp.beta1);
+    c.beta2 = static_cast<float>(hp.beta2);
+    c.omb2 = static_cast<float>(1.0 - hp.beta2);
+    c.step_size = static_cast<float>(hp.lr / bc1);
+    c.sqrt_bc2 = static_cast<float>(std::sqrt(bc2));
+    c.eps = static_cast<float>(hp.eps);
+    return c;
+}
+
+// Layout arithmetic shared by fsdp_layout / fsdp_flat_pack / fsdp_views.
+int compute_layout(const int64_t* numels, int32_t n, int32_t nd, shardstep_layout_info_t* info,
+                   int64_t* offsets) {
+    if (n < 0) return fail(SHARDSTEP_ERR_INVALID, "n_tensors must be >= 0 (got %d)", n);
+    if (nd < 1) return fail(SHARDSTEP_ERR_INVALID, "nd must be >= 1 (got %d)", nd);
+    if (n > 0 && numels == nullptr) return fail(SHARDSTEP_ERR_INVALID, "numels is NULL");
+    int64_t total = 0;
+    for (int32_t t = 0; t < n; ++t) {
+        if (numels[t] < 0)
+            return fail(SHARDSTEP_ERR_INVALID, "numel of tensor %d is negative", t);
+        if (numels[t] > INT64_MAX / 8 - total)
+            return fail(SHARDSTEP_ERR_INVALID, "unit too large");
+        if (offsets) offsets[t] = total;
+        total += numels[t];
+    }
+    const int64_t padded = (total + nd - 1) / nd * nd;
+    info->total = total;
+    info->padded = padded;
+    info->shard = padded / nd;
+    info->n_tensors = n;
+    info->nd = nd;
+    return SHARDSTEP_OK;
+}
+
+std::mutex g_occ_mu;
+struct OccEntry {
+    int dev;
+    const void* kernel;
+    int threads;
+    int blocks;
+};
+std::vector<OccEntry> g_occ;
+
+}  // namespace
+
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+int device_sms() {
+    static std::atomic<int> cache[256];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return 1;
+    int v = cache[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+        return 1;
+    cache[dev].store(sms, std::memory_order_relaxed);
+    return sms;
+}
+
+int resident_blocks(const void* kernel, int threads) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    {
+        std::lock_guard<std::mutex> lk(g_occ_mu);
+        for (const OccEntry& e : g_occ)
+            if (e.dev == dev && e.kernel == kernel && e.threads == threads) return e.blocks;
+    }
+    int blocks = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kernel, threads, 0) != cudaSuccess ||
+        blocks < 1)
+        blocks = 1;
+    std::lock_guard<std::mutex> lk(g_occ_mu);
+    g_occ.push_back(OccEntry{dev, kernel, threads, blocks});
+    return blocks;
+}
+
+}  // namespace shardstep
+
+using namespace shardstep;
+
+extern "C" {
+
+const char* shardstep_last_error(void) { return g_error.c_str(); }
+
+uint64_t shardstep_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int fsdp_layout(const int64_t* numels, int32_t n, int32_t nd, shardstep_layout_info_t* info,
+                int64_t* offsets, int64_t* lo, int64_t* hi) {
+    if (info == nullptr) return fail(SHARDSTEP_ERR_INVALID, "info is NULL");
+    std::vector<int64_t> off(n > 0 ? n : 0);
+    int rc = compute_layout(numels, n, nd, info, off.data());
+    if (rc != SHARDSTEP_OK) return rc;
+    if (offsets)
+        for (int32_t t = 0; t < n; ++t) offsets[t] = off[t];
+    const int64_t S = info->shard;
+    for (int32_t r = 0; r < nd && (lo || hi); ++r) {
+        const int64_t base = static_cast<int64_t>(r) * S;
+        for (int32_t t = 0; t < n; ++t) {
+            int64_t a = off[t] - base, b = off[t] + numels[t] - base;
+            a = a < 0 ? 0 : (a > S ? S : a);
+            b = b < 0 ? 0 : (b > S ? S : b);
+            if (lo) lo[static_cast<int64_t>(r) * n + t] = a;
+            if (hi) hi[static_cast<int64_t>(r) * n + t] = b;
+        }
+    }
+    return ok();
+}
+
+int fsdp_views(const int64_t* numels, int32_t n, int32_t nd, int32_t rank, void* base,
+               int32_t elem_size, void** ptrs, int64_t* counts) {
+    shardstep_layout_info_t info;
+    std::vector<int64_t> off(n > 0 ? n : 0);
+    int rc = compute_layout(numels, n, nd, &info, off.data());
+    if (rc != SHARDSTEP_OK) return rc;
+    if (rank >= nd) return fail(SHARDSTEP_ERR_INVALID, "rank %d >= nd %d", rank, nd);
+    if (elem_size <= 0) return fail(SHARDSTEP_ERR_INVALID, "elem_size must be > 0");
+    if (n > 0 && (ptrs == nullptr || counts == nullptr))
+        return fail(SHARDSTEP_ERR_INVALID, "ptrs / counts is NULL");
+    char* b = static_cast<char*>(base);
+    for (int32_t t = 0; t < n; ++t) {
+        if (rank < 0) {
+            ptrs[t] = b + off[t] * elem_size;
+            counts[t] = numels[t];
+        } else {
+            const int64_t S = info.shard, r0 = static_cast<int64_t>(rank) * S;
+            int64_t a = off[t] - r0, e = off[t] + numels[t] - r0;
+            a = a < 0 ? 0 : (a > S ? S : a);
+            e = e < 0 ? 0 : (e > S ? S : e);
+            ptrs[t] = b + a * elem_size;
+            counts[t] = e - a;
+        }
+    }
+    return ok();
+}
+
+// Turns (src, dst, bytes) triples into copy-kernel launches of <= kMaxCopySegs.
+namespace {
+struct CopyBatcher {
+    CopyTable t;
+    cudaStream_t stream;
+    int rc = SHARDSTEP_OK;
+    explicit CopyBatcher(cudaStream_t s) : stream(s) {
+        t.n = 0;
+        t.total_chunks = 0;
+    }
+    void add(const void* src, void* dst, int64_t bytes) {
+        if (bytes <= 0 || rc != SHARDSTEP_OK) return;
+        CopySeg& s = t.s[t.n];
+        s.src = static_cast<const char*>(src);
+        s.dst = static_cast<char*>(dst);
+        s.bytes = bytes;
+        const uintptr_t d = reinterpret_cast<uintptr_t>(dst);
+        const uintptr_t x = src ? (reinterpret_cast<uintptr_t>(src) ^ d) : 0;
+        int w = 16;
+        while (w > 1 && (x % w) != 0) w >>= 1;
+        int64_t head = static_cast<int64_t>((w - d % w) % w);
+        if (head > bytes) head = bytes;
+        s.width = w;
+        s.head = static_cast<int32_t>(head);
+        s.body = (bytes - head) / w;
+        s.chunk0 = t.total_chunks;
+        t.total_chunks += s.body > 0 ? (s.body + kCopyVecsPerChunk - 1) / kCopyVecsPerChunk : 1;
+        if (++t.n == kMaxCopySegs) flush();
+    }
+    void flush() {
+        if (t.n == 0 || rc != SHARDSTEP_OK) return;
+        cudaError_t e = launch_copy(t, stream);
+        if (e != cudaSuccess) rc = cuda_fail(e, "copy kernel launch");
+        t.n = 0;
+        t.total_chunks = 0;
+    }
+};
+}  // namespace
+
+int fsdp_flat_pack(const void* const* src, const int64_t* numels, int32_t n, int32_t nd,
+                   int32_t dtype, void* flat, void* stream) {
+    const int es = elem_size_of(dtype);
+    if (es == 0) return fail(SHARDSTEP_ERR_INVALID, "unknown dtype %d", dtype);
+    shardstep_layout_info_t info;
+    std::vector<int64_t> off(n > 0 ? n : 0);
+    int rc = compute_layout(numels, n, nd, &info, off.data());
+    if (rc != SHARDSTEP_OK) return rc;
+    if (info.padded == 0) return ok();
+    if (flat == nullptr) return fail(SHARDSTEP_ERR_INVALID, "flat is NULL");
+    if (n > 0 && src == nullptr) return fail(SHARDSTEP_ERR_INVALID, "src is NULL");
+    if (!aligned(flat, es)) return fail(SHARDSTEP_ERR_INVALID, "flat is not %d-byte aligned", es);
+    const Span fs = span(flat, info.padded * es);
+    for (int32_t t = 0; t < n; ++t) {
+        if (numels[t] == 0) continue;
+        if (src[t] == nullptr) return fail(SHARDSTEP_ERR_INVALID, "src[%d] is NULL", t);
+        if (!aligned(src[t], es))
+            return fail(SHARDSTEP_ERR_INVALID, "src[%d] is not %d-byte aligned", t, es);
+        if (overlap(span(src[t], numels[t] * es), fs))
+            return fail(SHARDSTEP_ERR_INVALID, "src[%d] overlaps flat", t);
+    }
+    CopyBatcher cb(static_cast<cudaStream_t>(stream));
+    char* f = static_cast<char*>(flat);
+    for (int32_t t = 0; t < n; ++t) cb.add(src[t], f + off[t] * es, numels[t] * es);
+    cb.add(nullptr, f + info.total * es, (info.padded - info.total) * es);
+    cb.flush();
+    return cb.rc == SHARDSTEP_OK ? ok() : cb.rc;
+}
+
+int fsdp_ag_unpack(const uint16_t* const* shards, int32_t nd, int64_t S, uint16_t* full,
+                   void* stream) {
+    if (nd < 1) return fail(SHARDSTEP_ERR_INVALID, "nd must be >= 1 (got %d)", nd);
+    if (nd > SHARDSTEP_MAX_ND)
+        return fail(SHARDSTEP_ERR_CAPACITY, "nd %d > %d", nd, SHARDSTEP_MAX_ND);
+    if (S < 0) return fail(SHARDSTEP_ERR_INVALID, "S must be >= 0");
+    if (S == 0) return ok();
+    if (shards == nullptr || full == nullptr)
+        return fail(SHARDSTEP_ERR_INVALID, "shards / full is NULL");
+    if (!aligned(full, 2)) return fail(SHARDSTEP_ERR_INVALID, "full is not 2-byte aligned");
+    const Span fs = span(full, static_cast<int64_t>(nd) * S * 2);
+    for (int32_t q = 0; q < nd; ++q) {
+        if (shards[q] == nullptr) return fail(SHARDSTEP_ERR_INVALID, "shards[%d] is NULL", q);
+        if (!aligned(shards[q], 2))
+            return fail(SHARDSTEP_ERR_INVALID, "shards[%d] is not 2-byte aligned", q);
+        if (shards[q] == full + static_cast<int64_t>(q) * S) continue;
+        if (overlap(span(shards[q], S * 2), fs))
+            return fail(SHARDSTEP_ERR_INVALID, "shards[%d] overlaps full", q);
+    }
+    CopyBatcher cb(static_cast<cudaStream_t>(stream));
+    for (int32_t q = 0; q < nd; ++q) {
+        uint16_t* dst = full + static_cast<int64_t>(q) * S;
+        if (shards[q] != dst) cb.add(shards[q], dst, S * 2);
+    }
+    cb.flush();
+    return cb.rc == SHARDSTEP_OK ? ok() : cb.rc;
+}
+
+int fsdp_grad_accumulate(const uint16_t* g, float* acc, int64_t n, float scale, int32_t first,
+                         void* stream) {
+    if (n < 0) return fail(SHARDSTEP_ERR_INVALID, "n must be >= 0");
+    if (n == 0) return ok();
+    if (g == nullptr || acc == nullptr) return fail(SHARDSTEP_ERR_INVALID, "g / acc is NULL");
+    if (!aligned(g, 2) || !aligned(acc, 4))
+        return fail(SHARDSTEP_ERR_INVALID, "g / acc misaligned for their element type");
+    if (overlap(span(g, n * 2), span(acc, n * 4)))
+        return fail(SHARDSTEP_ERR_INVALID, "g overlaps acc");
+    const bool vec = aligned(g, 16) && aligned(acc, 16);
+    cudaError_t e = launch_accumulate(g, acc, n, scale, first != 0, vec,
+                                      static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "accumulate kernel launch");
+    return ok();
+}
+
+int fsdp_rs_avg_adamw_cast(const void* const* grad_slices, int32_t grad_dtype, int32_t nd,
+                           int64_t S, float* master, float* m, float* v, uint16_t* out_bf16,
+                           const shardstep_adamw_t* hp, void* stream) {
+    const int gs = elem_size_of(grad_dtype);
+    if (gs == 0) return fail(SHARDSTEP_ERR_INVALID, "unknown grad dtype %d", grad_dtype);
+    if (nd < 1) return fail(SHARDSTEP_ERR_INVALID, "nd must be >= 1 (got %d)", nd);
+    if (nd > SHARDSTEP_MAX_ND)
+        return fail(SHARDSTEP_ERR_CAPACITY, "nd %d > %d", nd, SHARDSTEP_MAX_ND);
+    if (S < 0) return fail(SHARDSTEP_ERR_INVALID, "S must be >= 0");
+    if (hp == nullptr) return fail(SHARDSTEP_ERR_INVALID, "hp is NULL");
+    if (hp->step < 1) return fail(SHARDSTEP_ERR_INVALID, "step must be >= 1 (got %lld)",
+                                  static_cast<long long>(hp->step));
+    if (S == 0) return ok();
+    if (grad_slices == nullptr) return fail(SHARDSTEP_ERR_INVALID, "grad_slices is NULL");
+    if (!master || !m || !v || !out_bf16)
+        return fail(SHARDSTEP_ERR_INVALID, "master / m / v / out_bf16 is NULL");
+    if (!aligned(master, 4) || !aligned(m, 4) || !aligned(v, 4) || !aligned(out_bf16, 2))
+        return fail(SHARDSTEP_ERR_INVALID, "state or output misaligned for its element type");
+    const Span outs[4] = {span(master, S * 4), span(m, S * 4), span(v, S * 4),
+                          span(out_bf16, S * 2)};
+    for (int a = 0; a < 4; ++a)
+        for (int b = a + 1; b < 4; ++b)
+            if (overlap(outs[a], outs[b]))
+                return fail(SHARDSTEP_ERR_INVALID, "outputs %d and %d overlap", a, b);
+    PtrTable tab;
+    bool vec = aligned(master, 16) && aligned(m, 16) && aligned(v, 16) && aligned(out_bf16, 16);
+    for (int32_t q = 0; q < nd; ++q) {
+        const void* p = grad_slices[q];
+        if (p == nullptr) return fail(SHARDSTEP_ERR_INVALID, "grad_slices[%d] is NULL", q);
+        if (!aligned(p, gs))
+            return fail(SHARDSTEP_ERR_INVALID, "grad_slices[%d] misaligned for its dtype", q);
+        const Span gsn = span(p, S * gs);
+        for (int a = 0; a < 4; ++a)
+            if (overlap(gsn, outs[a]))
+                return fail(SHARDSTEP_ERR_INVALID, "grad_slices[%d] overlaps an output", q);
+        vec = vec && aligned(p, 16);
+        tab.p[q] = p;
+    }
+    for (int32_t q = nd; q < SHARDSTEP_MAX_ND; ++q) tab.p[q] = nullptr;
+    cudaError_t e = launch_rs_adamw_cast(tab, nd, grad_dtype == SHARDSTEP_DTYPE_F32, S, master, m,
+                                         v, out_bf16, adam_scalars(*hp), mean_op(nd), vec,
+                                         static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "fused step kernel launch");
+    return ok();
+}
+
+int ddp_bucket_plan(const int64_t* numels, int32_t n, int32_t elem_size, int64_t cap_bytes,
+                    int64_t* param_offset, int32_t* bucket_of_param, int64_t* bucket_offsets,
+                    int32_t* n_buckets) {
+    if (n < 0) return fail(SHARDSTEP_ERR_INVALID, "n must be >= 0");
+    if (elem_size <= 0 || cap_bytes <= 0)
+        return fail(SHARDSTEP_ERR_INVALID, "elem_size and cap_bytes must be > 0");
+    if (n_buckets == nullptr || bucket_offsets == nullptr)
+        return fail(SHARDSTEP_ERR_INVALID, "bucket_offsets / n_buckets is NULL");
+    if (n > 0 && (numels == nullptr || param_offset == nullptr || bucket_of_param == nullptr))
+        return fail(SHARDSTEP_ERR_INVALID, "numels / param_offset / bucket_of_param is NULL");
+    for (int32_t i = 0; i < n; ++i)
+        if (numels[i] < 0) return fail(SHARDSTEP_ERR_INVALID, "numel %d is negative", i);
+    int32_t nb = 0;
+    int64_t pos = 0, cur_bytes = 0;
+    bool open = false;
+    bucket_offsets[0] = 0;
+    for (int32_t i = n - 1; i >= 0; --i) {
+        const int64_t b = numels[i] * elem_size;
+        if (open && cur_bytes + b > cap_bytes) {
+            bucket_offsets[++nb] = pos;
+            cur_bytes = 0;
+            open = false;
+        }
+        open = true;
+        bucket_of_param[i] = nb;
+        param_offset[i] = pos;
+        pos += numels[i];
+        cur_bytes += b;
+    }
+    if (open) bucket_offsets[++nb] = pos;
+    *n_buckets = nb;
+    return ok();
+}
+
+int ddp_bucket_allreduce_avg(const uint16_t* const* rank_grads, int32_t nd,
+                             const int64_t* bucket_offsets, int32_t first, int32_t count,
+                             uint16_t* out, void* stream) {
+    if (nd < 1) return fail(SHARDSTEP_ERR_INVALID, "nd must be >= 1 (got %d)", nd);
+    if (nd > SHARDSTEP_MAX_ND)
+        return fail(SHARDSTEP_ERR_CAPACITY, "nd %d > %d", nd, SHARDSTEP_MAX_ND);
+    if (first < 0 || count < 0) return fail(SHARDSTEP_ERR_INVALID, "first / count negative");
+    if (count == 0) return ok();
+    if (bucket_offsets == nullptr || rank_grads == nullptr || out == nullptr)
+        return fail(SHARDSTEP_ERR_INVALID, "bucket_offsets / rank_grads / out is NULL");
+    for (int32_t b = first; b < first + count; ++b)
+        if (bucket_offsets[b] < 0 || bucket_offsets[b + 1] < bucket_offsets[b])
+            return fail(SHARDSTEP_ERR_INVALID, "bucket offsets must be non-decreasing");
+    const int64_t a0 = bucket_offsets[first], e0 = bucket_offsets[first + count];
+    if (!aligned(out, 2)) return fail(SHARDSTEP_ERR_INVALID, "out is not 2-byte aligned");
+    const Span os = span(out + a0, (e0 - a0) * 2);
+    for (int32_t q = 0; q < nd; ++q) {
+        if (rank_grads[q] == nullptr)
+            return fail(SHARDSTEP_ERR_INVALID, "rank_grads[%d] is NULL", q);
+        if (!aligned(rank_grads[q], 2))
+            return fail(SHARDSTEP_ERR_INVALID, "rank_grads[%d] is not 2-byte aligned", q);
+        if (overlap(span(rank_grads[q] + a0, (e0 - a0) * 2), os))
+            return fail(SHARDSTEP_ERR_INVALID, "rank_grads[%d] overlaps out", q);
+    }
+    const MeanOp mo = mean_op(nd);
+    for (int32_t b = first; b < first + count; ++b) {
+        const int64_t a = bucket_offsets[b], n = bucket_offsets[b + 1] - a;
+        if (n == 0) continue;
+        PtrTable tab;
+        bool vec = aligned(out + a, 16);
+        for (int32_t q = 0; q < SHARDSTEP_MAX_ND; ++q) {
+            tab.p[q] = q < nd ? rank_grads[q] + a : nullptr;
+            if (q < nd) vec = vec && aligned(tab.p[q], 16);
+        }
+        cudaError_t e = launch_allreduce_avg(tab, nd, n, out + a, mo, vec,
+                                             static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(e, "all-reduce kernel launch");
+    }
+    return ok();
+}
+
+double shardstep_state_bytes(double psi, int32_t nd, int32_t stage, double k) {
+    if (nd < 1) return -1.0;
+    switch (stage) {
+        case 0: return 2 * psi + 2 * psi + k * psi;
+        case 1: return 2 * psi + 2 * psi + k * psi / nd;
+        case 2: return 2 * psi + (2 * psi + k * psi) / nd;
+        case 3: return (2 * psi + 2 * psi + k * psi) / nd;
+        default: return -1.0;
+    }
+}
+
+double shardstep_comm_bytes(double psi, int32_t nd, int32_t kind, int32_t exact) {
+    if (nd < 1) return -1.0;
+    const double f = exact ? static_cast<double>(nd - 1) / nd : 1.0;
+    const double one = 2 * psi * f;  // one reduce-scatter or all-gather pass
+    switch (kind) {
+        case SHARDSTEP_COMM_REDUCE_SCATTER:
+        case SHARDSTEP_COMM_ALL_GATHER: return one;
+        case SHARDSTEP_COMM_ALL_REDUCE:
+        case SHARDSTEP_COMM_ZERO1:
+        case SHARDSTEP_COMM_ZERO2: return 2 * one;
+        case SHARDSTEP_COMM_ZERO3: return 3 * one;
+        default: return -1.0;
+    }
+}
+
+}  // extern "C"

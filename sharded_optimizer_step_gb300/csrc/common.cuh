@@ -1,0 +1,96 @@
+// Shared device helpers of libshardstep: streaming 16-byte loads and stores,
+// bf16 packing, and the per-element AdamW update.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "internal.h"
+#include "shardstep.h"
+
+namespace shardstep {
+
+constexpr int kThreads = 256;  // threads per block of every kernel here
+
+// ---------------------------------------------------------------- memory
+
+// Read-only stream, touched once: bypass L1, ask L2 for 256-byte fills.
+__device__ __forceinline__ uint4 ld_once(const void* p) {
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p));
+    return r;
+}
+
+// Read of data the same thread writes back later in the kernel (coherent
+// path).  Each address is read once, before the store that depends on it.
+__device__ __forceinline__ uint4 ld_rw(const void* p) {
+    uint4 r;
+    asm("ld.global.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+// Streaming store (evict-first in L2).
+__device__ __forceinline__ void st_stream(void* p, uint4 v) {
+    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// ------------------------------------------------------------------- bf16
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ float bf16_to_f32(uint16_t h) {
+    return __uint_as_float(static_cast<uint32_t>(h) << 16);
+}
+
+// Two fp32 -> packed bf16x2 (a in the low half), round to nearest even.
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ uint16_t f32_to_bf16(float a) {
+    __nv_bfloat16 h = __float2bfloat16_rn(a);
+    return *reinterpret_cast<uint16_t*>(&h);
+}
+
+// 16 bytes of bf16 -> 8 floats.
+__device__ __forceinline__ void unpack8(const uint4& r, float* f) {
+    f[0] = bf16_lo(r.x); f[1] = bf16_hi(r.x);
+    f[2] = bf16_lo(r.y); f[3] = bf16_hi(r.y);
+    f[4] = bf16_lo(r.z); f[5] = bf16_hi(r.z);
+    f[6] = bf16_lo(r.w); f[7] = bf16_hi(r.w);
+}
+__device__ __forceinline__ void unpack4f(const uint4& r, float* f) {
+    f[0] = __uint_as_float(r.x); f[1] = __uint_as_float(r.y);
+    f[2] = __uint_as_float(r.z); f[3] = __uint_as_float(r.w);
+}
+__device__ __forceinline__ uint4 pack4f(const float* f) {
+    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                      __float_as_uint(f[3]));
+}
+
+// ------------------------------------------------------------- arithmetic
+
+__device__ __forceinline__ float mean_of(float sum, const MeanOp& mo) {
+    return mo.pow2 ? __fmul_rn(sum, mo.inv_nd) : __fdiv_rn(sum, mo.nd);
+}
+
+// One AdamW element update, one IEEE rounding per operation, no contraction:
+//   p = p - (lr*wd)*p ; m = b1*m + (1-b1)*g ; v = b2*v + ((1-b2)*g)*g ;
+//   p = p - ((lr/bc1)*m) / (sqrt(v)/sqrt(bc2) + eps)
+__device__ __forceinline__ void adamw_elem(float g, float& p, float& m, float& v,
+                                           const AdamScalars& c) {
+    p = __fsub_rn(p, __fmul_rn(c.lr_wd, p));
+    m = __fadd_rn(__fmul_rn(c.beta1, m), __fmul_rn(c.omb1, g));
+    v = __fadd_rn(__fmul_rn(c.beta2, v), __fmul_rn(__fmul_rn(c.omb2, g), g));
+    const float den = __fadd_rn(__fdiv_rn(__fsqrt_rn(v), c.sqrt_bc2), c.eps);
+    p = __fsub_rn(p, __fdiv_rn(__fmul_rn(c.step_size, m), den));
+}
+
+}  // namespace shardstep

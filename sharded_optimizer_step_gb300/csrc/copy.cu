@@ -1,0 +1,181 @@
+// Copy-shaped kernels: the batched segment copy behind fsdp_flat_pack and
+// fsdp_ag_unpack, and the micro-batch gradient accumulation.
+//
+// Segment copy: one launch moves up to kMaxCopySegs byte ranges.  Each
+// segment is cut into chunks of 1024 vectors; blocks stride over the chunks
+// of all segments, so large and small tensors share one balanced grid.  The
+// vector width of a segment is the widest of 16/8/4/2/1 bytes for which
+// source and destination are congruent; a head of up to width-1 bytes brings
+// the destination to that alignment and the tail is copied byte-wise, both by
+// the lanes of the block that owns the segment's first / last chunk.
+#include "common.cuh"
+
+namespace shardstep {
+namespace {
+
+template <typename T>
+__device__ __forceinline__ T load_vec(const T* p) {
+    return *p;
+}
+template <>
+__device__ __forceinline__ uint4 load_vec<uint4>(const uint4* p) {
+    return ld_once(p);
+}
+template <typename T>
+__device__ __forceinline__ void store_vec(T* p, const T& v) {
+    *p = v;
+}
+template <>
+__device__ __forceinline__ void store_vec<uint4>(uint4* p, const uint4& v) {
+    st_stream(p, v);
+}
+
+template <typename T>
+__device__ __forceinline__ void copy_vecs(const char* src, char* dst, int64_t v0, int64_t v1) {
+    const T* s = reinterpret_cast<const T*>(src);
+    T* d = reinterpret_cast<T*>(dst);
+    constexpr int U = kCopyVecsPerChunk / kThreads;
+    if (src != nullptr) {
+        T r[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t k = v0 + u * kThreads + threadIdx.x;
+            if (k < v1) r[u] = load_vec<T>(s + k);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t k = v0 + u * kThreads + threadIdx.x;
+            if (k < v1) store_vec<T>(d + k, r[u]);
+        }
+    } else {
+        T z;
+        memset(&z, 0, sizeof(T));
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t k = v0 + u * kThreads + threadIdx.x;
+            if (k < v1) store_vec<T>(d + k, z);
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) copy_segments(CopyTable t) {
+    int seg = 0;
+    for (int64_t c = blockIdx.x; c < t.total_chunks; c += gridDim.x) {
+        while (seg + 1 < t.n && t.s[seg + 1].chunk0 <= c) ++seg;
+        const CopySeg& sg = t.s[seg];
+        const int64_t local = c - sg.chunk0;
+        const int64_t nchunks =
+            sg.body > 0 ? (sg.body + kCopyVecsPerChunk - 1) / kCopyVecsPerChunk : 1;
+        const char* src = sg.src ? sg.src + sg.head : nullptr;
+        char* dst = sg.dst + sg.head;
+        const int64_t v0 = local * kCopyVecsPerChunk;
+        const int64_t v1 = v0 + kCopyVecsPerChunk < sg.body ? v0 + kCopyVecsPerChunk : sg.body;
+        switch (sg.width) {
+            case 16: copy_vecs<uint4>(src, dst, v0, v1); break;
+            case 8: copy_vecs<uint2>(src, dst, v0, v1); break;
+            case 4: copy_vecs<uint32_t>(src, dst, v0, v1); break;
+            case 2: copy_vecs<uint16_t>(src, dst, v0, v1); break;
+            default: copy_vecs<uint8_t>(src, dst, v0, v1); break;
+        }
+        if (local == 0 && threadIdx.x < sg.head)
+            sg.dst[threadIdx.x] = sg.src ? sg.src[threadIdx.x] : 0;
+        if (local == nchunks - 1) {
+            const int64_t done = sg.head + sg.body * sg.width;
+            const int64_t tail = sg.bytes - done;
+            if (threadIdx.x < tail)
+                sg.dst[done + threadIdx.x] = sg.src ? sg.src[done + threadIdx.x] : 0;
+        }
+    }
+}
+
+// ------------------------------------------------------- accumulation
+
+template <bool FIRST>
+__device__ __forceinline__ void acc_scalar(const uint16_t* g, float* acc, int64_t j,
+                                           float scale) {
+    const float t = __fmul_rn(bf16_to_f32(g[j]), scale);
+    acc[j] = FIRST ? t : __fadd_rn(acc[j], t);
+}
+
+template <bool FIRST>
+__global__ void __launch_bounds__(kThreads)
+    accumulate_vec8(const uint16_t* __restrict__ g, float* __restrict__ acc, int64_t n,
+                    float scale) {
+    const int64_t nvec = n >> 3;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < nvec;
+         i += stride) {
+        const uint4 gr = ld_once(g + 8 * i);
+        float a[8];
+        if (!FIRST) {
+            unpack4f(ld_rw(acc + 8 * i), a);
+            unpack4f(ld_rw(acc + 8 * i + 4), a + 4);
+        }
+        float f[8];
+        unpack8(gr, f);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float t = __fmul_rn(f[k], scale);
+            a[k] = FIRST ? t : __fadd_rn(a[k], t);
+        }
+        st_stream(acc + 8 * i, pack4f(a));
+        st_stream(acc + 8 * i + 4, pack4f(a + 4));
+    }
+    if (blockIdx.x == 0 && threadIdx.x < (n & 7))
+        acc_scalar<FIRST>(g, acc, (nvec << 3) + threadIdx.x, scale);
+}
+
+template <bool FIRST>
+__global__ void __launch_bounds__(kThreads)
+    accumulate_scalar(const uint16_t* __restrict__ g, float* __restrict__ acc, int64_t n,
+                      float scale) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    for (int64_t j = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; j < n;
+         j += stride)
+        acc_scalar<FIRST>(g, acc, j, scale);
+}
+
+unsigned grid_for(const void* kernel, int64_t work_items) {
+    const int64_t want = (work_items + kThreads - 1) / kThreads;
+    const int64_t cap = static_cast<int64_t>(device_sms()) * resident_blocks(kernel, kThreads);
+    const int64_t g = want < cap ? want : cap;
+    return static_cast<unsigned>(g < 1 ? 1 : g);
+}
+
+}  // namespace
+
+cudaError_t launch_copy(const CopyTable& t, cudaStream_t stream) {
+    const int64_t cap = static_cast<int64_t>(device_sms()) *
+                        resident_blocks(reinterpret_cast<const void*>(copy_segments), kThreads);
+    const int64_t g = t.total_chunks < cap ? t.total_chunks : cap;
+    copy_segments<<<static_cast<unsigned>(g < 1 ? 1 : g), kThreads, 0, stream>>>(t);
+    note_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_accumulate(const uint16_t* g, float* acc, int64_t n, float scale, bool first,
+                              bool vec, cudaStream_t stream) {
+    if (vec) {
+        const int64_t items = (n >> 3) > 0 ? (n >> 3) : 1;
+        if (first) {
+            accumulate_vec8<true><<<grid_for(reinterpret_cast<const void*>(accumulate_vec8<true>),
+                                             items),
+                                    kThreads, 0, stream>>>(g, acc, n, scale);
+        } else {
+            accumulate_vec8<false><<<grid_for(reinterpret_cast<const void*>(accumulate_vec8<false>),
+                                              items),
+                                     kThreads, 0, stream>>>(g, acc, n, scale);
+        }
+    } else if (first) {
+        accumulate_scalar<true><<<grid_for(reinterpret_cast<const void*>(accumulate_scalar<true>), n),
+                                  kThreads, 0, stream>>>(g, acc, n, scale);
+    } else {
+        accumulate_scalar<false><<<grid_for(reinterpret_cast<const void*>(accumulate_scalar<false>),
+                                            n),
+                                   kThreads, 0, stream>>>(g, acc, n, scale);
+    }
+    note_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace shardstep

@@ -1,0 +1,67 @@
+"""One rank's sharded optimizer over a model's FSDP units.
+
+The rank keeps its shard of every unit back to back in one buffer per state
+(fp32 master, m, v and the bf16 parameter shard), so one fused launch updates
+the whole rank.  The N_d incoming gradient contributions (the reduce-scatter
+inputs: rank q's flat gradient, restricted to this rank's slices) are the
+buffers ``grad_in[q]`` laid out the same way, which the caller fills between
+steps.  ``gather_unit`` all-gathers one unit's bf16 shards into its full flat
+buffer and returns the per-tensor views.
+
+Buffers are allocated with torch once, at construction; ``step`` and
+``gather_unit`` allocate nothing.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import AdamW, fsdp_ag_unpack, fsdp_layout, fsdp_rs_avg_adamw_cast, fsdp_views
+
+
+def _numel(shape):
+    n = 1
+    for d in shape:
+        n *= int(d)
+    return n
+
+
+class RankShardOptimizer:
+    def __init__(self, unit_shapes, nd: int, rank: int, hp: AdamW, device="cuda",
+                 grad_dtype=torch.bfloat16):
+        if not 0 <= rank < nd:
+            raise ValueError("rank out of range")
+        self.unit_shapes = [list(u) for u in unit_shapes]
+        self.nd, self.rank, self.hp = nd, rank, hp
+        self.layouts = [fsdp_layout([_numel(s) for s in u], nd) for u in self.unit_shapes]
+        self.starts = []
+        pos = 0
+        for lay in self.layouts:
+            self.starts.append(pos)
+            pos += lay.shard
+        self.shard_total = pos
+        dev = torch.device(device)
+        self.master = torch.zeros(pos, dtype=torch.float32, device=dev)
+        self.m = torch.zeros(pos, dtype=torch.float32, device=dev)
+        self.v = torch.zeros(pos, dtype=torch.float32, device=dev)
+        self.params = torch.zeros(pos, dtype=torch.bfloat16, device=dev)
+        self.grad_in = [torch.zeros(pos, dtype=grad_dtype, device=dev) for _ in range(nd)]
+        self.t = 0
+
+    def unit_slice(self, buf, u):
+        """This rank's piece of unit u inside a rank-shard buffer."""
+        return buf[self.starts[u]:self.starts[u] + self.layouts[u].shard]
+
+    def step(self, stream=None):
+        """Reduce-scatter average + AdamW + bf16 cast over the whole rank shard."""
+        self.t += 1
+        fsdp_rs_avg_adamw_cast(self.grad_in, self.master, self.m, self.v, self.params, self.hp,
+                               self.t, stream=stream)
+
+    def gather_unit(self, u, peer_shards, full, stream=None):
+        """All-gather unit u: ``peer_shards[q]`` is rank q's bf16 shard (this
+        rank's own entry is ignored and taken from ``params``); ``full`` is the
+        unit's flat bf16 buffer of P elements.  Returns the tensor views."""
+        shards = list(peer_shards)
+        shards[self.rank] = self.unit_slice(self.params, u)
+        fsdp_ag_unpack(shards, full, stream=stream)
+        return fsdp_views(full, self.unit_shapes[u], self.nd)

@@ -1,0 +1,172 @@
+"""CPU checks of the C ABI: the library loads, exports every symbol the
+header declares, and its host-only entry points (layout, views, bucket plan,
+ledger, argument validation) agree with the oracle.  No call here reaches the
+GPU: validation rejects the arguments before any launch."""
+import ctypes
+import itertools
+import os
+import random
+import re
+
+import pytest
+
+import oracle
+import sharded_optimizer_step_gb300 as ss
+from sharded_optimizer_step_gb300 import _capi
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    ss.build()
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "shardstep.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w]*\s*\*?\s*([a-z_][a-z0-9_]*)\s*\(",
+                       text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_library_exports_every_declared_symbol():
+    names = _declared_functions()
+    assert len(names) >= 12
+    lib = ctypes.CDLL(_capi.lib_path())
+    for n in names:
+        assert hasattr(lib, n), n
+    # and the binding declares exactly these
+    assert sorted(_capi.SIGNATURES) == names
+
+
+def _layout_matches(numels, nd):
+    a = ss.fsdp_layout(numels, nd)
+    b = oracle.layout(numels, nd)
+    assert (a.total, a.padded, a.shard) == (b.total, b.padded, b.shard)
+    assert a.offsets == b.offsets
+    assert a.lo == b.lo and a.hi == b.hi
+
+
+def test_layout_matches_oracle_brute_force():
+    for K in range(0, 4):
+        for numels in itertools.product(range(0, 6), repeat=K):
+            for nd in range(1, 6):
+                _layout_matches(list(numels), nd)
+
+
+def test_layout_matches_oracle_on_model_units():
+    gpt2_block = [768 * 2304, 2304, 768 * 768, 768, 768 * 3072, 3072, 3072 * 768, 768,
+                  768, 768, 768, 768]
+    llama_layer = [2048 * 2048] * 4 + [2048 * 8192] * 2 + [8192 * 2048] + [2048, 2048]
+    for unit, nd in ((gpt2_block, 8), (llama_layer, 8), ([1024 * 1024, 1024 * 4096, 4096 * 1024], 4),
+                     ([5, 7, 11, 3], 6), ([1], 64)):
+        _layout_matches(unit, nd)
+
+
+def test_worked_example_views_through_the_abi():
+    # three (4,2) tensors on two ranks: pieces (count) per rank
+    shapes = [(4, 2)] * 3
+    numels = [8, 8, 8]
+    base = 0x10000
+    for r, want in ((0, [8, 4, 0]), (1, [0, 4, 8])):
+        ptrs = (_capi.c_vp * 3)()
+        counts = (_capi.c_i64 * 3)()
+        _capi.check("fsdp_views", _capi.lib().fsdp_views(
+            _capi.i64_array(numels), 3, 2, r, ctypes.c_void_p(base), 2, ptrs, counts))
+        assert list(counts) == want
+        lay = oracle.layout(numels, 2)
+        for t in range(3):
+            assert (ptrs[t] or 0) == base + 2 * lay.lo[r][t]
+    ptrs = (_capi.c_vp * 3)()
+    counts = (_capi.c_i64 * 3)()
+    _capi.check("fsdp_views", _capi.lib().fsdp_views(
+        _capi.i64_array(numels), 3, 2, -1, ctypes.c_void_p(base), 2, ptrs, counts))
+    assert [p - base for p in ptrs] == [0, 16, 32] and list(counts) == [8, 8, 8]
+    del shapes
+
+
+def test_bucket_plan_matches_oracle():
+    rng = random.Random(3)
+    for _ in range(300):
+        n = rng.randrange(0, 12)
+        numels = [rng.choice([0, 1, 3, 768, 2048, 5000]) for _ in range(n)]
+        es = rng.choice([1, 2, 4])
+        cap = rng.choice([1, 100, 4096, 10000, 1 << 20])
+        assert ss.ddp_bucket_plan(numels, es, cap) == tuple(
+            list(x) for x in oracle.bucket_plan(numels, es, cap))
+
+
+def test_bucket_plan_sweep_workload():
+    unit = [768, 768, 768 * 3072, 768 * 3072, 4096 * 4096]
+    numels = unit * 16 + [768 * 3072] * 3
+    assert sum(numels) == 351_035_392
+    for mib in (1, 4, 25, 64, 256):
+        got = ss.ddp_bucket_plan(numels, 2, mib << 20)
+        want = oracle.bucket_plan(numels, 2, mib << 20)
+        assert got == tuple(list(x) for x in want)
+        assert got[2][-1] == sum(numels)
+
+
+def test_ledger_matches_oracle():
+    for psi in (7e9, 1.2e9, 351e6):
+        for nd in (1, 2, 4, 8, 16):
+            for stage in range(4):
+                assert ss.state_bytes(psi, nd, stage) == pytest.approx(
+                    oracle.state_bytes_per_gpu(psi, nd, stage), rel=1e-15)
+            for kind in ("reduce_scatter", "all_gather", "all_reduce", "zero1", "zero2", "zero3"):
+                for exact in (False, True):
+                    assert ss.comm_bytes(psi, nd, kind, exact) == pytest.approx(
+                        oracle.comm_bytes_per_gpu(psi, nd, kind, exact), rel=1e-15)
+    with pytest.raises(ValueError):
+        ss.state_bytes(1e9, 8, 4)
+
+
+def _fused(slices, nd, S, master, m, v, out, dtype=_capi.DTYPE_BF16, step=1):
+    hp = _capi.AdamWHP(1e-3, 0.9, 0.999, 1e-8, 0.01, step)
+    return _capi.lib().fsdp_rs_avg_adamw_cast(_capi.ptr_array(slices), dtype, nd, S,
+                                              ctypes.c_void_p(master), ctypes.c_void_p(m),
+                                              ctypes.c_void_p(v), ctypes.c_void_p(out),
+                                              ctypes.byref(hp), None)
+
+
+def test_fused_step_rejects_bad_arguments_before_launch():
+    L = _capi.lib()
+    S = 1024
+    A = 1 << 40  # fake device addresses, never dereferenced: validation fails first
+    g = [A + k * (1 << 20) for k in range(8)]
+    st = [A + (1 << 30) + k * (1 << 20) for k in range(4)]
+    assert _fused(g, 0, S, *st) == _capi.ERR_INVALID
+    assert _fused(g * 9, 65, S, *st) == _capi.ERR_CAPACITY
+    assert _fused(g, 8, S, *st, step=0) == _capi.ERR_INVALID
+    assert _fused(g, 8, S, *st, dtype=7) == _capi.ERR_INVALID
+    assert _fused(g, 8, -1, *st) == _capi.ERR_INVALID
+    assert _fused(g[:7] + [0], 8, S, *st) == _capi.ERR_INVALID          # NULL slice
+    assert _fused(g, 8, S, st[0], st[0] + 8, st[2], st[3]) == _capi.ERR_INVALID  # m overlaps master
+    assert _fused(g[:7] + [st[3]], 8, S, *st) == _capi.ERR_INVALID      # grad overlaps output
+    assert _fused(g, 8, S, st[0] + 2, st[1], st[2], st[3]) == _capi.ERR_INVALID  # misaligned fp32
+    assert "misaligned" in L.shardstep_last_error().decode()
+    assert _fused(g, 8, 0, *st) == _capi.OK                             # nothing to do
+
+
+def test_other_entry_points_reject_bad_arguments():
+    L = _capi.lib()
+    A = 1 << 40
+    assert L.fsdp_ag_unpack(_capi.ptr_array([A, A + 3000]), 2, 1024, ctypes.c_void_p(A + 2048),
+                            None) == _capi.ERR_INVALID    # shard overlaps full
+    assert L.fsdp_ag_unpack(_capi.ptr_array([A]), 0, 16, ctypes.c_void_p(A), None) == \
+        _capi.ERR_INVALID
+    assert L.fsdp_grad_accumulate(ctypes.c_void_p(A), ctypes.c_void_p(A + 8), 64,
+                                  ctypes.c_float(0.25), 1, None) == _capi.ERR_INVALID
+    assert L.fsdp_flat_pack(_capi.ptr_array([A]), _capi.i64_array([16]), 1, 2, 9,
+                            ctypes.c_void_p(A + 4096), None) == _capi.ERR_INVALID
+    assert L.fsdp_flat_pack(_capi.ptr_array([A]), _capi.i64_array([16]), 1, 2,
+                            _capi.DTYPE_BF16, ctypes.c_void_p(A + 8), None) == _capi.ERR_INVALID
+    boff = _capi.i64_array([0, 10, 5])
+    assert L.ddp_bucket_allreduce_avg(_capi.ptr_array([A, A + 4096]), 2, boff, 0, 2,
+                                      ctypes.c_void_p(A + 8192), None) == _capi.ERR_INVALID
+    assert L.ddp_bucket_plan(_capi.i64_array([1]), 1, 2, 0, (_capi.c_i64 * 1)(),
+                             (_capi.c_i32 * 1)(), (_capi.c_i64 * 2)(),
+                             ctypes.byref(_capi.c_i32())) == _capi.ERR_INVALID
+    with pytest.raises(ss.ShardstepError):
+        ss.fsdp_layout([3, -1], 2)

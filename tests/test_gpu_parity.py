@@ -1,0 +1,314 @@
+"""GPU parity: every entry point of the C ABI against the CPU oracle on the
+same seeded inputs, element by element, at sizes that span several tiles,
+ragged tails, misaligned pointers and the degenerate cases (N_d = 1, one
+element, empty pieces).  Bar: bit-exact indexing and copies; fp32 state
+within 1e-6 relative; bf16 within 1 ulp.  The fused step is also required to
+be bit-exact, which its fixed operation order makes possible."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sharded_optimizer_step_gb300 as ss
+import synth
+from oracle.numerics import AdamWConfig
+from tests._cmp import assert_bf16, assert_bits, assert_f32
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+HP = AdamWConfig(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
+HPC = ss.AdamW(lr=HP.lr, beta1=HP.beta1, beta2=HP.beta2, eps=HP.eps, weight_decay=HP.weight_decay)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    ss.build()
+    synth.build_dev()
+
+
+def dev_bf16(u16, shift=0):
+    """numpy bf16 bits -> CUDA bf16 tensor starting `shift` elements into its
+    allocation (shift > 0 gives a misaligned pointer)."""
+    buf = torch.empty(u16.size + shift + 8, dtype=torch.bfloat16, device=DEV)
+    t = buf[shift:shift + u16.size]
+    t.copy_(torch.from_numpy(np.ascontiguousarray(u16).view(np.int16)).view(torch.bfloat16))
+    return t
+
+
+def dev_f32(x, shift=0):
+    buf = torch.empty(x.size + shift + 8, dtype=torch.float32, device=DEV)
+    t = buf[shift:shift + x.size]
+    t.copy_(torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)))
+    return t
+
+
+def host_bf16(t):
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def host_f32(t):
+    return t.contiguous().cpu().numpy()
+
+
+def _grads(seed, nd, P, dtype, step):
+    out = []
+    for q in range(nd):
+        st = synth.normal_stream(seed, (99, 1, step, q), 1e-3)
+        out.append(synth.host_fill(st, 0, P, dtype))
+    return out
+
+
+# ------------------------------------------------------------ fused step
+
+@pytest.mark.parametrize("nd", [1, 2, 3, 4, 5, 8, 16])
+@pytest.mark.parametrize("S", [1, 13, 4099])
+@pytest.mark.parametrize("gdt", ["bf16", "f32"])
+@pytest.mark.parametrize("shift", [0, 1])
+def test_fused_step_matches_oracle(nd, S, gdt, shift):
+    seed = nd * 1000 + S + (7 if gdt == "f32" else 0)
+    r = (S + 2 * nd) % nd
+    P = nd * S
+    p = synth.host_fill(synth.normal_stream(seed, (99, 2), 0.02), 0, S, "f32")
+    m = np.zeros(S, np.float32)
+    v = np.zeros(S, np.float32)
+    dp, dm, dv = dev_f32(p, shift), dev_f32(m, shift), dev_f32(v, shift)
+    out = torch.empty(S + 1, dtype=torch.bfloat16, device=DEV)[shift:shift + S]
+    for t in (1, 2, 3):
+        contribs = _grads(seed, nd, P, gdt, t)
+        mk = dev_bf16 if gdt == "bf16" else dev_f32
+        slices = [mk(c[r * S:(r + 1) * S], shift if q % 2 else 0) for q, c in enumerate(contribs)]
+        ss.fsdp_rs_avg_adamw_cast(slices, dp, dm, dv, out, HPC, t)
+        p, m, v, ob = oracle.fsdp_shard_step(contribs, r, S, p, m, v, HP, t)
+        torch.cuda.synchronize()
+        for name, got, want in (("master", host_f32(dp), p), ("m", host_f32(dm), m),
+                                ("v", host_f32(dv), v)):
+            assert_f32(got, want, f"{name} step {t}")
+            assert_bits(got, want, f"{name} step {t}")
+        assert_bf16(host_bf16(out), ob, f"bf16 step {t}")
+        assert_bits(host_bf16(out), ob, f"bf16 step {t}")
+
+
+@pytest.mark.parametrize("nd,gdt,S", [(8, "bf16", 152 * 256 * 8 * 2 + 5),
+                                      (4, "f32", 152 * 256 * 8 + 8 * 37 + 3),
+                                      (8, "bf16", 1 << 20)])
+def test_fused_step_multi_tile(nd, gdt, S):
+    seed = 5 + S
+    P = nd * S
+    r = 1 % nd
+    contribs = _grads(seed, nd, P, gdt, 1)
+    p = synth.host_fill(synth.normal_stream(seed, (99, 2), 0.02), 0, S, "f32")
+    m = (synth.host_fill(synth.normal_stream(seed, (99, 3), 1e-4), 0, S, "f32"))
+    v = np.abs(synth.host_fill(synth.normal_stream(seed, (99, 4), 1e-7), 0, S, "f32"))
+    dp, dm, dv = dev_f32(p), dev_f32(m), dev_f32(v)
+    out = torch.empty(S, dtype=torch.bfloat16, device=DEV)
+    mk = dev_bf16 if gdt == "bf16" else dev_f32
+    slices = [mk(c[r * S:(r + 1) * S]) for c in contribs]
+    ss.fsdp_rs_avg_adamw_cast(slices, dp, dm, dv, out, HPC, 7)
+    p, m, v, ob = oracle.fsdp_shard_step(contribs, r, S, p, m, v, HP, 7)
+    torch.cuda.synchronize()
+    assert_bits(host_f32(dp), p, "master")
+    assert_bits(host_f32(dm), m, "m")
+    assert_bits(host_f32(dv), v, "v")
+    assert_bits(host_bf16(out), ob, "bf16")
+
+
+def test_fused_step_padding_stays_zero():
+    # zero gradients and zero master (the padding of a FlatParameter) stay zero
+    S, nd = 1000, 4
+    z = torch.zeros(S, dtype=torch.bfloat16, device=DEV)
+    dp = torch.zeros(S, device=DEV)
+    dm = torch.zeros(S, device=DEV)
+    dv = torch.zeros(S, device=DEV)
+    out = torch.full((S,), 1.0, dtype=torch.bfloat16, device=DEV)
+    for t in (1, 2):
+        ss.fsdp_rs_avg_adamw_cast([z] * nd, dp, dm, dv, out, HPC, t)
+    torch.cuda.synchronize()
+    assert not dp.any() and not dm.any() and not dv.any() and not out.float().any()
+
+
+def test_fused_step_output_may_be_the_slot_of_the_full_buffer():
+    nd, S, r = 4, 4099, 2
+    contribs = _grads(11, nd, nd * S, "bf16", 1)
+    p = synth.host_fill(synth.normal_stream(11, (99, 2), 0.02), 0, S, "f32")
+    dp, dm, dv = dev_f32(p), torch.zeros(S, device=DEV), torch.zeros(S, device=DEV)
+    full = torch.zeros(nd * S, dtype=torch.bfloat16, device=DEV)
+    ss.fsdp_rs_avg_adamw_cast([dev_bf16(c[r * S:(r + 1) * S]) for c in contribs], dp, dm, dv,
+                              full[r * S:(r + 1) * S], HPC, 1)
+    _, _, _, ob = oracle.fsdp_shard_step(contribs, r, S, p, np.zeros(S, np.float32),
+                                         np.zeros(S, np.float32), HP, 1)
+    torch.cuda.synchronize()
+    h = host_bf16(full)
+    assert_bits(h[r * S:(r + 1) * S], ob, "slot")
+    assert not h[:r * S].any() and not h[(r + 1) * S:].any()
+
+
+# ---------------------------------------------------------------- packing
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("nd", [1, 3, 8])
+def test_flat_pack_matches_oracle(dtype, nd):
+    rng = np.random.default_rng(nd)
+    numels = [int(x) for x in rng.integers(0, 5000, size=150)] + [1 << 20, 3, 0, 77777]
+    shifts = [int(s) for s in rng.integers(0, 4, size=len(numels))]
+    host, dev = [], []
+    for k, (n, sh) in enumerate(zip(numels, shifts)):
+        st = synth.normal_stream(nd, (98, k), 0.02)
+        h = synth.host_fill(st, 0, n, dtype)
+        host.append(h)
+        dev.append(dev_bf16(h, sh) if dtype == "bf16" else dev_f32(h, sh))
+    flat = ss.fsdp_flat_pack(dev, nd)
+    want, lay = oracle.flat_pack(host, nd)
+    torch.cuda.synchronize()
+    got = host_bf16(flat) if dtype == "bf16" else host_f32(flat)
+    assert got.size == lay.padded
+    assert_bits(got.view(np.uint8), want.view(np.uint8), "flat")
+    # views of the packed buffer: whole tensors, and every rank's pieces
+    shapes = [(n,) for n in numels]
+    for t, v in enumerate(ss.fsdp_views(flat, shapes, nd)):
+        assert v.numel() == numels[t]
+    for r in range(nd):
+        shard = flat[r * lay.shard:(r + 1) * lay.shard]
+        pieces = ss.fsdp_views(shard, shapes, nd, r)
+        want_pieces = oracle.sharded_views(oracle.shard_of(want, lay, r), lay, r)
+        for a, b in zip(pieces, want_pieces):
+            ha = host_bf16(a) if dtype == "bf16" else host_f32(a)
+            assert_bits(ha.view(np.uint8), b.view(np.uint8), "piece")
+
+
+def test_flat_pack_misaligned_destination_segments():
+    # element offsets that are odd make source and destination incongruent
+    numels = [1, 2, 3, 5, 8, 13, 21, 34, 55, 89, 144, 233, 377, 610, 987, 1597, 2584]
+    host = [synth.host_fill(synth.normal_stream(1, (97, k), 1.0), 0, n, "bf16")
+            for k, n in enumerate(numels)]
+    dev = [dev_bf16(h, k % 8) for k, h in enumerate(host)]
+    flat = ss.fsdp_flat_pack(dev, 7)
+    want, _ = oracle.flat_pack(host, 7)
+    torch.cuda.synchronize()
+    assert_bits(host_bf16(flat), want, "flat")
+
+
+def test_worked_example_on_gpu():
+    tensors = [np.arange(1, 9, dtype=np.float32).reshape(4, 2) + 100 * (t + 1) for t in range(3)]
+    flat = ss.fsdp_flat_pack([dev_f32(t.reshape(-1)).view(4, 2) for t in tensors], 2)
+    want, lay = oracle.flat_pack(tensors, 2)
+    torch.cuda.synchronize()
+    assert_bits(host_f32(flat), want, "flat")
+    sizes = [[v.numel() for v in ss.fsdp_views(flat[r * 12:(r + 1) * 12], [(4, 2)] * 3, 2, r)]
+             for r in range(2)]
+    assert sizes == [[8, 4, 0], [0, 4, 8]]
+
+
+# ------------------------------------------------------------- all-gather
+
+@pytest.mark.parametrize("nd", [1, 2, 3, 8])
+@pytest.mark.parametrize("S", [1, 5, 1000, (1 << 20) + 3])
+def test_ag_unpack_matches_oracle(nd, S):
+    shards_h = [synth.host_fill(synth.normal_stream(nd, (96, q, S), 0.02), 0, S, "bf16")
+                for q in range(nd)]
+    shards = [dev_bf16(h, q % 3) for q, h in enumerate(shards_h)]
+    full = torch.empty(nd * S, dtype=torch.bfloat16, device=DEV)
+    ss.fsdp_ag_unpack(shards, full)
+    lay = oracle.layout([nd * S], nd)
+    want, _ = oracle.ag_unpack(shards_h, lay)
+    torch.cuda.synchronize()
+    assert_bits(host_bf16(full), want, "full")
+
+
+def test_ag_unpack_skips_the_rank_already_in_place():
+    nd, S = 4, 12345
+    shards_h = [synth.host_fill(synth.normal_stream(3, (95, q), 0.02), 0, S, "bf16")
+                for q in range(nd)]
+    full = torch.zeros(nd * S, dtype=torch.bfloat16, device=DEV)
+    full[2 * S:3 * S].copy_(dev_bf16(shards_h[2]))
+    shards = [dev_bf16(h) for h in shards_h]
+    shards[2] = full[2 * S:3 * S]
+    before = ss.launch_count()
+    ss.fsdp_ag_unpack(shards, full)
+    assert ss.launch_count() - before == 1
+    torch.cuda.synchronize()
+    assert_bits(host_bf16(full), np.concatenate(shards_h), "full")
+
+
+def test_ag_unpack_views_are_the_unit_tensors():
+    shapes = [(4096, 11008), (11008,), (3, 5), (4096,)]
+    numels = [int(np.prod(s)) for s in shapes]
+    nd = 8
+    host = [synth.host_fill(synth.normal_stream(2, (94, k), 0.02), 0, n, "bf16")
+            for k, n in enumerate(numels)]
+    flat = ss.fsdp_flat_pack([dev_bf16(h) for h in host], nd)
+    lay = ss.fsdp_layout(numels, nd)
+    shards = [flat[r * lay.shard:(r + 1) * lay.shard].clone() for r in range(nd)]
+    full = torch.empty(lay.padded, dtype=torch.bfloat16, device=DEV)
+    ss.fsdp_ag_unpack(shards, full)
+    views = ss.fsdp_views(full, shapes, nd)
+    torch.cuda.synchronize()
+    for v, h, s in zip(views, host, shapes):
+        assert tuple(v.shape) == s
+        assert_bits(host_bf16(v).reshape(-1), h, "view")
+
+
+# ----------------------------------------------------------- accumulation
+
+@pytest.mark.parametrize("n,shift", [(1, 0), (8, 0), (4099, 0), (4099, 1), (1 << 20, 0),
+                                     (152 * 256 * 8 * 3 + 7, 0)])
+def test_grad_accumulate_matches_oracle(n, shift):
+    M = 4
+    micro = [synth.host_fill(synth.normal_stream(n, (93, j), 1e-3, 0.01), 0, n, "bf16")
+             for j in range(M)]
+    acc = torch.full((n + shift + 4,), 7.0, device=DEV)[shift:shift + n]
+    scale = np.float32(1.0 / M)
+    for j in range(M):
+        ss.fsdp_grad_accumulate(dev_bf16(micro[j], shift), acc, float(scale), j == 0)
+    want = oracle.grad_accumulate(micro, scale)
+    torch.cuda.synchronize()
+    assert_bits(host_f32(acc), want, "acc")
+
+
+# ---------------------------------------------------------------- buckets
+
+@pytest.mark.parametrize("nd", [2, 3, 8])
+@pytest.mark.parametrize("cap", [64, 5000, 1 << 22])
+def test_ddp_bucketed_step_matches_oracle(nd, cap):
+    numels = [768, 3, 768 * 30, 5, 4096 * 3, 768, 1, 2000]
+    off, of, boff = ss.ddp_bucket_plan(numels, 2, cap)
+    assert (off, of, boff) == tuple(list(x) for x in oracle.bucket_plan(numels, 2, cap))
+    total = boff[-1]
+    grads_h = [synth.host_fill(synth.normal_stream(nd, (92, q), 1e-3), 0, total, "bf16")
+               for q in range(nd)]
+    grads = [dev_bf16(h, q % 2) for q, h in enumerate(grads_h)]
+    out = torch.empty(total, dtype=torch.bfloat16, device=DEV)
+    # bucket by bucket, as each becomes ready
+    for b in range(len(boff) - 1):
+        ss.ddp_bucket_allreduce_avg(grads, boff, out, first=b, count=1)
+    p = synth.host_fill(synth.normal_stream(nd, (92, 100), 0.02), 0, total, "f32")
+    dp, dm, dv = dev_f32(p), torch.zeros(total, device=DEV), torch.zeros(total, device=DEV)
+    pb = torch.empty(total, dtype=torch.bfloat16, device=DEV)
+    ss.fsdp_rs_avg_adamw_cast([out], dp, dm, dv, pb, HPC, 1)
+    z = np.zeros(total, np.float32)
+    avg, p1, m1, v1, pb1 = oracle.ddp_step(grads_h, boff, p, z, z, HP, 1)
+    torch.cuda.synchronize()
+    assert_bits(host_bf16(out), avg, "avg")
+    assert_bits(host_f32(dp), p1, "master")
+    assert_bits(host_f32(dm), m1, "m")
+    assert_bits(host_f32(dv), v1, "v")
+    assert_bits(host_bf16(pb), pb1, "params")
+
+
+def test_allreduce_equals_reduce_scatter_then_all_gather_on_gpu():
+    nd, S = 8, 10007
+    grads_h = [synth.host_fill(synth.normal_stream(4, (91, q), 1e-3), 0, nd * S, "bf16")
+               for q in range(nd)]
+    grads = [dev_bf16(h) for h in grads_h]
+    ar = torch.empty(nd * S, dtype=torch.bfloat16, device=DEV)
+    ss.ddp_bucket_allreduce_avg(grads, [0, nd * S], ar)
+    # the same average computed piece by piece, one rank slice per bucket, is
+    # the reduce-scatter followed by the all-gather of the pieces
+    ar2 = torch.empty(nd * S, dtype=torch.bfloat16, device=DEV)
+    ss.ddp_bucket_allreduce_avg(grads, [r * S for r in range(nd + 1)], ar2)
+    torch.cuda.synchronize()
+    want = np.concatenate([oracle.f32_to_bf16(oracle.rs_avg(grads_h, r, S)) for r in range(nd)])
+    assert_bits(host_bf16(ar), want, "AR")
+    assert_bits(host_bf16(ar2), want, "RS+AG")

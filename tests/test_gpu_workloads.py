@@ -1,0 +1,319 @@
+"""GPU parity on the five model-shaped workloads at full size.
+
+The 9.4M-parameter unit (N_d = 4, M = 4) is compared element by element with
+the oracle.  The larger workloads run in full on the GPU and are checked on
+sampled outputs that the oracle computes one by one from the same seeded
+inputs (every step, every micro-batch, every rank), plus properties that hold
+at any size.  The Llama-7B rank view runs in the launch configuration the
+benchmark times: one fused launch over the rank's 842,301,952-element shard
+and one all-gather of a 202,383,360-parameter layer unit."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sharded_optimizer_step_gb300 as ss
+import synth
+from oracle.numerics import AdamWConfig
+from sharded_optimizer_step_gb300.engine import RankShardOptimizer
+from synth import workloads as W
+from tests._cmp import assert_bf16, assert_bits, assert_f32
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    ss.build()
+    synth.build_dev()
+    yield
+    torch.cuda.empty_cache()
+
+
+def _hp(w):
+    return (AdamWConfig(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay),
+            ss.AdamW(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay))
+
+
+def _host_bf16(t):
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def _sample(n, k, rng, extra=()):
+    idx = set(int(i) for i in rng.integers(0, n, size=min(k, n)))
+    idx.update(i for i in range(min(n, 16)))
+    idx.update(i for i in range(max(0, n - 16), n))
+    idx.update(int(i) for i in extra if 0 <= i < n)
+    return np.array(sorted(idx), dtype=np.int64)
+
+
+# --------------------------------------------------- 9.4M unit, every element
+
+def test_unit_9m_every_element():
+    w = W.unit_9m()
+    hp, hpc = _hp(w)
+    nd, M = w.nd, w.micro
+    shapes = w.units[0]
+    numels = w.unit_numels(0)
+    # master weights: the unit's tensors packed into the fp32 FlatParameter
+    host_t, dev_t, off = [], [], 0
+    for n, s in zip(numels, shapes):
+        h = synth.host_fill(w.master_stream(0), off, n, "f32")
+        host_t.append(h.reshape(s))
+        dev_t.append(torch.from_numpy(h).to(DEV).view(s))
+        off += n
+    flat = ss.fsdp_flat_pack(dev_t, nd)
+    want_flat, lay = oracle.flat_pack(host_t, nd)
+    S, P = lay.shard, lay.padded
+    torch.cuda.synchronize()
+    assert_bits(flat.cpu().numpy(), want_flat, "packed master")
+
+    accs, accs_h = [], []
+    g = torch.empty(P, dtype=torch.bfloat16, device=DEV)
+    for q in range(nd):
+        acc = torch.empty(P, dtype=torch.float32, device=DEV)
+        micro_h = []
+        for j in range(M):
+            st = w.grad_stream(1, q, j, 0)
+            synth.dev_fill(st, g)
+            micro_h.append(synth.host_fill(st, 0, P, "bf16"))
+            ss.fsdp_grad_accumulate(g, acc, float(np.float32(1.0 / M)), j == 0)
+        torch.cuda.synchronize()
+        assert_bits(_host_bf16(g), micro_h[-1], "generator")
+        accs.append(acc)
+        accs_h.append(oracle.grad_accumulate(micro_h, np.float32(1.0 / M)))
+        assert_bits(acc.cpu().numpy(), accs_h[-1], f"accumulator rank {q}")
+
+    shards = []
+    for r in range(nd):
+        master = flat[r * S:(r + 1) * S].clone()
+        m = torch.zeros(S, device=DEV)
+        v = torch.zeros(S, device=DEV)
+        out = torch.empty(S, dtype=torch.bfloat16, device=DEV)
+        ss.fsdp_rs_avg_adamw_cast([a[r * S:(r + 1) * S] for a in accs], master, m, v, out, hpc, 1)
+        z = np.zeros(S, np.float32)
+        p1, m1, v1, o1 = oracle.fsdp_shard_step(accs_h, r, S, want_flat[r * S:(r + 1) * S], z, z,
+                                                hp, 1)
+        torch.cuda.synchronize()
+        for name, got, want in (("master", master, p1), ("m", m, m1), ("v", v, v1)):
+            gh = got.cpu().numpy()
+            assert_f32(gh, want, f"{name} rank {r}")
+            assert_bits(gh, want, f"{name} rank {r}")
+        assert_bf16(_host_bf16(out), o1, f"bf16 rank {r}")
+        assert_bits(_host_bf16(out), o1, f"bf16 rank {r}")
+        shards.append((out, o1))
+
+    full = torch.empty(P, dtype=torch.bfloat16, device=DEV)
+    ss.fsdp_ag_unpack([s for s, _ in shards], full)
+    want_full, want_views = oracle.ag_unpack([o for _, o in shards], lay, shapes)
+    views = ss.fsdp_views(full, shapes, nd)
+    torch.cuda.synchronize()
+    assert_bits(_host_bf16(full), want_full, "gathered unit")
+    for v, wv in zip(views, want_views):
+        assert tuple(v.shape) == wv.shape
+        assert_bits(_host_bf16(v), wv, "view")
+
+
+# ------------------------------------- per-unit emulation of all N_d ranks
+
+def _run_all_ranks(w, sample_per_unit=1024, seed=0):
+    """Every rank of every unit, all steps; oracle on sampled shard positions.
+    Fused outputs land in per-rank shard buffers that the all-gather copies
+    into the unit's full flat buffer."""
+    hp, hpc = _hp(w)
+    nd, M = w.nd, w.micro
+    rng = np.random.default_rng(seed)
+    maxP = max(w.unit_padded(u) for u in range(len(w.units)))
+    g = torch.empty(maxP, dtype=torch.bfloat16, device=DEV)
+    acc = [torch.empty(maxP, dtype=torch.float32 if M > 1 else torch.bfloat16, device=DEV)
+           for _ in range(nd)]
+    state = []
+    for u in range(len(w.units)):
+        S, P = w.unit_shard(u), w.unit_padded(u)
+        master = torch.empty(P, dtype=torch.float32, device=DEV)
+        synth.dev_fill(w.master_stream(u), master)
+        if P > w.unit_total(u):
+            master[w.unit_total(u):].zero_()
+        ranks = []
+        for r in range(nd):
+            idx = _sample(S, sample_per_unit, rng)
+            flat_idx = r * S + idx
+            p0 = synth.host_gather(w.master_stream(u), flat_idx, "f32")
+            p0[flat_idx >= w.unit_total(u)] = 0
+            ranks.append(dict(master=master[r * S:(r + 1) * S], m=torch.zeros(S, device=DEV),
+                              v=torch.zeros(S, device=DEV),
+                              out=torch.empty(S, dtype=torch.bfloat16, device=DEV),
+                              idx=idx, p=p0, mm=np.zeros(idx.size, np.float32),
+                              vv=np.zeros(idx.size, np.float32), ob=None))
+        state.append(dict(S=S, P=P, ranks=ranks,
+                          full=torch.empty(P, dtype=torch.bfloat16, device=DEV)))
+
+    for t in range(1, w.steps + 1):
+        for u, us in enumerate(state):
+            S, P, T = us["S"], us["P"], w.unit_total(u)
+            for q in range(nd):
+                for j in range(M):
+                    dst = (g if M > 1 else acc[q])[:P]
+                    synth.dev_fill(w.grad_stream(t, q, j, u), dst)
+                    if P > T:
+                        dst[T:].zero_()
+                    if M > 1:
+                        ss.fsdp_grad_accumulate(dst, acc[q][:P], float(np.float32(1.0 / M)),
+                                                j == 0)
+            for r, rs in enumerate(us["ranks"]):
+                ss.fsdp_rs_avg_adamw_cast([a[r * S:(r + 1) * S] for a in acc], rs["master"],
+                                          rs["m"], rs["v"], rs["out"], hpc, t)
+            ss.fsdp_ag_unpack([rs["out"] for rs in us["ranks"]], us["full"])
+            # oracle on the sampled positions of every rank
+            for r, rs in enumerate(us["ranks"]):
+                flat_idx = r * S + rs["idx"]
+                contribs = []
+                for q in range(nd):
+                    micro = []
+                    for j in range(M):
+                        gv = synth.host_gather(w.grad_stream(t, q, j, u), flat_idx, "bf16")
+                        gv[flat_idx >= T] = 0
+                        micro.append(gv)
+                    contribs.append(oracle.grad_accumulate(micro, np.float32(1.0 / M))
+                                    if M > 1 else micro[0])
+                rs["p"], rs["mm"], rs["vv"], rs["ob"] = oracle.fsdp_shard_step(
+                    contribs, 0, rs["idx"].size, rs["p"], rs["mm"], rs["vv"], hp, t)
+    torch.cuda.synchronize()
+    for u, us in enumerate(state):
+        S = us["S"]
+        full_h = None
+        for r, rs in enumerate(us["ranks"]):
+            it = torch.from_numpy(rs["idx"]).to(DEV)
+            assert_f32(rs["master"][it].cpu().numpy(), rs["p"], f"unit {u} rank {r} master")
+            assert_bits(rs["master"][it].cpu().numpy(), rs["p"], f"unit {u} rank {r} master")
+            assert_bits(rs["m"][it].cpu().numpy(), rs["mm"], f"unit {u} rank {r} m")
+            assert_bits(rs["v"][it].cpu().numpy(), rs["vv"], f"unit {u} rank {r} v")
+            assert_bits(_host_bf16(rs["out"][it]), rs["ob"], f"unit {u} rank {r} bf16")
+            # the gathered buffer holds every rank's shard at its slot
+            assert torch.equal(us["full"][r * S:(r + 1) * S].view(torch.int16),
+                               rs["out"].view(torch.int16))
+            assert_bf16(_host_bf16(us["full"][r * S + it]), rs["ob"], "gathered")
+        del full_h
+
+
+def test_gpt2_small_all_units_all_ranks():
+    _run_all_ranks(W.gpt2_small(), sample_per_unit=512)
+
+
+def test_llama_1b_all_units_all_ranks_with_accumulation_and_outliers():
+    _run_all_ranks(W.llama_1b(), sample_per_unit=256)
+
+
+# ------------------------------------------ Llama-7B rank view (bench launch)
+
+def test_llama_7b_rank_view_as_benchmarked():
+    w = W.llama_7b_rank_view()
+    hp, hpc = _hp(w)
+    r = w.extra["rank"]
+    opt = RankShardOptimizer(w.units, w.nd, r, hpc, device=DEV)
+    assert opt.shard_total == 842_301_952
+    W.dev_fill_rank_master(w, r, opt.master)
+    rng = np.random.default_rng(7)
+    parts, total = W.rank_shard_index(w)
+    bounds = [s for _, s, _ in parts] + [s - 1 for _, s, _ in parts[1:]]
+    idx = _sample(total, 200_000, rng, extra=bounds)
+    p = W.host_gather_rank_master(w, r, idx)
+    m = np.zeros(idx.size, np.float32)
+    v = np.zeros(idx.size, np.float32)
+    for t in range(1, w.steps + 1):
+        for q in range(w.nd):
+            W.dev_fill_rank_grad(w, t, r, q, 0, opt.grad_in[q])
+        launches = ss.launch_count()
+        opt.step()
+        assert ss.launch_count() - launches == 1      # one fused launch over the shard
+        contribs = [W.host_gather_rank_grad(w, t, r, q, 0, idx) for q in range(w.nd)]
+        p, m, v, ob = oracle.fsdp_shard_step(contribs, 0, idx.size, p, m, v, hp, t)
+    torch.cuda.synchronize()
+    it = torch.from_numpy(idx).to(DEV)
+    assert_f32(opt.master[it].cpu().numpy(), p, "master")
+    assert_bits(opt.master[it].cpu().numpy(), p, "master")
+    assert_bits(opt.m[it].cpu().numpy(), m, "m")
+    assert_bits(opt.v[it].cpu().numpy(), v, "v")
+    assert_bits(_host_bf16(opt.params[it]), ob, "bf16")
+
+    # all-gather of one layer unit: the other ranks' shards are seeded inputs
+    u = w.extra["ag_unit"]
+    S, P = w.unit_shard(u), w.unit_padded(u)
+    assert P == 202_383_360
+    peers = []
+    for q in range(w.nd):
+        s = torch.empty(S, dtype=torch.bfloat16, device=DEV)
+        if q != r:
+            synth.dev_fill(w.peer_shard_stream(w.steps, q, u), s)
+        peers.append(s)
+    full = torch.empty(P, dtype=torch.bfloat16, device=DEV)
+    views = opt.gather_unit(u, peers, full)
+    torch.cuda.synchronize()
+    assert [tuple(x.shape) for x in views] == [tuple(s) for s in w.units[u]]
+    for q in range(w.nd):
+        src = opt.unit_slice(opt.params, u) if q == r else peers[q]
+        assert torch.equal(full[q * S:(q + 1) * S].view(torch.int16), src.view(torch.int16))
+    loc = _sample(S, 4096, rng)
+    for q in range(w.nd):
+        if q == r:
+            continue
+        want = synth.host_gather(w.peer_shard_stream(w.steps, q, u), loc, "bf16")
+        assert_bits(_host_bf16(full[q * S + torch.from_numpy(loc).to(DEV)]), want, "peer shard")
+
+
+# ------------------------------------------------------- DDP bucket sweep
+
+def test_ddp_bucket_sweep_full_size():
+    w = W.ddp_sweep()
+    hp, hpc = _hp(w)
+    nd = w.nd
+    numels = w.unit_numels(0)
+    total = sum(numels)
+    rng = np.random.default_rng(3)
+    grads = [torch.empty(total, dtype=torch.bfloat16, device=DEV) for _ in range(nd)]
+    outs = {}
+    for mib in w.extra["caps_mib"]:
+        off, of, boff = ss.ddp_bucket_plan(numels, 2, mib << 20)
+        assert (off, of, boff) == tuple(list(x) for x in oracle.bucket_plan(numels, 2, mib << 20))
+        # rank q's gradient of parameter i is seeded per parameter, so the
+        # values do not depend on where the plan puts the parameter
+        for q in range(nd):
+            for i, n in enumerate(numels):
+                synth.dev_fill(w.grad_stream(1, q, 0, i), grads[q][off[i]:off[i] + n])
+        out = torch.empty(total, dtype=torch.bfloat16, device=DEV)
+        before = ss.launch_count()
+        ss.ddp_bucket_allreduce_avg(grads, boff, out)
+        assert ss.launch_count() - before == len(boff) - 1
+        # back to registration order for the comparison across caps
+        outs[mib] = torch.cat([out[off[i]:off[i] + n] for i, n in enumerate(numels)])
+        # oracle on sampled elements of sampled parameters
+        for i in rng.choice(len(numels), size=12, replace=False):
+            loc = _sample(numels[i], 512, rng)
+            gq = [synth.host_gather(w.grad_stream(1, q, 0, int(i)), loc, "bf16")
+                  for q in range(nd)]
+            want = oracle.bucket_allreduce_avg(gq, [0, loc.size])
+            got = _host_bf16(out[off[i] + torch.from_numpy(loc).to(DEV)])
+            assert_bits(got, want, f"cap {mib} MiB param {i}")
+    ref = outs[25]
+    for mib, o in outs.items():
+        assert torch.equal(o.view(torch.int16), ref.view(torch.int16)), mib
+    # replicated AdamW over every parameter with the averaged gradient
+    master = torch.empty(total, dtype=torch.float32, device=DEV)
+    synth.dev_fill(w.master_stream(0), master)
+    mm = torch.zeros(total, device=DEV)
+    vv = torch.zeros(total, device=DEV)
+    pb = torch.empty(total, dtype=torch.bfloat16, device=DEV)
+    ss.fsdp_rs_avg_adamw_cast([ref], master, mm, vv, pb, hpc, 1)
+    loc = _sample(total, 100_000, rng)
+    it = torch.from_numpy(loc).to(DEV)
+    p0 = synth.host_gather(w.master_stream(0), loc, "f32")
+    z = np.zeros(loc.size, np.float32)
+    _, p1, m1, v1, pb1 = oracle.ddp_step([_host_bf16(ref[it])], [0, loc.size], p0, z, z, hp, 1)
+    torch.cuda.synchronize()
+    assert_bits(master[it].cpu().numpy(), p1, "master")
+    assert_bits(mm[it].cpu().numpy(), m1, "m")
+    assert_bits(vv[it].cpu().numpy(), v1, "v")
+    assert_bits(_host_bf16(pb[it]), pb1, "params")
