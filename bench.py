@@ -27,7 +27,6 @@ import statistics
 import subprocess
 import sys
 import tempfile
-import threading
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -43,10 +42,14 @@ FUSED_PROFILE = os.path.join(ROOT, "profiles", "fused_step_llama7b_rank_view.md"
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=60)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-chunks", type=int, default=4)
+    ap.add_argument("--e2e-streams", type=int, default=4)
+    ap.add_argument("--layers", type=int, default=0,
+                    help="smaller case: only the first N layer units (for profiler captures)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-e2e", action="store_true")
@@ -153,7 +156,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
@@ -183,6 +186,16 @@ class ClockSampler:
 
 # ------------------------------------------------------------ our arm
 
+def workload(args):
+    from synth import workloads as W
+    w = W.llama_7b_rank_view()
+    if args.layers:
+        # a smaller case of the same kernel: the first N layer units only
+        w.units = w.units[:args.layers]
+        w.name = f"{w.name}_first{args.layers}layers"
+    return w
+
+
 def run_ours(args):
     import torch
     world, rank, local = dist_env()
@@ -190,13 +203,12 @@ def run_ours(args):
     torch.cuda.set_device(local)
     import __graft_entry__
     __graft_entry__.build()
-    import numpy as np
     import sharded_optimizer_step_gb300 as ss
     import synth
     from sharded_optimizer_step_gb300.engine import RankShardOptimizer
     from synth import workloads as W
 
-    w = W.llama_7b_rank_view()
+    w = workload(args)
     nd = w.nd
     r = rank % nd                       # GPU k holds rank k's view of its own replica
     dev = torch.device("cuda", local)
@@ -241,11 +253,13 @@ def run_ours(args):
     barrier(world)
     torch.cuda.synchronize()
     launches0 = ss.launch_count()
+    torch.cuda.nvtx.range_push("timed_region")
     t_start.record(stream)
     for k in range(args.steps):
         one_step(events[k])
     t_end.record(stream)
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
     barrier(world)
     launches = ss.launch_count() - launches0
     clk = clocks.stop()
@@ -257,6 +271,7 @@ def run_ours(args):
     value = all_bytes / (total_ms_max / 1e3) / 1e9
     ms_per_step = total_ms_max / args.steps
     fused_avg = sum(fused_ms) / len(fused_ms)
+    ag_avg = sum(ag_ms) / len(ag_ms)
     peak, peak_kind = measured_peak()
     achieved = fused_bytes / (fused_avg / 1e3) / 1e9
     traffic_per_elem = profiled_traffic()
@@ -265,8 +280,9 @@ def run_ours(args):
     # step, the gathered unit read back every step
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, torch, opt, peers, full, u, r, nd, stream, step_bytes)
-        e2e["value"] = allreduce_sum(world, e2e.pop("bytes")) / allreduce_max(world, e2e.pop("seconds")) / 1e9
+        e2e = run_e2e(args, torch, ss, opt, peers, full, u, r, nd, stream, step_bytes)
+        e2e["value"] = round(allreduce_sum(world, e2e.pop("bytes"))
+                             / allreduce_max(world, e2e.pop("seconds")) / 1e9, 1)
 
     cpu = None
     if rank == 0 and not args.no_cpu:
@@ -278,20 +294,27 @@ def run_ours(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded counter-based generator on the device; no data set or weights)",
-            "config": {"workload": w.name, "model_shape": "Llama-style 7B, 32 layer units + embedding unit",
+            "config": {"workload": w.name,
+                       "model_shape": f"Llama-style 7B, {len(w.units)} FSDP units",
                        "psi": w.psi, "nd": nd, "rank": r, "shard_elements": S,
-                       "grad_dtype": "bf16", "state_dtype": "f32",
-                       "ag_unit_params": Pu, "step": "fused rs_avg+AdamW+bf16 cast over the shard, then all-gather of one layer unit",
+                       "grad_dtype": "bf16", "state_dtype": "f32", "ag_unit_params": Pu,
+                       "step": "fused rs_avg+AdamW+bf16 cast over the rank shard (1 launch), "
+                               "then all-gather of one layer unit (1 launch)",
                        "bytes_per_step": step_bytes,
-                       "l2": "no flush: each step streams ~36 GB, >> 129 MB L2"},
+                       "l2": f"no flush: each step streams {step_bytes / 1e9:.1f} GB vs a 129 MB L2"},
             "params_per_s": round(S * world / (ms_per_step / 1e3), 1),
-            "fused_ms": round(fused_avg, 4), "ag_ms": round(sum(ag_ms) / len(ag_ms), 4),
-            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                         "frac": round(achieved / peak, 4),
-                         "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback 6800 GB/s",
+            "kernels": {"fused_ms": round(fused_avg, 4),
+                        "fused_gbs": round(achieved, 1),
+                        "ag_ms": round(ag_avg, 4),
+                        "ag_gbs": round(ag_bytes / (ag_avg / 1e3) / 1e9, 1)},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                         "unit": "GB/s", "frac": round(achieved / peak, 4),
+                         "peak_source": ("measured: MEASURED_PEAKS.json hbm_gbs (copy, burst)"
+                                         if peak_kind == "measured" else "fallback 6800 GB/s"),
                          "kernel": "rs_adamw_cast_vec8<8,bf16>",
                          "algorithmic_bytes_per_launch": fused_bytes,
-                         "traffic": None if traffic_per_elem is None else round(traffic_per_elem * S)},
+                         "traffic": (None if traffic_per_elem is None
+                                     else round(traffic_per_elem * S))},
             "e2e": e2e,
             "gpu_launches": launches,
             "clocks": clk,
@@ -303,7 +326,11 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def run_e2e(args, torch, opt, peers, full, u, r, nd, stream, step_bytes):
+def run_e2e(args, torch, ss, opt, peers, full, u, r, nd, stream, step_bytes):
+    """Host-resident gradients and peer shards copied in every step, the
+    gathered unit copied out.  The shard is cut into chunks: each chunk's 8
+    contributions are copied on a pool of copy streams while the fused
+    update of the previous chunk runs on the compute stream."""
     S = opt.shard_total
     host_g = [torch.empty(S, dtype=torch.bfloat16, pin_memory=True) for _ in range(nd)]
     for q in range(nd):
@@ -317,15 +344,43 @@ def run_e2e(args, torch, opt, peers, full, u, r, nd, stream, step_bytes):
     h2d = sum(x.numel() * 2 for x in host_g) + sum(x.numel() * 2 for q, x in enumerate(host_p)
                                                    if q != r)
     d2h = host_out.numel() * 2
+    n_chunks = max(1, args.e2e_chunks)
+    step8 = -(-S // (8 * n_chunks)) * 8
+    bounds = [min(S, c * step8) for c in range(n_chunks)] + [S]
+    copy_streams = [torch.cuda.Stream(device=stream.device) for _ in range(max(1, args.e2e_streams))]
 
     def e2e_step():
-        for q in range(nd):
-            opt.grad_in[q].copy_(host_g[q], non_blocking=True)
+        prev = stream.record_event()          # last step's kernels are done with the buffers
+        k = 0
+        chunk_ready = []
+        for c in range(n_chunks):
+            a, b = bounds[c], bounds[c + 1]
+            evs = []
+            for q in range(nd):
+                cs = copy_streams[k % len(copy_streams)]
+                k += 1
+                cs.wait_event(prev)
+                with torch.cuda.stream(cs):
+                    opt.grad_in[q][a:b].copy_(host_g[q][a:b], non_blocking=True)
+                evs.append(cs.record_event())
+            chunk_ready.append(evs)
+        peer_evs = []
         for q in range(nd):
             if q != r:
-                peers[q].copy_(host_p[q], non_blocking=True)
-        opt.step()
-        opt.gather_unit(u, peers, full)
+                cs = copy_streams[k % len(copy_streams)]
+                k += 1
+                cs.wait_event(prev)
+                with torch.cuda.stream(cs):
+                    peers[q].copy_(host_p[q], non_blocking=True)
+                peer_evs.append(cs.record_event())
+        opt.begin_step()
+        for c in range(n_chunks):
+            for e in chunk_ready[c]:
+                stream.wait_event(e)
+            opt.update_range(bounds[c], bounds[c + 1], stream=stream)
+        for e in peer_evs:
+            stream.wait_event(e)
+        opt.gather_unit(u, peers, full, stream=stream)
         host_out.copy_(full, non_blocking=True)
 
     e2e_step()
@@ -340,8 +395,10 @@ def run_e2e(args, torch, opt, peers, full, u, r, nd, stream, step_bytes):
     sec = a.elapsed_time(b) / 1e3
     return {"unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": args.e2e_steps, "ms_per_step": round(sec * 1e3 / args.e2e_steps, 3),
+            "h2d_gbs": round(h2d * args.e2e_steps / sec / 1e9, 1),
             "bytes": step_bytes * args.e2e_steps, "seconds": sec,
-            "path": "torch pinned-host copies + C-ABI calls on one stream"}
+            "path": (f"pinned host buffers -> {len(copy_streams)} copy streams, shard in "
+                     f"{n_chunks} chunks overlapped with the fused update; C-ABI calls")}
 
 
 # ------------------------------------------------------- CPU baseline / reference

@@ -52,10 +52,22 @@ class RankShardOptimizer:
         return buf[self.starts[u]:self.starts[u] + self.layouts[u].shard]
 
     def step(self, stream=None):
-        """Reduce-scatter average + AdamW + bf16 cast over the whole rank shard."""
+        """Reduce-scatter average + AdamW + bf16 cast over the whole rank shard
+        (one launch)."""
         self.t += 1
         fsdp_rs_avg_adamw_cast(self.grad_in, self.master, self.m, self.v, self.params, self.hp,
                                self.t, stream=stream)
+
+    def begin_step(self):
+        """Advance the step count for an update issued piece by piece with
+        ``update_range`` (e.g. overlapped with the arrival of the gradients)."""
+        self.t += 1
+
+    def update_range(self, a: int, b: int, stream=None):
+        """The fused update of shard positions [a, b) at the current step count."""
+        sl = slice(a, b)
+        fsdp_rs_avg_adamw_cast([g[sl] for g in self.grad_in], self.master[sl], self.m[sl],
+                               self.v[sl], self.params[sl], self.hp, self.t, stream=stream)
 
     def gather_unit(self, u, peer_shards, full, stream=None):
         """All-gather unit u: ``peer_shards[q]`` is rank q's bf16 shard (this
