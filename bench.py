@@ -34,7 +34,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "fused shard-step HBM GB/s (% of GB300 peak), params/s at Psi=7B, N_d=8"
-KERNEL_SOURCES = ["sharded_optimizer_step_gb300/csrc/step.cu",
+KERNEL_SOURCES = ["sharded_optimizer_step_gb300/csrc/step_tma.cu",
                   "sharded_optimizer_step_gb300/csrc/common.cuh"]
 FUSED_PROFILE = os.path.join(ROOT, "profiles", "fused_step_llama7b_rank_view.md")
 
@@ -263,6 +263,9 @@ def run_ours(args):
     barrier(world)
     launches = ss.launch_count() - launches0
     clk = clocks.stop()
+    status = ss.device_status()
+    if status:
+        raise RuntimeError(f"a TMA-staged wait ran out during the timed steps (status {status})")
     total_ms = t_start.elapsed_time(t_end)
     fused_ms = [e[0].elapsed_time(e[1]) for e in events]
     ag_ms = [e[1].elapsed_time(e[2]) for e in events]
@@ -311,7 +314,7 @@ def run_ours(args):
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "peak_source": ("measured: MEASURED_PEAKS.json hbm_gbs (copy, burst)"
                                          if peak_kind == "measured" else "fallback 6800 GB/s"),
-                         "kernel": "rs_adamw_cast_vec8<8,bf16>",
+                         "kernel": "rs_adamw_cast_tma<bf16> (TMA-staged, N_d = 8)",
                          "algorithmic_bytes_per_launch": fused_bytes,
                          "traffic": (None if traffic_per_elem is None
                                      else round(traffic_per_elem * S))},

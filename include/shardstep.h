@@ -168,8 +168,16 @@ int fsdp_grad_accumulate(const uint16_t* g, float* acc, int64_t n, float scale, 
  *   out_bf16         device, S bf16; may be the rank's slot of the full flat
  *                    parameter buffer (full + r*S).
  * The gradient inputs must not overlap any output; master, m, v and out_bf16
- * must not overlap one another.  Any alignment is accepted; when every
- * pointer is 16-byte aligned the kernel moves 16 bytes per access.
+ * must not overlap one another.  Any alignment is accepted.  Kernels, by
+ * decreasing speed: (1) TMA-staged -- needs S >= 4096, master / m / v and
+ * every slice 16-byte aligned, out_bf16 8-byte aligned, and two stages of
+ * 2048 x (N_d x grad bytes + 12) bytes within the per-block shared-memory
+ * limit (N_d <= 21 for bf16, <= 10 for fp32 on GB300); (2) register-staged,
+ * 4 elements per access -- needs state 16-byte, bf16 slices and out 8-byte,
+ * fp32 slices 16-byte alignment; (3) one element per access.  All three
+ * compute the same bits.  A TMA-staged launch whose internal wait runs out
+ * (about 2 s) sets a bit in the device status word; see
+ * shardstep_device_status. 
  * Errors: INVALID (null pointer, S < 0, step < 1, bad dtype, overlap),
  * CAPACITY (nd > SHARDSTEP_MAX_ND), CUDA (launch refused). */
 int fsdp_rs_avg_adamw_cast(const void* const* grad_slices, int32_t grad_dtype, int32_t nd,
@@ -252,6 +260,23 @@ double shardstep_state_bytes(double psi, int32_t nd, int32_t stage, double k);
 double shardstep_comm_bytes(double psi, int32_t nd, int32_t kind, int32_t exact);
 
 /* ------------------------------------------------------------ misc */
+
+/* Selects the kernels fsdp_rs_avg_adamw_cast may use, process-wide.
+ * SHARDSTEP_PATH_AUTO (default) and _TMA use the TMA-staged kernel whenever
+ * the arguments allow it; _REGISTER uses only the register-staged kernels.
+ * Returns the previous setting, or INVALID for an unknown value. */
+#define SHARDSTEP_PATH_AUTO 0
+#define SHARDSTEP_PATH_REGISTER 1
+#define SHARDSTEP_PATH_TMA 2
+int32_t shardstep_set_fused_path(int32_t path);
+
+/* Watchdog word of the current device: bit 0 = a consumer's wait for a
+ * staged tile ran out, bit 1 = the producer's wait for a free stage ran out
+ * (the launch then returned early and its results are incomplete).  0 means
+ * every TMA-staged launch so far completed its waits.  Synchronous (copies
+ * the word to *status); clear != 0 resets it afterwards.  Errors: INVALID
+ * (NULL), CUDA. */
+int shardstep_device_status(uint32_t* status, int32_t clear);
 
 /* Description of the last error on the calling thread ("" if none). */
 const char* shardstep_last_error(void);

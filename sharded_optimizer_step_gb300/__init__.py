@@ -22,6 +22,7 @@ __all__ = [
     "build", "ShardstepError", "AdamW", "Layout", "fsdp_layout", "fsdp_flat_pack", "fsdp_views",
     "fsdp_grad_accumulate", "fsdp_rs_avg_adamw_cast", "fsdp_ag_unpack", "ddp_bucket_plan",
     "ddp_bucket_allreduce_avg", "state_bytes", "comm_bytes", "launch_count", "MAX_ND",
+    "set_fused_path", "device_status",
 ]
 
 
@@ -258,6 +259,26 @@ def comm_bytes(psi: float, nd: int, kind: str, exact: bool = False) -> float:
     if r < 0:
         raise ValueError("bad kind or nd")
     return r
+
+
+def set_fused_path(path: str) -> str:
+    """Which kernels the fused step may use: "auto" (TMA-staged when the
+    arguments allow), "register" (register-staged only) or "tma".  Returns
+    the previous setting."""
+    codes = {"auto": _capi.PATH_AUTO, "register": _capi.PATH_REGISTER, "tma": _capi.PATH_TMA}
+    names = {v: k for k, v in codes.items()}
+    prev = _capi.lib().shardstep_set_fused_path(codes[path])
+    if prev < 0:
+        _capi.check("shardstep_set_fused_path", prev)
+    return names[prev]
+
+
+def device_status(clear: bool = False) -> int:
+    """Watchdog bits of the current device (0: no TMA-staged wait ran out)."""
+    st = ctypes.c_uint32(0)
+    _capi.check("shardstep_device_status",
+                _capi.lib().shardstep_device_status(ctypes.byref(st), int(bool(clear))))
+    return st.value
 
 
 def launch_count() -> int:

@@ -20,6 +20,9 @@ ERR_INVALID = -1
 ERR_CUDA = -3
 ERR_TIMEOUT = -4
 ERR_CAPACITY = -5
+PATH_AUTO = 0
+PATH_REGISTER = 1
+PATH_TMA = 2
 DTYPE_BF16 = 0
 DTYPE_F32 = 1
 MAX_ND = 64
@@ -51,6 +54,8 @@ SIGNATURES = {
     "shardstep_state_bytes": (c_f64, [c_f64, c_i32, c_i32, c_f64]),
     "shardstep_comm_bytes": (c_f64, [c_f64, c_i32, c_i32, c_i32]),
     "shardstep_last_error": (ctypes.c_char_p, []),
+    "shardstep_set_fused_path": (c_i32, [c_i32]),
+    "shardstep_device_status": (c_i32, [ctypes.POINTER(ctypes.c_uint32), c_i32]),
     "shardstep_launch_count": (c_u64, []),
 }
 

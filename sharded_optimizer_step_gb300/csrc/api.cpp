@@ -18,6 +18,7 @@ namespace {
 
 thread_local std::string g_error;
 std::atomic<uint64_t> g_launches{0};
+std::atomic<int> g_fused_path{SHARDSTEP_PATH_AUTO};
 
 int fail(int code, const char* fmt, ...) {
     char buf[512];
@@ -136,6 +137,21 @@ int device_sms() {
     return sms;
 }
 
+int device_smem_optin() {
+    static std::atomic<int> cache[256];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return 0;
+    int v = cache[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+    int optin = 0;
+    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess ||
+        optin < 1)
+        return 0;
+    cache[dev].store(optin, std::memory_order_relaxed);
+    return optin;
+}
+
 int resident_blocks(const void* kernel, int threads) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 1;
@@ -162,6 +178,22 @@ extern "C" {
 const char* shardstep_last_error(void) { return g_error.c_str(); }
 
 uint64_t shardstep_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int32_t shardstep_set_fused_path(int32_t path) {
+    if (path != SHARDSTEP_PATH_AUTO && path != SHARDSTEP_PATH_REGISTER &&
+        path != SHARDSTEP_PATH_TMA)
+        return fail(SHARDSTEP_ERR_INVALID, "unknown path %d", path);
+    return g_fused_path.exchange(path);
+}
+
+int shardstep_device_status(uint32_t* status, int32_t clear) {
+    if (status == nullptr) return fail(SHARDSTEP_ERR_INVALID, "status is NULL");
+    unsigned int s = 0;
+    cudaError_t e = read_device_status(&s, clear != 0);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device status word");
+    *status = s;
+    return ok();
+}
 
 int fsdp_layout(const int64_t* numels, int32_t n, int32_t nd, shardstep_layout_info_t* info,
                 int64_t* offsets, int64_t* lo, int64_t* hi) {
@@ -348,8 +380,11 @@ int fsdp_rs_avg_adamw_cast(const void* const* grad_slices, int32_t grad_dtype, i
         for (int b = a + 1; b < 4; ++b)
             if (overlap(outs[a], outs[b]))
                 return fail(SHARDSTEP_ERR_INVALID, "outputs %d and %d overlap", a, b);
+    // vector path: 4 elements per access -> 16-byte state, 8-byte bf16 (16-byte
+    // fp32) gradient slices, 8-byte bf16 output
     PtrTable tab;
-    bool vec = aligned(master, 16) && aligned(m, 16) && aligned(v, 16) && aligned(out_bf16, 16);
+    const uintptr_t gvec = grad_dtype == SHARDSTEP_DTYPE_F32 ? 16 : 8;
+    bool vec = aligned(master, 16) && aligned(m, 16) && aligned(v, 16) && aligned(out_bf16, 8);
     for (int32_t q = 0; q < nd; ++q) {
         const void* p = grad_slices[q];
         if (p == nullptr) return fail(SHARDSTEP_ERR_INVALID, "grad_slices[%d] is NULL", q);
@@ -359,13 +394,23 @@ int fsdp_rs_avg_adamw_cast(const void* const* grad_slices, int32_t grad_dtype, i
         for (int a = 0; a < 4; ++a)
             if (overlap(gsn, outs[a]))
                 return fail(SHARDSTEP_ERR_INVALID, "grad_slices[%d] overlaps an output", q);
-        vec = vec && aligned(p, 16);
+        vec = vec && aligned(p, gvec);
         tab.p[q] = p;
     }
     for (int32_t q = nd; q < SHARDSTEP_MAX_ND; ++q) tab.p[q] = nullptr;
-    cudaError_t e = launch_rs_adamw_cast(tab, nd, grad_dtype == SHARDSTEP_DTYPE_F32, S, master, m,
-                                         v, out_bf16, adam_scalars(*hp), mean_op(nd), vec,
-                                         static_cast<cudaStream_t>(stream));
+    const bool f32g = grad_dtype == SHARDSTEP_DTYPE_F32;
+    // TMA-staged path: bulk copies need 16-byte aligned sources; the two
+    // stages must fit in shared memory
+    bool tma = g_fused_path.load(std::memory_order_relaxed) != SHARDSTEP_PATH_REGISTER &&
+               S >= kTmaMinElements && aligned(master, 16) && aligned(m, 16) &&
+               aligned(v, 16) && aligned(out_bf16, 8);
+    for (int32_t q = 0; q < nd && tma; ++q) tma = aligned(tab.p[q], 16);
+    if (tma) tma = tma_step_smem_bytes(nd, f32g) <= static_cast<size_t>(device_smem_optin());
+    cudaError_t e =
+        tma ? launch_rs_adamw_cast_tma(tab, nd, f32g, S, master, m, v, out_bf16, adam_scalars(*hp),
+                                       mean_op(nd), static_cast<cudaStream_t>(stream))
+            : launch_rs_adamw_cast(tab, nd, f32g, S, master, m, v, out_bf16, adam_scalars(*hp),
+                                   mean_op(nd), vec, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "fused step kernel launch");
     return ok();
 }
@@ -433,10 +478,10 @@ int ddp_bucket_allreduce_avg(const uint16_t* const* rank_grads, int32_t nd,
         const int64_t a = bucket_offsets[b], n = bucket_offsets[b + 1] - a;
         if (n == 0) continue;
         PtrTable tab;
-        bool vec = aligned(out + a, 16);
+        bool vec = aligned(out + a, 8);
         for (int32_t q = 0; q < SHARDSTEP_MAX_ND; ++q) {
             tab.p[q] = q < nd ? rank_grads[q] + a : nullptr;
-            if (q < nd) vec = vec && aligned(tab.p[q], 16);
+            if (q < nd) vec = vec && aligned(tab.p[q], 8);
         }
         cudaError_t e = launch_allreduce_avg(tab, nd, n, out + a, mo, vec,
                                              static_cast<cudaStream_t>(stream));

@@ -24,6 +24,15 @@ __device__ __forceinline__ uint4 ld_once(const void* p) {
     return r;
 }
 
+// 8-byte variant of ld_once.
+__device__ __forceinline__ uint2 ld_once8(const void* p) {
+    uint2 r;
+    asm("ld.global.nc.L1::no_allocate.L2::256B.v2.u32 {%0,%1}, [%2];"
+        : "=r"(r.x), "=r"(r.y)
+        : "l"(p));
+    return r;
+}
+
 // Read of data the same thread writes back later in the kernel (coherent
 // path).  Each address is read once, before the store that depends on it.
 __device__ __forceinline__ uint4 ld_rw(const void* p) {
@@ -40,6 +49,22 @@ __device__ __forceinline__ void st_stream(void* p, uint4 v) {
                  "r"(v.z), "r"(v.w)
                  : "memory");
 }
+
+__device__ __forceinline__ void st_stream8(void* p, uint2 v) {
+    asm volatile("st.global.cs.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
+
+// Streaming (evict-first) accesses through the compiler's own intrinsics:
+// unlike volatile asm with a memory clobber, these let the scheduler overlap
+// one iteration's stores with the next iteration's loads.
+__device__ __forceinline__ uint2 ldcs8(const void* p) {
+    return __ldcs(reinterpret_cast<const uint2*>(p));
+}
+__device__ __forceinline__ uint4 ldcs16(const void* p) {
+    return __ldcs(reinterpret_cast<const uint4*>(p));
+}
+__device__ __forceinline__ void stcs8(void* p, uint2 v) { __stcs(reinterpret_cast<uint2*>(p), v); }
+__device__ __forceinline__ void stcs16(void* p, uint4 v) { __stcs(reinterpret_cast<uint4*>(p), v); }
 
 // ------------------------------------------------------------------- bf16
 

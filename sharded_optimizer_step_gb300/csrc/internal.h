@@ -54,6 +54,17 @@ cudaError_t launch_rs_adamw_cast(const PtrTable& tab, int nd, bool f32_grads, in
                                  float* master, float* m, float* v, uint16_t* out,
                                  const AdamScalars& c, const MeanOp& mo, bool vec,
                                  cudaStream_t stream);
+// TMA-staged fused step (step_tma.cu): dynamic shared memory it needs, the
+// launch, and the device watchdog status word.
+size_t tma_step_smem_bytes(int nd, bool f32_grads);
+cudaError_t launch_rs_adamw_cast_tma(const PtrTable& tab, int nd, bool f32_grads, int64_t S,
+                                     float* master, float* m, float* v, uint16_t* out,
+                                     const AdamScalars& c, const MeanOp& mo,
+                                     cudaStream_t stream);
+cudaError_t read_device_status(unsigned int* status, bool clear);
+int device_smem_optin();  // max dynamic shared memory per block (cached)
+constexpr int64_t kTmaMinElements = 4096;
+
 cudaError_t launch_allreduce_avg(const PtrTable& tab, int nd, int64_t n, uint16_t* out,
                                  const MeanOp& mo, bool vec, cudaStream_t stream);
 cudaError_t launch_copy(const CopyTable& t, cudaStream_t stream);

@@ -27,6 +27,18 @@ def _built():
         pytest.skip("no CUDA device")
     ss.build()
     synth.build_dev()
+    yield
+    # no TMA-staged wait ran out during the module
+    assert ss.device_status() == 0
+
+
+@pytest.fixture(params=["auto", "register"])
+def path(request):
+    """Run a fused-step test on the TMA-staged kernel (auto: used whenever the
+    arguments allow) and on the register-staged kernels only."""
+    prev = ss.set_fused_path(request.param)
+    yield request.param
+    ss.set_fused_path(prev)
 
 
 def dev_bf16(u16, shift=0):
@@ -64,10 +76,10 @@ def _grads(seed, nd, P, dtype, step):
 # ------------------------------------------------------------ fused step
 
 @pytest.mark.parametrize("nd", [1, 2, 3, 4, 5, 8, 16])
-@pytest.mark.parametrize("S", [1, 13, 4099])
+@pytest.mark.parametrize("S", [1, 13, 4099, 6151])
 @pytest.mark.parametrize("gdt", ["bf16", "f32"])
 @pytest.mark.parametrize("shift", [0, 1])
-def test_fused_step_matches_oracle(nd, S, gdt, shift):
+def test_fused_step_matches_oracle(nd, S, gdt, shift, path):
     seed = nd * 1000 + S + (7 if gdt == "f32" else 0)
     r = (S + 2 * nd) % nd
     P = nd * S
@@ -93,8 +105,13 @@ def test_fused_step_matches_oracle(nd, S, gdt, shift):
 
 @pytest.mark.parametrize("nd,gdt,S", [(8, "bf16", 152 * 256 * 8 * 2 + 5),
                                       (4, "f32", 152 * 256 * 8 + 8 * 37 + 3),
-                                      (8, "bf16", 1 << 20)])
-def test_fused_step_multi_tile(nd, gdt, S):
+                                      (8, "bf16", 1 << 20),
+                                      (8, "bf16", 2048 * 152 * 3 + 2048 + 8 * 5 + 7),
+                                      (16, "bf16", 2048 * 200 + 1000),
+                                      (8, "f32", 2048 * 160 + 16),
+                                      (21, "bf16", 70001), (22, "bf16", 70001),
+                                      (10, "f32", 70001), (11, "f32", 70001)])
+def test_fused_step_multi_tile(nd, gdt, S, path):
     seed = 5 + S
     P = nd * S
     r = 1 % nd
@@ -115,9 +132,9 @@ def test_fused_step_multi_tile(nd, gdt, S):
     assert_bits(host_bf16(out), ob, "bf16")
 
 
-def test_fused_step_padding_stays_zero():
+def test_fused_step_padding_stays_zero(path):
     # zero gradients and zero master (the padding of a FlatParameter) stay zero
-    S, nd = 1000, 4
+    S, nd = 10000, 4
     z = torch.zeros(S, dtype=torch.bfloat16, device=DEV)
     dp = torch.zeros(S, device=DEV)
     dm = torch.zeros(S, device=DEV)
@@ -129,8 +146,8 @@ def test_fused_step_padding_stays_zero():
     assert not dp.any() and not dm.any() and not dv.any() and not out.float().any()
 
 
-def test_fused_step_output_may_be_the_slot_of_the_full_buffer():
-    nd, S, r = 4, 4099, 2
+def test_fused_step_output_may_be_the_slot_of_the_full_buffer(path):
+    nd, S, r = 4, 40960, 2
     contribs = _grads(11, nd, nd * S, "bf16", 1)
     p = synth.host_fill(synth.normal_stream(11, (99, 2), 0.02), 0, S, "f32")
     dp, dm, dv = dev_f32(p), torch.zeros(S, device=DEV), torch.zeros(S, device=DEV)
