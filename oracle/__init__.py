@@ -28,6 +28,9 @@ Readings taken where the pages are silent (each is repeated where it is used):
   * Padding: zeros at the tail of the unit only, to a multiple of N_d.
   * Accumulation: micro-batches in order inside a rank first, each gradient
     scaled by fl32(1/M) as it is added; the first term starts the sum.
+  * Hybrid sharding: ranks k = g*F + j; the reduce sums inside each group
+    first (the group's reduce-scatter), then across groups (the all-reduce),
+    then divides by N_d.
   * Buckets: parameters walked in reverse registration order, a bucket is
     closed before a parameter that would take it over the cap, a parameter
     larger than the cap gets a bucket to itself, parameters are never split.
@@ -39,13 +42,16 @@ library routines, brute force).  No function is left unpinned.
 from .flat import (Layout, layout, flat_pack, shard_of, sharded_views, ag_unpack,
                    unpack_views)
 from .numerics import (AdamWConfig, adamw_scalars, adamw, bf16_to_f32, f32_to_bf16,
-                       grad_accumulate, rs_avg, fsdp_shard_step)
+                       grad_accumulate, rs_avg, fsdp_shard_step, hybrid_rs_avg,
+                       hybrid_shard_step)
 from .ddp import bucket_plan, bucket_allreduce_avg, ddp_step
-from .ledger import state_bytes_per_gpu, comm_bytes_per_gpu, GB
+from .ledger import (state_bytes_per_gpu, comm_bytes_per_gpu, hybrid_state_bytes_per_gpu,
+                     hybrid_comm_bytes_per_gpu, GB)
 
 __all__ = [
     "Layout", "layout", "flat_pack", "shard_of", "sharded_views", "ag_unpack", "unpack_views",
     "AdamWConfig", "adamw_scalars", "adamw", "bf16_to_f32", "f32_to_bf16", "grad_accumulate",
-    "rs_avg", "fsdp_shard_step", "bucket_plan", "bucket_allreduce_avg", "ddp_step",
-    "state_bytes_per_gpu", "comm_bytes_per_gpu", "GB",
+    "rs_avg", "fsdp_shard_step", "hybrid_rs_avg", "hybrid_shard_step", "bucket_plan",
+    "bucket_allreduce_avg", "ddp_step", "state_bytes_per_gpu", "comm_bytes_per_gpu",
+    "hybrid_state_bytes_per_gpu", "hybrid_comm_bytes_per_gpu", "GB",
 ]

@@ -54,3 +54,29 @@ def comm_bytes_per_gpu(psi: float, nd: int, kind: str, exact: bool = False) -> f
     if kind not in table:
         raise ValueError(kind)
     return table[kind]
+
+
+def hybrid_state_bytes_per_gpu(psi: float, shard_group: int, k: float = 12.0) -> float:
+    """Hybrid sharding ("PyTorch FSDP..." section 3.3): full sharding inside a
+    group of F GPUs, so the ZeRO-3 ledger with N_d replaced by F."""
+    return (2 * psi + 2 * psi + k * psi) / shard_group
+
+
+def hybrid_comm_bytes_per_gpu(psi: float, nd: int, shard_group: int, kind: str,
+                              exact: bool = False) -> float:
+    """Bytes sent per GPU per step under hybrid sharding, ring model, 16-bit
+    elements.  "intra": the gradient reduce-scatter and the parameter
+    all-gather inside the group of F (2 x 2Psi, factor (F-1)/F);
+    "inter": the all-reduce of the GPU's Psi/F shard across the R = N_d/F
+    groups (4 Psi/F, factor (R-1)/R).  This is the ZeRO-1/2 volume of the
+    "Infra: Data Parallel" ZeRO section applied to the two levels."""
+    if shard_group < 1 or nd % shard_group != 0:
+        raise ValueError("the sharding factor must divide N_d")
+    R = nd // shard_group
+    if kind == "intra":
+        f = (shard_group - 1) / shard_group if exact else 1.0
+        return 2 * (2 * psi * f) if shard_group > 1 else 0.0
+    if kind == "inter":
+        f = (R - 1) / R if exact else 1.0
+        return 4 * (psi / shard_group) * f if R > 1 else 0.0
+    raise ValueError(kind)

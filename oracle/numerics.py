@@ -186,3 +186,43 @@ def fsdp_shard_step(contribs, r: int, shard: int, p, m, v, hp: AdamWConfig, t: i
     g = rs_avg(contribs, r, shard)
     p, m, v = adamw(p, m, v, g, hp, t)
     return p, m, v, f32_to_bf16(p)
+
+
+# ------------------------------------------------------- hybrid sharding
+
+def hybrid_rs_avg(contribs, shard_group: int, f: int, shard: int):
+    """Hybrid sharding with sharding factor F ("PyTorch FSDP..." section 2,
+    sharding factor; section 3.3: full sharding inside groups of F GPUs,
+    replication across groups; "4.1 数据并行详解" section 6.3, HYBRID_SHARD).
+
+    The N_d = R x F ranks are ordered k = g*F + j (group g, position j).  A
+    unit is split into F shards of S elements and rank (g, f) holds shard f.
+    Its gradient is reduce-scattered inside its group, then all-reduced across
+    the R groups, then averaged over all N_d ranks:
+        s_g   = G_{gF} + G_{gF+1} + ... + G_{gF+F-1}      (in order j)
+        total = s_0 + s_1 + ... + s_{R-1}                  (in order g)
+        mean  = total / N_d
+    on elements [f*S, (f+1)*S) of each rank's flat gradient, in fp32.
+    F = N_d is rs_avg; F = 1 is the plain all-reduce average."""
+    nd = len(contribs)
+    if shard_group < 1 or nd % shard_group != 0:
+        raise ValueError("the sharding factor must divide N_d")
+    R = nd // shard_group
+    sl = [_upcast(c[f * shard:(f + 1) * shard]) for c in contribs]
+    total = None
+    for g in range(R):
+        s = sl[g * shard_group].copy()
+        for j in range(1, shard_group):
+            s = s + sl[g * shard_group + j]
+        total = s if total is None else total + s
+    return total / total.dtype.type(nd)
+
+
+def hybrid_shard_step(contribs, shard_group: int, f: int, shard: int, p, m, v,
+                      hp: AdamWConfig, t: int):
+    """One hybrid-sharded step on shard f (identical on each of the R groups
+    that replicate it): hybrid reduce, AdamW, bf16 cast.
+    Returns (p, m, v, p_bf16_bits)."""
+    g = hybrid_rs_avg(contribs, shard_group, f, shard)
+    p, m, v = adamw(p, m, v, g, hp, t)
+    return p, m, v, f32_to_bf16(p)
