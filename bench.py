@@ -36,7 +36,11 @@ if ROOT not in sys.path:
 METRIC = "fused shard-step HBM GB/s (% of GB300 peak), params/s at Psi=7B, N_d=8"
 KERNEL_SOURCES = ["sharded_optimizer_step_gb300/csrc/step_tma.cu",
                   "sharded_optimizer_step_gb300/csrc/common.cuh"]
-FUSED_PROFILE = os.path.join(ROOT, "profiles", "fused_step_llama7b_rank_view.md")
+FUSED_PROFILES = {
+    "llama_7b_rank0_nd8": os.path.join(ROOT, "profiles", "fused_step_llama7b_rank_view.md"),
+    "llama_7b_hybrid_nd16_f8_rank0": os.path.join(ROOT, "profiles",
+                                                  "fused_step_llama7b_hybrid_nd16_f8.md"),
+}
 
 
 def parse():
@@ -48,6 +52,9 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--e2e-chunks", type=int, default=4)
     ap.add_argument("--e2e-streams", type=int, default=4)
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="llama_7b_rank0_nd8",
+                    help="the Llama-7B rank view under full sharding (the default line), or "
+                         "under hybrid sharding with N_d = 16, F = 8")
     ap.add_argument("--layers", type=int, default=0,
                     help="smaller case: only the first N layer units (for profiler captures)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -118,12 +125,13 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def profiled_traffic():
-    """DRAM bytes per fused-kernel launch recorded from an ncu capture, if the
-    capture was taken on the current kernel source (else None)."""
+def profiled_traffic(workload_name):
+    """DRAM bytes per element of the fused kernel recorded from an ncu capture
+    of this workload, if the capture was taken on the current kernel source
+    (else None)."""
     try:
-        text = open(FUSED_PROFILE).read()
-    except OSError:
+        text = open(FUSED_PROFILES[workload_name]).read()
+    except (OSError, KeyError):
         return None
     m = re.search(r"traffic_bytes_per_element:\s*([0-9.]+)", text)
     h = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", text)
@@ -186,9 +194,15 @@ class ClockSampler:
 
 # ------------------------------------------------------------ our arm
 
+WORKLOADS = {
+    "llama_7b_rank0_nd8": "llama_7b_rank_view",
+    "llama_7b_hybrid_nd16_f8_rank0": "llama_7b_hybrid_view",
+}
+
+
 def workload(args):
     from synth import workloads as W
-    w = W.llama_7b_rank_view()
+    w = getattr(W, WORKLOADS[args.workload])()
     if args.layers:
         # a smaller case of the same kernel: the first N layer units only
         w.units = w.units[:args.layers]
@@ -209,19 +223,19 @@ def run_ours(args):
     from synth import workloads as W
 
     w = workload(args)
-    nd = w.nd
-    r = rank % nd                       # GPU k holds rank k's view of its own replica
+    nd, F = w.nd, w.F
+    r = rank % F                        # GPU k holds shard k mod F of its own replica
     dev = torch.device("cuda", local)
     hp = ss.AdamW(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
-    opt = RankShardOptimizer(w.units, nd, r, hp, device=dev)
+    opt = RankShardOptimizer(w.units, nd, r, hp, device=dev, shard_group=w.shard_group)
     S = opt.shard_total
     W.dev_fill_rank_master(w, r, opt.master)
     for q in range(nd):
         W.dev_fill_rank_grad(w, 1, r, q, 0, opt.grad_in[q])
     u = w.extra["ag_unit"]
     Su, Pu = w.unit_shard(u), w.unit_padded(u)
-    peers = [torch.empty(Su, dtype=torch.bfloat16, device=dev) for _ in range(nd)]
-    for q in range(nd):
+    peers = [torch.empty(Su, dtype=torch.bfloat16, device=dev) for _ in range(F)]
+    for q in range(F):
         if q != r:
             synth.dev_fill(w.peer_shard_stream(1, q, u), peers[q])
     full = torch.empty(Pu, dtype=torch.bfloat16, device=dev)
@@ -277,7 +291,7 @@ def run_ours(args):
     ag_avg = sum(ag_ms) / len(ag_ms)
     peak, peak_kind = measured_peak()
     achieved = fused_bytes / (fused_avg / 1e3) / 1e9
-    traffic_per_elem = profiled_traffic()
+    traffic_per_elem = profiled_traffic(args.workload)
 
     # end to end through the public API: pinned host inputs copied in every
     # step, the gathered unit read back every step
@@ -299,7 +313,8 @@ def run_ours(args):
             "data": "synthetic (seeded counter-based generator on the device; no data set or weights)",
             "config": {"workload": w.name,
                        "model_shape": f"Llama-style 7B, {len(w.units)} FSDP units",
-                       "psi": w.psi, "nd": nd, "rank": r, "shard_elements": S,
+                       "psi": w.psi, "nd": nd, "shard_group": F, "rank": r,
+                       "shard_elements": S,
                        "grad_dtype": "bf16", "state_dtype": "f32", "ag_unit_params": Pu,
                        "step": "fused rs_avg+AdamW+bf16 cast over the rank shard (1 launch), "
                                "then all-gather of one layer unit (1 launch)",
@@ -314,7 +329,8 @@ def run_ours(args):
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "peak_source": ("measured: MEASURED_PEAKS.json hbm_gbs (copy, burst)"
                                          if peak_kind == "measured" else "fallback 6800 GB/s"),
-                         "kernel": "rs_adamw_cast_tma<bf16> (TMA-staged, N_d = 8)",
+                         "kernel": f"rs_adamw_cast_tma<bf16> (TMA-staged, N_d = {nd}"
+                                   + (f", sharding factor {F})" if F != nd else ")"),
                          "algorithmic_bytes_per_launch": fused_bytes,
                          "traffic": (None if traffic_per_elem is None
                                      else round(traffic_per_elem * S))},
@@ -339,8 +355,8 @@ def run_e2e(args, torch, ss, opt, peers, full, u, r, nd, stream, step_bytes):
     for q in range(nd):
         host_g[q].copy_(opt.grad_in[q])
     host_p = [torch.empty(peers[0].numel(), dtype=torch.bfloat16, pin_memory=True)
-              for _ in range(nd)]
-    for q in range(nd):
+              for _ in range(len(peers))]
+    for q in range(len(peers)):
         host_p[q].copy_(peers[q])
     host_out = torch.empty(full.numel(), dtype=torch.bfloat16, pin_memory=True)
     torch.cuda.synchronize()
@@ -368,7 +384,7 @@ def run_e2e(args, torch, ss, opt, peers, full, u, r, nd, stream, step_bytes):
                 evs.append(cs.record_event())
             chunk_ready.append(evs)
         peer_evs = []
-        for q in range(nd):
+        for q in range(len(peers)):
             if q != r:
                 cs = copy_streams[k % len(copy_streams)]
                 k += 1
@@ -417,9 +433,16 @@ def _oracle_sample(w, r, n, step, rng_seed=0):
     contribs = [W.host_gather_rank_grad(w, step, r, q, 0, idx) for q in range(w.nd)]
     p = W.host_gather_rank_master(w, r, idx)
     u = w.extra["ag_unit"]
-    n_ag = max(1, n // (w.nd * 4))
-    shards = [synth.host_fill(w.peer_shard_stream(step, q, u), 0, n_ag, "bf16") for q in range(w.nd)]
+    n_ag = max(1, n // (w.F * 4))
+    shards = [synth.host_fill(w.peer_shard_stream(step, q, u), 0, n_ag, "bf16") for q in range(w.F)]
     return contribs, p, shards
+
+
+def _oracle_step(w, contribs, n, p, m, v, hp, t):
+    import oracle
+    if w.F == w.nd:
+        return oracle.fsdp_shard_step(contribs, 0, n, p, m, v, hp, t)
+    return oracle.hybrid_shard_step(contribs, w.F, 0, n, p, m, v, hp, t)
 
 
 def _time_oracle(w, contribs, p, shards, t):
@@ -430,12 +453,12 @@ def _time_oracle(w, contribs, p, shards, t):
     n = p.size
     m = np.zeros(n, np.float32)
     v = np.zeros(n, np.float32)
-    lay = oracle.layout([w.nd * shards[0].size], w.nd)
+    lay = oracle.layout([w.F * shards[0].size], w.F)
     t0 = time.perf_counter()
-    oracle.fsdp_shard_step(contribs, 0, n, p, m, v, hp, t)
+    _oracle_step(w, contribs, n, p, m, v, hp, t)
     oracle.ag_unpack(shards, lay)
     dt = time.perf_counter() - t0
-    bytes_ = (2 * w.nd + 26) * n + 4 * w.nd * shards[0].size
+    bytes_ = (2 * w.nd + 26) * n + 4 * w.F * shards[0].size
     return dt, bytes_
 
 
@@ -449,16 +472,15 @@ def cpu_baseline(w, r, budget_s=10.0, n=4_000_000):
         reps += 1
     return {"value": round(total_b / total_t / 1e9, 4), "unit": "GB/s", "cores": 1,
             "kind": "oracle",
-            "sample": f"{reps} x (fused step on {n} contiguous shard elements of the 7B rank view "
-                      f"+ all-gather of {shards[0].size * w.nd} bf16), numpy single-threaded"}
+            "sample": f"{reps} x (fused step on {n} contiguous shard elements of {w.name} "
+                      f"+ all-gather of {shards[0].size * w.F} bf16), numpy single-threaded"}
 
 
 def run_reference(args):
     world, rank, local = dist_env()
     if rank != 0:
         return
-    from synth import workloads as W
-    w = W.llama_7b_rank_view()
+    w = workload(args)
     r = 0
     n = 2_000_000
     contribs, p, shards = _oracle_sample(w, r, n, 1)
@@ -479,7 +501,7 @@ def run_reference(args):
                    "sample_elements_per_step": n},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": f"each step: fused step on {n} shard elements + all-gather of "
-                                   f"{shards[0].size * w.nd} bf16"},
+                                   f"{shards[0].size * w.F} bf16"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

@@ -184,6 +184,30 @@ int fsdp_rs_avg_adamw_cast(const void* const* grad_slices, int32_t grad_dtype, i
                            int64_t S, float* master, float* m, float* v, uint16_t* out_bf16,
                            const shardstep_adamw_t* hp, void* stream);
 
+/* fsdp_hybrid_rs_avg_adamw_cast -- device, one kernel pass.
+ * Hybrid sharding with sharding factor F = shard_group ([P2] section 2,
+ * sharding factor: F = 1 is full replication, F = N_d full sharding; [P2]
+ * section 3.3: full sharding inside groups of F GPUs, replication across the
+ * groups; [P3] section 6.3, HYBRID_SHARD).  The N_d = R x F ranks are ordered
+ * k = g*F + j (group g, position j); a unit is split into F shards of S
+ * elements and rank (g, f) holds shard f, replicated in each of the R groups.
+ * Its gradient is reduce-scattered inside its group, all-reduced across the
+ * groups and averaged over all N_d ranks; per element, in fp32:
+ *     s_g = G_{gF} + G_{gF+1} + ... + G_{gF+F-1}        (order j)
+ *     g   = (s_0 + s_1 + ... + s_{R-1}) / N_d            (order g)
+ * followed by the same AdamW update and bf16 cast as fsdp_rs_avg_adamw_cast.
+ * shard_group = nd gives exactly fsdp_rs_avg_adamw_cast; shard_group = 1 the
+ * plain all-reduce average of every rank.
+ *   grad_slices[nd]  rank k's contribution to shard f (S elements each), in
+ *                    rank order k = g*F + j.
+ *   shard_group      F >= 1, dividing nd.
+ * Other arguments, aliasing rules, kernel choice and errors as in
+ * fsdp_rs_avg_adamw_cast; INVALID when F does not divide nd. */
+int fsdp_hybrid_rs_avg_adamw_cast(const void* const* grad_slices, int32_t grad_dtype, int32_t nd,
+                                  int32_t shard_group, int64_t S, float* master, float* m,
+                                  float* v, uint16_t* out_bf16, const shardstep_adamw_t* hp,
+                                  void* stream);
+
 /* ------------------------------------------------------ all-gather */
 
 /* fsdp_ag_unpack -- device, one kernel.
@@ -258,6 +282,21 @@ double shardstep_state_bytes(double psi, int32_t nd, int32_t stage, double k);
 #define SHARDSTEP_COMM_ZERO2 4          /* 4Ψ                  */
 #define SHARDSTEP_COMM_ZERO3 5          /* 6Ψ                  */
 double shardstep_comm_bytes(double psi, int32_t nd, int32_t kind, int32_t exact);
+
+/* Hybrid sharding ledger ([P2] section 3.3): model-state bytes per GPU are
+ * the ZeRO-3 ledger with N_d replaced by F, (2Ψ + 2Ψ + kΨ)/F; per-GPU bytes
+ * sent per step, ring model, 16-bit elements (exact keeps the (n-1)/n
+ * factors):
+ *   SHARDSTEP_HYBRID_INTRA  reduce-scatter + all-gather inside the group of F:
+ *                           2 x 2Ψ (F-1)/F
+ *   SHARDSTEP_HYBRID_INTER  all-reduce of the GPU's Ψ/F shard across the
+ *                           R = N_d/F groups: 4 (Ψ/F) (R-1)/R
+ * Both return a negative value when F < 1 or F does not divide nd. */
+#define SHARDSTEP_HYBRID_INTRA 0
+#define SHARDSTEP_HYBRID_INTER 1
+double shardstep_hybrid_state_bytes(double psi, int32_t shard_group, double k);
+double shardstep_hybrid_comm_bytes(double psi, int32_t nd, int32_t shard_group, int32_t kind,
+                                   int32_t exact);
 
 /* ------------------------------------------------------------ misc */
 

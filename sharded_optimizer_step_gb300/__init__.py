@@ -22,7 +22,8 @@ __all__ = [
     "build", "ShardstepError", "AdamW", "Layout", "fsdp_layout", "fsdp_flat_pack", "fsdp_views",
     "fsdp_grad_accumulate", "fsdp_rs_avg_adamw_cast", "fsdp_ag_unpack", "ddp_bucket_plan",
     "ddp_bucket_allreduce_avg", "state_bytes", "comm_bytes", "launch_count", "MAX_ND",
-    "set_fused_path", "device_status",
+    "set_fused_path", "device_status", "fsdp_hybrid_rs_avg_adamw_cast", "hybrid_state_bytes",
+    "hybrid_comm_bytes",
 ]
 
 
@@ -165,6 +166,19 @@ def fsdp_rs_avg_adamw_cast(grad_slices, master, m, v, out_bf16, hp: AdamW, step:
     shard (in place) and the bf16 cast into ``out_bf16``, in one kernel pass.
     ``grad_slices[q]`` is rank q's contribution to this shard (S elements,
     all bf16 or all fp32)."""
+    _fused(grad_slices, master, m, v, out_bf16, hp, step, stream, None)
+
+
+def fsdp_hybrid_rs_avg_adamw_cast(grad_slices, shard_group: int, master, m, v, out_bf16,
+                                  hp: AdamW, step: int, stream=None):
+    """Hybrid sharding with sharding factor F = ``shard_group``: the N_d
+    contributions (rank order k = g*F + j) are summed inside each group of F,
+    then across the groups, averaged over N_d, and the shard is updated and
+    cast as in ``fsdp_rs_avg_adamw_cast``."""
+    _fused(grad_slices, master, m, v, out_bf16, hp, step, stream, int(shard_group))
+
+
+def _fused(grad_slices, master, m, v, out_bf16, hp, step, stream, shard_group):
     import torch
     if not grad_slices:
         raise ValueError("need at least one gradient slice")
@@ -180,11 +194,17 @@ def fsdp_rs_avg_adamw_cast(grad_slices, master, m, v, out_bf16, hp: AdamW, step:
     if master.dtype != torch.float32 or out_bf16.dtype != torch.bfloat16 or out_bf16.numel() != S:
         raise ValueError("master fp32 and out bf16 with S elements")
     hpc = hp.at_step(step)
-    _capi.check("fsdp_rs_avg_adamw_cast", _capi.lib().fsdp_rs_avg_adamw_cast(
-        _capi.ptr_array([g.data_ptr() for g in grad_slices]), _dtype_code(grad_slices[0]),
-        len(grad_slices), S, ctypes.c_void_p(master.data_ptr()), ctypes.c_void_p(m.data_ptr()),
-        ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(out_bf16.data_ptr()), ctypes.byref(hpc),
-        _stream(stream, master.device)))
+    ptrs = _capi.ptr_array([g.data_ptr() for g in grad_slices])
+    state = (ctypes.c_void_p(master.data_ptr()), ctypes.c_void_p(m.data_ptr()),
+             ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(out_bf16.data_ptr()))
+    if shard_group is None:
+        _capi.check("fsdp_rs_avg_adamw_cast", _capi.lib().fsdp_rs_avg_adamw_cast(
+            ptrs, _dtype_code(grad_slices[0]), len(grad_slices), S, *state, ctypes.byref(hpc),
+            _stream(stream, master.device)))
+    else:
+        _capi.check("fsdp_hybrid_rs_avg_adamw_cast", _capi.lib().fsdp_hybrid_rs_avg_adamw_cast(
+            ptrs, _dtype_code(grad_slices[0]), len(grad_slices), shard_group, S, *state,
+            ctypes.byref(hpc), _stream(stream, master.device)))
 
 
 # ------------------------------------------------------------- all-gather
@@ -279,6 +299,22 @@ def device_status(clear: bool = False) -> int:
     _capi.check("shardstep_device_status",
                 _capi.lib().shardstep_device_status(ctypes.byref(st), int(bool(clear))))
     return st.value
+
+
+def hybrid_state_bytes(psi: float, shard_group: int, k: float = 12.0) -> float:
+    r = _capi.lib().shardstep_hybrid_state_bytes(psi, shard_group, k)
+    if r < 0:
+        raise ValueError("bad sharding factor")
+    return r
+
+
+def hybrid_comm_bytes(psi: float, nd: int, shard_group: int, kind: str,
+                      exact: bool = False) -> float:
+    code = {"intra": 0, "inter": 1}[kind]
+    r = _capi.lib().shardstep_hybrid_comm_bytes(psi, nd, shard_group, code, int(exact))
+    if r < 0:
+        raise ValueError("the sharding factor must divide N_d")
+    return r
 
 
 def launch_count() -> int:

@@ -48,11 +48,15 @@ SIGNATURES = {
     "fsdp_grad_accumulate": (c_i32, [c_vp, c_vp, c_i64, c_f32, c_i32, c_vp]),
     "fsdp_rs_avg_adamw_cast": (c_i32, [P_vp, c_i32, c_i32, c_i64, c_vp, c_vp, c_vp, c_vp,
                                        ctypes.POINTER(AdamWHP), c_vp]),
+    "fsdp_hybrid_rs_avg_adamw_cast": (c_i32, [P_vp, c_i32, c_i32, c_i32, c_i64, c_vp, c_vp, c_vp,
+                                              c_vp, ctypes.POINTER(AdamWHP), c_vp]),
     "fsdp_ag_unpack": (c_i32, [P_vp, c_i32, c_i64, c_vp, c_vp]),
     "ddp_bucket_plan": (c_i32, [P_i64, c_i32, c_i32, c_i64, P_i64, P_i32, P_i64, P_i32]),
     "ddp_bucket_allreduce_avg": (c_i32, [P_vp, c_i32, P_i64, c_i32, c_i32, c_vp, c_vp]),
     "shardstep_state_bytes": (c_f64, [c_f64, c_i32, c_i32, c_f64]),
     "shardstep_comm_bytes": (c_f64, [c_f64, c_i32, c_i32, c_i32]),
+    "shardstep_hybrid_state_bytes": (c_f64, [c_f64, c_i32, c_f64]),
+    "shardstep_hybrid_comm_bytes": (c_f64, [c_f64, c_i32, c_i32, c_i32, c_i32]),
     "shardstep_last_error": (ctypes.c_char_p, []),
     "shardstep_set_fused_path": (c_i32, [c_i32]),
     "shardstep_device_status": (c_i32, [ctypes.POINTER(ctypes.c_uint32), c_i32]),

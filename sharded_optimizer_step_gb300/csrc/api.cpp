@@ -55,11 +55,12 @@ int elem_size_of(int32_t dtype) {
     return dtype == SHARDSTEP_DTYPE_BF16 ? 2 : dtype == SHARDSTEP_DTYPE_F32 ? 4 : 0;
 }
 
-MeanOp mean_op(int nd) {
+MeanOp mean_op(int nd, int group) {
     MeanOp mo;
     mo.nd = static_cast<float>(nd);
     mo.pow2 = (nd & (nd - 1)) == 0;
     mo.inv_nd = 1.0f / static_cast<float>(nd);  // exact when nd is a power of two
+    mo.group = group;
     return mo;
 }
 
@@ -356,9 +357,15 @@ int fsdp_grad_accumulate(const uint16_t* g, float* acc, int64_t n, float scale, 
     return ok();
 }
 
-int fsdp_rs_avg_adamw_cast(const void* const* grad_slices, int32_t grad_dtype, int32_t nd,
-                           int64_t S, float* master, float* m, float* v, uint16_t* out_bf16,
-                           const shardstep_adamw_t* hp, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The fused step with the slices reduced in groups of `group` ranks
+// (group == nd: plain rank order).
+int fused_step(const void* const* grad_slices, int32_t grad_dtype, int32_t nd, int32_t group,
+               int64_t S, float* master, float* m, float* v, uint16_t* out_bf16,
+               const shardstep_adamw_t* hp, void* stream) {
     const int gs = elem_size_of(grad_dtype);
     if (gs == 0) return fail(SHARDSTEP_ERR_INVALID, "unknown grad dtype %d", grad_dtype);
     if (nd < 1) return fail(SHARDSTEP_ERR_INVALID, "nd must be >= 1 (got %d)", nd);
@@ -406,13 +413,57 @@ int fsdp_rs_avg_adamw_cast(const void* const* grad_slices, int32_t grad_dtype, i
                aligned(v, 16) && aligned(out_bf16, 8);
     for (int32_t q = 0; q < nd && tma; ++q) tma = aligned(tab.p[q], 16);
     if (tma) tma = tma_step_smem_bytes(nd, f32g) <= static_cast<size_t>(device_smem_optin());
+    const MeanOp mo = mean_op(nd, group);
     cudaError_t e =
         tma ? launch_rs_adamw_cast_tma(tab, nd, f32g, S, master, m, v, out_bf16, adam_scalars(*hp),
-                                       mean_op(nd), static_cast<cudaStream_t>(stream))
+                                       mo, static_cast<cudaStream_t>(stream))
             : launch_rs_adamw_cast(tab, nd, f32g, S, master, m, v, out_bf16, adam_scalars(*hp),
-                                   mean_op(nd), vec, static_cast<cudaStream_t>(stream));
+                                   mo, vec, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "fused step kernel launch");
     return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+int fsdp_rs_avg_adamw_cast(const void* const* grad_slices, int32_t grad_dtype, int32_t nd,
+                           int64_t S, float* master, float* m, float* v, uint16_t* out_bf16,
+                           const shardstep_adamw_t* hp, void* stream) {
+    return fused_step(grad_slices, grad_dtype, nd, nd, S, master, m, v, out_bf16, hp, stream);
+}
+
+int fsdp_hybrid_rs_avg_adamw_cast(const void* const* grad_slices, int32_t grad_dtype, int32_t nd,
+                                  int32_t shard_group, int64_t S, float* master, float* m,
+                                  float* v, uint16_t* out_bf16, const shardstep_adamw_t* hp,
+                                  void* stream) {
+    if (shard_group < 1 || nd < 1 || nd % shard_group != 0)
+        return fail(SHARDSTEP_ERR_INVALID,
+                    "the sharding factor %d must be >= 1 and divide nd = %d", shard_group, nd);
+    return fused_step(grad_slices, grad_dtype, nd, shard_group, S, master, m, v, out_bf16, hp,
+                      stream);
+}
+
+double shardstep_hybrid_state_bytes(double psi, int32_t shard_group, double k) {
+    if (shard_group < 1) return -1.0;
+    return (2 * psi + 2 * psi + k * psi) / shard_group;
+}
+
+double shardstep_hybrid_comm_bytes(double psi, int32_t nd, int32_t shard_group, int32_t kind,
+                                   int32_t exact) {
+    if (shard_group < 1 || nd < 1 || nd % shard_group != 0) return -1.0;
+    const int32_t R = nd / shard_group;
+    if (kind == SHARDSTEP_HYBRID_INTRA) {
+        if (shard_group == 1) return 0.0;
+        const double f = exact ? static_cast<double>(shard_group - 1) / shard_group : 1.0;
+        return 2 * (2 * psi * f);
+    }
+    if (kind == SHARDSTEP_HYBRID_INTER) {
+        if (R == 1) return 0.0;
+        const double f = exact ? static_cast<double>(R - 1) / R : 1.0;
+        return 4 * (psi / shard_group) * f;
+    }
+    return -1.0;
 }
 
 int ddp_bucket_plan(const int64_t* numels, int32_t n, int32_t elem_size, int64_t cap_bytes,
@@ -473,7 +524,7 @@ int ddp_bucket_allreduce_avg(const uint16_t* const* rank_grads, int32_t nd,
         if (overlap(span(rank_grads[q] + a0, (e0 - a0) * 2), os))
             return fail(SHARDSTEP_ERR_INVALID, "rank_grads[%d] overlaps out", q);
     }
-    const MeanOp mo = mean_op(nd);
+    const MeanOp mo = mean_op(nd, nd);
     for (int32_t b = first; b < first + count; ++b) {
         const int64_t a = bucket_offsets[b], n = bucket_offsets[b + 1] - a;
         if (n == 0) continue;

@@ -102,6 +102,42 @@ __device__ __forceinline__ uint4 pack4f(const float* f) {
 
 // ------------------------------------------------------------- arithmetic
 
+// Reduction of rank slices in the fixed order the method uses: slices arrive
+// in rank order; every `group` consecutive slices are summed first, then the
+// group sums are added in order.  With group == N_d this is the plain
+// left-to-right rank-order sum (the compare below never fires).
+template <int W>
+struct GroupSum {
+    float s[W], tot[W];
+    int c;
+    bool have;
+    __device__ __forceinline__ void first(const float* t) {
+#pragma unroll
+        for (int k = 0; k < W; ++k) s[k] = t[k];
+        c = 1;
+        have = false;
+    }
+    __device__ __forceinline__ void add(const float* t, int group) {
+        if (c == group) {
+#pragma unroll
+            for (int k = 0; k < W; ++k) {
+                tot[k] = have ? __fadd_rn(tot[k], s[k]) : s[k];
+                s[k] = t[k];
+            }
+            have = true;
+            c = 1;
+        } else {
+#pragma unroll
+            for (int k = 0; k < W; ++k) s[k] = __fadd_rn(s[k], t[k]);
+            ++c;
+        }
+    }
+    __device__ __forceinline__ void result(float* g) const {
+#pragma unroll
+        for (int k = 0; k < W; ++k) g[k] = have ? __fadd_rn(tot[k], s[k]) : s[k];
+    }
+};
+
 __device__ __forceinline__ float mean_of(float sum, const MeanOp& mo) {
     return mo.pow2 ? __fmul_rn(sum, mo.inv_nd) : __fdiv_rn(sum, mo.nd);
 }

@@ -14,12 +14,16 @@ struct AdamScalars {
     float lr_wd, beta1, omb1, beta2, omb2, step_size, sqrt_bc2, eps;
 };
 
-// How the reduce turns the rank sum into a mean: multiply by the exact
-// reciprocal when N_d is a power of two (identical to dividing), else divide.
+// How the reduce turns the N_d rank slices into a mean: the slices are summed
+// in groups of `group` consecutive ranks (group == N_d: one rank-order sum;
+// 1 < group < N_d: hybrid sharding, group sums first, then across groups),
+// then the total is multiplied by the exact reciprocal when N_d is a power of
+// two (identical to dividing) or divided by N_d.
 struct MeanOp {
     float inv_nd;
     float nd;
     int pow2;
+    int group;
 };
 
 struct PtrTable {

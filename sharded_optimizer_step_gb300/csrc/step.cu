@@ -55,27 +55,35 @@ __device__ __forceinline__ float grad_scalar(const void* base, int64_t j) {
     return bf16_to_f32(static_cast<const uint16_t*>(base)[j]);
 }
 
-// Sum of the N_d slices at 4 consecutive elements, in rank order.
+// Sum of the N_d slices at 4 consecutive elements, in the order GroupSum
+// fixes (rank order; grouped for hybrid sharding).
 template <int ND, bool F32G>
-__device__ __forceinline__ void reduce4(const PtrTable& tab, int nd, int64_t i, float* g) {
+__device__ __forceinline__ void reduce4(const PtrTable& tab, int nd, int group, int64_t i,
+                                        float* g) {
+    GroupSum<4> acc;
     if constexpr (ND != kRuntimeND) {
         GradVec<F32G> gv[ND];
 #pragma unroll
         for (int q = 0; q < ND; ++q) gv[q].load(tab.p[q], i);
-        gv[0].to_f32(g);
+        {
+            float t[4];
+            gv[0].to_f32(t);
+            acc.first(t);
+        }
 #pragma unroll
         for (int q = 1; q < ND; ++q) {
             float t[4];
             gv[q].to_f32(t);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) g[k] = __fadd_rn(g[k], t[k]);
+            acc.add(t, group);
         }
     } else {
         // any N_d: groups of four slices in flight at a time
         {
             GradVec<F32G> g0;
             g0.load(tab.p[0], i);
-            g0.to_f32(g);
+            float t[4];
+            g0.to_f32(t);
+            acc.first(t);
         }
         int q = 1;
         for (; q + 4 <= nd; q += 4) {
@@ -86,8 +94,7 @@ __device__ __forceinline__ void reduce4(const PtrTable& tab, int nd, int64_t i, 
             for (int u = 0; u < 4; ++u) {
                 float t[4];
                 gv[u].to_f32(t);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) g[k] = __fadd_rn(g[k], t[k]);
+                acc.add(t, group);
             }
         }
         for (; q < nd; ++q) {
@@ -95,17 +102,24 @@ __device__ __forceinline__ void reduce4(const PtrTable& tab, int nd, int64_t i, 
             gq.load(tab.p[q], i);
             float t[4];
             gq.to_f32(t);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) g[k] = __fadd_rn(g[k], t[k]);
+            acc.add(t, group);
         }
     }
+    acc.result(g);
 }
 
 template <bool F32G>
-__device__ __forceinline__ float reduce1(const PtrTable& tab, int nd, int64_t j) {
-    float s = grad_scalar<F32G>(tab.p[0], j);
-    for (int q = 1; q < nd; ++q) s = __fadd_rn(s, grad_scalar<F32G>(tab.p[q], j));
-    return s;
+__device__ __forceinline__ float reduce1(const PtrTable& tab, int nd, int group, int64_t j) {
+    GroupSum<1> acc;
+    float t = grad_scalar<F32G>(tab.p[0], j);
+    acc.first(&t);
+    for (int q = 1; q < nd; ++q) {
+        t = grad_scalar<F32G>(tab.p[q], j);
+        acc.add(&t, group);
+    }
+    float g;
+    acc.result(&g);
+    return g;
 }
 
 // --------------------------------------------------- fused step kernels
@@ -115,7 +129,7 @@ __device__ __forceinline__ void step_scalar(const PtrTable& tab, int nd, int64_t
                                             float* __restrict__ P, float* __restrict__ M,
                                             float* __restrict__ V, uint16_t* __restrict__ out,
                                             const AdamScalars& c, const MeanOp& mo) {
-    const float g = mean_of(reduce1<F32G>(tab, nd, j), mo);
+    const float g = mean_of(reduce1<F32G>(tab, nd, mo.group, j), mo);
     float p = P[j], m = M[j], v = V[j];
     adamw_elem(g, p, m, v, c);
     P[j] = p;
@@ -141,7 +155,7 @@ __global__ void __launch_bounds__(kStepThreads, kStepMinBlocks)
         const uint4 m0 = ldcs16(M + 4 * i);
         const uint4 v0 = ldcs16(V + 4 * i);
         float g[4];
-        reduce4<ND, F32G>(tab, nd, i, g);
+        reduce4<ND, F32G>(tab, nd, mo.group, i, g);
         float p[4], m[4], v[4];
         unpack4f(p0, p);
         unpack4f(m0, m);
@@ -179,14 +193,14 @@ __global__ void __launch_bounds__(kStepThreads, kStepMinBlocks)
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * kStepThreads + threadIdx.x; i < nvec;
          i += stride) {
         float g[4];
-        reduce4<ND, false>(tab, nd, i, g);
+        reduce4<ND, false>(tab, nd, mo.group, i, g);
 #pragma unroll
         for (int k = 0; k < 4; ++k) g[k] = mean_of(g[k], mo);
         stcs8(out + 4 * i, make_uint2(pack_bf16x2(g[0], g[1]), pack_bf16x2(g[2], g[3])));
     }
     if (blockIdx.x == 0 && threadIdx.x < (n & 3)) {
         const int64_t j = (nvec << 2) + threadIdx.x;
-        out[j] = f32_to_bf16(mean_of(reduce1<false>(tab, nd, j), mo));
+        out[j] = f32_to_bf16(mean_of(reduce1<false>(tab, nd, mo.group, j), mo));
     }
 }
 
@@ -196,7 +210,7 @@ __global__ void __launch_bounds__(kThreads)
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
     for (int64_t j = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; j < n;
          j += stride)
-        out[j] = f32_to_bf16(mean_of(reduce1<false>(tab, nd, j), mo));
+        out[j] = f32_to_bf16(mean_of(reduce1<false>(tab, nd, mo.group, j), mo));
 }
 
 // --------------------------------------------------------------- launch

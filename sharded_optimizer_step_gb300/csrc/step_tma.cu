@@ -8,7 +8,9 @@
 // they wait on the stage's barrier, reduce the N_d slices in rank order from
 // shared memory, run AdamW, and write master / m / v and the bf16 parameter
 // straight to HBM with streaming stores; each warp then arrives on the
-// stage's "empty" barrier so the producer can refill it.  Two stages of
+// stage's "empty" barrier so the producer can refill it.  The slices are
+// summed in the order GroupSum fixes (rank order, grouped for hybrid
+// sharding).  Two stages of
 // 2048 x (N_d x grad bytes + 12) bytes are in flight per SM (114 KB at N_d =
 // 8, bf16).  Tiles are dealt round-robin over the grid.  Measured on GB300
 // against the register-staged kernel (4 elements / thread, 512-thread
@@ -179,14 +181,19 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         const uint8_t* st = smem + s * stage_bytes;
         const uint8_t* sst = st + nd * slice_bytes;
         for (int e = tid * 4; e < n; e += kConsumers * 4) {
-            float g[4];
-            load4_smem<F32G>(st + e * gsz, g);
+            GroupSum<4> acc;
+            {
+                float t[4];
+                load4_smem<F32G>(st + e * gsz, t);
+                acc.first(t);
+            }
             for (int q = 1; q < nd; ++q) {
                 float t[4];
                 load4_smem<F32G>(st + q * slice_bytes + e * gsz, t);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) g[k] = __fadd_rn(g[k], t[k]);
+                acc.add(t, mo.group);
             }
+            float g[4];
+            acc.result(g);
             const float4 pp = *reinterpret_cast<const float4*>(sst + e * 4);
             const float4 mm = *reinterpret_cast<const float4*>(sst + kTile * 4 + e * 4);
             const float4 vv = *reinterpret_cast<const float4*>(sst + 2 * kTile * 4 + e * 4);
@@ -206,8 +213,15 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     }
     if (blockIdx.x == 0 && tid < S - s_main) {
         const int64_t jx = s_main + tid;
-        float sum = grad1<F32G>(tab.p[0], jx);
-        for (int q = 1; q < nd; ++q) sum = __fadd_rn(sum, grad1<F32G>(tab.p[q], jx));
+        GroupSum<1> acc;
+        float t = grad1<F32G>(tab.p[0], jx);
+        acc.first(&t);
+        for (int q = 1; q < nd; ++q) {
+            t = grad1<F32G>(tab.p[q], jx);
+            acc.add(&t, mo.group);
+        }
+        float sum;
+        acc.result(&sum);
         float p = P[jx], m = M[jx], v = V[jx];
         adamw_elem(mean_of(sum, mo), p, m, v, c);
         P[jx] = p;

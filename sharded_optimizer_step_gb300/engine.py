@@ -15,7 +15,8 @@ from __future__ import annotations
 
 import torch
 
-from . import AdamW, fsdp_ag_unpack, fsdp_layout, fsdp_rs_avg_adamw_cast, fsdp_views
+from . import (AdamW, fsdp_ag_unpack, fsdp_hybrid_rs_avg_adamw_cast, fsdp_layout,
+               fsdp_rs_avg_adamw_cast, fsdp_views)
 
 
 def _numel(shape):
@@ -27,12 +28,18 @@ def _numel(shape):
 
 class RankShardOptimizer:
     def __init__(self, unit_shapes, nd: int, rank: int, hp: AdamW, device="cuda",
-                 grad_dtype=torch.bfloat16):
-        if not 0 <= rank < nd:
+                 grad_dtype=torch.bfloat16, shard_group: int = 0):
+        """``shard_group`` = F enables hybrid sharding: units are split into F
+        shards, ``rank`` is the shard index 0..F-1 inside the rank's group,
+        and the N_d contributions come in rank order k = g*F + j."""
+        self.F = shard_group or nd
+        if nd % self.F != 0:
+            raise ValueError("the sharding factor must divide N_d")
+        if not 0 <= rank < self.F:
             raise ValueError("rank out of range")
         self.unit_shapes = [list(u) for u in unit_shapes]
         self.nd, self.rank, self.hp = nd, rank, hp
-        self.layouts = [fsdp_layout([_numel(s) for s in u], nd) for u in self.unit_shapes]
+        self.layouts = [fsdp_layout([_numel(s) for s in u], self.F) for u in self.unit_shapes]
         self.starts = []
         pos = 0
         for lay in self.layouts:
@@ -55,8 +62,14 @@ class RankShardOptimizer:
         """Reduce-scatter average + AdamW + bf16 cast over the whole rank shard
         (one launch)."""
         self.t += 1
-        fsdp_rs_avg_adamw_cast(self.grad_in, self.master, self.m, self.v, self.params, self.hp,
-                               self.t, stream=stream)
+        self._update(self.grad_in, self.master, self.m, self.v, self.params, stream)
+
+    def _update(self, grads, master, m, v, params, stream):
+        if self.F == self.nd:
+            fsdp_rs_avg_adamw_cast(grads, master, m, v, params, self.hp, self.t, stream=stream)
+        else:
+            fsdp_hybrid_rs_avg_adamw_cast(grads, self.F, master, m, v, params, self.hp, self.t,
+                                          stream=stream)
 
     def begin_step(self):
         """Advance the step count for an update issued piece by piece with
@@ -66,14 +79,15 @@ class RankShardOptimizer:
     def update_range(self, a: int, b: int, stream=None):
         """The fused update of shard positions [a, b) at the current step count."""
         sl = slice(a, b)
-        fsdp_rs_avg_adamw_cast([g[sl] for g in self.grad_in], self.master[sl], self.m[sl],
-                               self.v[sl], self.params[sl], self.hp, self.t, stream=stream)
+        self._update([g[sl] for g in self.grad_in], self.master[sl], self.m[sl], self.v[sl],
+                     self.params[sl], stream)
 
     def gather_unit(self, u, peer_shards, full, stream=None):
-        """All-gather unit u: ``peer_shards[q]`` is rank q's bf16 shard (this
-        rank's own entry is ignored and taken from ``params``); ``full`` is the
-        unit's flat bf16 buffer of P elements.  Returns the tensor views."""
+        """All-gather unit u inside the rank's shard group: ``peer_shards[q]``
+        is shard q's bf16 piece (q < F; this rank's own entry is ignored and
+        taken from ``params``); ``full`` is the unit's flat bf16 buffer of P
+        elements.  Returns the tensor views."""
         shards = list(peer_shards)
         shards[self.rank] = self.unit_slice(self.params, u)
         fsdp_ag_unpack(shards, full, stream=stream)
-        return fsdp_views(full, self.unit_shapes[u], self.nd)
+        return fsdp_views(full, self.unit_shapes[u], self.F)

@@ -36,7 +36,12 @@ class Workload:
     beta2: float = 0.999
     eps: float = 1e-8
     weight_decay: float = 0.01
+    shard_group: int = 0            # hybrid sharding factor F (0: F = nd, full sharding)
     extra: dict = field(default_factory=dict)
+
+    @property
+    def F(self):
+        return self.shard_group or self.nd
 
     def unit_numels(self, u):
         out = []
@@ -52,10 +57,10 @@ class Workload:
 
     def unit_padded(self, u):
         T = self.unit_total(u)
-        return -(-T // self.nd) * self.nd
+        return -(-T // self.F) * self.F
 
     def unit_shard(self, u):
-        return self.unit_padded(u) // self.nd
+        return self.unit_padded(u) // self.F
 
     @property
     def psi(self):
@@ -115,6 +120,17 @@ def llama_7b_rank_view() -> Workload:
                     extra={"rank": 0, "ag_unit": 0})
 
 
+def llama_7b_hybrid_view() -> Workload:
+    """Hybrid sharding of the Llama-style 7B model: N_d = 16 ranks in 2 groups
+    of F = 8 (sharded inside a group, replicated across the two); one rank's
+    view, i.e. its shard f = 0 of every unit and the 16 ranks' gradient
+    contributions to it."""
+    h, f, v = 4096, 11008, 32000
+    units = [_llama_layer(h, f) for _ in range(32)] + [[(v, h), (v, h), (h,)]]
+    return Workload("llama_7b_hybrid_nd16_f8_rank0", 6, units, nd=16, micro=1, steps=5,
+                    shard_group=8, extra={"rank": 0, "ag_unit": 0})
+
+
 def ddp_sweep() -> Workload:
     """Replicated DDP bucketing: 16 x [768, 768, (768,3072), (768,3072),
     (4096,4096)] + 3 x (768,3072), bf16 gradients, N_d = 8, bucket caps of 1,
@@ -125,13 +141,16 @@ def ddp_sweep() -> Workload:
                     extra={"caps_mib": [1, 4, 25, 64, 256]})
 
 
-ALL = {w().name: w for w in (unit_9m, gpt2_small, llama_1b, llama_7b_rank_view, ddp_sweep)}
+ALL = {w().name: w for w in (unit_9m, gpt2_small, llama_1b, llama_7b_rank_view,
+                               llama_7b_hybrid_view, ddp_sweep)}
 
 
 # ------------------------------------------------- one rank's shard of all units
 # A rank keeps its shard of every unit back to back: shard index i of the
 # rank's concatenated shard belongs to unit u at local position i - start_u,
-# which is element r*S_u + (i - start_u) of that unit's flat buffer.
+# which is element r*S_u + (i - start_u) of that unit's flat buffer (r is the
+# shard index: the rank itself under full sharding, its position in the group
+# under hybrid sharding).
 
 def rank_shard_index(w: Workload):
     """[(unit, start in the rank's concatenated shard, S_u)] and the total."""

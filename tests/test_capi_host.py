@@ -170,3 +170,30 @@ def test_other_entry_points_reject_bad_arguments():
                              ctypes.byref(_capi.c_i32())) == _capi.ERR_INVALID
     with pytest.raises(ss.ShardstepError):
         ss.fsdp_layout([3, -1], 2)
+
+
+def test_hybrid_ledger_matches_oracle():
+    for psi in (7e9, 351e6):
+        for nd, F in ((8, 1), (8, 2), (8, 4), (8, 8), (16, 8), (6, 3)):
+            assert ss.hybrid_state_bytes(psi, F) == pytest.approx(
+                oracle.hybrid_state_bytes_per_gpu(psi, F), rel=1e-15)
+            for kind in ("intra", "inter"):
+                for exact in (False, True):
+                    assert ss.hybrid_comm_bytes(psi, nd, F, kind, exact) == pytest.approx(
+                        oracle.hybrid_comm_bytes_per_gpu(psi, nd, F, kind, exact), rel=1e-15,
+                        abs=0)
+    with pytest.raises(ValueError):
+        ss.hybrid_comm_bytes(1e9, 8, 3, "intra")
+
+
+def test_hybrid_step_rejects_a_factor_that_does_not_divide():
+    L = _capi.lib()
+    A = 1 << 40
+    g = [A + k * (1 << 20) for k in range(8)]
+    st = [A + (1 << 30) + k * (1 << 20) for k in range(4)]
+    hp = _capi.AdamWHP(1e-3, 0.9, 0.999, 1e-8, 0.01, 1)
+    for F in (0, 3, 5, 16, -2):
+        rc = L.fsdp_hybrid_rs_avg_adamw_cast(_capi.ptr_array(g), _capi.DTYPE_BF16, 8, F, 1024,
+                                             *[ctypes.c_void_p(x) for x in st], ctypes.byref(hp),
+                                             None)
+        assert rc == _capi.ERR_INVALID, F

@@ -132,6 +132,52 @@ def test_fused_step_multi_tile(nd, gdt, S, path):
     assert_bits(host_bf16(out), ob, "bf16")
 
 
+@pytest.mark.parametrize("nd,F", [(2, 1), (4, 2), (6, 3), (8, 1), (8, 2), (8, 4), (8, 8),
+                                  (16, 8), (16, 4)])
+@pytest.mark.parametrize("gdt,S,shift", [("bf16", 13, 0), ("bf16", 70001, 0), ("bf16", 4099, 1),
+                                         ("f32", 6151, 0), ("f32", 4099, 1)])
+def test_hybrid_step_matches_oracle(nd, F, gdt, S, shift, path):
+    seed = 31 * nd + F + S
+    f = (S + F - 1) % F
+    p = synth.host_fill(synth.normal_stream(seed, (97, 2), 0.02), 0, S, "f32")
+    m = np.zeros(S, np.float32)
+    v = np.zeros(S, np.float32)
+    dp, dm, dv = dev_f32(p, shift), dev_f32(m, shift), dev_f32(v, shift)
+    out = torch.empty(S + 1, dtype=torch.bfloat16, device=DEV)[shift:shift + S]
+    for t in (1, 2):
+        contribs = _grads(seed, nd, F * S, gdt, t)
+        mk = dev_bf16 if gdt == "bf16" else dev_f32
+        slices = [mk(c[f * S:(f + 1) * S], shift if k % 2 else 0) for k, c in enumerate(contribs)]
+        ss.fsdp_hybrid_rs_avg_adamw_cast(slices, F, dp, dm, dv, out, HPC, t)
+        p, m, v, ob = oracle.hybrid_shard_step(contribs, F, f, S, p, m, v, HP, t)
+        torch.cuda.synchronize()
+        for name, got, want in (("master", host_f32(dp), p), ("m", host_f32(dm), m),
+                                ("v", host_f32(dv), v)):
+            assert_f32(got, want, f"{name} step {t}")
+            assert_bits(got, want, f"{name} step {t}")
+        assert_bits(host_bf16(out), ob, f"bf16 step {t}")
+
+
+def test_hybrid_group_order_is_not_the_flat_order(path):
+    # the nested sum keeps what the flat rank-order sum rounds away
+    S, nd, F = 4096, 4, 2
+    vals = [2.0 ** 24, 1.0, 1.0, 1.0]
+    slices = [torch.full((S,), x, dtype=torch.float32, device=DEV) for x in vals]
+    res = {}
+    for name, call in (("hybrid", lambda *a: ss.fsdp_hybrid_rs_avg_adamw_cast(slices, F, *a)),
+                       ("flat", lambda *a: ss.fsdp_rs_avg_adamw_cast(slices, *a))):
+        dp = torch.zeros(S, device=DEV)
+        dm = torch.zeros(S, device=DEV)
+        dv = torch.zeros(S, device=DEV)
+        out = torch.empty(S, dtype=torch.bfloat16, device=DEV)
+        # beta1 = 0, lr = 0: m = (1 - 0) * g holds the reduced gradient exactly
+        call(dp, dm, dv, out, ss.AdamW(lr=0.0, beta1=0.0, beta2=0.5, eps=1.0, weight_decay=0.0), 1)
+        res[name] = host_f32(dm)
+    torch.cuda.synchronize()
+    assert np.all(res["hybrid"] == np.float32(4194304.5))
+    assert np.all(res["flat"] == np.float32(4194304.0))
+
+
 def test_fused_step_padding_stays_zero(path):
     # zero gradients and zero master (the padding of a FlatParameter) stay zero
     S, nd = 10000, 4

@@ -264,6 +264,50 @@ def test_llama_7b_rank_view_as_benchmarked():
         assert_bits(_host_bf16(full[q * S + torch.from_numpy(loc).to(DEV)]), want, "peer shard")
 
 
+def test_llama_7b_hybrid_view_as_benchmarked():
+    # N_d = 16 ranks in two groups of F = 8: rank (g=0, f=0)'s shard of every
+    # unit, with all 16 contributions, one fused launch
+    w = W.llama_7b_hybrid_view()
+    hp, hpc = _hp(w)
+    f = w.extra["rank"]
+    opt = RankShardOptimizer(w.units, w.nd, f, hpc, device=DEV, shard_group=w.F)
+    assert opt.shard_total == 842_301_952
+    W.dev_fill_rank_master(w, f, opt.master)
+    rng = np.random.default_rng(11)
+    parts, total = W.rank_shard_index(w)
+    idx = _sample(total, 100_000, rng, extra=[s for _, s, _ in parts])
+    p = W.host_gather_rank_master(w, f, idx)
+    m = np.zeros(idx.size, np.float32)
+    v = np.zeros(idx.size, np.float32)
+    for t in (1, 2):
+        for k in range(w.nd):
+            W.dev_fill_rank_grad(w, t, f, k, 0, opt.grad_in[k])
+        launches = ss.launch_count()
+        opt.step()
+        assert ss.launch_count() - launches == 1
+        contribs = [W.host_gather_rank_grad(w, t, f, k, 0, idx) for k in range(w.nd)]
+        p, m, v, ob = oracle.hybrid_shard_step(contribs, w.F, 0, idx.size, p, m, v, hp, t)
+    torch.cuda.synchronize()
+    it = torch.from_numpy(idx).to(DEV)
+    assert_bits(opt.master[it].cpu().numpy(), p, "master")
+    assert_bits(opt.m[it].cpu().numpy(), m, "m")
+    assert_bits(opt.v[it].cpu().numpy(), v, "v")
+    assert_bits(_host_bf16(opt.params[it]), ob, "bf16")
+    # all-gather inside the group of 8
+    u = w.extra["ag_unit"]
+    S, P = w.unit_shard(u), w.unit_padded(u)
+    peers = [torch.empty(S, dtype=torch.bfloat16, device=DEV) for _ in range(w.F)]
+    for q in range(1, w.F):
+        synth.dev_fill(w.peer_shard_stream(2, q, u), peers[q])
+    full = torch.empty(P, dtype=torch.bfloat16, device=DEV)
+    views = opt.gather_unit(u, peers, full)
+    torch.cuda.synchronize()
+    assert [tuple(x.shape) for x in views] == [tuple(s) for s in w.units[u]]
+    assert torch.equal(full[:S].view(torch.int16), opt.unit_slice(opt.params, u).view(torch.int16))
+    for q in range(1, w.F):
+        assert torch.equal(full[q * S:(q + 1) * S].view(torch.int16), peers[q].view(torch.int16))
+
+
 # ------------------------------------------------------- DDP bucket sweep
 
 def test_ddp_bucket_sweep_full_size():
