@@ -31,6 +31,9 @@ Readings taken where the pages are silent (each is repeated where it is used):
   * Hybrid sharding: ranks k = g*F + j; the reduce sums inside each group
     first (the group's reduce-scatter), then across groups (the all-reduce),
     then divides by N_d.
+  * FSDP2: c = ceil(d0/N_d) rows of each parameter per rank (possibly none);
+    rank-major communication buffers, each rank's rows of every parameter
+    zero-padded to c rows.
   * Buckets: parameters walked in reverse registration order, a bucket is
     closed before a parameter that would take it over the cap, a parameter
     larger than the cap gets a bucket to itself, parameters are never split.
@@ -45,6 +48,8 @@ from .numerics import (AdamWConfig, adamw_scalars, adamw, bf16_to_f32, f32_to_bf
                        grad_accumulate, rs_avg, fsdp_shard_step, hybrid_rs_avg,
                        hybrid_shard_step)
 from .ddp import bucket_plan, bucket_allreduce_avg, ddp_step
+from .fsdp2 import (Fsdp2Layout, fsdp2_layout, local_shards, chunk_cat, local_buffer,
+                    all_gather_copy_out)
 from .ledger import (state_bytes_per_gpu, comm_bytes_per_gpu, hybrid_state_bytes_per_gpu,
                      hybrid_comm_bytes_per_gpu, GB)
 
@@ -53,5 +58,6 @@ __all__ = [
     "AdamWConfig", "adamw_scalars", "adamw", "bf16_to_f32", "f32_to_bf16", "grad_accumulate",
     "rs_avg", "fsdp_shard_step", "hybrid_rs_avg", "hybrid_shard_step", "bucket_plan",
     "bucket_allreduce_avg", "ddp_step", "state_bytes_per_gpu", "comm_bytes_per_gpu",
-    "hybrid_state_bytes_per_gpu", "hybrid_comm_bytes_per_gpu", "GB",
+    "hybrid_state_bytes_per_gpu", "hybrid_comm_bytes_per_gpu", "GB", "Fsdp2Layout",
+    "fsdp2_layout", "local_shards", "chunk_cat", "local_buffer", "all_gather_copy_out",
 ]
