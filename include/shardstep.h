@@ -223,6 +223,54 @@ int fsdp_hybrid_rs_avg_adamw_cast(const void* const* grad_slices, int32_t grad_d
 int fsdp_ag_unpack(const uint16_t* const* shards, int32_t nd, int64_t S, uint16_t* full,
                    void* stream);
 
+/* ---------------------------------------------------------- FSDP2 */
+
+/* FSDP2 per-parameter sharding along dim 0 ([P1] section "FSDP2：分别记录每个
+ * 参数的分片" and its figure: each parameter of a fully_shard group is split
+ * along dim 0 -- a (4,2) weight on two ranks is (2,2) locally, an (8,4)
+ * weight on four ranks (2,4) -- while the group is still communicated with
+ * one all-gather and one reduce-scatter).  Parameter t has dim0[t] rows of
+ * row[t] elements (row = product of the trailing dims, 1 for a vector).
+ * Rank r holds rows [r*c_t, min((r+1)*c_t, dim0[t])), c_t = ceil(dim0[t] /
+ * nd), possibly none.  A rank's local buffer of the group concatenates, in
+ * registration order, its rows of every parameter zero-padded to c_t rows:
+ * local = sum_t c_t * row[t] elements; parameter t starts at offset[t].  The
+ * group's communication buffers are rank-major: nd pieces of `local`.
+ *
+ * fsdp2_layout -- host only: chunk[n] (c_t), offset[n] (may be NULL) and
+ * *local.  Errors: INVALID for n < 0, nd < 1, negative sizes, NULL arrays. */
+int fsdp2_layout(const int64_t* dim0, const int64_t* row, int32_t n, int32_t nd, int64_t* chunk,
+                 int64_t* offset, int64_t* local);
+
+/* fsdp2_local_views -- host only: DTensor.to_local() of rank `rank` inside its
+ * local buffer `base`: ptrs[t] = base + offset[t] elements, rows[t] = the
+ * rows it holds (the local shape is (rows[t], trailing dims)). */
+int fsdp2_local_views(const int64_t* dim0, const int64_t* row, int32_t n, int32_t nd,
+                      int32_t rank, void* base, int32_t elem_size, void** ptrs, int64_t* rows);
+
+/* fsdp2_chunk_cat -- device, batched copy.  One rank's reduce-scatter input:
+ *     out[r*local + offset[t] + k] = grads[t][r*c_t*row[t] + k]   (held rows)
+ *                                  = 0                             (padding rows)
+ * for every rank piece r and parameter t, so that
+ * fsdp_rs_avg_adamw_cast over the N_d ranks' buffers (slices at r*local)
+ * reduce-scatters the group.
+ *   grads[n]  host array of device pointers, full contiguous tensors.
+ *   out       device, nd*local elements, must not overlap any gradient.
+ *   dtype     SHARDSTEP_DTYPE_BF16 or _F32. */
+int fsdp2_chunk_cat(const void* const* grads, const int64_t* dim0, const int64_t* row, int32_t n,
+                    int32_t nd, int32_t dtype, void* out, void* stream);
+
+/* fsdp2_all_gather_copy_out -- device, batched copy.  All-gather of the ranks'
+ * local buffers straight into the full per-parameter tensors (no
+ * intermediate gather buffer):
+ *     params[t][r*c_t*row[t] + k] = local_bufs[r][offset[t] + k]   (held rows)
+ *   local_bufs[nd]  host array of device pointers, `local` elements each.
+ *   params[n]       host array of device pointers, full contiguous tensors of
+ *                   dim0[t]*row[t] elements; must not overlap the buffers. */
+int fsdp2_all_gather_copy_out(const void* const* local_bufs, const int64_t* dim0,
+                              const int64_t* row, int32_t n, int32_t nd, int32_t dtype,
+                              void* const* params, void* stream);
+
 /* ---------------------------------------------------- DDP buckets */
 
 /* ddp_bucket_plan -- host only.

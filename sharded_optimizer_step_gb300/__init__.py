@@ -23,7 +23,8 @@ __all__ = [
     "fsdp_grad_accumulate", "fsdp_rs_avg_adamw_cast", "fsdp_ag_unpack", "ddp_bucket_plan",
     "ddp_bucket_allreduce_avg", "state_bytes", "comm_bytes", "launch_count", "MAX_ND",
     "set_fused_path", "device_status", "fsdp_hybrid_rs_avg_adamw_cast", "hybrid_state_bytes",
-    "hybrid_comm_bytes",
+    "hybrid_comm_bytes", "Fsdp2Layout", "fsdp2_layout", "fsdp2_local_views", "fsdp2_chunk_cat",
+    "fsdp2_all_gather_copy_out",
 ]
 
 
@@ -224,6 +225,100 @@ def fsdp_ag_unpack(shards, full, stream=None):
         _capi.ptr_array([s.data_ptr() for s in shards]), nd, S, ctypes.c_void_p(full.data_ptr()),
         _stream(stream, full.device)))
     return full
+
+
+# ----------------------------------------------------------------- FSDP2
+
+def _dims(shapes):
+    d0, row = [], []
+    for s in shapes:
+        s = tuple(int(d) for d in s)
+        if not s:
+            raise ValueError("scalar parameters have no dim 0")
+        r = 1
+        for d in s[1:]:
+            r *= d
+        d0.append(s[0])
+        row.append(r)
+    return d0, row
+
+
+@dataclass
+class Fsdp2Layout:
+    shapes: list
+    nd: int
+    chunk: list     # rows per rank of each parameter
+    offset: list    # element offset of each parameter in a rank's local buffer
+    local: int      # elements of a rank's local buffer
+
+
+def fsdp2_layout(shapes, nd: int) -> Fsdp2Layout:
+    """Per-parameter dim-0 sharding of one group (host only)."""
+    d0, row = _dims(shapes)
+    n = len(shapes)
+    chunk = (_capi.c_i64 * max(1, n))()
+    off = (_capi.c_i64 * max(1, n))()
+    local = _capi.c_i64(0)
+    _capi.check("fsdp2_layout", _capi.lib().fsdp2_layout(
+        _capi.i64_array(d0), _capi.i64_array(row), n, nd, chunk, off, ctypes.byref(local)))
+    return Fsdp2Layout([tuple(s) for s in shapes], nd, list(chunk[:n]), list(off[:n]),
+                       local.value)
+
+
+def fsdp2_local_views(buf, shapes, nd: int, rank: int):
+    """Rank ``rank``'s local tensors (rows, trailing dims) inside its local
+    buffer, as DTensor.to_local() shows them."""
+    d0, row = _dims(shapes)
+    n = len(shapes)
+    ptrs = (_capi.c_vp * max(1, n))()
+    rows = (_capi.c_i64 * max(1, n))()
+    es = buf.element_size()
+    _capi.check("fsdp2_local_views", _capi.lib().fsdp2_local_views(
+        _capi.i64_array(d0), _capi.i64_array(row), n, nd, rank, ctypes.c_void_p(buf.data_ptr()),
+        es, ptrs, rows))
+    out = []
+    for t, s in enumerate(shapes):
+        off = ((ptrs[t] or buf.data_ptr()) - buf.data_ptr()) // es
+        k = rows[t] * row[t]
+        out.append(buf[off:off + k].view((rows[t],) + tuple(s[1:])))
+    return out
+
+
+def fsdp2_chunk_cat(grads, nd: int, out=None, stream=None):
+    """One rank's reduce-scatter input of a group: nd rank pieces of the
+    local length, each rank's rows of every gradient zero-padded."""
+    import torch
+    _need_cuda(*grads)
+    shapes = [tuple(g.shape) for g in grads]
+    lay = fsdp2_layout(shapes, nd)
+    if out is None:
+        out = torch.empty(nd * lay.local, dtype=grads[0].dtype, device=grads[0].device)
+    _need_cuda(out)
+    if out.numel() != nd * lay.local or any(g.dtype != out.dtype for g in grads):
+        raise ValueError("out must have nd * local elements of the gradients' dtype")
+    d0, row = _dims(shapes)
+    _capi.check("fsdp2_chunk_cat", _capi.lib().fsdp2_chunk_cat(
+        _capi.ptr_array([g.data_ptr() for g in grads]), _capi.i64_array(d0), _capi.i64_array(row),
+        len(grads), nd, _dtype_code(out), ctypes.c_void_p(out.data_ptr()),
+        _stream(stream, out.device)))
+    return out
+
+
+def fsdp2_all_gather_copy_out(local_bufs, params, stream=None):
+    """All-gather the ranks' local buffers straight into the full
+    per-parameter tensors ``params`` (global shapes)."""
+    _need_cuda(*local_bufs, *params)
+    shapes = [tuple(p.shape) for p in params]
+    nd = len(local_bufs)
+    lay = fsdp2_layout(shapes, nd)
+    if any(b.numel() != lay.local or b.dtype != params[0].dtype for b in local_bufs):
+        raise ValueError("local buffers must have the local length and the params' dtype")
+    d0, row = _dims(shapes)
+    _capi.check("fsdp2_all_gather_copy_out", _capi.lib().fsdp2_all_gather_copy_out(
+        _capi.ptr_array([b.data_ptr() for b in local_bufs]), _capi.i64_array(d0),
+        _capi.i64_array(row), len(params), nd, _dtype_code(params[0]),
+        _capi.ptr_array([p.data_ptr() for p in params]), _stream(stream, params[0].device)))
+    return params
 
 
 # ----------------------------------------------------------- DDP buckets

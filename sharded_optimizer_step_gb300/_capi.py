@@ -51,6 +51,10 @@ SIGNATURES = {
     "fsdp_hybrid_rs_avg_adamw_cast": (c_i32, [P_vp, c_i32, c_i32, c_i32, c_i64, c_vp, c_vp, c_vp,
                                               c_vp, ctypes.POINTER(AdamWHP), c_vp]),
     "fsdp_ag_unpack": (c_i32, [P_vp, c_i32, c_i64, c_vp, c_vp]),
+    "fsdp2_layout": (c_i32, [P_i64, P_i64, c_i32, c_i32, P_i64, P_i64, P_i64]),
+    "fsdp2_local_views": (c_i32, [P_i64, P_i64, c_i32, c_i32, c_i32, c_vp, c_i32, P_vp, P_i64]),
+    "fsdp2_chunk_cat": (c_i32, [P_vp, P_i64, P_i64, c_i32, c_i32, c_i32, c_vp, c_vp]),
+    "fsdp2_all_gather_copy_out": (c_i32, [P_vp, P_i64, P_i64, c_i32, c_i32, c_i32, P_vp, c_vp]),
     "ddp_bucket_plan": (c_i32, [P_i64, c_i32, c_i32, c_i64, P_i64, P_i32, P_i64, P_i32]),
     "ddp_bucket_allreduce_avg": (c_i32, [P_vp, c_i32, P_i64, c_i32, c_i32, c_vp, c_vp]),
     "shardstep_state_bytes": (c_f64, [c_f64, c_i32, c_i32, c_f64]),

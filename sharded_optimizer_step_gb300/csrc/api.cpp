@@ -466,6 +466,156 @@ double shardstep_hybrid_comm_bytes(double psi, int32_t nd, int32_t shard_group, 
     return -1.0;
 }
 
+// ------------------------------------------------------------- FSDP2
+
+}  // extern "C"
+
+namespace {
+
+// Per-parameter dim-0 layout shared by the FSDP2 entry points.
+struct Fsdp2Plan {
+    std::vector<int64_t> chunk, offset;
+    int64_t local = 0;
+};
+
+int fsdp2_plan(const int64_t* dim0, const int64_t* row, int32_t n, int32_t nd, Fsdp2Plan* plan) {
+    if (n < 0) return fail(SHARDSTEP_ERR_INVALID, "n must be >= 0");
+    if (nd < 1) return fail(SHARDSTEP_ERR_INVALID, "nd must be >= 1 (got %d)", nd);
+    if (n > 0 && (dim0 == nullptr || row == nullptr))
+        return fail(SHARDSTEP_ERR_INVALID, "dim0 / row is NULL");
+    plan->chunk.assign(n, 0);
+    plan->offset.assign(n, 0);
+    int64_t pos = 0;
+    for (int32_t t = 0; t < n; ++t) {
+        if (dim0[t] < 0 || row[t] < 0)
+            return fail(SHARDSTEP_ERR_INVALID, "parameter %d has a negative size", t);
+        const int64_t c = (dim0[t] + nd - 1) / nd;
+        if (row[t] > 0 && c > (INT64_MAX / 16 - pos) / row[t])
+            return fail(SHARDSTEP_ERR_INVALID, "group too large");
+        plan->chunk[t] = c;
+        plan->offset[t] = pos;
+        pos += c * row[t];
+    }
+    plan->local = pos;
+    return SHARDSTEP_OK;
+}
+
+int64_t rows_of(const Fsdp2Plan& p, const int64_t* dim0, int32_t r, int32_t t) {
+    const int64_t left = dim0[t] - static_cast<int64_t>(r) * p.chunk[t];
+    return left < 0 ? 0 : (left < p.chunk[t] ? left : p.chunk[t]);
+}
+
+}  // namespace
+
+extern "C" {
+
+int fsdp2_layout(const int64_t* dim0, const int64_t* row, int32_t n, int32_t nd, int64_t* chunk,
+                 int64_t* offset, int64_t* local) {
+    if (local == nullptr) return fail(SHARDSTEP_ERR_INVALID, "local is NULL");
+    Fsdp2Plan plan;
+    int rc = fsdp2_plan(dim0, row, n, nd, &plan);
+    if (rc != SHARDSTEP_OK) return rc;
+    for (int32_t t = 0; t < n; ++t) {
+        if (chunk) chunk[t] = plan.chunk[t];
+        if (offset) offset[t] = plan.offset[t];
+    }
+    *local = plan.local;
+    return ok();
+}
+
+int fsdp2_local_views(const int64_t* dim0, const int64_t* row, int32_t n, int32_t nd,
+                      int32_t rank, void* base, int32_t elem_size, void** ptrs, int64_t* rows) {
+    Fsdp2Plan plan;
+    int rc = fsdp2_plan(dim0, row, n, nd, &plan);
+    if (rc != SHARDSTEP_OK) return rc;
+    if (rank < 0 || rank >= nd) return fail(SHARDSTEP_ERR_INVALID, "rank %d out of range", rank);
+    if (elem_size <= 0) return fail(SHARDSTEP_ERR_INVALID, "elem_size must be > 0");
+    if (n > 0 && (ptrs == nullptr || rows == nullptr))
+        return fail(SHARDSTEP_ERR_INVALID, "ptrs / rows is NULL");
+    for (int32_t t = 0; t < n; ++t) {
+        ptrs[t] = static_cast<char*>(base) + plan.offset[t] * elem_size;
+        rows[t] = rows_of(plan, dim0, rank, t);
+    }
+    return ok();
+}
+
+int fsdp2_chunk_cat(const void* const* grads, const int64_t* dim0, const int64_t* row, int32_t n,
+                    int32_t nd, int32_t dtype, void* out, void* stream) {
+    const int es = elem_size_of(dtype);
+    if (es == 0) return fail(SHARDSTEP_ERR_INVALID, "unknown dtype %d", dtype);
+    Fsdp2Plan plan;
+    int rc = fsdp2_plan(dim0, row, n, nd, &plan);
+    if (rc != SHARDSTEP_OK) return rc;
+    if (plan.local == 0) return ok();
+    if (out == nullptr || (n > 0 && grads == nullptr))
+        return fail(SHARDSTEP_ERR_INVALID, "grads / out is NULL");
+    if (!aligned(out, es)) return fail(SHARDSTEP_ERR_INVALID, "out is not %d-byte aligned", es);
+    const Span os = span(out, static_cast<int64_t>(nd) * plan.local * es);
+    for (int32_t t = 0; t < n; ++t) {
+        const int64_t bytes = dim0[t] * row[t] * es;
+        if (bytes == 0) continue;
+        if (grads[t] == nullptr) return fail(SHARDSTEP_ERR_INVALID, "grads[%d] is NULL", t);
+        if (!aligned(grads[t], es))
+            return fail(SHARDSTEP_ERR_INVALID, "grads[%d] is not %d-byte aligned", t, es);
+        if (overlap(span(grads[t], bytes), os))
+            return fail(SHARDSTEP_ERR_INVALID, "grads[%d] overlaps out", t);
+    }
+    CopyBatcher cb(static_cast<cudaStream_t>(stream));
+    char* o = static_cast<char*>(out);
+    for (int32_t r = 0; r < nd; ++r)
+        for (int32_t t = 0; t < n; ++t) {
+            const int64_t rows = rows_of(plan, dim0, r, t), seg = plan.chunk[t] * row[t];
+            char* dst = o + (static_cast<int64_t>(r) * plan.local + plan.offset[t]) * es;
+            const int64_t have = rows * row[t];
+            cb.add(static_cast<const char*>(grads[t]) +
+                       static_cast<int64_t>(r) * plan.chunk[t] * row[t] * es,
+                   dst, have * es);
+            cb.add(nullptr, dst + have * es, (seg - have) * es);  // zero padding rows
+        }
+    cb.flush();
+    return cb.rc == SHARDSTEP_OK ? ok() : cb.rc;
+}
+
+int fsdp2_all_gather_copy_out(const void* const* local_bufs, const int64_t* dim0,
+                              const int64_t* row, int32_t n, int32_t nd, int32_t dtype,
+                              void* const* params, void* stream) {
+    const int es = elem_size_of(dtype);
+    if (es == 0) return fail(SHARDSTEP_ERR_INVALID, "unknown dtype %d", dtype);
+    Fsdp2Plan plan;
+    int rc = fsdp2_plan(dim0, row, n, nd, &plan);
+    if (rc != SHARDSTEP_OK) return rc;
+    if (plan.local == 0) return ok();
+    if (local_bufs == nullptr || (n > 0 && params == nullptr))
+        return fail(SHARDSTEP_ERR_INVALID, "local_bufs / params is NULL");
+    for (int32_t r = 0; r < nd; ++r) {
+        if (local_bufs[r] == nullptr)
+            return fail(SHARDSTEP_ERR_INVALID, "local_bufs[%d] is NULL", r);
+        if (!aligned(local_bufs[r], es))
+            return fail(SHARDSTEP_ERR_INVALID, "local_bufs[%d] is not %d-byte aligned", r, es);
+    }
+    for (int32_t t = 0; t < n; ++t) {
+        const int64_t bytes = dim0[t] * row[t] * es;
+        if (bytes == 0) continue;
+        if (params[t] == nullptr) return fail(SHARDSTEP_ERR_INVALID, "params[%d] is NULL", t);
+        if (!aligned(params[t], es))
+            return fail(SHARDSTEP_ERR_INVALID, "params[%d] is not %d-byte aligned", t, es);
+        for (int32_t r = 0; r < nd; ++r)
+            if (overlap(span(params[t], bytes), span(local_bufs[r], plan.local * es)))
+                return fail(SHARDSTEP_ERR_INVALID, "params[%d] overlaps local_bufs[%d]", t, r);
+    }
+    CopyBatcher cb(static_cast<cudaStream_t>(stream));
+    for (int32_t t = 0; t < n; ++t)
+        for (int32_t r = 0; r < nd; ++r) {
+            const int64_t have = rows_of(plan, dim0, r, t) * row[t];
+            cb.add(static_cast<const char*>(local_bufs[r]) + plan.offset[t] * es,
+                   static_cast<char*>(params[t]) +
+                       static_cast<int64_t>(r) * plan.chunk[t] * row[t] * es,
+                   have * es);
+        }
+    cb.flush();
+    return cb.rc == SHARDSTEP_OK ? ok() : cb.rc;
+}
+
 int ddp_bucket_plan(const int64_t* numels, int32_t n, int32_t elem_size, int64_t cap_bytes,
                     int64_t* param_offset, int32_t* bucket_of_param, int64_t* bucket_offsets,
                     int32_t* n_buckets) {

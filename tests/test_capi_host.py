@@ -8,6 +8,7 @@ import os
 import random
 import re
 
+import numpy as np
 import pytest
 
 import oracle
@@ -197,3 +198,50 @@ def test_hybrid_step_rejects_a_factor_that_does_not_divide():
                                              *[ctypes.c_void_p(x) for x in st], ctypes.byref(hp),
                                              None)
         assert rc == _capi.ERR_INVALID, F
+
+
+def test_fsdp2_layout_matches_oracle():
+    dims = [(0,), (1,), (3,), (5,), (2, 3), (7, 1), (4, 2), (5, 2, 2), (11008, 4096), (4096,)]
+    for n in range(1, 4):
+        for shapes in itertools.product(dims, repeat=n):
+            for nd in (1, 2, 3, 8):
+                a = ss.fsdp2_layout(list(shapes), nd)
+                b = oracle.fsdp2_layout(list(shapes), nd)
+                assert (a.chunk, a.offset, a.local) == (b.chunk, b.offset, b.local)
+
+
+def test_fsdp2_local_views_of_the_page_examples():
+    L = _capi.lib()
+    base = 0x20000
+    for shapes, nd, want_rows in (([(4, 2)] * 3, 2, [2, 2, 2]), ([(8, 4)], 4, [2])):
+        d0 = [s[0] for s in shapes]
+        row = [int(np.prod(s[1:])) for s in shapes]
+        n = len(shapes)
+        for r in range(nd):
+            ptrs = (_capi.c_vp * n)()
+            rows = (_capi.c_i64 * n)()
+            _capi.check("fsdp2_local_views", L.fsdp2_local_views(
+                _capi.i64_array(d0), _capi.i64_array(row), n, nd, r, ctypes.c_void_p(base), 2,
+                ptrs, rows))
+            assert list(rows) == want_rows
+            lay = oracle.fsdp2_layout(shapes, nd)
+            assert [p - base for p in ptrs] == [2 * o for o in lay.offset]
+
+
+def test_fsdp2_entry_points_reject_bad_arguments():
+    L = _capi.lib()
+    A = 1 << 40
+    d0, row = _capi.i64_array([8, 3]), _capi.i64_array([4, 1])
+    local = _capi.c_i64()
+    assert L.fsdp2_layout(d0, row, 2, 0, None, None, ctypes.byref(local)) == _capi.ERR_INVALID
+    assert L.fsdp2_layout(_capi.i64_array([-1]), row, 1, 2, None, None,
+                          ctypes.byref(local)) == _capi.ERR_INVALID
+    # gradient overlapping the output buffer
+    assert L.fsdp2_chunk_cat(_capi.ptr_array([A, A + 4096]), d0, row, 2, 2, _capi.DTYPE_BF16,
+                             ctypes.c_void_p(A + 16), None) == _capi.ERR_INVALID
+    assert L.fsdp2_chunk_cat(_capi.ptr_array([A, A + 4096]), d0, row, 2, 2, 5,
+                             ctypes.c_void_p(A + 1 << 20), None) == _capi.ERR_INVALID
+    # parameter overlapping a local buffer
+    assert L.fsdp2_all_gather_copy_out(_capi.ptr_array([A, A + 4096]), d0, row, 2, 2,
+                                       _capi.DTYPE_BF16, _capi.ptr_array([A + 32, A + 8192]),
+                                       None) == _capi.ERR_INVALID

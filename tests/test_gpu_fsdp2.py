@@ -1,0 +1,166 @@
+"""GPU parity of the FSDP2 per-parameter Shard(0) path against the oracle:
+chunk-cat (the reduce-scatter input), the fused step on the padded local
+buffers, and the all-gather straight into full per-parameter tensors, on
+uneven dim 0, misaligned tensors and the model-shaped groups."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sharded_optimizer_step_gb300 as ss
+import synth
+from oracle.numerics import AdamWConfig
+from synth import workloads as W
+from tests._cmp import assert_bits
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+HP = AdamWConfig()
+HPC = ss.AdamW()
+
+SHAPE_SETS = [
+    [(4, 2), (4, 2), (4, 2)],
+    [(8, 4)],
+    [(7, 3), (5,), (9, 2), (1, 17), (0, 4), (3,)],
+    [(2304, 768), (2304,), (768, 768), (768,), (3072, 768), (3072,), (768, 3072), (768,),
+     (768,), (768,), (768,), (768,)],
+    [(4097, 5), (13,), (1030, 3)],
+]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    ss.build()
+    synth.build_dev()
+
+
+def _dev(h, shift=0):
+    dt = torch.bfloat16 if h.dtype == np.uint16 else torch.float32
+    buf = torch.empty(h.size + shift + 8, dtype=dt, device=DEV)
+    t = buf[shift:shift + h.size]
+    src = torch.from_numpy(np.ascontiguousarray(h).view(np.int16 if h.dtype == np.uint16
+                                                        else np.float32))
+    t.copy_(src.view(dt))
+    return t
+
+
+def _host(t):
+    if t.dtype == torch.bfloat16:
+        return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    return t.contiguous().cpu().numpy()
+
+
+def _tensors(shapes, seed, dtype):
+    return [synth.host_fill(synth.normal_stream(seed, (90, t), 1e-3), 0, int(np.prod(s)),
+                            dtype).reshape(s) for t, s in enumerate(shapes)]
+
+
+@pytest.mark.parametrize("shapes", SHAPE_SETS, ids=lambda s: f"{len(s)}params")
+@pytest.mark.parametrize("nd", [1, 2, 4, 8])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_chunk_cat_and_copy_out_match_oracle(shapes, nd, dtype):
+    host = _tensors(shapes, nd, dtype)
+    dev = [_dev(h.reshape(-1), t % 3).view(s) for t, (h, s) in enumerate(zip(host, shapes))]
+    lay = oracle.fsdp2_layout(shapes, nd)
+    cc = ss.fsdp2_chunk_cat(dev, nd)
+    want = oracle.chunk_cat(host, lay)
+    torch.cuda.synchronize()
+    assert_bits(_host(cc), want, "chunk_cat")
+    # local views have the DTensor local shapes
+    for r in range(nd):
+        loc = ss.fsdp2_local_views(cc[r * lay.local:(r + 1) * lay.local], shapes, nd, r)
+        for t, (a, b) in enumerate(zip(loc, oracle.local_shards(host, lay, r))):
+            assert tuple(a.shape) == b.shape
+            assert_bits(_host(a).reshape(-1), b.reshape(-1), f"local {r} {t}")
+    # all-gather the rank pieces back into full tensors
+    bufs = [cc[r * lay.local:(r + 1) * lay.local].clone() for r in range(nd)]
+    outs = [torch.full(s, 7.0, dtype=dev[0].dtype, device=DEV) for s in shapes]
+    ss.fsdp2_all_gather_copy_out(bufs, outs)
+    torch.cuda.synchronize()
+    for o, h in zip(outs, host):
+        assert_bits(_host(o).reshape(-1), h.reshape(-1), "copy-out")
+
+
+@pytest.mark.parametrize("shapes", SHAPE_SETS[2:], ids=lambda s: f"{len(s)}params")
+@pytest.mark.parametrize("nd", [2, 8])
+def test_fsdp2_step_matches_oracle(shapes, nd):
+    # every rank: chunk-cat its gradients; rank r: fused step on its padded
+    # local buffer with the nd pieces r; then the all-gather copy-out
+    lay = oracle.fsdp2_layout(shapes, nd)
+    masters = [synth.host_fill(synth.normal_stream(3, (89, t), 0.02), 0, int(np.prod(s)),
+                               "f32").reshape(s) for t, s in enumerate(shapes)]
+    state = []
+    for r in range(nd):
+        p = oracle.local_buffer(masters, lay, r)
+        state.append(dict(p=p, m=np.zeros(lay.local, np.float32), v=np.zeros(lay.local, np.float32),
+                          dp=_dev(p), dm=torch.zeros(lay.local, device=DEV),
+                          dv=torch.zeros(lay.local, device=DEV),
+                          out=torch.empty(lay.local, dtype=torch.bfloat16, device=DEV)))
+    for t in (1, 2):
+        grads = [_tensors(shapes, 100 * t + q, "bf16") for q in range(nd)]
+        cc_h = [oracle.chunk_cat(g, lay) for g in grads]
+        cc = [ss.fsdp2_chunk_cat([_dev(x.reshape(-1)).view(x.shape) for x in g], nd) for g in grads]
+        for r, st in enumerate(state):
+            ss.fsdp_rs_avg_adamw_cast([c[r * lay.local:(r + 1) * lay.local] for c in cc],
+                                      st["dp"], st["dm"], st["dv"], st["out"], HPC, t)
+            st["p"], st["m"], st["v"], st["ob"] = oracle.fsdp_shard_step(
+                cc_h, r, lay.local, st["p"], st["m"], st["v"], HP, t)
+    params = [torch.empty(s, dtype=torch.bfloat16, device=DEV) for s in shapes]
+    ss.fsdp2_all_gather_copy_out([st["out"] for st in state], params)
+    want_params = oracle.all_gather_copy_out([st["ob"] for st in state], lay)
+    torch.cuda.synchronize()
+    for st in state:
+        assert_bits(_host(st["dp"]), st["p"], "master")
+        assert_bits(_host(st["dm"]), st["m"], "m")
+        assert_bits(_host(st["dv"]), st["v"], "v")
+        assert_bits(_host(st["out"]), st["ob"], "bf16 local")
+    for a, b in zip(params, want_params):
+        assert_bits(_host(a).reshape(-1), b.reshape(-1), "gathered parameter")
+
+
+def test_fsdp2_llama_layer_group_full_size():
+    # one Llama-7B layer as an FSDP2 group on 8 ranks, every rank emulated:
+    # chunk-cat of each rank's full gradients, 8 fused steps, copy-out
+    w = W.llama_7b_rank_view()
+    shapes = w.units[0]
+    nd = 8
+    lay = ss.fsdp2_layout(shapes, nd)
+    assert lay.local == 202_383_360 // 8
+    olay = oracle.fsdp2_layout(shapes, nd)
+    grads = [[torch.empty(s, dtype=torch.bfloat16, device=DEV) for s in shapes] for _ in range(nd)]
+    for q in range(nd):
+        for t, g in enumerate(grads[q]):
+            synth.dev_fill(w.grad_stream(1, q, 0, 100 + t), g)
+    cc = [ss.fsdp2_chunk_cat(grads[q], nd) for q in range(nd)]
+    rng = np.random.default_rng(5)
+    masters = [torch.empty(s, dtype=torch.float32, device=DEV) for s in shapes]
+    for t, mt in enumerate(masters):
+        synth.dev_fill(w.master_stream(100 + t), mt)
+    local_master = ss.fsdp2_chunk_cat(masters, nd)
+    outs = []
+    for r in range(nd):
+        sl = slice(r * lay.local, (r + 1) * lay.local)
+        mm = torch.zeros(lay.local, device=DEV)
+        vv = torch.zeros(lay.local, device=DEV)
+        out = torch.empty(lay.local, dtype=torch.bfloat16, device=DEV)
+        ss.fsdp_rs_avg_adamw_cast([c[sl] for c in cc], local_master[sl], mm, vv, out, HPC, 1)
+        outs.append(out)
+    params = [torch.empty(s, dtype=torch.bfloat16, device=DEV) for s in shapes]
+    ss.fsdp2_all_gather_copy_out(outs, params)
+    torch.cuda.synchronize()
+    # oracle on sampled rows of every parameter
+    for t, s in enumerate(shapes):
+        rows = np.unique(np.concatenate([rng.integers(0, s[0], 24), [0, s[0] - 1]]))
+        row = int(np.prod(s[1:]))
+        cols = np.unique(np.concatenate([rng.integers(0, row, 16), [0, row - 1]]))
+        flat_idx = (rows[:, None] * row + cols[None, :]).reshape(-1)
+        gq = [synth.host_gather(w.grad_stream(1, q, 0, 100 + t), flat_idx, "bf16")
+              for q in range(nd)]
+        p0 = synth.host_gather(w.master_stream(100 + t), flat_idx, "f32")
+        z = np.zeros(flat_idx.size, np.float32)
+        _, _, _, ob = oracle.fsdp_shard_step(gq, 0, flat_idx.size, p0, z, z, HP, 1)
+        got = _host(params[t].reshape(-1)[torch.from_numpy(flat_idx).to(DEV)])
+        assert_bits(got, ob, f"param {t}")
+    del olay
