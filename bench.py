@@ -53,7 +53,7 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--e2e-chunks", type=int, default=4)
     ap.add_argument("--e2e-streams", type=int, default=4)
-    ap.add_argument("--workload", choices=sorted(WORKLOADS) + ["llama_7b_fsdp2_layer_nd8"],
+    ap.add_argument("--workload", choices=sorted(WORKLOADS) + [FSDP2_WORKLOAD],
                     default="llama_7b_rank0_nd8",
                     help="the Llama-7B rank view under full sharding (the default line), or "
                          "under hybrid sharding with N_d = 16, F = 8")
@@ -199,7 +199,9 @@ class ClockSampler:
 WORKLOADS = {
     "llama_7b_rank0_nd8": "llama_7b_rank_view",
     "llama_7b_hybrid_nd16_f8_rank0": "llama_7b_hybrid_view",
+    "llama_7b_rank0_nd8_fp16_scaled": "llama_7b_rank_view",
 }
+LOSS_SCALE = 65536.0
 
 
 def workload(args):
@@ -229,7 +231,15 @@ def run_ours(args):
     r = rank % F                        # GPU k holds shard k mod F of its own replica
     dev = torch.device("cuda", local)
     hp = ss.AdamW(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
-    opt = RankShardOptimizer(w.units, nd, r, hp, device=dev, shard_group=w.shard_group)
+    # fp16 gradients under dynamic loss scaling: the gradients arrive
+    # multiplied by the scale; check, scaled step and scale update per step
+    scaled = args.workload.endswith("_fp16_scaled")
+    if scaled:
+        w.grad_sigma *= LOSS_SCALE
+        w.name = args.workload
+    opt = RankShardOptimizer(w.units, nd, r, hp, device=dev, shard_group=w.shard_group,
+                             grad_dtype=torch.float16 if scaled else torch.bfloat16)
+    scaler = ss.GradScaler(LOSS_SCALE, device=dev) if scaled else None
     S = opt.shard_total
     W.dev_fill_rank_master(w, r, opt.master)
     for q in range(nd):
@@ -245,25 +255,35 @@ def run_ours(args):
 
     fused_bytes = (2 * nd + 26) * S
     ag_bytes = 4 * Pu                     # read + write every bf16 element of the unit
-    step_bytes = fused_bytes + ag_bytes
+    check_bytes = 2 * nd * S if scaled else 0   # the non-finite check reads the slices
+    step_bytes = check_bytes + fused_bytes + ag_bytes
     stream = torch.cuda.current_stream(dev)
 
     def one_step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        opt.step()
+        if scaled:
+            scaler.check(opt.grad_in)
         if ev is not None:
             ev[1].record(stream)
-        opt.gather_unit(u, peers, full)
+        if scaled:
+            opt.t += 1
+            scaler.step(opt.grad_in, opt.master, opt.m, opt.v, opt.params, hp, opt.t)
+            scaler.update()
+        else:
+            opt.step()
         if ev is not None:
             ev[2].record(stream)
+        opt.gather_unit(u, peers, full)
+        if ev is not None:
+            ev[3].record(stream)
 
     clocks = ClockSampler(smi_index(local))
     clocks.start()
     for _ in range(args.warmup):
         one_step()
     torch.cuda.synchronize()
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     barrier(world)
@@ -283,8 +303,9 @@ def run_ours(args):
     if status:
         raise RuntimeError(f"a TMA-staged wait ran out during the timed steps (status {status})")
     total_ms = t_start.elapsed_time(t_end)
-    fused_ms = [e[0].elapsed_time(e[1]) for e in events]
-    ag_ms = [e[1].elapsed_time(e[2]) for e in events]
+    check_ms = [e[0].elapsed_time(e[1]) for e in events]
+    fused_ms = [e[1].elapsed_time(e[2]) for e in events]
+    ag_ms = [e[2].elapsed_time(e[3]) for e in events]
     total_ms_max = allreduce_max(world, total_ms)
     all_bytes = allreduce_sum(world, step_bytes * args.steps)
     value = all_bytes / (total_ms_max / 1e3) / 1e9
@@ -298,7 +319,7 @@ def run_ours(args):
     # end to end through the public API: pinned host inputs copied in every
     # step, the gathered unit read back every step
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not scaled:
         e2e = run_e2e(args, torch, ss, opt, peers, full, u, r, nd, stream, step_bytes)
         e2e["value"] = round(allreduce_sum(world, e2e.pop("bytes"))
                              / allreduce_max(world, e2e.pop("seconds")) / 1e9, 1)
@@ -317,13 +338,20 @@ def run_ours(args):
                        "model_shape": f"Llama-style 7B, {len(w.units)} FSDP units",
                        "psi": w.psi, "nd": nd, "shard_group": F, "rank": r,
                        "shard_elements": S,
-                       "grad_dtype": "bf16", "state_dtype": "f32", "ag_unit_params": Pu,
-                       "step": "fused rs_avg+AdamW+bf16 cast over the rank shard (1 launch), "
-                               "then all-gather of one layer unit (1 launch)",
+                       "grad_dtype": "f16" if scaled else "bf16", "state_dtype": "f32",
+                       "ag_unit_params": Pu,
+                       "step": ("non-finite check of the unscaled mean (1 launch), scaled fused "
+                                "rs_avg+AdamW+bf16 cast (1 launch), loss-scale update (1 launch), "
+                                "then all-gather of one layer unit (1 launch)" if scaled else
+                                "fused rs_avg+AdamW+bf16 cast over the rank shard (1 launch), "
+                                "then all-gather of one layer unit (1 launch)"),
                        "bytes_per_step": step_bytes,
                        "l2": f"no flush: each step streams {step_bytes / 1e9:.1f} GB vs a 129 MB L2"},
             "params_per_s": round(S * world / (ms_per_step / 1e3), 1),
-            "kernels": {"fused_ms": round(fused_avg, 4),
+            "kernels": {**({"check_ms": round(sum(check_ms) / len(check_ms), 4),
+                           "check_gbs": round(check_bytes / (sum(check_ms) / len(check_ms) / 1e3)
+                                              / 1e9, 1)} if scaled else {}),
+                        "fused_ms": round(fused_avg, 4),
                         "fused_gbs": round(achieved, 1),
                         "ag_ms": round(ag_avg, 4),
                         "ag_gbs": round(ag_bytes / (ag_avg / 1e3) / 1e9, 1)},
@@ -331,7 +359,7 @@ def run_ours(args):
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "peak_source": ("measured: MEASURED_PEAKS.json hbm_gbs (copy, burst)"
                                          if peak_kind == "measured" else "fallback 6800 GB/s"),
-                         "kernel": f"rs_adamw_cast_tma<bf16> (TMA-staged, N_d = {nd}"
+                         "kernel": f"rs_adamw_cast_tma<{'f16' if scaled else 'bf16'}> (TMA-staged, N_d = {nd}"
                                    + (f", sharding factor {F})" if F != nd else ")"),
                          "algorithmic_bytes_per_launch": fused_bytes,
                          "traffic": (None if traffic_per_elem is None

@@ -50,6 +50,7 @@ extern "C" {
 
 #define SHARDSTEP_DTYPE_BF16 0
 #define SHARDSTEP_DTYPE_F32 1
+#define SHARDSTEP_DTYPE_F16 2 /* IEEE half: gradients under fp16 loss scaling */
 
 #define SHARDSTEP_MAX_ND 64 /* largest N_d a kernel accepts */
 
@@ -161,7 +162,7 @@ int fsdp_grad_accumulate(const uint16_t* g, float* acc, int64_t n, float scale, 
  *   grad_slices[nd]  host array of device pointers: grad_slices[q] is rank
  *                    q's contribution to this rank's shard, S elements of
  *                    grad_dtype (i.e. rank q's flat gradient + r*S).
- *   grad_dtype       SHARDSTEP_DTYPE_BF16 or _F32.
+ *   grad_dtype       SHARDSTEP_DTYPE_BF16, _F32 or _F16 (upcast exactly).
  *   nd               1 <= N_d <= SHARDSTEP_MAX_ND (N_d = 1 is a plain,
  *                    unsharded AdamW + cast over S elements).
  *   master, m, v     device, S fp32 each, updated in place.
@@ -207,6 +208,59 @@ int fsdp_hybrid_rs_avg_adamw_cast(const void* const* grad_slices, int32_t grad_d
                                   int32_t shard_group, int64_t S, float* master, float* m,
                                   float* v, uint16_t* out_bf16, const shardstep_adamw_t* hp,
                                   void* stream);
+
+/* ------------------------------------------------ gradient scaler */
+
+/* Sharded gradient scaler for fp16 loss scaling ([P2] section 3.5: a sharded
+ * gradient scaler adapted to parameter sharding keeps gradient scaling
+ * mathematically equivalent; the page gives no mechanism).  Reading: the loss
+ * is multiplied by a scale s, so the fp16 gradients (SHARDSTEP_DTYPE_F16)
+ * arrive multiplied by s; each rank multiplies its reduced shard gradient by
+ * 1/s and checks it for inf / NaN; the flags are OR-ed over all ranks (one
+ * shared device word: calling the check for every rank's shard is the
+ * all-reduce); a flagged step changes no parameter, moment or bf16 output on
+ * any rank; the scale then backs off, or grows after growth_interval clean
+ * steps.  One step:
+ *     fsdp_grad_unscale_check(rank r's slices ...)      for every rank r
+ *     fsdp_scaled_rs_avg_adamw_cast(rank r ...)          for every rank r
+ *     fsdp_grad_scaler_update(...)                       once
+ *
+ * The scale lives in a device word the caller owns (read, never written, by
+ * the check and the step; written by the update), so a step needs no
+ * host-side knowledge of it: each kernel computes inv = fl32(1 / *scale).
+ *
+ * fsdp_grad_unscale_check -- device.  Sets *found_inf to 1 when any element
+ * of g = fl(reduced mean of the slices * inv) (the reduce in the order of
+ * fsdp_hybrid_rs_avg_adamw_cast; shard_group = nd is the plain rank order)
+ * is inf or NaN; never clears it.  Reads the slices only.
+ *   scale      device, one fp32 word: the current loss scale s.
+ *   found_inf  device, one 4-byte word, zero at the start of the step. */
+int fsdp_grad_unscale_check(const void* const* grad_slices, int32_t grad_dtype, int32_t nd,
+                            int32_t shard_group, int64_t S, const float* scale,
+                            uint32_t* found_inf, void* stream);
+
+/* fsdp_scaled_rs_avg_adamw_cast -- device, one kernel pass.  The fused step
+ * of fsdp_hybrid_rs_avg_adamw_cast on the unscaled gradient
+ *     g = fl(reduced mean * fl32(1 / *scale))
+ * when *found_inf is 0 at launch; when it is non-zero every CTA returns at
+ * once and nothing is written.  Other arguments as
+ * fsdp_hybrid_rs_avg_adamw_cast. */
+int fsdp_scaled_rs_avg_adamw_cast(const void* const* grad_slices, int32_t grad_dtype, int32_t nd,
+                                  int32_t shard_group, int64_t S, float* master, float* m,
+                                  float* v, uint16_t* out_bf16, const shardstep_adamw_t* hp,
+                                  const float* scale, const uint32_t* found_inf, void* stream);
+
+/* fsdp_grad_scaler_update -- device, one thread.  fp32 arithmetic:
+ *     found:  scale = scale * backoff_factor, growth_tracker = 0
+ *     else:   growth_tracker += 1; when it reaches growth_interval the scale
+ *             becomes scale * growth_factor if that is finite, and the
+ *             tracker returns to 0
+ * then *found_inf = 0 for the next step.  All three are device words
+ * (float, int32, uint32) the caller owns.  INVALID for NULL or
+ * growth_interval < 1. */
+int fsdp_grad_scaler_update(float* scale, int32_t* growth_tracker, uint32_t* found_inf,
+                            float growth_factor, float backoff_factor, int32_t growth_interval,
+                            void* stream);
 
 /* ------------------------------------------------------ all-gather */
 

@@ -66,7 +66,9 @@ def _dtype_code(t):
         return _capi.DTYPE_BF16
     if t.dtype == torch.float32:
         return _capi.DTYPE_F32
-    raise TypeError(f"unsupported dtype {t.dtype} (bf16 or fp32)")
+    if t.dtype == torch.float16:
+        return _capi.DTYPE_F16
+    raise TypeError(f"unsupported dtype {t.dtype} (bf16, fp16 or fp32)")
 
 
 def _need_cuda(*tensors):
@@ -206,6 +208,59 @@ def _fused(grad_slices, master, m, v, out_bf16, hp, step, stream, shard_group):
         _capi.check("fsdp_hybrid_rs_avg_adamw_cast", _capi.lib().fsdp_hybrid_rs_avg_adamw_cast(
             ptrs, _dtype_code(grad_slices[0]), len(grad_slices), shard_group, S, *state,
             ctypes.byref(hpc), _stream(stream, master.device)))
+
+
+# -------------------------------------------------------- gradient scaler
+
+class GradScaler:
+    """Sharded dynamic loss scaling over the emulated ranks (fp16 gradients):
+    device words for the scale, the growth tracker and the found-inf flag,
+    and the three C-ABI calls of one step.  Nothing synchronises with the
+    host; read ``scale`` / ``found_inf`` when needed."""
+
+    def __init__(self, init_scale: float = 65536.0, growth_factor: float = 2.0,
+                 backoff_factor: float = 0.5, growth_interval: int = 2000, device="cuda"):
+        import torch
+        self.scale = torch.tensor([init_scale], dtype=torch.float32, device=device)
+        self.tracker = torch.zeros(1, dtype=torch.int32, device=device)
+        self.found_inf = torch.zeros(1, dtype=torch.int32, device=device)
+        self.growth_factor, self.backoff_factor = growth_factor, backoff_factor
+        self.growth_interval = growth_interval
+
+    def check(self, grad_slices, shard_group: int | None = None, stream=None):
+        """OR this shard's non-finite flag (of the mean times 1/scale) into
+        ``found_inf``."""
+        _need_cuda(*grad_slices)
+        S = grad_slices[0].numel()
+        nd = len(grad_slices)
+        _capi.check("fsdp_grad_unscale_check", _capi.lib().fsdp_grad_unscale_check(
+            _capi.ptr_array([g.data_ptr() for g in grad_slices]), _dtype_code(grad_slices[0]),
+            nd, shard_group or nd, S, ctypes.c_void_p(self.scale.data_ptr()),
+            ctypes.c_void_p(self.found_inf.data_ptr()), _stream(stream, grad_slices[0].device)))
+
+    def step(self, grad_slices, master, m, v, out_bf16, hp: AdamW, step: int,
+             shard_group: int | None = None, stream=None):
+        """The fused update on the unscaled gradient, skipped on the device
+        when any rank's check found inf/NaN."""
+        _need_cuda(*grad_slices, master, m, v, out_bf16)
+        S = master.numel()
+        nd = len(grad_slices)
+        hpc = hp.at_step(step)
+        _capi.check("fsdp_scaled_rs_avg_adamw_cast", _capi.lib().fsdp_scaled_rs_avg_adamw_cast(
+            _capi.ptr_array([g.data_ptr() for g in grad_slices]), _dtype_code(grad_slices[0]),
+            nd, shard_group or nd, S, ctypes.c_void_p(master.data_ptr()),
+            ctypes.c_void_p(m.data_ptr()), ctypes.c_void_p(v.data_ptr()),
+            ctypes.c_void_p(out_bf16.data_ptr()), ctypes.byref(hpc),
+            ctypes.c_void_p(self.scale.data_ptr()), ctypes.c_void_p(self.found_inf.data_ptr()),
+            _stream(stream, master.device)))
+
+    def update(self, stream=None):
+        """Back off or grow the scale and reset ``found_inf``."""
+        _capi.check("fsdp_grad_scaler_update", _capi.lib().fsdp_grad_scaler_update(
+            ctypes.c_void_p(self.scale.data_ptr()), ctypes.c_void_p(self.tracker.data_ptr()),
+            ctypes.c_void_p(self.found_inf.data_ptr()), ctypes.c_float(self.growth_factor),
+            ctypes.c_float(self.backoff_factor), self.growth_interval,
+            _stream(stream, self.scale.device)))
 
 
 # ------------------------------------------------------------- all-gather

@@ -25,6 +25,7 @@ PATH_REGISTER = 1
 PATH_TMA = 2
 DTYPE_BF16 = 0
 DTYPE_F32 = 1
+DTYPE_F16 = 2
 MAX_ND = 64
 COMM_KINDS = {"reduce_scatter": 0, "all_gather": 1, "all_reduce": 2, "ddp": 2,
               "zero1": 3, "zero2": 4, "zero3": 5}
@@ -50,6 +51,10 @@ SIGNATURES = {
                                        ctypes.POINTER(AdamWHP), c_vp]),
     "fsdp_hybrid_rs_avg_adamw_cast": (c_i32, [P_vp, c_i32, c_i32, c_i32, c_i64, c_vp, c_vp, c_vp,
                                               c_vp, ctypes.POINTER(AdamWHP), c_vp]),
+    "fsdp_grad_unscale_check": (c_i32, [P_vp, c_i32, c_i32, c_i32, c_i64, c_vp, c_vp, c_vp]),
+    "fsdp_scaled_rs_avg_adamw_cast": (c_i32, [P_vp, c_i32, c_i32, c_i32, c_i64, c_vp, c_vp, c_vp,
+                                              c_vp, ctypes.POINTER(AdamWHP), c_vp, c_vp, c_vp]),
+    "fsdp_grad_scaler_update": (c_i32, [c_vp, c_vp, c_vp, c_f32, c_f32, c_i32, c_vp]),
     "fsdp_ag_unpack": (c_i32, [P_vp, c_i32, c_i64, c_vp, c_vp]),
     "fsdp2_layout": (c_i32, [P_i64, P_i64, c_i32, c_i32, P_i64, P_i64, P_i64]),
     "fsdp2_local_views": (c_i32, [P_i64, P_i64, c_i32, c_i32, c_i32, c_vp, c_i32, P_vp, P_i64]),

@@ -52,7 +52,12 @@ bool overlap(Span a, Span b) {
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 int elem_size_of(int32_t dtype) {
-    return dtype == SHARDSTEP_DTYPE_BF16 ? 2 : dtype == SHARDSTEP_DTYPE_F32 ? 4 : 0;
+    switch (dtype) {
+        case SHARDSTEP_DTYPE_BF16:
+        case SHARDSTEP_DTYPE_F16: return 2;
+        case SHARDSTEP_DTYPE_F32: return 4;
+        default: return 0;
+    }
 }
 
 MeanOp mean_op(int nd, int group) {
@@ -61,6 +66,9 @@ MeanOp mean_op(int nd, int group) {
     mo.pow2 = (nd & (nd - 1)) == 0;
     mo.inv_nd = 1.0f / static_cast<float>(nd);  // exact when nd is a power of two
     mo.group = group;
+    mo.inv_scale = 1.0f;
+    mo.scaled = 0;
+    mo.scale = nullptr;
     return mo;
 }
 
@@ -361,11 +369,45 @@ int fsdp_grad_accumulate(const uint16_t* g, float* acc, int64_t n, float scale, 
 
 namespace {
 
+// Validates N_d gradient slices of S elements, fills `tab`, and reports
+// whether they suit the register-staged vector path (8-byte 16-bit slices,
+// 16-byte fp32 slices) and the TMA-staged path (16-byte slices).
+int take_slices(const void* const* grad_slices, int32_t grad_dtype, int32_t nd, int64_t S,
+                const Span* outs, int n_outs, PtrTable* tab, bool* vec, bool* tma) {
+    const int gs = elem_size_of(grad_dtype);
+    if (gs == 0) return fail(SHARDSTEP_ERR_INVALID, "unknown grad dtype %d", grad_dtype);
+    if (nd < 1) return fail(SHARDSTEP_ERR_INVALID, "nd must be >= 1 (got %d)", nd);
+    if (nd > SHARDSTEP_MAX_ND)
+        return fail(SHARDSTEP_ERR_CAPACITY, "nd %d > %d", nd, SHARDSTEP_MAX_ND);
+    if (grad_slices == nullptr) return fail(SHARDSTEP_ERR_INVALID, "grad_slices is NULL");
+    const uintptr_t gvec = grad_dtype == SHARDSTEP_DTYPE_F32 ? 16 : 8;
+    *vec = true;
+    *tma = true;
+    for (int32_t q = 0; q < nd; ++q) {
+        const void* p = grad_slices[q];
+        if (p == nullptr) return fail(SHARDSTEP_ERR_INVALID, "grad_slices[%d] is NULL", q);
+        if (!aligned(p, gs))
+            return fail(SHARDSTEP_ERR_INVALID, "grad_slices[%d] misaligned for its dtype", q);
+        const Span gsn = span(p, S * gs);
+        for (int a = 0; a < n_outs; ++a)
+            if (overlap(gsn, outs[a]))
+                return fail(SHARDSTEP_ERR_INVALID, "grad_slices[%d] overlaps an output", q);
+        *vec = *vec && aligned(p, gvec);
+        *tma = *tma && aligned(p, 16);
+        tab->p[q] = p;
+    }
+    for (int32_t q = nd; q < SHARDSTEP_MAX_ND; ++q) tab->p[q] = nullptr;
+    return SHARDSTEP_OK;
+}
+
 // The fused step with the slices reduced in groups of `group` ranks
-// (group == nd: plain rank order).
+// (group == nd: plain rank order); with `scaled`, the mean is multiplied by
+// inv_scale and a non-zero *skip at launch leaves everything unchanged.
 int fused_step(const void* const* grad_slices, int32_t grad_dtype, int32_t nd, int32_t group,
                int64_t S, float* master, float* m, float* v, uint16_t* out_bf16,
-               const shardstep_adamw_t* hp, void* stream) {
+               const shardstep_adamw_t* hp, void* stream, const float* scale = nullptr,
+               const unsigned int* skip = nullptr) {
+    int rc = SHARDSTEP_OK;
     const int gs = elem_size_of(grad_dtype);
     if (gs == 0) return fail(SHARDSTEP_ERR_INVALID, "unknown grad dtype %d", grad_dtype);
     if (nd < 1) return fail(SHARDSTEP_ERR_INVALID, "nd must be >= 1 (got %d)", nd);
@@ -376,7 +418,6 @@ int fused_step(const void* const* grad_slices, int32_t grad_dtype, int32_t nd, i
     if (hp->step < 1) return fail(SHARDSTEP_ERR_INVALID, "step must be >= 1 (got %lld)",
                                   static_cast<long long>(hp->step));
     if (S == 0) return ok();
-    if (grad_slices == nullptr) return fail(SHARDSTEP_ERR_INVALID, "grad_slices is NULL");
     if (!master || !m || !v || !out_bf16)
         return fail(SHARDSTEP_ERR_INVALID, "master / m / v / out_bf16 is NULL");
     if (!aligned(master, 4) || !aligned(m, 4) || !aligned(v, 4) || !aligned(out_bf16, 2))
@@ -387,38 +428,30 @@ int fused_step(const void* const* grad_slices, int32_t grad_dtype, int32_t nd, i
         for (int b = a + 1; b < 4; ++b)
             if (overlap(outs[a], outs[b]))
                 return fail(SHARDSTEP_ERR_INVALID, "outputs %d and %d overlap", a, b);
-    // vector path: 4 elements per access -> 16-byte state, 8-byte bf16 (16-byte
-    // fp32) gradient slices, 8-byte bf16 output
+    // vector path: 4 elements per access -> 16-byte state, 8-byte 16-bit
+    // (16-byte fp32) gradient slices, 8-byte bf16 output
     PtrTable tab;
-    const uintptr_t gvec = grad_dtype == SHARDSTEP_DTYPE_F32 ? 16 : 8;
-    bool vec = aligned(master, 16) && aligned(m, 16) && aligned(v, 16) && aligned(out_bf16, 8);
-    for (int32_t q = 0; q < nd; ++q) {
-        const void* p = grad_slices[q];
-        if (p == nullptr) return fail(SHARDSTEP_ERR_INVALID, "grad_slices[%d] is NULL", q);
-        if (!aligned(p, gs))
-            return fail(SHARDSTEP_ERR_INVALID, "grad_slices[%d] misaligned for its dtype", q);
-        const Span gsn = span(p, S * gs);
-        for (int a = 0; a < 4; ++a)
-            if (overlap(gsn, outs[a]))
-                return fail(SHARDSTEP_ERR_INVALID, "grad_slices[%d] overlaps an output", q);
-        vec = vec && aligned(p, gvec);
-        tab.p[q] = p;
-    }
-    for (int32_t q = nd; q < SHARDSTEP_MAX_ND; ++q) tab.p[q] = nullptr;
-    const bool f32g = grad_dtype == SHARDSTEP_DTYPE_F32;
+    bool vec = false, tma = false;
+    rc = take_slices(grad_slices, grad_dtype, nd, S, outs, 4, &tab, &vec, &tma);
+    if (rc != SHARDSTEP_OK) return rc;
+    vec = vec && aligned(master, 16) && aligned(m, 16) && aligned(v, 16) && aligned(out_bf16, 8);
     // TMA-staged path: bulk copies need 16-byte aligned sources; the two
     // stages must fit in shared memory
-    bool tma = g_fused_path.load(std::memory_order_relaxed) != SHARDSTEP_PATH_REGISTER &&
-               S >= kTmaMinElements && aligned(master, 16) && aligned(m, 16) &&
-               aligned(v, 16) && aligned(out_bf16, 8);
-    for (int32_t q = 0; q < nd && tma; ++q) tma = aligned(tab.p[q], 16);
-    if (tma) tma = tma_step_smem_bytes(nd, f32g) <= static_cast<size_t>(device_smem_optin());
-    const MeanOp mo = mean_op(nd, group);
+    tma = tma && g_fused_path.load(std::memory_order_relaxed) != SHARDSTEP_PATH_REGISTER &&
+          S >= kTmaMinElements && aligned(master, 16) && aligned(m, 16) && aligned(v, 16) &&
+          aligned(out_bf16, 8);
+    if (tma)
+        tma = tma_step_smem_bytes(nd, grad_dtype) <= static_cast<size_t>(device_smem_optin());
+    MeanOp mo = mean_op(nd, group);
+    mo.scaled = scale != nullptr;
+    mo.scale = scale;
     cudaError_t e =
-        tma ? launch_rs_adamw_cast_tma(tab, nd, f32g, S, master, m, v, out_bf16, adam_scalars(*hp),
-                                       mo, static_cast<cudaStream_t>(stream))
-            : launch_rs_adamw_cast(tab, nd, f32g, S, master, m, v, out_bf16, adam_scalars(*hp),
-                                   mo, vec, static_cast<cudaStream_t>(stream));
+        tma ? launch_rs_adamw_cast_tma(tab, nd, grad_dtype, S, master, m, v, out_bf16,
+                                       adam_scalars(*hp), mo, skip,
+                                       static_cast<cudaStream_t>(stream))
+            : launch_rs_adamw_cast(tab, nd, grad_dtype, S, master, m, v, out_bf16,
+                                   adam_scalars(*hp), mo, skip, vec,
+                                   static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "fused step kernel launch");
     return ok();
 }
@@ -442,6 +475,62 @@ int fsdp_hybrid_rs_avg_adamw_cast(const void* const* grad_slices, int32_t grad_d
                     "the sharding factor %d must be >= 1 and divide nd = %d", shard_group, nd);
     return fused_step(grad_slices, grad_dtype, nd, shard_group, S, master, m, v, out_bf16, hp,
                       stream);
+}
+
+int fsdp_grad_unscale_check(const void* const* grad_slices, int32_t grad_dtype, int32_t nd,
+                            int32_t shard_group, int64_t S, const float* scale,
+                            uint32_t* found_inf, void* stream) {
+    if (shard_group < 1 || nd < 1 || nd % shard_group != 0)
+        return fail(SHARDSTEP_ERR_INVALID,
+                    "the sharding factor %d must be >= 1 and divide nd = %d", shard_group, nd);
+    if (S < 0) return fail(SHARDSTEP_ERR_INVALID, "S must be >= 0");
+    if (found_inf == nullptr || scale == nullptr)
+        return fail(SHARDSTEP_ERR_INVALID, "found_inf / scale is NULL");
+    if (!aligned(found_inf, 4) || !aligned(scale, 4))
+        return fail(SHARDSTEP_ERR_INVALID, "found_inf / scale misaligned");
+    if (S == 0) return ok();
+    PtrTable tab;
+    bool vec = false, tma = false;
+    const Span fs = span(found_inf, 4);
+    int rc = take_slices(grad_slices, grad_dtype, nd, S, &fs, 1, &tab, &vec, &tma);
+    if (rc != SHARDSTEP_OK) return rc;
+    MeanOp mo = mean_op(nd, shard_group);
+    mo.scaled = 1;
+    mo.scale = scale;
+    cudaError_t e = launch_nonfinite_check(tab, nd, grad_dtype, S, mo, found_inf, vec,
+                                           static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "non-finite check launch");
+    return ok();
+}
+
+int fsdp_scaled_rs_avg_adamw_cast(const void* const* grad_slices, int32_t grad_dtype, int32_t nd,
+                                  int32_t shard_group, int64_t S, float* master, float* m,
+                                  float* v, uint16_t* out_bf16, const shardstep_adamw_t* hp,
+                                  const float* scale, const uint32_t* found_inf, void* stream) {
+    if (shard_group < 1 || nd < 1 || nd % shard_group != 0)
+        return fail(SHARDSTEP_ERR_INVALID,
+                    "the sharding factor %d must be >= 1 and divide nd = %d", shard_group, nd);
+    if (found_inf == nullptr || scale == nullptr)
+        return fail(SHARDSTEP_ERR_INVALID, "found_inf / scale is NULL");
+    if (!aligned(found_inf, 4) || !aligned(scale, 4))
+        return fail(SHARDSTEP_ERR_INVALID, "found_inf / scale misaligned");
+    return fused_step(grad_slices, grad_dtype, nd, shard_group, S, master, m, v, out_bf16, hp,
+                      stream, scale, found_inf);
+}
+
+int fsdp_grad_scaler_update(float* scale, int32_t* growth_tracker, uint32_t* found_inf,
+                            float growth_factor, float backoff_factor, int32_t growth_interval,
+                            void* stream) {
+    if (scale == nullptr || growth_tracker == nullptr || found_inf == nullptr)
+        return fail(SHARDSTEP_ERR_INVALID, "scale / growth_tracker / found_inf is NULL");
+    if (!aligned(scale, 4) || !aligned(growth_tracker, 4) || !aligned(found_inf, 4))
+        return fail(SHARDSTEP_ERR_INVALID, "scaler words must be 4-byte aligned");
+    if (growth_interval < 1) return fail(SHARDSTEP_ERR_INVALID, "growth_interval must be >= 1");
+    cudaError_t e = launch_scaler_update(scale, growth_tracker, found_inf, growth_factor,
+                                         backoff_factor, growth_interval,
+                                         static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "scaler update launch");
+    return ok();
 }
 
 double shardstep_hybrid_state_bytes(double psi, int32_t shard_group, double k) {

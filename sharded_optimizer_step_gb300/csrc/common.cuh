@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -139,7 +140,25 @@ struct GroupSum {
 };
 
 __device__ __forceinline__ float mean_of(float sum, const MeanOp& mo) {
-    return mo.pow2 ? __fmul_rn(sum, mo.inv_nd) : __fdiv_rn(sum, mo.nd);
+    const float g = mo.pow2 ? __fmul_rn(sum, mo.inv_nd) : __fdiv_rn(sum, mo.nd);
+    return mo.scaled ? __fmul_rn(g, mo.inv_scale) : g;
+}
+
+// Reads the loss scale of a scaled reduction: inv_scale = 1 / *scale (IEEE
+// division, fp32).
+__device__ __forceinline__ MeanOp resolve_scale(MeanOp mo) {
+    if (mo.scaled) mo.inv_scale = __fdiv_rn(1.0f, __ldcg(mo.scale));
+    return mo;
+}
+
+// A gradient scaler's skip word: non-zero means this step changes nothing.
+__device__ __forceinline__ bool skip_step(const unsigned int* skip) {
+    return skip != nullptr && __ldcg(skip) != 0u;
+}
+
+// fp16 bits -> fp32 (exact).
+__device__ __forceinline__ float f16_to_f32(uint16_t h) {
+    return __half2float(__ushort_as_half(h));
 }
 
 // One AdamW element update, one IEEE rounding per operation, no contraction:

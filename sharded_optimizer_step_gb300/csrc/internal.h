@@ -19,12 +19,23 @@ struct AdamScalars {
 // 1 < group < N_d: hybrid sharding, group sums first, then across groups),
 // then the total is multiplied by the exact reciprocal when N_d is a power of
 // two (identical to dividing) or divided by N_d.
+// With `scaled` set, the mean is then multiplied by inv_scale, the gradient
+// scaler's 1/s, which each kernel computes at start from the device word
+// *scale (resolve_scale).
 struct MeanOp {
     float inv_nd;
     float nd;
     int pow2;
     int group;
+    float inv_scale;
+    int scaled;
+    const float* scale;
 };
+
+// Gradient element types the fused kernels read (the C ABI's dtype codes).
+constexpr int kGradBF16 = SHARDSTEP_DTYPE_BF16;
+constexpr int kGradF32 = SHARDSTEP_DTYPE_F32;
+constexpr int kGradF16 = SHARDSTEP_DTYPE_F16;
 
 struct PtrTable {
     const void* p[SHARDSTEP_MAX_ND];
@@ -54,17 +65,26 @@ int device_sms();                                   // SMs of the current device
 int resident_blocks(const void* kernel, int threads);  // per SM, cached per kernel
 
 // Launchers (return the CUDA error of the launch).
-cudaError_t launch_rs_adamw_cast(const PtrTable& tab, int nd, bool f32_grads, int64_t S,
+// `skip` (may be null): a device word; when it holds a non-zero value at
+// launch the kernel changes nothing (the gradient scaler's skipped step).
+cudaError_t launch_rs_adamw_cast(const PtrTable& tab, int nd, int grad_type, int64_t S,
                                  float* master, float* m, float* v, uint16_t* out,
-                                 const AdamScalars& c, const MeanOp& mo, bool vec,
-                                 cudaStream_t stream);
+                                 const AdamScalars& c, const MeanOp& mo,
+                                 const unsigned int* skip, bool vec, cudaStream_t stream);
 // TMA-staged fused step (step_tma.cu): dynamic shared memory it needs, the
 // launch, and the device watchdog status word.
-size_t tma_step_smem_bytes(int nd, bool f32_grads);
-cudaError_t launch_rs_adamw_cast_tma(const PtrTable& tab, int nd, bool f32_grads, int64_t S,
+size_t tma_step_smem_bytes(int nd, int grad_type);
+cudaError_t launch_rs_adamw_cast_tma(const PtrTable& tab, int nd, int grad_type, int64_t S,
                                      float* master, float* m, float* v, uint16_t* out,
                                      const AdamScalars& c, const MeanOp& mo,
-                                     cudaStream_t stream);
+                                     const unsigned int* skip, cudaStream_t stream);
+// Gradient scaler (step.cu): the non-finite check of the unscaled mean and
+// the scale update.
+cudaError_t launch_nonfinite_check(const PtrTable& tab, int nd, int grad_type, int64_t S,
+                                   const MeanOp& mo, unsigned int* found, bool vec,
+                                   cudaStream_t stream);
+cudaError_t launch_scaler_update(float* scale, int* tracker, unsigned int* found,
+                                 float growth, float backoff, int interval, cudaStream_t stream);
 cudaError_t read_device_status(unsigned int* status, bool clear);
 int device_smem_optin();  // max dynamic shared memory per block (cached)
 constexpr int64_t kTmaMinElements = 4096;

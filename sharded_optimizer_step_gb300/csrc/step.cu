@@ -1,14 +1,17 @@
-// The fused sharded optimizer step (reduce-scatter average + AdamW + bf16
-// cast in one pass over the shard) and the DDP bucket all-reduce average.
+// Register-staged kernels: the fused sharded optimizer step (reduce-scatter
+// average + AdamW + bf16 cast in one pass over the shard) for the cases the
+// TMA-staged kernel does not take, the DDP bucket all-reduce average, and
+// the gradient scaler's non-finite check and scale update.
 //
-// Both are HBM-bound streams: per shard element the fused kernel reads N_d
-// gradient slices (2 B each, bf16) and the fp32 master/m/v (12 B), and writes
-// master/m/v (12 B) and the bf16 parameter (2 B) -- 2*N_d + 26 bytes, each
-// byte touched once.  Each thread owns 4 consecutive elements per iteration:
-// one 8-byte load per bf16 slice (16 bytes for fp32 slices), one 16-byte load
-// per fp32 state array, every load of the iteration issued before any
-// arithmetic; all accesses are streaming (evict-first) loads and stores.  Blocks of 512 threads are capped at 64 registers so that 32
-// warps per SM keep requests in flight; the grid is three times the resident
+// All are HBM-bound streams: per shard element the fused kernel reads N_d
+// gradient slices (2 B each for bf16 / fp16, 4 B for fp32) and the fp32
+// master/m/v (12 B), and writes master/m/v (12 B) and the bf16 parameter
+// (2 B), each byte touched once.  Each thread owns 4 consecutive elements per
+// iteration: one 8-byte load per 16-bit slice (16 bytes for fp32 slices),
+// one 16-byte load per fp32 state array, every load of the iteration issued
+// before any arithmetic; all accesses are streaming (evict-first) loads and
+// stores.  Blocks of 512 threads are capped at 64 registers so that 32 warps
+// per SM keep requests in flight; the grid is three times the resident
 // capacity (SMs x 2 blocks) and strides over the shard.  Measured on GB300
 // against 8-elements-per-thread blocks of 256 at 112 registers, this shape
 // moves the same bytes about 6% faster.
@@ -18,18 +21,17 @@ namespace shardstep {
 namespace {
 
 constexpr int kRuntimeND = 0;
+constexpr int kStepThreads = 512;  // block of the fused / all-reduce / check kernels
+constexpr int kStepMinBlocks = 2;  // 2 x 512 threads per SM -> <= 64 registers
+constexpr int kGridOversub = 3;    // blocks launched per resident block slot
 
 // ----------------------------------------------------------------- loads
 
-constexpr int kStepThreads = 512;  // block of the fused / all-reduce kernels
-constexpr int kStepMinBlocks = 2;   // 2 x 512 threads per SM -> <= 64 registers
-constexpr int kGridOversub = 3;     // blocks launched per resident block slot
-
-template <bool F32G>
+template <int GT>
 struct GradVec;  // 4 gradient elements of one slice
 
 template <>
-struct GradVec<false> {
+struct GradVec<kGradBF16> {
     uint2 r;
     __device__ __forceinline__ void load(const void* base, int64_t i) {
         r = ldcs8(static_cast<const uint16_t*>(base) + 4 * i);
@@ -41,7 +43,21 @@ struct GradVec<false> {
 };
 
 template <>
-struct GradVec<true> {
+struct GradVec<kGradF16> {
+    uint2 r;
+    __device__ __forceinline__ void load(const void* base, int64_t i) {
+        r = ldcs8(static_cast<const uint16_t*>(base) + 4 * i);
+    }
+    __device__ __forceinline__ void to_f32(float* f) const {
+        f[0] = f16_to_f32(static_cast<uint16_t>(r.x & 0xFFFFu));
+        f[1] = f16_to_f32(static_cast<uint16_t>(r.x >> 16));
+        f[2] = f16_to_f32(static_cast<uint16_t>(r.y & 0xFFFFu));
+        f[3] = f16_to_f32(static_cast<uint16_t>(r.y >> 16));
+    }
+};
+
+template <>
+struct GradVec<kGradF32> {
     uint4 a;
     __device__ __forceinline__ void load(const void* base, int64_t i) {
         a = ldcs16(static_cast<const float*>(base) + 4 * i);
@@ -49,20 +65,21 @@ struct GradVec<true> {
     __device__ __forceinline__ void to_f32(float* f) const { unpack4f(a, f); }
 };
 
-template <bool F32G>
+template <int GT>
 __device__ __forceinline__ float grad_scalar(const void* base, int64_t j) {
-    if (F32G) return static_cast<const float*>(base)[j];
+    if (GT == kGradF32) return static_cast<const float*>(base)[j];
+    if (GT == kGradF16) return f16_to_f32(static_cast<const uint16_t*>(base)[j]);
     return bf16_to_f32(static_cast<const uint16_t*>(base)[j]);
 }
 
 // Sum of the N_d slices at 4 consecutive elements, in the order GroupSum
 // fixes (rank order; grouped for hybrid sharding).
-template <int ND, bool F32G>
+template <int ND, int GT>
 __device__ __forceinline__ void reduce4(const PtrTable& tab, int nd, int group, int64_t i,
                                         float* g) {
     GroupSum<4> acc;
     if constexpr (ND != kRuntimeND) {
-        GradVec<F32G> gv[ND];
+        GradVec<GT> gv[ND];
 #pragma unroll
         for (int q = 0; q < ND; ++q) gv[q].load(tab.p[q], i);
         {
@@ -79,7 +96,7 @@ __device__ __forceinline__ void reduce4(const PtrTable& tab, int nd, int group, 
     } else {
         // any N_d: groups of four slices in flight at a time
         {
-            GradVec<F32G> g0;
+            GradVec<GT> g0;
             g0.load(tab.p[0], i);
             float t[4];
             g0.to_f32(t);
@@ -87,7 +104,7 @@ __device__ __forceinline__ void reduce4(const PtrTable& tab, int nd, int group, 
         }
         int q = 1;
         for (; q + 4 <= nd; q += 4) {
-            GradVec<F32G> gv[4];
+            GradVec<GT> gv[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) gv[u].load(tab.p[q + u], i);
 #pragma unroll
@@ -98,7 +115,7 @@ __device__ __forceinline__ void reduce4(const PtrTable& tab, int nd, int group, 
             }
         }
         for (; q < nd; ++q) {
-            GradVec<F32G> gq;
+            GradVec<GT> gq;
             gq.load(tab.p[q], i);
             float t[4];
             gq.to_f32(t);
@@ -108,13 +125,13 @@ __device__ __forceinline__ void reduce4(const PtrTable& tab, int nd, int group, 
     acc.result(g);
 }
 
-template <bool F32G>
+template <int GT>
 __device__ __forceinline__ float reduce1(const PtrTable& tab, int nd, int group, int64_t j) {
     GroupSum<1> acc;
-    float t = grad_scalar<F32G>(tab.p[0], j);
+    float t = grad_scalar<GT>(tab.p[0], j);
     acc.first(&t);
     for (int q = 1; q < nd; ++q) {
-        t = grad_scalar<F32G>(tab.p[q], j);
+        t = grad_scalar<GT>(tab.p[q], j);
         acc.add(&t, group);
     }
     float g;
@@ -124,12 +141,12 @@ __device__ __forceinline__ float reduce1(const PtrTable& tab, int nd, int group,
 
 // --------------------------------------------------- fused step kernels
 
-template <bool F32G>
+template <int GT>
 __device__ __forceinline__ void step_scalar(const PtrTable& tab, int nd, int64_t j,
                                             float* __restrict__ P, float* __restrict__ M,
                                             float* __restrict__ V, uint16_t* __restrict__ out,
                                             const AdamScalars& c, const MeanOp& mo) {
-    const float g = mean_of(reduce1<F32G>(tab, nd, mo.group, j), mo);
+    const float g = mean_of(reduce1<GT>(tab, nd, mo.group, j), mo);
     float p = P[j], m = M[j], v = V[j];
     adamw_elem(g, p, m, v, c);
     P[j] = p;
@@ -138,14 +155,16 @@ __device__ __forceinline__ void step_scalar(const PtrTable& tab, int nd, int64_t
     out[j] = f32_to_bf16(p);
 }
 
-// Aligned operands (gradient slices and the bf16 output 8-byte aligned for
-// bf16, 16-byte for fp32 slices; state 16-byte aligned): 4 elements per
-// thread per iteration, then the (< 4 element) tail by block 0.
-template <int ND, bool F32G>
+// Aligned operands (16-bit gradient slices and the bf16 output 8-byte
+// aligned, fp32 slices and the state 16-byte aligned): 4 elements per thread
+// per iteration, then the (< 4 element) tail by block 0.
+template <int ND, int GT>
 __global__ void __launch_bounds__(kStepThreads, kStepMinBlocks)
     rs_adamw_cast_vec4(PtrTable tab, int nd, int64_t S, float* __restrict__ P,
                        float* __restrict__ M, float* __restrict__ V, uint16_t* __restrict__ out,
-                       AdamScalars c, MeanOp mo) {
+                       AdamScalars c, MeanOp mo, const unsigned int* skip) {
+    if (skip_step(skip)) return;
+    mo = resolve_scale(mo);
     const int64_t nvec = S >> 2;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kStepThreads;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * kStepThreads + threadIdx.x; i < nvec;
@@ -155,7 +174,7 @@ __global__ void __launch_bounds__(kStepThreads, kStepMinBlocks)
         const uint4 m0 = ldcs16(M + 4 * i);
         const uint4 v0 = ldcs16(V + 4 * i);
         float g[4];
-        reduce4<ND, F32G>(tab, nd, mo.group, i, g);
+        reduce4<ND, GT>(tab, nd, mo.group, i, g);
         float p[4], m[4], v[4];
         unpack4f(p0, p);
         unpack4f(m0, m);
@@ -168,19 +187,22 @@ __global__ void __launch_bounds__(kStepThreads, kStepMinBlocks)
         stcs8(out + 4 * i, make_uint2(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3])));
     }
     if (blockIdx.x == 0 && threadIdx.x < (S & 3))
-        step_scalar<F32G>(tab, nd, (nvec << 2) + threadIdx.x, P, M, V, out, c, mo);
+        step_scalar<GT>(tab, nd, (nvec << 2) + threadIdx.x, P, M, V, out, c, mo);
 }
 
 // Any alignment: one element per thread per iteration.
-template <bool F32G>
+template <int GT>
 __global__ void __launch_bounds__(kThreads)
     rs_adamw_cast_scalar(PtrTable tab, int nd, int64_t S, float* __restrict__ P,
                          float* __restrict__ M, float* __restrict__ V,
-                         uint16_t* __restrict__ out, AdamScalars c, MeanOp mo) {
+                         uint16_t* __restrict__ out, AdamScalars c, MeanOp mo,
+                         const unsigned int* skip) {
+    if (skip_step(skip)) return;
+    mo = resolve_scale(mo);
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
     for (int64_t j = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; j < S;
          j += stride)
-        step_scalar<F32G>(tab, nd, j, P, M, V, out, c, mo);
+        step_scalar<GT>(tab, nd, j, P, M, V, out, c, mo);
 }
 
 // ------------------------------------------------ bucket all-reduce avg
@@ -193,14 +215,14 @@ __global__ void __launch_bounds__(kStepThreads, kStepMinBlocks)
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * kStepThreads + threadIdx.x; i < nvec;
          i += stride) {
         float g[4];
-        reduce4<ND, false>(tab, nd, mo.group, i, g);
+        reduce4<ND, kGradBF16>(tab, nd, mo.group, i, g);
 #pragma unroll
         for (int k = 0; k < 4; ++k) g[k] = mean_of(g[k], mo);
         stcs8(out + 4 * i, make_uint2(pack_bf16x2(g[0], g[1]), pack_bf16x2(g[2], g[3])));
     }
     if (blockIdx.x == 0 && threadIdx.x < (n & 3)) {
         const int64_t j = (nvec << 2) + threadIdx.x;
-        out[j] = f32_to_bf16(mean_of(reduce1<false>(tab, nd, mo.group, j), mo));
+        out[j] = f32_to_bf16(mean_of(reduce1<kGradBF16>(tab, nd, mo.group, j), mo));
     }
 }
 
@@ -210,7 +232,69 @@ __global__ void __launch_bounds__(kThreads)
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
     for (int64_t j = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; j < n;
          j += stride)
-        out[j] = f32_to_bf16(mean_of(reduce1<false>(tab, nd, mo.group, j), mo));
+        out[j] = f32_to_bf16(mean_of(reduce1<kGradBF16>(tab, nd, mo.group, j), mo));
+}
+
+// ------------------------------------------------------ gradient scaler
+
+__device__ __forceinline__ bool not_finite(float x) {
+    return (__float_as_uint(x) & 0x7F800000u) == 0x7F800000u;
+}
+
+// Sets *found when any unscaled mean gradient is inf or NaN.  Reads the
+// slices only (2 B per fp16 slice element); one atomic per warp that saw one.
+template <int ND, int GT>
+__global__ void __launch_bounds__(kStepThreads, kStepMinBlocks)
+    nonfinite_check_vec4(PtrTable tab, int nd, int64_t S, MeanOp mo, unsigned int* found) {
+    mo = resolve_scale(mo);
+    bool bad = false;
+    const int64_t nvec = S >> 2;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kStepThreads;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kStepThreads + threadIdx.x; i < nvec;
+         i += stride) {
+        float g[4];
+        reduce4<ND, GT>(tab, nd, mo.group, i, g);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) bad |= not_finite(mean_of(g[k], mo));
+    }
+    if (blockIdx.x == 0 && threadIdx.x < (S & 3))
+        bad |= not_finite(mean_of(reduce1<GT>(tab, nd, mo.group, (nvec << 2) + threadIdx.x), mo));
+    if (__any_sync(0xFFFFFFFFu, bad) && (threadIdx.x & 31) == 0) atomicOr(found, 1u);
+}
+
+template <int GT>
+__global__ void __launch_bounds__(kThreads)
+    nonfinite_check_scalar(PtrTable tab, int nd, int64_t S, MeanOp mo, unsigned int* found) {
+    mo = resolve_scale(mo);
+    bool bad = false;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    for (int64_t j = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; j < S;
+         j += stride)
+        bad |= not_finite(mean_of(reduce1<GT>(tab, nd, mo.group, j), mo));
+    if (__any_sync(0xFFFFFFFFu, bad) && (threadIdx.x & 31) == 0) atomicOr(found, 1u);
+}
+
+// Dynamic loss-scale update, one thread: backoff on a found inf/NaN, growth
+// after `interval` clean steps in a row (kept only when finite); the found
+// word is consumed and reset for the next step.
+__global__ void scaler_update_kernel(float* scale, int* tracker, unsigned int* found,
+                                     float growth, float backoff, int interval) {
+    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    const float s = *scale;
+    if (*found != 0u) {
+        *scale = __fmul_rn(s, backoff);
+        *tracker = 0;
+    } else {
+        const int t = *tracker + 1;
+        if (t == interval) {
+            const float grown = __fmul_rn(s, growth);
+            if (!not_finite(grown)) *scale = grown;
+            *tracker = 0;
+        } else {
+            *tracker = t;
+        }
+    }
+    *found = 0u;
 }
 
 // --------------------------------------------------------------- launch
@@ -224,30 +308,47 @@ unsigned grid_for(const void* kernel, int64_t work_items, int threads = kThreads
     return static_cast<unsigned>(g < 1 ? 1 : g);
 }
 
-template <int ND, bool F32G>
-cudaError_t go_vec(const PtrTable& tab, int nd, int64_t S, float* P, float* M, float* V,
-                   uint16_t* out, const AdamScalars& c, const MeanOp& mo, cudaStream_t s) {
-    auto k = rs_adamw_cast_vec4<ND, F32G>;
-    const unsigned grid = grid_for(reinterpret_cast<const void*>(k), (S >> 2) > 0 ? (S >> 2) : 1,
-                                   kStepThreads, kGridOversub);
-    k<<<grid, kStepThreads, 0, s>>>(tab, nd, S, P, M, V, out, c, mo);
+struct StepArgs {
+    PtrTable tab;
+    int nd;
+    int64_t S;
+    float *P, *M, *V;
+    uint16_t* out;
+    AdamScalars c;
+    MeanOp mo;
+    const unsigned int* skip;
+};
+
+template <int ND, int GT>
+cudaError_t go_vec(const StepArgs& a, cudaStream_t s) {
+    auto k = rs_adamw_cast_vec4<ND, GT>;
+    const unsigned grid = grid_for(reinterpret_cast<const void*>(k),
+                                   (a.S >> 2) > 0 ? (a.S >> 2) : 1, kStepThreads, kGridOversub);
+    k<<<grid, kStepThreads, 0, s>>>(a.tab, a.nd, a.S, a.P, a.M, a.V, a.out, a.c, a.mo, a.skip);
     note_launch();
     return cudaGetLastError();
 }
 
-template <bool F32G>
-cudaError_t dispatch_vec(const PtrTable& tab, int nd, int64_t S, float* P, float* M, float* V,
-                         uint16_t* out, const AdamScalars& c, const MeanOp& mo,
-                         cudaStream_t s) {
-    switch (nd) {
-        case 1: return go_vec<1, F32G>(tab, nd, S, P, M, V, out, c, mo, s);
-        case 2: return go_vec<2, F32G>(tab, nd, S, P, M, V, out, c, mo, s);
-        case 3: return go_vec<3, F32G>(tab, nd, S, P, M, V, out, c, mo, s);
-        case 4: return go_vec<4, F32G>(tab, nd, S, P, M, V, out, c, mo, s);
-        case 8: return go_vec<8, F32G>(tab, nd, S, P, M, V, out, c, mo, s);
-        case 16: return go_vec<16, F32G>(tab, nd, S, P, M, V, out, c, mo, s);
-        default: return go_vec<kRuntimeND, F32G>(tab, nd, S, P, M, V, out, c, mo, s);
+template <int GT>
+cudaError_t dispatch_vec(const StepArgs& a, cudaStream_t s) {
+    switch (a.nd) {
+        case 1: return go_vec<1, GT>(a, s);
+        case 2: return go_vec<2, GT>(a, s);
+        case 3: return go_vec<3, GT>(a, s);
+        case 4: return go_vec<4, GT>(a, s);
+        case 8: return go_vec<8, GT>(a, s);
+        case 16: return go_vec<16, GT>(a, s);
+        default: return go_vec<kRuntimeND, GT>(a, s);
     }
+}
+
+template <int GT>
+cudaError_t go_scalar(const StepArgs& a, cudaStream_t s) {
+    const unsigned grid = grid_for(reinterpret_cast<const void*>(rs_adamw_cast_scalar<GT>), a.S);
+    rs_adamw_cast_scalar<GT><<<grid, kThreads, 0, s>>>(a.tab, a.nd, a.S, a.P, a.M, a.V, a.out, a.c,
+                                                       a.mo, a.skip);
+    note_launch();
+    return cudaGetLastError();
 }
 
 template <int ND>
@@ -261,27 +362,46 @@ cudaError_t go_ar(const PtrTable& tab, int nd, int64_t n, uint16_t* out, const M
     return cudaGetLastError();
 }
 
-}  // namespace
-
-cudaError_t launch_rs_adamw_cast(const PtrTable& tab, int nd, bool f32_grads, int64_t S,
-                                 float* master, float* m, float* v, uint16_t* out,
-                                 const AdamScalars& c, const MeanOp& mo, bool vec,
-                                 cudaStream_t stream) {
-    if (vec) {
-        return f32_grads ? dispatch_vec<true>(tab, nd, S, master, m, v, out, c, mo, stream)
-                         : dispatch_vec<false>(tab, nd, S, master, m, v, out, c, mo, stream);
-    }
-    const void* kp = f32_grads ? reinterpret_cast<const void*>(rs_adamw_cast_scalar<true>)
-                               : reinterpret_cast<const void*>(rs_adamw_cast_scalar<false>);
-    const unsigned grid = grid_for(kp, S);
-    if (f32_grads)
-        rs_adamw_cast_scalar<true><<<grid, kThreads, 0, stream>>>(tab, nd, S, master, m, v, out, c,
-                                                                  mo);
-    else
-        rs_adamw_cast_scalar<false><<<grid, kThreads, 0, stream>>>(tab, nd, S, master, m, v, out,
-                                                                   c, mo);
+template <int ND, int GT>
+cudaError_t go_check(const PtrTable& tab, int nd, int64_t S, const MeanOp& mo,
+                     unsigned int* found, cudaStream_t s) {
+    auto k = nonfinite_check_vec4<ND, GT>;
+    const unsigned grid = grid_for(reinterpret_cast<const void*>(k), (S >> 2) > 0 ? (S >> 2) : 1,
+                                   kStepThreads, kGridOversub);
+    k<<<grid, kStepThreads, 0, s>>>(tab, nd, S, mo, found);
     note_launch();
     return cudaGetLastError();
+}
+
+template <int GT>
+cudaError_t dispatch_check(const PtrTable& tab, int nd, int64_t S, const MeanOp& mo,
+                           unsigned int* found, bool vec, cudaStream_t s) {
+    if (!vec) {
+        const unsigned grid =
+            grid_for(reinterpret_cast<const void*>(nonfinite_check_scalar<GT>), S);
+        nonfinite_check_scalar<GT><<<grid, kThreads, 0, s>>>(tab, nd, S, mo, found);
+        note_launch();
+        return cudaGetLastError();
+    }
+    switch (nd) {
+        case 4: return go_check<4, GT>(tab, nd, S, mo, found, s);
+        case 8: return go_check<8, GT>(tab, nd, S, mo, found, s);
+        default: return go_check<kRuntimeND, GT>(tab, nd, S, mo, found, s);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_rs_adamw_cast(const PtrTable& tab, int nd, int grad_type, int64_t S,
+                                 float* master, float* m, float* v, uint16_t* out,
+                                 const AdamScalars& c, const MeanOp& mo,
+                                 const unsigned int* skip, bool vec, cudaStream_t stream) {
+    const StepArgs a{tab, nd, S, master, m, v, out, c, mo, skip};
+    switch (grad_type) {
+        case kGradF32: return vec ? dispatch_vec<kGradF32>(a, stream) : go_scalar<kGradF32>(a, stream);
+        case kGradF16: return vec ? dispatch_vec<kGradF16>(a, stream) : go_scalar<kGradF16>(a, stream);
+        default: return vec ? dispatch_vec<kGradBF16>(a, stream) : go_scalar<kGradBF16>(a, stream);
+    }
 }
 
 cudaError_t launch_allreduce_avg(const PtrTable& tab, int nd, int64_t n, uint16_t* out,
@@ -297,6 +417,23 @@ cudaError_t launch_allreduce_avg(const PtrTable& tab, int nd, int64_t n, uint16_
     }
     const unsigned grid = grid_for(reinterpret_cast<const void*>(allreduce_avg_scalar), n);
     allreduce_avg_scalar<<<grid, kThreads, 0, stream>>>(tab, nd, n, out, mo);
+    note_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_nonfinite_check(const PtrTable& tab, int nd, int grad_type, int64_t S,
+                                   const MeanOp& mo, unsigned int* found, bool vec,
+                                   cudaStream_t stream) {
+    switch (grad_type) {
+        case kGradF32: return dispatch_check<kGradF32>(tab, nd, S, mo, found, vec, stream);
+        case kGradF16: return dispatch_check<kGradF16>(tab, nd, S, mo, found, vec, stream);
+        default: return dispatch_check<kGradBF16>(tab, nd, S, mo, found, vec, stream);
+    }
+}
+
+cudaError_t launch_scaler_update(float* scale, int* tracker, unsigned int* found, float growth,
+                                 float backoff, int interval, cudaStream_t stream) {
+    scaler_update_kernel<<<1, 32, 0, stream>>>(scale, tracker, found, growth, backoff, interval);
     note_launch();
     return cudaGetLastError();
 }

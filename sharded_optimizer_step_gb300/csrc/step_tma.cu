@@ -86,11 +86,17 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
         : "memory");
 }
 
-template <bool F32G>
+template <int GT>
 __device__ __forceinline__ void load4_smem(const uint8_t* p, float* f) {
-    if (F32G) {
+    if (GT == kGradF32) {
         const float4 x = *reinterpret_cast<const float4*>(p);
         f[0] = x.x; f[1] = x.y; f[2] = x.z; f[3] = x.w;
+    } else if (GT == kGradF16) {
+        const uint2 r = *reinterpret_cast<const uint2*>(p);
+        f[0] = f16_to_f32(static_cast<uint16_t>(r.x & 0xFFFFu));
+        f[1] = f16_to_f32(static_cast<uint16_t>(r.x >> 16));
+        f[2] = f16_to_f32(static_cast<uint16_t>(r.y & 0xFFFFu));
+        f[3] = f16_to_f32(static_cast<uint16_t>(r.y >> 16));
     } else {
         const uint2 r = *reinterpret_cast<const uint2*>(p);
         f[0] = bf16_lo(r.x); f[1] = bf16_hi(r.x);
@@ -98,9 +104,10 @@ __device__ __forceinline__ void load4_smem(const uint8_t* p, float* f) {
     }
 }
 
-template <bool F32G>
+template <int GT>
 __device__ __forceinline__ float grad1(const void* base, int64_t j) {
-    if (F32G) return static_cast<const float*>(base)[j];
+    if (GT == kGradF32) return static_cast<const float*>(base)[j];
+    if (GT == kGradF16) return f16_to_f32(static_cast<const uint16_t*>(base)[j]);
     return bf16_to_f32(static_cast<const uint16_t*>(base)[j]);
 }
 
@@ -108,12 +115,16 @@ __device__ __forceinline__ float grad1(const void* base, int64_t j) {
 // one possibly shorter, still a multiple of 8 elements, so every bulk copy is
 // a multiple of 16 bytes); the final S - S_main < 8 elements are done by
 // block 0 with ordinary loads.
-template <bool F32G>
+template <int GT>
 __global__ void __launch_bounds__(kTmaThreads, 1)
     rs_adamw_cast_tma(PtrTable tab, int nd, int64_t S, float* __restrict__ P,
                       float* __restrict__ M, float* __restrict__ V, uint16_t* __restrict__ out,
-                      AdamScalars c, MeanOp mo) {
-    constexpr uint32_t gsz = F32G ? 4 : 2;
+                      AdamScalars c, MeanOp mo, const unsigned int* skip) {
+    // a skipped step (gradient scaler found inf/NaN): every thread returns
+    // before any barrier or copy exists
+    if (skip_step(skip)) return;
+    mo = resolve_scale(mo);
+    constexpr uint32_t gsz = GT == kGradF32 ? 4 : 2;
     const uint32_t slice_bytes = kTile * gsz;
     const uint32_t stage_bytes = nd * slice_bytes + 3 * kTile * 4;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -184,12 +195,12 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
             GroupSum<4> acc;
             {
                 float t[4];
-                load4_smem<F32G>(st + e * gsz, t);
+                load4_smem<GT>(st + e * gsz, t);
                 acc.first(t);
             }
             for (int q = 1; q < nd; ++q) {
                 float t[4];
-                load4_smem<F32G>(st + q * slice_bytes + e * gsz, t);
+                load4_smem<GT>(st + q * slice_bytes + e * gsz, t);
                 acc.add(t, mo.group);
             }
             float g[4];
@@ -214,10 +225,10 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     if (blockIdx.x == 0 && tid < S - s_main) {
         const int64_t jx = s_main + tid;
         GroupSum<1> acc;
-        float t = grad1<F32G>(tab.p[0], jx);
+        float t = grad1<GT>(tab.p[0], jx);
         acc.first(&t);
         for (int q = 1; q < nd; ++q) {
-            t = grad1<F32G>(tab.p[q], jx);
+            t = grad1<GT>(tab.p[q], jx);
             acc.add(&t, mo.group);
         }
         float sum;
@@ -235,27 +246,30 @@ int g_smem_set[256];  // per device: dynamic shared memory attribute applied
 
 }  // namespace
 
-size_t tma_step_smem_bytes(int nd, bool f32_grads) {
-    const size_t gsz = f32_grads ? 4 : 2;
+size_t tma_step_smem_bytes(int nd, int grad_type) {
+    const size_t gsz = grad_type == kGradF32 ? 4 : 2;
     return static_cast<size_t>(kStages) * kTile * (nd * gsz + 12) + 2 * kStages * sizeof(uint64_t);
 }
 
-cudaError_t launch_rs_adamw_cast_tma(const PtrTable& tab, int nd, bool f32_grads, int64_t S,
+cudaError_t launch_rs_adamw_cast_tma(const PtrTable& tab, int nd, int grad_type, int64_t S,
                                      float* master, float* m, float* v, uint16_t* out,
                                      const AdamScalars& c, const MeanOp& mo,
-                                     cudaStream_t stream) {
+                                     const unsigned int* skip, cudaStream_t stream) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    const size_t smem = tma_step_smem_bytes(nd, f32_grads);
+    const size_t smem = tma_step_smem_bytes(nd, grad_type);
     if (dev >= 0 && dev < 256 && !g_smem_set[dev]) {
         int optin = 0;
         e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(rs_adamw_cast_tma<false>,
+        e = cudaFuncSetAttribute(rs_adamw_cast_tma<kGradBF16>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(rs_adamw_cast_tma<true>,
+        e = cudaFuncSetAttribute(rs_adamw_cast_tma<kGradF32>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(rs_adamw_cast_tma<kGradF16>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
         if (e != cudaSuccess) return e;
         g_smem_set[dev] = 1;
@@ -264,12 +278,16 @@ cudaError_t launch_rs_adamw_cast_tma(const PtrTable& tab, int nd, bool f32_grads
     int64_t grid = device_sms();
     if (grid > ntiles) grid = ntiles;
     if (grid < 1) grid = 1;
-    if (f32_grads)
-        rs_adamw_cast_tma<true><<<static_cast<unsigned>(grid), kTmaThreads, smem, stream>>>(
-            tab, nd, S, master, m, v, out, c, mo);
+    const unsigned g = static_cast<unsigned>(grid);
+    if (grad_type == kGradF32)
+        rs_adamw_cast_tma<kGradF32><<<g, kTmaThreads, smem, stream>>>(tab, nd, S, master, m, v,
+                                                                     out, c, mo, skip);
+    else if (grad_type == kGradF16)
+        rs_adamw_cast_tma<kGradF16><<<g, kTmaThreads, smem, stream>>>(tab, nd, S, master, m, v,
+                                                                     out, c, mo, skip);
     else
-        rs_adamw_cast_tma<false><<<static_cast<unsigned>(grid), kTmaThreads, smem, stream>>>(
-            tab, nd, S, master, m, v, out, c, mo);
+        rs_adamw_cast_tma<kGradBF16><<<g, kTmaThreads, smem, stream>>>(tab, nd, S, master, m, v,
+                                                                      out, c, mo, skip);
     note_launch();
     return cudaGetLastError();
 }

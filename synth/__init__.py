@@ -122,6 +122,10 @@ def _host_lib():
         lib.synth_fill_f32.argtypes = [P, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int]
         lib.synth_gather_bf16.argtypes = [P, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
         lib.synth_gather_f32.argtypes = [P, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
+        lib.synth_fill_f16.argtypes = [P, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int]
+        lib.synth_gather_f16.argtypes = [P, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
+        lib.synth_f32bits_to_f16.argtypes = [ctypes.c_uint32]
+        lib.synth_f32bits_to_f16.restype = ctypes.c_uint16
         lib.synth_mix64.argtypes = [ctypes.c_uint64]
         lib.synth_mix64.restype = ctypes.c_uint64
         lib.synth_normal.argtypes = [ctypes.c_uint64, ctypes.c_uint64]
@@ -139,7 +143,7 @@ def _dev_lib():
             build_dev()
         lib = ctypes.CDLL(DEV_LIB)
         P = ctypes.POINTER(Stream)
-        for name in ("synth_dev_fill_bf16", "synth_dev_fill_f32"):
+        for name in ("synth_dev_fill_bf16", "synth_dev_fill_f32", "synth_dev_fill_f16"):
             f = getattr(lib, name)
             f.argtypes = [P, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]
             f.restype = ctypes.c_int
@@ -155,9 +159,13 @@ def _threads() -> int:
 
 def host_fill(st: Stream, start: int, n: int, dtype: str, out: np.ndarray | None = None,
               nthreads: int | None = None) -> np.ndarray:
-    """Elements start..start+n-1 as uint16 (bf16 bits) or float32."""
+    """Elements start..start+n-1 as uint16 (bf16 / fp16 bits) or float32."""
     lib = _host_lib()
-    if dtype == "bf16":
+    if dtype == "f16":
+        arr = out if out is not None else np.empty(n, dtype=np.uint16)
+        assert arr.dtype == np.uint16 and arr.size == n and arr.flags.c_contiguous
+        lib.synth_fill_f16(ctypes.byref(st), start, n, arr.ctypes.data, nthreads or _threads())
+    elif dtype == "bf16":
         arr = out if out is not None else np.empty(n, dtype=np.uint16)
         assert arr.dtype == np.uint16 and arr.size == n and arr.flags.c_contiguous
         lib.synth_fill_bf16(ctypes.byref(st), start, n, arr.ctypes.data, nthreads or _threads())
@@ -174,7 +182,10 @@ def host_gather(st: Stream, idx, dtype: str) -> np.ndarray:
     """Elements idx[i] (any order) as uint16 (bf16 bits) or float32."""
     lib = _host_lib()
     idx = np.ascontiguousarray(np.asarray(idx, dtype=np.int64))
-    if dtype == "bf16":
+    if dtype == "f16":
+        out = np.empty(idx.size, dtype=np.uint16)
+        lib.synth_gather_f16(ctypes.byref(st), idx.ctypes.data, idx.size, out.ctypes.data)
+    elif dtype == "bf16":
         out = np.empty(idx.size, dtype=np.uint16)
         lib.synth_gather_bf16(ctypes.byref(st), idx.ctypes.data, idx.size, out.ctypes.data)
     elif dtype == "f32":
@@ -192,7 +203,7 @@ def host_normal(key: int, n: int) -> float:
 # ---------------------------------------------------------------- device API
 
 def dev_fill(st: Stream, tensor, start: int = 0) -> None:
-    """Fill a contiguous CUDA tensor (torch.bfloat16 or torch.float32) with
+    """Fill a contiguous CUDA tensor (torch.bfloat16, float16 or float32) with
     elements start..start+numel-1 of the stream, on torch's current stream."""
     import torch
     assert tensor.is_cuda and tensor.is_contiguous()
@@ -201,6 +212,9 @@ def dev_fill(st: Stream, tensor, start: int = 0) -> None:
     if tensor.dtype == torch.bfloat16:
         rc = lib.synth_dev_fill_bf16(ctypes.byref(st), start, tensor.numel(),
                                      ctypes.c_void_p(tensor.data_ptr()), stream)
+    elif tensor.dtype == torch.float16:
+        rc = lib.synth_dev_fill_f16(ctypes.byref(st), start, tensor.numel(),
+                                    ctypes.c_void_p(tensor.data_ptr()), stream)
     elif tensor.dtype == torch.float32:
         rc = lib.synth_dev_fill_f32(ctypes.byref(st), start, tensor.numel(),
                                     ctypes.c_void_p(tensor.data_ptr()), stream)

@@ -82,4 +82,26 @@ SYN_FN uint16_t syn_f32bits_to_bf16(uint32_t b) {
     return (uint16_t)(r >> 16);
 }
 
+/* fp32 bits -> IEEE half bits, round to nearest even, with subnormal
+ * results, overflow to infinity at 65520 and NaN kept quiet. */
+SYN_FN uint16_t syn_f32bits_to_f16(uint32_t b) {
+    const uint32_t sign = (b >> 16) & 0x8000u;
+    const uint32_t a = b & 0x7FFFFFFFu;
+    if (a >= 0x7F800000u) return (uint16_t)(sign | (a > 0x7F800000u ? 0x7E00u : 0x7C00u));
+    if (a >= 0x477FF000u) return (uint16_t)(sign | 0x7C00u);   /* >= 65520: infinity */
+    if (a < 0x38800000u) {                                      /* below 2^-14 */
+        if (a < 0x33000000u) return (uint16_t)sign;             /* below 2^-25: zero */
+        const uint32_t mant = (a & 0x7FFFFFu) | 0x800000u;
+        const uint32_t shift = 126u - (a >> 23);                /* 14 .. 24 */
+        uint32_t q = mant >> shift;
+        const uint32_t rem = mant & ((1u << shift) - 1u);
+        const uint32_t half = 1u << (shift - 1u);
+        if (rem > half || (rem == half && (q & 1u))) ++q;
+        return (uint16_t)(sign | q);
+    }
+    uint32_t r = a - (112u << 23);                              /* rebias 127 -> 15 */
+    r = (r + 0xFFFu + ((r >> 13) & 1u)) >> 13;
+    return (uint16_t)(sign | r);
+}
+
 #endif /* SYNTH_GEN_H */

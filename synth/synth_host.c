@@ -21,18 +21,28 @@ static inline uint16_t syn_to_bf16(const syn_stream_t* st, uint64_t n) {
     return syn_f32bits_to_bf16(b);
 }
 
+static inline uint16_t syn_to_f16(const syn_stream_t* st, uint64_t n) {
+    float f = syn_to_f32(st, n);
+    uint32_t b;
+    memcpy(&b, &f, 4);
+    return syn_f32bits_to_f16(b);
+}
+
 typedef struct {
     syn_stream_t st;
     int64_t start, lo, hi;
     void* out;
-    int is_bf16;
+    int is_bf16;   /* 1: bf16, 2: fp16, 0: fp32 */
 } job_t;
 
 static void* worker(void* arg) {
     job_t* j = (job_t*)arg;
-    if (j->is_bf16) {
+    if (j->is_bf16 == 1) {
         uint16_t* o = (uint16_t*)j->out;
         for (int64_t i = j->lo; i < j->hi; ++i) o[i] = syn_to_bf16(&j->st, (uint64_t)(j->start + i));
+    } else if (j->is_bf16 == 2) {
+        uint16_t* o = (uint16_t*)j->out;
+        for (int64_t i = j->lo; i < j->hi; ++i) o[i] = syn_to_f16(&j->st, (uint64_t)(j->start + i));
     } else {
         float* o = (float*)j->out;
         for (int64_t i = j->lo; i < j->hi; ++i) o[i] = syn_to_f32(&j->st, (uint64_t)(j->start + i));
@@ -76,6 +86,16 @@ void synth_fill_bf16(const syn_stream_t* st, int64_t start, int64_t n, uint16_t*
 void synth_fill_f32(const syn_stream_t* st, int64_t start, int64_t n, float* out, int nthreads) {
     fill(st, start, n, out, 0, nthreads);
 }
+
+void synth_fill_f16(const syn_stream_t* st, int64_t start, int64_t n, uint16_t* out, int nthreads) {
+    fill(st, start, n, out, 2, nthreads);
+}
+
+void synth_gather_f16(const syn_stream_t* st, const int64_t* idx, int64_t n, uint16_t* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = syn_to_f16(st, (uint64_t)idx[i]);
+}
+
+uint16_t synth_f32bits_to_f16(uint32_t b) { return syn_f32bits_to_f16(b); }
 
 /* out[i] = element idx[i] of the stream. */
 void synth_gather_bf16(const syn_stream_t* st, const int64_t* idx, int64_t n, uint16_t* out) {
