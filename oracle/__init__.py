@@ -37,6 +37,8 @@ Readings taken where the pages are silent (each is repeated where it is used):
   * Gradient scaler: the reduced mean is multiplied by 1/s in fp32 and
     checked for inf/NaN; the flags are OR-ed over all ranks; a flagged step
     changes no state; the scale backs off or grows like dynamic loss scaling.
+  * Checkpoint: a load at N_d' re-slices the unit's flat state (the saved
+    shards concatenated, cut to T) with the FlatParameter layout of N_d'.
   * Buckets: parameters walked in reverse registration order, a bucket is
     closed before a parameter that would take it over the cap, a parameter
     larger than the cap gets a bucket to itself, parameters are never split.
@@ -53,6 +55,7 @@ from .numerics import (AdamWConfig, adamw_scalars, adamw, bf16_to_f32, f32_to_bf
 from .ddp import bucket_plan, bucket_allreduce_avg, ddp_step
 from .scaler import (f16_to_f32, unscaled_mean, found_inf, scaled_shard_step,
                      scaler_update)
+from . import checkpoint
 from .fsdp2 import (Fsdp2Layout, fsdp2_layout, local_shards, chunk_cat, local_buffer,
                     all_gather_copy_out)
 from .ledger import (state_bytes_per_gpu, comm_bytes_per_gpu, hybrid_state_bytes_per_gpu,
@@ -66,4 +69,5 @@ __all__ = [
     "hybrid_state_bytes_per_gpu", "hybrid_comm_bytes_per_gpu", "GB", "Fsdp2Layout",
     "fsdp2_layout", "local_shards", "chunk_cat", "local_buffer", "all_gather_copy_out",
     "f16_to_f32", "unscaled_mean", "found_inf", "scaled_shard_step", "scaler_update",
+    "checkpoint",
 ]
