@@ -53,7 +53,7 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--e2e-chunks", type=int, default=4)
     ap.add_argument("--e2e-streams", type=int, default=4)
-    ap.add_argument("--workload", choices=sorted(WORKLOADS) + [FSDP2_WORKLOAD],
+    ap.add_argument("--workload", choices=sorted(WORKLOADS) + [FSDP2_WORKLOAD, CKPT_WORKLOAD],
                     default="llama_7b_rank0_nd8",
                     help="the Llama-7B rank view under full sharding (the default line), or "
                          "under hybrid sharding with N_d = 16, F = 8")
@@ -670,8 +670,71 @@ def run_fsdp2(args):
         }))
 
 
+# ------------------------------------------------------------ checkpoint
+
+CKPT_WORKLOAD = "ckpt_gpt2_small_nd8_to_nd4"
+
+
+def run_ckpt(args):
+    """Sharded checkpoint of the GPT-2-small-shaped model: every one of 8
+    ranks saves its fp32 master / m / v shards (device -> pinned host -> its
+    own file, ranks in parallel), then 4 ranks of a new layout load their
+    resharded state (pieces of the saved files -> pinned host -> device)."""
+    import shutil
+    import torch
+    torch.cuda.set_device(0)
+    import __graft_entry__
+    __graft_entry__.build()
+    import sharded_optimizer_step_gb300 as ss
+    from sharded_optimizer_step_gb300 import checkpoint as ck
+    from sharded_optimizer_step_gb300.engine import RankShardOptimizer
+    from synth import workloads as W
+    w = W.gpt2_small()
+    hp = ss.AdamW()
+    old = [RankShardOptimizer(w.units, 8, r, hp, device="cuda:0") for r in range(8)]
+    for o in old:
+        W.dev_fill_rank_master(w, o.rank, o.master)
+        for q in range(8):
+            W.dev_fill_rank_grad(w, 1, o.rank, q, 0, o.grad_in[q])
+        o.step()
+    new = [RankShardOptimizer(w.units, 4, r, hp, device="cuda:0") for r in range(4)]
+    torch.cuda.synchronize()
+    state_bytes = sum(3 * 4 * o.shard_total for o in old)
+    directory = tempfile.mkdtemp(prefix="shst_ckpt_")
+    saves, loads = [], []
+    try:
+        for _ in range(max(1, args.steps)):
+            t0 = time.perf_counter()
+            ck.save(directory, old)
+            t1 = time.perf_counter()
+            ck.load(directory, new)
+            t2 = time.perf_counter()
+            saves.append(t1 - t0)
+            loads.append(t2 - t1)
+        disk = sum(os.path.getsize(ck.rank_file(directory, r)) for r in range(8))
+    finally:
+        shutil.rmtree(directory, ignore_errors=True)
+    sv, ld = statistics.median(saves), statistics.median(loads)
+    print(json.dumps({
+        "metric": "sharded checkpoint save / load GB/s (fp32 master + moments)",
+        "value": round(state_bytes / sv / 1e9, 2), "unit": "GB/s", "n_gpus": 1,
+        "steps": len(saves), "warmup": 0, "ms_per_step": round(1e3 * (sv + ld), 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": {"workload": CKPT_WORKLOAD, "state_bytes": state_bytes,
+                                        "file_bytes": disk, "save_ranks": 8, "load_ranks": 4,
+                                        "directory": "a temporary directory under /tmp"},
+        "save_gbs": round(state_bytes / sv / 1e9, 2), "load_gbs": round(state_bytes / ld / 1e9, 2),
+        "save_s": round(sv, 3), "load_s": round(ld, 3),
+        "roofline": None, "e2e": None, "gpu_launches": 0, "clocks": None, "cpu_baseline": None,
+        "note": "host-IO bound (device <-> pinned host copies and file reads / writes); "
+                "no GPU kernel runs"}))
+
+
 def main():
     args = parse()
+    if args.workload == CKPT_WORKLOAD:
+        run_ckpt(args)
+        return
     if args.workload == FSDP2_WORKLOAD:
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "unavailable":

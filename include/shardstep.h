@@ -46,7 +46,8 @@ extern "C" {
 #define SHARDSTEP_ERR_INVALID (-1)  /* bad pointer, size, dtype, rank or overlap */
 #define SHARDSTEP_ERR_CUDA (-3)     /* the CUDA runtime refused a launch or query */
 #define SHARDSTEP_ERR_TIMEOUT (-4)  /* a host-side wait ran past its limit */
-#define SHARDSTEP_ERR_CAPACITY (-5) /* more ranks than SHARDSTEP_MAX_ND */
+#define SHARDSTEP_ERR_CAPACITY (-5) /* more ranks than SHARDSTEP_MAX_ND / a full buffer */
+#define SHARDSTEP_ERR_IO (-6)       /* a checkpoint file could not be written or read back */
 
 #define SHARDSTEP_DTYPE_BF16 0
 #define SHARDSTEP_DTYPE_F32 1
@@ -399,6 +400,70 @@ double shardstep_comm_bytes(double psi, int32_t nd, int32_t kind, int32_t exact)
 double shardstep_hybrid_state_bytes(double psi, int32_t shard_group, double k);
 double shardstep_hybrid_comm_bytes(double psi, int32_t nd, int32_t shard_group, int32_t kind,
                                    int32_t exact);
+
+/* ----------------------------------------------------- checkpoint */
+
+/* Sharded checkpoint ([P1] section "Checkpoint：让各张卡保存自己的分片": with
+ * the model state spread over the GPUs, each rank saves the shards it owns
+ * and the metadata needed to restore them; a load reads according to the
+ * target sharding layout, so the rank count may change between saving and
+ * loading; optimizer state is saved with the weights).  Host only: the
+ * caller stages device state through host memory.
+ *
+ * A rank file holds a 64-byte header (magic "SHSTCKPT", version 1, nd, rank,
+ * section count, step), the element count T_u of every unit's
+ * FlatParameter, a section table and the sections, each at a 4096-byte
+ * aligned offset with an FNV-1a checksum (64-bit, over little-endian 64-bit
+ * words, a trailing partial word zero-padded).  It is written to
+ * "<path>.tmp" and renamed into place. */
+typedef struct {
+    int32_t unit;     /* unit index, 0 <= unit < n_units        */
+    int32_t kind;     /* caller's tag, e.g. 0 master, 1 m, 2 v  */
+    int64_t bytes;
+    const void* data; /* host memory                            */
+} shardstep_ckpt_section_t;
+
+typedef struct {
+    int32_t nd, rank, n_units, n_sections;
+    int64_t step;
+} shardstep_ckpt_info_t;
+
+/* One piece of a reshard plan, in elements of a unit's FlatParameter. */
+typedef struct {
+    int32_t old_rank;   /* saved rank file to read                 */
+    int32_t pad_;
+    int64_t old_offset; /* element offset in that rank's shard     */
+    int64_t new_offset; /* element offset in the new rank's shard  */
+    int64_t count;
+} shardstep_ckpt_piece_t;
+
+/* Writes rank `rank`'s file of a checkpoint taken with nd ranks.
+ * Errors: INVALID (arguments), IO (create / write / rename failed). */
+int shardstep_ckpt_save_rank(const char* path, int32_t nd, int32_t rank, int64_t step,
+                             const int64_t* unit_totals, int32_t n_units,
+                             const shardstep_ckpt_section_t* sections, int32_t n_sections);
+
+/* Header of a rank file; unit_totals (may be NULL) receives up to cap_units
+ * unit element counts.  The tables' checksum is verified.  Errors: IO. */
+int shardstep_ckpt_info(const char* path, shardstep_ckpt_info_t* info, int64_t* unit_totals,
+                        int32_t cap_units);
+
+/* Reads `bytes` bytes at `byte_offset` of the section (unit, kind) into dst
+ * (host).  Errors: INVALID (no such section, range outside it), IO. */
+int shardstep_ckpt_read(const char* path, int32_t unit, int32_t kind, int64_t byte_offset,
+                        int64_t bytes, void* dst);
+
+/* Reads every section of a rank file and checks its checksum.  Errors: IO
+ * on the first mismatch. */
+int shardstep_ckpt_verify(const char* path);
+
+/* The pieces of the saved shards (old_nd ranks, FlatParameter layout of a
+ * unit of `total` elements) that make up rank new_rank's shard under new_nd
+ * ranks, in new-offset order; positions at or past `total` are padding (zero)
+ * and in no piece.  pieces[cap]; *n_pieces receives the count (CAPACITY when
+ * it exceeds cap). */
+int fsdp_reshard_plan(int64_t total, int32_t old_nd, int32_t new_nd, int32_t new_rank,
+                      shardstep_ckpt_piece_t* pieces, int32_t cap, int32_t* n_pieces);
 
 /* ------------------------------------------------------------ misc */
 

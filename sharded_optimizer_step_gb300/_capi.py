@@ -20,6 +20,7 @@ ERR_INVALID = -1
 ERR_CUDA = -3
 ERR_TIMEOUT = -4
 ERR_CAPACITY = -5
+ERR_IO = -6
 PATH_AUTO = 0
 PATH_REGISTER = 1
 PATH_TMA = 2
@@ -39,6 +40,20 @@ class AdamWHP(ctypes.Structure):
 class LayoutInfo(ctypes.Structure):
     _fields_ = [("total", c_i64), ("padded", c_i64), ("shard", c_i64), ("n_tensors", c_i32),
                 ("nd", c_i32)]
+
+
+class CkptSection(ctypes.Structure):
+    _fields_ = [("unit", c_i32), ("kind", c_i32), ("bytes", c_i64), ("data", c_vp)]
+
+
+class CkptInfo(ctypes.Structure):
+    _fields_ = [("nd", c_i32), ("rank", c_i32), ("n_units", c_i32), ("n_sections", c_i32),
+                ("step", c_i64)]
+
+
+class CkptPiece(ctypes.Structure):
+    _fields_ = [("old_rank", c_i32), ("pad_", c_i32), ("old_offset", c_i64),
+                ("new_offset", c_i64), ("count", c_i64)]
 
 
 # name -> (restype, argtypes), exactly the declarations of include/shardstep.h
@@ -66,6 +81,13 @@ SIGNATURES = {
     "shardstep_comm_bytes": (c_f64, [c_f64, c_i32, c_i32, c_i32]),
     "shardstep_hybrid_state_bytes": (c_f64, [c_f64, c_i32, c_f64]),
     "shardstep_hybrid_comm_bytes": (c_f64, [c_f64, c_i32, c_i32, c_i32, c_i32]),
+    "shardstep_ckpt_save_rank": (c_i32, [ctypes.c_char_p, c_i32, c_i32, c_i64, P_i64, c_i32,
+                                         ctypes.POINTER(CkptSection), c_i32]),
+    "shardstep_ckpt_info": (c_i32, [ctypes.c_char_p, ctypes.POINTER(CkptInfo), P_i64, c_i32]),
+    "shardstep_ckpt_read": (c_i32, [ctypes.c_char_p, c_i32, c_i32, c_i64, c_i64, c_vp]),
+    "shardstep_ckpt_verify": (c_i32, [ctypes.c_char_p]),
+    "fsdp_reshard_plan": (c_i32, [c_i64, c_i32, c_i32, c_i32, ctypes.POINTER(CkptPiece), c_i32,
+                                  P_i32]),
     "shardstep_last_error": (ctypes.c_char_p, []),
     "shardstep_set_fused_path": (c_i32, [c_i32]),
     "shardstep_device_status": (c_i32, [ctypes.POINTER(ctypes.c_uint32), c_i32]),

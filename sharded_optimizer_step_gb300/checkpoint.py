@@ -1,0 +1,122 @@
+"""Sharded checkpoints of RankShardOptimizer state.
+
+Each rank writes the shards it owns -- fp32 master weights and both AdamW
+moments of every unit -- to a file of its own, with the step count and every
+unit's element count; a load under another rank count (or sharding factor)
+reads, for each unit, only the pieces of the saved shards that make up the
+new rank's shard.  File format, checksums and the reshard plan are native
+(libshardstep: shardstep_ckpt_*, fsdp_reshard_plan); this module stages the
+device state through pinned host memory.
+
+Under hybrid sharding the F shards of one group are saved (the other groups
+hold identical replicas); a load into any sharding factor works the same way.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from concurrent.futures import ThreadPoolExecutor
+
+from . import _capi
+
+KIND_MASTER, KIND_M, KIND_V = 0, 1, 2
+_KINDS = (KIND_MASTER, KIND_M, KIND_V)
+
+
+def rank_file(directory: str, rank: int) -> str:
+    return os.path.join(directory, f"rank{rank:05d}.shst")
+
+
+def _states(opt):
+    return (opt.master, opt.m, opt.v)
+
+
+def save_rank(directory: str, opt) -> str:
+    """Write ``opt``'s shard state to ``directory`` (rank = opt.rank of opt.F
+    shards).  Synchronises with the device."""
+    import torch
+    os.makedirs(directory, exist_ok=True)
+    host = []
+    for buf in _states(opt):
+        h = torch.empty(buf.numel(), dtype=torch.float32, pin_memory=True)
+        h.copy_(buf, non_blocking=True)
+        host.append(h)
+    torch.cuda.synchronize(opt.master.device)
+    n_units = len(opt.layouts)
+    secs = (_capi.CkptSection * max(1, 3 * n_units))()
+    k = 0
+    for u, lay in enumerate(opt.layouts):
+        for kind, h in zip(_KINDS, host):
+            secs[k] = _capi.CkptSection(u, kind, lay.shard * 4, h.data_ptr() + opt.starts[u] * 4)
+            k += 1
+    path = rank_file(directory, opt.rank)
+    _capi.check("shardstep_ckpt_save_rank", _capi.lib().shardstep_ckpt_save_rank(
+        path.encode(), opt.F, opt.rank, opt.t, _capi.i64_array([l.total for l in opt.layouts]),
+        n_units, secs, k))
+    return path
+
+
+def save(directory: str, opts, threads: int = 8):
+    """Write every rank of a checkpoint (one optimizer per rank of one shard
+    group), ranks in parallel."""
+    with ThreadPoolExecutor(max(1, min(threads, len(opts)))) as ex:
+        return list(ex.map(lambda o: save_rank(directory, o), opts))
+
+
+def info(directory: str, rank: int = 0):
+    """(nd, step, unit totals) of a saved checkpoint."""
+    inf = _capi.CkptInfo()
+    path = rank_file(directory, rank).encode()
+    L = _capi.lib()
+    _capi.check("shardstep_ckpt_info", L.shardstep_ckpt_info(path, ctypes.byref(inf), None, 0))
+    totals = (_capi.c_i64 * max(1, inf.n_units))()
+    _capi.check("shardstep_ckpt_info", L.shardstep_ckpt_info(path, ctypes.byref(inf), totals,
+                                                             inf.n_units))
+    return inf.nd, inf.step, list(totals[:inf.n_units])
+
+
+def verify(directory: str) -> None:
+    """Check every section checksum of every rank file (raises on a mismatch)."""
+    nd, _, _ = info(directory)
+    for r in range(nd):
+        _capi.check("shardstep_ckpt_verify",
+                    _capi.lib().shardstep_ckpt_verify(rank_file(directory, r).encode()))
+
+
+def plan(total: int, old_nd: int, new_nd: int, new_rank: int):
+    """Reshard pieces (old_rank, old_offset, new_offset, count) of one unit."""
+    cap = old_nd + 2
+    pieces = (_capi.CkptPiece * cap)()
+    n = _capi.c_i32(0)
+    _capi.check("fsdp_reshard_plan", _capi.lib().fsdp_reshard_plan(
+        total, old_nd, new_nd, new_rank, pieces, cap, ctypes.byref(n)))
+    return [(p.old_rank, p.old_offset, p.new_offset, p.count) for p in pieces[:n.value]]
+
+
+def load_rank(directory: str, opt) -> None:
+    """Fill ``opt``'s master / m / v (and step count) from a checkpoint saved
+    under any rank count; padding positions of the new layout are zero."""
+    import torch
+    old_nd, step, totals = info(directory)
+    mine = [l.total for l in opt.layouts]
+    if totals != mine:
+        raise ValueError("checkpoint units do not match the optimizer's units")
+    L = _capi.lib()
+    host = [torch.zeros(opt.shard_total, dtype=torch.float32, pin_memory=True) for _ in _KINDS]
+    for u, lay in enumerate(opt.layouts):
+        for q, off, new_off, count in plan(lay.total, old_nd, opt.F, opt.rank):
+            path = rank_file(directory, q).encode()
+            for kind, h in zip(_KINDS, host):
+                dst = h.data_ptr() + (opt.starts[u] + new_off) * 4
+                _capi.check("shardstep_ckpt_read", L.shardstep_ckpt_read(
+                    path, u, kind, off * 4, count * 4, ctypes.c_void_p(dst)))
+    for buf, h in zip(_states(opt), host):
+        buf.copy_(h, non_blocking=True)
+    torch.cuda.synchronize(opt.master.device)
+    opt.t = step
+
+
+def load(directory: str, opts, threads: int = 8) -> None:
+    """Load every optimizer (one per rank of the new layout), in parallel."""
+    with ThreadPoolExecutor(max(1, min(threads, len(opts)))) as ex:
+        list(ex.map(lambda o: load_rank(directory, o), opts))

@@ -133,6 +133,12 @@ std::vector<OccEntry> g_occ;
 
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
+// Error reporting for ckpt.cpp: the message is fmt with one string and one
+// integer argument (either may be unused).
+int ckpt_fail(int code, const char* fmt, const char* a, long long b) {
+    return fail(code, fmt, a, b);
+}
+
 int device_sms() {
     static std::atomic<int> cache[256];
     int dev = 0;
