@@ -15,12 +15,38 @@ from __future__ import annotations
 
 import ctypes
 import os
+import threading
+import weakref
 from concurrent.futures import ThreadPoolExecutor
 
 from . import _capi
 
 KIND_MASTER, KIND_M, KIND_V = 0, 1, 2
 _KINDS = (KIND_MASTER, KIND_M, KIND_V)
+
+# pinned host staging per optimizer, kept for its next save or load: pinning
+# ~12 bytes per shard element costs more than the copies and the file IO
+_STAGING = weakref.WeakKeyDictionary()
+_STAGING_LOCK = threading.Lock()
+
+
+def _staging(opt):
+    import torch
+    with _STAGING_LOCK:
+        bufs = _STAGING.get(opt)
+    if bufs is None or bufs[0].numel() != opt.shard_total:
+        bufs = [torch.empty(opt.shard_total, dtype=torch.float32, pin_memory=True)
+                for _ in _KINDS]
+        with _STAGING_LOCK:
+            _STAGING[opt] = bufs
+    return bufs
+
+
+def release_staging(opt) -> None:
+    """Drop ``opt``'s pinned staging buffers (they are reused by every later
+    save and load of the same optimizer until then)."""
+    with _STAGING_LOCK:
+        _STAGING.pop(opt, None)
 
 
 def rank_file(directory: str, rank: int) -> str:
@@ -36,11 +62,9 @@ def save_rank(directory: str, opt) -> str:
     shards).  Synchronises with the device."""
     import torch
     os.makedirs(directory, exist_ok=True)
-    host = []
-    for buf in _states(opt):
-        h = torch.empty(buf.numel(), dtype=torch.float32, pin_memory=True)
+    host = _staging(opt)
+    for buf, h in zip(_states(opt), host):
         h.copy_(buf, non_blocking=True)
-        host.append(h)
     torch.cuda.synchronize(opt.master.device)
     n_units = len(opt.layouts)
     secs = (_capi.CkptSection * max(1, 3 * n_units))()
@@ -102,8 +126,12 @@ def load_rank(directory: str, opt) -> None:
     if totals != mine:
         raise ValueError("checkpoint units do not match the optimizer's units")
     L = _capi.lib()
-    host = [torch.zeros(opt.shard_total, dtype=torch.float32, pin_memory=True) for _ in _KINDS]
+    host = _staging(opt)
     for u, lay in enumerate(opt.layouts):
+        # positions past the unit's total are padding: no piece covers them
+        covered = max(0, min(lay.shard, lay.total - opt.rank * lay.shard))
+        for h in host:
+            h[opt.starts[u] + covered:opt.starts[u] + lay.shard].zero_()
         for q, off, new_off, count in plan(lay.total, old_nd, opt.F, opt.rank):
             path = rank_file(directory, q).encode()
             for kind, h in zip(_KINDS, host):

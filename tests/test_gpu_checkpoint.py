@@ -95,3 +95,30 @@ def test_hybrid_group_checkpoint_round_trip(tmp_path):
         for u in range(len(o.layouts)):
             got = o.master[o.starts[u]:o.starts[u] + o.layouts[u].shard].cpu().numpy()
             assert got.tobytes() == saved[u][0][s].tobytes()
+
+
+def test_reload_through_used_staging_restores_padding(tmp_path):
+    """Save and load reuse each optimizer's pinned staging: a load after a
+    save of other values must still give zeros at the padding positions of
+    the new layout (N_d = 5 pads every GPT-2 unit)."""
+    w = W.gpt2_small()
+    old = _opts(w, 8)
+    _train(w, old, 1)
+    saved = _host_state(old)
+    a, b = tmp_path / "a", tmp_path / "b"
+    ck.save(str(a), old)
+    new = _opts(w, 5)
+    assert any(lay.padded > lay.total for lay in new[0].layouts)
+    for o in new:
+        for buf in (o.master, o.m, o.v):
+            buf.uniform_(1.0, 2.0)       # padding positions included
+    ck.save(str(b), new)                 # staging now holds these values
+    ck.load(str(a), new)
+    for o in new:
+        for u, lay in enumerate(o.layouts):
+            for k, name in enumerate(("master", "m", "v")):
+                want = ock.reshard(saved[u][k], lay.total, o.F, o.rank)
+                got = getattr(o, name)[o.starts[u]:o.starts[u] + lay.shard].cpu().numpy()
+                assert got.tobytes() == want.tobytes(), (o.rank, u, name)
+    for o in new:
+        ck.release_staging(o)
