@@ -35,12 +35,18 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "fused shard-step HBM GB/s (% of GB300 peak), params/s at Psi=7B, N_d=8"
-KERNEL_SOURCES = ["sharded_optimizer_step_gb300/csrc/step_tma.cu",
-                  "sharded_optimizer_step_gb300/csrc/common.cuh"]
-FUSED_PROFILES = {
-    "llama_7b_rank0_nd8": os.path.join(ROOT, "profiles", "fused_step_llama7b_rank_view.md"),
-    "llama_7b_hybrid_nd16_f8_rank0": os.path.join(ROOT, "profiles",
-                                                  "fused_step_llama7b_hybrid_nd16_f8.md"),
+TMA_SOURCES = ["sharded_optimizer_step_gb300/csrc/step_tma.cu",
+               "sharded_optimizer_step_gb300/csrc/common.cuh"]
+REGISTER_SOURCES = ["sharded_optimizer_step_gb300/csrc/step.cu",
+                    "sharded_optimizer_step_gb300/csrc/common.cuh"]
+# per bench line: the ncu summary of its dominant kernel (DRAM bytes per
+# element, recorded with the hash of the sources that kernel is built from)
+PROFILES = {
+    "llama_7b_rank0_nd8": ("fused_step_llama7b_rank_view.md", TMA_SOURCES),
+    "llama_7b_hybrid_nd16_f8_rank0": ("fused_step_llama7b_hybrid_nd16_f8.md", TMA_SOURCES),
+    "llama_7b_rank0_nd8_fp16_scaled": ("scaled_step_llama7b_rank_view_fp16.md", TMA_SOURCES),
+    "llama_1b_rank0_nd8_m4": ("accumulate_llama1b_rank_view_m4.md", TMA_SOURCES),
+    "ddp_nd8_buckets": ("ddp_buckets_nd8_adamw.md", REGISTER_SOURCES),
 }
 
 
@@ -53,14 +59,21 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--e2e-chunks", type=int, default=4)
     ap.add_argument("--e2e-streams", type=int, default=4)
-    ap.add_argument("--workload", choices=sorted(WORKLOADS) + [FSDP2_WORKLOAD, CKPT_WORKLOAD],
+    ap.add_argument("--workload", choices=sorted(WORKLOADS) + [FSDP2_WORKLOAD, CKPT_WORKLOAD,
+                                                             ACCUM_WORKLOAD, DDP_WORKLOAD],
                     default="llama_7b_rank0_nd8",
-                    help="the Llama-7B rank view under full sharding (the default line), or "
-                         "under hybrid sharding with N_d = 16, F = 8")
+                    help="the Llama-7B rank view under full sharding (the default line); the "
+                         "other lines time the other steps of the path")
     ap.add_argument("--layers", type=int, default=0,
                     help="smaller case: only the first N layer units (for profiler captures)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--tma-stages", type=int, default=0,
+                    help="shared-memory stages of the TMA-staged kernels "
+                         "(0: about 128 KB of tiles in flight per SM)")
+    ap.add_argument("--kernel-path", choices=["auto", "register", "tma"], default="auto",
+                    help="streaming kernels: TMA-staged where they measured faster (auto), "
+                         "register-staged only, or TMA-staged wherever the arguments allow")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     return ap.parse_args()
@@ -119,27 +132,41 @@ def measured_peak():
         return 6800.0, "fallback"
 
 
-def kernel_source_hash():
+def kernel_source_hash(sources=TMA_SOURCES):
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in sources:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
 def profiled_traffic(workload_name):
-    """DRAM bytes per element of the fused kernel recorded from an ncu capture
-    of this workload, if the capture was taken on the current kernel source
-    (else None)."""
+    """DRAM bytes per element of a bench line's dominant kernel, recorded from
+    an ncu capture of this workload, if the capture was taken on the current
+    source of that kernel (else None)."""
     try:
-        text = open(FUSED_PROFILES[workload_name]).read()
+        name, sources = PROFILES[workload_name]
+        text = open(os.path.join(ROOT, "profiles", name)).read()
     except (OSError, KeyError):
         return None
     m = re.search(r"traffic_bytes_per_element:\s*([0-9.]+)", text)
     h = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", text)
-    if not m or not h or h.group(1) != kernel_source_hash():
+    if not m or not h or h.group(1) != kernel_source_hash(sources):
         return None
     return float(m.group(1))
+
+
+def _apply_stages(args):
+    import sharded_optimizer_step_gb300 as ss
+    ss.set_tma_stages(args.tma_stages)
+    ss.set_fused_path(args.kernel_path)
+
+
+def _stages_name(args):
+    if args.kernel_path != "auto":
+        return f"{args.kernel_path}-staged kernels" + (
+            "" if args.tma_stages == 0 else f", {args.tma_stages} stages")
+    return "auto" if args.tma_stages == 0 else args.tma_stages
 
 
 def smi_index(local: int) -> str:
@@ -221,6 +248,7 @@ def run_ours(args):
     torch.cuda.set_device(local)
     import __graft_entry__
     __graft_entry__.build()
+    _apply_stages(args)
     import sharded_optimizer_step_gb300 as ss
     import synth
     from sharded_optimizer_step_gb300.engine import RankShardOptimizer
@@ -314,7 +342,8 @@ def run_ours(args):
     ag_avg = sum(ag_ms) / len(ag_ms)
     peak, peak_kind = measured_peak()
     achieved = fused_bytes / (fused_avg / 1e3) / 1e9
-    traffic_per_elem = profiled_traffic(args.workload)
+    traffic_per_elem = (None if args.layers or args.kernel_path != "auto" or args.tma_stages
+                        else profiled_traffic(args.workload))
 
     # end to end through the public API: pinned host inputs copied in every
     # step, the gathered unit read back every step
@@ -334,7 +363,7 @@ def run_ours(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded counter-based generator on the device; no data set or weights)",
-            "config": {"workload": w.name,
+            "config": {"workload": w.name, "tma_stages": _stages_name(args),
                        "model_shape": f"Llama-style 7B, {len(w.units)} FSDP units",
                        "psi": w.psi, "nd": nd, "shard_group": F, "rank": r,
                        "shard_elements": S,
@@ -359,7 +388,7 @@ def run_ours(args):
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "peak_source": ("measured: MEASURED_PEAKS.json hbm_gbs (copy, burst)"
                                          if peak_kind == "measured" else "fallback 6800 GB/s"),
-                         "kernel": f"rs_adamw_cast_tma<{'f16' if scaled else 'bf16'}> (TMA-staged, N_d = {nd}"
+                         "kernel": f"staged_stream<AdamOp<{'f16' if scaled else 'bf16'}>> (TMA-staged, N_d = {nd}"
                                    + (f", sharding factor {F})" if F != nd else ")"),
                          "algorithmic_bytes_per_launch": fused_bytes,
                          "traffic": (None if traffic_per_elem is None
@@ -563,6 +592,7 @@ def run_fsdp2(args):
     torch.cuda.set_device(local_rank)
     import __graft_entry__
     __graft_entry__.build()
+    _apply_stages(args)
     import sharded_optimizer_step_gb300 as ss
     import synth
     from synth import workloads as W
@@ -648,7 +678,8 @@ def run_fsdp2(args):
             "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded counter-based generator on the device; no data set or weights)",
-            "config": {"workload": FSDP2_WORKLOAD, "group": "one Llama-7B layer (9 parameters, "
+            "config": {"workload": FSDP2_WORKLOAD, "tma_stages": _stages_name(args),
+                       "group": "one Llama-7B layer (9 parameters, "
                        "202,383,360 elements)", "nd": nd, "local_elements": L,
                        "step": "8 x chunk-cat of a rank's full bf16 gradients, 8 x fused step on "
                                "the padded local buffers, all-gather copy-out into the 9 full "
@@ -664,7 +695,7 @@ def run_fsdp2(args):
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "peak_source": ("measured: MEASURED_PEAKS.json hbm_gbs (copy, burst)"
                                          if peak_kind == "measured" else "fallback 6800 GB/s"),
-                         "kernel": "rs_adamw_cast_tma<bf16> on one rank's local buffer",
+                         "kernel": "staged_stream<AdamOp<bf16>> on one rank's local buffer",
                          "algorithmic_bytes_per_launch": fused_launch, "traffic": None},
             "e2e": None, "gpu_launches": launches, "clocks": clk, "cpu_baseline": None,
         }))
@@ -685,6 +716,7 @@ def run_ckpt(args):
     torch.cuda.set_device(0)
     import __graft_entry__
     __graft_entry__.build()
+    _apply_stages(args)
     import sharded_optimizer_step_gb300 as ss
     from sharded_optimizer_step_gb300 import checkpoint as ck
     from sharded_optimizer_step_gb300.engine import RankShardOptimizer
@@ -703,6 +735,12 @@ def run_ckpt(args):
     directory = tempfile.mkdtemp(prefix="shst_ckpt_")
     saves, loads = [], []
     try:
+        # the first save and load also pin each optimizer's host staging
+        t0 = time.perf_counter()
+        ck.save(directory, old)
+        t1 = time.perf_counter()
+        ck.load(directory, new)
+        first = (t1 - t0, time.perf_counter() - t1)
         for _ in range(max(1, args.steps)):
             t0 = time.perf_counter()
             ck.save(directory, old)
@@ -725,13 +763,402 @@ def run_ckpt(args):
                                         "directory": "a temporary directory under /tmp"},
         "save_gbs": round(state_bytes / sv / 1e9, 2), "load_gbs": round(state_bytes / ld / 1e9, 2),
         "save_s": round(sv, 3), "load_s": round(ld, 3),
+        "first_save_s": round(first[0], 3), "first_load_s": round(first[1], 3),
+        "staging": "pinned host buffers per optimizer, pinned by the first save / load "
+                   "(untimed, reported as first_*) and reused",
         "roofline": None, "e2e": None, "gpu_launches": 0, "clocks": None, "cpu_baseline": None,
         "note": "host-IO bound (device <-> pinned host copies and file reads / writes); "
                 "no GPU kernel runs"}))
 
 
+# ------------------------------------------- micro-batch accumulation (fp32)
+
+ACCUM_WORKLOAD = "llama_1b_rank0_nd8_m4"
+
+
+def _timed_loop(torch, stream, args, one_step, n_events):
+    """Warm-up, then args.steps timed steps with n_events CUDA events each;
+    returns (total ms, per-step event lists, clocks, launches)."""
+    import sharded_optimizer_step_gb300 as ss
+    clocks = ClockSampler(smi_index(torch.cuda.current_device()))
+    clocks.start()
+    for _ in range(args.warmup):
+        one_step(None)
+    torch.cuda.synchronize()
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(n_events)]
+              for _ in range(args.steps)]
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    launches0 = ss.launch_count()
+    torch.cuda.nvtx.range_push("timed_region")
+    a.record(stream)
+    for k in range(args.steps):
+        one_step(events[k])
+    b.record(stream)
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
+    launches = ss.launch_count() - launches0
+    clk = clocks.stop()
+    if ss.device_status():
+        raise RuntimeError("a TMA-staged wait ran out during the timed steps")
+    return a.elapsed_time(b), events, clk, launches
+
+
+def _avg_ms(events, i, j):
+    return sum(e[i].elapsed_time(e[j]) for e in events) / len(events)
+
+
+def _traffic(workload_name, elements, args):
+    """ncu DRAM bytes of one launch of the line's dominant kernel, scaled from
+    the profile's bytes per element (None for smaller cases, other kernel
+    choices or a kernel changed since the capture)."""
+    per = profiled_traffic(workload_name)
+    if per is None or args.layers or args.kernel_path != "auto" or args.tma_stages:
+        return None
+    return round(per * elements)
+
+
+def _roofline(achieved, kernel, bytes_per_launch, traffic=None):
+    peak, kind = measured_peak()
+    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "peak_source": ("measured: MEASURED_PEAKS.json hbm_gbs (copy, burst)"
+                            if kind == "measured" else "fallback 6800 GB/s"),
+            "kernel": kernel, "algorithmic_bytes_per_launch": bytes_per_launch,
+            "traffic": traffic}
+
+
+def _accum_oracle_sample(w, n, t):
+    """Oracle time of a contiguous sample of n shard elements of one rank's
+    view: M micro-batch accumulations of the N_d contributions, then the
+    fused step on the fp32 accumulators."""
+    import numpy as np
+    import oracle
+    from oracle.numerics import AdamWConfig
+    from synth import workloads as W
+    idx = np.arange(1_000_000, 1_000_000 + n, dtype=np.int64)
+    micro = [[W.host_gather_rank_grad(w, 1, 0, q, j, idx) for j in range(w.micro)]
+             for q in range(w.nd)]
+    p = W.host_gather_rank_master(w, 0, idx)
+    hp = AdamWConfig(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
+    m = np.zeros(n, np.float32)
+    v = np.zeros(n, np.float32)
+    t0 = time.perf_counter()
+    accs = [oracle.grad_accumulate(micro[q], np.float32(1.0 / w.micro)) for q in range(w.nd)]
+    oracle.fsdp_shard_step(accs, 0, n, p, m, v, hp, t)
+    dt = time.perf_counter() - t0
+    return dt, (6 + 10 * (w.micro - 1)) * w.nd * n + (4 * w.nd + 26) * n
+
+
+def run_accum(args):
+    """One rank's view of the Llama-style 1B model (17 units, N_d = 8) with
+    M = 4 micro-batches: every one of the 8 contributions to this rank's
+    shard is accumulated in fp32 over the 4 bf16 micro-batch gradients
+    (acc = g*(1/M), then acc += g*(1/M); one launch per micro-batch over the
+    8 contributions side by side), then one fused step reads the 8 fp32
+    accumulators, then one layer unit is all-gathered.  The accumulate work
+    per step equals a real rank's (N_d shard slices = one full gradient)."""
+    if args.impl == "reference":
+        return _accum_reference(args)
+    import torch
+    torch.cuda.set_device(0)
+    import __graft_entry__
+    __graft_entry__.build()
+    _apply_stages(args)
+    import sharded_optimizer_step_gb300 as ss
+    import synth
+    from sharded_optimizer_step_gb300.engine import RankShardOptimizer
+    from synth import workloads as W
+    w = W.llama_1b()
+    if args.layers:
+        w.units = w.units[:args.layers]      # smaller case: the first N layer units
+    nd, M, r = w.nd, w.micro, 0
+    dev = torch.device("cuda", 0)
+    hp = ss.AdamW(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
+    opt = RankShardOptimizer(w.units, nd, r, hp, device=dev, grad_dtype=torch.float32)
+    S = opt.shard_total
+    acc = torch.empty(nd * S, dtype=torch.float32, device=dev)
+    opt.grad_in = [acc[q * S:(q + 1) * S] for q in range(nd)]
+    micro = [torch.empty(nd * S, dtype=torch.bfloat16, device=dev) for _ in range(M)]
+    for j in range(M):
+        for q in range(nd):
+            W.dev_fill_rank_grad(w, 1, r, q, j, micro[j][q * S:(q + 1) * S])
+    W.dev_fill_rank_master(w, r, opt.master)
+    u = 0
+    Su, Pu = w.unit_shard(u), w.unit_padded(u)
+    peers = [torch.empty(Su, dtype=torch.bfloat16, device=dev) for _ in range(nd)]
+    for q in range(1, nd):
+        synth.dev_fill(w.peer_shard_stream(1, q, u), peers[q])
+    full = torch.empty(Pu, dtype=torch.bfloat16, device=dev)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+    inv_m = float(1.0 / M)
+    acc_bytes = (6 + 10 * (M - 1)) * nd * S
+    fused_bytes = (4 * nd + 26) * S
+    ag_bytes = 4 * Pu
+    step_bytes = acc_bytes + fused_bytes + ag_bytes
+
+    def one_step(ev):
+        if ev is not None:
+            ev[0].record(stream)
+        for j in range(M):
+            ss.fsdp_grad_accumulate(micro[j], acc, inv_m, j == 0, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        opt.step(stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+        opt.gather_unit(u, peers, full, stream=stream)
+        if ev is not None:
+            ev[3].record(stream)
+
+    total_ms, events, clk, launches = _timed_loop(torch, stream, args, one_step, 4)
+    acc_ms, fused_ms, ag_ms = _avg_ms(events, 0, 1), _avg_ms(events, 1, 2), _avg_ms(events, 2, 3)
+    ms = total_ms / args.steps
+    acc_gbs = acc_bytes / (acc_ms / 1e3) / 1e9
+    fused_gbs = fused_bytes / (fused_ms / 1e3) / 1e9
+    cpu = None
+    if not args.no_cpu:
+        n, tt, tb, reps = 1_000_000, 0.0, 0, 0
+        while tt < args.cpu_seconds and reps < 20:
+            dt, b = _accum_oracle_sample(w, n, reps + 1)
+            tt, tb, reps = tt + dt, tb + b, reps + 1
+        cpu = {"value": round(tb / tt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"{reps} x (accumulate 4 micro-batches of 8 contributions + fused "
+                         f"step) on {n} contiguous shard elements, numpy single-threaded"}
+    print(json.dumps({
+        "metric": "micro-batch accumulate + fused fp32-accumulator step HBM GB/s, "
+                  "Llama-1B rank view, N_d=8, M=4",
+        "value": round(step_bytes / (ms / 1e3) / 1e9, 1), "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded counter-based generator on the device; no data set or weights)",
+        "config": {"workload": ACCUM_WORKLOAD + (f"_first{args.layers}layers" if args.layers
+                                                 else ""),
+                   "tma_stages": _stages_name(args),
+                   "model_shape": f"Llama-style 1B, {len(w.units)} FSDP units",
+                   "psi": w.psi, "nd": nd, "micro_batches": M, "rank": r, "shard_elements": S,
+                   "grad_dtype": "bf16 micro-batch gradients, fp32 accumulators",
+                   "step": "4 accumulate launches over the 8 contributions (first writes, "
+                           "then read-add-write), fused rs_avg+AdamW+bf16 cast on the fp32 "
+                           "accumulators (1 launch), all-gather of one layer unit (1 launch)",
+                   "bytes_per_step": step_bytes,
+                   "l2": f"no flush: each step streams {step_bytes / 1e9:.1f} GB vs a 129 MB L2"},
+        "params_per_s": round(S / (ms / 1e3), 1),
+        "kernels": {"accumulate_ms": round(acc_ms, 4), "accumulate_gbs": round(acc_gbs, 1),
+                    "fused_ms": round(fused_ms, 4), "fused_gbs": round(fused_gbs, 1),
+                    "fused_frac": round(fused_gbs / measured_peak()[0], 4),
+                    "ag_ms": round(ag_ms, 4),
+                    "ag_gbs": round(ag_bytes / (ag_ms / 1e3) / 1e9, 1)},
+        "roofline": _roofline(acc_gbs, f"staged_stream<AccumOp> (4 launches over {nd} x {S} elements)",
+                              acc_bytes // M, _traffic(ACCUM_WORKLOAD, nd * S, args)),
+        "e2e": None, "e2e_note": "device-resident micro-batch gradients; the end-to-end "
+                                 "line is the default workload's",
+        "gpu_launches": launches, "clocks": clk, "cpu_baseline": cpu}))
+
+
+def _accum_reference(args):
+    from synth import workloads as W
+    w = W.llama_1b()
+    n = 500_000
+    for k in range(args.warmup):
+        _accum_oracle_sample(w, n, k + 1)
+    ts, bs = [], []
+    for k in range(args.steps):
+        dt, b = _accum_oracle_sample(w, n, args.warmup + k + 1)
+        ts.append(dt)
+        bs.append(b)
+    value = round(sum(bs) / sum(ts) / 1e9, 4)
+    print(json.dumps({
+        "impl": "reference", "metric": "micro-batch accumulate + fused fp32-accumulator step "
+                                       "HBM GB/s, Llama-1B rank view, N_d=8, M=4",
+        "value": value, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(1e3 * sum(ts) / len(ts), 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": {"workload": ACCUM_WORKLOAD, "sample_elements_per_step": n},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"each step: {n} contiguous shard elements"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0}}))
+
+
+# ------------------------------------------------- DDP buckets + full AdamW
+
+DDP_WORKLOAD = "ddp_nd8_buckets"
+
+
+def _ddp_oracle_sample(w, numels, n_params, t):
+    """Oracle time of the DDP step on the first n_params parameters (whole
+    parameters, one bucket each at the default cap's plan order)."""
+    import numpy as np
+    import oracle
+    import synth
+    from oracle.numerics import AdamWConfig
+    sel = numels[:n_params]
+    total = sum(sel)
+    grads = [np.concatenate([synth.host_fill(w.grad_stream(1, q, 0, i), 0, n, "bf16")
+                             for i, n in enumerate(sel)]) for q in range(w.nd)]
+    p = synth.host_fill(w.master_stream(0), 0, total, "f32")
+    z = np.zeros(total, np.float32)
+    hp = AdamWConfig(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
+    bounds = [0]
+    for n in sel:
+        bounds.append(bounds[-1] + n)
+    t0 = time.perf_counter()
+    oracle.ddp_step(grads, bounds, p, z, z.copy(), hp, t)
+    return time.perf_counter() - t0, (2 * w.nd + 2) * total + 28 * total, total
+
+
+def run_ddp(args):
+    """Replicated DDP on 8 emulated ranks: 80 blocks' worth of parameters
+    (Psi = 351,035,392 bf16) bucketed in reverse registration order at a
+    25 MiB cap; each bucket's 8 rank gradients are averaged (fp32 sum in rank
+    order, bf16 out; one launch per bucket), then one full AdamW + bf16 cast
+    over all Psi parameters.  The caps 1, 4, 64 and 256 MiB are timed too
+    (all-reduce only)."""
+    from synth import workloads as W
+    w = W.ddp_sweep()
+    numels = w.unit_numels(0)
+    if args.layers:
+        numels = numels[:5 * args.layers]    # smaller case: the first N blocks' parameters
+    if args.impl == "reference":
+        n_params = 4
+        ts, bs = [], []
+        for k in range(args.warmup + args.steps):
+            dt, b, total = _ddp_oracle_sample(w, numels, n_params, k + 1)
+            if k >= args.warmup:
+                ts.append(dt)
+                bs.append(b)
+        value = round(sum(bs) / sum(ts) / 1e9, 4)
+        print(json.dumps({
+            "impl": "reference", "metric": "DDP bucket all-reduce avg + full AdamW HBM GB/s, "
+                                           "Psi=351M, N_d=8, 25 MiB buckets",
+            "value": value, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(1e3 * sum(ts) / len(ts), 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "config": {"workload": DDP_WORKLOAD,
+                                            "sample_params": n_params, "sample_elements": total},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"the first {n_params} parameters ({total} elements)"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}))
+        return
+    import torch
+    torch.cuda.set_device(0)
+    import __graft_entry__
+    __graft_entry__.build()
+    _apply_stages(args)
+    import sharded_optimizer_step_gb300 as ss
+    import synth
+    nd = w.nd
+    total = sum(numels)
+    dev = torch.device("cuda", 0)
+    grads = [torch.empty(total, dtype=torch.bfloat16, device=dev) for _ in range(nd)]
+    hp = ss.AdamW(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
+    plans = {}
+    for mib in w.extra["caps_mib"]:
+        plans[mib] = ss.ddp_bucket_plan(numels, 2, mib << 20)
+    off, _, boff = plans[25]
+    for q in range(nd):
+        for i, n in enumerate(numels):
+            synth.dev_fill(w.grad_stream(1, q, 0, i), grads[q][off[i]:off[i] + n])
+    out = torch.empty(total, dtype=torch.bfloat16, device=dev)
+    master = torch.empty(total, dtype=torch.float32, device=dev)
+    synth.dev_fill(w.master_stream(0), master)
+    mm = torch.zeros(total, device=dev)
+    vv = torch.zeros(total, device=dev)
+    pb = torch.empty(total, dtype=torch.bfloat16, device=dev)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+    ar_bytes = (2 * nd + 2) * total
+    adam_bytes = 28 * total
+    step_bytes = ar_bytes + adam_bytes
+    t = [0]
+
+    def one_step(ev):
+        if ev is not None:
+            ev[0].record(stream)
+        ss.ddp_bucket_allreduce_avg(grads, boff, out, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        t[0] += 1
+        ss.fsdp_rs_avg_adamw_cast([out], master, mm, vv, pb, hp, t[0], stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+
+    total_ms, events, clk, launches = _timed_loop(torch, stream, args, one_step, 3)
+    ar_ms, adam_ms = _avg_ms(events, 0, 1), _avg_ms(events, 1, 2)
+    ms = total_ms / args.steps
+    # the other caps: all-reduce only, same gradients (the values per bucket
+    # differ in placement, not in amount of work)
+    by_cap = {}
+    for mib, (_, _, bo) in plans.items():
+        for _ in range(3):
+            ss.ddp_bucket_allreduce_avg(grads, bo, out, stream=stream)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        reps = 20
+        a.record(stream)
+        for _ in range(reps):
+            ss.ddp_bucket_allreduce_avg(grads, bo, out, stream=stream)
+        b.record(stream)
+        torch.cuda.synchronize()
+        cap_ms = a.elapsed_time(b) / reps
+        by_cap[f"{mib}MiB"] = {"buckets": len(bo) - 1, "ms": round(cap_ms, 4),
+                               "gbs": round(ar_bytes / (cap_ms / 1e3) / 1e9, 1)}
+    ar_gbs = ar_bytes / (ar_ms / 1e3) / 1e9
+    adam_gbs = adam_bytes / (adam_ms / 1e3) / 1e9
+    cpu = None
+    if not args.no_cpu:
+        tt, tb, reps, n_params = 0.0, 0, 0, 4
+        while tt < args.cpu_seconds and reps < 20:
+            dt, b, n_el = _ddp_oracle_sample(w, numels, n_params, reps + 1)
+            tt, tb, reps = tt + dt, tb + b, reps + 1
+        cpu = {"value": round(tb / tt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"{reps} x the DDP step on the first {n_params} parameters "
+                         f"({n_el} elements), numpy single-threaded"}
+    print(json.dumps({
+        "metric": "DDP bucket all-reduce avg + full AdamW HBM GB/s, Psi=351M, N_d=8, "
+                  "25 MiB buckets",
+        "value": round(step_bytes / (ms / 1e3) / 1e9, 1), "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded counter-based generator on the device; no data set or weights)",
+        "config": {"workload": DDP_WORKLOAD + (f"_first{args.layers}blocks" if args.layers
+                                               else ""),
+                   "tma_stages": _stages_name(args),
+                   "psi": total, "nd": nd, "cap_mib": 25,
+                   "buckets": len(boff) - 1,
+                   "step": "one all-reduce-avg launch per bucket (8 bf16 rank gradients -> "
+                           "bf16 mean), then fused AdamW + bf16 cast over all parameters "
+                           "(1 launch, N_d = 1)",
+                   "bytes_per_step": step_bytes,
+                   "l2": f"no flush: each step streams {step_bytes / 1e9:.1f} GB vs a 129 MB L2"},
+        "kernels": {"allreduce_ms": round(ar_ms, 4), "allreduce_gbs": round(ar_gbs, 1),
+                    "allreduce_frac": round(ar_gbs / measured_peak()[0], 4),
+                    "adamw_ms": round(adam_ms, 4), "adamw_gbs": round(adam_gbs, 1),
+                    "allreduce_by_cap": by_cap},
+        "roofline": _roofline(adam_gbs, ("staged_stream<AdamOp<bf16>> at N_d = 1 (full AdamW)"
+                                         if args.kernel_path == "tma" else
+                                         "rs_adamw_cast_vec4<1, bf16> (register-staged full "
+                                         "AdamW; the TMA-staged kernel is slower at N_d = 1)"),
+                              adam_bytes, _traffic(DDP_WORKLOAD, total, args)),
+        "roofline_allreduce": _roofline(ar_gbs, f"staged_stream<MeanOutOp> at N_d = 8 ({len(boff) - 1} "
+                                                f"launches, one per bucket)", ar_bytes),
+        "e2e": None, "e2e_note": "device-resident gradients; the end-to-end line is the "
+                                 "default workload's",
+        "gpu_launches": launches, "clocks": clk, "cpu_baseline": cpu}))
+
+
 def main():
     args = parse()
+    if args.workload == ACCUM_WORKLOAD:
+        run_accum(args)
+        return
+    if args.workload == DDP_WORKLOAD:
+        run_ddp(args)
+        return
     if args.workload == CKPT_WORKLOAD:
         run_ckpt(args)
         return

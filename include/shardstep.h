@@ -467,14 +467,29 @@ int fsdp_reshard_plan(int64_t total, int32_t old_nd, int32_t new_nd, int32_t new
 
 /* ------------------------------------------------------------ misc */
 
-/* Selects the kernels fsdp_rs_avg_adamw_cast may use, process-wide.
- * SHARDSTEP_PATH_AUTO (default) and _TMA use the TMA-staged kernel whenever
- * the arguments allow it; _REGISTER uses only the register-staged kernels.
- * Returns the previous setting, or INVALID for an unknown value. */
+/* Selects the kernels the streaming calls may use, process-wide: the fused
+ * steps (plain, hybrid, scaled), fsdp_grad_accumulate,
+ * ddp_bucket_allreduce_avg and fsdp_grad_unscale_check.
+ * SHARDSTEP_PATH_TMA uses the TMA-staged kernels whenever the arguments
+ * allow it (every source 16-byte aligned, at least 4096 elements, two stages
+ * in shared memory); _REGISTER uses only the register-staged kernels;
+ * _AUTO (default) uses the TMA-staged kernels where they measured faster:
+ * the fused steps at N_d >= 3, the bucket all-reduce at N_d >= 3 on buckets
+ * of at least 8M elements, the accumulation and the check always.  All give
+ * bit-identical results.  Returns the previous setting, or INVALID for an
+ * unknown value. */
 #define SHARDSTEP_PATH_AUTO 0
 #define SHARDSTEP_PATH_REGISTER 1
 #define SHARDSTEP_PATH_TMA 2
 int32_t shardstep_set_fused_path(int32_t path);
+
+/* Sets the shared-memory stages of each TMA-staged launch, process-wide:
+ * 0 (default) = enough stages for about 128 KB of tiles in flight per SM
+ * (at least 2, at most 16); 2..16 = that many, or as many as fit if fewer,
+ * rounded down to one of the instantiated counts 2, 3, 4, 6, 8, 12, 16.
+ * A tuning control only: results do not depend on it.  Returns the previous
+ * setting, or INVALID for other values. */
+int32_t shardstep_set_tma_stages(int32_t stages);
 
 /* Watchdog word of the current device: bit 0 = a consumer's wait for a
  * staged tile ran out, bit 1 = the producer's wait for a free stage ran out

@@ -432,7 +432,8 @@ def comm_bytes(psi: float, nd: int, kind: str, exact: bool = False) -> float:
 
 
 def set_fused_path(path: str) -> str:
-    """Which kernels the fused step may use: "auto" (TMA-staged when the
+    """Which kernels the streaming calls (fused steps, accumulation, bucket
+    all-reduce, non-finite check) may use: "auto" (TMA-staged when the
     arguments allow), "register" (register-staged only) or "tma".  Returns
     the previous setting."""
     codes = {"auto": _capi.PATH_AUTO, "register": _capi.PATH_REGISTER, "tma": _capi.PATH_TMA}
@@ -441,6 +442,16 @@ def set_fused_path(path: str) -> str:
     if prev < 0:
         _capi.check("shardstep_set_fused_path", prev)
     return names[prev]
+
+
+def set_tma_stages(stages: int) -> int:
+    """Shared-memory stages of each TMA-staged launch (0: about 128 KB of
+    tiles in flight per SM; else 2..16, limited to what fits).  Tuning only;
+    returns the previous setting."""
+    prev = _capi.lib().shardstep_set_tma_stages(int(stages))
+    if prev < 0:
+        _capi.check("shardstep_set_tma_stages", prev)
+    return prev
 
 
 def device_status(clear: bool = False) -> int:

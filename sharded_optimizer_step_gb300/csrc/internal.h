@@ -71,13 +71,26 @@ cudaError_t launch_rs_adamw_cast(const PtrTable& tab, int nd, int grad_type, int
                                  float* master, float* m, float* v, uint16_t* out,
                                  const AdamScalars& c, const MeanOp& mo,
                                  const unsigned int* skip, bool vec, cudaStream_t stream);
-// TMA-staged fused step (step_tma.cu): dynamic shared memory it needs, the
-// launch, and the device watchdog status word.
-size_t tma_step_smem_bytes(int nd, int grad_type);
+// TMA-staged kernels (step_tma.cu).  Each needs every source 16-byte aligned,
+// at least kTmaMinElements elements and two stages in shared memory (the
+// *_fits checks: the fused step's stage holds N_d slices + 3 state arrays,
+// the all-reduce's and the check's N_d slices).  set_tma_stage_limit fixes
+// the stages per launch (0: about 128 KB of tiles in flight per SM; returns
+// the previous setting).
+bool tma_step_fits(int nd, int grad_type);
+bool tma_reduce_fits(int nd, int grad_type);
+int set_tma_stage_limit(int stages);
 cudaError_t launch_rs_adamw_cast_tma(const PtrTable& tab, int nd, int grad_type, int64_t S,
                                      float* master, float* m, float* v, uint16_t* out,
                                      const AdamScalars& c, const MeanOp& mo,
                                      const unsigned int* skip, cudaStream_t stream);
+cudaError_t launch_accumulate_tma(const uint16_t* g, float* acc, int64_t n, float scale,
+                                  bool first, cudaStream_t stream);
+cudaError_t launch_allreduce_avg_tma(const PtrTable& tab, int nd, int64_t n, uint16_t* out,
+                                     const MeanOp& mo, cudaStream_t stream);
+cudaError_t launch_nonfinite_check_tma(const PtrTable& tab, int nd, int grad_type, int64_t S,
+                                       const MeanOp& mo, unsigned int* found,
+                                       cudaStream_t stream);
 // Gradient scaler (step.cu): the non-finite check of the unscaled mean and
 // the scale update.
 cudaError_t launch_nonfinite_check(const PtrTable& tab, int nd, int grad_type, int64_t S,

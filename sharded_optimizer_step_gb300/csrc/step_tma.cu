@@ -1,26 +1,29 @@
-// The fused sharded step with TMA bulk staging (the default path when every
-// pointer is 16-byte aligned and the stages fit in shared memory).
+// TMA bulk-staged streaming kernels: the fused sharded step (reduce-scatter
+// average + AdamW + bf16 cast), the micro-batch gradient accumulation, the
+// DDP bucket all-reduce average and the gradient scaler's non-finite check.
+// They are the default path whenever every source is 16-byte aligned and at
+// least two stages fit in shared memory.
 //
-// One CTA per SM, 17 warps.  Warp 16's first lane is the producer: for each
-// tile of 2048 shard elements it issues one cp.async.bulk per gradient slice
-// and per state array (master, m, v) from HBM into a shared-memory stage and
-// completes them on that stage's mbarrier (expect-tx).  Warps 0..15 consume:
-// they wait on the stage's barrier, reduce the N_d slices in rank order from
-// shared memory, run AdamW, and write master / m / v and the bf16 parameter
-// straight to HBM with streaming stores; each warp then arrives on the
-// stage's "empty" barrier so the producer can refill it.  The slices are
-// summed in the order GroupSum fixes (rank order, grouped for hybrid
-// sharding).  Two stages of
-// 2048 x (N_d x grad bytes + 12) bytes are in flight per SM (114 KB at N_d =
-// 8, bf16).  Tiles are dealt round-robin over the grid.  Measured on GB300
-// against the register-staged kernel (4 elements / thread, 512-thread
-// blocks) on the same GPU: 4.98 ms vs 5.43 ms for an 842M-element shard at
-// N_d = 8.
+// One skeleton serves all four.  One CTA per SM, 17 warps.  Warp 16's first
+// lane is the producer: for each tile of 2048 elements it issues one
+// cp.async.bulk per input array (a gradient slice, a state array, an
+// accumulator) from HBM into a shared-memory stage and completes them on that
+// stage's mbarrier (expect-tx).  Warps 0..15 consume: they wait on the
+// stage's barrier, compute on 4 elements per thread from shared memory and
+// write the results straight to HBM with streaming stores, then each warp
+// arrives on the stage's "empty" barrier so the producer can refill it.
+// Tiles are dealt round-robin over the grid.  The number of stages is chosen
+// per launch so that about 128 KB of tiles are in flight per SM (2 stages of
+// 57 KB for the fused step at N_d = 8 and bf16, 4 of 28 KB at N_d = 1, 8
+// of 12 KB for an accumulation), at least 2 and at most 16, rounded down to
+// one of the instantiated counts 2, 3, 4, 6, 8, 12, 16.
 //
 // Every wait is bounded (about two seconds of %globaltimer).  A wait that
 // runs out sets a bit in the device status word (shardstep_device_status),
 // the producer then waits, again bounded, for the copies it already issued,
 // and the CTA returns.  Nothing here spins on another CTA or on the host.
+#include <atomic>
+
 #include "common.cuh"
 
 namespace shardstep {
@@ -31,11 +34,19 @@ __device__ unsigned int g_device_status = 0;
 namespace {
 
 constexpr int kTile = 2048;
-constexpr int kStages = 2;
+constexpr int kMaxStages = 16;
+// Reads kept in flight per SM: the stage count is chosen so that about this
+// many bytes of tiles are staged (at least 2 stages).  Measured on GB300 for
+// the fused step at N_d = 8 (57 KB stages), N_d = 1 (28 KB), the bucket
+// all-reduce (32 KB) and the accumulation (12 KB): each is fastest at 100 to
+// 130 KB per SM; filling all 227 KB of shared memory is slower (5.51 vs
+// 5.15 ms for the N_d = 8 step over 842M elements).
+constexpr size_t kTargetInflight = 128 * 1024;
 constexpr int kConsumerWarps = 16;
 constexpr int kConsumers = kConsumerWarps * 32;   // 512: 4 elements each per tile
 constexpr int kTmaThreads = kConsumers + 32;      // + the producer warp
 constexpr unsigned long long kWaitNs = 2000000000ull;
+constexpr size_t kBarrierBytes = 2 * kMaxStages * sizeof(uint64_t);
 
 constexpr unsigned kStatusConsumerTimeout = 1u;
 constexpr unsigned kStatusProducerTimeout = 2u;
@@ -86,6 +97,7 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
         : "memory");
 }
 
+// 4 consecutive gradient elements of type GT from shared memory, as fp32.
 template <int GT>
 __device__ __forceinline__ void load4_smem(const uint8_t* p, float* f) {
     if (GT == kGradF32) {
@@ -111,30 +123,88 @@ __device__ __forceinline__ float grad1(const void* base, int64_t j) {
     return bf16_to_f32(static_cast<const uint16_t*>(base)[j]);
 }
 
-// S_main = S rounded down to a multiple of 8 is covered by tiles (the last
-// one possibly shorter, still a multiple of 8 elements, so every bulk copy is
-// a multiple of 16 bytes); the final S - S_main < 8 elements are done by
-// block 0 with ordinary loads.
 template <int GT>
-__global__ void __launch_bounds__(kTmaThreads, 1)
-    rs_adamw_cast_tma(PtrTable tab, int nd, int64_t S, float* __restrict__ P,
-                      float* __restrict__ M, float* __restrict__ V, uint16_t* __restrict__ out,
-                      AdamScalars c, MeanOp mo, const unsigned int* skip) {
-    // a skipped step (gradient scaler found inf/NaN): every thread returns
-    // before any barrier or copy exists
-    if (skip_step(skip)) return;
-    mo = resolve_scale(mo);
-    constexpr uint32_t gsz = GT == kGradF32 ? 4 : 2;
-    const uint32_t slice_bytes = kTile * gsz;
-    const uint32_t stage_bytes = nd * slice_bytes + 3 * kTile * 4;
+__host__ __device__ constexpr uint32_t grad_bytes() {
+    return GT == kGradF32 ? 4u : 2u;
+}
+
+// The N_d slices of one tile reduced at 4 consecutive elements, in the order
+// GroupSum fixes (rank order; grouped for hybrid sharding), from a stage that
+// holds the slices back to back (kTile elements each).
+template <int GT>
+__device__ __forceinline__ void reduce4_smem(const uint8_t* st, int nd, int group, int e,
+                                             float* g) {
+    constexpr uint32_t gsz = grad_bytes<GT>();
+    GroupSum<4> acc;
+    {
+        float t[4];
+        load4_smem<GT>(st + e * gsz, t);
+        acc.first(t);
+    }
+    for (int q = 1; q < nd; ++q) {
+        float t[4];
+        load4_smem<GT>(st + q * (kTile * gsz) + e * gsz, t);
+        acc.add(t, group);
+    }
+    acc.result(g);
+}
+
+// The same sum at one element, read from global memory (the < 8 tail).
+template <int GT>
+__device__ __forceinline__ float reduce1_global(const PtrTable& tab, int nd, int group,
+                                                int64_t j) {
+    GroupSum<1> acc;
+    float t = grad1<GT>(tab.p[0], j);
+    acc.first(&t);
+    for (int q = 1; q < nd; ++q) {
+        t = grad1<GT>(tab.p[q], j);
+        acc.add(&t, group);
+    }
+    float s;
+    acc.result(&s);
+    return s;
+}
+
+__device__ __forceinline__ bool not_finite(float x) {
+    return (__float_as_uint(x) & 0x7F800000u) == 0x7F800000u;
+}
+
+// ------------------------------------------------------------ the skeleton
+//
+// An Op (passed by value as the kernel parameter, read-only) provides
+//   State                                  per-thread mutable state
+//   skipped()                              true: every thread returns at once
+//   init()                                 the thread's State
+//   stage_bytes()                          one stage (a multiple of 16 bytes)
+//   tx_bytes(n)                            bytes the copies of an n-element tile bring
+//   issue(stage, e0, n, bar)               the producer lane's bulk copies of a tile
+//   consume(stage, e0, e, state)           4 elements at tile offset e
+//   tail(j, state)                         element j past the tiles, global loads
+//   finish(state, lane)                    whole consumer warps, after the loop
+//
+// n_main = n rounded down to a multiple of 8 is covered by tiles (the last one
+// possibly shorter, still a multiple of 8 elements, so every bulk copy is a
+// multiple of 16 bytes); the final n - n_main < 8 elements go to block 0's
+// first threads with ordinary loads.
+static_assert(kConsumers * 4 == kTile, "one group of 4 elements per consumer thread per tile");
+
+// NST, the number of stages, is a compile-time constant: with a runtime count
+// the same kernel issued 24% more instructions and ran 1.4% slower (5.15 vs
+// 5.08 ms for the N_d = 8 step over 842M elements).
+template <class Op, int NST>
+__global__ void __launch_bounds__(kTmaThreads, 1) staged_stream(const Op op, int64_t n) {
+    constexpr int nst = NST;
+    if (op.skipped()) return;
+    typename Op::State state = op.init();
+    const uint32_t stage_bytes = op.stage_bytes();
     extern __shared__ __align__(128) uint8_t smem[];
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * stage_bytes);
-    uint64_t* empty = full + kStages;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(nst) * stage_bytes);
+    uint64_t* empty = full + nst;
     const int tid = threadIdx.x;
-    const int64_t s_main = S & ~static_cast<int64_t>(7);
-    const int64_t ntiles = (s_main + kTile - 1) / kTile;
+    const int64_t n_main = n & ~static_cast<int64_t>(7);
+    const int64_t ntiles = (n_main + kTile - 1) / kTile;
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < nst; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kConsumerWarps);
         }
@@ -147,149 +217,343 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     if (tid >= kConsumers) {  // producer warp
         if (tid != kConsumers) return;
         int64_t j = 0;
+        int s = 0;
+        uint32_t use = 0;
         bool ok = true;
         for (; j < my_tiles; ++j) {
-            const int s = static_cast<int>(j % kStages);
-            const uint32_t use = static_cast<uint32_t>(j / kStages);
             if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1u)) {
                 ok = false;
                 break;
             }
             const int64_t e0 = (static_cast<int64_t>(blockIdx.x) + j * gridDim.x) * kTile;
-            const int64_t n = s_main - e0 < kTile ? s_main - e0 : kTile;
-            const uint32_t gb = static_cast<uint32_t>(n) * gsz, sb = static_cast<uint32_t>(n) * 4;
-            uint8_t* st = smem + s * stage_bytes;
-            mbar_expect_tx(&full[s], nd * gb + 3 * sb);
-            for (int q = 0; q < nd; ++q)
-                bulk_load(st + q * slice_bytes, static_cast<const uint8_t*>(tab.p[q]) + e0 * gsz,
-                          gb, &full[s]);
-            uint8_t* sst = st + nd * slice_bytes;
-            bulk_load(sst, P + e0, sb, &full[s]);
-            bulk_load(sst + kTile * 4, M + e0, sb, &full[s]);
-            bulk_load(sst + 2 * kTile * 4, V + e0, sb, &full[s]);
+            const uint32_t cnt = static_cast<uint32_t>(n_main - e0 < kTile ? n_main - e0 : kTile);
+            mbar_expect_tx(&full[s], op.tx_bytes(cnt));
+            op.issue(smem + static_cast<size_t>(s) * stage_bytes, e0, cnt, &full[s]);
+            if (++s == nst) {
+                s = 0;
+                ++use;
+            }
         }
         if (!ok) {
             atomicOr(&g_device_status, kStatusProducerTimeout);
             // the copies already issued land in this CTA's shared memory:
             // wait for them (bounded) before the CTA may exit
-            for (int64_t k = j > kStages ? j - kStages : 0; k < j; ++k)
-                mbar_wait(&full[k % kStages], static_cast<uint32_t>(k / kStages) & 1u);
+            for (int64_t k = j > nst ? j - nst : 0; k < j; ++k)
+                mbar_wait(&full[k % nst], static_cast<uint32_t>(k / nst) & 1u);
         }
         return;
     }
 
-    // consumers
+    // consumers: every lane waits (each gets the barrier's acquire), the
+    // warp takes one decision
     const int lane = tid & 31;
+    const int e = tid * 4;
+    int s = 0;
+    uint32_t use = 0;
     for (int64_t j = 0; j < my_tiles; ++j) {
-        const int s = static_cast<int>(j % kStages);
-        const uint32_t use = static_cast<uint32_t>(j / kStages);
-        if (!mbar_wait(&full[s], use & 1u)) {
-            atomicOr(&g_device_status, kStatusConsumerTimeout);
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[s], use & 1u))) {
+            if (lane == 0) atomicOr(&g_device_status, kStatusConsumerTimeout);
             return;
         }
         const int64_t e0 = (static_cast<int64_t>(blockIdx.x) + j * gridDim.x) * kTile;
-        const int64_t n = s_main - e0 < kTile ? s_main - e0 : kTile;
-        const uint8_t* st = smem + s * stage_bytes;
-        const uint8_t* sst = st + nd * slice_bytes;
-        for (int e = tid * 4; e < n; e += kConsumers * 4) {
-            GroupSum<4> acc;
-            {
-                float t[4];
-                load4_smem<GT>(st + e * gsz, t);
-                acc.first(t);
-            }
-            for (int q = 1; q < nd; ++q) {
-                float t[4];
-                load4_smem<GT>(st + q * slice_bytes + e * gsz, t);
-                acc.add(t, mo.group);
-            }
-            float g[4];
-            acc.result(g);
-            const float4 pp = *reinterpret_cast<const float4*>(sst + e * 4);
-            const float4 mm = *reinterpret_cast<const float4*>(sst + kTile * 4 + e * 4);
-            const float4 vv = *reinterpret_cast<const float4*>(sst + 2 * kTile * 4 + e * 4);
-            float p[4] = {pp.x, pp.y, pp.z, pp.w};
-            float m[4] = {mm.x, mm.y, mm.z, mm.w};
-            float v[4] = {vv.x, vv.y, vv.z, vv.w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) adamw_elem(mean_of(g[k], mo), p[k], m[k], v[k], c);
-            const int64_t ge = e0 + e;
-            stcs16(P + ge, pack4f(p));
-            stcs16(M + ge, pack4f(m));
-            stcs16(V + ge, pack4f(v));
-            stcs8(out + ge, make_uint2(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3])));
-        }
+        const int64_t cnt = n_main - e0 < kTile ? n_main - e0 : kTile;
+        if (e < cnt) op.consume(smem + static_cast<size_t>(s) * stage_bytes, e0, e, state);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
-    }
-    if (blockIdx.x == 0 && tid < S - s_main) {
-        const int64_t jx = s_main + tid;
-        GroupSum<1> acc;
-        float t = grad1<GT>(tab.p[0], jx);
-        acc.first(&t);
-        for (int q = 1; q < nd; ++q) {
-            t = grad1<GT>(tab.p[q], jx);
-            acc.add(&t, mo.group);
+        if (++s == nst) {
+            s = 0;
+            ++use;
         }
-        float sum;
-        acc.result(&sum);
-        float p = P[jx], m = M[jx], v = V[jx];
-        adamw_elem(mean_of(sum, mo), p, m, v, c);
-        P[jx] = p;
-        M[jx] = m;
-        V[jx] = v;
-        out[jx] = f32_to_bf16(p);
+    }
+    if (blockIdx.x == 0 && tid < n - n_main) op.tail(n_main + tid, state);
+    op.finish(state, lane);
+}
+
+// ------------------------------------------------------------------ ops
+
+// The fused sharded step: N_d gradient slices + master / m / v in; master /
+// m / v and the bf16 parameter out.  Stage: the slices, then the 3 state
+// arrays, kTile elements each.
+template <int GT>
+struct AdamOp {
+    PtrTable tab;
+    int nd;
+    float* P;
+    float* M;
+    float* V;
+    uint16_t* out;
+    AdamScalars c;
+    MeanOp mo;
+    const unsigned int* skip;
+
+    using State = MeanOp;
+    static constexpr uint32_t gsz = grad_bytes<GT>();
+    __device__ bool skipped() const { return skip_step(skip); }
+    __device__ State init() const { return resolve_scale(mo); }
+    __host__ __device__ uint32_t stage_bytes() const {
+        return static_cast<uint32_t>(nd) * kTile * gsz + 3u * kTile * 4u;
+    }
+    __device__ uint32_t tx_bytes(uint32_t n) const { return nd * n * gsz + 3u * n * 4u; }
+    __device__ void issue(uint8_t* st, int64_t e0, uint32_t n, uint64_t* bar) const {
+        for (int q = 0; q < nd; ++q)
+            bulk_load(st + q * (kTile * gsz), static_cast<const uint8_t*>(tab.p[q]) + e0 * gsz,
+                      n * gsz, bar);
+        uint8_t* sst = st + nd * (kTile * gsz);
+        bulk_load(sst, P + e0, n * 4, bar);
+        bulk_load(sst + kTile * 4, M + e0, n * 4, bar);
+        bulk_load(sst + 2 * kTile * 4, V + e0, n * 4, bar);
+    }
+    __device__ void consume(const uint8_t* st, int64_t e0, int e, State& m0) const {
+        float g[4];
+        reduce4_smem<GT>(st, nd, m0.group, e, g);
+        const uint8_t* sst = st + nd * (kTile * gsz);
+        const float4 pp = *reinterpret_cast<const float4*>(sst + e * 4);
+        const float4 mm = *reinterpret_cast<const float4*>(sst + kTile * 4 + e * 4);
+        const float4 vv = *reinterpret_cast<const float4*>(sst + 2 * kTile * 4 + e * 4);
+        float p[4] = {pp.x, pp.y, pp.z, pp.w};
+        float m[4] = {mm.x, mm.y, mm.z, mm.w};
+        float v[4] = {vv.x, vv.y, vv.z, vv.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) adamw_elem(mean_of(g[k], m0), p[k], m[k], v[k], c);
+        const int64_t ge = e0 + e;
+        stcs16(P + ge, pack4f(p));
+        stcs16(M + ge, pack4f(m));
+        stcs16(V + ge, pack4f(v));
+        stcs8(out + ge, make_uint2(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3])));
+    }
+    __device__ void tail(int64_t j, State& m0) const {
+        float p = P[j], m = M[j], v = V[j];
+        adamw_elem(mean_of(reduce1_global<GT>(tab, nd, m0.group, j), m0), p, m, v, c);
+        P[j] = p;
+        M[j] = m;
+        V[j] = v;
+        out[j] = f32_to_bf16(p);
+    }
+    __device__ void finish(State&, int) const {}
+};
+
+// Micro-batch accumulation: acc = g*scale (first) or acc + g*scale, one
+// rounding per operation.  Stage: the bf16 gradient tile, then (not first)
+// the fp32 accumulator tile.
+template <bool FIRST>
+struct AccumOp {
+    const uint16_t* g;
+    float* acc;
+    float scale;
+
+    struct State {};
+    __device__ bool skipped() const { return false; }
+    __device__ State init() const { return State{}; }
+    __host__ __device__ uint32_t stage_bytes() const {
+        return kTile * 2u + (FIRST ? 0u : kTile * 4u);
+    }
+    __device__ uint32_t tx_bytes(uint32_t n) const { return n * 2u + (FIRST ? 0u : n * 4u); }
+    __device__ void issue(uint8_t* st, int64_t e0, uint32_t n, uint64_t* bar) const {
+        bulk_load(st, g + e0, n * 2, bar);
+        if (!FIRST) bulk_load(st + kTile * 2, acc + e0, n * 4, bar);
+    }
+    __device__ void consume(const uint8_t* st, int64_t e0, int e, State&) const {
+        float f[4], a[4];
+        load4_smem<kGradBF16>(st + e * 2, f);
+        if (!FIRST) {
+            const float4 x = *reinterpret_cast<const float4*>(st + kTile * 2 + e * 4);
+            a[0] = x.x; a[1] = x.y; a[2] = x.z; a[3] = x.w;
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float t = __fmul_rn(f[k], scale);
+            a[k] = FIRST ? t : __fadd_rn(a[k], t);
+        }
+        stcs16(acc + e0 + e, pack4f(a));
+    }
+    __device__ void tail(int64_t j, State&) const {
+        const float t = __fmul_rn(bf16_to_f32(g[j]), scale);
+        acc[j] = FIRST ? t : __fadd_rn(acc[j], t);
+    }
+    __device__ void finish(State&, int) const {}
+};
+
+// DDP bucket all-reduce average: N_d bf16 slices in, the bf16 mean out.
+struct MeanOutOp {
+    PtrTable tab;
+    int nd;
+    uint16_t* out;
+    MeanOp mo;
+
+    using State = MeanOp;
+    __device__ bool skipped() const { return false; }
+    __device__ State init() const { return mo; }
+    __host__ __device__ uint32_t stage_bytes() const {
+        return static_cast<uint32_t>(nd) * kTile * 2u;
+    }
+    __device__ uint32_t tx_bytes(uint32_t n) const { return nd * n * 2u; }
+    __device__ void issue(uint8_t* st, int64_t e0, uint32_t n, uint64_t* bar) const {
+        for (int q = 0; q < nd; ++q)
+            bulk_load(st + q * (kTile * 2), static_cast<const uint16_t*>(tab.p[q]) + e0, n * 2,
+                      bar);
+    }
+    __device__ void consume(const uint8_t* st, int64_t e0, int e, State& m0) const {
+        float g[4];
+        reduce4_smem<kGradBF16>(st, nd, m0.group, e, g);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) g[k] = mean_of(g[k], m0);
+        stcs8(out + e0 + e, make_uint2(pack_bf16x2(g[0], g[1]), pack_bf16x2(g[2], g[3])));
+    }
+    __device__ void tail(int64_t j, State& m0) const {
+        out[j] = f32_to_bf16(mean_of(reduce1_global<kGradBF16>(tab, nd, m0.group, j), m0));
+    }
+    __device__ void finish(State&, int) const {}
+};
+
+// Gradient scaler's check: sets *found when any unscaled mean gradient is
+// inf or NaN.  Reads the slices only; one atomic per warp that saw one.
+template <int GT>
+struct CheckOp {
+    PtrTable tab;
+    int nd;
+    MeanOp mo;
+    unsigned int* found;
+
+    struct State {
+        MeanOp mo;
+        bool bad;
+    };
+    static constexpr uint32_t gsz = grad_bytes<GT>();
+    __device__ bool skipped() const { return false; }
+    __device__ State init() const { return State{resolve_scale(mo), false}; }
+    __host__ __device__ uint32_t stage_bytes() const {
+        return static_cast<uint32_t>(nd) * kTile * gsz;
+    }
+    __device__ uint32_t tx_bytes(uint32_t n) const { return nd * n * gsz; }
+    __device__ void issue(uint8_t* st, int64_t e0, uint32_t n, uint64_t* bar) const {
+        for (int q = 0; q < nd; ++q)
+            bulk_load(st + q * (kTile * gsz), static_cast<const uint8_t*>(tab.p[q]) + e0 * gsz,
+                      n * gsz, bar);
+    }
+    __device__ void consume(const uint8_t* st, int64_t, int e, State& s) const {
+        float g[4];
+        reduce4_smem<GT>(st, nd, s.mo.group, e, g);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) s.bad |= not_finite(mean_of(g[k], s.mo));
+    }
+    __device__ void tail(int64_t j, State& s) const {
+        s.bad |= not_finite(mean_of(reduce1_global<GT>(tab, nd, s.mo.group, j), s.mo));
+    }
+    __device__ void finish(State& s, int lane) const {
+        if (__any_sync(0xFFFFFFFFu, s.bad) && lane == 0) atomicOr(found, 1u);
+    }
+};
+
+// --------------------------------------------------------------- launch
+
+std::atomic<int> g_stage_limit{0};  // 0: about kTargetInflight bytes of stages
+
+// The stage counts instantiated; a launch takes the largest one not above
+// what it asks for.
+constexpr int kStageSet[] = {2, 3, 4, 6, 8, 12, 16};
+
+int stages_for(size_t stage_bytes) {
+    const size_t optin = static_cast<size_t>(device_smem_optin());
+    size_t fit = optin > kBarrierBytes ? (optin - kBarrierBytes) / stage_bytes : 0;
+    if (fit > static_cast<size_t>(kMaxStages)) fit = kMaxStages;
+    const int lim = g_stage_limit.load(std::memory_order_relaxed);
+    size_t want = lim >= 2 ? static_cast<size_t>(lim) : kTargetInflight / stage_bytes;
+    if (want > fit) want = fit;
+    int nst = 2;
+    for (int k : kStageSet)
+        if (static_cast<size_t>(k) <= want) nst = k;
+    return nst;
+}
+
+template <class Op, int NST>
+cudaError_t launch_stages(const Op& op, int64_t n, cudaStream_t stream) {
+    static int attr_set[256];  // per instantiation: dynamic shared memory opt-in applied
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 256 && !attr_set[dev]) {
+        e = cudaFuncSetAttribute(staged_stream<Op, NST>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, device_smem_optin());
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = 1;
+    }
+    const size_t smem = static_cast<size_t>(NST) * op.stage_bytes() + kBarrierBytes;
+    const int64_t ntiles = ((n & ~static_cast<int64_t>(7)) + kTile - 1) / kTile;
+    int64_t grid = device_sms();
+    if (grid > ntiles) grid = ntiles;
+    if (grid < 1) grid = 1;
+    staged_stream<Op, NST><<<static_cast<unsigned>(grid), kTmaThreads, smem, stream>>>(op, n);
+    note_launch();
+    return cudaGetLastError();
+}
+
+template <class Op>
+cudaError_t launch_staged(const Op& op, int64_t n, cudaStream_t stream) {
+    switch (stages_for(op.stage_bytes())) {
+        case 3: return launch_stages<Op, 3>(op, n, stream);
+        case 4: return launch_stages<Op, 4>(op, n, stream);
+        case 6: return launch_stages<Op, 6>(op, n, stream);
+        case 8: return launch_stages<Op, 8>(op, n, stream);
+        case 12: return launch_stages<Op, 12>(op, n, stream);
+        case 16: return launch_stages<Op, 16>(op, n, stream);
+        default: return launch_stages<Op, 2>(op, n, stream);
     }
 }
 
-int g_smem_set[256];  // per device: dynamic shared memory attribute applied
+bool fits_two_stages(size_t stage_bytes) {
+    return 2 * stage_bytes + kBarrierBytes <= static_cast<size_t>(device_smem_optin());
+}
 
 }  // namespace
 
-size_t tma_step_smem_bytes(int nd, int grad_type) {
+bool tma_step_fits(int nd, int grad_type) {
     const size_t gsz = grad_type == kGradF32 ? 4 : 2;
-    return static_cast<size_t>(kStages) * kTile * (nd * gsz + 12) + 2 * kStages * sizeof(uint64_t);
+    return fits_two_stages(static_cast<size_t>(kTile) * (nd * gsz + 12));
 }
+
+bool tma_reduce_fits(int nd, int grad_type) {
+    const size_t gsz = grad_type == kGradF32 ? 4 : 2;
+    return fits_two_stages(static_cast<size_t>(kTile) * nd * gsz);
+}
+
+int set_tma_stage_limit(int stages) { return g_stage_limit.exchange(stages); }
 
 cudaError_t launch_rs_adamw_cast_tma(const PtrTable& tab, int nd, int grad_type, int64_t S,
                                      float* master, float* m, float* v, uint16_t* out,
                                      const AdamScalars& c, const MeanOp& mo,
                                      const unsigned int* skip, cudaStream_t stream) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    const size_t smem = tma_step_smem_bytes(nd, grad_type);
-    if (dev >= 0 && dev < 256 && !g_smem_set[dev]) {
-        int optin = 0;
-        e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(rs_adamw_cast_tma<kGradBF16>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(rs_adamw_cast_tma<kGradF32>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(rs_adamw_cast_tma<kGradF16>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
-        if (e != cudaSuccess) return e;
-        g_smem_set[dev] = 1;
+    switch (grad_type) {
+        case kGradF32:
+            return launch_staged(AdamOp<kGradF32>{tab, nd, master, m, v, out, c, mo, skip}, S,
+                                 stream);
+        case kGradF16:
+            return launch_staged(AdamOp<kGradF16>{tab, nd, master, m, v, out, c, mo, skip}, S,
+                                 stream);
+        default:
+            return launch_staged(AdamOp<kGradBF16>{tab, nd, master, m, v, out, c, mo, skip}, S,
+                                 stream);
     }
-    const int64_t ntiles = ((S & ~static_cast<int64_t>(7)) + kTile - 1) / kTile;
-    int64_t grid = device_sms();
-    if (grid > ntiles) grid = ntiles;
-    if (grid < 1) grid = 1;
-    const unsigned g = static_cast<unsigned>(grid);
-    if (grad_type == kGradF32)
-        rs_adamw_cast_tma<kGradF32><<<g, kTmaThreads, smem, stream>>>(tab, nd, S, master, m, v,
-                                                                     out, c, mo, skip);
-    else if (grad_type == kGradF16)
-        rs_adamw_cast_tma<kGradF16><<<g, kTmaThreads, smem, stream>>>(tab, nd, S, master, m, v,
-                                                                     out, c, mo, skip);
-    else
-        rs_adamw_cast_tma<kGradBF16><<<g, kTmaThreads, smem, stream>>>(tab, nd, S, master, m, v,
-                                                                      out, c, mo, skip);
-    note_launch();
-    return cudaGetLastError();
+}
+
+cudaError_t launch_accumulate_tma(const uint16_t* g, float* acc, int64_t n, float scale,
+                                  bool first, cudaStream_t stream) {
+    if (first) return launch_staged(AccumOp<true>{g, acc, scale}, n, stream);
+    return launch_staged(AccumOp<false>{g, acc, scale}, n, stream);
+}
+
+cudaError_t launch_allreduce_avg_tma(const PtrTable& tab, int nd, int64_t n, uint16_t* out,
+                                     const MeanOp& mo, cudaStream_t stream) {
+    return launch_staged(MeanOutOp{tab, nd, out, mo}, n, stream);
+}
+
+cudaError_t launch_nonfinite_check_tma(const PtrTable& tab, int nd, int grad_type, int64_t S,
+                                       const MeanOp& mo, unsigned int* found,
+                                       cudaStream_t stream) {
+    switch (grad_type) {
+        case kGradF32: return launch_staged(CheckOp<kGradF32>{tab, nd, mo, found}, S, stream);
+        case kGradF16: return launch_staged(CheckOp<kGradF16>{tab, nd, mo, found}, S, stream);
+        default: return launch_staged(CheckOp<kGradBF16>{tab, nd, mo, found}, S, stream);
+    }
 }
 
 cudaError_t read_device_status(unsigned int* status, bool clear) {

@@ -32,10 +32,11 @@ def _built():
     assert ss.device_status() == 0
 
 
-@pytest.fixture(params=["auto", "register"])
+@pytest.fixture(params=["auto", "register", "tma"])
 def path(request):
-    """Run a fused-step test on the TMA-staged kernel (auto: used whenever the
-    arguments allow) and on the register-staged kernels only."""
+    """Run a test under each kernel choice: auto (TMA-staged where it measured
+    faster), register-staged only, and TMA-staged wherever the arguments
+    allow (also at N_d = 1, 2 and on small buckets)."""
     prev = ss.set_fused_path(request.param)
     yield request.param
     ss.set_fused_path(prev)
@@ -375,3 +376,72 @@ def test_allreduce_equals_reduce_scatter_then_all_gather_on_gpu():
     want = np.concatenate([oracle.f32_to_bf16(oracle.rs_avg(grads_h, r, S)) for r in range(nd)])
     assert_bits(host_bf16(ar), want, "AR")
     assert_bits(host_bf16(ar2), want, "RS+AG")
+
+
+# ------------------------------------- TMA-staged kernels under stage caps
+# The stage count of a TMA-staged launch (chosen for ~128 KB in flight, or
+# set) changes only how many tiles are in flight, never a result: every case is
+# bit-exact against the oracle under each cap, with tiles dealt unevenly over
+# the grid and a ragged tail of < 8 elements.
+
+@pytest.fixture(params=[0, 2, 3, 16])
+def stages(request):
+    prev = ss.set_tma_stages(request.param)
+    yield request.param
+    ss.set_tma_stages(prev)
+
+
+@pytest.mark.parametrize("nd,gdt,S", [(1, "bf16", 2048 * 152 * 2 + 8 * 3 + 5),
+                                      (8, "bf16", 2048 * 152 + 2048 * 7 + 16 + 3),
+                                      (3, "f32", 70001), (16, "bf16", 70001)])
+def test_fused_step_under_stage_caps(nd, gdt, S, stages):
+    seed = 11 + S + nd
+    contribs = _grads(seed, nd, nd * S, gdt, 1)
+    r = nd - 1
+    p = synth.host_fill(synth.normal_stream(seed, (99, 2), 0.02), 0, S, "f32")
+    m = synth.host_fill(synth.normal_stream(seed, (99, 3), 1e-4), 0, S, "f32")
+    v = np.abs(synth.host_fill(synth.normal_stream(seed, (99, 4), 1e-7), 0, S, "f32"))
+    dp, dm, dv = dev_f32(p), dev_f32(m), dev_f32(v)
+    out = torch.empty(S, dtype=torch.bfloat16, device=DEV)
+    mk = dev_bf16 if gdt == "bf16" else dev_f32
+    ss.fsdp_rs_avg_adamw_cast([mk(c[r * S:(r + 1) * S]) for c in contribs], dp, dm, dv, out,
+                              HPC, 3)
+    p, m, v, ob = oracle.fsdp_shard_step(contribs, r, S, p, m, v, HP, 3)
+    torch.cuda.synchronize()
+    assert_bits(host_f32(dp), p, "master")
+    assert_bits(host_f32(dm), m, "m")
+    assert_bits(host_f32(dv), v, "v")
+    assert_bits(host_bf16(out), ob, "bf16")
+
+
+@pytest.mark.parametrize("n", [4096, 2048 * 152 * 3 + 8 * 11 + 5, (1 << 21) + 7])
+def test_grad_accumulate_under_stage_caps(n, stages, path):
+    M = 3
+    micro = [synth.host_fill(synth.normal_stream(n, (94, j), 1e-3, 0.01), 0, n, "bf16")
+             for j in range(M)]
+    acc = torch.full((n,), 7.0, device=DEV)
+    scale = np.float32(1.0 / M)
+    for j in range(M):
+        ss.fsdp_grad_accumulate(dev_bf16(micro[j]), acc, float(scale), j == 0)
+    want = oracle.grad_accumulate(micro, scale)
+    torch.cuda.synchronize()
+    assert_bits(host_f32(acc), want, "acc")
+
+
+@pytest.mark.parametrize("nd", [1, 2, 8, 13])
+def test_bucket_allreduce_under_stage_caps(nd, stages, path):
+    # buckets: two TMA-eligible ones (16-byte aligned starts, >= 4096
+    # elements, one with a ragged tail), a small one, and one whose start is
+    # not 16-byte aligned (register-staged)
+    boff = [0, 8192, 8192 + 70000, 8192 + 70000 + 4099, 8192 + 70000 + 4099 + 100,
+            8192 + 70000 + 4099 + 100 + 9001]
+    total = boff[-1]
+    grads_h = [synth.host_fill(synth.normal_stream(nd, (95, q), 1e-3), 0, total, "bf16")
+               for q in range(nd)]
+    grads = [dev_bf16(h) for h in grads_h]
+    out = torch.empty(total, dtype=torch.bfloat16, device=DEV)
+    for b in range(len(boff) - 1):
+        ss.ddp_bucket_allreduce_avg(grads, boff, out, first=b, count=1)
+    want = oracle.bucket_allreduce_avg(grads_h, boff)
+    torch.cuda.synchronize()
+    assert_bits(host_bf16(out), want, "avg")

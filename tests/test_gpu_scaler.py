@@ -31,7 +31,7 @@ def _built():
     assert ss.device_status() == 0
 
 
-@pytest.fixture(params=["auto", "register"])
+@pytest.fixture(params=["auto", "register", "tma"])
 def path(request):
     prev = ss.set_fused_path(request.param)
     yield request.param
@@ -198,3 +198,30 @@ def test_llama_7b_rank_view_fp16_scaled_full_size():
     assert_bits(v[it].cpu().numpy(), vv, "v")
     assert_bits(_host(out[it]), ob, "bf16")
     assert np.float32(sc.scale.item()) == s_o
+
+
+@pytest.fixture(params=[0, 2, 16])
+def stages(request):
+    prev = ss.set_tma_stages(request.param)
+    yield request.param
+    ss.set_tma_stages(prev)
+
+
+@pytest.mark.parametrize("where", [None, ("mid", 0), ("last_tile", 7), ("tail", 3),
+                                   ("first", 5)])
+def test_check_finds_one_planted_value_anywhere(where, stages, path):
+    """One inf / NaN in one rank's slice is found wherever it sits (a tile's
+    middle, the last full tile, the ragged tail past the tiles, element 0);
+    a clean gradient sets nothing."""
+    nd, S = 8, 2048 * 152 + 2048 * 5 + 8 * 3 + 5
+    hs = [synth.host_fill(synth.normal_stream(9, (84, q), 0.3), 0, S, "f16") for q in range(nd)]
+    if where is not None:
+        kind, q = where
+        pos = {"mid": 2048 * 77 + 1001, "last_tile": (S & ~7) - 1, "tail": S - 2,
+               "first": 0}[kind]
+        hs[q][pos] = 0x7C00 if kind != "tail" else 0x7E00   # +inf, or a NaN
+    sc = ss.GradScaler(init_scale=512.0, device=DEV)
+    sc.check([_dev(h, "f16") for h in hs])
+    want = osc.found_inf([(h, "f16") for h in hs], nd, 0, S, np.float32(1.0 / 512.0))
+    torch.cuda.synchronize()
+    assert bool(int(sc.found_inf.item())) == want == (where is not None)
