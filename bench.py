@@ -732,26 +732,32 @@ def run_ckpt(args):
     new = [RankShardOptimizer(w.units, 4, r, hp, device="cuda:0") for r in range(4)]
     torch.cuda.synchronize()
     state_bytes = sum(3 * 4 * o.shard_total for o in old)
-    directory = tempfile.mkdtemp(prefix="shst_ckpt_")
+    root = tempfile.mkdtemp(prefix="shst_ckpt_")
     saves, loads = [], []
     try:
-        # the first save and load also pin each optimizer's host staging
-        t0 = time.perf_counter()
-        ck.save(directory, old)
-        t1 = time.perf_counter()
-        ck.load(directory, new)
-        first = (t1 - t0, time.perf_counter() - t1)
-        for _ in range(max(1, args.steps)):
+        # every save goes to a new directory (as a training run's periodic
+        # checkpoints do); the previous one is removed outside the timing.
+        # The first save and load also pin each optimizer's host staging.
+        prev = None
+        first = None
+        for k in range(max(1, args.steps) + 1):
+            directory = os.path.join(root, f"step{k}")
             t0 = time.perf_counter()
             ck.save(directory, old)
             t1 = time.perf_counter()
             ck.load(directory, new)
             t2 = time.perf_counter()
-            saves.append(t1 - t0)
-            loads.append(t2 - t1)
-        disk = sum(os.path.getsize(ck.rank_file(directory, r)) for r in range(8))
+            if k == 0:
+                first = (t1 - t0, t2 - t1)
+            else:
+                saves.append(t1 - t0)
+                loads.append(t2 - t1)
+            if prev is not None:
+                shutil.rmtree(prev, ignore_errors=True)
+            prev = directory
+        disk = sum(os.path.getsize(ck.rank_file(prev, r)) for r in range(8))
     finally:
-        shutil.rmtree(directory, ignore_errors=True)
+        shutil.rmtree(root, ignore_errors=True)
     sv, ld = statistics.median(saves), statistics.median(loads)
     print(json.dumps({
         "metric": "sharded checkpoint save / load GB/s (fp32 master + moments)",
