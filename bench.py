@@ -74,6 +74,8 @@ def parse():
     ap.add_argument("--kernel-path", choices=["auto", "register", "tma"], default="auto",
                     help="streaming kernels: TMA-staged where they measured faster (auto), "
                          "register-staged only, or TMA-staged wherever the arguments allow")
+    ap.add_argument("--no-dependent-launch", action="store_true",
+                    help="launch every bucket of an all-reduce call as an ordinary launch")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     return ap.parse_args()
@@ -160,6 +162,7 @@ def _apply_stages(args):
     import sharded_optimizer_step_gb300 as ss
     ss.set_tma_stages(args.tma_stages)
     ss.set_fused_path(args.kernel_path)
+    ss.set_dependent_launch(not args.no_dependent_launch)
 
 
 def _stages_name(args):
@@ -1134,6 +1137,7 @@ def run_ddp(args):
         "config": {"workload": DDP_WORKLOAD + (f"_first{args.layers}blocks" if args.layers
                                                else ""),
                    "tma_stages": _stages_name(args),
+                   "dependent_launch": not args.no_dependent_launch,
                    "psi": total, "nd": nd, "cap_mib": 25,
                    "buckets": len(boff) - 1,
                    "step": "one all-reduce-avg launch per bucket (8 bf16 rank gradients -> "
@@ -1154,6 +1158,9 @@ def run_ddp(args):
                                                 f"launches, one per bucket)", ar_bytes),
         "e2e": None, "e2e_note": "device-resident gradients; the end-to-end line is the "
                                  "default workload's",
+        "note": "buckets after the first of the call are launched as programmatic dependents "
+                "of the previous bucket's kernel" if not args.no_dependent_launch else
+                "every bucket an ordinary launch",
         "gpu_launches": launches, "clocks": clk, "cpu_baseline": cpu}))
 
 

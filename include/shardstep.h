@@ -475,13 +475,20 @@ int fsdp_reshard_plan(int64_t total, int32_t old_nd, int32_t new_nd, int32_t new
  * in shared memory); _REGISTER uses only the register-staged kernels;
  * _AUTO (default) uses the TMA-staged kernels where they measured faster:
  * the fused steps at N_d >= 3, the bucket all-reduce at N_d >= 3 on buckets
- * of at least 8M elements, the accumulation and the check always.  All give
+ * of at least 32M elements, the accumulation and the check always.  All give
  * bit-identical results.  Returns the previous setting, or INVALID for an
  * unknown value. */
 #define SHARDSTEP_PATH_AUTO 0
 #define SHARDSTEP_PATH_REGISTER 1
 #define SHARDSTEP_PATH_TMA 2
 int32_t shardstep_set_fused_path(int32_t path);
+
+/* Whether the second and later buckets of one ddp_bucket_allreduce_avg call
+ * are launched as programmatic dependents of the previous bucket's kernel
+ * (they may start while it drains; each still ends after it), process-wide.
+ * 1 (default) = yes, 0 = ordinary launches.  Results do not depend on it.
+ * Returns the previous setting. */
+int32_t shardstep_set_dependent_launch(int32_t enable);
 
 /* Sets the shared-memory stages of each TMA-staged launch, process-wide:
  * 0 (default) = enough stages for about 128 KB of tiles in flight per SM

@@ -454,6 +454,13 @@ def set_tma_stages(stages: int) -> int:
     return prev
 
 
+def set_dependent_launch(enable: bool) -> bool:
+    """Whether later buckets of one all-reduce call are launched as
+    programmatic dependents of the previous bucket (default True).  Results
+    do not depend on it; returns the previous setting."""
+    return bool(_capi.lib().shardstep_set_dependent_launch(int(bool(enable))))
+
+
 def device_status(clear: bool = False) -> int:
     """Watchdog bits of the current device (0: no TMA-staged wait ran out)."""
     st = ctypes.c_uint32(0)

@@ -91,6 +91,7 @@ SIGNATURES = {
     "shardstep_last_error": (ctypes.c_char_p, []),
     "shardstep_set_fused_path": (c_i32, [c_i32]),
     "shardstep_set_tma_stages": (c_i32, [c_i32]),
+    "shardstep_set_dependent_launch": (c_i32, [c_i32]),
     "shardstep_device_status": (c_i32, [ctypes.POINTER(ctypes.c_uint32), c_i32]),
     "shardstep_launch_count": (c_u64, []),
 }

@@ -19,6 +19,7 @@ namespace {
 thread_local std::string g_error;
 std::atomic<uint64_t> g_launches{0};
 std::atomic<int> g_fused_path{SHARDSTEP_PATH_AUTO};
+std::atomic<int> g_dependent_launch{1};
 
 // Whether a launch of n elements goes to a TMA-staged kernel (the caller
 // still checks alignment and the stage size).  PATH_REGISTER: never;
@@ -26,9 +27,11 @@ std::atomic<int> g_fused_path{SHARDSTEP_PATH_AUTO};
 // register-staged kernel of the same operation --
 //   fused step: N_d >= 3 (at N_d = 1 and 2 the register kernel moved 6.5 vs
 //     6.1 TB/s; at N_d = 8, 6.9 vs 6.5);
-//   bucket all-reduce: N_d >= 3 and buckets of at least 8M elements (small
-//     buckets pay the pipeline fill once per launch: 67 buckets of a 351M
-//     gradient took 1.21 ms vs 1.18 ms, 3 buckets 0.89 vs 0.91 ms);
+//   bucket all-reduce: N_d >= 3 and buckets of at least 32M elements (later
+//     buckets of a call are dependent launches that overlap the previous
+//     bucket's drain, which favours the register-staged kernel's finer
+//     grid: a 351M gradient in 33 buckets took 0.908 ms register-staged vs
+//     0.924 ms with TMA from 8M elements; in 3 buckets 0.894 vs 0.880 ms);
 //   accumulation and the non-finite check: always (6.5 vs 6.0 and 7.3 vs
 //     6.9 TB/s).
 enum class TmaOp { kStep, kAllReduce, kAccumulate, kCheck };
@@ -38,7 +41,7 @@ bool use_tma(TmaOp op, int64_t n, int nd = 0) {
     if (path == SHARDSTEP_PATH_TMA) return true;
     switch (op) {
         case TmaOp::kStep: return nd >= 3;
-        case TmaOp::kAllReduce: return nd >= 3 && n >= (int64_t{8} << 20);
+        case TmaOp::kAllReduce: return nd >= 3 && n >= (int64_t{32} << 20);
         default: return true;
     }
 }
@@ -222,6 +225,10 @@ int32_t shardstep_set_fused_path(int32_t path) {
         path != SHARDSTEP_PATH_TMA)
         return fail(SHARDSTEP_ERR_INVALID, "unknown path %d", path);
     return g_fused_path.exchange(path);
+}
+
+int32_t shardstep_set_dependent_launch(int32_t enable) {
+    return g_dependent_launch.exchange(enable != 0 ? 1 : 0);
 }
 
 int32_t shardstep_set_tma_stages(int32_t stages) {
@@ -802,6 +809,11 @@ int ddp_bucket_allreduce_avg(const uint16_t* const* rank_grads, int32_t nd,
             return fail(SHARDSTEP_ERR_INVALID, "rank_grads[%d] overlaps out", q);
     }
     const MeanOp mo = mean_op(nd, nd);
+    // the first launch of the call waits for everything before it in the
+    // stream (the producers of the gradients); later buckets only follow
+    // this call's own launches, on disjoint outputs, so they go out as
+    // programmatic dependents and overlap the previous bucket's drain
+    bool pdl = false;
     for (int32_t b = first; b < first + count; ++b) {
         const int64_t a = bucket_offsets[b], n = bucket_offsets[b + 1] - a;
         if (n == 0) continue;
@@ -815,11 +827,12 @@ int ddp_bucket_allreduce_avg(const uint16_t* const* rank_grads, int32_t nd,
                 tma = tma && aligned(tab.p[q], 16);
             }
         }
-        cudaError_t e = tma ? launch_allreduce_avg_tma(tab, nd, n, out + a, mo,
+        cudaError_t e = tma ? launch_allreduce_avg_tma(tab, nd, n, out + a, mo, pdl,
                                                        static_cast<cudaStream_t>(stream))
-                            : launch_allreduce_avg(tab, nd, n, out + a, mo, vec,
+                            : launch_allreduce_avg(tab, nd, n, out + a, mo, vec, pdl,
                                                    static_cast<cudaStream_t>(stream));
         if (e != cudaSuccess) return cuda_fail(e, "all-reduce kernel launch");
+        pdl = g_dependent_launch.load(std::memory_order_relaxed) != 0;
     }
     return ok();
 }

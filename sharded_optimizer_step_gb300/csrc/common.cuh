@@ -67,6 +67,17 @@ __device__ __forceinline__ uint4 ldcs16(const void* p) {
 __device__ __forceinline__ void stcs8(void* p, uint2 v) { __stcs(reinterpret_cast<uint2*>(p), v); }
 __device__ __forceinline__ void stcs16(void* p, uint4 v) { __stcs(reinterpret_cast<uint4*>(p), v); }
 
+// ------------------------------------------------- dependent launches
+
+// Programmatic dependent launch: let the next grid of the stream, if it was
+// launched as a dependent, be scheduled once every CTA of this grid has
+// started; and wait for the grid this one depends on (if any) to complete
+// and its memory to be visible.  Both return at once for ordinary launches.
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------------- bf16
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }

@@ -59,6 +59,26 @@ struct CopyTable {
 };
 constexpr int kCopyVecsPerChunk = 1024;  // 256 threads x 4
 
+// Launches `kernel` as a programmatic dependent of the previous kernel in
+// `stream`: it may start while that kernel drains.  Only for launches whose
+// kernel neither reads nor writes anything the previous kernel writes, and
+// which wait (pdl_wait) for it before they end.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // Launch bookkeeping (api.cpp).
 void note_launch();
 int device_sms();                                   // SMs of the current device (cached)
@@ -86,8 +106,10 @@ cudaError_t launch_rs_adamw_cast_tma(const PtrTable& tab, int nd, int grad_type,
                                      const unsigned int* skip, cudaStream_t stream);
 cudaError_t launch_accumulate_tma(const uint16_t* g, float* acc, int64_t n, float scale,
                                   bool first, cudaStream_t stream);
+// pdl: launch as a programmatic dependent of the previous bucket's kernel
+// (later buckets of one ddp_bucket_allreduce_avg call).
 cudaError_t launch_allreduce_avg_tma(const PtrTable& tab, int nd, int64_t n, uint16_t* out,
-                                     const MeanOp& mo, cudaStream_t stream);
+                                     const MeanOp& mo, bool pdl, cudaStream_t stream);
 cudaError_t launch_nonfinite_check_tma(const PtrTable& tab, int nd, int grad_type, int64_t S,
                                        const MeanOp& mo, unsigned int* found,
                                        cudaStream_t stream);
@@ -103,7 +125,7 @@ int device_smem_optin();  // max dynamic shared memory per block (cached)
 constexpr int64_t kTmaMinElements = 4096;
 
 cudaError_t launch_allreduce_avg(const PtrTable& tab, int nd, int64_t n, uint16_t* out,
-                                 const MeanOp& mo, bool vec, cudaStream_t stream);
+                                 const MeanOp& mo, bool vec, bool pdl, cudaStream_t stream);
 cudaError_t launch_copy(const CopyTable& t, cudaStream_t stream);
 cudaError_t launch_accumulate(const uint16_t* g, float* acc, int64_t n, float scale, bool first,
                               bool vec, cudaStream_t stream);

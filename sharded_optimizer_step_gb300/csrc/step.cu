@@ -207,9 +207,13 @@ __global__ void __launch_bounds__(kThreads)
 
 // ------------------------------------------------ bucket all-reduce avg
 
+// Both all-reduce kernels may run as programmatic dependents of the previous
+// bucket's kernel: they trigger their own dependents at start and wait for
+// the grid they depend on before they end (no-ops for ordinary launches).
 template <int ND>
 __global__ void __launch_bounds__(kStepThreads, kStepMinBlocks)
     allreduce_avg_vec4(PtrTable tab, int nd, int64_t n, uint16_t* __restrict__ out, MeanOp mo) {
+    pdl_trigger();
     const int64_t nvec = n >> 2;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kStepThreads;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * kStepThreads + threadIdx.x; i < nvec;
@@ -224,15 +228,18 @@ __global__ void __launch_bounds__(kStepThreads, kStepMinBlocks)
         const int64_t j = (nvec << 2) + threadIdx.x;
         out[j] = f32_to_bf16(mean_of(reduce1<kGradBF16>(tab, nd, mo.group, j), mo));
     }
+    pdl_wait();
 }
 
 __global__ void __launch_bounds__(kThreads)
     allreduce_avg_scalar(PtrTable tab, int nd, int64_t n, uint16_t* __restrict__ out,
                          MeanOp mo) {
+    pdl_trigger();
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
     for (int64_t j = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; j < n;
          j += stride)
         out[j] = f32_to_bf16(mean_of(reduce1<kGradBF16>(tab, nd, mo.group, j), mo));
+    pdl_wait();
 }
 
 // ------------------------------------------------------ gradient scaler
@@ -353,13 +360,19 @@ cudaError_t go_scalar(const StepArgs& a, cudaStream_t s) {
 
 template <int ND>
 cudaError_t go_ar(const PtrTable& tab, int nd, int64_t n, uint16_t* out, const MeanOp& mo,
-                  cudaStream_t s) {
+                  bool pdl, cudaStream_t s) {
     auto k = allreduce_avg_vec4<ND>;
     const unsigned grid = grid_for(reinterpret_cast<const void*>(k), (n >> 2) > 0 ? (n >> 2) : 1,
                                    kStepThreads, kGridOversub);
-    k<<<grid, kStepThreads, 0, s>>>(tab, nd, n, out, mo);
+    cudaError_t e;
+    if (pdl) {
+        e = launch_dependent(k, dim3(grid), dim3(kStepThreads), 0, s, tab, nd, n, out, mo);
+    } else {
+        k<<<grid, kStepThreads, 0, s>>>(tab, nd, n, out, mo);
+        e = cudaGetLastError();
+    }
     note_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 template <int ND, int GT>
@@ -405,20 +418,27 @@ cudaError_t launch_rs_adamw_cast(const PtrTable& tab, int nd, int grad_type, int
 }
 
 cudaError_t launch_allreduce_avg(const PtrTable& tab, int nd, int64_t n, uint16_t* out,
-                                 const MeanOp& mo, bool vec, cudaStream_t stream) {
+                                 const MeanOp& mo, bool vec, bool pdl, cudaStream_t stream) {
     if (vec) {
         switch (nd) {
-            case 1: return go_ar<1>(tab, nd, n, out, mo, stream);
-            case 2: return go_ar<2>(tab, nd, n, out, mo, stream);
-            case 4: return go_ar<4>(tab, nd, n, out, mo, stream);
-            case 8: return go_ar<8>(tab, nd, n, out, mo, stream);
-            default: return go_ar<kRuntimeND>(tab, nd, n, out, mo, stream);
+            case 1: return go_ar<1>(tab, nd, n, out, mo, pdl, stream);
+            case 2: return go_ar<2>(tab, nd, n, out, mo, pdl, stream);
+            case 4: return go_ar<4>(tab, nd, n, out, mo, pdl, stream);
+            case 8: return go_ar<8>(tab, nd, n, out, mo, pdl, stream);
+            default: return go_ar<kRuntimeND>(tab, nd, n, out, mo, pdl, stream);
         }
     }
     const unsigned grid = grid_for(reinterpret_cast<const void*>(allreduce_avg_scalar), n);
-    allreduce_avg_scalar<<<grid, kThreads, 0, stream>>>(tab, nd, n, out, mo);
+    cudaError_t e;
+    if (pdl) {
+        e = launch_dependent(allreduce_avg_scalar, dim3(grid), dim3(kThreads), 0, stream, tab, nd,
+                             n, out, mo);
+    } else {
+        allreduce_avg_scalar<<<grid, kThreads, 0, stream>>>(tab, nd, n, out, mo);
+        e = cudaGetLastError();
+    }
     note_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t launch_nonfinite_check(const PtrTable& tab, int nd, int grad_type, int64_t S,

@@ -445,3 +445,36 @@ def test_bucket_allreduce_under_stage_caps(nd, stages, path):
     want = oracle.bucket_allreduce_avg(grads_h, boff)
     torch.cuda.synchronize()
     assert_bits(host_bf16(out), want, "avg")
+
+
+@pytest.mark.parametrize("dependent", [True, False])
+def test_bucket_allreduce_dependent_launches_keep_stream_order(dependent, path):
+    """Later buckets of one call may start while the previous bucket's kernel
+    drains; the first waits for the gradients' producer (a torch kernel just
+    before the call) and a torch kernel right after the call sees every
+    bucket's result."""
+    nd = 4
+    # buckets that take the TMA-staged kernel under path "tma" (>= 4096
+    # elements, 16-byte aligned starts) between ones that cannot, two
+    # consecutive large ones, a ragged tail
+    sizes = [9_000_000, 104, 4096, 8_388_616, 8_388_608, 336, 70_000, 8, 8_388_608, 4099]
+    boff = [0]
+    for z in sizes:
+        boff.append(boff[-1] + z)
+    total = boff[-1]
+    grads_h = [synth.host_fill(synth.normal_stream(17, (96, q), 1e-3), 0, total, "bf16")
+               for q in range(nd)]
+    staged = [dev_bf16(h) for h in grads_h]
+    grads = [torch.empty_like(g) for g in staged]
+    out = torch.full((total,), 5.0, dtype=torch.bfloat16, device=DEV)
+    prev = ss.set_dependent_launch(dependent)
+    try:
+        for g, s in zip(grads, staged):
+            g.copy_(s)                      # the producer, on the same stream
+        ss.ddp_bucket_allreduce_avg(grads, boff, out)
+        seen = out.clone()                  # the consumer, on the same stream
+    finally:
+        ss.set_dependent_launch(prev)
+    want = oracle.bucket_allreduce_avg(grads_h, boff)
+    torch.cuda.synchronize()
+    assert_bits(host_bf16(seen), want, "avg")
