@@ -716,7 +716,10 @@ def run_ckpt(args):
     resharded state (pieces of the saved files -> pinned host -> device)."""
     import shutil
     import torch
-    torch.cuda.set_device(0)
+    world, rank, local = dist_env()
+    if rank != 0:
+        return                          # host-IO line: one process
+    torch.cuda.set_device(local)
     import __graft_entry__
     __graft_entry__.build()
     _apply_stages(args)
@@ -785,9 +788,10 @@ def run_ckpt(args):
 ACCUM_WORKLOAD = "llama_1b_rank0_nd8_m4"
 
 
-def _timed_loop(torch, stream, args, one_step, n_events):
-    """Warm-up, then args.steps timed steps with n_events CUDA events each;
-    returns (total ms, per-step event lists, clocks, launches)."""
+def _timed_loop(torch, stream, args, one_step, n_events, world=1):
+    """Warm-up, then args.steps timed steps with n_events CUDA events each,
+    bracketed by a barrier and a device synchronize on both sides; returns
+    (total ms, max over ranks; per-step event lists; clocks; launches)."""
     import sharded_optimizer_step_gb300 as ss
     clocks = ClockSampler(smi_index(torch.cuda.current_device()))
     clocks.start()
@@ -798,6 +802,7 @@ def _timed_loop(torch, stream, args, one_step, n_events):
               for _ in range(args.steps)]
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
+    barrier(world)
     torch.cuda.synchronize()
     launches0 = ss.launch_count()
     torch.cuda.nvtx.range_push("timed_region")
@@ -807,11 +812,12 @@ def _timed_loop(torch, stream, args, one_step, n_events):
     b.record(stream)
     torch.cuda.synchronize()
     torch.cuda.nvtx.range_pop()
+    barrier(world)
     launches = ss.launch_count() - launches0
     clk = clocks.stop()
     if ss.device_status():
         raise RuntimeError("a TMA-staged wait ran out during the timed steps")
-    return a.elapsed_time(b), events, clk, launches
+    return allreduce_max(world, a.elapsed_time(b)), events, clk, launches
 
 
 def _avg_ms(events, i, j):
@@ -868,10 +874,12 @@ def run_accum(args):
     8 contributions side by side), then one fused step reads the 8 fp32
     accumulators, then one layer unit is all-gathered.  The accumulate work
     per step equals a real rank's (N_d shard slices = one full gradient)."""
+    world, rank, local = dist_env()
     if args.impl == "reference":
-        return _accum_reference(args)
+        return _accum_reference(args) if rank == 0 else None
+    init_dist(world)
     import torch
-    torch.cuda.set_device(0)
+    torch.cuda.set_device(local)
     import __graft_entry__
     __graft_entry__.build()
     _apply_stages(args)
@@ -882,8 +890,9 @@ def run_accum(args):
     w = W.llama_1b()
     if args.layers:
         w.units = w.units[:args.layers]      # smaller case: the first N layer units
-    nd, M, r = w.nd, w.micro, 0
-    dev = torch.device("cuda", 0)
+    nd, M = w.nd, w.micro
+    r = rank % nd                       # GPU k holds rank k mod N_d's view of its own replica
+    dev = torch.device("cuda", local)
     hp = ss.AdamW(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
     opt = RankShardOptimizer(w.units, nd, r, hp, device=dev, grad_dtype=torch.float32)
     S = opt.shard_total
@@ -922,9 +931,13 @@ def run_accum(args):
         if ev is not None:
             ev[3].record(stream)
 
-    total_ms, events, clk, launches = _timed_loop(torch, stream, args, one_step, 4)
+    total_ms, events, clk, launches = _timed_loop(torch, stream, args, one_step, 4, world)
     acc_ms, fused_ms, ag_ms = _avg_ms(events, 0, 1), _avg_ms(events, 1, 2), _avg_ms(events, 2, 3)
     ms = total_ms / args.steps
+    all_bytes = allreduce_sum(world, step_bytes)
+    if rank != 0:
+        _finish_dist(world)
+        return
     acc_gbs = acc_bytes / (acc_ms / 1e3) / 1e9
     fused_gbs = fused_bytes / (fused_ms / 1e3) / 1e9
     cpu = None
@@ -939,7 +952,7 @@ def run_accum(args):
     print(json.dumps({
         "metric": "micro-batch accumulate + fused fp32-accumulator step HBM GB/s, "
                   "Llama-1B rank view, N_d=8, M=4",
-        "value": round(step_bytes / (ms / 1e3) / 1e9, 1), "unit": "GB/s", "n_gpus": 1,
+        "value": round(all_bytes / (ms / 1e3) / 1e9, 1), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded counter-based generator on the device; no data set or weights)",
@@ -954,7 +967,7 @@ def run_accum(args):
                            "accumulators (1 launch), all-gather of one layer unit (1 launch)",
                    "bytes_per_step": step_bytes,
                    "l2": f"no flush: each step streams {step_bytes / 1e9:.1f} GB vs a 129 MB L2"},
-        "params_per_s": round(S / (ms / 1e3), 1),
+        "params_per_s": round(S * world / (ms / 1e3), 1),
         "kernels": {"accumulate_ms": round(acc_ms, 4), "accumulate_gbs": round(acc_gbs, 1),
                     "fused_ms": round(fused_ms, 4), "fused_gbs": round(fused_gbs, 1),
                     "fused_frac": round(fused_gbs / measured_peak()[0], 4),
@@ -965,6 +978,13 @@ def run_accum(args):
         "e2e": None, "e2e_note": "device-resident micro-batch gradients; the end-to-end "
                                  "line is the default workload's",
         "gpu_launches": launches, "clocks": clk, "cpu_baseline": cpu}))
+    _finish_dist(world)
+
+
+def _finish_dist(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
 
 
 def _accum_reference(args):
@@ -1031,7 +1051,10 @@ def run_ddp(args):
     numels = w.unit_numels(0)
     if args.layers:
         numels = numels[:5 * args.layers]    # smaller case: the first N blocks' parameters
+    world, rank, local = dist_env()
     if args.impl == "reference":
+        if rank != 0:
+            return
         n_params = 4
         ts, bs = [], []
         for k in range(args.warmup + args.steps):
@@ -1053,8 +1076,9 @@ def run_ddp(args):
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}))
         return
+    init_dist(world)
     import torch
-    torch.cuda.set_device(0)
+    torch.cuda.set_device(local)
     import __graft_entry__
     __graft_entry__.build()
     _apply_stages(args)
@@ -1062,7 +1086,7 @@ def run_ddp(args):
     import synth
     nd = w.nd
     total = sum(numels)
-    dev = torch.device("cuda", 0)
+    dev = torch.device("cuda", local)
     grads = [torch.empty(total, dtype=torch.bfloat16, device=dev) for _ in range(nd)]
     hp = ss.AdamW(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
     plans = {}
@@ -1096,9 +1120,10 @@ def run_ddp(args):
         if ev is not None:
             ev[2].record(stream)
 
-    total_ms, events, clk, launches = _timed_loop(torch, stream, args, one_step, 3)
+    total_ms, events, clk, launches = _timed_loop(torch, stream, args, one_step, 3, world)
     ar_ms, adam_ms = _avg_ms(events, 0, 1), _avg_ms(events, 1, 2)
     ms = total_ms / args.steps
+    all_bytes = allreduce_sum(world, step_bytes)
     # the other caps: all-reduce only, same gradients (the values per bucket
     # differ in placement, not in amount of work)
     by_cap = {}
@@ -1116,6 +1141,9 @@ def run_ddp(args):
         cap_ms = a.elapsed_time(b) / reps
         by_cap[f"{mib}MiB"] = {"buckets": len(bo) - 1, "ms": round(cap_ms, 4),
                                "gbs": round(ar_bytes / (cap_ms / 1e3) / 1e9, 1)}
+    if rank != 0:
+        _finish_dist(world)
+        return
     ar_gbs = ar_bytes / (ar_ms / 1e3) / 1e9
     adam_gbs = adam_bytes / (adam_ms / 1e3) / 1e9
     cpu = None
@@ -1130,7 +1158,7 @@ def run_ddp(args):
     print(json.dumps({
         "metric": "DDP bucket all-reduce avg + full AdamW HBM GB/s, Psi=351M, N_d=8, "
                   "25 MiB buckets",
-        "value": round(step_bytes / (ms / 1e3) / 1e9, 1), "unit": "GB/s", "n_gpus": 1,
+        "value": round(all_bytes / (ms / 1e3) / 1e9, 1), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded counter-based generator on the device; no data set or weights)",
@@ -1162,6 +1190,7 @@ def run_ddp(args):
                 "of the previous bucket's kernel" if not args.no_dependent_launch else
                 "every bucket an ordinary launch",
         "gpu_launches": launches, "clocks": clk, "cpu_baseline": cpu}))
+    _finish_dist(world)
 
 
 def main():
