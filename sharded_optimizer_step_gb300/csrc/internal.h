@@ -59,6 +59,22 @@ struct CopyTable {
 };
 constexpr int kCopyVecsPerChunk = 1024;  // 256 threads x 4
 
+// Byte ranges for the TMA-staged copy: source, destination and size all
+// multiples of 16 bytes; cut into tiles of kBulkChunk bytes (2048 vectors of
+// 16 bytes, one staged tile each).
+constexpr int kBulkChunk = 32768;
+struct BulkSeg {
+    const char* src;
+    char* dst;
+    int64_t bytes;
+    int64_t chunk0;  // first chunk index of this segment in the launch
+};
+struct BulkTable {
+    BulkSeg s[kMaxCopySegs];
+    int32_t n;
+    int64_t total_chunks;
+};
+
 // Launches `kernel` as a programmatic dependent of the previous kernel in
 // `stream`: it may start while that kernel drains.  Only for launches whose
 // kernel neither reads nor writes anything the previous kernel writes, and
@@ -127,6 +143,9 @@ constexpr int64_t kTmaMinElements = 4096;
 cudaError_t launch_allreduce_avg(const PtrTable& tab, int nd, int64_t n, uint16_t* out,
                                  const MeanOp& mo, bool vec, bool pdl, cudaStream_t stream);
 cudaError_t launch_copy(const CopyTable& t, cudaStream_t stream);
+// TMA-staged segment copy (step_tma.cu): tiles brought into shared memory by
+// cp.async.bulk, written out by the consumer warps.
+cudaError_t launch_bulk_copy(const BulkTable& t, cudaStream_t stream);
 cudaError_t launch_accumulate(const uint16_t* g, float* acc, int64_t n, float scale, bool first,
                               bool vec, cudaStream_t stream);
 

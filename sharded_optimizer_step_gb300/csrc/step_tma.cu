@@ -176,7 +176,7 @@ __device__ __forceinline__ bool not_finite(float x) {
 //   skipped()                              true: every thread returns at once
 //   init()                                 the thread's State
 //   stage_bytes()                          one stage (a multiple of 16 bytes)
-//   tx_bytes(n)                            bytes the copies of an n-element tile bring
+//   tx_bytes(e0, n)                        bytes the copies of the n-element tile at e0 bring
 //   issue(stage, e0, n, bar)               the producer lane's bulk copies of a tile
 //   consume(stage, e0, e, state)           4 elements at tile offset e
 //   tail(j, state)                         element j past the tiles, global loads
@@ -227,7 +227,7 @@ __device__ __forceinline__ void staged_body(const Op& op, int64_t n) {
             }
             const int64_t e0 = (static_cast<int64_t>(blockIdx.x) + j * gridDim.x) * kTile;
             const uint32_t cnt = static_cast<uint32_t>(n_main - e0 < kTile ? n_main - e0 : kTile);
-            mbar_expect_tx(&full[s], op.tx_bytes(cnt));
+            mbar_expect_tx(&full[s], op.tx_bytes(e0, cnt));
             op.issue(smem + static_cast<size_t>(s) * stage_bytes, e0, cnt, &full[s]);
             if (++s == nst) {
                 s = 0;
@@ -305,7 +305,7 @@ struct AdamOp {
     __host__ __device__ uint32_t stage_bytes() const {
         return static_cast<uint32_t>(nd) * kTile * gsz + 3u * kTile * 4u;
     }
-    __device__ uint32_t tx_bytes(uint32_t n) const { return nd * n * gsz + 3u * n * 4u; }
+    __device__ uint32_t tx_bytes(int64_t, uint32_t n) const { return nd * n * gsz + 3u * n * 4u; }
     __device__ void issue(uint8_t* st, int64_t e0, uint32_t n, uint64_t* bar) const {
         for (int q = 0; q < nd; ++q)
             bulk_load(st + q * (kTile * gsz), static_cast<const uint8_t*>(tab.p[q]) + e0 * gsz,
@@ -359,7 +359,7 @@ struct AccumOp {
     __host__ __device__ uint32_t stage_bytes() const {
         return kTile * 2u + (FIRST ? 0u : kTile * 4u);
     }
-    __device__ uint32_t tx_bytes(uint32_t n) const { return n * 2u + (FIRST ? 0u : n * 4u); }
+    __device__ uint32_t tx_bytes(int64_t, uint32_t n) const { return n * 2u + (FIRST ? 0u : n * 4u); }
     __device__ void issue(uint8_t* st, int64_t e0, uint32_t n, uint64_t* bar) const {
         bulk_load(st, g + e0, n * 2, bar);
         if (!FIRST) bulk_load(st + kTile * 2, acc + e0, n * 4, bar);
@@ -398,7 +398,7 @@ struct MeanOutOp {
     __host__ __device__ uint32_t stage_bytes() const {
         return static_cast<uint32_t>(nd) * kTile * 2u;
     }
-    __device__ uint32_t tx_bytes(uint32_t n) const { return nd * n * 2u; }
+    __device__ uint32_t tx_bytes(int64_t, uint32_t n) const { return nd * n * 2u; }
     __device__ void issue(uint8_t* st, int64_t e0, uint32_t n, uint64_t* bar) const {
         for (int q = 0; q < nd; ++q)
             bulk_load(st + q * (kTile * 2), static_cast<const uint16_t*>(tab.p[q]) + e0, n * 2,
@@ -436,7 +436,7 @@ struct CheckOp {
     __host__ __device__ uint32_t stage_bytes() const {
         return static_cast<uint32_t>(nd) * kTile * gsz;
     }
-    __device__ uint32_t tx_bytes(uint32_t n) const { return nd * n * gsz; }
+    __device__ uint32_t tx_bytes(int64_t, uint32_t n) const { return nd * n * gsz; }
     __device__ void issue(uint8_t* st, int64_t e0, uint32_t n, uint64_t* bar) const {
         for (int q = 0; q < nd; ++q)
             bulk_load(st + q * (kTile * gsz), static_cast<const uint8_t*>(tab.p[q]) + e0 * gsz,
@@ -454,6 +454,63 @@ struct CheckOp {
     __device__ void finish(State& s, int lane) const {
         if (__any_sync(0xFFFFFFFFu, s.bad) && lane == 0) atomicOr(found, 1u);
     }
+};
+
+// Segment copy: byte ranges whose source, destination and size are multiples
+// of 16 bytes.  Elements are 16-byte vectors; segment k owns tiles
+// [chunk0_k, chunk0_k + ceil(vectors_k / kTile)) of the index space, so no
+// tile straddles two segments and a segment's last tile may be short.  The
+// producer brings each tile in with one bulk copy; the consumers write it out
+// with streaming stores (TMA stores for both directions measured slower:
+// 0.133 vs 0.130 ms for a 405 MB all-gather).
+struct CopyOp {
+    BulkTable t;
+
+    struct State {};
+    __device__ bool skipped() const { return false; }
+    __device__ State init() const { return State{}; }
+    __host__ __device__ uint32_t stage_bytes() const { return kTile * 16u; }
+    // segment of tile e0 / kTile (chunk0 increasing), and the tile's vectors
+    __device__ __forceinline__ const BulkSeg& seg_of(int64_t e0) const {
+        const int64_t tile = e0 / kTile;
+        int lo = 0, hi = t.n - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (t.s[mid].chunk0 <= tile) lo = mid;
+            else hi = mid - 1;
+        }
+        return t.s[lo];
+    }
+    __device__ __forceinline__ uint32_t vecs(const BulkSeg& sg, int64_t e0) const {
+        const int64_t left = sg.bytes / 16 - (e0 - sg.chunk0 * kTile);
+        return static_cast<uint32_t>(left < kTile ? left : kTile);
+    }
+    __device__ uint32_t tx_bytes(int64_t e0, uint32_t) const { return vecs(seg_of(e0), e0) * 16u; }
+    __device__ void issue(uint8_t* st, int64_t e0, uint32_t, uint64_t* bar) const {
+        const BulkSeg& sg = seg_of(e0);
+        bulk_load(st, sg.src + (e0 - sg.chunk0 * kTile) * 16, vecs(sg, e0) * 16u, bar);
+    }
+    __device__ void consume(const uint8_t* st, int64_t e0, int e, State&) const {
+        const BulkSeg& sg = seg_of(e0);
+        const int nv = static_cast<int>(vecs(sg, e0));
+        char* dst = sg.dst + (e0 - sg.chunk0 * kTile) * 16;
+        // 4 vectors per thread, spaced a warp apart so each store
+        // instruction of a warp writes 512 contiguous bytes
+        const int lane = e & 127, base = (e >> 7) << 7;
+        uint4 v[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int x = base + (lane >> 2) + 32 * k;
+            if (x < nv) v[k] = *reinterpret_cast<const uint4*>(st + x * 16);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int x = base + (lane >> 2) + 32 * k;
+            if (x < nv) stcs16(dst + x * 16, v[k]);
+        }
+    }
+    __device__ void tail(int64_t, State&) const {}
+    __device__ void finish(State&, int) const {}
 };
 
 // --------------------------------------------------------------- launch
@@ -572,6 +629,10 @@ cudaError_t launch_nonfinite_check_tma(const PtrTable& tab, int nd, int grad_typ
         case kGradF16: return launch_staged(CheckOp<kGradF16>{tab, nd, mo, found}, S, stream);
         default: return launch_staged(CheckOp<kGradBF16>{tab, nd, mo, found}, S, stream);
     }
+}
+
+cudaError_t launch_bulk_copy(const BulkTable& t, cudaStream_t stream) {
+    return launch_staged(CopyOp{t}, t.total_chunks * kTile, stream);
 }
 
 cudaError_t read_device_status(unsigned int* status, bool clear) {

@@ -36,6 +36,16 @@ def _built():
     synth.build_dev()
 
 
+@pytest.fixture(params=["auto", "register", "tma"])
+def path(request):
+    """Each kernel choice: auto, register-staged only (vector copies), and
+    TMA-staged wherever the arguments allow (bulk copies of every aligned
+    range)."""
+    prev = ss.set_fused_path(request.param)
+    yield request.param
+    ss.set_fused_path(prev)
+
+
 def _dev(h, shift=0):
     dt = torch.bfloat16 if h.dtype == np.uint16 else torch.float32
     buf = torch.empty(h.size + shift + 8, dtype=dt, device=DEV)
@@ -60,7 +70,7 @@ def _tensors(shapes, seed, dtype):
 @pytest.mark.parametrize("shapes", SHAPE_SETS, ids=lambda s: f"{len(s)}params")
 @pytest.mark.parametrize("nd", [1, 2, 4, 8])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
-def test_chunk_cat_and_copy_out_match_oracle(shapes, nd, dtype):
+def test_chunk_cat_and_copy_out_match_oracle(shapes, nd, dtype, path):
     host = _tensors(shapes, nd, dtype)
     dev = [_dev(h.reshape(-1), t % 3).view(s) for t, (h, s) in enumerate(zip(host, shapes))]
     lay = oracle.fsdp2_layout(shapes, nd)
@@ -85,7 +95,7 @@ def test_chunk_cat_and_copy_out_match_oracle(shapes, nd, dtype):
 
 @pytest.mark.parametrize("shapes", SHAPE_SETS[2:], ids=lambda s: f"{len(s)}params")
 @pytest.mark.parametrize("nd", [2, 8])
-def test_fsdp2_step_matches_oracle(shapes, nd):
+def test_fsdp2_step_matches_oracle(shapes, nd, path):
     # every rank: chunk-cat its gradients; rank r: fused step on its padded
     # local buffer with the nd pieces r; then the all-gather copy-out
     lay = oracle.fsdp2_layout(shapes, nd)

@@ -213,7 +213,7 @@ def test_fused_step_output_may_be_the_slot_of_the_full_buffer(path):
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("nd", [1, 3, 8])
-def test_flat_pack_matches_oracle(dtype, nd):
+def test_flat_pack_matches_oracle(dtype, nd, path):
     rng = np.random.default_rng(nd)
     numels = [int(x) for x in rng.integers(0, 5000, size=150)] + [1 << 20, 3, 0, 77777]
     shifts = [int(s) for s in rng.integers(0, 4, size=len(numels))]
@@ -242,7 +242,7 @@ def test_flat_pack_matches_oracle(dtype, nd):
             assert_bits(ha.view(np.uint8), b.view(np.uint8), "piece")
 
 
-def test_flat_pack_misaligned_destination_segments():
+def test_flat_pack_misaligned_destination_segments(path):
     # element offsets that are odd make source and destination incongruent
     numels = [1, 2, 3, 5, 8, 13, 21, 34, 55, 89, 144, 233, 377, 610, 987, 1597, 2584]
     host = [synth.host_fill(synth.normal_stream(1, (97, k), 1.0), 0, n, "bf16")
@@ -269,7 +269,7 @@ def test_worked_example_on_gpu():
 
 @pytest.mark.parametrize("nd", [1, 2, 3, 8])
 @pytest.mark.parametrize("S", [1, 5, 1000, (1 << 20) + 3])
-def test_ag_unpack_matches_oracle(nd, S):
+def test_ag_unpack_matches_oracle(nd, S, path):
     shards_h = [synth.host_fill(synth.normal_stream(nd, (96, q, S), 0.02), 0, S, "bf16")
                 for q in range(nd)]
     shards = [dev_bf16(h, q % 3) for q, h in enumerate(shards_h)]
@@ -296,7 +296,7 @@ def test_ag_unpack_skips_the_rank_already_in_place():
     assert_bits(host_bf16(full), np.concatenate(shards_h), "full")
 
 
-def test_ag_unpack_views_are_the_unit_tensors():
+def test_ag_unpack_views_are_the_unit_tensors(path):
     shapes = [(4096, 11008), (11008,), (3, 5), (4096,)]
     numels = [int(np.prod(s)) for s in shapes]
     nd = 8
@@ -312,6 +312,29 @@ def test_ag_unpack_views_are_the_unit_tensors():
     for v, h, s in zip(views, host, shapes):
         assert tuple(v.shape) == s
         assert_bits(host_bf16(v).reshape(-1), h, "view")
+
+
+@pytest.mark.parametrize("shift", [0, 3, 5])
+def test_bulk_copy_with_congruent_unaligned_ends(shift, path):
+    """Sources and destinations congruent modulo 16 bytes but not aligned:
+    the bulk copy takes the aligned body, the vector copy the head and tail
+    bytes; more than 64 bulk ranges in one call flush mid-way; chunk counts
+    that do not divide the grid evenly."""
+    nd = 8
+    numels = [8 * 16384 + 8 * k + 5 for k in range(70)] + [3 * 1024 * 1024 + 1]
+    host = [synth.host_fill(synth.normal_stream(5, (93, k), 0.02), 0, n, "bf16")
+            for k, n in enumerate(numels)]
+    # every source starts `shift` elements into its allocation; the
+    # destination offsets follow the layout, so some ranges are congruent
+    flat = ss.fsdp_flat_pack([dev_bf16(h, shift) for h in host], nd)
+    want, lay = oracle.flat_pack(host, nd)
+    shards = [flat[r * lay.shard:(r + 1) * lay.shard].clone() for r in range(nd)]
+    full = torch.empty(lay.padded, dtype=torch.bfloat16, device=DEV)
+    ss.fsdp_ag_unpack(shards, full)
+    torch.cuda.synchronize()
+    assert_bits(host_bf16(flat), want, "flat")
+    assert_bits(host_bf16(full), want, "gathered")
+    assert ss.device_status() == 0
 
 
 # ----------------------------------------------------------- accumulation
