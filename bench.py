@@ -348,6 +348,8 @@ def run_ours(args):
     traffic_per_elem = (None if args.layers or args.kernel_path != "auto" or args.tma_stages
                         else profiled_traffic(args.workload))
 
+    pack = _time_flat_pack(torch, ss, w, u, nd if F == nd else F, dev, stream)
+
     # end to end through the public API: pinned host inputs copied in every
     # step, the gathered unit read back every step
     e2e = None
@@ -386,7 +388,8 @@ def run_ours(args):
                         "fused_ms": round(fused_avg, 4),
                         "fused_gbs": round(achieved, 1),
                         "ag_ms": round(ag_avg, 4),
-                        "ag_gbs": round(ag_bytes / (ag_avg / 1e3) / 1e9, 1)},
+                        "ag_gbs": round(ag_bytes / (ag_avg / 1e3) / 1e9, 1),
+                        **pack},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "peak_source": ("measured: MEASURED_PEAKS.json hbm_gbs (copy, burst)"
@@ -405,6 +408,35 @@ def run_ours(args):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def _time_flat_pack(torch, ss, w, u, nd, dev, stream, reps=20):
+    """flat_pack of one unit's tensors (a layer unit of the workload) into its
+    padded FlatParameter, timed on its own outside the step: the one-time
+    layout copy of every unit.  2 B read + 2 B written per element."""
+    import synth
+    shapes = w.units[u]
+    tensors = []
+    for k, sh in enumerate(shapes):
+        t = torch.empty(sh, dtype=torch.bfloat16, device=dev)
+        synth.dev_fill(w.peer_shard_stream(2, k, u), t.view(-1))
+        tensors.append(t)
+    lay = ss.fsdp_layout([t.numel() for t in tensors], nd)
+    flat = torch.empty(lay.padded, dtype=torch.bfloat16, device=dev)
+    for _ in range(3):
+        ss.fsdp_flat_pack(tensors, nd, flat=flat)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(reps):
+        ss.fsdp_flat_pack(tensors, nd, flat=flat)
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / reps
+    bytes_ = 4 * lay.total
+    return {"flat_pack_ms": round(ms, 4), "flat_pack_gbs": round(bytes_ / (ms / 1e3) / 1e9, 1),
+            "flat_pack_elements": lay.total}
 
 
 def run_e2e(args, torch, ss, opt, peers, full, u, r, nd, stream, step_bytes):
