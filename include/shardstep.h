@@ -366,6 +366,49 @@ int ddp_bucket_allreduce_avg(const uint16_t* const* rank_grads, int32_t nd,
                              const int64_t* bucket_offsets, int32_t first, int32_t count,
                              uint16_t* out, void* stream);
 
+/* ---------------------------------------------- DDP bucket readiness
+ * Host only.  [P3] section 4.2: a bucket is all-reduced as soon as every
+ * gradient in it is ready, so the buckets' reductions overlap the rest of
+ * backward; [P3] section 4.2 also names the failure: a parameter that the
+ * forward pass did not use never gets a gradient, its bucket never fills and
+ * the all-reduce waits forever (the case find_unused_parameters covers).
+ * Reading: the N_d emulated ranks (host threads) mark each parameter's
+ * gradient ready; a caller waits for a bucket on the host with a limit and
+ * launches its all-reduce only when every rank has marked every parameter
+ * in it.  A wait that runs out returns TIMEOUT and names one missing
+ * (rank, parameter); no kernel is launched for the bucket and nothing waits
+ * on the GPU.  The table lives in caller-provided host memory of
+ * ddp_ready_bytes() bytes, 8-byte aligned; marks from several threads are
+ * atomic; a wait may run concurrently with marks. */
+
+/* Bytes of the table for n_params parameters in n_buckets buckets and nd
+ * ranks; -1 for invalid sizes. */
+int64_t ddp_ready_bytes(int32_t n_params, int32_t n_buckets, int32_t nd);
+
+/* Sets up the table: bucket_of_param[n_params] (host, from ddp_bucket_plan)
+ * gives each parameter's bucket; every (rank, parameter) starts unmarked.
+ * Errors: INVALID (NULL, misaligned, bucket index out of range), CAPACITY
+ * (table_bytes too small). */
+int ddp_ready_init(void* table, int64_t table_bytes, const int32_t* bucket_of_param,
+                   int32_t n_params, int32_t n_buckets, int32_t nd);
+
+/* Rank `rank` has the gradient of parameter `param`.  *bucket_done (may be
+ * NULL) receives the bucket this mark completed on all ranks, else -1.
+ * Errors: INVALID (uninitialised table, out of range, marked twice). */
+int ddp_ready_mark(void* table, int32_t rank, int32_t param, int32_t* bucket_done);
+
+/* Waits up to timeout_us microseconds (host, sleeping between checks) until
+ * every rank has marked every parameter of `bucket`.  OK when it has;
+ * TIMEOUT otherwise, with *missing_rank / *missing_param (either may be NULL)
+ * naming one (rank, parameter) that never arrived (-1 when ready).  Errors:
+ * INVALID. */
+int ddp_ready_wait(void* table, int32_t bucket, int64_t timeout_us, int32_t* missing_rank,
+                   int32_t* missing_param);
+
+/* Unmarks everything for the next iteration (no marks or waits may run
+ * concurrently).  Errors: INVALID. */
+int ddp_ready_reset(void* table);
+
 /* --------------------------------------------------------- ledger */
 
 /* Model-state bytes per GPU ([P1] ZeRO figure; [P3] section 7), 16-bit

@@ -415,6 +415,69 @@ def ddp_bucket_allreduce_avg(rank_grads, bucket_offsets, out, first: int = 0,
     return out
 
 
+class BucketNotReady(TimeoutError):
+    """A bucket's wait ran out: `rank` never marked `param` ready."""
+
+    def __init__(self, msg, bucket, rank, param):
+        super().__init__(msg)
+        self.bucket, self.rank, self.param = bucket, rank, param
+
+
+class BucketReadiness:
+    """Host-side readiness of the DDP buckets across N_d emulated ranks
+    (libshardstep's ddp_ready_*): ranks -- host threads -- mark parameters
+    whose gradients they have; a bucket's all-reduce is launched only after
+    ``wait`` saw every rank's every parameter of it.  Marks and waits release
+    the interpreter lock, so rank threads run while a caller waits."""
+
+    def __init__(self, bucket_of_param, n_buckets: int, nd: int):
+        L = _capi.lib()
+        n = int(L.ddp_ready_bytes(len(bucket_of_param), n_buckets, nd))
+        if n < 0:
+            raise ValueError("bad parameter / bucket / rank counts")
+        self._buf = (ctypes.c_uint64 * ((n + 7) // 8))()     # 8-byte aligned host memory
+        self._ptr = ctypes.c_void_p(ctypes.addressof(self._buf))
+        self.n_buckets, self.nd = n_buckets, nd
+        bop = (_capi.c_i32 * max(1, len(bucket_of_param)))(*[int(b) for b in bucket_of_param])
+        _capi.check("ddp_ready_init", L.ddp_ready_init(self._ptr, n, bop, len(bucket_of_param),
+                                                       n_buckets, nd))
+
+    def mark(self, rank: int, param: int):
+        """Rank `rank` has param's gradient; returns the bucket this completed
+        on every rank, or None."""
+        done = _capi.c_i32(-1)
+        _capi.check("ddp_ready_mark", _capi.lib().ddp_ready_mark(self._ptr, rank, param,
+                                                                 ctypes.byref(done)))
+        return done.value if done.value >= 0 else None
+
+    def wait(self, bucket: int, timeout_s: float) -> None:
+        """Return once the bucket is ready; raise BucketNotReady after
+        timeout_s seconds, naming a (rank, parameter) that never arrived."""
+        mr, mp = _capi.c_i32(-1), _capi.c_i32(-1)
+        L = _capi.lib()
+        rc = L.ddp_ready_wait(self._ptr, bucket, int(timeout_s * 1e6), ctypes.byref(mr),
+                              ctypes.byref(mp))
+        if rc == _capi.ERR_TIMEOUT:
+            raise BucketNotReady(L.shardstep_last_error().decode(), bucket, mr.value, mp.value)
+        _capi.check("ddp_ready_wait", rc)
+
+    def reset(self) -> None:
+        _capi.check("ddp_ready_reset", _capi.lib().ddp_ready_reset(self._ptr))
+
+
+def ddp_allreduce_as_ready(rank_grads, bucket_offsets, out, ready: BucketReadiness,
+                           timeout_s: float = 10.0, stream=None):
+    """Bucket by bucket, in bucket order: wait on the host until every rank
+    marked the bucket's gradients, then launch its all-reduce average.  A
+    bucket that never fills raises BucketNotReady before anything is launched
+    for it (the buckets before it are already reduced)."""
+    for b in range(len(bucket_offsets) - 1):
+        ready.wait(b, timeout_s)
+        ddp_bucket_allreduce_avg(rank_grads, bucket_offsets, out, first=b, count=1,
+                                 stream=stream)
+    return out
+
+
 # ---------------------------------------------------------------- ledger
 
 def state_bytes(psi: float, nd: int, stage: int, k: float = 12.0) -> float:

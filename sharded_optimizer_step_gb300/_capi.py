@@ -89,6 +89,11 @@ SIGNATURES = {
     "fsdp_reshard_plan": (c_i32, [c_i64, c_i32, c_i32, c_i32, ctypes.POINTER(CkptPiece), c_i32,
                                   P_i32]),
     "shardstep_last_error": (ctypes.c_char_p, []),
+    "ddp_ready_bytes": (c_i64, [c_i32, c_i32, c_i32]),
+    "ddp_ready_init": (c_i32, [c_vp, c_i64, c_vp, c_i32, c_i32, c_i32]),
+    "ddp_ready_mark": (c_i32, [c_vp, c_i32, c_i32, c_vp]),
+    "ddp_ready_wait": (c_i32, [c_vp, c_i32, c_i64, c_vp, c_vp]),
+    "ddp_ready_reset": (c_i32, [c_vp]),
     "shardstep_set_fused_path": (c_i32, [c_i32]),
     "shardstep_set_tma_stages": (c_i32, [c_i32]),
     "shardstep_set_dependent_launch": (c_i32, [c_i32]),

@@ -169,6 +169,19 @@ int ckpt_fail(int code, const char* fmt, const char* a, long long b) {
     return fail(code, fmt, a, b);
 }
 
+// Error reporting for the host-only translation units (bucket readiness).
+int ready_fail(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_error = buf;
+    return code;
+}
+
+int ready_ok() { return ok(); }
+
 int device_sms() {
     static std::atomic<int> cache[256];
     int dev = 0;
