@@ -56,8 +56,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--e2e-steps", type=int, default=3)
-    ap.add_argument("--e2e-chunks", type=int, default=4)
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-chunks", type=int, default=8)
     ap.add_argument("--e2e-streams", type=int, default=4)
     ap.add_argument("--workload", choices=sorted(WORKLOADS) + [FSDP2_WORKLOAD, CKPT_WORKLOAD,
                                                              ACCUM_WORKLOAD, DDP_WORKLOAD],
@@ -442,8 +442,12 @@ def _time_flat_pack(torch, ss, w, u, nd, dev, stream, reps=20):
 def run_e2e(args, torch, ss, opt, peers, full, u, r, nd, stream, step_bytes):
     """Host-resident gradients and peer shards copied in every step, the
     gathered unit copied out.  The shard is cut into chunks: each chunk's 8
-    contributions are copied on a pool of copy streams while the fused
-    update of the previous chunk runs on the compute stream."""
+    contributions are copied on a pool of copy streams while the fused update
+    of the previous chunk runs on the compute stream.  Steps overlap as far
+    as the buffers allow: a chunk's gradient buffers are refilled as soon as
+    the previous step's update of that chunk is done, the peers' shards once
+    the previous all-gather has read them, and the gathered unit is read
+    back on its own stream while the next step's copies run."""
     S = opt.shard_total
     host_g = [torch.empty(S, dtype=torch.bfloat16, pin_memory=True) for _ in range(nd)]
     for q in range(nd):
@@ -461,9 +465,17 @@ def run_e2e(args, torch, ss, opt, peers, full, u, r, nd, stream, step_bytes):
     step8 = -(-S // (8 * n_chunks)) * 8
     bounds = [min(S, c * step8) for c in range(n_chunks)] + [S]
     copy_streams = [torch.cuda.Stream(device=stream.device) for _ in range(max(1, args.e2e_streams))]
+    d2h_stream = torch.cuda.Stream(device=stream.device)
+    # events of the previous step that free a buffer for the next one
+    free = {"chunk": [None] * n_chunks, "peers": None, "full": None}
 
-    def e2e_step():
-        prev = stream.record_event()          # last step's kernels are done with the buffers
+    def after(cs, ev, start):
+        if ev is not None:
+            cs.wait_event(ev)
+        if start is not None:
+            cs.wait_event(start)
+
+    def e2e_step(start=None):
         k = 0
         chunk_ready = []
         for c in range(n_chunks):
@@ -472,7 +484,7 @@ def run_e2e(args, torch, ss, opt, peers, full, u, r, nd, stream, step_bytes):
             for q in range(nd):
                 cs = copy_streams[k % len(copy_streams)]
                 k += 1
-                cs.wait_event(prev)
+                after(cs, free["chunk"][c], start)
                 with torch.cuda.stream(cs):
                     opt.grad_in[q][a:b].copy_(host_g[q][a:b], non_blocking=True)
                 evs.append(cs.record_event())
@@ -482,7 +494,7 @@ def run_e2e(args, torch, ss, opt, peers, full, u, r, nd, stream, step_bytes):
             if q != r:
                 cs = copy_streams[k % len(copy_streams)]
                 k += 1
-                cs.wait_event(prev)
+                after(cs, free["peers"], start)
                 with torch.cuda.stream(cs):
                     peers[q].copy_(host_p[q], non_blocking=True)
                 peer_evs.append(cs.record_event())
@@ -491,18 +503,27 @@ def run_e2e(args, torch, ss, opt, peers, full, u, r, nd, stream, step_bytes):
             for e in chunk_ready[c]:
                 stream.wait_event(e)
             opt.update_range(bounds[c], bounds[c + 1], stream=stream)
+            free["chunk"][c] = stream.record_event()
         for e in peer_evs:
             stream.wait_event(e)
+        if free["full"] is not None:
+            stream.wait_event(free["full"])      # the previous read-back is done with `full`
         opt.gather_unit(u, peers, full, stream=stream)
-        host_out.copy_(full, non_blocking=True)
+        gathered = stream.record_event()
+        free["peers"] = gathered
+        d2h_stream.wait_event(gathered)
+        with torch.cuda.stream(d2h_stream):
+            host_out.copy_(full, non_blocking=True)
+        free["full"] = d2h_stream.record_event()
 
     e2e_step()
     torch.cuda.synchronize()
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
     a.record(stream)
-    for _ in range(args.e2e_steps):
-        e2e_step()
+    for k in range(args.e2e_steps):
+        e2e_step(a if k == 0 else None)
+    stream.wait_event(free["full"])              # the last read-back is inside the timing
     b.record(stream)
     torch.cuda.synchronize()
     sec = a.elapsed_time(b) / 1e3
@@ -511,7 +532,8 @@ def run_e2e(args, torch, ss, opt, peers, full, u, r, nd, stream, step_bytes):
             "h2d_gbs": round(h2d * args.e2e_steps / sec / 1e9, 1),
             "bytes": step_bytes * args.e2e_steps, "seconds": sec,
             "path": (f"pinned host buffers -> {len(copy_streams)} copy streams, shard in "
-                     f"{n_chunks} chunks overlapped with the fused update; C-ABI calls")}
+                     f"{n_chunks} chunks overlapped with the fused update; steps overlap per "
+                     f"chunk; read-back on its own stream; C-ABI calls")}
 
 
 # ------------------------------------------------------- CPU baseline / reference
