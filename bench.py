@@ -354,9 +354,23 @@ def run_ours(args):
     # step, the gathered unit read back every step
     e2e = None
     if not args.no_e2e and not scaled:
-        e2e = run_e2e(args, torch, ss, opt, peers, full, u, r, nd, stream, step_bytes)
-        e2e["value"] = round(allreduce_sum(world, e2e.pop("bytes"))
-                             / allreduce_max(world, e2e.pop("seconds")) / 1e9, 1)
+        try:
+            e2e = run_e2e(args, torch, ss, opt, peers, full, u, r, nd, stream, step_bytes)
+            failed = ""
+        except RuntimeError as exc:          # e.g. the host cannot pin this much memory
+            failed = str(exc).splitlines()[0][:200]
+            torch.cuda.synchronize()
+        # every rank takes part in the same reductions, whatever happened
+        n_failed = allreduce_sum(world, 1.0 if failed else 0.0)
+        got_bytes = allreduce_sum(world, 0.0 if failed else float(e2e["bytes"]))
+        got_sec = allreduce_max(world, 0.0 if failed else e2e["seconds"])
+        if n_failed:
+            e2e = {"value": None, "unit": "GB/s", "unavailable":
+                   f"end-to-end leg failed on {int(n_failed)} rank(s): {failed or 'another rank'}"}
+        else:
+            e2e.pop("bytes")
+            e2e.pop("seconds")
+            e2e["value"] = round(got_bytes / got_sec / 1e9, 1)
 
     cpu = None
     if rank == 0 and not args.no_cpu:
