@@ -518,7 +518,10 @@ int fsdp_reshard_plan(int64_t total, int32_t old_nd, int32_t new_nd, int32_t new
  * in shared memory); _REGISTER uses only the register-staged kernels;
  * _AUTO (default) uses the TMA-staged kernels where they measured faster:
  * the fused steps at N_d >= 3, the bucket all-reduce at N_d >= 3 on buckets
- * of at least 32M elements, the accumulation and the check always.  All give
+ * of at least 32M elements, the accumulation and the check always.  The
+ * copies (flat_pack, ag_unpack, FSDP2 chunk-cat / copy-out) send the
+ * 16-byte-aligned body of every range to a 16-byte vector copy except under
+ * _REGISTER, which keeps them on the generic segment copy.  All give
  * bit-identical results.  Returns the previous setting, or INVALID for an
  * unknown value. */
 #define SHARDSTEP_PATH_AUTO 0

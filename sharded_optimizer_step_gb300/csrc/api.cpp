@@ -34,13 +34,10 @@ std::atomic<int> g_dependent_launch{1};
 //     0.924 ms with TMA from 8M elements; in 3 buckets 0.894 vs 0.880 ms);
 //   accumulation and the non-finite check: always (6.5 vs 6.0 and 7.3 vs
 //     6.9 TB/s).
-//   copies: ranges of at least kBulkMinBytes (n counts bytes here).
-enum class TmaOp { kStep, kAllReduce, kAccumulate, kCheck, kCopy };
-constexpr int64_t kBulkMinBytes = 65536;
+enum class TmaOp { kStep, kAllReduce, kAccumulate, kCheck };
 bool use_tma(TmaOp op, int64_t n, int nd = 0) {
     const int path = g_fused_path.load(std::memory_order_relaxed);
     if (path == SHARDSTEP_PATH_REGISTER) return false;
-    if (op == TmaOp::kCopy) return n >= (path == SHARDSTEP_PATH_TMA ? 16 : kBulkMinBytes);
     if (n < kTmaMinElements) return false;
     if (path == SHARDSTEP_PATH_TMA) return true;
     switch (op) {
@@ -314,9 +311,15 @@ int fsdp_views(const int64_t* numels, int32_t n, int32_t nd, int32_t rank, void*
 
 // Turns (src, dst, bytes) triples into copy-kernel launches of <= kMaxCopySegs.
 namespace {
+// Whether the 16-byte-aligned body of a copy range goes to copy16 (every
+// kernel choice but PATH_REGISTER, which keeps all copies on copy_segments).
+bool use_copy16() {
+    return g_fused_path.load(std::memory_order_relaxed) != SHARDSTEP_PATH_REGISTER;
+}
+
 struct CopyBatcher {
     CopyTable t;
-    BulkTable bt;
+    AlignedTable bt;
     cudaStream_t stream;
     int rc = SHARDSTEP_OK;
     explicit CopyBatcher(cudaStream_t s) : stream(s) {
@@ -326,34 +329,34 @@ struct CopyBatcher {
         bt.total_chunks = 0;
     }
     // A range whose source and destination are congruent modulo 16 bytes
-    // goes to the bulk copy for its 16-byte-aligned body (when the kernel
-    // choice allows it); the unaligned head and tail bytes, zero fills and
-    // everything else go to the vector copy.
+    // goes to copy16 for its 16-byte-aligned body (unless the register path
+    // is forced); the unaligned head and tail bytes, zero fills and
+    // everything else go to copy_segments.
     void add(const void* src, void* dst, int64_t bytes) {
         if (bytes <= 0 || rc != SHARDSTEP_OK) return;
         const uintptr_t d = reinterpret_cast<uintptr_t>(dst);
         if (src != nullptr && ((reinterpret_cast<uintptr_t>(src) ^ d) & 15u) == 0) {
             const int64_t head = static_cast<int64_t>((16 - d % 16) % 16);
             const int64_t body = bytes > head ? ((bytes - head) & ~int64_t{15}) : 0;
-            if (use_tma(TmaOp::kCopy, body)) {
+            if (body > 0 && use_copy16()) {
                 const char* s8 = static_cast<const char*>(src);
                 char* d8 = static_cast<char*>(dst);
                 add_vector(s8, d8, head);
-                add_bulk(s8 + head, d8 + head, body);
+                add_aligned(s8 + head, d8 + head, body);
                 add_vector(s8 + head + body, d8 + head + body, bytes - head - body);
                 return;
             }
         }
         add_vector(src, dst, bytes);
     }
-    void add_bulk(const char* src, char* dst, int64_t bytes) {
-        BulkSeg& s = bt.s[bt.n];
+    void add_aligned(const char* src, char* dst, int64_t bytes) {
+        AlignedSeg& s = bt.s[bt.n];
         s.src = src;
         s.dst = dst;
         s.bytes = bytes;
         s.chunk0 = bt.total_chunks;
-        bt.total_chunks += (bytes + kBulkChunk - 1) / kBulkChunk;
-        if (++bt.n == kMaxCopySegs) flush_bulk();
+        bt.total_chunks += (bytes + kAlignedChunk - 1) / kAlignedChunk;
+        if (++bt.n == kMaxCopySegs) flush_aligned();
     }
     void add_vector(const void* src, void* dst, int64_t bytes) {
         if (bytes <= 0 || rc != SHARDSTEP_OK) return;
@@ -381,15 +384,15 @@ struct CopyBatcher {
         t.n = 0;
         t.total_chunks = 0;
     }
-    void flush_bulk() {
+    void flush_aligned() {
         if (bt.n == 0 || rc != SHARDSTEP_OK) return;
-        cudaError_t e = launch_bulk_copy(bt, stream);
-        if (e != cudaSuccess) rc = cuda_fail(e, "bulk copy kernel launch");
+        cudaError_t e = launch_copy16(bt, stream);
+        if (e != cudaSuccess) rc = cuda_fail(e, "aligned copy kernel launch");
         bt.n = 0;
         bt.total_chunks = 0;
     }
     void flush() {
-        flush_bulk();
+        flush_aligned();
         flush_vector();
     }
 };

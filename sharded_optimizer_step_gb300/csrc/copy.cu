@@ -1,5 +1,14 @@
-// Copy-shaped kernels: the batched segment copy behind fsdp_flat_pack and
-// fsdp_ag_unpack, and the micro-batch gradient accumulation.
+// Copy-shaped kernels: the batched segment copies behind fsdp_flat_pack,
+// fsdp_ag_unpack and the FSDP2 chunk-cat / copy-out, and the register-staged
+// micro-batch gradient accumulation.
+//
+// Aligned copy (copy16): ranges whose source, destination and size are all
+// multiples of 16 bytes, one block per 16 KB chunk (256 threads x 4
+// vectors, streaming loads and stores), the chunks of every range in one
+// grid that the hardware schedules at full occupancy (32 registers).  On
+// GB300 it moved a 405 MB all-gather at 6.82 TB/s, against 6.19 TB/s for
+// the same copy staged through shared memory by bulk copies (one persistent
+// CTA per SM) and 6.67 TB/s for torch's device copy of the same size.
 //
 // Segment copy: one launch moves up to kMaxCopySegs byte ranges.  Each
 // segment is cut into chunks of 1024 vectors; blocks stride over the chunks
@@ -88,6 +97,33 @@ __global__ void __launch_bounds__(kThreads) copy_segments(CopyTable t) {
     }
 }
 
+__global__ void __launch_bounds__(kThreads, 8) copy16(AlignedTable t) {
+    const int64_t c = blockIdx.x;
+    int lo = 0, hi = t.n - 1;  // the range owning chunk c (chunk0 increasing)
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (t.s[mid].chunk0 <= c) lo = mid;
+        else hi = mid - 1;
+    }
+    const AlignedSeg& sg = t.s[lo];
+    constexpr int kVecs = kAlignedChunk / 16;  // 1024 = 256 threads x 4
+    const int64_t v0 = (c - sg.chunk0) * kVecs;
+    const int64_t nv = sg.bytes / 16;
+    const uint4* src = reinterpret_cast<const uint4*>(sg.src);
+    uint4* dst = reinterpret_cast<uint4*>(sg.dst);
+    uint4 r[kVecs / kThreads];
+#pragma unroll
+    for (int u = 0; u < kVecs / kThreads; ++u) {
+        const int64_t k = v0 + u * kThreads + threadIdx.x;
+        if (k < nv) r[u] = ld_once(src + k);
+    }
+#pragma unroll
+    for (int u = 0; u < kVecs / kThreads; ++u) {
+        const int64_t k = v0 + u * kThreads + threadIdx.x;
+        if (k < nv) st_stream(dst + k, r[u]);
+    }
+}
+
 // ------------------------------------------------------- accumulation
 
 template <bool FIRST>
@@ -149,6 +185,12 @@ cudaError_t launch_copy(const CopyTable& t, cudaStream_t stream) {
                         resident_blocks(reinterpret_cast<const void*>(copy_segments), kThreads);
     const int64_t g = t.total_chunks < cap ? t.total_chunks : cap;
     copy_segments<<<static_cast<unsigned>(g < 1 ? 1 : g), kThreads, 0, stream>>>(t);
+    note_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_copy16(const AlignedTable& t, cudaStream_t stream) {
+    copy16<<<static_cast<unsigned>(t.total_chunks), kThreads, 0, stream>>>(t);
     note_launch();
     return cudaGetLastError();
 }

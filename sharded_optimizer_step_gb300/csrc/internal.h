@@ -59,18 +59,18 @@ struct CopyTable {
 };
 constexpr int kCopyVecsPerChunk = 1024;  // 256 threads x 4
 
-// Byte ranges for the TMA-staged copy: source, destination and size all
-// multiples of 16 bytes; cut into tiles of kBulkChunk bytes (2048 vectors of
-// 16 bytes, one staged tile each).
-constexpr int kBulkChunk = 32768;
-struct BulkSeg {
+// Byte ranges for the aligned copy: source, destination and size all
+// multiples of 16 bytes; cut into chunks of kAlignedChunk bytes, one block
+// each.
+constexpr int kAlignedChunk = 16384;
+struct AlignedSeg {
     const char* src;
     char* dst;
     int64_t bytes;
-    int64_t chunk0;  // first chunk index of this segment in the launch
+    int64_t chunk0;  // first chunk index of this range in the launch
 };
-struct BulkTable {
-    BulkSeg s[kMaxCopySegs];
+struct AlignedTable {
+    AlignedSeg s[kMaxCopySegs];
     int32_t n;
     int64_t total_chunks;
 };
@@ -143,9 +143,8 @@ constexpr int64_t kTmaMinElements = 4096;
 cudaError_t launch_allreduce_avg(const PtrTable& tab, int nd, int64_t n, uint16_t* out,
                                  const MeanOp& mo, bool vec, bool pdl, cudaStream_t stream);
 cudaError_t launch_copy(const CopyTable& t, cudaStream_t stream);
-// TMA-staged segment copy (step_tma.cu): tiles brought into shared memory by
-// cp.async.bulk, written out by the consumer warps.
-cudaError_t launch_bulk_copy(const BulkTable& t, cudaStream_t stream);
+// Aligned copy (copy.cu): one block per 16 KB chunk of 16-byte vectors.
+cudaError_t launch_copy16(const AlignedTable& t, cudaStream_t stream);
 cudaError_t launch_accumulate(const uint16_t* g, float* acc, int64_t n, float scale, bool first,
                               bool vec, cudaStream_t stream);
 

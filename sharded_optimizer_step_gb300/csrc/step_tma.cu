@@ -1,4 +1,4 @@
-// TMA bulk-staged streaming kernels: the fused sharded step (reduce-scatter
+// TMA-staged streaming kernels: the fused sharded step (reduce-scatter
 // average + AdamW + bf16 cast), the micro-batch gradient accumulation, the
 // DDP bucket all-reduce average and the gradient scaler's non-finite check.
 // They are the default path whenever every source is 16-byte aligned and at
@@ -456,63 +456,6 @@ struct CheckOp {
     }
 };
 
-// Segment copy: byte ranges whose source, destination and size are multiples
-// of 16 bytes.  Elements are 16-byte vectors; segment k owns tiles
-// [chunk0_k, chunk0_k + ceil(vectors_k / kTile)) of the index space, so no
-// tile straddles two segments and a segment's last tile may be short.  The
-// producer brings each tile in with one bulk copy; the consumers write it out
-// with streaming stores (TMA stores for both directions measured slower:
-// 0.133 vs 0.130 ms for a 405 MB all-gather).
-struct CopyOp {
-    BulkTable t;
-
-    struct State {};
-    __device__ bool skipped() const { return false; }
-    __device__ State init() const { return State{}; }
-    __host__ __device__ uint32_t stage_bytes() const { return kTile * 16u; }
-    // segment of tile e0 / kTile (chunk0 increasing), and the tile's vectors
-    __device__ __forceinline__ const BulkSeg& seg_of(int64_t e0) const {
-        const int64_t tile = e0 / kTile;
-        int lo = 0, hi = t.n - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (t.s[mid].chunk0 <= tile) lo = mid;
-            else hi = mid - 1;
-        }
-        return t.s[lo];
-    }
-    __device__ __forceinline__ uint32_t vecs(const BulkSeg& sg, int64_t e0) const {
-        const int64_t left = sg.bytes / 16 - (e0 - sg.chunk0 * kTile);
-        return static_cast<uint32_t>(left < kTile ? left : kTile);
-    }
-    __device__ uint32_t tx_bytes(int64_t e0, uint32_t) const { return vecs(seg_of(e0), e0) * 16u; }
-    __device__ void issue(uint8_t* st, int64_t e0, uint32_t, uint64_t* bar) const {
-        const BulkSeg& sg = seg_of(e0);
-        bulk_load(st, sg.src + (e0 - sg.chunk0 * kTile) * 16, vecs(sg, e0) * 16u, bar);
-    }
-    __device__ void consume(const uint8_t* st, int64_t e0, int e, State&) const {
-        const BulkSeg& sg = seg_of(e0);
-        const int nv = static_cast<int>(vecs(sg, e0));
-        char* dst = sg.dst + (e0 - sg.chunk0 * kTile) * 16;
-        // 4 vectors per thread, spaced a warp apart so each store
-        // instruction of a warp writes 512 contiguous bytes
-        const int lane = e & 127, base = (e >> 7) << 7;
-        uint4 v[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int x = base + (lane >> 2) + 32 * k;
-            if (x < nv) v[k] = *reinterpret_cast<const uint4*>(st + x * 16);
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int x = base + (lane >> 2) + 32 * k;
-            if (x < nv) stcs16(dst + x * 16, v[k]);
-        }
-    }
-    __device__ void tail(int64_t, State&) const {}
-    __device__ void finish(State&, int) const {}
-};
-
 // --------------------------------------------------------------- launch
 
 std::atomic<int> g_stage_limit{0};  // 0: about kTargetInflight bytes of stages
@@ -629,10 +572,6 @@ cudaError_t launch_nonfinite_check_tma(const PtrTable& tab, int nd, int grad_typ
         case kGradF16: return launch_staged(CheckOp<kGradF16>{tab, nd, mo, found}, S, stream);
         default: return launch_staged(CheckOp<kGradBF16>{tab, nd, mo, found}, S, stream);
     }
-}
-
-cudaError_t launch_bulk_copy(const BulkTable& t, cudaStream_t stream) {
-    return launch_staged(CopyOp{t}, t.total_chunks * kTile, stream);
 }
 
 cudaError_t read_device_status(unsigned int* status, bool clear) {

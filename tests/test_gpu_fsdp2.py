@@ -38,9 +38,9 @@ def _built():
 
 @pytest.fixture(params=["auto", "register", "tma"])
 def path(request):
-    """Each kernel choice: auto, register-staged only (vector copies), and
-    TMA-staged wherever the arguments allow (bulk copies of every aligned
-    range)."""
+    """Each kernel choice: auto and tma (aligned copy bodies on the 16-byte
+    copy), and register-staged only (every copy on the generic vector
+    copy)."""
     prev = ss.set_fused_path(request.param)
     yield request.param
     ss.set_fused_path(prev)

@@ -291,7 +291,9 @@ def test_ag_unpack_skips_the_rank_already_in_place():
     shards[2] = full[2 * S:3 * S]
     before = ss.launch_count()
     ss.fsdp_ag_unpack(shards, full)
-    assert ss.launch_count() - before == 1
+    # one launch per copy kind at most: the 16-byte copy of aligned bodies,
+    # the vector copy of the rest (the shard in place is in neither)
+    assert 1 <= ss.launch_count() - before <= 2
     torch.cuda.synchronize()
     assert_bits(host_bf16(full), np.concatenate(shards_h), "full")
 
@@ -315,11 +317,11 @@ def test_ag_unpack_views_are_the_unit_tensors(path):
 
 
 @pytest.mark.parametrize("shift", [0, 3, 5])
-def test_bulk_copy_with_congruent_unaligned_ends(shift, path):
+def test_aligned_copy_with_congruent_unaligned_ends(shift, path):
     """Sources and destinations congruent modulo 16 bytes but not aligned:
-    the bulk copy takes the aligned body, the vector copy the head and tail
-    bytes; more than 64 bulk ranges in one call flush mid-way; chunk counts
-    that do not divide the grid evenly."""
+    the 16-byte copy takes the aligned body, the vector copy the head and
+    tail bytes; more than 64 aligned ranges in one call flush mid-way;
+    ranges whose last 16 KB chunk is short."""
     nd = 8
     numels = [8 * 16384 + 8 * k + 5 for k in range(70)] + [3 * 1024 * 1024 + 1]
     host = [synth.host_fill(synth.normal_stream(5, (93, k), 0.02), 0, n, "bf16")
