@@ -39,13 +39,16 @@ TMA_SOURCES = ["sharded_optimizer_step_gb300/csrc/step_tma.cu",
                "sharded_optimizer_step_gb300/csrc/common.cuh"]
 REGISTER_SOURCES = ["sharded_optimizer_step_gb300/csrc/step.cu",
                     "sharded_optimizer_step_gb300/csrc/common.cuh"]
+COPY_SOURCES = ["sharded_optimizer_step_gb300/csrc/copy.cu",
+                "sharded_optimizer_step_gb300/csrc/common.cuh"]
 # per bench line: the ncu summary of its dominant kernel (DRAM bytes per
 # element, recorded with the hash of the sources that kernel is built from)
 PROFILES = {
-    "llama_7b_rank0_nd8": ("fused_step_llama7b_rank_view.md", TMA_SOURCES),
-    "llama_7b_hybrid_nd16_f8_rank0": ("fused_step_llama7b_hybrid_nd16_f8.md", TMA_SOURCES),
-    "llama_7b_rank0_nd8_fp16_scaled": ("scaled_step_llama7b_rank_view_fp16.md", TMA_SOURCES),
-    "llama_1b_rank0_nd8_m4": ("accumulate_llama1b_rank_view_m4.md", TMA_SOURCES),
+    "llama_7b_rank0_nd8": ("fused_step_llama7b_rank_view.md", REGISTER_SOURCES),
+    "llama_7b_hybrid_nd16_f8_rank0": ("fused_step_llama7b_hybrid_nd16_f8.md", REGISTER_SOURCES),
+    "llama_7b_rank0_nd8_fp16_scaled": ("scaled_step_llama7b_rank_view_fp16.md",
+                                       REGISTER_SOURCES),
+    "llama_1b_rank0_nd8_m4": ("accumulate_llama1b_rank_view_m4.md", COPY_SOURCES),
     "ddp_nd8_buckets": ("ddp_buckets_nd8_adamw.md", REGISTER_SOURCES),
 }
 
@@ -135,10 +138,15 @@ def measured_peak():
 
 
 def kernel_source_hash(sources=TMA_SOURCES):
+    """Hash of the code in `sources` with comments and blank space removed, so
+    that a comment-only edit keeps a profile's figures valid."""
     h = hashlib.sha256()
     for rel in sources:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 
@@ -329,6 +337,7 @@ def run_ours(args):
     torch.cuda.nvtx.range_pop()
     barrier(world)
     launches = ss.launch_count() - launches0
+    fused_kernel = ss.last_kernel()     # the fused step is each step's last streaming call
     clk = clocks.stop()
     status = ss.device_status()
     if status:
@@ -408,8 +417,8 @@ def run_ours(args):
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "peak_source": ("measured: MEASURED_PEAKS.json hbm_gbs (copy, burst)"
                                          if peak_kind == "measured" else "fallback 6800 GB/s"),
-                         "kernel": f"staged_stream<AdamOp<{'f16' if scaled else 'bf16'}>> (TMA-staged, N_d = {nd}"
-                                   + (f", sharding factor {F})" if F != nd else ")"),
+                         "kernel": f"{fused_kernel}, N_d = {nd}"
+                                   + (f", sharding factor {F}" if F != nd else ""),
                          "algorithmic_bytes_per_launch": fused_bytes,
                          "traffic": (None if traffic_per_elem is None
                                      else round(traffic_per_elem * S))},
@@ -732,6 +741,7 @@ def run_fsdp2(args):
     torch.cuda.nvtx.range_pop()
     barrier(world)
     launches = ss.launch_count() - launches0
+    fused_kernel = ss.last_kernel()
     clk = clocks.stop()
     if ss.device_status():
         raise RuntimeError("a TMA-staged wait ran out during the timed steps")
@@ -766,7 +776,7 @@ def run_fsdp2(args):
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "peak_source": ("measured: MEASURED_PEAKS.json hbm_gbs (copy, burst)"
                                          if peak_kind == "measured" else "fallback 6800 GB/s"),
-                         "kernel": "staged_stream<AdamOp<bf16>> on one rank's local buffer",
+                         "kernel": f"{fused_kernel} on one rank's local buffer",
                          "algorithmic_bytes_per_launch": fused_launch, "traffic": None},
             "e2e": None, "gpu_launches": launches, "clocks": clk, "cpu_baseline": None,
         }))
@@ -984,12 +994,14 @@ def run_accum(args):
     fused_bytes = (4 * nd + 26) * S
     ag_bytes = 4 * Pu
     step_bytes = acc_bytes + fused_bytes + ag_bytes
+    kernel_names = {}
 
     def one_step(ev):
         if ev is not None:
             ev[0].record(stream)
         for j in range(M):
             ss.fsdp_grad_accumulate(micro[j], acc, inv_m, j == 0, stream=stream)
+        kernel_names["accumulate"] = ss.last_kernel()
         if ev is not None:
             ev[1].record(stream)
         opt.step(stream=stream)
@@ -1041,7 +1053,8 @@ def run_accum(args):
                     "fused_frac": round(fused_gbs / measured_peak()[0], 4),
                     "ag_ms": round(ag_ms, 4),
                     "ag_gbs": round(ag_bytes / (ag_ms / 1e3) / 1e9, 1)},
-        "roofline": _roofline(acc_gbs, f"staged_stream<AccumOp> (4 launches over {nd} x {S} elements)",
+        "roofline": _roofline(acc_gbs, f"{kernel_names['accumulate']} "
+                                       f"(4 launches over {nd} x {S} elements)",
                               acc_bytes // M, _traffic(ACCUM_WORKLOAD, nd * S, args)),
         "e2e": None, "e2e_note": "device-resident micro-batch gradients; the end-to-end "
                                  "line is the default workload's",
@@ -1176,15 +1189,18 @@ def run_ddp(args):
     adam_bytes = 28 * total
     step_bytes = ar_bytes + adam_bytes
     t = [0]
+    kernel_names = {}
 
     def one_step(ev):
         if ev is not None:
             ev[0].record(stream)
         ss.ddp_bucket_allreduce_avg(grads, boff, out, stream=stream)
+        kernel_names["allreduce"] = ss.last_kernel()
         if ev is not None:
             ev[1].record(stream)
         t[0] += 1
         ss.fsdp_rs_avg_adamw_cast([out], master, mm, vv, pb, hp, t[0], stream=stream)
+        kernel_names["adamw"] = ss.last_kernel()
         if ev is not None:
             ev[2].record(stream)
 
@@ -1245,13 +1261,11 @@ def run_ddp(args):
                     "allreduce_frac": round(ar_gbs / measured_peak()[0], 4),
                     "adamw_ms": round(adam_ms, 4), "adamw_gbs": round(adam_gbs, 1),
                     "allreduce_by_cap": by_cap},
-        "roofline": _roofline(adam_gbs, ("staged_stream<AdamOp<bf16>> at N_d = 1 (full AdamW)"
-                                         if args.kernel_path == "tma" else
-                                         "rs_adamw_cast_vec4<1, bf16> (register-staged full "
-                                         "AdamW; the TMA-staged kernel is slower at N_d = 1)"),
+        "roofline": _roofline(adam_gbs, f"{kernel_names['adamw']} at N_d = 1 (full AdamW)",
                               adam_bytes, _traffic(DDP_WORKLOAD, total, args)),
-        "roofline_allreduce": _roofline(ar_gbs, f"staged_stream<MeanOutOp> at N_d = 8 ({len(boff) - 1} "
-                                                f"launches, one per bucket)", ar_bytes),
+        "roofline_allreduce": _roofline(ar_gbs, f"{kernel_names['allreduce']} at N_d = 8 "
+                                                f"({len(boff) - 1} launches, one per bucket; "
+                                                f"the last bucket's kernel named)", ar_bytes),
         "e2e": None, "e2e_note": "device-resident gradients; the end-to-end line is the "
                                  "default workload's",
         "note": "buckets after the first of the call are launched as programmatic dependents "

@@ -170,14 +170,15 @@ int fsdp_grad_accumulate(const uint16_t* g, float* acc, int64_t n, float scale, 
  *   out_bf16         device, S bf16; may be the rank's slot of the full flat
  *                    parameter buffer (full + r*S).
  * The gradient inputs must not overlap any output; master, m, v and out_bf16
- * must not overlap one another.  Any alignment is accepted.  Kernels, by
- * decreasing speed: (1) TMA-staged -- needs S >= 4096, master / m / v and
- * every slice 16-byte aligned, out_bf16 8-byte aligned, and two stages of
- * 2048 x (N_d x grad bytes + 12) bytes within the per-block shared-memory
- * limit (N_d <= 21 for bf16, <= 10 for fp32 on GB300); (2) register-staged,
- * 4 elements per access -- needs state 16-byte, bf16 slices and out 8-byte,
- * fp32 slices 16-byte alignment; (3) one element per access.  All three
- * compute the same bits.  A TMA-staged launch whose internal wait runs out
+ * must not overlap one another.  Any alignment is accepted.  Kernels:
+ * (1) register-staged, 4 elements per access -- needs state 16-byte, bf16
+ * slices and out 8-byte, fp32 slices 16-byte alignment; the default where
+ * N_d is 1 to 5, 8 or 16 (16 not with fp32 slices); (2) TMA-staged --
+ * needs S >= 4096, master / m / v and every slice 16-byte aligned, out_bf16
+ * 8-byte aligned, and two stages of 2048 x (N_d x grad bytes + 12) bytes
+ * within the per-block shared-memory limit (N_d <= 21 for bf16, <= 10 for
+ * fp32 on GB300); the default for other N_d >= 3; (3) one element per
+ * access.  All three compute the same bits.  A TMA-staged launch whose internal wait runs out
  * (about 2 s) sets a bit in the device status word; see
  * shardstep_device_status. 
  * Errors: INVALID (null pointer, S < 0, step < 1, bad dtype, overlap),
@@ -517,9 +518,10 @@ int fsdp_reshard_plan(int64_t total, int32_t old_nd, int32_t new_nd, int32_t new
  * allow it (every source 16-byte aligned, at least 4096 elements, two stages
  * in shared memory); _REGISTER uses only the register-staged kernels;
  * _AUTO (default) uses the TMA-staged kernels where they measured faster:
- * the fused steps at N_d >= 3, the bucket all-reduce at N_d >= 3 on buckets
- * of at least 32M elements, the accumulation and the check always.  The
- * copies (flat_pack, ag_unpack, FSDP2 chunk-cat / copy-out) send the
+ * the fused steps at N_d = 6, 7, 9..15 and above 16 (and at 16 with fp32
+ * slices), the bucket all-reduce at N_d >= 3 on buckets of at least 32M
+ * elements, the check at N_d = 3, 5..7 and above 8, the accumulation never.
+ * The copies (flat_pack, ag_unpack, FSDP2 chunk-cat / copy-out) send the
  * 16-byte-aligned body of every range to a 16-byte vector copy except under
  * _REGISTER, which keeps them on the generic segment copy.  All give
  * bit-identical results.  Returns the previous setting, or INVALID for an
@@ -557,6 +559,13 @@ const char* shardstep_last_error(void);
 
 /* Kernels this library has launched in this process (all threads). */
 uint64_t shardstep_launch_count(void);
+
+/* Name of the kernel that the calling thread's last successful streaming
+ * call launched (fused steps, accumulation, non-finite check; for the bucket
+ * all-reduce, the kernel of its last non-empty bucket), e.g.
+ * "rs_adamw_cast_vec4<8, bf16> (register-staged)"; "" before the first.
+ * Host only; the string stays valid until the thread's next such call. */
+const char* shardstep_last_kernel(void);
 
 #ifdef __cplusplus
 }

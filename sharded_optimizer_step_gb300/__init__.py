@@ -21,7 +21,8 @@ from .build import build
 __all__ = [
     "build", "ShardstepError", "AdamW", "Layout", "fsdp_layout", "fsdp_flat_pack", "fsdp_views",
     "fsdp_grad_accumulate", "fsdp_rs_avg_adamw_cast", "fsdp_ag_unpack", "ddp_bucket_plan",
-    "ddp_bucket_allreduce_avg", "state_bytes", "comm_bytes", "launch_count", "MAX_ND",
+    "ddp_bucket_allreduce_avg", "state_bytes", "comm_bytes", "launch_count", "last_kernel",
+    "MAX_ND",
     "set_fused_path", "device_status", "fsdp_hybrid_rs_avg_adamw_cast", "hybrid_state_bytes",
     "hybrid_comm_bytes", "Fsdp2Layout", "fsdp2_layout", "fsdp2_local_views", "fsdp2_chunk_cat",
     "fsdp2_all_gather_copy_out",
@@ -496,8 +497,9 @@ def comm_bytes(psi: float, nd: int, kind: str, exact: bool = False) -> float:
 
 def set_fused_path(path: str) -> str:
     """Which kernels the streaming calls (fused steps, accumulation, bucket
-    all-reduce, non-finite check) may use: "auto" (TMA-staged when the
-    arguments allow), "register" (register-staged only) or "tma".  Returns
+    all-reduce, non-finite check) may use: "auto" (TMA-staged where it
+    measured faster and the arguments allow), "register" (register-staged
+    only) or "tma" (TMA-staged whenever the arguments allow).  Returns
     the previous setting."""
     codes = {"auto": _capi.PATH_AUTO, "register": _capi.PATH_REGISTER, "tma": _capi.PATH_TMA}
     names = {v: k for k, v in codes.items()}
@@ -551,3 +553,10 @@ def hybrid_comm_bytes(psi: float, nd: int, shard_group: int, kind: str,
 def launch_count() -> int:
     """Kernels libshardstep has launched in this process."""
     return int(_capi.lib().shardstep_launch_count())
+
+
+def last_kernel() -> str:
+    """Name of the kernel this thread's last streaming call launched (fused
+    step, accumulation, non-finite check, bucket all-reduce); "" before the
+    first."""
+    return _capi.lib().shardstep_last_kernel().decode()

@@ -99,6 +99,7 @@ SIGNATURES = {
     "shardstep_set_dependent_launch": (c_i32, [c_i32]),
     "shardstep_device_status": (c_i32, [ctypes.POINTER(ctypes.c_uint32), c_i32]),
     "shardstep_launch_count": (c_u64, []),
+    "shardstep_last_kernel": (ctypes.c_char_p, []),
 }
 
 _lib = None

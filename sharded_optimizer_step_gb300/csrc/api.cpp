@@ -17,6 +17,19 @@ namespace shardstep {
 namespace {
 
 thread_local std::string g_error;
+thread_local char g_last_kernel[128] = "";
+
+// Records which kernel the calling thread's last streaming call launched.
+void note_kernel(const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_kernel, sizeof g_last_kernel, fmt, ap);
+    va_end(ap);
+}
+
+const char* dtype_name(int dtype) {
+    return dtype == SHARDSTEP_DTYPE_F32 ? "f32" : dtype == SHARDSTEP_DTYPE_F16 ? "f16" : "bf16";
+}
 std::atomic<uint64_t> g_launches{0};
 std::atomic<int> g_fused_path{SHARDSTEP_PATH_AUTO};
 std::atomic<int> g_dependent_launch{1};
@@ -25,25 +38,35 @@ std::atomic<int> g_dependent_launch{1};
 // still checks alignment and the stage size).  PATH_REGISTER: never;
 // PATH_TMA: always; PATH_AUTO: where it measured faster on GB300 against the
 // register-staged kernel of the same operation --
-//   fused step: N_d >= 3 (at N_d = 1 and 2 the register kernel moved 6.5 vs
-//     6.1 TB/s; at N_d = 8, 6.9 vs 6.5);
-//   bucket all-reduce: N_d >= 3 and buckets of at least 32M elements (later
-//     buckets of a call are dependent launches that overlap the previous
-//     bucket's drain, which favours the register-staged kernel's finer
-//     grid: a 351M gradient in 33 buckets took 0.908 ms register-staged vs
-//     0.924 ms with TMA from 8M elements; in 3 buckets 0.894 vs 0.880 ms);
-//   accumulation and the non-finite check: always (6.5 vs 6.0 and 7.3 vs
-//     6.9 TB/s).
+//   fused step: only at N_d = 6, 7 and 9..15 (the register kernel's
+//     runtime loop there: 5.9 vs 6.5 TB/s at N_d = 6, 5.5 vs 7.0 at 12),
+//     N_d > 16, and 16 fp32 slices, whose register kernel spills (at N_d =
+//     8 the register kernel moved 7.13 vs 6.88 TB/s, at N_d = 1..5 and 16
+//     it was faster as well);
+//   bucket all-reduce: N_d >= 3 and buckets of at least 32M elements (one
+//     400M bucket at N_d = 4: 6.9 vs 6.4 TB/s; at N_d = 8: 7.05 vs 6.98);
+//   non-finite check: N_d >= 3 but not 4 or 8, the counts the register
+//     kernel is compiled for (at N_d = 4: 6.3 vs 5.7 TB/s; at 8: 7.4 vs 7.3);
+//   accumulation: never (7.0 vs 6.0 TB/s for the first micro-batch, 7.2 vs
+//     6.6 for the others).
 enum class TmaOp { kStep, kAllReduce, kAccumulate, kCheck };
-bool use_tma(TmaOp op, int64_t n, int nd = 0) {
+bool register_step_kernel(int nd, int grad_dtype) {
+    switch (nd) {
+        case 1: case 2: case 3: case 4: case 5: case 8: return true;
+        case 16: return grad_dtype != SHARDSTEP_DTYPE_F32;
+        default: return false;
+    }
+}
+bool use_tma(TmaOp op, int64_t n, int nd = 0, int grad_dtype = SHARDSTEP_DTYPE_BF16) {
     const int path = g_fused_path.load(std::memory_order_relaxed);
     if (path == SHARDSTEP_PATH_REGISTER) return false;
     if (n < kTmaMinElements) return false;
     if (path == SHARDSTEP_PATH_TMA) return true;
     switch (op) {
-        case TmaOp::kStep: return nd >= 3;
+        case TmaOp::kStep: return nd >= 3 && !register_step_kernel(nd, grad_dtype);
         case TmaOp::kAllReduce: return nd >= 3 && n >= (int64_t{32} << 20);
-        default: return true;
+        case TmaOp::kCheck: return nd >= 3 && nd != 4 && nd != 8;
+        default: return false;
     }
 }
 
@@ -231,6 +254,8 @@ using namespace shardstep;
 extern "C" {
 
 const char* shardstep_last_error(void) { return g_error.c_str(); }
+
+const char* shardstep_last_kernel(void) { return g_last_kernel; }
 
 uint64_t shardstep_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
@@ -471,6 +496,8 @@ int fsdp_grad_accumulate(const uint16_t* g, float* acc, int64_t n, float scale, 
                         : launch_accumulate(g, acc, n, scale, first != 0, vec,
                                             static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "accumulate kernel launch");
+    note_kernel(tma ? "staged_stream<AccumOp> (TMA-staged)"
+                    : vec ? "accumulate_vec8 (register-staged)" : "accumulate_scalar");
     return ok();
 }
 
@@ -546,7 +573,7 @@ int fused_step(const void* const* grad_slices, int32_t grad_dtype, int32_t nd, i
     vec = vec && aligned(master, 16) && aligned(m, 16) && aligned(v, 16) && aligned(out_bf16, 8);
     // TMA-staged path: bulk copies need 16-byte aligned sources; the two
     // stages must fit in shared memory
-    tma = tma && use_tma(TmaOp::kStep, S, nd) && aligned(master, 16) && aligned(m, 16) && aligned(v, 16) &&
+    tma = tma && use_tma(TmaOp::kStep, S, nd, grad_dtype) && aligned(master, 16) && aligned(m, 16) && aligned(v, 16) &&
           aligned(out_bf16, 8) && tma_step_fits(nd, grad_dtype);
     MeanOp mo = mean_op(nd, group);
     mo.scaled = scale != nullptr;
@@ -559,6 +586,12 @@ int fused_step(const void* const* grad_slices, int32_t grad_dtype, int32_t nd, i
                                    adam_scalars(*hp), mo, skip, vec,
                                    static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "fused step kernel launch");
+    if (tma)
+        note_kernel("staged_stream<AdamOp<%s>> (TMA-staged)", dtype_name(grad_dtype));
+    else if (vec)
+        note_kernel("rs_adamw_cast_vec4<%d, %s> (register-staged)", nd, dtype_name(grad_dtype));
+    else
+        note_kernel("rs_adamw_cast_scalar<%s>", dtype_name(grad_dtype));
     return ok();
 }
 
@@ -609,6 +642,12 @@ int fsdp_grad_unscale_check(const void* const* grad_slices, int32_t grad_dtype, 
                         : launch_nonfinite_check(tab, nd, grad_dtype, S, mo, found_inf, vec,
                                                  static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "non-finite check launch");
+    if (tma)
+        note_kernel("staged_stream<CheckOp<%s>> (TMA-staged)", dtype_name(grad_dtype));
+    else if (vec)
+        note_kernel("nonfinite_check_vec4<%s> (register-staged)", dtype_name(grad_dtype));
+    else
+        note_kernel("nonfinite_check_scalar<%s>", dtype_name(grad_dtype));
     return ok();
 }
 
@@ -896,6 +935,8 @@ int ddp_bucket_allreduce_avg(const uint16_t* const* rank_grads, int32_t nd,
                             : launch_allreduce_avg(tab, nd, n, out + a, mo, vec, pdl,
                                                    static_cast<cudaStream_t>(stream));
         if (e != cudaSuccess) return cuda_fail(e, "all-reduce kernel launch");
+        note_kernel(tma ? "staged_stream<MeanOutOp> (TMA-staged)"
+                        : vec ? "allreduce_avg_vec4 (register-staged)" : "allreduce_avg_scalar");
         pdl = g_dependent_launch.load(std::memory_order_relaxed) != 0;
     }
     return ok();

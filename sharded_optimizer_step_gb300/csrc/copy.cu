@@ -133,8 +133,12 @@ __device__ __forceinline__ void acc_scalar(const uint16_t* g, float* acc, int64_
     acc[j] = FIRST ? t : __fadd_rn(acc[j], t);
 }
 
+// One 8-element vector per thread in a one-pass grid (the loop strides only
+// past 2^31 - 1 blocks); 8 blocks per SM, at most 32 registers.  Against a
+// grid-stride loop over one wave of blocks this moved 7.0 vs 6.0 TB/s on
+// GB300 for the first micro-batch and 7.2 vs 6.6 TB/s for the others.
 template <bool FIRST>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 8)
     accumulate_vec8(const uint16_t* __restrict__ g, float* __restrict__ acc, int64_t n,
                     float scale) {
     const int64_t nvec = n >> 3;
@@ -178,6 +182,13 @@ unsigned grid_for(const void* kernel, int64_t work_items) {
     return static_cast<unsigned>(g < 1 ? 1 : g);
 }
 
+unsigned grid_one_pass(int64_t vectors) {
+    const int64_t want = (vectors + kThreads - 1) / kThreads;
+    const int64_t cap = (int64_t{1} << 31) - 1;
+    const int64_t g = want < cap ? want : cap;
+    return static_cast<unsigned>(g < 1 ? 1 : g);
+}
+
 }  // namespace
 
 cudaError_t launch_copy(const CopyTable& t, cudaStream_t stream) {
@@ -198,16 +209,11 @@ cudaError_t launch_copy16(const AlignedTable& t, cudaStream_t stream) {
 cudaError_t launch_accumulate(const uint16_t* g, float* acc, int64_t n, float scale, bool first,
                               bool vec, cudaStream_t stream) {
     if (vec) {
-        const int64_t items = (n >> 3) > 0 ? (n >> 3) : 1;
-        if (first) {
-            accumulate_vec8<true><<<grid_for(reinterpret_cast<const void*>(accumulate_vec8<true>),
-                                             items),
-                                    kThreads, 0, stream>>>(g, acc, n, scale);
-        } else {
-            accumulate_vec8<false><<<grid_for(reinterpret_cast<const void*>(accumulate_vec8<false>),
-                                              items),
-                                     kThreads, 0, stream>>>(g, acc, n, scale);
-        }
+        const unsigned grid = grid_one_pass(n >> 3);
+        if (first)
+            accumulate_vec8<true><<<grid, kThreads, 0, stream>>>(g, acc, n, scale);
+        else
+            accumulate_vec8<false><<<grid, kThreads, 0, stream>>>(g, acc, n, scale);
     } else if (first) {
         accumulate_scalar<true><<<grid_for(reinterpret_cast<const void*>(accumulate_scalar<true>), n),
                                   kThreads, 0, stream>>>(g, acc, n, scale);

@@ -6,24 +6,26 @@
 // All are HBM-bound streams: per shard element the fused kernel reads N_d
 // gradient slices (2 B each for bf16 / fp16, 4 B for fp32) and the fp32
 // master/m/v (12 B), and writes master/m/v (12 B) and the bf16 parameter
-// (2 B), each byte touched once.  Each thread owns 4 consecutive elements per
-// iteration: one 8-byte load per 16-bit slice (16 bytes for fp32 slices),
-// one 16-byte load per fp32 state array, every load of the iteration issued
-// before any arithmetic; all accesses are streaming (evict-first) loads and
-// stores.  Blocks of 512 threads are capped at 64 registers so that 32 warps
-// per SM keep requests in flight; the grid is three times the resident
-// capacity (SMs x 2 blocks) and strides over the shard.  Measured on GB300
-// against 8-elements-per-thread blocks of 256 at 112 registers, this shape
-// moves the same bytes about 6% faster.
+// (2 B), each byte touched once.  Each thread owns 4 consecutive elements:
+// one 8-byte load per 16-bit slice (16 bytes for fp32 slices), one 16-byte
+// load per fp32 state array, every load issued before any arithmetic; all
+// accesses are streaming (evict-first) loads and stores.  Blocks of 128
+// threads are capped at 64 registers so that 8 of them (32 warps) fit on an
+// SM, and the grid covers the whole range in one pass (one 4-element vector
+// per thread; the loop only strides if the range needs more than 2^31 - 1
+// blocks), so the blocks resident at any time work on neighbouring
+// addresses.  Measured on GB300 at 842M elements and N_d = 8: a one-pass grid
+// of 512-thread blocks took 4.85 ms where a grid-stride loop over three waves
+// of the same blocks took 5.32 ms (same GPU); 128-thread blocks took 1% less
+// again, and the TMA-staged kernel 4% more (4.88 vs 5.08 ms, same GPU).
 #include "common.cuh"
 
 namespace shardstep {
 namespace {
 
 constexpr int kRuntimeND = 0;
-constexpr int kStepThreads = 512;  // block of the fused / all-reduce / check kernels
-constexpr int kStepMinBlocks = 2;  // 2 x 512 threads per SM -> <= 64 registers
-constexpr int kGridOversub = 3;    // blocks launched per resident block slot
+constexpr int kStepThreads = 128;  // block of the fused / all-reduce / check kernels
+constexpr int kStepMinBlocks = 8;  // 8 x 128 threads per SM -> <= 64 registers
 
 // ----------------------------------------------------------------- loads
 
@@ -210,19 +212,28 @@ __global__ void __launch_bounds__(kThreads)
 // Both all-reduce kernels may run as programmatic dependents of the previous
 // bucket's kernel: they trigger their own dependents at start and wait for
 // the grid they depend on before they end (no-ops for ordinary launches).
+// The all-reduce and the check move few bytes per 4-element vector (6 B per
+// element at N_d = 2), so each block takes `vpt` rows of kStepThreads vectors
+// (a contiguous run of vpt x kStepThreads vectors) to keep the rate of block
+// launches per SM down; the launcher picks vpt from the bytes per vector.
 template <int ND>
 __global__ void __launch_bounds__(kStepThreads, kStepMinBlocks)
-    allreduce_avg_vec4(PtrTable tab, int nd, int64_t n, uint16_t* __restrict__ out, MeanOp mo) {
+    allreduce_avg_vec4(PtrTable tab, int nd, int64_t n, uint16_t* __restrict__ out, MeanOp mo,
+                       int vpt) {
     pdl_trigger();
     const int64_t nvec = n >> 2;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * kStepThreads;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kStepThreads + threadIdx.x; i < nvec;
-         i += stride) {
-        float g[4];
-        reduce4<ND, kGradBF16>(tab, nd, mo.group, i, g);
+    const int64_t run = static_cast<int64_t>(kStepThreads) * vpt;
+    for (int64_t b0 = static_cast<int64_t>(blockIdx.x) * run; b0 < nvec;
+         b0 += static_cast<int64_t>(gridDim.x) * run) {
+        for (int k = 0; k < vpt; ++k) {
+            const int64_t i = b0 + static_cast<int64_t>(k) * kStepThreads + threadIdx.x;
+            if (i >= nvec) break;
+            float g[4];
+            reduce4<ND, kGradBF16>(tab, nd, mo.group, i, g);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) g[k] = mean_of(g[k], mo);
-        stcs8(out + 4 * i, make_uint2(pack_bf16x2(g[0], g[1]), pack_bf16x2(g[2], g[3])));
+            for (int e = 0; e < 4; ++e) g[e] = mean_of(g[e], mo);
+            stcs8(out + 4 * i, make_uint2(pack_bf16x2(g[0], g[1]), pack_bf16x2(g[2], g[3])));
+        }
     }
     if (blockIdx.x == 0 && threadIdx.x < (n & 3)) {
         const int64_t j = (nvec << 2) + threadIdx.x;
@@ -252,17 +263,22 @@ __device__ __forceinline__ bool not_finite(float x) {
 // slices only (2 B per fp16 slice element); one atomic per warp that saw one.
 template <int ND, int GT>
 __global__ void __launch_bounds__(kStepThreads, kStepMinBlocks)
-    nonfinite_check_vec4(PtrTable tab, int nd, int64_t S, MeanOp mo, unsigned int* found) {
+    nonfinite_check_vec4(PtrTable tab, int nd, int64_t S, MeanOp mo, unsigned int* found,
+                         int vpt) {
     mo = resolve_scale(mo);
     bool bad = false;
     const int64_t nvec = S >> 2;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * kStepThreads;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kStepThreads + threadIdx.x; i < nvec;
-         i += stride) {
-        float g[4];
-        reduce4<ND, GT>(tab, nd, mo.group, i, g);
+    const int64_t run = static_cast<int64_t>(kStepThreads) * vpt;
+    for (int64_t b0 = static_cast<int64_t>(blockIdx.x) * run; b0 < nvec;
+         b0 += static_cast<int64_t>(gridDim.x) * run) {
+        for (int k = 0; k < vpt; ++k) {
+            const int64_t i = b0 + static_cast<int64_t>(k) * kStepThreads + threadIdx.x;
+            if (i >= nvec) break;
+            float g[4];
+            reduce4<ND, GT>(tab, nd, mo.group, i, g);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) bad |= not_finite(mean_of(g[k], mo));
+            for (int e = 0; e < 4; ++e) bad |= not_finite(mean_of(g[e], mo));
+        }
     }
     if (blockIdx.x == 0 && threadIdx.x < (S & 3))
         bad |= not_finite(mean_of(reduce1<GT>(tab, nd, mo.group, (nvec << 2) + threadIdx.x), mo));
@@ -306,13 +322,32 @@ __global__ void scaler_update_kernel(float* scale, int* tracker, unsigned int* f
 
 // --------------------------------------------------------------- launch
 
-unsigned grid_for(const void* kernel, int64_t work_items, int threads = kThreads,
-                  int oversub = 1) {
+unsigned grid_for(const void* kernel, int64_t work_items, int threads = kThreads) {
     const int64_t want = (work_items + threads - 1) / threads;
-    const int64_t cap =
-        static_cast<int64_t>(device_sms()) * resident_blocks(kernel, threads) * oversub;
+    const int64_t cap = static_cast<int64_t>(device_sms()) * resident_blocks(kernel, threads);
     const int64_t g = want < cap ? want : cap;
     return static_cast<unsigned>(g < 1 ? 1 : g);
+}
+
+// One pass: a block per vpt x kStepThreads vectors, at most 2^31 - 1 blocks.
+unsigned grid_one_pass(int64_t vectors, int vpt = 1) {
+    const int64_t run = static_cast<int64_t>(kStepThreads) * vpt;
+    const int64_t want = (vectors + run - 1) / run;
+    const int64_t cap = (int64_t{1} << 31) - 1;
+    const int64_t g = want < cap ? want : cap;
+    return static_cast<unsigned>(g < 1 ? 1 : g);
+}
+
+// Vectors per thread for a kernel that moves `bytes_per_vector` per 4-element
+// vector: enough for a block to move about kBlockBytes, at most 8.  Measured
+// on GB300 (400M elements, bf16): the N_d = 2 all-reduce moved 3.0 TB/s with
+// one vector per thread, 5.5 / 5.7 / 5.7 TB/s with blocks of 8 / 16 / 32 KB;
+// the N_d = 4 check 4.6 / 5.5 / 6.0 / 6.3 TB/s.
+constexpr int kBlockBytes = 32768;
+int vectors_per_thread(int bytes_per_vector) {
+    const int per_row = kStepThreads * bytes_per_vector;
+    const int v = (kBlockBytes + per_row - 1) / per_row;
+    return v < 1 ? 1 : (v > 8 ? 8 : v);
 }
 
 struct StepArgs {
@@ -329,8 +364,7 @@ struct StepArgs {
 template <int ND, int GT>
 cudaError_t go_vec(const StepArgs& a, cudaStream_t s) {
     auto k = rs_adamw_cast_vec4<ND, GT>;
-    const unsigned grid = grid_for(reinterpret_cast<const void*>(k),
-                                   (a.S >> 2) > 0 ? (a.S >> 2) : 1, kStepThreads, kGridOversub);
+    const unsigned grid = grid_one_pass(a.S >> 2);
     k<<<grid, kStepThreads, 0, s>>>(a.tab, a.nd, a.S, a.P, a.M, a.V, a.out, a.c, a.mo, a.skip);
     note_launch();
     return cudaGetLastError();
@@ -362,13 +396,13 @@ template <int ND>
 cudaError_t go_ar(const PtrTable& tab, int nd, int64_t n, uint16_t* out, const MeanOp& mo,
                   bool pdl, cudaStream_t s) {
     auto k = allreduce_avg_vec4<ND>;
-    const unsigned grid = grid_for(reinterpret_cast<const void*>(k), (n >> 2) > 0 ? (n >> 2) : 1,
-                                   kStepThreads, kGridOversub);
+    const int vpt = vectors_per_thread(4 * (2 * nd + 2));
+    const unsigned grid = grid_one_pass(n >> 2, vpt);
     cudaError_t e;
     if (pdl) {
-        e = launch_dependent(k, dim3(grid), dim3(kStepThreads), 0, s, tab, nd, n, out, mo);
+        e = launch_dependent(k, dim3(grid), dim3(kStepThreads), 0, s, tab, nd, n, out, mo, vpt);
     } else {
-        k<<<grid, kStepThreads, 0, s>>>(tab, nd, n, out, mo);
+        k<<<grid, kStepThreads, 0, s>>>(tab, nd, n, out, mo, vpt);
         e = cudaGetLastError();
     }
     note_launch();
@@ -379,9 +413,9 @@ template <int ND, int GT>
 cudaError_t go_check(const PtrTable& tab, int nd, int64_t S, const MeanOp& mo,
                      unsigned int* found, cudaStream_t s) {
     auto k = nonfinite_check_vec4<ND, GT>;
-    const unsigned grid = grid_for(reinterpret_cast<const void*>(k), (S >> 2) > 0 ? (S >> 2) : 1,
-                                   kStepThreads, kGridOversub);
-    k<<<grid, kStepThreads, 0, s>>>(tab, nd, S, mo, found);
+    const int vpt = vectors_per_thread(4 * nd * (GT == kGradF32 ? 4 : 2));
+    const unsigned grid = grid_one_pass(S >> 2, vpt);
+    k<<<grid, kStepThreads, 0, s>>>(tab, nd, S, mo, found, vpt);
     note_launch();
     return cudaGetLastError();
 }

@@ -245,3 +245,21 @@ def test_fsdp2_entry_points_reject_bad_arguments():
     assert L.fsdp2_all_gather_copy_out(_capi.ptr_array([A, A + 4096]), d0, row, 2, 2,
                                        _capi.DTYPE_BF16, _capi.ptr_array([A + 32, A + 8192]),
                                        None) == _capi.ERR_INVALID
+
+
+def test_last_kernel_is_empty_until_a_launch():
+    """A call that validation rejects launches nothing and names no kernel."""
+    import threading
+    seen = []
+
+    def body():
+        seen.append(ss.last_kernel())
+        L = _capi.lib()
+        rc = L.fsdp_grad_accumulate(None, None, 16, ctypes.c_float(1.0), 1, None)
+        seen.append((rc, ss.last_kernel()))
+
+    t = threading.Thread(target=body)
+    t.start()
+    t.join()
+    assert seen[0] == ""
+    assert seen[1][0] < 0 and seen[1][1] == ""

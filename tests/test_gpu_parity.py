@@ -503,3 +503,37 @@ def test_bucket_allreduce_dependent_launches_keep_stream_order(dependent, path):
     want = oracle.bucket_allreduce_avg(grads_h, boff)
     torch.cuda.synchronize()
     assert_bits(host_bf16(seen), want, "avg")
+
+
+# ------------------------------------------------- which kernel ran
+
+def test_auto_path_names_the_kernel_it_launched():
+    """The automatic choice, as shardstep_last_kernel reports it: the
+    register-staged fused kernel at N_d = 8, the TMA-staged one at N_d = 6,
+    TMA-staged whenever forced."""
+    S = 8192
+    master = torch.zeros(S, device=DEV)
+    m = torch.zeros(S, device=DEV)
+    v = torch.zeros(S, device=DEV)
+    out = torch.empty(S, dtype=torch.bfloat16, device=DEV)
+    prev = ss.set_fused_path("auto")
+    try:
+        for nd, want in [(8, "rs_adamw_cast_vec4<8, bf16> (register-staged)"),
+                         (6, "staged_stream<AdamOp<bf16>> (TMA-staged)")]:
+            g = [torch.zeros(S, dtype=torch.bfloat16, device=DEV) for _ in range(nd)]
+            ss.fsdp_rs_avg_adamw_cast(g, master, m, v, out, HPC, 1)
+            assert ss.last_kernel() == want
+        g = [torch.zeros(S, dtype=torch.bfloat16, device=DEV) for _ in range(8)]
+        ss.set_fused_path("tma")
+        ss.fsdp_rs_avg_adamw_cast(g, master, m, v, out, HPC, 1)
+        assert ss.last_kernel() == "staged_stream<AdamOp<bf16>> (TMA-staged)"
+        ss.set_fused_path("register")
+        ss.fsdp_rs_avg_adamw_cast([x[1:] for x in g], master[1:], m[1:], v[1:], out[1:], HPC, 1)
+        assert ss.last_kernel() == "rs_adamw_cast_scalar<bf16>"
+        acc = torch.zeros(S, device=DEV)
+        ss.set_fused_path("auto")
+        ss.fsdp_grad_accumulate(g[0], acc, 0.25, True)
+        assert ss.last_kernel() == "accumulate_vec8 (register-staged)"
+        torch.cuda.synchronize()
+    finally:
+        ss.set_fused_path(prev)
