@@ -1,8 +1,11 @@
 // TMA-staged streaming kernels: the fused sharded step (reduce-scatter
 // average + AdamW + bf16 cast), the micro-batch gradient accumulation, the
 // DDP bucket all-reduce average and the gradient scaler's non-finite check.
-// They are the default path whenever every source is 16-byte aligned and at
-// least two stages fit in shared memory.
+// They need every source 16-byte aligned and two stages in shared memory.
+// The automatic kernel choice takes them where they measured faster than the
+// one-pass register-staged kernels: the fused step and the check at the N_d
+// those are not compiled for, the all-reduce on buckets of 32M elements and
+// more at N_d >= 3.
 //
 // One skeleton serves all four.  One CTA per SM, 17 warps.  Warp 16's first
 // lane is the producer: for each tile of 2048 elements it issues one
