@@ -2,6 +2,7 @@
 // FlatParameter layout and bucket planning, the AdamW scalar derivation, and
 // dispatch to the kernels.  Nothing here allocates device memory.
 #include <atomic>
+#include <initializer_list>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -25,6 +26,14 @@ void note_kernel(const char* fmt, ...) {
     va_start(ap, fmt);
     vsnprintf(g_last_kernel, sizeof g_last_kernel, fmt, ap);
     va_end(ap);
+}
+
+// Whether nd is one of the counts a register-staged kernel is compiled for
+// (the others take its loop over any N_d).
+bool compiled_nd(int nd, std::initializer_list<int> counts) {
+    for (int c : counts)
+        if (c == nd) return true;
+    return false;
 }
 
 const char* dtype_name(int dtype) {
@@ -588,8 +597,11 @@ int fused_step(const void* const* grad_slices, int32_t grad_dtype, int32_t nd, i
     if (e != cudaSuccess) return cuda_fail(e, "fused step kernel launch");
     if (tma)
         note_kernel("staged_stream<AdamOp<%s>> (TMA-staged)", dtype_name(grad_dtype));
-    else if (vec)
+    else if (vec && compiled_nd(nd, {1, 2, 3, 4, 8, 16}))
         note_kernel("rs_adamw_cast_vec4<%d, %s> (register-staged)", nd, dtype_name(grad_dtype));
+    else if (vec)
+        note_kernel("rs_adamw_cast_vec4<any N_d = %d, %s> (register-staged)", nd,
+                    dtype_name(grad_dtype));
     else
         note_kernel("rs_adamw_cast_scalar<%s>", dtype_name(grad_dtype));
     return ok();
@@ -644,8 +656,11 @@ int fsdp_grad_unscale_check(const void* const* grad_slices, int32_t grad_dtype, 
     if (e != cudaSuccess) return cuda_fail(e, "non-finite check launch");
     if (tma)
         note_kernel("staged_stream<CheckOp<%s>> (TMA-staged)", dtype_name(grad_dtype));
+    else if (vec && compiled_nd(nd, {4, 8}))
+        note_kernel("nonfinite_check_vec4<%d, %s> (register-staged)", nd, dtype_name(grad_dtype));
     else if (vec)
-        note_kernel("nonfinite_check_vec4<%s> (register-staged)", dtype_name(grad_dtype));
+        note_kernel("nonfinite_check_vec4<any N_d = %d, %s> (register-staged)", nd,
+                    dtype_name(grad_dtype));
     else
         note_kernel("nonfinite_check_scalar<%s>", dtype_name(grad_dtype));
     return ok();
@@ -935,8 +950,14 @@ int ddp_bucket_allreduce_avg(const uint16_t* const* rank_grads, int32_t nd,
                             : launch_allreduce_avg(tab, nd, n, out + a, mo, vec, pdl,
                                                    static_cast<cudaStream_t>(stream));
         if (e != cudaSuccess) return cuda_fail(e, "all-reduce kernel launch");
-        note_kernel(tma ? "staged_stream<MeanOutOp> (TMA-staged)"
-                        : vec ? "allreduce_avg_vec4 (register-staged)" : "allreduce_avg_scalar");
+        if (tma)
+            note_kernel("staged_stream<MeanOutOp> (TMA-staged)");
+        else if (vec && compiled_nd(nd, {1, 2, 4, 8}))
+            note_kernel("allreduce_avg_vec4<%d> (register-staged)", nd);
+        else if (vec)
+            note_kernel("allreduce_avg_vec4<any N_d = %d> (register-staged)", nd);
+        else
+            note_kernel("allreduce_avg_scalar");
         pdl = g_dependent_launch.load(std::memory_order_relaxed) != 0;
     }
     return ok();

