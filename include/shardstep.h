@@ -522,8 +522,10 @@ int fsdp_reshard_plan(int64_t total, int32_t old_nd, int32_t new_nd, int32_t new
  * slices), the bucket all-reduce at N_d >= 3 on buckets of at least 32M
  * elements, the check at N_d = 3, 5..7 and above 8, the accumulation never.
  * The copies (flat_pack, ag_unpack, FSDP2 chunk-cat / copy-out) send the
- * 16-byte-aligned body of every range to a 16-byte vector copy except under
- * _REGISTER, which keeps them on the generic segment copy.  All give
+ * body of every range between its first and last 16-byte boundary of the
+ * destination to a 16-byte vector copy (realigning the source when it is
+ * not congruent) except under _REGISTER, which keeps them on the generic
+ * segment copy.  All give
  * bit-identical results.  Returns the previous setting, or INVALID for an
  * unknown value. */
 #define SHARDSTEP_PATH_AUTO 0

@@ -345,15 +345,17 @@ int fsdp_views(const int64_t* numels, int32_t n, int32_t nd, int32_t rank, void*
 
 // Turns (src, dst, bytes) triples into copy-kernel launches of <= kMaxCopySegs.
 namespace {
-// Whether the 16-byte-aligned body of a copy range goes to copy16 (every
-// kernel choice but PATH_REGISTER, which keeps all copies on copy_segments).
+// Whether the body of a copy range between its first and last 16-byte
+// boundary of the destination goes to copy16 / copy16_shift (every kernel
+// choice but PATH_REGISTER, which keeps all copies on copy_segments).
 bool use_copy16() {
     return g_fused_path.load(std::memory_order_relaxed) != SHARDSTEP_PATH_REGISTER;
 }
 
 struct CopyBatcher {
     CopyTable t;
-    AlignedTable bt;
+    AlignedTable bt;  // 16-byte aligned source and destination (copy16)
+    AlignedTable st;  // aligned destination, unaligned source (copy16_shift)
     cudaStream_t stream;
     int rc = SHARDSTEP_OK;
     explicit CopyBatcher(cudaStream_t s) : stream(s) {
@@ -361,36 +363,40 @@ struct CopyBatcher {
         t.total_chunks = 0;
         bt.n = 0;
         bt.total_chunks = 0;
+        st.n = 0;
+        st.total_chunks = 0;
     }
-    // A range whose source and destination are congruent modulo 16 bytes
-    // goes to copy16 for its 16-byte-aligned body (unless the register path
-    // is forced); the unaligned head and tail bytes, zero fills and
-    // everything else go to copy_segments.
+    // The body of a range between its first and last 16-byte boundary of the
+    // destination goes to copy16 when the source is congruent to the
+    // destination modulo 16 bytes, else to copy16_shift (unless the register
+    // path is forced); the head and tail bytes, zero fills and everything
+    // under PATH_REGISTER go to copy_segments.
     void add(const void* src, void* dst, int64_t bytes) {
         if (bytes <= 0 || rc != SHARDSTEP_OK) return;
         const uintptr_t d = reinterpret_cast<uintptr_t>(dst);
-        if (src != nullptr && ((reinterpret_cast<uintptr_t>(src) ^ d) & 15u) == 0) {
+        if (src != nullptr && use_copy16()) {
             const int64_t head = static_cast<int64_t>((16 - d % 16) % 16);
             const int64_t body = bytes > head ? ((bytes - head) & ~int64_t{15}) : 0;
-            if (body > 0 && use_copy16()) {
+            if (body > 0) {
                 const char* s8 = static_cast<const char*>(src);
                 char* d8 = static_cast<char*>(dst);
+                const bool congruent = ((reinterpret_cast<uintptr_t>(src) ^ d) & 15u) == 0;
                 add_vector(s8, d8, head);
-                add_aligned(s8 + head, d8 + head, body);
+                add_chunked(congruent ? bt : st, s8 + head, d8 + head, body);
                 add_vector(s8 + head + body, d8 + head + body, bytes - head - body);
                 return;
             }
         }
         add_vector(src, dst, bytes);
     }
-    void add_aligned(const char* src, char* dst, int64_t bytes) {
-        AlignedSeg& s = bt.s[bt.n];
+    void add_chunked(AlignedTable& tab, const char* src, char* dst, int64_t bytes) {
+        AlignedSeg& s = tab.s[tab.n];
         s.src = src;
         s.dst = dst;
         s.bytes = bytes;
-        s.chunk0 = bt.total_chunks;
-        bt.total_chunks += (bytes + kAlignedChunk - 1) / kAlignedChunk;
-        if (++bt.n == kMaxCopySegs) flush_aligned();
+        s.chunk0 = tab.total_chunks;
+        tab.total_chunks += (bytes + kAlignedChunk - 1) / kAlignedChunk;
+        if (++tab.n == kMaxCopySegs) flush_chunked(tab);
     }
     void add_vector(const void* src, void* dst, int64_t bytes) {
         if (bytes <= 0 || rc != SHARDSTEP_OK) return;
@@ -418,15 +424,16 @@ struct CopyBatcher {
         t.n = 0;
         t.total_chunks = 0;
     }
-    void flush_aligned() {
-        if (bt.n == 0 || rc != SHARDSTEP_OK) return;
-        cudaError_t e = launch_copy16(bt, stream);
+    void flush_chunked(AlignedTable& tab) {
+        if (tab.n == 0 || rc != SHARDSTEP_OK) return;
+        cudaError_t e = &tab == &bt ? launch_copy16(tab, stream) : launch_copy16_shift(tab, stream);
         if (e != cudaSuccess) rc = cuda_fail(e, "aligned copy kernel launch");
-        bt.n = 0;
-        bt.total_chunks = 0;
+        tab.n = 0;
+        tab.total_chunks = 0;
     }
     void flush() {
-        flush_aligned();
+        flush_chunked(bt);
+        flush_chunked(st);
         flush_vector();
     }
 };

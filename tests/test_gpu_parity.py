@@ -274,6 +274,31 @@ def test_flat_pack_matches_oracle(dtype, nd, path):
             assert_bits(ha.view(np.uint8), b.view(np.uint8), "piece")
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_flat_pack_every_source_and_destination_offset(dtype, path):
+    """A tensor packed behind a filler of o elements (destination offset o)
+    from a source that starts s elements into its allocation, for every o
+    and s below 16 bytes and lengths around the 16-byte vector and the
+    16 KB chunk: every pairing of source and destination alignment,
+    including the ones the realigning copy takes."""
+    es = 2 if dtype == "bf16" else 4
+    per16 = 16 // es
+    mk = dev_bf16 if dtype == "bf16" else dev_f32
+    for n in (1, per16 - 1, per16 + 1, 8192 // es * 2 + 3, 70001):
+        body = synth.host_fill(synth.normal_stream(n, (95, 1), 0.02), 0, n, dtype)
+        for o in range(per16):
+            filler = synth.host_fill(synth.normal_stream(n, (95, 2, o), 0.02), 0, o, dtype)
+            for sh in range(per16):
+                host = [filler, body] if o else [body]
+                dev = [mk(filler)] if o else []
+                dev.append(mk(body, sh))
+                flat = ss.fsdp_flat_pack(dev, 1)
+                want, _ = oracle.flat_pack(host, 1)
+                torch.cuda.synchronize()
+                got = host_bf16(flat) if dtype == "bf16" else host_f32(flat)
+                assert_bits(got, want, f"n={n} o={o} s={sh}")
+
+
 def test_flat_pack_misaligned_destination_segments(path):
     # element offsets that are odd make source and destination incongruent
     numels = [1, 2, 3, 5, 8, 13, 21, 34, 55, 89, 144, 233, 377, 610, 987, 1597, 2584]
@@ -323,9 +348,10 @@ def test_ag_unpack_skips_the_rank_already_in_place():
     shards[2] = full[2 * S:3 * S]
     before = ss.launch_count()
     ss.fsdp_ag_unpack(shards, full)
-    # one launch per copy kind at most: the 16-byte copy of aligned bodies,
-    # the vector copy of the rest (the shard in place is in neither)
-    assert 1 <= ss.launch_count() - before <= 2
+    # one launch per copy kind at most: the 16-byte copy of congruent bodies,
+    # the realigning copy of the others, the vector copy of the rest (the
+    # shard in place is in none)
+    assert 1 <= ss.launch_count() - before <= 3
     torch.cuda.synchronize()
     assert_bits(host_bf16(full), np.concatenate(shards_h), "full")
 
