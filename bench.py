@@ -35,6 +35,8 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "fused shard-step HBM GB/s (% of GB300 peak), params/s at Psi=7B, N_d=8"
+RAGGED_METRIC = ("flat_pack + all-gather HBM GB/s of a ragged Llama-7B layer unit "
+                 "(tensors at odd element offsets), N_d=8")
 TMA_SOURCES = ["sharded_optimizer_step_gb300/csrc/step_tma.cu",
                "sharded_optimizer_step_gb300/csrc/common.cuh"]
 REGISTER_SOURCES = ["sharded_optimizer_step_gb300/csrc/step.cu",
@@ -50,6 +52,7 @@ PROFILES = {
                                        REGISTER_SOURCES),
     "llama_1b_rank0_nd8_m4": ("accumulate_llama1b_rank_view_m4.md", COPY_SOURCES),
     "ddp_nd8_buckets": ("ddp_buckets_nd8_adamw.md", REGISTER_SOURCES),
+    "llama_7b_layer_ragged_nd8": ("pack_gather_llama7b_layer_ragged.md", COPY_SOURCES),
 }
 
 
@@ -63,7 +66,8 @@ def parse():
     ap.add_argument("--e2e-chunks", type=int, default=8)
     ap.add_argument("--e2e-streams", type=int, default=4)
     ap.add_argument("--workload", choices=sorted(WORKLOADS) + [FSDP2_WORKLOAD, CKPT_WORKLOAD,
-                                                             ACCUM_WORKLOAD, DDP_WORKLOAD],
+                                                             ACCUM_WORKLOAD, DDP_WORKLOAD,
+                                                             RAGGED_WORKLOAD],
                     default="llama_7b_rank0_nd8",
                     help="the Llama-7B rank view under full sharding (the default line); the "
                          "other lines time the other steps of the path")
@@ -782,6 +786,145 @@ def run_fsdp2(args):
         }))
 
 
+# ------------------------------------------------------- ragged pack / gather
+
+RAGGED_WORKLOAD = "llama_7b_layer_ragged_nd8"
+
+
+def _ragged_unit():
+    """The Llama-7B layer unit's 9 tensors, each one element longer, so that
+    every tensor after the first starts at an odd element offset of the
+    FlatParameter and the 8 shard slots sit 4 bytes off 16-byte boundaries."""
+    from synth import workloads as W
+    w = W.llama_7b_rank_view()
+    shapes = w.units[w.extra["ag_unit"]]
+    return w, [math.prod(sh) + 1 for sh in shapes]
+
+
+def _ragged_oracle(numels, nd, scale, step):
+    """The oracle's pack and all-gather on a unit scaled down by `scale`;
+    returns (seconds, algorithmic bytes)."""
+    import numpy as np
+    import oracle
+    import synth
+    small = [max(1, n // scale) | 1 for n in numels]
+    tensors = [synth.host_fill(synth.normal_stream(17, (93, step, k), 0.02), 0, n, "bf16")
+               for k, n in enumerate(small)]
+    t0 = time.perf_counter()
+    flat, lay = oracle.flat_pack(tensors, nd)
+    shards = [oracle.shard_of(flat, lay, q) for q in range(nd)]
+    oracle.ag_unpack(shards, lay)
+    dt = time.perf_counter() - t0
+    return dt, 4 * sum(small) + 4 * lay.padded
+
+
+def run_ragged(args):
+    import torch
+    world, rank, local = dist_env()
+    init_dist(world)
+    nd = 8
+    w, numels = _ragged_unit()
+    if args.impl == "reference":
+        if rank == 0:
+            tt, tb = 0.0, 0
+            for k in range(args.warmup + args.steps):
+                dt, b = _ragged_oracle(numels, nd, 64, k)
+                if k >= args.warmup:
+                    tt, tb = tt + dt, tb + b
+            v = tb / tt / 1e9
+            print(json.dumps({
+                "impl": "reference", "metric": RAGGED_METRIC, "value": round(v, 4),
+                "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": round(tt / args.steps * 1e3, 3), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": RAGGED_WORKLOAD, "nd": nd, "sample": "unit / 64"},
+                "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1,
+                                 "kind": "oracle",
+                                 "sample": "each step: pack + all-gather of the unit scaled "
+                                           "down 64x, numpy single-threaded"},
+                "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}))
+        _finish_dist(world)
+        return
+    torch.cuda.set_device(local)
+    import __graft_entry__
+    __graft_entry__.build()
+    _apply_stages(args)
+    import sharded_optimizer_step_gb300 as ss
+    import synth
+    dev = torch.device("cuda", local)
+    tensors = []
+    for k, n in enumerate(numels):
+        t = torch.empty(n, dtype=torch.bfloat16, device=dev)
+        synth.dev_fill(synth.normal_stream(17, (93, 0, k), 0.02), t)
+        tensors.append(t)
+    lay = ss.fsdp_layout(numels, nd)
+    flat = torch.empty(lay.padded, dtype=torch.bfloat16, device=dev)
+    S = lay.shard
+    shards = [torch.empty(S, dtype=torch.bfloat16, device=dev) for _ in range(nd)]
+    for q in range(nd):
+        synth.dev_fill(synth.normal_stream(17, (94, q), 0.02), shards[q])
+    full = torch.empty(nd * S, dtype=torch.bfloat16, device=dev)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+    pack_bytes = 4 * lay.total + 2 * (lay.padded - lay.total)   # zero pad written only
+    ag_bytes = 4 * nd * S
+    step_bytes = pack_bytes + ag_bytes
+
+    def one_step(ev):
+        if ev is not None:
+            ev[0].record(stream)
+        ss.fsdp_flat_pack(tensors, nd, flat=flat)
+        if ev is not None:
+            ev[1].record(stream)
+        ss.fsdp_ag_unpack(shards, full)
+        if ev is not None:
+            ev[2].record(stream)
+
+    total_ms, events, clk, launches = _timed_loop(torch, stream, args, one_step, 3, world)
+    pack_ms, ag_ms = _avg_ms(events, 0, 1), _avg_ms(events, 1, 2)
+    ms = total_ms / args.steps
+    all_bytes = allreduce_sum(world, step_bytes)
+    if rank != 0:
+        _finish_dist(world)
+        return
+    pack_gbs = pack_bytes / (pack_ms / 1e3) / 1e9
+    ag_gbs = ag_bytes / (ag_ms / 1e3) / 1e9
+    cpu = None
+    if not args.no_cpu:
+        tt, tb, reps = 0.0, 0, 0
+        while tt < args.cpu_seconds and reps < 20:
+            dt, b = _ragged_oracle(numels, nd, 64, reps)
+            tt, tb, reps = tt + dt, tb + b, reps + 1
+        cpu = {"value": round(tb / tt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"{reps} x pack + all-gather of the unit scaled down 64x, numpy "
+                         f"single-threaded"}
+    offs = sorted({(o * 2) % 16 for o in lay.offsets} | {(q * S * 2) % 16 for q in range(nd)})
+    print(json.dumps({
+        "metric": RAGGED_METRIC,
+        "value": round(all_bytes / (ms / 1e3) / 1e9, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded counter-based generator on the device; no data set or weights)",
+        "config": {"workload": RAGGED_WORKLOAD, "tma_stages": _stages_name(args), "nd": nd,
+                   "tensors": len(numels), "elements": lay.total, "padded": lay.padded,
+                   "shard": S, "byte_offsets_mod_16": offs,
+                   "step": "flat_pack of the 9 tensors (1 call), all-gather of the 8 shards "
+                           "(1 call)",
+                   "bytes_per_step": step_bytes,
+                   "l2": f"no flush: each step streams {step_bytes / 1e9:.2f} GB vs a 129 MB L2"},
+        "kernels": {"flat_pack_ms": round(pack_ms, 4), "flat_pack_gbs": round(pack_gbs, 1),
+                    "ag_ms": round(ag_ms, 4), "ag_gbs": round(ag_gbs, 1)},
+        "roofline": _roofline(pack_gbs, "flat_pack: copy16_shift for the tensors at odd "
+                              "offsets, copy16 for the congruent ones, copy_segments for "
+                              "heads, tails and the zero pad", pack_bytes,
+                              _traffic(RAGGED_WORKLOAD, lay.total, args)),
+        "e2e": None, "e2e_note": "device-resident tensors; the end-to-end line is the "
+                                 "default workload's",
+        "gpu_launches": launches, "clocks": clk, "cpu_baseline": cpu}))
+    _finish_dist(world)
+
+
 # ------------------------------------------------------------ checkpoint
 
 CKPT_WORKLOAD = "ckpt_gpt2_small_nd8_to_nd4"
@@ -1285,6 +1428,9 @@ def main():
         return
     if args.workload == CKPT_WORKLOAD:
         run_ckpt(args)
+        return
+    if args.workload == RAGGED_WORKLOAD:
+        run_ragged(args)
         return
     if args.workload == FSDP2_WORKLOAD:
         if args.impl == "reference":
