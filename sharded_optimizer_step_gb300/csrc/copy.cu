@@ -193,9 +193,11 @@ __device__ __forceinline__ void acc_scalar(const uint16_t* g, float* acc, int64_
 }
 
 // One 8-element vector per thread in a one-pass grid (the loop strides only
-// past 2^31 - 1 blocks); 8 blocks per SM, at most 32 registers.  Against a
-// grid-stride loop over one wave of blocks this moved 7.0 vs 6.0 TB/s on
-// GB300 for the first micro-batch and 7.2 vs 6.6 TB/s for the others.
+// past 2^31 - 1 blocks); 8 blocks per SM, at most 32 registers.  On GB300
+// (1.2G elements) this moved 7.0 TB/s for the first micro-batch and 7.2 TB/s
+// for the others, against 6.0 and 6.6 TB/s for the TMA-staged kernel; the
+// same kernel with a grid-stride loop over one wave of blocks moved 5.7 TB/s
+// over a whole accumulation.
 template <bool FIRST>
 __global__ void __launch_bounds__(kThreads, 8)
     accumulate_vec8(const uint16_t* __restrict__ g, float* __restrict__ acc, int64_t n,
