@@ -178,9 +178,9 @@ int fsdp_grad_accumulate(const uint16_t* g, float* acc, int64_t n, float scale, 
  * 8-byte aligned, and two stages of 2048 x (N_d x grad bytes + 12) bytes
  * within the per-block shared-memory limit (N_d <= 21 for bf16, <= 10 for
  * fp32 on GB300); the default for other N_d >= 3; (3) one element per
- * access.  All three compute the same bits.  A TMA-staged launch whose internal wait runs out
- * (about 2 s) sets a bit in the device status word; see
- * shardstep_device_status. 
+ * access.  All three compute the same bits.  A TMA-staged launch whose
+ * internal wait runs out (about 2 s) sets a bit in the device status word;
+ * see shardstep_device_status.
  * Errors: INVALID (null pointer, S < 0, step < 1, bad dtype, overlap),
  * CAPACITY (nd > SHARDSTEP_MAX_ND), CUDA (launch refused). */
 int fsdp_rs_avg_adamw_cast(const void* const* grad_slices, int32_t grad_dtype, int32_t nd,
@@ -210,6 +210,55 @@ int fsdp_hybrid_rs_avg_adamw_cast(const void* const* grad_slices, int32_t grad_d
                                   int32_t shard_group, int64_t S, float* master, float* m,
                                   float* v, uint16_t* out_bf16, const shardstep_adamw_t* hp,
                                   void* stream);
+
+/* ---------------------------------------- device-resident step count */
+
+/* AdamW step state kept in device memory, so that a training step needs no
+ * host work: the advance, the fused update and the all-gather can be
+ * captured once in a CUDA graph and replayed every iteration.  The caller
+ * allocates it (device memory, 8-byte aligned, sizeof 56 bytes); the fields
+ * are written only by the calls below.  The per-step scalars are derived as
+ * the host-scalar entry points derive them, so both give the same bits:
+ * beta^t is the running product of t factors in double, then 1 - beta^t,
+ * lr / (1 - beta1^t), sqrt(1 - beta2^t), lr * wd, 1 - beta, each in double
+ * and rounded once to fp32 (the host does the same from hp->step). */
+typedef struct {
+    int64_t step;         /* t of the scalars below; 0 = none yet          */
+    double beta1_pow;     /* beta1^t                                        */
+    double beta2_pow;     /* beta2^t                                        */
+    float scalars[8];     /* fp32 scalars of step t (layout internal)       */
+} shardstep_adamw_state_t;
+
+/* shardstep_adamw_state_init -- device, one thread.  Sets *state to step
+ * `step` >= 0 of hp's betas (the powers from the host's running product);
+ * for step >= 1 also that step's scalars, so a state restored at the step of
+ * a checkpoint continues exactly.  hp->step is ignored.  Asynchronous on
+ * `stream`.  Errors: INVALID (null or misaligned state, null hp, step < 0),
+ * CUDA. */
+int shardstep_adamw_state_init(shardstep_adamw_state_t* state, const shardstep_adamw_t* hp,
+                               int64_t step, void* stream);
+
+/* shardstep_adamw_state_advance -- device, one thread.  Moves *state from
+ * step t to t + 1 (beta powers times the betas) and derives the scalars of
+ * step t + 1 from hp's lr, betas, eps and weight decay, which the call
+ * passes by value (a captured graph replays the values it was captured
+ * with).  hp->step is ignored.  Errors as shardstep_adamw_state_init. */
+int shardstep_adamw_state_advance(shardstep_adamw_state_t* state, const shardstep_adamw_t* hp,
+                                  void* stream);
+
+/* fsdp_state_rs_avg_adamw_cast -- device, one kernel pass.  The fused step
+ * of fsdp_hybrid_rs_avg_adamw_cast (shard_group = nd: of
+ * fsdp_rs_avg_adamw_cast) with the AdamW scalars read on the device from
+ * *state, which must hold a step >= 1 (an advance or an init with step >= 1
+ * before it in stream order); the result is bit-identical to the host-scalar
+ * call at hp->step = state->step.  The call does no host work that depends
+ * on the step, so it can be captured in a CUDA graph.  Other arguments,
+ * aliasing rules, kernel choice and errors as in
+ * fsdp_hybrid_rs_avg_adamw_cast; INVALID for a null or misaligned state. */
+int fsdp_state_rs_avg_adamw_cast(const void* const* grad_slices, int32_t grad_dtype, int32_t nd,
+                                 int32_t shard_group, int64_t S, float* master, float* m,
+                                 float* v, uint16_t* out_bf16,
+                                 const shardstep_adamw_state_t* state, void* stream);
 
 /* ------------------------------------------------ gradient scaler */
 

@@ -25,7 +25,7 @@ __all__ = [
     "MAX_ND",
     "set_fused_path", "device_status", "fsdp_hybrid_rs_avg_adamw_cast", "hybrid_state_bytes",
     "hybrid_comm_bytes", "Fsdp2Layout", "fsdp2_layout", "fsdp2_local_views", "fsdp2_chunk_cat",
-    "fsdp2_all_gather_copy_out",
+    "fsdp2_all_gather_copy_out", "AdamWState", "fsdp_state_rs_avg_adamw_cast",
 ]
 
 
@@ -209,6 +209,64 @@ def _fused(grad_slices, master, m, v, out_bf16, hp, step, stream, shard_group):
         _capi.check("fsdp_hybrid_rs_avg_adamw_cast", _capi.lib().fsdp_hybrid_rs_avg_adamw_cast(
             ptrs, _dtype_code(grad_slices[0]), len(grad_slices), shard_group, S, *state,
             ctypes.byref(hpc), _stream(stream, master.device)))
+
+
+class AdamWState:
+    """The AdamW step count and its fp32 scalars in device memory
+    (``shardstep_adamw_state_t``), so that a step needs no host work:
+    ``advance`` then ``fsdp_state_rs_avg_adamw_cast`` (and the all-gather)
+    can be captured in a CUDA graph once and replayed every iteration.
+    The hyper-parameters are passed by value at each ``advance``; a captured
+    graph replays the ones it was captured with."""
+
+    def __init__(self, hp: AdamW, step: int = 0, device="cuda", stream=None):
+        import torch
+        self.hp = hp
+        # 56 bytes, 8-byte aligned
+        self.buf = torch.zeros(_capi.ADAMW_STATE_BYTES // 8, dtype=torch.float64, device=device)
+        self.init(step, stream)
+
+    def init(self, step: int, stream=None):
+        """Set the state to step ``step`` (>= 0; scalars too from step 1)."""
+        _capi.check("shardstep_adamw_state_init", _capi.lib().shardstep_adamw_state_init(
+            ctypes.c_void_p(self.buf.data_ptr()), ctypes.byref(self.hp.at_step(1)), int(step),
+            _stream(stream, self.buf.device)))
+
+    def advance(self, stream=None):
+        """Step t -> t + 1 on the device."""
+        _capi.check("shardstep_adamw_state_advance", _capi.lib().shardstep_adamw_state_advance(
+            ctypes.c_void_p(self.buf.data_ptr()), ctypes.byref(self.hp.at_step(1)),
+            _stream(stream, self.buf.device)))
+
+    def step(self) -> int:
+        """The current step count (reads the device; synchronises)."""
+        import torch
+        return int(self.buf[:1].view(torch.int64).item())
+
+
+def fsdp_state_rs_avg_adamw_cast(grad_slices, master, m, v, out_bf16, state: AdamWState,
+                                 shard_group: int | None = None, stream=None):
+    """The fused step (hybrid with ``shard_group`` = F) with the AdamW scalars
+    read on the device from ``state``, which must be at a step >= 1."""
+    import torch
+    if not grad_slices:
+        raise ValueError("need at least one gradient slice")
+    _need_cuda(*grad_slices, master, m, v, out_bf16, state.buf)
+    S = master.numel()
+    for g in grad_slices:
+        if g.dtype != grad_slices[0].dtype or g.numel() != S:
+            raise ValueError("gradient slices must share dtype and have S elements")
+    for t in (master, m, v):
+        if t.dtype != torch.float32 or t.numel() != S:
+            raise ValueError("master / m / v must be fp32 with S elements")
+    if out_bf16.dtype != torch.bfloat16 or out_bf16.numel() != S:
+        raise ValueError("out must be bf16 with S elements")
+    _capi.check("fsdp_state_rs_avg_adamw_cast", _capi.lib().fsdp_state_rs_avg_adamw_cast(
+        _capi.ptr_array([g.data_ptr() for g in grad_slices]), _dtype_code(grad_slices[0]),
+        len(grad_slices), shard_group or len(grad_slices), S, ctypes.c_void_p(master.data_ptr()),
+        ctypes.c_void_p(m.data_ptr()), ctypes.c_void_p(v.data_ptr()),
+        ctypes.c_void_p(out_bf16.data_ptr()), ctypes.c_void_p(state.buf.data_ptr()),
+        _stream(stream, master.device)))
 
 
 # -------------------------------------------------------- gradient scaler

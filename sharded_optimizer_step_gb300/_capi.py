@@ -100,7 +100,14 @@ SIGNATURES = {
     "shardstep_device_status": (c_i32, [ctypes.POINTER(ctypes.c_uint32), c_i32]),
     "shardstep_launch_count": (c_u64, []),
     "shardstep_last_kernel": (ctypes.c_char_p, []),
+    "shardstep_adamw_state_init": (c_i32, [c_vp, ctypes.POINTER(AdamWHP), c_i64, c_vp]),
+    "shardstep_adamw_state_advance": (c_i32, [c_vp, ctypes.POINTER(AdamWHP), c_vp]),
+    "fsdp_state_rs_avg_adamw_cast": (c_i32, [c_vp, c_i32, c_i32, c_i32, c_i64, c_vp, c_vp, c_vp,
+                                             c_vp, c_vp, c_vp]),
 }
+
+# Size in bytes of shardstep_adamw_state_t (int64 step, two doubles, 8 floats).
+ADAMW_STATE_BYTES = 56
 
 _lib = None
 

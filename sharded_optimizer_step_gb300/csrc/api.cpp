@@ -5,6 +5,7 @@
 #include <initializer_list>
 #include <cmath>
 #include <cstdarg>
+#include <cstddef>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -143,7 +144,7 @@ AdamScalars adam_scalars(const shardstep_adamw_t& hp) {
     }
     const double bc1 = 1.0 - b1t;
     const double bc2 = 1.0 - b2t;
-    AdamScalars c;
+    AdamScalars c{};
     c.lr_wd = static_cast<float>(hp.lr * hp.weight_decay);
     c.beta1 = static_cast<float>(hp.beta1);
     c.omb1 = static_cast<float>(1.0 - hp.beta1);
@@ -555,10 +556,13 @@ int take_slices(const void* const* grad_slices, int32_t grad_dtype, int32_t nd, 
 // The fused step with the slices reduced in groups of `group` ranks
 // (group == nd: plain rank order); with `scaled`, the mean is multiplied by
 // inv_scale and a non-zero *skip at launch leaves everything unchanged.
+// `hp` gives the AdamW scalars on the host; with `state` instead, the
+// kernels read them from the device-resident step state.
 int fused_step(const void* const* grad_slices, int32_t grad_dtype, int32_t nd, int32_t group,
                int64_t S, float* master, float* m, float* v, uint16_t* out_bf16,
                const shardstep_adamw_t* hp, void* stream, const float* scale = nullptr,
-               const unsigned int* skip = nullptr) {
+               const unsigned int* skip = nullptr,
+               const shardstep_adamw_state_t* state = nullptr) {
     int rc = SHARDSTEP_OK;
     const int gs = elem_size_of(grad_dtype);
     if (gs == 0) return fail(SHARDSTEP_ERR_INVALID, "unknown grad dtype %d", grad_dtype);
@@ -566,9 +570,18 @@ int fused_step(const void* const* grad_slices, int32_t grad_dtype, int32_t nd, i
     if (nd > SHARDSTEP_MAX_ND)
         return fail(SHARDSTEP_ERR_CAPACITY, "nd %d > %d", nd, SHARDSTEP_MAX_ND);
     if (S < 0) return fail(SHARDSTEP_ERR_INVALID, "S must be >= 0");
-    if (hp == nullptr) return fail(SHARDSTEP_ERR_INVALID, "hp is NULL");
-    if (hp->step < 1) return fail(SHARDSTEP_ERR_INVALID, "step must be >= 1 (got %lld)",
-                                  static_cast<long long>(hp->step));
+    AdamScalars c{};
+    if (state != nullptr) {
+        if (!aligned(state, 8)) return fail(SHARDSTEP_ERR_INVALID, "state misaligned");
+        // the device address of the state's scalars (no host access to it)
+        c.dev = reinterpret_cast<const float*>(reinterpret_cast<const char*>(state) +
+                                               offsetof(shardstep_adamw_state_t, scalars));
+    } else {
+        if (hp == nullptr) return fail(SHARDSTEP_ERR_INVALID, "hp is NULL");
+        if (hp->step < 1) return fail(SHARDSTEP_ERR_INVALID, "step must be >= 1 (got %lld)",
+                                      static_cast<long long>(hp->step));
+        c = adam_scalars(*hp);
+    }
     if (S == 0) return ok();
     if (!master || !m || !v || !out_bf16)
         return fail(SHARDSTEP_ERR_INVALID, "master / m / v / out_bf16 is NULL");
@@ -595,12 +608,10 @@ int fused_step(const void* const* grad_slices, int32_t grad_dtype, int32_t nd, i
     mo.scaled = scale != nullptr;
     mo.scale = scale;
     cudaError_t e =
-        tma ? launch_rs_adamw_cast_tma(tab, nd, grad_dtype, S, master, m, v, out_bf16,
-                                       adam_scalars(*hp), mo, skip,
-                                       static_cast<cudaStream_t>(stream))
-            : launch_rs_adamw_cast(tab, nd, grad_dtype, S, master, m, v, out_bf16,
-                                   adam_scalars(*hp), mo, skip, vec,
-                                   static_cast<cudaStream_t>(stream));
+        tma ? launch_rs_adamw_cast_tma(tab, nd, grad_dtype, S, master, m, v, out_bf16, c, mo,
+                                       skip, static_cast<cudaStream_t>(stream))
+            : launch_rs_adamw_cast(tab, nd, grad_dtype, S, master, m, v, out_bf16, c, mo, skip,
+                                   vec, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "fused step kernel launch");
     if (tma)
         note_kernel("staged_stream<AdamOp<%s>> (TMA-staged)", dtype_name(grad_dtype));
@@ -633,6 +644,47 @@ int fsdp_hybrid_rs_avg_adamw_cast(const void* const* grad_slices, int32_t grad_d
                     "the sharding factor %d must be >= 1 and divide nd = %d", shard_group, nd);
     return fused_step(grad_slices, grad_dtype, nd, shard_group, S, master, m, v, out_bf16, hp,
                       stream);
+}
+
+int fsdp_state_rs_avg_adamw_cast(const void* const* grad_slices, int32_t grad_dtype, int32_t nd,
+                                 int32_t shard_group, int64_t S, float* master, float* m,
+                                 float* v, uint16_t* out_bf16,
+                                 const shardstep_adamw_state_t* state, void* stream) {
+    if (shard_group < 1 || nd < 1 || nd % shard_group != 0)
+        return fail(SHARDSTEP_ERR_INVALID,
+                    "the sharding factor %d must be >= 1 and divide nd = %d", shard_group, nd);
+    if (state == nullptr) return fail(SHARDSTEP_ERR_INVALID, "state is NULL");
+    return fused_step(grad_slices, grad_dtype, nd, shard_group, S, master, m, v, out_bf16,
+                      nullptr, stream, nullptr, nullptr, state);
+}
+
+int shardstep_adamw_state_init(shardstep_adamw_state_t* state, const shardstep_adamw_t* hp,
+                               int64_t step, void* stream) {
+    if (state == nullptr || hp == nullptr) return fail(SHARDSTEP_ERR_INVALID, "state / hp is NULL");
+    if (!aligned(state, 8)) return fail(SHARDSTEP_ERR_INVALID, "state misaligned");
+    if (step < 0) return fail(SHARDSTEP_ERR_INVALID, "step must be >= 0");
+    // the running products of step factors, as adam_scalars forms them
+    double b1p = 1.0, b2p = 1.0;
+    for (int64_t k = 0; k < step; ++k) {
+        b1p *= hp->beta1;
+        b2p *= hp->beta2;
+        if (b1p == 0.0 && b2p == 0.0) break;
+    }
+    cudaError_t e = launch_adamw_state_set(state, step, b1p, b2p, hp->lr, hp->beta1, hp->beta2,
+                                           hp->eps, hp->weight_decay,
+                                           static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "state init launch");
+    return ok();
+}
+
+int shardstep_adamw_state_advance(shardstep_adamw_state_t* state, const shardstep_adamw_t* hp,
+                                  void* stream) {
+    if (state == nullptr || hp == nullptr) return fail(SHARDSTEP_ERR_INVALID, "state / hp is NULL");
+    if (!aligned(state, 8)) return fail(SHARDSTEP_ERR_INVALID, "state misaligned");
+    cudaError_t e = launch_adamw_state_advance(state, hp->lr, hp->beta1, hp->beta2, hp->eps,
+                                               hp->weight_decay, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "state advance launch");
+    return ok();
 }
 
 int fsdp_grad_unscale_check(const void* const* grad_slices, int32_t grad_dtype, int32_t nd,

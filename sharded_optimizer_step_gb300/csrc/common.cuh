@@ -175,6 +175,22 @@ __device__ __forceinline__ float f16_to_f32(uint16_t h) {
 // One AdamW element update, one IEEE rounding per operation, no contraction:
 //   p = p - (lr*wd)*p ; m = b1*m + (1-b1)*g ; v = b2*v + ((1-b2)*g)*g ;
 //   p = p - ((lr/bc1)*m) / (sqrt(v)/sqrt(bc2) + eps)
+// The scalars a kernel computes with: the host's, or those of a device-
+// resident step state (read once per thread at kernel start, through L2).
+__device__ __forceinline__ AdamScalars resolve_adam(AdamScalars c) {
+    if (c.dev != nullptr) {
+        c.lr_wd = __ldcg(c.dev + 0);
+        c.beta1 = __ldcg(c.dev + 1);
+        c.omb1 = __ldcg(c.dev + 2);
+        c.beta2 = __ldcg(c.dev + 3);
+        c.omb2 = __ldcg(c.dev + 4);
+        c.step_size = __ldcg(c.dev + 5);
+        c.sqrt_bc2 = __ldcg(c.dev + 6);
+        c.eps = __ldcg(c.dev + 7);
+    }
+    return c;
+}
+
 __device__ __forceinline__ void adamw_elem(float g, float& p, float& m, float& v,
                                            const AdamScalars& c) {
     p = __fsub_rn(p, __fmul_rn(c.lr_wd, p));

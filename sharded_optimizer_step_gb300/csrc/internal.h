@@ -3,16 +3,31 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <stddef.h>
 #include <stdint.h>
 
 #include "shardstep.h"
 
 namespace shardstep {
 
-// fp32 per-step scalars of the AdamW update (derived on the host in double).
+// fp32 per-step scalars of the AdamW update (derived in double, on the host
+// or by the state-advance kernel).  With `dev` set, each kernel replaces the
+// eight values at its start by the eight floats at dev (the scalars of a
+// device-resident step state, in this field order).
 struct AdamScalars {
     float lr_wd, beta1, omb1, beta2, omb2, step_size, sqrt_bc2, eps;
+    const float* dev;
 };
+static_assert(offsetof(shardstep_adamw_state_t, scalars) == 24, "state layout");
+
+// The device-resident step state (api.cpp / step.cu): init writes step t's
+// powers (and scalars for t >= 1), advance moves t to t + 1.
+cudaError_t launch_adamw_state_set(shardstep_adamw_state_t* state, int64_t step, double b1p,
+                                   double b2p, double lr, double beta1, double beta2, double eps,
+                                   double wd, cudaStream_t stream);
+cudaError_t launch_adamw_state_advance(shardstep_adamw_state_t* state, double lr, double beta1,
+                                       double beta2, double eps, double wd,
+                                       cudaStream_t stream);
 
 // How the reduce turns the N_d rank slices into a mean: the slices are summed
 // in groups of `group` consecutive ranks (group == N_d: one rank-order sum;

@@ -301,10 +301,13 @@ struct AdamOp {
     MeanOp mo;
     const unsigned int* skip;
 
-    using State = MeanOp;
+    struct State {
+        MeanOp mo;
+        AdamScalars c;
+    };
     static constexpr uint32_t gsz = grad_bytes<GT>();
     __device__ bool skipped() const { return skip_step(skip); }
-    __device__ State init() const { return resolve_scale(mo); }
+    __device__ State init() const { return State{resolve_scale(mo), resolve_adam(c)}; }
     __host__ __device__ uint32_t stage_bytes() const {
         return static_cast<uint32_t>(nd) * kTile * gsz + 3u * kTile * 4u;
     }
@@ -318,9 +321,9 @@ struct AdamOp {
         bulk_load(sst + kTile * 4, M + e0, n * 4, bar);
         bulk_load(sst + 2 * kTile * 4, V + e0, n * 4, bar);
     }
-    __device__ void consume(const uint8_t* st, int64_t e0, int e, State& m0) const {
+    __device__ void consume(const uint8_t* st, int64_t e0, int e, State& s) const {
         float g[4];
-        reduce4_smem<GT>(st, nd, m0.group, e, g);
+        reduce4_smem<GT>(st, nd, s.mo.group, e, g);
         const uint8_t* sst = st + nd * (kTile * gsz);
         const float4 pp = *reinterpret_cast<const float4*>(sst + e * 4);
         const float4 mm = *reinterpret_cast<const float4*>(sst + kTile * 4 + e * 4);
@@ -329,16 +332,16 @@ struct AdamOp {
         float m[4] = {mm.x, mm.y, mm.z, mm.w};
         float v[4] = {vv.x, vv.y, vv.z, vv.w};
 #pragma unroll
-        for (int k = 0; k < 4; ++k) adamw_elem(mean_of(g[k], m0), p[k], m[k], v[k], c);
+        for (int k = 0; k < 4; ++k) adamw_elem(mean_of(g[k], s.mo), p[k], m[k], v[k], s.c);
         const int64_t ge = e0 + e;
         stcs16(P + ge, pack4f(p));
         stcs16(M + ge, pack4f(m));
         stcs16(V + ge, pack4f(v));
         stcs8(out + ge, make_uint2(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3])));
     }
-    __device__ void tail(int64_t j, State& m0) const {
+    __device__ void tail(int64_t j, State& s) const {
         float p = P[j], m = M[j], v = V[j];
-        adamw_elem(mean_of(reduce1_global<GT>(tab, nd, m0.group, j), m0), p, m, v, c);
+        adamw_elem(mean_of(reduce1_global<GT>(tab, nd, s.mo.group, j), s.mo), p, m, v, s.c);
         P[j] = p;
         M[j] = m;
         V[j] = v;

@@ -263,3 +263,31 @@ def test_last_kernel_is_empty_until_a_launch():
     t.join()
     assert seen[0] == ""
     assert seen[1][0] < 0 and seen[1][1] == ""
+
+
+class _AdamWState(ctypes.Structure):
+    """shardstep_adamw_state_t as the header declares it."""
+    _fields_ = [("step", ctypes.c_int64), ("beta1_pow", ctypes.c_double),
+                ("beta2_pow", ctypes.c_double), ("scalars", ctypes.c_float * 8)]
+
+
+def test_adamw_state_layout_and_validation():
+    assert ctypes.sizeof(_AdamWState) == _capi.ADAMW_STATE_BYTES == 56
+    assert _AdamWState.scalars.offset == 24
+    L = _capi.lib()
+    hp = ss.AdamW().at_step(1)
+    # rejected before any launch: no state, no hp, a misaligned state, a negative step
+    assert L.shardstep_adamw_state_init(None, ctypes.byref(hp), 0, None) < 0
+    assert "NULL" in L.shardstep_last_error().decode()
+    assert L.shardstep_adamw_state_init(ctypes.c_void_p(4096), None, 0, None) < 0
+    assert L.shardstep_adamw_state_init(ctypes.c_void_p(4100), ctypes.byref(hp), 0, None) < 0
+    assert "misaligned" in L.shardstep_last_error().decode()
+    assert L.shardstep_adamw_state_init(ctypes.c_void_p(4096), ctypes.byref(hp), -1, None) < 0
+    assert L.shardstep_adamw_state_advance(None, ctypes.byref(hp), None) < 0
+    assert L.shardstep_adamw_state_advance(ctypes.c_void_p(4100), ctypes.byref(hp), None) < 0
+    ptrs = _capi.ptr_array([4096])
+    assert L.fsdp_state_rs_avg_adamw_cast(ptrs, 0, 1, 1, 16, None, None, None, None, None,
+                                          None) < 0
+    assert "state is NULL" in L.shardstep_last_error().decode()
+    assert L.fsdp_state_rs_avg_adamw_cast(ptrs, 0, 4, 3, 16, None, None, None, None,
+                                          ctypes.c_void_p(4096), None) < 0
