@@ -15,8 +15,8 @@ from __future__ import annotations
 
 import torch
 
-from . import (AdamW, fsdp_ag_unpack, fsdp_hybrid_rs_avg_adamw_cast, fsdp_layout,
-               fsdp_rs_avg_adamw_cast, fsdp_views)
+from . import (AdamW, AdamWState, fsdp_ag_unpack, fsdp_hybrid_rs_avg_adamw_cast, fsdp_layout,
+               fsdp_rs_avg_adamw_cast, fsdp_state_rs_avg_adamw_cast, fsdp_views)
 
 
 def _numel(shape):
@@ -81,6 +81,21 @@ class RankShardOptimizer:
         sl = slice(a, b)
         self._update([g[sl] for g in self.grad_in], self.master[sl], self.m[sl], self.v[sl],
                      self.params[sl], stream)
+
+    def device_step_state(self) -> AdamWState:
+        """Moves the step count to the device (an ``AdamWState`` at the
+        current count) for ``step_on_device``; returns it."""
+        self.state = AdamWState(self.hp, self.t, device=self.master.device)
+        return self.state
+
+    def step_on_device(self, stream=None):
+        """The step of ``step`` with the count advanced and the AdamW scalars
+        derived on the device: the same launches every call, so it can be
+        captured in a CUDA graph.  Needs ``device_step_state`` first; the
+        host count ``t`` is not advanced."""
+        self.state.advance(stream)
+        fsdp_state_rs_avg_adamw_cast(self.grad_in, self.master, self.m, self.v, self.params,
+                                     self.state, shard_group=self.F, stream=stream)
 
     def gather_unit(self, u, peer_shards, full, stream=None):
         """All-gather unit u inside the rank's shard group: ``peer_shards[q]``

@@ -125,7 +125,6 @@ def test_state_restored_at_a_step_continues_exactly(k):
     nd, S = 8, 6151
     a = _Shard(S, 3)
     b = a.clone()
-    c = a.clone()
     g = _grads(nd, S, torch.bfloat16, 3, k)
     # init at step k carries step k's scalars; one advance gives step k + 1's
     st = ss.AdamWState(HP, k, device=DEV)
@@ -139,7 +138,6 @@ def test_state_restored_at_a_step_continues_exactly(k):
     torch.cuda.synchronize()
     a.assert_equal(b, f"advanced to {k + 1}")
     assert st.step() == k + 1
-    del c
 
 
 @pytest.mark.parametrize("path_name", ["auto", "tma"])
@@ -203,3 +201,39 @@ def test_step_captured_in_a_cuda_graph_replays_as_consecutive_steps(path_name):
         assert st.step() == 4
     finally:
         ss.set_fused_path(prev)
+
+
+def test_rank_optimizer_step_on_device_in_a_graph():
+    """RankShardOptimizer.step_on_device captured once equals step() run
+    eagerly, over three replays of a two-unit hybrid rank view."""
+    from sharded_optimizer_step_gb300.engine import RankShardOptimizer
+    units = [[(300, 40), (40,)], [(97, 13)]]
+    a = RankShardOptimizer(units, 8, 1, HP, device=DEV, shard_group=4)
+    b = RankShardOptimizer(units, 8, 1, HP, device=DEV, shard_group=4)
+    synth.dev_fill(synth.normal_stream(4, (88, 1), 0.02), a.master)
+    b.master.copy_(a.master)
+    b.device_step_state()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):           # warm-up, then undone
+        b.step_on_device()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    b.master.copy_(a.master)
+    b.m.zero_()
+    b.v.zero_()
+    b.state.init(0)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        b.step_on_device()
+    for t in range(1, 4):
+        for q in range(8):
+            synth.dev_fill(synth.normal_stream(4, (88, 2, t, q), 1e-3), a.grad_in[q])
+            b.grad_in[q].copy_(a.grad_in[q])
+        a.step()
+        g.replay()
+        torch.cuda.synchronize()
+        for x, y in ((a.master, b.master), (a.m, b.m), (a.v, b.v)):
+            assert torch.equal(x.view(torch.int32), y.view(torch.int32)), t
+        assert torch.equal(a.params.view(torch.int16), b.params.view(torch.int16)), t
+    assert b.state.step() == 3
