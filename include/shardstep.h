@@ -242,9 +242,14 @@ int shardstep_adamw_state_init(shardstep_adamw_state_t* state, const shardstep_a
  * step t to t + 1 (beta powers times the betas) and derives the scalars of
  * step t + 1 from hp's lr, betas, eps and weight decay, which the call
  * passes by value (a captured graph replays the values it was captured
- * with).  hp->step is ignored.  Errors as shardstep_adamw_state_init. */
+ * with).  hp->step is ignored.
+ *   skip   NULL, or a device word: when it holds a non-zero value as the
+ *          kernel runs, the state is left unchanged -- pass the gradient
+ *          scaler's found_inf so that a skipped step does not count, as an
+ *          optimizer step that the scaler skips does not.
+ * Errors as shardstep_adamw_state_init, and INVALID for a misaligned skip. */
 int shardstep_adamw_state_advance(shardstep_adamw_state_t* state, const shardstep_adamw_t* hp,
-                                  void* stream);
+                                  const uint32_t* skip, void* stream);
 
 /* fsdp_state_rs_avg_adamw_cast -- device, one kernel pass.  The fused step
  * of fsdp_hybrid_rs_avg_adamw_cast (shard_group = nd: of
@@ -289,6 +294,20 @@ int fsdp_state_rs_avg_adamw_cast(const void* const* grad_slices, int32_t grad_dt
 int fsdp_grad_unscale_check(const void* const* grad_slices, int32_t grad_dtype, int32_t nd,
                             int32_t shard_group, int64_t S, const float* scale,
                             uint32_t* found_inf, void* stream);
+
+/* fsdp_state_scaled_rs_avg_adamw_cast -- device, one kernel pass.  The step
+ * of fsdp_scaled_rs_avg_adamw_cast (unscaled by 1 / *scale, skipped when
+ * *found_inf is non-zero) with the AdamW scalars read from *state, as in
+ * fsdp_state_rs_avg_adamw_cast.  With the check before it, an advance
+ * whose skip word is found_inf and fsdp_grad_scaler_update after it, the
+ * whole loss-scaled step runs from device words and can be captured in a
+ * CUDA graph.  Arguments and errors as fsdp_scaled_rs_avg_adamw_cast, with
+ * state in place of hp. */
+int fsdp_state_scaled_rs_avg_adamw_cast(const void* const* grad_slices, int32_t grad_dtype,
+                                        int32_t nd, int32_t shard_group, int64_t S,
+                                        float* master, float* m, float* v, uint16_t* out_bf16,
+                                        const shardstep_adamw_state_t* state, const float* scale,
+                                        const uint32_t* found_inf, void* stream);
 
 /* fsdp_scaled_rs_avg_adamw_cast -- device, one kernel pass.  The fused step
  * of fsdp_hybrid_rs_avg_adamw_cast on the unscaled gradient

@@ -232,10 +232,14 @@ class AdamWState:
             ctypes.c_void_p(self.buf.data_ptr()), ctypes.byref(self.hp.at_step(1)), int(step),
             _stream(stream, self.buf.device)))
 
-    def advance(self, stream=None):
-        """Step t -> t + 1 on the device."""
+    def advance(self, skip=None, stream=None):
+        """Step t -> t + 1 on the device; with ``skip`` (a device int32 word,
+        e.g. a GradScaler's ``found_inf``) non-zero when it runs, no change."""
+        if skip is not None:
+            _need_cuda(skip)
         _capi.check("shardstep_adamw_state_advance", _capi.lib().shardstep_adamw_state_advance(
             ctypes.c_void_p(self.buf.data_ptr()), ctypes.byref(self.hp.at_step(1)),
+            ctypes.c_void_p(skip.data_ptr() if skip is not None else None),
             _stream(stream, self.buf.device)))
 
     def step(self) -> int:
@@ -312,6 +316,26 @@ class GradScaler:
             ctypes.c_void_p(out_bf16.data_ptr()), ctypes.byref(hpc),
             ctypes.c_void_p(self.scale.data_ptr()), ctypes.c_void_p(self.found_inf.data_ptr()),
             _stream(stream, master.device)))
+
+    def step_state(self, grad_slices, master, m, v, out_bf16, state, shard_group: int | None = None,
+                   stream=None):
+        """``step`` with the AdamW scalars read on the device from ``state``
+        (an ``AdamWState``): with ``check`` before it, ``state.advance(
+        skip=self.found_inf)`` and ``update`` after, a loss-scaled step made
+        of device words only, which a CUDA graph can capture."""
+        _need_cuda(*grad_slices, master, m, v, out_bf16, state.buf)
+        S = master.numel()
+        nd = len(grad_slices)
+        _capi.check("fsdp_state_scaled_rs_avg_adamw_cast",
+                    _capi.lib().fsdp_state_scaled_rs_avg_adamw_cast(
+                        _capi.ptr_array([g.data_ptr() for g in grad_slices]),
+                        _dtype_code(grad_slices[0]), nd, shard_group or nd, S,
+                        ctypes.c_void_p(master.data_ptr()), ctypes.c_void_p(m.data_ptr()),
+                        ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(out_bf16.data_ptr()),
+                        ctypes.c_void_p(state.buf.data_ptr()),
+                        ctypes.c_void_p(self.scale.data_ptr()),
+                        ctypes.c_void_p(self.found_inf.data_ptr()),
+                        _stream(stream, master.device)))
 
     def update(self, stream=None):
         """Back off or grow the scale and reset ``found_inf``."""

@@ -101,7 +101,9 @@ SIGNATURES = {
     "shardstep_launch_count": (c_u64, []),
     "shardstep_last_kernel": (ctypes.c_char_p, []),
     "shardstep_adamw_state_init": (c_i32, [c_vp, ctypes.POINTER(AdamWHP), c_i64, c_vp]),
-    "shardstep_adamw_state_advance": (c_i32, [c_vp, ctypes.POINTER(AdamWHP), c_vp]),
+    "shardstep_adamw_state_advance": (c_i32, [c_vp, ctypes.POINTER(AdamWHP), c_vp, c_vp]),
+    "fsdp_state_scaled_rs_avg_adamw_cast": (c_i32, [c_vp, c_i32, c_i32, c_i32, c_i64, c_vp, c_vp,
+                                                    c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
     "fsdp_state_rs_avg_adamw_cast": (c_i32, [c_vp, c_i32, c_i32, c_i32, c_i64, c_vp, c_vp, c_vp,
                                              c_vp, c_vp, c_vp]),
 }

@@ -678,11 +678,13 @@ int shardstep_adamw_state_init(shardstep_adamw_state_t* state, const shardstep_a
 }
 
 int shardstep_adamw_state_advance(shardstep_adamw_state_t* state, const shardstep_adamw_t* hp,
-                                  void* stream) {
+                                  const uint32_t* skip, void* stream) {
     if (state == nullptr || hp == nullptr) return fail(SHARDSTEP_ERR_INVALID, "state / hp is NULL");
     if (!aligned(state, 8)) return fail(SHARDSTEP_ERR_INVALID, "state misaligned");
+    if (skip != nullptr && !aligned(skip, 4)) return fail(SHARDSTEP_ERR_INVALID, "skip misaligned");
     cudaError_t e = launch_adamw_state_advance(state, hp->lr, hp->beta1, hp->beta2, hp->eps,
-                                               hp->weight_decay, static_cast<cudaStream_t>(stream));
+                                               hp->weight_decay, skip,
+                                               static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "state advance launch");
     return ok();
 }
@@ -723,6 +725,23 @@ int fsdp_grad_unscale_check(const void* const* grad_slices, int32_t grad_dtype, 
     else
         note_kernel("nonfinite_check_scalar<%s>", dtype_name(grad_dtype));
     return ok();
+}
+
+int fsdp_state_scaled_rs_avg_adamw_cast(const void* const* grad_slices, int32_t grad_dtype,
+                                        int32_t nd, int32_t shard_group, int64_t S,
+                                        float* master, float* m, float* v, uint16_t* out_bf16,
+                                        const shardstep_adamw_state_t* state, const float* scale,
+                                        const uint32_t* found_inf, void* stream) {
+    if (shard_group < 1 || nd < 1 || nd % shard_group != 0)
+        return fail(SHARDSTEP_ERR_INVALID,
+                    "the sharding factor %d must be >= 1 and divide nd = %d", shard_group, nd);
+    if (state == nullptr) return fail(SHARDSTEP_ERR_INVALID, "state is NULL");
+    if (found_inf == nullptr || scale == nullptr)
+        return fail(SHARDSTEP_ERR_INVALID, "found_inf / scale is NULL");
+    if (!aligned(found_inf, 4) || !aligned(scale, 4))
+        return fail(SHARDSTEP_ERR_INVALID, "found_inf / scale misaligned");
+    return fused_step(grad_slices, grad_dtype, nd, shard_group, S, master, m, v, out_bf16,
+                      nullptr, stream, scale, found_inf, state);
 }
 
 int fsdp_scaled_rs_avg_adamw_cast(const void* const* grad_slices, int32_t grad_dtype, int32_t nd,

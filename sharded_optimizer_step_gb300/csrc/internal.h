@@ -27,7 +27,7 @@ cudaError_t launch_adamw_state_set(shardstep_adamw_state_t* state, int64_t step,
                                    double wd, cudaStream_t stream);
 cudaError_t launch_adamw_state_advance(shardstep_adamw_state_t* state, double lr, double beta1,
                                        double beta2, double eps, double wd,
-                                       cudaStream_t stream);
+                                       const unsigned int* skip, cudaStream_t stream);
 
 // How the reduce turns the N_d rank slices into a mean: the slices are summed
 // in groups of `group` consecutive ranks (group == N_d: one rank-order sum;

@@ -315,50 +315,6 @@ __global__ void scaler_update_kernel(float* scale, int* tracker, unsigned int* f
     *found = 0u;
 }
 
-// ------------------------------------------- device-resident step state
-
-// Step t's fp32 scalars from the powers beta1^t, beta2^t, in AdamScalars'
-// field order: every value formed in double (IEEE round to nearest) and
-// rounded once to fp32, the operations the host performs for hp->step = t.
-__device__ void derive_adam_scalars(float* out, double b1p, double b2p, double lr, double beta1,
-                                    double beta2, double eps, double wd) {
-    out[0] = __double2float_rn(__dmul_rn(lr, wd));
-    out[1] = __double2float_rn(beta1);
-    out[2] = __double2float_rn(__dsub_rn(1.0, beta1));
-    out[3] = __double2float_rn(beta2);
-    out[4] = __double2float_rn(__dsub_rn(1.0, beta2));
-    out[5] = __double2float_rn(__ddiv_rn(lr, __dsub_rn(1.0, b1p)));
-    out[6] = __double2float_rn(__dsqrt_rn(__dsub_rn(1.0, b2p)));
-    out[7] = __double2float_rn(eps);
-}
-
-__global__ void adamw_state_set_kernel(shardstep_adamw_state_t* st, int64_t step, double b1p,
-                                       double b2p, double lr, double beta1, double beta2,
-                                       double eps, double wd) {
-    if (threadIdx.x != 0 || blockIdx.x != 0) return;
-    st->step = step;
-    st->beta1_pow = b1p;
-    st->beta2_pow = b2p;
-    if (step >= 1) {
-        derive_adam_scalars(st->scalars, b1p, b2p, lr, beta1, beta2, eps, wd);
-    } else {
-        for (int k = 0; k < 8; ++k) st->scalars[k] = 0.0f;
-    }
-}
-
-// t -> t + 1: each power times its beta (the next factor of the host's
-// running product), then step t + 1's scalars.
-__global__ void adamw_state_advance_kernel(shardstep_adamw_state_t* st, double lr, double beta1,
-                                           double beta2, double eps, double wd) {
-    if (threadIdx.x != 0 || blockIdx.x != 0) return;
-    const double b1p = __dmul_rn(st->beta1_pow, beta1);
-    const double b2p = __dmul_rn(st->beta2_pow, beta2);
-    st->step += 1;
-    st->beta1_pow = b1p;
-    st->beta2_pow = b2p;
-    derive_adam_scalars(st->scalars, b1p, b2p, lr, beta1, beta2, eps, wd);
-}
-
 // --------------------------------------------------------------- launch
 
 unsigned grid_for(const void* kernel, int64_t work_items, int threads = kThreads) {
@@ -522,23 +478,6 @@ cudaError_t launch_nonfinite_check(const PtrTable& tab, int nd, int grad_type, i
         case kGradF16: return dispatch_check<kGradF16>(tab, nd, S, mo, found, vec, stream);
         default: return dispatch_check<kGradBF16>(tab, nd, S, mo, found, vec, stream);
     }
-}
-
-cudaError_t launch_adamw_state_set(shardstep_adamw_state_t* state, int64_t step, double b1p,
-                                   double b2p, double lr, double beta1, double beta2, double eps,
-                                   double wd, cudaStream_t stream) {
-    adamw_state_set_kernel<<<1, 32, 0, stream>>>(state, step, b1p, b2p, lr, beta1, beta2, eps,
-                                                 wd);
-    note_launch();
-    return cudaGetLastError();
-}
-
-cudaError_t launch_adamw_state_advance(shardstep_adamw_state_t* state, double lr, double beta1,
-                                       double beta2, double eps, double wd,
-                                       cudaStream_t stream) {
-    adamw_state_advance_kernel<<<1, 32, 0, stream>>>(state, lr, beta1, beta2, eps, wd);
-    note_launch();
-    return cudaGetLastError();
 }
 
 cudaError_t launch_scaler_update(float* scale, int* tracker, unsigned int* found, float growth,

@@ -93,7 +93,7 @@ class RankShardOptimizer:
         derived on the device: the same launches every call, so it can be
         captured in a CUDA graph.  Needs ``device_step_state`` first; the
         host count ``t`` is not advanced."""
-        self.state.advance(stream)
+        self.state.advance(stream=stream)
         fsdp_state_rs_avg_adamw_cast(self.grad_in, self.master, self.m, self.v, self.params,
                                      self.state, shard_group=self.F, stream=stream)
 

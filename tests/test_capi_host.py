@@ -283,8 +283,12 @@ def test_adamw_state_layout_and_validation():
     assert L.shardstep_adamw_state_init(ctypes.c_void_p(4100), ctypes.byref(hp), 0, None) < 0
     assert "misaligned" in L.shardstep_last_error().decode()
     assert L.shardstep_adamw_state_init(ctypes.c_void_p(4096), ctypes.byref(hp), -1, None) < 0
-    assert L.shardstep_adamw_state_advance(None, ctypes.byref(hp), None) < 0
-    assert L.shardstep_adamw_state_advance(ctypes.c_void_p(4100), ctypes.byref(hp), None) < 0
+    assert L.shardstep_adamw_state_advance(None, ctypes.byref(hp), None, None) < 0
+    assert L.shardstep_adamw_state_advance(ctypes.c_void_p(4100), ctypes.byref(hp), None,
+                                           None) < 0
+    assert L.shardstep_adamw_state_advance(ctypes.c_void_p(4096), ctypes.byref(hp),
+                                           ctypes.c_void_p(4098), None) < 0
+    assert "skip misaligned" in L.shardstep_last_error().decode()
     ptrs = _capi.ptr_array([4096])
     assert L.fsdp_state_rs_avg_adamw_cast(ptrs, 0, 1, 1, 16, None, None, None, None, None,
                                           None) < 0

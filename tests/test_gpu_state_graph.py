@@ -237,3 +237,63 @@ def test_rank_optimizer_step_on_device_in_a_graph():
             assert torch.equal(x.view(torch.int32), y.view(torch.int32)), t
         assert torch.equal(a.params.view(torch.int16), b.params.view(torch.int16)), t
     assert b.state.step() == 3
+
+
+def test_loss_scaled_step_captured_in_a_cuda_graph():
+    """check + advance (skipped with found_inf) + scaled update from the
+    state + scale update, captured once and replayed over four iterations,
+    the second with an inf in one gradient: equal to the host path in which
+    the skipped step does not count (AdamW steps 1, -, 2, 3); the scale
+    backs off once and the state's count ends at 3."""
+    nd, S = 8, 6151 * 4
+    a = _Shard(S, 21)
+    b = a.clone()
+    sa = ss.GradScaler(init_scale=1024.0, device=DEV)
+    sb = ss.GradScaler(init_scale=1024.0, device=DEV)
+    st = ss.AdamWState(HP, 0, device=DEV)
+    g_in = [torch.empty(S, dtype=torch.float16, device=DEV) for _ in range(nd)]
+    for q in range(nd):
+        synth.dev_fill(synth.normal_stream(21, (87, 0, q), 1e-3 * 1024.0), g_in[q])
+
+    def step_b():
+        sb.check(g_in)
+        st.advance(skip=sb.found_inf)
+        sb.step_state(g_in, b.master, b.m, b.v, b.out, st)
+        sb.update()
+
+    b0 = b.clone()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):            # warm-up, then undone
+        step_b()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    b = b0
+    sb.scale.fill_(1024.0)
+    sb.tracker.zero_()
+    sb.found_inf.zero_()
+    st.init(0)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step_b()
+    t_host = 0
+    for it in range(4):
+        fresh = [torch.empty(S, dtype=torch.float16, device=DEV) for _ in range(nd)]
+        for q in range(nd):
+            synth.dev_fill(synth.normal_stream(21, (87, it + 1, q), 1e-3 * 1024.0), fresh[q])
+        if it == 1:
+            fresh[3][17] = float("inf")
+        for q in range(nd):
+            g_in[q].copy_(fresh[q])
+        skipped = it == 1
+        if not skipped:
+            t_host += 1
+        sa.check(fresh)
+        sa.step(fresh, a.master, a.m, a.v, a.out, HP, max(t_host, 1))
+        sa.update()
+        graph.replay()
+        torch.cuda.synchronize()
+        a.assert_equal(b, f"iteration {it}")
+        assert sa.scale.item() == sb.scale.item()
+        assert st.step() == t_host
+    assert sa.scale.item() == 512.0
