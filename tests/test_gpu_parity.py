@@ -567,7 +567,7 @@ def test_bucket_allreduce_dependent_launches_keep_stream_order(dependent, path):
 
 def test_auto_path_names_the_kernel_it_launched():
     """The automatic choice, as shardstep_last_kernel reports it: the
-    register-staged fused kernel at N_d = 8, the TMA-staged one at N_d = 6,
+    register-staged fused kernel at N_d = 8, the TMA-staged one at N_d = 7,
     TMA-staged whenever forced."""
     S = 8192
     master = torch.zeros(S, device=DEV)
@@ -577,7 +577,7 @@ def test_auto_path_names_the_kernel_it_launched():
     prev = ss.set_fused_path("auto")
     try:
         for nd, want in [(8, "rs_adamw_cast_vec4<8, bf16> (register-staged)"),
-                         (6, "staged_stream<AdamOp<bf16>> (TMA-staged)")]:
+                         (7, "staged_stream<AdamOp<bf16>> (TMA-staged)")]:
             g = [torch.zeros(S, dtype=torch.bfloat16, device=DEV) for _ in range(nd)]
             ss.fsdp_rs_avg_adamw_cast(g, master, m, v, out, HPC, 1)
             assert ss.last_kernel() == want
