@@ -925,6 +925,65 @@ def run_ragged(args):
     _finish_dist(world)
 
 
+def run_fsdp2_reference(args):
+    """The oracle's FSDP2 group step (chunk-cat of every rank's gradients,
+    the fused update of every rank's local buffer, all-gather copy-out) on
+    the Llama-7B layer group with every dimension 0 divided by 16, numpy on
+    one core; rank 0 alone under torchrun."""
+    import numpy as np
+    import oracle
+    import synth
+    from oracle.numerics import AdamWConfig
+    from synth import workloads as W
+    world, rank, _ = dist_env()
+    init_dist(world)
+    if rank == 0:
+        w = W.llama_7b_rank_view()
+        shapes = [(max(1, sh[0] // 16),) + tuple(sh[1:]) for sh in w.units[0]]
+        nd = w.nd
+        lay = oracle.fsdp2_layout(shapes, nd)
+        hp = AdamWConfig(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
+        n = sum(math.prod(sh) for sh in shapes)
+        grads = [[synth.host_fill(synth.normal_stream(19, (86, q, k), 1e-3), 0, math.prod(sh),
+                                  "bf16").reshape(sh) for k, sh in enumerate(shapes)]
+                 for q in range(nd)]
+        master = oracle.chunk_cat([synth.host_fill(synth.normal_stream(19, (85, k), 0.02), 0,
+                                                   math.prod(sh), "f32").reshape(sh)
+                                   for k, sh in enumerate(shapes)], lay)
+        m = np.zeros_like(master)
+        v = np.zeros_like(master)
+        L = lay.local
+        cc_b, fused_b, ag_b = _fsdp2_bytes(shapes, nd, L)
+        tt = 0.0
+        for k in range(args.warmup + args.steps):
+            t0 = time.perf_counter()
+            rs_in = [oracle.chunk_cat(grads[q], lay) for q in range(nd)]
+            outs = []
+            for r in range(nd):
+                sl = slice(r * L, (r + 1) * L)
+                p1, m1, v1, o1 = oracle.fsdp_shard_step([x for x in rs_in], r, L, master[sl],
+                                                        m[sl], v[sl], hp, k + 1)
+                master[sl], m[sl], v[sl] = p1, m1, v1
+                outs.append(o1)
+            oracle.all_gather_copy_out(outs, lay)
+            if k >= args.warmup:
+                tt += time.perf_counter() - t0
+        val = (cc_b + fused_b + ag_b) * args.steps / tt / 1e9
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": round(val, 4), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(tt / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": FSDP2_WORKLOAD, "nd": nd,
+                       "sample": f"the layer group with dimension 0 divided by 16 ({n} elements)"},
+            "cpu_baseline": {"value": round(val, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": "each step: chunk-cat, 8 fused updates and the copy-out "
+                                       "of the scaled-down group, numpy single-threaded"},
+            "e2e": {"value": round(val, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}))
+    _finish_dist(world)
+
+
 # ------------------------------------------------------------ checkpoint
 
 CKPT_WORKLOAD = "ckpt_gpt2_small_nd8_to_nd4"
@@ -1434,8 +1493,7 @@ def main():
         return
     if args.workload == FSDP2_WORKLOAD:
         if args.impl == "reference":
-            print(json.dumps({"impl": "reference", "unavailable":
-                              "the FSDP2 group line has no CPU arm; use the default workload"}))
+            run_fsdp2_reference(args)
             return
         run_fsdp2(args)
     elif args.impl == "reference":

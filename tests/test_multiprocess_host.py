@@ -134,7 +134,8 @@ def test_sharded_step_across_two_processes_equals_the_emulation():
 
 
 @pytest.mark.parametrize("workload", ["llama_7b_rank0_nd8", "llama_1b_rank0_nd8_m4",
-                                      "ddp_nd8_buckets", "llama_7b_layer_ragged_nd8"])
+                                      "ddp_nd8_buckets", "llama_7b_layer_ragged_nd8",
+                                      "llama_7b_fsdp2_layer_nd8"])
 def test_reference_arm_under_torchrun_prints_once(workload):
     """Launched the way the N > 1 runs are, the oracle arm runs on rank 0
     alone and prints one JSON line; the other rank exits 0."""
