@@ -989,6 +989,74 @@ def run_fsdp2_reference(args):
 CKPT_WORKLOAD = "ckpt_gpt2_small_nd8_to_nd4"
 
 
+def run_ckpt_reference(args):
+    """The same checkpoint with numpy on the host: the 8 ranks' fp32 master /
+    m / v shards of every unit written with numpy.save, then the 4 new
+    ranks' shards read back and resharded by the oracle; rank 0 alone."""
+    import shutil
+    import numpy as np
+    import synth
+    from oracle import checkpoint as oracle_ckpt
+    from synth import workloads as W
+    world, rank, _ = dist_env()
+    init_dist(world)
+    if rank == 0:
+        w = W.gpt2_small()
+        totals = [sum(math.prod(sh) for sh in u) for u in w.units]
+        old_nd, new_nd = 8, 4
+        shards = {}                     # (rank, unit, kind) -> fp32 array
+        for u, T in enumerate(totals):
+            S = -(-T // old_nd)
+            for kind in range(3):
+                flat = np.zeros(S * old_nd, np.float32)
+                flat[:T] = synth.host_fill(synth.normal_stream(23, (84, u, kind), 0.02), 0, T,
+                                           "f32")
+                for r in range(old_nd):
+                    shards[(r, u, kind)] = flat[r * S:(r + 1) * S].copy()
+        state_bytes = sum(a.nbytes for a in shards.values())
+        root = tempfile.mkdtemp(prefix="shst_ckref_")
+        saves, loads = [], []
+        try:
+            for k in range(args.warmup + max(1, args.steps)):
+                d = os.path.join(root, f"step{k}")
+                os.makedirs(d)
+                t0 = time.perf_counter()
+                for (r, u, kind), a in shards.items():
+                    np.save(os.path.join(d, f"{r}_{u}_{kind}.npy"), a)
+                t1 = time.perf_counter()
+                for u, T in enumerate(totals):
+                    for kind in range(3):
+                        old = [np.load(os.path.join(d, f"{r}_{u}_{kind}.npy"))
+                               for r in range(old_nd)]
+                        for nr in range(new_nd):
+                            oracle_ckpt.reshard(old, T, new_nd, nr)
+                t2 = time.perf_counter()
+                if k >= args.warmup:
+                    saves.append(t1 - t0)
+                    loads.append(t2 - t1)
+                shutil.rmtree(d, ignore_errors=True)
+        finally:
+            shutil.rmtree(root, ignore_errors=True)
+        sv, ld = statistics.median(saves), statistics.median(loads)
+        val = state_bytes / sv / 1e9
+        print(json.dumps({
+            "impl": "reference",
+            "metric": "sharded checkpoint save / load GB/s (fp32 master + moments)",
+            "value": round(val, 3), "unit": "GB/s", "n_gpus": world, "steps": len(saves),
+            "warmup": args.warmup, "ms_per_step": round(1e3 * (sv + ld), 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": CKPT_WORKLOAD, "old_nd": old_nd, "new_nd": new_nd,
+                       "state_bytes": state_bytes, "load_gbs": round(state_bytes / ld / 1e9, 3)},
+            "cpu_baseline": {"value": round(val, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": "the whole GPT-2-small optimizer state: numpy.save per "
+                                       "rank, unit and kind, then numpy.load + the oracle's "
+                                       "reshard for the 4 new ranks"},
+            "e2e": {"value": round(val, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}))
+    _finish_dist(world)
+
+
 def run_ckpt(args):
     """Sharded checkpoint of the GPT-2-small-shaped model: every one of 8
     ranks saves its fp32 master / m / v shards (device -> pinned host -> its
@@ -1486,7 +1554,10 @@ def main():
         run_ddp(args)
         return
     if args.workload == CKPT_WORKLOAD:
-        run_ckpt(args)
+        if args.impl == "reference":
+            run_ckpt_reference(args)
+        else:
+            run_ckpt(args)
         return
     if args.workload == RAGGED_WORKLOAD:
         run_ragged(args)
