@@ -297,3 +297,36 @@ def test_loss_scaled_step_captured_in_a_cuda_graph():
         assert sa.scale.item() == sb.scale.item()
         assert st.step() == t_host
     assert sa.scale.item() == 512.0
+
+
+@pytest.mark.parametrize("S", [1, 3, 5, 4097])
+def test_state_step_on_ragged_and_tiny_shards(S, path):
+    """Shards of a few elements (the tail that block 0 handles) and a ragged
+    one, 3 steps, against the host-scalar call."""
+    nd = 4
+    a = _Shard(S, 40 + S)
+    b = a.clone()
+    st = ss.AdamWState(HP, 0, device=DEV)
+    for t in range(1, 4):
+        g = _grads(nd, S, torch.bfloat16, 40 + S, t)
+        ss.fsdp_rs_avg_adamw_cast(g, a.master, a.m, a.v, a.out, HP, t)
+        st.advance()
+        ss.fsdp_state_rs_avg_adamw_cast(g, b.master, b.m, b.v, b.out, st)
+        torch.cuda.synchronize()
+        a.assert_equal(b, f"S={S} step {t}")
+
+
+def test_state_at_a_late_step():
+    """Restored at step 10^6 (the beta powers long underflowed or tiny) and
+    advanced once: the bits of the host-scalar call at 10^6 + 1."""
+    nd, S = 2, 8191
+    a = _Shard(S, 77)
+    b = a.clone()
+    g = _grads(nd, S, torch.bfloat16, 77, 1)
+    st = ss.AdamWState(HP, 10 ** 6, device=DEV)
+    st.advance()
+    ss.fsdp_rs_avg_adamw_cast(g, a.master, a.m, a.v, a.out, HP, 10 ** 6 + 1)
+    ss.fsdp_state_rs_avg_adamw_cast(g, b.master, b.m, b.v, b.out, st)
+    torch.cuda.synchronize()
+    a.assert_equal(b, "late step")
+    assert st.step() == 10 ** 6 + 1
