@@ -81,6 +81,10 @@ def parse():
     ap.add_argument("--kernel-path", choices=["auto", "register", "tma"], default="auto",
                     help="streaming kernels: TMA-staged where they measured faster (auto), "
                          "register-staged only, or TMA-staged wherever the arguments allow")
+    ap.add_argument("--graph", action="store_true",
+                    help="default / hybrid lines: the step count and AdamW scalars on the "
+                         "device, the fused update and the all-gather replayed from CUDA "
+                         "graphs captured once")
     ap.add_argument("--no-dependent-launch", action="store_true",
                     help="launch every bucket of an all-reduce call as an ordinary launch")
     ap.add_argument("--no-e2e", action="store_true")
@@ -321,6 +325,39 @@ def run_ours(args):
         if ev is not None:
             ev[3].record(stream)
 
+    graph_launches = 0
+    if args.graph:
+        if scaled:
+            raise SystemExit("--graph: the default and hybrid lines only")
+        # the step count on the device; the update (advance + fused launch)
+        # and the all-gather each captured once, after an eager warm-up
+        opt.device_step_state()
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            opt.step_on_device()
+            opt.gather_unit(u, peers, full)
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        g_update, g_gather = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        l0 = ss.launch_count()
+        with torch.cuda.graph(g_update):
+            opt.step_on_device()
+        with torch.cuda.graph(g_gather):
+            opt.gather_unit(u, peers, full)
+        graph_launches = ss.launch_count() - l0     # kernels per replayed step
+
+        def one_step(ev=None):            # noqa: F811 -- the graph form of the step
+            if ev is not None:
+                ev[0].record(stream)
+                ev[1].record(stream)
+            g_update.replay()
+            if ev is not None:
+                ev[2].record(stream)
+            g_gather.replay()
+            if ev is not None:
+                ev[3].record(stream)
+
     clocks = ClockSampler(smi_index(local))
     clocks.start()
     for _ in range(args.warmup):
@@ -340,7 +377,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     torch.cuda.nvtx.range_pop()
     barrier(world)
-    launches = ss.launch_count() - launches0
+    launches = ss.launch_count() - launches0 + graph_launches * args.steps
     fused_kernel = ss.last_kernel()     # the fused step is each step's last streaming call
     clk = clocks.stop()
     status = ss.device_status()
@@ -366,7 +403,7 @@ def run_ours(args):
     # end to end through the public API: pinned host inputs copied in every
     # step, the gathered unit read back every step
     e2e = None
-    if not args.no_e2e and not scaled:
+    if not args.no_e2e and not scaled and not args.graph:
         try:
             e2e = run_e2e(args, torch, ss, opt, peers, full, u, r, nd, stream, step_bytes)
             failed = ""
@@ -396,6 +433,7 @@ def run_ours(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded counter-based generator on the device; no data set or weights)",
             "config": {"workload": w.name, "tma_stages": _stages_name(args),
+                       "graph": bool(args.graph),
                        "model_shape": f"Llama-style 7B, {len(w.units)} FSDP units",
                        "psi": w.psi, "nd": nd, "shard_group": F, "rank": r,
                        "shard_elements": S,
@@ -404,6 +442,10 @@ def run_ours(args):
                        "step": ("non-finite check of the unscaled mean (1 launch), scaled fused "
                                 "rs_avg+AdamW+bf16 cast (1 launch), loss-scale update (1 launch), "
                                 "then all-gather of one layer unit (1 launch)" if scaled else
+                                "step count advanced on the device (1 launch), fused "
+                                "rs_avg+AdamW+bf16 cast reading its scalars there (1 launch), "
+                                "all-gather of one layer unit (1 launch), replayed from two "
+                                "CUDA graphs" if args.graph else
                                 "fused rs_avg+AdamW+bf16 cast over the rank shard (1 launch), "
                                 "then all-gather of one layer unit (1 launch)"),
                        "bytes_per_step": step_bytes,
@@ -427,7 +469,10 @@ def run_ours(args):
                          "traffic": (None if traffic_per_elem is None
                                      else round(traffic_per_elem * S))},
             "e2e": e2e,
+            **({"e2e_note": "the end-to-end leg runs without --graph"} if args.graph else {}),
             "gpu_launches": launches,
+            **({"gpu_launches_note": f"{graph_launches} kernels per replayed step, counted "
+                                     f"when the graphs were captured"} if args.graph else {}),
             "clocks": clk,
             "cpu_baseline": cpu,
         }

@@ -176,17 +176,25 @@ __device__ __forceinline__ float f16_to_f32(uint16_t h) {
 //   p = p - (lr*wd)*p ; m = b1*m + (1-b1)*g ; v = b2*v + ((1-b2)*g)*g ;
 //   p = p - ((lr/bc1)*m) / (sqrt(v)/sqrt(bc2) + eps)
 // The scalars a kernel computes with: the host's, or those of a device-
-// resident step state (read once per thread at kernel start, through L2).
+// resident step state.  The state's eight floats are read once per block
+// (eight lanes of warp 0, through L1) and shared through shared memory: read
+// by every thread, the one 32-byte line became a hot spot in L2 that more
+// than doubled the 7B-shard step's time.  Every thread of the block must
+// call it (it synchronises the block when c.dev is set; c.dev is the same
+// for the whole grid).
 __device__ __forceinline__ AdamScalars resolve_adam(AdamScalars c) {
     if (c.dev != nullptr) {
-        c.lr_wd = __ldcg(c.dev + 0);
-        c.beta1 = __ldcg(c.dev + 1);
-        c.omb1 = __ldcg(c.dev + 2);
-        c.beta2 = __ldcg(c.dev + 3);
-        c.omb2 = __ldcg(c.dev + 4);
-        c.step_size = __ldcg(c.dev + 5);
-        c.sqrt_bc2 = __ldcg(c.dev + 6);
-        c.eps = __ldcg(c.dev + 7);
+        __shared__ float sc[8];
+        if (threadIdx.x < 8) sc[threadIdx.x] = __ldg(c.dev + threadIdx.x);
+        __syncthreads();
+        c.lr_wd = sc[0];
+        c.beta1 = sc[1];
+        c.omb1 = sc[2];
+        c.beta2 = sc[3];
+        c.omb2 = sc[4];
+        c.step_size = sc[5];
+        c.sqrt_bc2 = sc[6];
+        c.eps = sc[7];
     }
     return c;
 }

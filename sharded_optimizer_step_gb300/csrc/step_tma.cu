@@ -50,6 +50,8 @@ constexpr int kConsumers = kConsumerWarps * 32;   // 512: 4 elements each per ti
 constexpr int kTmaThreads = kConsumers + 32;      // + the producer warp
 constexpr unsigned long long kWaitNs = 2000000000ull;
 constexpr size_t kBarrierBytes = 2 * kMaxStages * sizeof(uint64_t);
+// Left for the kernels' static shared memory (the step scalars' broadcast).
+constexpr size_t kStaticSmemReserve = 1024;
 
 constexpr unsigned kStatusConsumerTimeout = 1u;
 constexpr unsigned kStatusProducerTimeout = 2u;
@@ -471,7 +473,7 @@ std::atomic<int> g_stage_limit{0};  // 0: about kTargetInflight bytes of stages
 constexpr int kStageSet[] = {2, 3, 4, 6, 8, 12, 16};
 
 int stages_for(size_t stage_bytes) {
-    const size_t optin = static_cast<size_t>(device_smem_optin());
+    const size_t optin = static_cast<size_t>(device_smem_optin()) - kStaticSmemReserve;
     size_t fit = optin > kBarrierBytes ? (optin - kBarrierBytes) / stage_bytes : 0;
     if (fit > static_cast<size_t>(kMaxStages)) fit = kMaxStages;
     const int lim = g_stage_limit.load(std::memory_order_relaxed);
@@ -491,7 +493,8 @@ cudaError_t launch_stages(const Op& op, int64_t n, cudaStream_t stream, bool pdl
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 256 && !attr_set[dev]) {
         e = cudaFuncSetAttribute(staged_stream<Op, NST>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, device_smem_optin());
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 device_smem_optin() - static_cast<int>(kStaticSmemReserve));
         if (e != cudaSuccess) return e;
         attr_set[dev] = 1;
     }
@@ -525,7 +528,8 @@ cudaError_t launch_staged(const Op& op, int64_t n, cudaStream_t stream, bool pdl
 }
 
 bool fits_two_stages(size_t stage_bytes) {
-    return 2 * stage_bytes + kBarrierBytes <= static_cast<size_t>(device_smem_optin());
+    return 2 * stage_bytes + kBarrierBytes + kStaticSmemReserve <=
+           static_cast<size_t>(device_smem_optin());
 }
 
 }  // namespace
