@@ -173,7 +173,7 @@ int fsdp_grad_accumulate(const uint16_t* g, float* acc, int64_t n, float scale, 
  * must not overlap one another.  Any alignment is accepted.  Kernels:
  * (1) register-staged, 4 elements per access -- needs state 16-byte, bf16
  * slices and out 8-byte, fp32 slices 16-byte alignment; the default where
- * N_d is 1 to 6, 8, 12 or 16 (12 and 16 not with fp32 slices), and where
+ * N_d is 1 to 8, 12 or 16 (5, 7, 12 and 16 not with fp32 slices), and where
  * two TMA stages do not fit; (2) TMA-staged --
  * needs S >= 4096, master / m / v and every slice 16-byte aligned, out_bf16
  * 8-byte aligned, and two stages of 2048 x (N_d x grad bytes + 12) bytes
@@ -587,8 +587,8 @@ int fsdp_reshard_plan(int64_t total, int32_t old_nd, int32_t new_nd, int32_t new
  * allow it (every source 16-byte aligned, at least 4096 elements, two stages
  * in shared memory); _REGISTER uses only the register-staged kernels;
  * _AUTO (default) uses the TMA-staged kernels where they measured faster:
- * the fused steps at N_d = 7, 9..11, 13..15 and above 16 (and at 12 and 16
- * with fp32 slices), the bucket all-reduce at N_d >= 3 on buckets of at
+ * the fused steps at N_d = 9..11, 13..15 and above 16 (and at 5, 7, 12 and
+ * 16 with fp32 slices), the bucket all-reduce at N_d >= 3 on buckets of at
  * least 32M elements, the check at N_d = 3, 5..7 and above 8, the
  * accumulation never.  The copies (flat_pack, ag_unpack, FSDP2 chunk-cat /
  * copy-out) send the body of every range between its first and last 16-byte

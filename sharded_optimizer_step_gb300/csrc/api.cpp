@@ -48,11 +48,12 @@ std::atomic<int> g_dependent_launch{1};
 // still checks alignment and the stage size).  PATH_REGISTER: never;
 // PATH_TMA: always; PATH_AUTO: where it measured faster on GB300 against the
 // register-staged kernel of the same operation --
-//   fused step: only at N_d = 7, 9..11, 13..15 (the register kernel's loop
-//     over any N_d there: 6.1 vs 6.5 TB/s at N_d = 7), N_d > 16, and 12 or 16
-//     fp32 slices, whose register kernels would spill (at N_d = 8 the
-//     register kernel moved 7.13 vs 6.88 TB/s; at 6, compiled, 6.8 vs 6.3;
-//     at 12 the two were level; at 1..5 and 16 it was faster as well);
+//   fused step: only at N_d = 9..11, 13..15 (the register kernel's loop
+//     over any N_d there: 5.7 vs 6.7 TB/s at N_d = 9), N_d > 16, and 5, 7,
+//     12 or 16 fp32 slices, whose register kernels would spill (at N_d = 8
+//     the register kernel moved 7.13 vs 6.88 TB/s; at 6, compiled, 6.8 vs
+//     6.3; at 5 and 7 on the up-to-8 kernel 6.6 vs 6.2 and 6.7 vs 6.5; at
+//     12 the two were level; at 1..4 and 16 it was faster as well);
 //   bucket all-reduce: N_d >= 3 and buckets of at least 32M elements (one
 //     400M bucket at N_d = 4: 6.9 vs 6.4 TB/s; at N_d = 8: 7.05 vs 6.98);
 //   non-finite check: N_d >= 3 but not 4 or 8, the counts the register
@@ -62,8 +63,8 @@ std::atomic<int> g_dependent_launch{1};
 enum class TmaOp { kStep, kAllReduce, kAccumulate, kCheck };
 bool register_step_kernel(int nd, int grad_dtype) {
     switch (nd) {
-        case 1: case 2: case 3: case 4: case 5: case 6: case 8: return true;
-        case 12: case 16: return grad_dtype != SHARDSTEP_DTYPE_F32;
+        case 1: case 2: case 3: case 4: case 6: case 8: return true;
+        case 5: case 7: case 12: case 16: return grad_dtype != SHARDSTEP_DTYPE_F32;
         default: return false;
     }
 }
@@ -618,6 +619,9 @@ int fused_step(const void* const* grad_slices, int32_t grad_dtype, int32_t nd, i
     else if (vec && (compiled_nd(nd, {1, 2, 3, 4, 6, 8, 16}) ||
                      (nd == 12 && grad_dtype != SHARDSTEP_DTYPE_F32)))
         note_kernel("rs_adamw_cast_vec4<%d, %s> (register-staged)", nd, dtype_name(grad_dtype));
+    else if (vec && (nd == 5 || nd == 7) && grad_dtype != SHARDSTEP_DTYPE_F32)
+        note_kernel("rs_adamw_cast_vec4<up to 8: %d, %s> (register-staged)", nd,
+                    dtype_name(grad_dtype));
     else if (vec)
         note_kernel("rs_adamw_cast_vec4<any N_d = %d, %s> (register-staged)", nd,
                     dtype_name(grad_dtype));

@@ -80,7 +80,29 @@ template <int ND, int GT>
 __device__ __forceinline__ void reduce4(const PtrTable& tab, int nd, int group, int64_t i,
                                         float* g) {
     GroupSum<4> acc;
-    if constexpr (ND != kRuntimeND) {
+    if constexpr (ND < 0) {
+        // up to -ND slices, every load in flight at once, the first nd used
+        // (N_d = 5 and 7 on the 8-slice kernel: 6.6 and 6.7 TB/s where the
+        // loop below moved 5.8 and 6.1 and the TMA-staged kernel 6.2 and 6.5)
+        constexpr int NM = -ND;
+        GradVec<GT> gv[NM];
+#pragma unroll
+        for (int q = 0; q < NM; ++q)
+            if (q < nd) gv[q].load(tab.p[q], i);
+        {
+            float t[4];
+            gv[0].to_f32(t);
+            acc.first(t);
+        }
+#pragma unroll
+        for (int q = 1; q < NM; ++q) {
+            if (q < nd) {
+                float t[4];
+                gv[q].to_f32(t);
+                acc.add(t, group);
+            }
+        }
+    } else if constexpr (ND != kRuntimeND) {
         GradVec<GT> gv[ND];
 #pragma unroll
         for (int q = 0; q < ND; ++q) gv[q].load(tab.p[q], i);
@@ -372,6 +394,9 @@ cudaError_t dispatch_vec(const StepArgs& a, cudaStream_t s) {
         case 2: return go_vec<2, GT>(a, s);
         case 3: return go_vec<3, GT>(a, s);
         case 4: return go_vec<4, GT>(a, s);
+        case 5: case 7:  // 8 fp32 slices would spill at 64 registers: the loop instead
+            if constexpr (GT != kGradF32) return go_vec<-8, GT>(a, s);
+            else return go_vec<kRuntimeND, GT>(a, s);
         case 6: return go_vec<6, GT>(a, s);
         case 8: return go_vec<8, GT>(a, s);
         case 12:  // 12 fp32 slices would spill at 64 registers: the loop instead

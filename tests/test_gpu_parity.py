@@ -162,7 +162,8 @@ def test_hybrid_step_matches_oracle(nd, F, gdt, S, shift, path):
 @pytest.mark.parametrize("nd,F,gdt", [(6, 6, "bf16"), (7, 7, "bf16"), (12, 12, "bf16"),
                                       (13, 13, "bf16"), (24, 24, "bf16"), (64, 64, "bf16"),
                                       (6, 6, "f32"), (13, 13, "f32"), (24, 8, "bf16"),
-                                      (12, 4, "bf16"), (12, 3, "f32"), (64, 16, "bf16")])
+                                      (12, 4, "bf16"), (12, 3, "f32"), (64, 16, "bf16"),
+                                      (5, 1, "bf16"), (7, 7, "f32"), (5, 5, "f32")])
 def test_fused_step_any_nd_matches_oracle(nd, F, gdt, path):
     """N_d without a compiled register kernel: the slices are loaded in
     batches (8 16-bit or 4 fp32 slices), the last batch partial, and with
@@ -567,8 +568,8 @@ def test_bucket_allreduce_dependent_launches_keep_stream_order(dependent, path):
 
 def test_auto_path_names_the_kernel_it_launched():
     """The automatic choice, as shardstep_last_kernel reports it: the
-    register-staged fused kernel at N_d = 8, the TMA-staged one at N_d = 7,
-    TMA-staged whenever forced."""
+    register-staged fused kernel at N_d = 8 and its up-to-8 form at 7, the
+    TMA-staged one at N_d = 9, TMA-staged whenever forced."""
     S = 8192
     master = torch.zeros(S, device=DEV)
     m = torch.zeros(S, device=DEV)
@@ -577,7 +578,8 @@ def test_auto_path_names_the_kernel_it_launched():
     prev = ss.set_fused_path("auto")
     try:
         for nd, want in [(8, "rs_adamw_cast_vec4<8, bf16> (register-staged)"),
-                         (7, "staged_stream<AdamOp<bf16>> (TMA-staged)")]:
+                         (7, "rs_adamw_cast_vec4<up to 8: 7, bf16> (register-staged)"),
+                         (9, "staged_stream<AdamOp<bf16>> (TMA-staged)")]:
             g = [torch.zeros(S, dtype=torch.bfloat16, device=DEV) for _ in range(nd)]
             ss.fsdp_rs_avg_adamw_cast(g, master, m, v, out, HPC, 1)
             assert ss.last_kernel() == want
