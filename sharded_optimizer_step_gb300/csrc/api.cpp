@@ -54,10 +54,15 @@ std::atomic<int> g_dependent_launch{1};
 //     the register kernel moved 7.13 vs 6.88 TB/s; at 6, compiled, 6.8 vs
 //     6.3; at 5 and 7 on the up-to-8 kernel 6.6 vs 6.2 and 6.7 vs 6.5; at
 //     12 the two were level; at 1..4 and 16 it was faster as well);
-//   bucket all-reduce: N_d >= 3 and buckets of at least 32M elements (one
-//     400M bucket at N_d = 4: 6.9 vs 6.4 TB/s; at N_d = 8: 7.05 vs 6.98);
+//   bucket all-reduce: at N_d = 4 and 8 on buckets of at least 32M
+//     elements (one 400M bucket at N_d = 4: 6.9 vs 6.4 TB/s; at N_d = 8:
+//     7.05 vs 6.98), at every N_d > 3 without a compiled register kernel
+//     on every bucket (N_d = 7: 6.5 vs 5.9 TB/s on one bucket, 6.1 vs 5.8
+//     on 25 MiB buckets); never at N_d = 1..3 (N_d = 3 on the up-to-8
+//     register kernel: 4.6 vs 4.2 TB/s);
 //   non-finite check: N_d >= 3 but not 4 or 8, the counts the register
-//     kernel is compiled for (at N_d = 4: 6.3 vs 5.7 TB/s; at 8: 7.4 vs 7.3);
+//     kernel is compiled for (at N_d = 4: 6.3 vs 5.7 TB/s; at 8: 7.4 vs
+//     7.3), nor 3 with 16-bit slices (up-to-8 form: 3.7 vs 3.3 TB/s);
 //   accumulation: never (7.0 vs 6.0 TB/s for the first micro-batch, 7.2 vs
 //     6.6 for the others).
 enum class TmaOp { kStep, kAllReduce, kAccumulate, kCheck };
@@ -75,8 +80,13 @@ bool use_tma(TmaOp op, int64_t n, int nd = 0, int grad_dtype = SHARDSTEP_DTYPE_B
     if (path == SHARDSTEP_PATH_TMA) return true;
     switch (op) {
         case TmaOp::kStep: return nd >= 3 && !register_step_kernel(nd, grad_dtype);
-        case TmaOp::kAllReduce: return nd >= 3 && n >= (int64_t{32} << 20);
-        case TmaOp::kCheck: return nd >= 3 && nd != 4 && nd != 8;
+        case TmaOp::kAllReduce:
+            if (nd <= 3) return false;
+            if (nd == 4 || nd == 8) return n >= (int64_t{32} << 20);
+            return true;
+        case TmaOp::kCheck:
+            if (nd == 3) return grad_dtype == SHARDSTEP_DTYPE_F32;
+            return nd >= 3 && nd != 4 && nd != 8;
         default: return false;
     }
 }
@@ -714,7 +724,7 @@ int fsdp_grad_unscale_check(const void* const* grad_slices, int32_t grad_dtype, 
     MeanOp mo = mean_op(nd, shard_group);
     mo.scaled = 1;
     mo.scale = scale;
-    tma = tma && use_tma(TmaOp::kCheck, S, nd) && tma_reduce_fits(nd, grad_dtype);
+    tma = tma && use_tma(TmaOp::kCheck, S, nd, grad_dtype) && tma_reduce_fits(nd, grad_dtype);
     cudaError_t e = tma ? launch_nonfinite_check_tma(tab, nd, grad_dtype, S, mo, found_inf,
                                                      static_cast<cudaStream_t>(stream))
                         : launch_nonfinite_check(tab, nd, grad_dtype, S, mo, found_inf, vec,
@@ -724,6 +734,9 @@ int fsdp_grad_unscale_check(const void* const* grad_slices, int32_t grad_dtype, 
         note_kernel("staged_stream<CheckOp<%s>> (TMA-staged)", dtype_name(grad_dtype));
     else if (vec && compiled_nd(nd, {4, 8}))
         note_kernel("nonfinite_check_vec4<%d, %s> (register-staged)", nd, dtype_name(grad_dtype));
+    else if (vec && nd == 3 && grad_dtype != SHARDSTEP_DTYPE_F32)
+        note_kernel("nonfinite_check_vec4<up to 8: 3, %s> (register-staged)",
+                    dtype_name(grad_dtype));
     else if (vec)
         note_kernel("nonfinite_check_vec4<any N_d = %d, %s> (register-staged)", nd,
                     dtype_name(grad_dtype));
@@ -1037,6 +1050,8 @@ int ddp_bucket_allreduce_avg(const uint16_t* const* rank_grads, int32_t nd,
             note_kernel("staged_stream<MeanOutOp> (TMA-staged)");
         else if (vec && compiled_nd(nd, {1, 2, 4, 8}))
             note_kernel("allreduce_avg_vec4<%d> (register-staged)", nd);
+        else if (vec && nd == 3)
+            note_kernel("allreduce_avg_vec4<up to 8: 3> (register-staged)");
         else if (vec)
             note_kernel("allreduce_avg_vec4<any N_d = %d> (register-staged)", nd);
         else

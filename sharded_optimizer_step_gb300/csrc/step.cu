@@ -455,6 +455,9 @@ cudaError_t dispatch_check(const PtrTable& tab, int nd, int64_t S, const MeanOp&
         return cudaGetLastError();
     }
     switch (nd) {
+        case 3:
+            if constexpr (GT != kGradF32) return go_check<-8, GT>(tab, nd, S, mo, found, s);
+            else return go_check<kRuntimeND, GT>(tab, nd, S, mo, found, s);
         case 4: return go_check<4, GT>(tab, nd, S, mo, found, s);
         case 8: return go_check<8, GT>(tab, nd, S, mo, found, s);
         default: return go_check<kRuntimeND, GT>(tab, nd, S, mo, found, s);
@@ -481,6 +484,7 @@ cudaError_t launch_allreduce_avg(const PtrTable& tab, int nd, int64_t n, uint16_
         switch (nd) {
             case 1: return go_ar<1>(tab, nd, n, out, mo, pdl, stream);
             case 2: return go_ar<2>(tab, nd, n, out, mo, pdl, stream);
+            case 3: return go_ar<-8>(tab, nd, n, out, mo, pdl, stream);
             case 4: return go_ar<4>(tab, nd, n, out, mo, pdl, stream);
             case 8: return go_ar<8>(tab, nd, n, out, mo, pdl, stream);
             default: return go_ar<kRuntimeND>(tab, nd, n, out, mo, pdl, stream);
