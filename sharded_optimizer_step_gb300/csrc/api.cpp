@@ -60,11 +60,10 @@ std::atomic<int> g_dependent_launch{1};
 //     on every bucket (N_d = 7: 6.5 vs 5.9 TB/s on one bucket, 6.1 vs 5.8
 //     on 25 MiB buckets); never at N_d = 1..3 (N_d = 3 on the up-to-8
 //     register kernel: 4.6 vs 4.2 TB/s);
-//   non-finite check: at every N_d but 4 and 8, the counts the register
-//     kernel is compiled for (at N_d = 4: 6.3 vs 5.7 TB/s; at 8: 7.4 vs
-//     7.3), and 3 with 16-bit slices (up-to-8 form: 3.7 vs 3.3 TB/s); at
-//     N_d = 1 and 2 the register kernel's loop read 1.4 and 2.6 TB/s, the
-//     TMA-staged kernel 2.1 and 3.2;
+//   non-finite check: at every N_d but 1, 2, 4 and 8, the counts the
+//     register kernel is compiled for (at N_d = 1 / 2 / 4 / 8: 5.0 vs 2.1,
+//     6.0 vs 3.2, 6.7 vs 5.7, 7.4 vs 7.3 TB/s), and 3 with 16-bit slices
+//     (up-to-8 form: 3.7 vs 3.3 TB/s);
 //   accumulation: never (7.0 vs 6.0 TB/s for the first micro-batch, 7.2 vs
 //     6.6 for the others).
 enum class TmaOp { kStep, kAllReduce, kAccumulate, kCheck };
@@ -88,7 +87,7 @@ bool use_tma(TmaOp op, int64_t n, int nd = 0, int grad_dtype = SHARDSTEP_DTYPE_B
             return true;
         case TmaOp::kCheck:
             if (nd == 3) return grad_dtype == SHARDSTEP_DTYPE_F32;
-            return nd != 4 && nd != 8;
+            return nd != 1 && nd != 2 && nd != 4 && nd != 8;
         default: return false;
     }
 }
@@ -734,7 +733,7 @@ int fsdp_grad_unscale_check(const void* const* grad_slices, int32_t grad_dtype, 
     if (e != cudaSuccess) return cuda_fail(e, "non-finite check launch");
     if (tma)
         note_kernel("staged_stream<CheckOp<%s>> (TMA-staged)", dtype_name(grad_dtype));
-    else if (vec && compiled_nd(nd, {4, 8}))
+    else if (vec && compiled_nd(nd, {1, 2, 4, 8}))
         note_kernel("nonfinite_check_vec4<%d, %s> (register-staged)", nd, dtype_name(grad_dtype));
     else if (vec && nd == 3 && grad_dtype != SHARDSTEP_DTYPE_F32)
         note_kernel("nonfinite_check_vec4<up to 8: 3, %s> (register-staged)",
