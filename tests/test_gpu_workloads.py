@@ -264,33 +264,54 @@ def test_llama_7b_rank_view_as_benchmarked():
         assert_bits(_host_bf16(full[q * S + torch.from_numpy(loc).to(DEV)]), want, "peer shard")
 
 
-def test_llama_7b_rank_view_register_path_equals_tma_path_everywhere():
-    """The register-staged fallback and the TMA-staged kernel give the same
-    bits on every one of the 842M shard elements over two steps (the TMA
-    path is checked against the oracle on samples above)."""
+def test_llama_7b_rank_view_every_kernel_and_the_graph_agree_everywhere():
+    """The register-staged kernel (the default, checked against the oracle
+    on samples above), the TMA-staged kernel and the device-state step
+    replayed from a CUDA graph give the same bits on every one of the 842M
+    shard elements over two steps."""
     w = W.llama_7b_rank_view()
     _, hpc = _hp(w)
     r = w.extra["rank"]
     a = RankShardOptimizer(w.units, w.nd, r, hpc, device=DEV)
     b = RankShardOptimizer(w.units, w.nd, r, hpc, device=DEV)
-    b.grad_in = a.grad_in                 # one set of gradient buffers for both
+    c = RankShardOptimizer(w.units, w.nd, r, hpc, device=DEV)
+    b.grad_in = a.grad_in                 # one set of gradient buffers for all
+    c.grad_in = a.grad_in
     W.dev_fill_rank_master(w, r, a.master)
     b.master.copy_(a.master)
+    c.master.copy_(a.master)
+    c.device_step_state()
     prev = ss.set_fused_path("auto")
     try:
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):     # warm-up outside the capture, then undone
+            c.step_on_device()
+        torch.cuda.current_stream().wait_stream(side)
+        c.master.copy_(a.master)
+        c.m.zero_()
+        c.v.zero_()
+        c.state.init(0)
+        with torch.cuda.graph(graph):
+            c.step_on_device()
         for t in (1, 2):
             for q in range(w.nd):
                 W.dev_fill_rank_grad(w, t, r, q, 0, a.grad_in[q])
             ss.set_fused_path("auto")
             a.step()
-            ss.set_fused_path("register")
+            ss.set_fused_path("tma")
             b.step()
+            graph.replay()
     finally:
         ss.set_fused_path(prev)
     torch.cuda.synchronize()
-    for name in ("master", "m", "v"):
-        assert torch.equal(getattr(a, name).view(torch.int32), getattr(b, name).view(torch.int32)), name
-    assert torch.equal(a.params.view(torch.int16), b.params.view(torch.int16))
+    assert c.state.step() == 2
+    for other in (b, c):
+        for name in ("master", "m", "v"):
+            assert torch.equal(getattr(a, name).view(torch.int32),
+                               getattr(other, name).view(torch.int32)), name
+        assert torch.equal(a.params.view(torch.int16), other.params.view(torch.int16))
     assert ss.device_status() == 0
 
 
