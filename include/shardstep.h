@@ -177,7 +177,7 @@ int fsdp_grad_accumulate(const uint16_t* g, float* acc, int64_t n, float scale, 
  * two TMA stages do not fit; (2) TMA-staged --
  * needs S >= 4096, master / m / v and every slice 16-byte aligned, out_bf16
  * 8-byte aligned, and two stages of 2048 x (N_d x grad bytes + 12) bytes
- * within the per-block shared-memory limit (N_d <= 21 for bf16, <= 10 for
+ * within the per-block shared-memory limit (N_d <= 22 for bf16, <= 11 for
  * fp32 on GB300); the default for other N_d >= 3; (3) one element per
  * access.  All three compute the same bits.  A TMA-staged launch whose
  * internal wait runs out (about 2 s) sets a bit in the device status word;
