@@ -111,7 +111,8 @@ def test_fused_step_matches_oracle(nd, S, gdt, shift, path):
                                       (16, "bf16", 2048 * 200 + 1000),
                                       (8, "f32", 2048 * 160 + 16),
                                       (21, "bf16", 70001), (22, "bf16", 70001),
-                                      (10, "f32", 70001), (11, "f32", 70001)])
+                                      (23, "bf16", 70001), (10, "f32", 70001),
+                                      (11, "f32", 70001), (12, "f32", 70001)])
 def test_fused_step_multi_tile(nd, gdt, S, path):
     seed = 5 + S
     P = nd * S
