@@ -568,6 +568,23 @@ int take_slices(const void* const* grad_slices, int32_t grad_dtype, int32_t nd, 
 // The fused step with the slices reduced in groups of `group` ranks
 // (group == nd: plain rank order); with `scaled`, the mean is multiplied by
 // inv_scale and a non-zero *skip at launch leaves everything unchanged.
+// Shared argument checks of the hybrid / scaled entry points (INVALID with a
+// message, or SHARDSTEP_OK).
+int check_shard_group(int32_t nd, int32_t shard_group) {
+    if (shard_group < 1 || nd < 1 || nd % shard_group != 0)
+        return fail(SHARDSTEP_ERR_INVALID,
+                    "the sharding factor %d must be >= 1 and divide nd = %d", shard_group, nd);
+    return SHARDSTEP_OK;
+}
+
+int check_scaler_words(const float* scale, const uint32_t* found_inf) {
+    if (found_inf == nullptr || scale == nullptr)
+        return fail(SHARDSTEP_ERR_INVALID, "found_inf / scale is NULL");
+    if (!aligned(found_inf, 4) || !aligned(scale, 4))
+        return fail(SHARDSTEP_ERR_INVALID, "found_inf / scale misaligned");
+    return SHARDSTEP_OK;
+}
+
 // `hp` gives the AdamW scalars on the host; with `state` instead, the
 // kernels read them from the device-resident step state.
 int fused_step(const void* const* grad_slices, int32_t grad_dtype, int32_t nd, int32_t group,
@@ -655,9 +672,7 @@ int fsdp_hybrid_rs_avg_adamw_cast(const void* const* grad_slices, int32_t grad_d
                                   int32_t shard_group, int64_t S, float* master, float* m,
                                   float* v, uint16_t* out_bf16, const shardstep_adamw_t* hp,
                                   void* stream) {
-    if (shard_group < 1 || nd < 1 || nd % shard_group != 0)
-        return fail(SHARDSTEP_ERR_INVALID,
-                    "the sharding factor %d must be >= 1 and divide nd = %d", shard_group, nd);
+    if (int rc = check_shard_group(nd, shard_group); rc != SHARDSTEP_OK) return rc;
     return fused_step(grad_slices, grad_dtype, nd, shard_group, S, master, m, v, out_bf16, hp,
                       stream);
 }
@@ -666,9 +681,7 @@ int fsdp_state_rs_avg_adamw_cast(const void* const* grad_slices, int32_t grad_dt
                                  int32_t shard_group, int64_t S, float* master, float* m,
                                  float* v, uint16_t* out_bf16,
                                  const shardstep_adamw_state_t* state, void* stream) {
-    if (shard_group < 1 || nd < 1 || nd % shard_group != 0)
-        return fail(SHARDSTEP_ERR_INVALID,
-                    "the sharding factor %d must be >= 1 and divide nd = %d", shard_group, nd);
+    if (int rc = check_shard_group(nd, shard_group); rc != SHARDSTEP_OK) return rc;
     if (state == nullptr) return fail(SHARDSTEP_ERR_INVALID, "state is NULL");
     return fused_step(grad_slices, grad_dtype, nd, shard_group, S, master, m, v, out_bf16,
                       nullptr, stream, nullptr, nullptr, state);
@@ -708,14 +721,9 @@ int shardstep_adamw_state_advance(shardstep_adamw_state_t* state, const shardste
 int fsdp_grad_unscale_check(const void* const* grad_slices, int32_t grad_dtype, int32_t nd,
                             int32_t shard_group, int64_t S, const float* scale,
                             uint32_t* found_inf, void* stream) {
-    if (shard_group < 1 || nd < 1 || nd % shard_group != 0)
-        return fail(SHARDSTEP_ERR_INVALID,
-                    "the sharding factor %d must be >= 1 and divide nd = %d", shard_group, nd);
+    if (int rc = check_shard_group(nd, shard_group); rc != SHARDSTEP_OK) return rc;
     if (S < 0) return fail(SHARDSTEP_ERR_INVALID, "S must be >= 0");
-    if (found_inf == nullptr || scale == nullptr)
-        return fail(SHARDSTEP_ERR_INVALID, "found_inf / scale is NULL");
-    if (!aligned(found_inf, 4) || !aligned(scale, 4))
-        return fail(SHARDSTEP_ERR_INVALID, "found_inf / scale misaligned");
+    if (int rc = check_scaler_words(scale, found_inf); rc != SHARDSTEP_OK) return rc;
     if (S == 0) return ok();
     PtrTable tab;
     bool vec = false, tma = false;
@@ -751,14 +759,9 @@ int fsdp_state_scaled_rs_avg_adamw_cast(const void* const* grad_slices, int32_t 
                                         float* master, float* m, float* v, uint16_t* out_bf16,
                                         const shardstep_adamw_state_t* state, const float* scale,
                                         const uint32_t* found_inf, void* stream) {
-    if (shard_group < 1 || nd < 1 || nd % shard_group != 0)
-        return fail(SHARDSTEP_ERR_INVALID,
-                    "the sharding factor %d must be >= 1 and divide nd = %d", shard_group, nd);
+    if (int rc = check_shard_group(nd, shard_group); rc != SHARDSTEP_OK) return rc;
     if (state == nullptr) return fail(SHARDSTEP_ERR_INVALID, "state is NULL");
-    if (found_inf == nullptr || scale == nullptr)
-        return fail(SHARDSTEP_ERR_INVALID, "found_inf / scale is NULL");
-    if (!aligned(found_inf, 4) || !aligned(scale, 4))
-        return fail(SHARDSTEP_ERR_INVALID, "found_inf / scale misaligned");
+    if (int rc = check_scaler_words(scale, found_inf); rc != SHARDSTEP_OK) return rc;
     return fused_step(grad_slices, grad_dtype, nd, shard_group, S, master, m, v, out_bf16,
                       nullptr, stream, scale, found_inf, state);
 }
@@ -767,13 +770,8 @@ int fsdp_scaled_rs_avg_adamw_cast(const void* const* grad_slices, int32_t grad_d
                                   int32_t shard_group, int64_t S, float* master, float* m,
                                   float* v, uint16_t* out_bf16, const shardstep_adamw_t* hp,
                                   const float* scale, const uint32_t* found_inf, void* stream) {
-    if (shard_group < 1 || nd < 1 || nd % shard_group != 0)
-        return fail(SHARDSTEP_ERR_INVALID,
-                    "the sharding factor %d must be >= 1 and divide nd = %d", shard_group, nd);
-    if (found_inf == nullptr || scale == nullptr)
-        return fail(SHARDSTEP_ERR_INVALID, "found_inf / scale is NULL");
-    if (!aligned(found_inf, 4) || !aligned(scale, 4))
-        return fail(SHARDSTEP_ERR_INVALID, "found_inf / scale misaligned");
+    if (int rc = check_shard_group(nd, shard_group); rc != SHARDSTEP_OK) return rc;
+    if (int rc = check_scaler_words(scale, found_inf); rc != SHARDSTEP_OK) return rc;
     return fused_step(grad_slices, grad_dtype, nd, shard_group, S, master, m, v, out_bf16, hp,
                       stream, scale, found_inf);
 }
