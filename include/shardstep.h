@@ -602,9 +602,13 @@ int fsdp_reshard_plan(int64_t total, int32_t old_nd, int32_t new_nd, int32_t new
 #define SHARDSTEP_PATH_TMA 2
 int32_t shardstep_set_fused_path(int32_t path);
 
-/* Whether the second and later buckets of one ddp_bucket_allreduce_avg call
- * are launched as programmatic dependents of the previous bucket's kernel
- * (they may start while it drains; each still ends after it), process-wide.
+/* Whether the second and later kernels of one call are launched as
+ * programmatic dependents of the previous kernel of that call (they may
+ * start while it drains; each still ends after it), process-wide: the
+ * buckets of ddp_bucket_allreduce_avg and the copy kernels of
+ * fsdp_flat_pack, fsdp_ag_unpack, fsdp2_chunk_cat and
+ * fsdp2_all_gather_copy_out.  The first kernel of a call is always an
+ * ordinary launch, so it waits for everything before it in the stream.
  * 1 (default) = yes, 0 = ordinary launches.  Results do not depend on it.
  * Returns the previous setting. */
 int32_t shardstep_set_dependent_launch(int32_t enable);

@@ -371,6 +371,12 @@ struct CopyBatcher {
     AlignedTable st;  // aligned destination, unaligned source (copy16_shift)
     cudaStream_t stream;
     int rc = SHARDSTEP_OK;
+    // whether this call has launched a kernel: the first launch waits for
+    // everything before it in the stream, the later ones (disjoint copies
+    // of the same call) go out as programmatic dependents of the previous
+    // unless dependent launches are switched off
+    bool launched = false;
+    const bool pdl_ok = g_dependent_launch.load(std::memory_order_relaxed) != 0;
     explicit CopyBatcher(cudaStream_t s) : stream(s) {
         t.n = 0;
         t.total_chunks = 0;
@@ -432,15 +438,19 @@ struct CopyBatcher {
     }
     void flush_vector() {
         if (t.n == 0 || rc != SHARDSTEP_OK) return;
-        cudaError_t e = launch_copy(t, stream);
+        cudaError_t e = launch_copy(t, launched && pdl_ok, stream);
         if (e != cudaSuccess) rc = cuda_fail(e, "copy kernel launch");
+        launched = true;
         t.n = 0;
         t.total_chunks = 0;
     }
     void flush_chunked(AlignedTable& tab) {
         if (tab.n == 0 || rc != SHARDSTEP_OK) return;
-        cudaError_t e = &tab == &bt ? launch_copy16(tab, stream) : launch_copy16_shift(tab, stream);
+        const bool pdl = launched && pdl_ok;
+        cudaError_t e = &tab == &bt ? launch_copy16(tab, pdl, stream)
+                                    : launch_copy16_shift(tab, pdl, stream);
         if (e != cudaSuccess) rc = cuda_fail(e, "aligned copy kernel launch");
+        launched = true;
         tab.n = 0;
         tab.total_chunks = 0;
     }

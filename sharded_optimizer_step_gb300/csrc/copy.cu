@@ -29,6 +29,14 @@
 // source and destination are congruent; a head of up to width-1 bytes brings
 // the destination to that alignment and the tail is copied byte-wise, both by
 // the lanes of the block that owns the segment's first / last chunk.
+//
+// One call's copies are disjoint and read nothing the call writes, so the
+// second and later launches of a call go out as programmatic dependents:
+// each copy kernel lets the next one be scheduled as soon as all of its own
+// blocks have started, and every block waits for the previous grid of the
+// call before it ends (both no-ops for an ordinary launch).  A call that
+// mixes congruent and realigned ranges, heads and tails then runs without
+// an idle gap between its kernels.
 #include "common.cuh"
 
 namespace shardstep {
@@ -80,6 +88,7 @@ __device__ __forceinline__ void copy_vecs(const char* src, char* dst, int64_t v0
 }
 
 __global__ void __launch_bounds__(kThreads) copy_segments(CopyTable t) {
+    pdl_trigger();
     int seg = 0;
     for (int64_t c = blockIdx.x; c < t.total_chunks; c += gridDim.x) {
         while (seg + 1 < t.n && t.s[seg + 1].chunk0 <= c) ++seg;
@@ -107,9 +116,11 @@ __global__ void __launch_bounds__(kThreads) copy_segments(CopyTable t) {
                 sg.dst[done + threadIdx.x] = sg.src ? sg.src[done + threadIdx.x] : 0;
         }
     }
+    pdl_wait();
 }
 
 __global__ void __launch_bounds__(kThreads, 8) copy16(AlignedTable t) {
+    pdl_trigger();
     const int64_t c = blockIdx.x;
     int lo = 0, hi = t.n - 1;  // the range owning chunk c (chunk0 increasing)
     while (lo < hi) {
@@ -134,6 +145,7 @@ __global__ void __launch_bounds__(kThreads, 8) copy16(AlignedTable t) {
         const int64_t k = v0 + u * kThreads + threadIdx.x;
         if (k < nv) st_stream(dst + k, r[u]);
     }
+    pdl_wait();
 }
 
 // Bytes [delta, delta + 16) of the 32-byte pair (a, b), delta = 4 * ws + sh / 8.
@@ -150,6 +162,7 @@ __device__ __forceinline__ uint4 shift_pair(const uint4& a, const uint4& b, int 
 }
 
 __global__ void __launch_bounds__(kThreads, 5) copy16_shift(AlignedTable t) {
+    pdl_trigger();
     const int64_t c = blockIdx.x;
     int lo = 0, hi = t.n - 1;  // the range owning chunk c (chunk0 increasing)
     while (lo < hi) {
@@ -181,6 +194,7 @@ __global__ void __launch_bounds__(kThreads, 5) copy16_shift(AlignedTable t) {
         const int64_t k = v0 + u * kThreads + threadIdx.x;
         if (k < nv) st_stream(dst + k, shift_pair(a[u], b[u], ws, sh));
     }
+    pdl_wait();
 }
 
 // ------------------------------------------------------- accumulation
@@ -250,27 +264,35 @@ unsigned grid_one_pass(int64_t vectors) {
     return static_cast<unsigned>(g < 1 ? 1 : g);
 }
 
+template <typename Table>
+cudaError_t launch_table(void (*kernel)(Table), unsigned grid, const Table& t, bool pdl,
+                         cudaStream_t stream) {
+    cudaError_t e;
+    if (pdl) {
+        e = launch_dependent(kernel, dim3(grid), dim3(kThreads), 0, stream, t);
+    } else {
+        kernel<<<grid, kThreads, 0, stream>>>(t);
+        e = cudaGetLastError();
+    }
+    note_launch();
+    return e;
+}
+
 }  // namespace
 
-cudaError_t launch_copy(const CopyTable& t, cudaStream_t stream) {
+cudaError_t launch_copy(const CopyTable& t, bool pdl, cudaStream_t stream) {
     const int64_t cap = static_cast<int64_t>(device_sms()) *
                         resident_blocks(reinterpret_cast<const void*>(copy_segments), kThreads);
     const int64_t g = t.total_chunks < cap ? t.total_chunks : cap;
-    copy_segments<<<static_cast<unsigned>(g < 1 ? 1 : g), kThreads, 0, stream>>>(t);
-    note_launch();
-    return cudaGetLastError();
+    return launch_table(copy_segments, static_cast<unsigned>(g < 1 ? 1 : g), t, pdl, stream);
 }
 
-cudaError_t launch_copy16(const AlignedTable& t, cudaStream_t stream) {
-    copy16<<<static_cast<unsigned>(t.total_chunks), kThreads, 0, stream>>>(t);
-    note_launch();
-    return cudaGetLastError();
+cudaError_t launch_copy16(const AlignedTable& t, bool pdl, cudaStream_t stream) {
+    return launch_table(copy16, static_cast<unsigned>(t.total_chunks), t, pdl, stream);
 }
 
-cudaError_t launch_copy16_shift(const AlignedTable& t, cudaStream_t stream) {
-    copy16_shift<<<static_cast<unsigned>(t.total_chunks), kThreads, 0, stream>>>(t);
-    note_launch();
-    return cudaGetLastError();
+cudaError_t launch_copy16_shift(const AlignedTable& t, bool pdl, cudaStream_t stream) {
+    return launch_table(copy16_shift, static_cast<unsigned>(t.total_chunks), t, pdl, stream);
 }
 
 cudaError_t launch_accumulate(const uint16_t* g, float* acc, int64_t n, float scale, bool first,

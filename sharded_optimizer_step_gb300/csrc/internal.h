@@ -157,12 +157,16 @@ constexpr int64_t kTmaMinElements = 4096;
 
 cudaError_t launch_allreduce_avg(const PtrTable& tab, int nd, int64_t n, uint16_t* out,
                                  const MeanOp& mo, bool vec, bool pdl, cudaStream_t stream);
-cudaError_t launch_copy(const CopyTable& t, cudaStream_t stream);
+// The copy launchers' `pdl`: launch as a programmatic dependent of the
+// previous kernel in the stream (only for a later launch of the same batch
+// of disjoint copies; every copy kernel waits for its predecessor before it
+// ends, so the batch's last kernel completes after all of them).
+cudaError_t launch_copy(const CopyTable& t, bool pdl, cudaStream_t stream);
 // Aligned copy (copy.cu): one block per 16 KB chunk of 16-byte vectors.
-cudaError_t launch_copy16(const AlignedTable& t, cudaStream_t stream);
+cudaError_t launch_copy16(const AlignedTable& t, bool pdl, cudaStream_t stream);
 // Realigning copy (copy.cu): like copy16, but every source starts 1..15
 // bytes past a 16-byte boundary (destinations and sizes 16-byte multiples).
-cudaError_t launch_copy16_shift(const AlignedTable& t, cudaStream_t stream);
+cudaError_t launch_copy16_shift(const AlignedTable& t, bool pdl, cudaStream_t stream);
 cudaError_t launch_accumulate(const uint16_t* g, float* acc, int64_t n, float scale, bool first,
                               bool vec, cudaStream_t stream);
 

@@ -313,6 +313,46 @@ def test_flat_pack_misaligned_destination_segments(path):
     assert_bits(host_bf16(flat), want, "flat")
 
 
+@pytest.mark.parametrize("dependent", [True, False])
+def test_copy_launches_of_one_call_keep_stream_order(dependent):
+    """A pack of 203 bf16 tensors at mixed offsets (congruent, realigned and
+    byte-wise ranges, more than 64 of each kind, so every copy kernel runs
+    several times and the later launches are programmatic dependents of the
+    earlier ones) between a torch producer that writes its sources and a
+    torch consumer that reads the packed buffer right after it, on the same
+    stream; then the all-gather of shards at odd slot offsets the same way."""
+    nd = 8
+    rng = np.random.default_rng(5)
+    numels = [1 << 20] + [int(x) for x in rng.integers(1, 20000, size=200)] + [3 << 20, 5]
+    shifts = [int(s) for s in rng.integers(0, 8, size=len(numels))]
+    host = [synth.host_fill(synth.normal_stream(6, (94, k), 0.02), 0, n, "bf16")
+            for k, n in enumerate(numels)]
+    staged = [dev_bf16(h, sh) for h, sh in zip(host, shifts)]
+    srcs = [dev_bf16(np.zeros(n, np.uint16), sh) for n, sh in zip(numels, shifts)]
+    want, lay = oracle.flat_pack(host, nd)
+    S = lay.shard
+    shards_h = [want[r * S:(r + 1) * S] for r in range(nd)]
+    staged_sh = [dev_bf16(h, r % 8) for r, h in enumerate(shards_h)]
+    shards = [dev_bf16(np.zeros(S, np.uint16), r % 8) for r in range(nd)]
+    full = torch.empty(nd * S, dtype=torch.bfloat16, device=DEV)
+    torch.cuda.synchronize()
+    prev = ss.set_dependent_launch(dependent)
+    try:
+        for s, t in zip(srcs, staged):
+            s.copy_(t)                      # the producer, on the same stream
+        flat = ss.fsdp_flat_pack(srcs, nd)
+        seen = flat.clone()                 # the consumer, on the same stream
+        for s, t in zip(shards, staged_sh):
+            s.copy_(t)
+        ss.fsdp_ag_unpack(shards, full)
+        seen_full = full.clone()
+    finally:
+        ss.set_dependent_launch(prev)
+    torch.cuda.synchronize()
+    assert_bits(host_bf16(seen), want, "flat")
+    assert_bits(host_bf16(seen_full), want, "full")
+
+
 def test_worked_example_on_gpu():
     tensors = [np.arange(1, 9, dtype=np.float32).reshape(4, 2) + 100 * (t + 1) for t in range(3)]
     flat = ss.fsdp_flat_pack([dev_f32(t.reshape(-1)).view(4, 2) for t in tensors], 2)
