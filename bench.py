@@ -50,7 +50,8 @@ PROFILES = {
     "llama_7b_hybrid_nd16_f8_rank0": ("fused_step_llama7b_hybrid_nd16_f8.md", REGISTER_SOURCES),
     "llama_7b_rank0_nd8_fp16_scaled": ("scaled_step_llama7b_rank_view_fp16.md",
                                        REGISTER_SOURCES),
-    "llama_1b_rank0_nd8_m4": ("accumulate_llama1b_rank_view_m4.md", COPY_SOURCES),
+    "llama_1b_rank0_nd8_m4": ("accumulate_llama1b_rank_view_m4.md",
+                              COPY_SOURCES + ["sharded_optimizer_step_gb300/csrc/accum_step.cu"]),
     "ddp_nd8_buckets": ("ddp_buckets_nd8_adamw.md", REGISTER_SOURCES),
     "llama_7b_layer_ragged_nd8": ("pack_gather_llama7b_layer_ragged.md", COPY_SOURCES),
 }
@@ -86,7 +87,12 @@ def parse():
                          "device, the fused update and the all-gather replayed from CUDA "
                          "graphs captured once")
     ap.add_argument("--no-dependent-launch", action="store_true",
-                    help="launch every bucket of an all-reduce call as an ordinary launch")
+                    help="launch every bucket of an all-reduce call, and every copy kernel "
+                         "of a pack / all-gather call, as an ordinary launch")
+    ap.add_argument("--accum-two-pass", action="store_true",
+                    help="accumulation line: accumulate every micro-batch with its own launch "
+                         "and run the fused step on the accumulators (the last micro-batch "
+                         "is otherwise accumulated inside the fused step)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     return ap.parse_args()
@@ -1256,7 +1262,20 @@ def _accum_oracle_sample(w, n, t):
     accs = [oracle.grad_accumulate(micro[q], np.float32(1.0 / w.micro)) for q in range(w.nd)]
     oracle.fsdp_shard_step(accs, 0, n, p, m, v, hp, t)
     dt = time.perf_counter() - t0
-    return dt, (6 + 10 * (w.micro - 1)) * w.nd * n + (4 * w.nd + 26) * n
+    acc_b, fused_b = _accum_bytes(w.nd, w.micro, True)
+    return dt, (acc_b + fused_b) * n
+
+
+def _accum_bytes(nd, M, fused_last):
+    """Algorithmic bytes per shard element of the accumulation (all launches
+    over the nd contributions) and of the fused step.  Each micro-batch
+    accumulate reads bf16 and writes fp32 (6 B), after the first also reads
+    fp32 (10 B).  fused_last: the last micro-batch is accumulated inside the
+    fused step, which reads per contribution the fp32 accumulator and the
+    bf16 gradient (6 B) and no accumulator is written for it."""
+    if fused_last:
+        return (6 + 10 * (M - 2)) * nd, 6 * nd + 26
+    return (6 + 10 * (M - 1)) * nd, 4 * nd + 26
 
 
 def run_accum(args):
@@ -1305,21 +1324,28 @@ def run_accum(args):
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream(dev)
     inv_m = float(1.0 / M)
-    acc_bytes = (6 + 10 * (M - 1)) * nd * S
-    fused_bytes = (4 * nd + 26) * S
+    fused_last = not args.accum_two_pass
+    n_acc = M - 1 if fused_last else M        # accumulate launches per step
+    acc_b, fused_b = _accum_bytes(nd, M, fused_last)
+    acc_bytes, fused_bytes = acc_b * S, fused_b * S
     ag_bytes = 4 * Pu
     step_bytes = acc_bytes + fused_bytes + ag_bytes
     kernel_names = {}
+    last = [micro[M - 1][q * S:(q + 1) * S] for q in range(nd)]
 
     def one_step(ev):
         if ev is not None:
             ev[0].record(stream)
-        for j in range(M):
+        for j in range(n_acc):
             ss.fsdp_grad_accumulate(micro[j], acc, inv_m, j == 0, stream=stream)
         kernel_names["accumulate"] = ss.last_kernel()
         if ev is not None:
             ev[1].record(stream)
-        opt.step(stream=stream)
+        if fused_last:
+            opt.step_with_last_micro_batch(last, inv_m, stream=stream)
+        else:
+            opt.step(stream=stream)
+        kernel_names["fused"] = ss.last_kernel()
         if ev is not None:
             ev[2].record(stream)
         opt.gather_unit(u, peers, full, stream=stream)
@@ -1357,20 +1383,27 @@ def run_accum(args):
                    "model_shape": f"Llama-style 1B, {len(w.units)} FSDP units",
                    "psi": w.psi, "nd": nd, "micro_batches": M, "rank": r, "shard_elements": S,
                    "grad_dtype": "bf16 micro-batch gradients, fp32 accumulators",
-                   "step": "4 accumulate launches over the 8 contributions (first writes, "
-                           "then read-add-write), fused rs_avg+AdamW+bf16 cast on the fp32 "
-                           "accumulators (1 launch), all-gather of one layer unit (1 launch)",
+                   "step": (f"{n_acc} accumulate launches over the {nd} contributions (first "
+                            "writes, then read-add-write), "
+                            + ("the last micro-batch accumulated inside the fused rs_avg+AdamW+"
+                               "bf16 cast launch (reads the fp32 accumulators and the bf16 "
+                               "gradients)" if fused_last else
+                               "fused rs_avg+AdamW+bf16 cast on the fp32 accumulators (1 "
+                               "launch)")
+                            + ", all-gather of one layer unit (1 launch)"),
                    "bytes_per_step": step_bytes,
                    "l2": f"no flush: each step streams {step_bytes / 1e9:.1f} GB vs a 129 MB L2"},
         "params_per_s": round(S * world / (ms / 1e3), 1),
         "kernels": {"accumulate_ms": round(acc_ms, 4), "accumulate_gbs": round(acc_gbs, 1),
+                    "fused_kernel": kernel_names["fused"],
                     "fused_ms": round(fused_ms, 4), "fused_gbs": round(fused_gbs, 1),
                     "fused_frac": round(fused_gbs / measured_peak()[0], 4),
                     "ag_ms": round(ag_ms, 4),
                     "ag_gbs": round(ag_bytes / (ag_ms / 1e3) / 1e9, 1)},
         "roofline": _roofline(acc_gbs, f"{kernel_names['accumulate']} "
-                                       f"(4 launches over {nd} x {S} elements)",
-                              acc_bytes // M, _traffic(ACCUM_WORKLOAD, nd * S, args)),
+                                       f"({n_acc} launches over {nd} x {S} elements)",
+                              acc_bytes // n_acc, _traffic(ACCUM_WORKLOAD, nd * S, args)
+                              if fused_last else None),
         "e2e": None, "e2e_note": "device-resident micro-batch gradients; the end-to-end "
                                  "line is the default workload's",
         "gpu_launches": launches, "clocks": clk, "cpu_baseline": cpu}))

@@ -188,6 +188,37 @@ int fsdp_rs_avg_adamw_cast(const void* const* grad_slices, int32_t grad_dtype, i
                            int64_t S, float* master, float* m, float* v, uint16_t* out_bf16,
                            const shardstep_adamw_t* hp, void* stream);
 
+/* fsdp_accumulate_rs_avg_adamw_cast -- device, one kernel pass.
+ * The last of M micro-batches ([P1] section "Naïve Data Parallelism": the
+ * gradients accumulate locally and only the last micro-batch synchronises)
+ * accumulated and reduce-scattered in the same pass.  Rank q's contribution
+ * to this rank's shard is the value fsdp_grad_accumulate(first = 0) would
+ * store for the last micro-batch,
+ *     G_q[i] = acc_slices[q][i] + bf16->fp32(last_slices[q][i]) * scale
+ * (fp32, the product rounded, then the sum), and the step proceeds exactly
+ * as fsdp_rs_avg_adamw_cast with fp32 slices G_q: the same bits as
+ * fsdp_grad_accumulate on every rank's slice followed by the fused step.
+ * The accumulators are read, not written: afterwards they still hold
+ * micro-batches 0..M-2.  Per shard element it moves 6*N_d + 26 bytes where
+ * the two calls move 14*N_d + 26.
+ *   acc_slices[nd]   host array of device pointers: rank q's fp32
+ *                    accumulator (micro-batches 0..M-2) + r*S, S elements.
+ *   last_slices[nd]  host array of device pointers: rank q's bf16 gradient
+ *                    of the last micro-batch + r*S, S elements.
+ *   scale            the fp32 value of 1/M, as given to fsdp_grad_accumulate.
+ *   nd, S, master, m, v, out_bf16, hp: as in fsdp_rs_avg_adamw_cast.
+ * No input slice may overlap an output; the outputs must not overlap one
+ * another.  Any alignment is accepted; accumulator slices and state 16-byte
+ * aligned with bf16 slices and out_bf16 8-byte aligned take the vector
+ * kernel (4 elements per access), anything else one element per access.
+ * Errors: INVALID (null pointer, S < 0, step < 1, overlap), CAPACITY
+ * (nd > SHARDSTEP_MAX_ND), CUDA (launch refused). */
+int fsdp_accumulate_rs_avg_adamw_cast(const float* const* acc_slices,
+                                      const uint16_t* const* last_slices, int32_t nd, int64_t S,
+                                      float scale, float* master, float* m, float* v,
+                                      uint16_t* out_bf16, const shardstep_adamw_t* hp,
+                                      void* stream);
+
 /* fsdp_hybrid_rs_avg_adamw_cast -- device, one kernel pass.
  * Hybrid sharding with sharding factor F = shard_group ([P2] section 2,
  * sharding factor: F = 1 is full replication, F = N_d full sharding; [P2]

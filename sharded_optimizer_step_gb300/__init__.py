@@ -26,6 +26,7 @@ __all__ = [
     "set_fused_path", "device_status", "fsdp_hybrid_rs_avg_adamw_cast", "hybrid_state_bytes",
     "hybrid_comm_bytes", "Fsdp2Layout", "fsdp2_layout", "fsdp2_local_views", "fsdp2_chunk_cat",
     "fsdp2_all_gather_copy_out", "AdamWState", "fsdp_state_rs_avg_adamw_cast",
+    "fsdp_accumulate_rs_avg_adamw_cast",
 ]
 
 
@@ -171,6 +172,38 @@ def fsdp_rs_avg_adamw_cast(grad_slices, master, m, v, out_bf16, hp: AdamW, step:
     ``grad_slices[q]`` is rank q's contribution to this shard (S elements,
     all bf16 or all fp32)."""
     _fused(grad_slices, master, m, v, out_bf16, hp, step, stream, None)
+
+
+def fsdp_accumulate_rs_avg_adamw_cast(acc_slices, last_slices, scale: float, master, m, v,
+                                      out_bf16, hp: AdamW, step: int, stream=None):
+    """The last micro-batch accumulated and the shard stepped in one pass:
+    rank q's contribution is ``acc_slices[q] + last_slices[q] * scale`` (fp32
+    accumulators of micro-batches 0..M-2, bf16 gradients of the last one,
+    ``scale`` = 1/M), then the step of ``fsdp_rs_avg_adamw_cast``.  The
+    accumulators are read, not written."""
+    import torch
+    if not acc_slices or len(acc_slices) != len(last_slices):
+        raise ValueError("need as many accumulator slices as last-micro-batch slices (>= 1)")
+    _need_cuda(*acc_slices, *last_slices, master, m, v, out_bf16)
+    S = master.numel()
+    for a, g in zip(acc_slices, last_slices):
+        if a.dtype != torch.float32 or g.dtype != torch.bfloat16 or a.numel() != S \
+                or g.numel() != S:
+            raise ValueError("accumulator slices fp32, last slices bf16, S elements each")
+    for t in (master, m, v):
+        if t.dtype != torch.float32 or t.numel() != S:
+            raise ValueError("master / m / v must be fp32 with S elements")
+    if out_bf16.dtype != torch.bfloat16 or out_bf16.numel() != S:
+        raise ValueError("out_bf16 must be bf16 with S elements")
+    hpc = hp.at_step(step)
+    _capi.check("fsdp_accumulate_rs_avg_adamw_cast",
+                _capi.lib().fsdp_accumulate_rs_avg_adamw_cast(
+                    _capi.ptr_array([a.data_ptr() for a in acc_slices]),
+                    _capi.ptr_array([g.data_ptr() for g in last_slices]), len(acc_slices), S,
+                    ctypes.c_float(scale), ctypes.c_void_p(master.data_ptr()),
+                    ctypes.c_void_p(m.data_ptr()), ctypes.c_void_p(v.data_ptr()),
+                    ctypes.c_void_p(out_bf16.data_ptr()), ctypes.byref(hpc),
+                    _stream(stream, master.device)))
 
 
 def fsdp_hybrid_rs_avg_adamw_cast(grad_slices, shard_group: int, master, m, v, out_bf16,

@@ -575,9 +575,6 @@ int take_slices(const void* const* grad_slices, int32_t grad_dtype, int32_t nd, 
     return SHARDSTEP_OK;
 }
 
-// The fused step with the slices reduced in groups of `group` ranks
-// (group == nd: plain rank order); with `scaled`, the mean is multiplied by
-// inv_scale and a non-zero *skip at launch leaves everything unchanged.
 // Shared argument checks of the hybrid / scaled entry points (INVALID with a
 // message, or SHARDSTEP_OK).
 int check_shard_group(int32_t nd, int32_t shard_group) {
@@ -597,6 +594,9 @@ int check_scaler_words(const float* scale, const uint32_t* found_inf) {
 
 // `hp` gives the AdamW scalars on the host; with `state` instead, the
 // kernels read them from the device-resident step state.
+// The fused step with the slices reduced in groups of `group` ranks
+// (group == nd: plain rank order); with `scaled`, the mean is multiplied by
+// inv_scale and a non-zero *skip at launch leaves everything unchanged.
 int fused_step(const void* const* grad_slices, int32_t grad_dtype, int32_t nd, int32_t group,
                int64_t S, float* master, float* m, float* v, uint16_t* out_bf16,
                const shardstep_adamw_t* hp, void* stream, const float* scale = nullptr,
@@ -676,6 +676,53 @@ int fsdp_rs_avg_adamw_cast(const void* const* grad_slices, int32_t grad_dtype, i
                            int64_t S, float* master, float* m, float* v, uint16_t* out_bf16,
                            const shardstep_adamw_t* hp, void* stream) {
     return fused_step(grad_slices, grad_dtype, nd, nd, S, master, m, v, out_bf16, hp, stream);
+}
+
+int fsdp_accumulate_rs_avg_adamw_cast(const float* const* acc_slices,
+                                      const uint16_t* const* last_slices, int32_t nd, int64_t S,
+                                      float scale, float* master, float* m, float* v,
+                                      uint16_t* out_bf16, const shardstep_adamw_t* hp,
+                                      void* stream) {
+    if (nd < 1) return fail(SHARDSTEP_ERR_INVALID, "nd must be >= 1 (got %d)", nd);
+    if (nd > SHARDSTEP_MAX_ND)
+        return fail(SHARDSTEP_ERR_CAPACITY, "nd %d > %d", nd, SHARDSTEP_MAX_ND);
+    if (S < 0) return fail(SHARDSTEP_ERR_INVALID, "S must be >= 0");
+    if (hp == nullptr) return fail(SHARDSTEP_ERR_INVALID, "hp is NULL");
+    if (hp->step < 1)
+        return fail(SHARDSTEP_ERR_INVALID, "step must be >= 1 (got %lld)",
+                    static_cast<long long>(hp->step));
+    if (S == 0) return ok();
+    if (!master || !m || !v || !out_bf16)
+        return fail(SHARDSTEP_ERR_INVALID, "master / m / v / out_bf16 is NULL");
+    if (!aligned(master, 4) || !aligned(m, 4) || !aligned(v, 4) || !aligned(out_bf16, 2))
+        return fail(SHARDSTEP_ERR_INVALID, "state or output misaligned for its element type");
+    const Span outs[4] = {span(master, S * 4), span(m, S * 4), span(v, S * 4),
+                          span(out_bf16, S * 2)};
+    for (int a = 0; a < 4; ++a)
+        for (int b = a + 1; b < 4; ++b)
+            if (overlap(outs[a], outs[b]))
+                return fail(SHARDSTEP_ERR_INVALID, "outputs %d and %d overlap", a, b);
+    PtrTable acc, last;
+    bool vec_a = false, vec_l = false, tma = false;
+    int rc = take_slices(reinterpret_cast<const void* const*>(acc_slices), SHARDSTEP_DTYPE_F32,
+                         nd, S, outs, 4, &acc, &vec_a, &tma);
+    if (rc != SHARDSTEP_OK) return rc;
+    rc = take_slices(reinterpret_cast<const void* const*>(last_slices), SHARDSTEP_DTYPE_BF16, nd,
+                     S, outs, 4, &last, &vec_l, &tma);
+    if (rc != SHARDSTEP_OK) return rc;
+    const bool vec = vec_a && vec_l && aligned(master, 16) && aligned(m, 16) &&
+                     aligned(v, 16) && aligned(out_bf16, 8);
+    cudaError_t e = launch_accum_rs_adamw_cast(acc, last, nd, S, scale, master, m, v, out_bf16,
+                                               adam_scalars(*hp), mean_op(nd, nd), vec,
+                                               static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "fused accumulate + step kernel launch");
+    if (vec && compiled_nd(nd, {1, 2, 4, 8}))
+        note_kernel("accum_rs_adamw_cast_vec4<%d> (register-staged)", nd);
+    else if (vec)
+        note_kernel("accum_rs_adamw_cast_vec4<any N_d = %d> (register-staged)", nd);
+    else
+        note_kernel("accum_rs_adamw_cast_scalar");
+    return ok();
 }
 
 int fsdp_hybrid_rs_avg_adamw_cast(const void* const* grad_slices, int32_t grad_dtype, int32_t nd,

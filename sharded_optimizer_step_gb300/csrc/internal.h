@@ -169,5 +169,12 @@ cudaError_t launch_copy16(const AlignedTable& t, bool pdl, cudaStream_t stream);
 cudaError_t launch_copy16_shift(const AlignedTable& t, bool pdl, cudaStream_t stream);
 cudaError_t launch_accumulate(const uint16_t* g, float* acc, int64_t n, float scale, bool first,
                               bool vec, cudaStream_t stream);
+// The last micro-batch's accumulation fused into the step (accum_step.cu):
+// fp32 accumulator slices `acc`, bf16 last micro-batch slices `last`; `vec`:
+// accumulators and state 16-byte aligned, bf16 slices and output 8-byte.
+cudaError_t launch_accum_rs_adamw_cast(const PtrTable& acc, const PtrTable& last, int nd,
+                                       int64_t S, float scale, float* master, float* m,
+                                       float* v, uint16_t* out, const AdamScalars& c,
+                                       const MeanOp& mo, bool vec, cudaStream_t stream);
 
 }  // namespace shardstep

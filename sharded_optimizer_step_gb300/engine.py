@@ -15,8 +15,9 @@ from __future__ import annotations
 
 import torch
 
-from . import (AdamW, AdamWState, fsdp_ag_unpack, fsdp_hybrid_rs_avg_adamw_cast, fsdp_layout,
-               fsdp_rs_avg_adamw_cast, fsdp_state_rs_avg_adamw_cast, fsdp_views)
+from . import (AdamW, AdamWState, fsdp_accumulate_rs_avg_adamw_cast, fsdp_ag_unpack,
+               fsdp_hybrid_rs_avg_adamw_cast, fsdp_layout, fsdp_rs_avg_adamw_cast,
+               fsdp_state_rs_avg_adamw_cast, fsdp_views)
 
 
 def _numel(shape):
@@ -70,6 +71,18 @@ class RankShardOptimizer:
         else:
             fsdp_hybrid_rs_avg_adamw_cast(grads, self.F, master, m, v, params, self.hp, self.t,
                                           stream=stream)
+
+    def step_with_last_micro_batch(self, last, scale: float, stream=None):
+        """The step of ``step`` where ``grad_in`` holds fp32 accumulators of
+        micro-batches 0..M-2 and ``last[q]`` is contribution q's bf16
+        gradient of the last micro-batch (laid out like ``grad_in[q]``):
+        the last accumulation (``scale`` = 1/M) runs inside the fused launch
+        and ``grad_in`` is left as it was.  Plain sharding only."""
+        if self.F != self.nd:
+            raise ValueError("the fused last-micro-batch step is for plain sharding")
+        self.t += 1
+        fsdp_accumulate_rs_avg_adamw_cast(self.grad_in, last, scale, self.master, self.m, self.v,
+                                          self.params, self.hp, self.t, stream=stream)
 
     def begin_step(self):
         """Advance the step count for an update issued piece by piece with

@@ -150,6 +150,34 @@ def test_fused_step_rejects_bad_arguments_before_launch():
     assert _fused(g, 8, 0, *st) == _capi.OK                             # nothing to do
 
 
+def test_accumulate_step_rejects_bad_arguments_before_launch():
+    L = _capi.lib()
+    S = 1024
+    A = 1 << 40  # fake device addresses, never dereferenced: validation fails first
+    acc = [A + k * (1 << 20) for k in range(8)]
+    last = [A + (1 << 28) + k * (1 << 20) for k in range(8)]
+    st = [A + (1 << 30) + k * (1 << 20) for k in range(4)]
+
+    def call(acc, last, nd, S, *state, step=1):
+        hp = ss.AdamW().at_step(step)
+        return L.fsdp_accumulate_rs_avg_adamw_cast(
+            _capi.ptr_array(acc), _capi.ptr_array(last), nd, S, ctypes.c_float(0.25),
+            *[ctypes.c_void_p(a) for a in state], ctypes.byref(hp), None)
+
+    assert call(acc, last, 0, S, *st) == _capi.ERR_INVALID
+    assert call(acc * 9, last * 9, 65, S, *st) == _capi.ERR_CAPACITY
+    assert call(acc, last, 8, S, *st, step=0) == _capi.ERR_INVALID
+    assert call(acc, last, 8, -1, *st) == _capi.ERR_INVALID
+    assert call(acc[:7] + [0], last, 8, S, *st) == _capi.ERR_INVALID       # NULL accumulator
+    assert call(acc, last[:7] + [0], 8, S, *st) == _capi.ERR_INVALID       # NULL last slice
+    assert call(acc, last[:7] + [st[3]], 8, S, *st) == _capi.ERR_INVALID   # input overlaps out
+    assert "overlaps" in L.shardstep_last_error().decode()
+    assert call(acc[:7] + [st[1]], last, 8, S, *st) == _capi.ERR_INVALID   # acc overlaps m
+    assert call(acc, last, 8, S, st[0], st[0] + 8, st[2], st[3]) == _capi.ERR_INVALID
+    assert call(acc[:7] + [acc[7] + 2], last, 8, S, *st) == _capi.ERR_INVALID  # misaligned fp32
+    assert call(acc, last, 8, 0, *st) == _capi.OK                           # nothing to do
+
+
 def test_other_entry_points_reject_bad_arguments():
     L = _capi.lib()
     A = 1 << 40

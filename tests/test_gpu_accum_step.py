@@ -1,0 +1,147 @@
+"""GPU parity of fsdp_accumulate_rs_avg_adamw_cast: the last micro-batch's
+accumulation fused into the sharded step.  The expected values are the
+oracle's accumulation over all M micro-batches followed by its shard step;
+the accumulators must still hold micro-batches 0..M-2 afterwards."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sharded_optimizer_step_gb300 as ss
+import synth
+from oracle.numerics import AdamWConfig
+from tests._cmp import assert_bf16, assert_bits, assert_f32
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+HP = AdamWConfig(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
+HPC = ss.AdamW(lr=HP.lr, beta1=HP.beta1, beta2=HP.beta2, eps=HP.eps, weight_decay=HP.weight_decay)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    ss.build()
+    yield
+
+
+def dev(x, shift=0):
+    """numpy (bf16 bits as uint16, or fp32) -> CUDA tensor starting `shift`
+    elements into its allocation."""
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.uint16:
+        buf = torch.empty(x.size + shift + 8, dtype=torch.bfloat16, device=DEV)
+        t = buf[shift:shift + x.size]
+        t.copy_(torch.from_numpy(x.view(np.int16)).view(torch.bfloat16))
+    else:
+        buf = torch.empty(x.size + shift + 8, dtype=torch.float32, device=DEV)
+        t = buf[shift:shift + x.size]
+        t.copy_(torch.from_numpy(x.astype(np.float32)))
+    return t
+
+
+def host(t):
+    if t.dtype == torch.bfloat16:
+        return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    return t.contiguous().cpu().numpy()
+
+
+def _micro(seed, nd, M, S):
+    """micro[q][j]: rank q's bf16 gradient slice of micro-batch j."""
+    return [[synth.host_fill(synth.normal_stream(seed, (91, q, j), 1e-3), 0, S, "bf16")
+             for j in range(M)] for q in range(nd)]
+
+
+def _state(seed, S):
+    p = synth.host_fill(synth.normal_stream(seed, (91, 100), 0.02), 0, S, "f32")
+    m = synth.host_fill(synth.normal_stream(seed, (91, 101), 1e-4), 0, S, "f32")
+    v = np.abs(synth.host_fill(synth.normal_stream(seed, (91, 102), 1e-7), 0, S, "f32"))
+    return p, m, v
+
+
+def _check(nd, S, M, step, shift):
+    seed = 31 * nd + S + M
+    micro = _micro(seed, nd, M, S)
+    scale = np.float32(1.0 / M)
+    p, m, v = _state(seed, S)
+    dp, dm, dv = dev(p, shift), dev(m, shift), dev(v, shift)
+    out = torch.empty(S + 1, dtype=torch.bfloat16, device=DEV)[shift:shift + S]
+    accs = []
+    for q in range(nd):
+        acc = dev(np.zeros(S, np.float32), shift if q % 2 else 0)
+        for j in range(M - 1):
+            ss.fsdp_grad_accumulate(dev(micro[q][j]), acc, float(scale), j == 0)
+        accs.append(acc)
+    last = [dev(micro[q][M - 1], shift if q % 3 == 1 else 0) for q in range(nd)]
+    ss.fsdp_accumulate_rs_avg_adamw_cast(accs, last, float(scale), dp, dm, dv, out, HPC, step)
+    contribs = [oracle.grad_accumulate(micro[q], scale) for q in range(nd)]
+    wp, wm, wv, wo = oracle.fsdp_shard_step(contribs, 0, S, p, m, v, HP, step)
+    torch.cuda.synchronize()
+    for name, got, want in (("master", host(dp), wp), ("m", host(dm), wm), ("v", host(dv), wv)):
+        assert_f32(got, want, name)
+        assert_bits(got, want, name)
+    assert_bf16(host(out), wo, "bf16")
+    assert_bits(host(out), wo, "bf16")
+    for q in range(nd):  # the accumulators are read, not written
+        assert_bits(host(accs[q]), oracle.grad_accumulate(micro[q][:M - 1], scale), "acc")
+
+
+@pytest.mark.parametrize("nd", [1, 2, 3, 4, 5, 8, 9, 16])
+@pytest.mark.parametrize("S", [1, 13, 4099])
+@pytest.mark.parametrize("shift", [0, 1])
+def test_accumulate_step_matches_oracle(nd, S, shift):
+    _check(nd, S, M=3, step=1 + nd % 3, shift=shift)
+
+
+@pytest.mark.parametrize("nd,S,M", [(8, 152 * 128 * 6 * 2 + 7, 4), (8, 1 << 18, 2),
+                                    (4, 70001, 5), (6, 65537, 3)])
+def test_accumulate_step_multi_wave(nd, S, M):
+    _check(nd, S, M, step=7, shift=0)
+
+
+@pytest.mark.parametrize("nd,S", [(8, (1 << 20) + 3), (3, 100003)])
+def test_accumulate_step_equals_the_two_call_path(nd, S):
+    """Same bits as fsdp_grad_accumulate on the last micro-batch followed by
+    the fused step on the fp32 accumulators, on the device."""
+    M = 4
+    scale = np.float32(1.0 / M)
+    micro = _micro(S, nd, M, S)
+    p, m, v = _state(S, S)
+    accs = []
+    for q in range(nd):
+        acc = torch.empty(S, dtype=torch.float32, device=DEV)
+        for j in range(M - 1):
+            ss.fsdp_grad_accumulate(dev(micro[q][j]), acc, float(scale), j == 0)
+        accs.append(acc)
+    last = [dev(micro[q][M - 1]) for q in range(nd)]
+    a = [dev(x) for x in (p, m, v)] + [torch.empty(S, dtype=torch.bfloat16, device=DEV)]
+    b = [t.clone() for t in a]
+    ss.fsdp_accumulate_rs_avg_adamw_cast(accs, last, float(scale), *a, HPC, 3)
+    for q in range(nd):
+        ss.fsdp_grad_accumulate(last[q], accs[q], float(scale), False)
+    ss.fsdp_rs_avg_adamw_cast(accs, *b, HPC, 3)
+    torch.cuda.synchronize()
+    for x, y, name in zip(a, b, ("master", "m", "v", "bf16")):
+        assert torch.equal(x.view(torch.int32) if x.dtype == torch.float32
+                           else x.view(torch.int16),
+                           y.view(torch.int32) if y.dtype == torch.float32
+                           else y.view(torch.int16)), name
+
+
+def test_accumulate_step_names_its_kernel():
+    S = 4096
+    accs = [torch.zeros(S, device=DEV) for _ in range(8)]
+    last = [torch.zeros(S, dtype=torch.bfloat16, device=DEV) for _ in range(8)]
+    st = [torch.zeros(S, device=DEV) for _ in range(3)] + [
+        torch.empty(S, dtype=torch.bfloat16, device=DEV)]
+    ss.fsdp_accumulate_rs_avg_adamw_cast(accs, last, 0.5, *st, HPC, 1)
+    assert ss.last_kernel() == "accum_rs_adamw_cast_vec4<8> (register-staged)"
+    ss.fsdp_accumulate_rs_avg_adamw_cast(accs[:6], last[:6], 0.5, *st, HPC, 1)
+    assert ss.last_kernel() == "accum_rs_adamw_cast_vec4<any N_d = 6> (register-staged)"
+    ss.fsdp_accumulate_rs_avg_adamw_cast([a[1:] for a in accs[:2]], [t[1:] for t in last[:2]],
+                                         0.5,
+                                         *[t[1:] for t in st], HPC, 1)
+    assert ss.last_kernel() == "accum_rs_adamw_cast_scalar"
+    torch.cuda.synchronize()
