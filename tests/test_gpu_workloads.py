@@ -6,7 +6,9 @@ sampled outputs that the oracle computes one by one from the same seeded
 inputs (every step, every micro-batch, every rank), plus properties that hold
 at any size.  The Llama-7B rank view runs in the launch configuration the
 benchmark times: one fused launch over the rank's 842,301,952-element shard
-and one all-gather of a 202,383,360-parameter layer unit."""
+and one all-gather of a 202,383,360-parameter layer unit; so does the
+Llama-1B accumulation view (three accumulate launches over the 8
+contributions, the fourth micro-batch inside one fused launch)."""
 import numpy as np
 import pytest
 import torch
@@ -262,6 +264,58 @@ def test_llama_7b_rank_view_as_benchmarked():
             continue
         want = synth.host_gather(w.peer_shard_stream(w.steps, q, u), loc, "bf16")
         assert_bits(_host_bf16(full[q * S + torch.from_numpy(loc).to(DEV)]), want, "peer shard")
+
+
+def test_llama_1b_rank_view_accumulation_as_benchmarked():
+    """The accumulation line's launches: per step M - 1 accumulate launches
+    over the 8 contributions side by side, then the last micro-batch inside
+    the fused step (one launch over the whole 150,610,176-element shard);
+    the oracle accumulates all M micro-batches and steps, on sampled shard
+    positions, and the accumulators still hold micro-batches 0..M-2."""
+    w = W.llama_1b()
+    hp, hpc = _hp(w)
+    nd, M, r = w.nd, w.micro, 0
+    opt = RankShardOptimizer(w.units, nd, r, hpc, device=DEV, grad_dtype=torch.float32)
+    S = opt.shard_total
+    assert S == 150_610_176 and M == 4
+    acc = torch.empty(nd * S, dtype=torch.float32, device=DEV)
+    opt.grad_in = [acc[q * S:(q + 1) * S] for q in range(nd)]
+    micro = [torch.empty(nd * S, dtype=torch.bfloat16, device=DEV) for _ in range(M)]
+    last = [micro[M - 1][q * S:(q + 1) * S] for q in range(nd)]
+    W.dev_fill_rank_master(w, r, opt.master)
+    rng = np.random.default_rng(11)
+    parts, total = W.rank_shard_index(w)
+    assert total == S
+    bounds = [s for _, s, _ in parts] + [s - 1 for _, s, _ in parts[1:]]
+    idx = _sample(S, 100_000, rng, extra=bounds)
+    p = W.host_gather_rank_master(w, r, idx)
+    m = np.zeros(idx.size, np.float32)
+    v = np.zeros(idx.size, np.float32)
+    inv_m = np.float32(1.0 / M)
+    for t in range(1, 4):
+        for j in range(M):
+            for q in range(nd):
+                W.dev_fill_rank_grad(w, t, r, q, j, micro[j][q * S:(q + 1) * S])
+        launches = ss.launch_count()
+        for j in range(M - 1):
+            ss.fsdp_grad_accumulate(micro[j], acc, float(inv_m), j == 0)
+        opt.step_with_last_micro_batch(last, float(inv_m))
+        assert ss.launch_count() - launches == M
+        assert ss.last_kernel() == "accum_rs_adamw_cast_vec4<8> (register-staged)"
+        grads = [[W.host_gather_rank_grad(w, t, r, q, j, idx) for j in range(M)]
+                 for q in range(nd)]
+        contribs = [oracle.grad_accumulate(grads[q], inv_m) for q in range(nd)]
+        p, m, v, ob = oracle.fsdp_shard_step(contribs, 0, idx.size, p, m, v, hp, t)
+    torch.cuda.synchronize()
+    it = torch.from_numpy(idx).to(DEV)
+    assert_f32(opt.master[it].cpu().numpy(), p, "master")
+    assert_bits(opt.master[it].cpu().numpy(), p, "master")
+    assert_bits(opt.m[it].cpu().numpy(), m, "m")
+    assert_bits(opt.v[it].cpu().numpy(), v, "v")
+    assert_bits(_host_bf16(opt.params[it]), ob, "bf16")
+    for q in (0, nd - 1):
+        assert_bits(opt.grad_in[q][it].cpu().numpy(),
+                    oracle.grad_accumulate(grads[q][:M - 1], inv_m), f"accumulator {q}")
 
 
 def test_llama_7b_rank_view_every_kernel_and_the_graph_agree_everywhere():
