@@ -584,6 +584,25 @@ int check_shard_group(int32_t nd, int32_t shard_group) {
     return SHARDSTEP_OK;
 }
 
+// master / m / v (fp32) and out_bf16 of a step over S > 0 elements: present,
+// aligned for their element type and pairwise disjoint; fills their spans.
+int check_step_outputs(int64_t S, const float* master, const float* m, const float* v,
+                       const uint16_t* out_bf16, Span* outs) {
+    if (!master || !m || !v || !out_bf16)
+        return fail(SHARDSTEP_ERR_INVALID, "master / m / v / out_bf16 is NULL");
+    if (!aligned(master, 4) || !aligned(m, 4) || !aligned(v, 4) || !aligned(out_bf16, 2))
+        return fail(SHARDSTEP_ERR_INVALID, "state or output misaligned for its element type");
+    outs[0] = span(master, S * 4);
+    outs[1] = span(m, S * 4);
+    outs[2] = span(v, S * 4);
+    outs[3] = span(out_bf16, S * 2);
+    for (int a = 0; a < 4; ++a)
+        for (int b = a + 1; b < 4; ++b)
+            if (overlap(outs[a], outs[b]))
+                return fail(SHARDSTEP_ERR_INVALID, "outputs %d and %d overlap", a, b);
+    return SHARDSTEP_OK;
+}
+
 int check_scaler_words(const float* scale, const uint32_t* found_inf) {
     if (found_inf == nullptr || scale == nullptr)
         return fail(SHARDSTEP_ERR_INVALID, "found_inf / scale is NULL");
@@ -622,16 +641,9 @@ int fused_step(const void* const* grad_slices, int32_t grad_dtype, int32_t nd, i
         c = adam_scalars(*hp);
     }
     if (S == 0) return ok();
-    if (!master || !m || !v || !out_bf16)
-        return fail(SHARDSTEP_ERR_INVALID, "master / m / v / out_bf16 is NULL");
-    if (!aligned(master, 4) || !aligned(m, 4) || !aligned(v, 4) || !aligned(out_bf16, 2))
-        return fail(SHARDSTEP_ERR_INVALID, "state or output misaligned for its element type");
-    const Span outs[4] = {span(master, S * 4), span(m, S * 4), span(v, S * 4),
-                          span(out_bf16, S * 2)};
-    for (int a = 0; a < 4; ++a)
-        for (int b = a + 1; b < 4; ++b)
-            if (overlap(outs[a], outs[b]))
-                return fail(SHARDSTEP_ERR_INVALID, "outputs %d and %d overlap", a, b);
+    Span outs[4];
+    if (int rc = check_step_outputs(S, master, m, v, out_bf16, outs); rc != SHARDSTEP_OK)
+        return rc;
     // vector path: 4 elements per access -> 16-byte state, 8-byte 16-bit
     // (16-byte fp32) gradient slices, 8-byte bf16 output
     PtrTable tab;
@@ -692,16 +704,9 @@ int fsdp_accumulate_rs_avg_adamw_cast(const float* const* acc_slices,
         return fail(SHARDSTEP_ERR_INVALID, "step must be >= 1 (got %lld)",
                     static_cast<long long>(hp->step));
     if (S == 0) return ok();
-    if (!master || !m || !v || !out_bf16)
-        return fail(SHARDSTEP_ERR_INVALID, "master / m / v / out_bf16 is NULL");
-    if (!aligned(master, 4) || !aligned(m, 4) || !aligned(v, 4) || !aligned(out_bf16, 2))
-        return fail(SHARDSTEP_ERR_INVALID, "state or output misaligned for its element type");
-    const Span outs[4] = {span(master, S * 4), span(m, S * 4), span(v, S * 4),
-                          span(out_bf16, S * 2)};
-    for (int a = 0; a < 4; ++a)
-        for (int b = a + 1; b < 4; ++b)
-            if (overlap(outs[a], outs[b]))
-                return fail(SHARDSTEP_ERR_INVALID, "outputs %d and %d overlap", a, b);
+    Span outs[4];
+    if (int rc = check_step_outputs(S, master, m, v, out_bf16, outs); rc != SHARDSTEP_OK)
+        return rc;
     PtrTable acc, last;
     bool vec_a = false, vec_l = false, tma = false;
     int rc = take_slices(reinterpret_cast<const void* const*>(acc_slices), SHARDSTEP_DTYPE_F32,
