@@ -17,7 +17,9 @@
 // before any arithmetic (one 16-byte load per accumulator slice, one 8-byte
 // load per bf16 slice, one 16-byte load per state array), streaming loads
 // and stores.  With N_d = 8 that is 60 registers of loads per thread, so
-// the register cap is raised to 80 (6 blocks per SM).
+// the register cap is raised to 80 (6 blocks per SM).  Compiled for N_d =
+// 1, 2, 3, 4, 6 and 8, an up-to-8 form for 5 and 7, and a loop over batches
+// of 4 slices for the rest.
 #include "common.cuh"
 
 namespace shardstep {
@@ -26,30 +28,35 @@ namespace {
 constexpr int kAccThreads = 128;
 constexpr int kAccRuntimeND = 0;  // any N_d: slices in batches of 4
 
+// ND > 0: exactly ND slices; ND < 0: up to -ND slices, every load in flight
+// at once and the first nd used; kAccRuntimeND: any N_d in batches of 4.
+// Kernels holding the loads of 6 or more slices get 80 registers (6 blocks
+// per SM); at a 64-register cap the 6- and 8-slice kernels spilled.
 template <int ND>
 constexpr int acc_min_blocks() {
-    return ND == 8 || ND == kAccRuntimeND ? 6 : 8;
+    return ND >= 6 || ND < 0 || ND == kAccRuntimeND ? 6 : 8;
 }
 
 // Slice contributions at 4 consecutive elements, summed in rank order.
 template <int ND>
 __device__ __forceinline__ void accum_reduce4(const PtrTable& acc, const PtrTable& last,
                                               int nd, float scale, int64_t i, float* g) {
-    constexpr int B = ND == kAccRuntimeND ? 4 : ND;
+    constexpr int B = ND > 0 ? ND : (ND < 0 ? -ND : 4);
+    constexpr bool kGuard = ND <= 0;
     float s[4];
     for (int q0 = 0; q0 < nd; q0 += B) {
         uint4 a[B];
         uint2 b[B];
 #pragma unroll
         for (int u = 0; u < B; ++u) {
-            if (ND != kAccRuntimeND || q0 + u < nd) {
+            if (!kGuard || q0 + u < nd) {
                 a[u] = ldcs16(static_cast<const float*>(acc.p[q0 + u]) + 4 * i);
                 b[u] = ldcs8(static_cast<const uint16_t*>(last.p[q0 + u]) + 4 * i);
             }
         }
 #pragma unroll
         for (int u = 0; u < B; ++u) {
-            if (ND != kAccRuntimeND || q0 + u < nd) {
+            if (!kGuard || q0 + u < nd) {
                 float t[4];
                 unpack4f(a[u], t);
                 const float f[4] = {bf16_lo(b[u].x), bf16_hi(b[u].x), bf16_lo(b[u].y),
@@ -156,7 +163,12 @@ cudaError_t launch_accum_rs_adamw_cast(const PtrTable& acc, const PtrTable& last
         switch (nd) {
             case 1: return go_accum<1>(acc, last, nd, S, scale, master, m, v, out, c, mo, stream);
             case 2: return go_accum<2>(acc, last, nd, S, scale, master, m, v, out, c, mo, stream);
+            case 3: return go_accum<3>(acc, last, nd, S, scale, master, m, v, out, c, mo, stream);
             case 4: return go_accum<4>(acc, last, nd, S, scale, master, m, v, out, c, mo, stream);
+            case 5:
+            case 7:
+                return go_accum<-8>(acc, last, nd, S, scale, master, m, v, out, c, mo, stream);
+            case 6: return go_accum<6>(acc, last, nd, S, scale, master, m, v, out, c, mo, stream);
             case 8: return go_accum<8>(acc, last, nd, S, scale, master, m, v, out, c, mo, stream);
             default:
                 return go_accum<kAccRuntimeND>(acc, last, nd, S, scale, master, m, v, out, c, mo,

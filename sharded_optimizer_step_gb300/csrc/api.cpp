@@ -721,8 +721,10 @@ int fsdp_accumulate_rs_avg_adamw_cast(const float* const* acc_slices,
                                                adam_scalars(*hp), mean_op(nd, nd), vec,
                                                static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "fused accumulate + step kernel launch");
-    if (vec && compiled_nd(nd, {1, 2, 4, 8}))
+    if (vec && compiled_nd(nd, {1, 2, 3, 4, 6, 8}))
         note_kernel("accum_rs_adamw_cast_vec4<%d> (register-staged)", nd);
+    else if (vec && (nd == 5 || nd == 7))
+        note_kernel("accum_rs_adamw_cast_vec4<up to 8: %d> (register-staged)", nd);
     else if (vec)
         note_kernel("accum_rs_adamw_cast_vec4<any N_d = %d> (register-staged)", nd);
     else

@@ -88,7 +88,7 @@ def _check(nd, S, M, step, shift):
         assert_bits(host(accs[q]), oracle.grad_accumulate(micro[q][:M - 1], scale), "acc")
 
 
-@pytest.mark.parametrize("nd", [1, 2, 3, 4, 5, 8, 9, 16])
+@pytest.mark.parametrize("nd", [1, 2, 3, 4, 5, 6, 7, 8, 9, 16])
 @pytest.mark.parametrize("S", [1, 13, 4099])
 @pytest.mark.parametrize("shift", [0, 1])
 def test_accumulate_step_matches_oracle(nd, S, shift):
@@ -139,7 +139,12 @@ def test_accumulate_step_names_its_kernel():
     ss.fsdp_accumulate_rs_avg_adamw_cast(accs, last, 0.5, *st, HPC, 1)
     assert ss.last_kernel() == "accum_rs_adamw_cast_vec4<8> (register-staged)"
     ss.fsdp_accumulate_rs_avg_adamw_cast(accs[:6], last[:6], 0.5, *st, HPC, 1)
-    assert ss.last_kernel() == "accum_rs_adamw_cast_vec4<any N_d = 6> (register-staged)"
+    assert ss.last_kernel() == "accum_rs_adamw_cast_vec4<6> (register-staged)"
+    ss.fsdp_accumulate_rs_avg_adamw_cast(accs[:5], last[:5], 0.5, *st, HPC, 1)
+    assert ss.last_kernel() == "accum_rs_adamw_cast_vec4<up to 8: 5> (register-staged)"
+    more = accs + accs[:1]
+    ss.fsdp_accumulate_rs_avg_adamw_cast(more, last + last[:1], 0.5, *st, HPC, 1)
+    assert ss.last_kernel() == "accum_rs_adamw_cast_vec4<any N_d = 9> (register-staged)"
     ss.fsdp_accumulate_rs_avg_adamw_cast([a[1:] for a in accs[:2]], [t[1:] for t in last[:2]],
                                          0.5,
                                          *[t[1:] for t in st], HPC, 1)
