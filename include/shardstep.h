@@ -297,6 +297,21 @@ int fsdp_state_rs_avg_adamw_cast(const void* const* grad_slices, int32_t grad_dt
                                  float* v, uint16_t* out_bf16,
                                  const shardstep_adamw_state_t* state, void* stream);
 
+/* fsdp_state_accumulate_rs_avg_adamw_cast -- device, one kernel pass.
+ * fsdp_accumulate_rs_avg_adamw_cast with the AdamW scalars read on the device
+ * from a step state (shardstep_adamw_state_init / _advance), so that the
+ * call launches the same kernel with the same arguments every step and can
+ * be captured in a CUDA graph.  `state`: device, 8-byte aligned, at a step
+ * >= 1 (advance it before the call).  Errors: those of
+ * fsdp_accumulate_rs_avg_adamw_cast, and INVALID for a NULL or misaligned
+ * state. */
+int fsdp_state_accumulate_rs_avg_adamw_cast(const float* const* acc_slices,
+                                            const uint16_t* const* last_slices, int32_t nd,
+                                            int64_t S, float scale, float* master, float* m,
+                                            float* v, uint16_t* out_bf16,
+                                            const shardstep_adamw_state_t* state,
+                                            void* stream);
+
 /* ------------------------------------------------ gradient scaler */
 
 /* Sharded gradient scaler for fp16 loss scaling ([P2] section 3.5: a sharded

@@ -26,7 +26,7 @@ __all__ = [
     "set_fused_path", "device_status", "fsdp_hybrid_rs_avg_adamw_cast", "hybrid_state_bytes",
     "hybrid_comm_bytes", "Fsdp2Layout", "fsdp2_layout", "fsdp2_local_views", "fsdp2_chunk_cat",
     "fsdp2_all_gather_copy_out", "AdamWState", "fsdp_state_rs_avg_adamw_cast",
-    "fsdp_accumulate_rs_avg_adamw_cast",
+    "fsdp_accumulate_rs_avg_adamw_cast", "fsdp_state_accumulate_rs_avg_adamw_cast",
 ]
 
 
@@ -181,6 +181,35 @@ def fsdp_accumulate_rs_avg_adamw_cast(acc_slices, last_slices, scale: float, mas
     accumulators of micro-batches 0..M-2, bf16 gradients of the last one,
     ``scale`` = 1/M), then the step of ``fsdp_rs_avg_adamw_cast``.  The
     accumulators are read, not written."""
+    S = _accum_args(acc_slices, last_slices, master, m, v, out_bf16)
+    hpc = hp.at_step(step)
+    _capi.check("fsdp_accumulate_rs_avg_adamw_cast",
+                _capi.lib().fsdp_accumulate_rs_avg_adamw_cast(
+                    *_accum_ptrs(acc_slices, last_slices, S, scale, master, m, v, out_bf16),
+                    ctypes.byref(hpc), _stream(stream, master.device)))
+
+
+def fsdp_state_accumulate_rs_avg_adamw_cast(acc_slices, last_slices, scale: float, master, m,
+                                            v, out_bf16, state: AdamWState, stream=None):
+    """``fsdp_accumulate_rs_avg_adamw_cast`` with the AdamW scalars read on the
+    device from ``state`` (at a step >= 1): CUDA-graph capturable."""
+    S = _accum_args(acc_slices, last_slices, master, m, v, out_bf16)
+    _need_cuda(state.buf)
+    _capi.check("fsdp_state_accumulate_rs_avg_adamw_cast",
+                _capi.lib().fsdp_state_accumulate_rs_avg_adamw_cast(
+                    *_accum_ptrs(acc_slices, last_slices, S, scale, master, m, v, out_bf16),
+                    ctypes.c_void_p(state.buf.data_ptr()), _stream(stream, master.device)))
+
+
+def _accum_ptrs(acc_slices, last_slices, S, scale, master, m, v, out_bf16):
+    return (_capi.ptr_array([a.data_ptr() for a in acc_slices]),
+            _capi.ptr_array([g.data_ptr() for g in last_slices]), len(acc_slices), S,
+            ctypes.c_float(scale), ctypes.c_void_p(master.data_ptr()),
+            ctypes.c_void_p(m.data_ptr()), ctypes.c_void_p(v.data_ptr()),
+            ctypes.c_void_p(out_bf16.data_ptr()))
+
+
+def _accum_args(acc_slices, last_slices, master, m, v, out_bf16):
     import torch
     if not acc_slices or len(acc_slices) != len(last_slices):
         raise ValueError("need as many accumulator slices as last-micro-batch slices (>= 1)")
@@ -195,15 +224,7 @@ def fsdp_accumulate_rs_avg_adamw_cast(acc_slices, last_slices, scale: float, mas
             raise ValueError("master / m / v must be fp32 with S elements")
     if out_bf16.dtype != torch.bfloat16 or out_bf16.numel() != S:
         raise ValueError("out_bf16 must be bf16 with S elements")
-    hpc = hp.at_step(step)
-    _capi.check("fsdp_accumulate_rs_avg_adamw_cast",
-                _capi.lib().fsdp_accumulate_rs_avg_adamw_cast(
-                    _capi.ptr_array([a.data_ptr() for a in acc_slices]),
-                    _capi.ptr_array([g.data_ptr() for g in last_slices]), len(acc_slices), S,
-                    ctypes.c_float(scale), ctypes.c_void_p(master.data_ptr()),
-                    ctypes.c_void_p(m.data_ptr()), ctypes.c_void_p(v.data_ptr()),
-                    ctypes.c_void_p(out_bf16.data_ptr()), ctypes.byref(hpc),
-                    _stream(stream, master.device)))
+    return S
 
 
 def fsdp_hybrid_rs_avg_adamw_cast(grad_slices, shard_group: int, master, m, v, out_bf16,

@@ -603,6 +603,24 @@ int check_step_outputs(int64_t S, const float* master, const float* m, const flo
     return SHARDSTEP_OK;
 }
 
+// The AdamW scalars of a step: from a device-resident step state (its device
+// address; the host never reads it) when `state` is set, else from `hp`.
+int adam_source(const shardstep_adamw_t* hp, const shardstep_adamw_state_t* state,
+                AdamScalars* c) {
+    if (state != nullptr) {
+        if (!aligned(state, 8)) return fail(SHARDSTEP_ERR_INVALID, "state misaligned");
+        c->dev = reinterpret_cast<const float*>(reinterpret_cast<const char*>(state) +
+                                                offsetof(shardstep_adamw_state_t, scalars));
+        return SHARDSTEP_OK;
+    }
+    if (hp == nullptr) return fail(SHARDSTEP_ERR_INVALID, "hp is NULL");
+    if (hp->step < 1)
+        return fail(SHARDSTEP_ERR_INVALID, "step must be >= 1 (got %lld)",
+                    static_cast<long long>(hp->step));
+    *c = adam_scalars(*hp);
+    return SHARDSTEP_OK;
+}
+
 int check_scaler_words(const float* scale, const uint32_t* found_inf) {
     if (found_inf == nullptr || scale == nullptr)
         return fail(SHARDSTEP_ERR_INVALID, "found_inf / scale is NULL");
@@ -629,17 +647,7 @@ int fused_step(const void* const* grad_slices, int32_t grad_dtype, int32_t nd, i
         return fail(SHARDSTEP_ERR_CAPACITY, "nd %d > %d", nd, SHARDSTEP_MAX_ND);
     if (S < 0) return fail(SHARDSTEP_ERR_INVALID, "S must be >= 0");
     AdamScalars c{};
-    if (state != nullptr) {
-        if (!aligned(state, 8)) return fail(SHARDSTEP_ERR_INVALID, "state misaligned");
-        // the device address of the state's scalars (no host access to it)
-        c.dev = reinterpret_cast<const float*>(reinterpret_cast<const char*>(state) +
-                                               offsetof(shardstep_adamw_state_t, scalars));
-    } else {
-        if (hp == nullptr) return fail(SHARDSTEP_ERR_INVALID, "hp is NULL");
-        if (hp->step < 1) return fail(SHARDSTEP_ERR_INVALID, "step must be >= 1 (got %lld)",
-                                      static_cast<long long>(hp->step));
-        c = adam_scalars(*hp);
-    }
+    if (int rc = adam_source(hp, state, &c); rc != SHARDSTEP_OK) return rc;
     if (S == 0) return ok();
     Span outs[4];
     if (int rc = check_step_outputs(S, master, m, v, out_bf16, outs); rc != SHARDSTEP_OK)
@@ -680,29 +688,18 @@ int fused_step(const void* const* grad_slices, int32_t grad_dtype, int32_t nd, i
     return ok();
 }
 
-}  // namespace
-
-extern "C" {
-
-int fsdp_rs_avg_adamw_cast(const void* const* grad_slices, int32_t grad_dtype, int32_t nd,
-                           int64_t S, float* master, float* m, float* v, uint16_t* out_bf16,
-                           const shardstep_adamw_t* hp, void* stream) {
-    return fused_step(grad_slices, grad_dtype, nd, nd, S, master, m, v, out_bf16, hp, stream);
-}
-
-int fsdp_accumulate_rs_avg_adamw_cast(const float* const* acc_slices,
-                                      const uint16_t* const* last_slices, int32_t nd, int64_t S,
-                                      float scale, float* master, float* m, float* v,
-                                      uint16_t* out_bf16, const shardstep_adamw_t* hp,
-                                      void* stream) {
+// The last micro-batch accumulated inside the fused step; the AdamW scalars
+// from `hp` on the host or from a device-resident step `state`.
+int accum_step(const float* const* acc_slices, const uint16_t* const* last_slices, int32_t nd,
+               int64_t S, float scale, float* master, float* m, float* v, uint16_t* out_bf16,
+               const shardstep_adamw_t* hp, const shardstep_adamw_state_t* state,
+               void* stream) {
     if (nd < 1) return fail(SHARDSTEP_ERR_INVALID, "nd must be >= 1 (got %d)", nd);
     if (nd > SHARDSTEP_MAX_ND)
         return fail(SHARDSTEP_ERR_CAPACITY, "nd %d > %d", nd, SHARDSTEP_MAX_ND);
     if (S < 0) return fail(SHARDSTEP_ERR_INVALID, "S must be >= 0");
-    if (hp == nullptr) return fail(SHARDSTEP_ERR_INVALID, "hp is NULL");
-    if (hp->step < 1)
-        return fail(SHARDSTEP_ERR_INVALID, "step must be >= 1 (got %lld)",
-                    static_cast<long long>(hp->step));
+    AdamScalars c{};
+    if (int rc = adam_source(hp, state, &c); rc != SHARDSTEP_OK) return rc;
     if (S == 0) return ok();
     Span outs[4];
     if (int rc = check_step_outputs(S, master, m, v, out_bf16, outs); rc != SHARDSTEP_OK)
@@ -718,7 +715,7 @@ int fsdp_accumulate_rs_avg_adamw_cast(const float* const* acc_slices,
     const bool vec = vec_a && vec_l && aligned(master, 16) && aligned(m, 16) &&
                      aligned(v, 16) && aligned(out_bf16, 8);
     cudaError_t e = launch_accum_rs_adamw_cast(acc, last, nd, S, scale, master, m, v, out_bf16,
-                                               adam_scalars(*hp), mean_op(nd, nd), vec,
+                                               c, mean_op(nd, nd), vec,
                                                static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "fused accumulate + step kernel launch");
     if (vec && compiled_nd(nd, {1, 2, 3, 4, 6, 8}))
@@ -730,6 +727,37 @@ int fsdp_accumulate_rs_avg_adamw_cast(const float* const* acc_slices,
     else
         note_kernel("accum_rs_adamw_cast_scalar");
     return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+int fsdp_rs_avg_adamw_cast(const void* const* grad_slices, int32_t grad_dtype, int32_t nd,
+                           int64_t S, float* master, float* m, float* v, uint16_t* out_bf16,
+                           const shardstep_adamw_t* hp, void* stream) {
+    return fused_step(grad_slices, grad_dtype, nd, nd, S, master, m, v, out_bf16, hp, stream);
+}
+
+int fsdp_accumulate_rs_avg_adamw_cast(const float* const* acc_slices,
+                                      const uint16_t* const* last_slices, int32_t nd, int64_t S,
+                                      float scale, float* master, float* m, float* v,
+                                      uint16_t* out_bf16, const shardstep_adamw_t* hp,
+                                      void* stream) {
+    if (hp == nullptr) return fail(SHARDSTEP_ERR_INVALID, "hp is NULL");
+    return accum_step(acc_slices, last_slices, nd, S, scale, master, m, v, out_bf16, hp, nullptr,
+                      stream);
+}
+
+int fsdp_state_accumulate_rs_avg_adamw_cast(const float* const* acc_slices,
+                                            const uint16_t* const* last_slices, int32_t nd,
+                                            int64_t S, float scale, float* master, float* m,
+                                            float* v, uint16_t* out_bf16,
+                                            const shardstep_adamw_state_t* state,
+                                            void* stream) {
+    if (state == nullptr) return fail(SHARDSTEP_ERR_INVALID, "state is NULL");
+    return accum_step(acc_slices, last_slices, nd, S, scale, master, m, v, out_bf16, nullptr,
+                      state, stream);
 }
 
 int fsdp_hybrid_rs_avg_adamw_cast(const void* const* grad_slices, int32_t grad_dtype, int32_t nd,

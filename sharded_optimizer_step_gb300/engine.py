@@ -17,7 +17,8 @@ import torch
 
 from . import (AdamW, AdamWState, fsdp_accumulate_rs_avg_adamw_cast, fsdp_ag_unpack,
                fsdp_hybrid_rs_avg_adamw_cast, fsdp_layout, fsdp_rs_avg_adamw_cast,
-               fsdp_state_rs_avg_adamw_cast, fsdp_views)
+               fsdp_state_accumulate_rs_avg_adamw_cast, fsdp_state_rs_avg_adamw_cast,
+               fsdp_views)
 
 
 def _numel(shape):
@@ -109,6 +110,17 @@ class RankShardOptimizer:
         self.state.advance(stream=stream)
         fsdp_state_rs_avg_adamw_cast(self.grad_in, self.master, self.m, self.v, self.params,
                                      self.state, shard_group=self.F, stream=stream)
+
+    def step_with_last_micro_batch_on_device(self, last, scale: float, stream=None):
+        """``step_with_last_micro_batch`` with the count advanced and the AdamW
+        scalars derived on the device (see ``step_on_device``): capturable in
+        a CUDA graph together with the accumulate launches.  Plain sharding
+        only; needs ``device_step_state`` first."""
+        if self.F != self.nd:
+            raise ValueError("the fused last-micro-batch step is for plain sharding")
+        self.state.advance(stream=stream)
+        fsdp_state_accumulate_rs_avg_adamw_cast(self.grad_in, last, scale, self.master, self.m,
+                                                self.v, self.params, self.state, stream=stream)
 
     def gather_unit(self, u, peer_shards, full, stream=None):
         """All-gather unit u inside the rank's shard group: ``peer_shards[q]``

@@ -176,6 +176,15 @@ def test_accumulate_step_rejects_bad_arguments_before_launch():
     assert call(acc, last, 8, S, st[0], st[0] + 8, st[2], st[3]) == _capi.ERR_INVALID
     assert call(acc[:7] + [acc[7] + 2], last, 8, S, *st) == _capi.ERR_INVALID  # misaligned fp32
     assert call(acc, last, 8, 0, *st) == _capi.OK                           # nothing to do
+    sp = [ctypes.c_void_p(a) for a in st]
+    assert L.fsdp_state_accumulate_rs_avg_adamw_cast(
+        _capi.ptr_array(acc), _capi.ptr_array(last), 8, S, ctypes.c_float(0.25), *sp, None,
+        None) == _capi.ERR_INVALID
+    assert "state is NULL" in L.shardstep_last_error().decode()
+    assert L.fsdp_state_accumulate_rs_avg_adamw_cast(
+        _capi.ptr_array(acc), _capi.ptr_array(last), 8, S, ctypes.c_float(0.25), *sp,
+        ctypes.c_void_p(A + 4), None) == _capi.ERR_INVALID
+    assert "misaligned" in L.shardstep_last_error().decode()
 
 
 def test_other_entry_points_reject_bad_arguments():

@@ -24,6 +24,7 @@ def _built():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     ss.build()
+    synth.build_dev()
     yield
 
 
@@ -150,3 +151,55 @@ def test_accumulate_step_names_its_kernel():
                                          *[t[1:] for t in st], HPC, 1)
     assert ss.last_kernel() == "accum_rs_adamw_cast_scalar"
     torch.cuda.synchronize()
+
+
+def test_accumulation_step_on_device_captured_in_a_cuda_graph():
+    """The accumulation step (M - 1 accumulate launches over the contributions,
+    then the last micro-batch inside the fused step on the device step
+    state) captured once in a CUDA graph and replayed over three steps
+    equals the host-scalar path run eagerly, bit for bit."""
+    from sharded_optimizer_step_gb300.engine import RankShardOptimizer
+    units = [[(300, 40), (40,)], [(97, 13), (5,)]]
+    nd, M = 8, 4
+    inv_m = float(np.float32(1.0 / M))
+    a = RankShardOptimizer(units, nd, 2, HPC, device=DEV, grad_dtype=torch.float32)
+    b = RankShardOptimizer(units, nd, 2, HPC, device=DEV, grad_dtype=torch.float32)
+    S = a.shard_total
+    synth.dev_fill(synth.normal_stream(5, (89, 1), 0.02), a.master)
+    b.master.copy_(a.master)
+    micro = [[torch.empty(S, dtype=torch.bfloat16, device=DEV) for _ in range(nd)]
+             for _ in range(M)]
+
+    def accumulate(opt):
+        for j in range(M - 1):
+            for q in range(nd):
+                ss.fsdp_grad_accumulate(micro[j][q], opt.grad_in[q], inv_m, j == 0)
+
+    b.device_step_state()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):           # warm-up, then undone
+        accumulate(b)
+        b.step_with_last_micro_batch_on_device(micro[M - 1], inv_m)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    b.master.copy_(a.master)
+    b.m.zero_()
+    b.v.zero_()
+    b.state.init(0)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        accumulate(b)
+        b.step_with_last_micro_batch_on_device(micro[M - 1], inv_m)
+    for t in range(1, 4):
+        for j in range(M):
+            for q in range(nd):
+                synth.dev_fill(synth.normal_stream(5, (89, 2, t, j, q), 1e-3), micro[j][q])
+        accumulate(a)
+        a.step_with_last_micro_batch(micro[M - 1], inv_m)
+        g.replay()
+        torch.cuda.synchronize()
+        for x, y in ((a.master, b.master), (a.m, b.m), (a.v, b.v)):
+            assert torch.equal(x.view(torch.int32), y.view(torch.int32)), t
+        assert torch.equal(a.params.view(torch.int16), b.params.view(torch.int16)), t
+    assert b.state.step() == 3
