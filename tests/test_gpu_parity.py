@@ -353,6 +353,46 @@ def test_copy_launches_of_one_call_keep_stream_order(dependent):
     assert_bits(host_bf16(seen_full), want, "full")
 
 
+def test_copy_launches_of_one_call_replay_from_a_cuda_graph():
+    """A pack of 150 bf16 tensors at mixed offsets (several launches of each
+    copy kernel, the later ones programmatic dependents) and the all-gather
+    of its shards at odd slot offsets, captured once in a CUDA graph and
+    replayed on fresh inputs: bit-exact against the oracle every time."""
+    nd = 4
+    rng = np.random.default_rng(9)
+    numels = [int(x) for x in rng.integers(1, 9000, size=149)] + [1 << 18]
+    shifts = [int(s) for s in rng.integers(0, 8, size=len(numels))]
+    srcs = [dev_bf16(np.zeros(n, np.uint16), sh) for n, sh in zip(numels, shifts)]
+    lay = oracle.layout(numels, nd)
+    S = lay.shard
+    flat = torch.empty(lay.padded, dtype=torch.bfloat16, device=DEV)
+    shards = [dev_bf16(np.zeros(S, np.uint16), r % 8) for r in range(nd)]
+    full = torch.empty(nd * S, dtype=torch.bfloat16, device=DEV)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):           # warm-up outside the capture
+        ss.fsdp_flat_pack(srcs, nd, flat=flat)
+        ss.fsdp_ag_unpack(shards, full)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        ss.fsdp_flat_pack(srcs, nd, flat=flat)
+        for r in range(nd):
+            shards[r].copy_(flat[r * S:(r + 1) * S])
+        ss.fsdp_ag_unpack(shards, full)
+    for it in range(3):
+        host = [synth.host_fill(synth.normal_stream(it, (93, k), 0.02), 0, n, "bf16")
+                for k, n in enumerate(numels)]
+        for s, h in zip(srcs, host):
+            s.copy_(torch.from_numpy(h.view(np.int16)).view(torch.bfloat16))
+        g.replay()
+        want, _ = oracle.flat_pack(host, nd)
+        torch.cuda.synchronize()
+        assert_bits(host_bf16(flat), want, f"flat, replay {it}")
+        assert_bits(host_bf16(full), want, f"full, replay {it}")
+
+
 def test_worked_example_on_gpu():
     tensors = [np.arange(1, 9, dtype=np.float32).reshape(4, 2) + 100 * (t + 1) for t in range(3)]
     flat = ss.fsdp_flat_pack([dev_f32(t.reshape(-1)).view(4, 2) for t in tensors], 2)
