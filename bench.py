@@ -83,9 +83,9 @@ def parse():
                     help="streaming kernels: TMA-staged where they measured faster (auto), "
                          "register-staged only, or TMA-staged wherever the arguments allow")
     ap.add_argument("--graph", action="store_true",
-                    help="default / hybrid lines: the step count and AdamW scalars on the "
-                         "device, the fused update and the all-gather replayed from CUDA "
-                         "graphs captured once")
+                    help="default / hybrid / accumulation lines: the step count and AdamW "
+                         "scalars on the device, the accumulate launches, the fused update "
+                         "and the all-gather replayed from CUDA graphs captured once")
     ap.add_argument("--no-dependent-launch", action="store_true",
                     help="launch every bucket of an all-reduce call, and every copy kernel "
                          "of a pack / all-gather call, as an ordinary launch")
@@ -1352,7 +1352,53 @@ def run_accum(args):
         if ev is not None:
             ev[3].record(stream)
 
+    graph_launches = 0
+    if args.graph:
+        if not fused_last:
+            raise SystemExit("--graph: the accumulation line with the fused last micro-batch")
+        # the step count on the device; the accumulate launches, the update
+        # (advance + fused launch) and the all-gather each captured once,
+        # after an eager warm-up
+        opt.device_step_state()
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            for j in range(n_acc):
+                ss.fsdp_grad_accumulate(micro[j], acc, inv_m, j == 0)
+            opt.step_with_last_micro_batch_on_device(last, inv_m)
+            opt.gather_unit(u, peers, full)
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        g_acc, g_update, g_gather = (torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(),
+                                     torch.cuda.CUDAGraph())
+        l0 = ss.launch_count()
+        with torch.cuda.graph(g_acc):
+            for j in range(n_acc):
+                ss.fsdp_grad_accumulate(micro[j], acc, inv_m, j == 0)
+        kernel_names["accumulate"] = ss.last_kernel()
+        with torch.cuda.graph(g_update):
+            opt.step_with_last_micro_batch_on_device(last, inv_m)
+        kernel_names["fused"] = ss.last_kernel()
+        with torch.cuda.graph(g_gather):
+            opt.gather_unit(u, peers, full)
+        graph_launches = ss.launch_count() - l0     # kernels per replayed step
+
+        def one_step(ev):                 # noqa: F811 -- the graph form of the step
+            if ev is not None:
+                ev[0].record(stream)
+            g_acc.replay()
+            if ev is not None:
+                ev[1].record(stream)
+            g_update.replay()
+            if ev is not None:
+                ev[2].record(stream)
+            g_gather.replay()
+            if ev is not None:
+                ev[3].record(stream)
+
     total_ms, events, clk, launches = _timed_loop(torch, stream, args, one_step, 4, world)
+    if args.graph:
+        launches = graph_launches * args.steps
     acc_ms, fused_ms, ag_ms = _avg_ms(events, 0, 1), _avg_ms(events, 1, 2), _avg_ms(events, 2, 3)
     ms = total_ms / args.steps
     all_bytes = allreduce_sum(world, step_bytes)
@@ -1379,7 +1425,7 @@ def run_accum(args):
         "data": "synthetic (seeded counter-based generator on the device; no data set or weights)",
         "config": {"workload": ACCUM_WORKLOAD + (f"_first{args.layers}layers" if args.layers
                                                  else ""),
-                   "tma_stages": _stages_name(args),
+                   "tma_stages": _stages_name(args), "graph": bool(args.graph),
                    "model_shape": f"Llama-style 1B, {len(w.units)} FSDP units",
                    "psi": w.psi, "nd": nd, "micro_batches": M, "rank": r, "shard_elements": S,
                    "grad_dtype": "bf16 micro-batch gradients, fp32 accumulators",
