@@ -97,7 +97,8 @@ def test_accumulate_step_matches_oracle(nd, S, shift):
 
 
 @pytest.mark.parametrize("nd,S,M", [(8, 152 * 128 * 6 * 2 + 7, 4), (8, 1 << 18, 2),
-                                    (4, 70001, 5), (6, 65537, 3)])
+                                    (4, 70001, 5), (6, 65537, 3), (7, 40003, 2),
+                                    (64, 4099, 2), (33, 1031, 3)])
 def test_accumulate_step_multi_wave(nd, S, M):
     _check(nd, S, M, step=7, shift=0)
 
