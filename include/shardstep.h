@@ -205,19 +205,23 @@ int fsdp_rs_avg_adamw_cast(const void* const* grad_slices, int32_t grad_dtype, i
  *                    accumulator (micro-batches 0..M-2) + r*S, S elements.
  *   last_slices[nd]  host array of device pointers: rank q's bf16 gradient
  *                    of the last micro-batch + r*S, S elements.
+ *   shard_group      F: nd for plain sharding (rank-order sum), else the
+ *                    sharding factor of hybrid sharding, summed in the order
+ *                    of fsdp_hybrid_rs_avg_adamw_cast (F must divide nd).
  *   scale            the fp32 value of 1/M, as given to fsdp_grad_accumulate.
  *   nd, S, master, m, v, out_bf16, hp: as in fsdp_rs_avg_adamw_cast.
  * No input slice may overlap an output; the outputs must not overlap one
  * another.  Any alignment is accepted; accumulator slices and state 16-byte
  * aligned with bf16 slices and out_bf16 8-byte aligned take the vector
  * kernel (4 elements per access), anything else one element per access.
- * Errors: INVALID (null pointer, S < 0, step < 1, overlap), CAPACITY
- * (nd > SHARDSTEP_MAX_ND), CUDA (launch refused). */
+ * Errors: INVALID (null pointer, S < 0, step < 1, overlap, a shard_group
+ * that does not divide nd), CAPACITY (nd > SHARDSTEP_MAX_ND), CUDA (launch
+ * refused). */
 int fsdp_accumulate_rs_avg_adamw_cast(const float* const* acc_slices,
-                                      const uint16_t* const* last_slices, int32_t nd, int64_t S,
-                                      float scale, float* master, float* m, float* v,
-                                      uint16_t* out_bf16, const shardstep_adamw_t* hp,
-                                      void* stream);
+                                      const uint16_t* const* last_slices, int32_t nd,
+                                      int32_t shard_group, int64_t S, float scale, float* master,
+                                      float* m, float* v, uint16_t* out_bf16,
+                                      const shardstep_adamw_t* hp, void* stream);
 
 /* fsdp_hybrid_rs_avg_adamw_cast -- device, one kernel pass.
  * Hybrid sharding with sharding factor F = shard_group ([P2] section 2,
@@ -307,8 +311,9 @@ int fsdp_state_rs_avg_adamw_cast(const void* const* grad_slices, int32_t grad_dt
  * state. */
 int fsdp_state_accumulate_rs_avg_adamw_cast(const float* const* acc_slices,
                                             const uint16_t* const* last_slices, int32_t nd,
-                                            int64_t S, float scale, float* master, float* m,
-                                            float* v, uint16_t* out_bf16,
+                                            int32_t shard_group, int64_t S, float scale,
+                                            float* master, float* m, float* v,
+                                            uint16_t* out_bf16,
                                             const shardstep_adamw_state_t* state,
                                             void* stream);
 

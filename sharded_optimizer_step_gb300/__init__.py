@@ -175,35 +175,42 @@ def fsdp_rs_avg_adamw_cast(grad_slices, master, m, v, out_bf16, hp: AdamW, step:
 
 
 def fsdp_accumulate_rs_avg_adamw_cast(acc_slices, last_slices, scale: float, master, m, v,
-                                      out_bf16, hp: AdamW, step: int, stream=None):
+                                      out_bf16, hp: AdamW, step: int,
+                                      shard_group: int | None = None, stream=None):
     """The last micro-batch accumulated and the shard stepped in one pass:
     rank q's contribution is ``acc_slices[q] + last_slices[q] * scale`` (fp32
     accumulators of micro-batches 0..M-2, bf16 gradients of the last one,
-    ``scale`` = 1/M), then the step of ``fsdp_rs_avg_adamw_cast``.  The
-    accumulators are read, not written."""
+    ``scale`` = 1/M), then the step of ``fsdp_rs_avg_adamw_cast`` (of the
+    hybrid step with ``shard_group`` = F).  The accumulators are read, not
+    written."""
     S = _accum_args(acc_slices, last_slices, master, m, v, out_bf16)
     hpc = hp.at_step(step)
     _capi.check("fsdp_accumulate_rs_avg_adamw_cast",
                 _capi.lib().fsdp_accumulate_rs_avg_adamw_cast(
-                    *_accum_ptrs(acc_slices, last_slices, S, scale, master, m, v, out_bf16),
+                    *_accum_ptrs(acc_slices, last_slices, shard_group, S, scale, master, m, v,
+                                 out_bf16),
                     ctypes.byref(hpc), _stream(stream, master.device)))
 
 
 def fsdp_state_accumulate_rs_avg_adamw_cast(acc_slices, last_slices, scale: float, master, m,
-                                            v, out_bf16, state: AdamWState, stream=None):
+                                            v, out_bf16, state: AdamWState,
+                                            shard_group: int | None = None, stream=None):
     """``fsdp_accumulate_rs_avg_adamw_cast`` with the AdamW scalars read on the
     device from ``state`` (at a step >= 1): CUDA-graph capturable."""
     S = _accum_args(acc_slices, last_slices, master, m, v, out_bf16)
     _need_cuda(state.buf)
     _capi.check("fsdp_state_accumulate_rs_avg_adamw_cast",
                 _capi.lib().fsdp_state_accumulate_rs_avg_adamw_cast(
-                    *_accum_ptrs(acc_slices, last_slices, S, scale, master, m, v, out_bf16),
+                    *_accum_ptrs(acc_slices, last_slices, shard_group, S, scale, master, m, v,
+                                 out_bf16),
                     ctypes.c_void_p(state.buf.data_ptr()), _stream(stream, master.device)))
 
 
-def _accum_ptrs(acc_slices, last_slices, S, scale, master, m, v, out_bf16):
+def _accum_ptrs(acc_slices, last_slices, shard_group, S, scale, master, m, v, out_bf16):
+    nd = len(acc_slices)
     return (_capi.ptr_array([a.data_ptr() for a in acc_slices]),
-            _capi.ptr_array([g.data_ptr() for g in last_slices]), len(acc_slices), S,
+            _capi.ptr_array([g.data_ptr() for g in last_slices]), nd,
+            int(shard_group) if shard_group else nd, S,
             ctypes.c_float(scale), ctypes.c_void_p(master.data_ptr()),
             ctypes.c_void_p(m.data_ptr()), ctypes.c_void_p(v.data_ptr()),
             ctypes.c_void_p(out_bf16.data_ptr()))

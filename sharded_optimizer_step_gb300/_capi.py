@@ -66,10 +66,11 @@ SIGNATURES = {
                                        ctypes.POINTER(AdamWHP), c_vp]),
     "fsdp_hybrid_rs_avg_adamw_cast": (c_i32, [P_vp, c_i32, c_i32, c_i32, c_i64, c_vp, c_vp, c_vp,
                                               c_vp, ctypes.POINTER(AdamWHP), c_vp]),
-    "fsdp_accumulate_rs_avg_adamw_cast": (c_i32, [P_vp, P_vp, c_i32, c_i64, c_f32, c_vp, c_vp,
-                                                  c_vp, c_vp, ctypes.POINTER(AdamWHP), c_vp]),
-    "fsdp_state_accumulate_rs_avg_adamw_cast": (c_i32, [P_vp, P_vp, c_i32, c_i64, c_f32, c_vp,
-                                                        c_vp, c_vp, c_vp, c_vp, c_vp]),
+    "fsdp_accumulate_rs_avg_adamw_cast": (c_i32, [P_vp, P_vp, c_i32, c_i32, c_i64, c_f32, c_vp,
+                                                  c_vp, c_vp, c_vp, ctypes.POINTER(AdamWHP),
+                                                  c_vp]),
+    "fsdp_state_accumulate_rs_avg_adamw_cast": (c_i32, [P_vp, P_vp, c_i32, c_i32, c_i64, c_f32,
+                                                        c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
     "fsdp_grad_unscale_check": (c_i32, [P_vp, c_i32, c_i32, c_i32, c_i64, c_vp, c_vp, c_vp]),
     "fsdp_scaled_rs_avg_adamw_cast": (c_i32, [P_vp, c_i32, c_i32, c_i32, c_i64, c_vp, c_vp, c_vp,
                                               c_vp, ctypes.POINTER(AdamWHP), c_vp, c_vp, c_vp]),

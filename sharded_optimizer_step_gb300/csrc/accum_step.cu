@@ -7,8 +7,9 @@
 // accumulator and a write of the accumulator (10 B) before the fused step
 // reads the accumulator again (4 B).  This kernel takes both at once: slice
 // q's contribution is acc_q + fl(g_q * scale), computed in registers exactly
-// as the accumulation would have stored it, then summed in rank order,
-// averaged, AdamW-updated and cast like the plain fused step.  The
+// as the accumulation would have stored it, then summed in rank order (in
+// groups of F ranks under hybrid sharding), averaged, AdamW-updated and cast
+// like the plain fused step.  The
 // accumulators are only read.  Per shard element it moves 6 * N_d + 26 bytes
 // where the two passes move 14 * N_d + 26 (74 against 138 at N_d = 8).
 //
@@ -37,13 +38,17 @@ constexpr int acc_min_blocks() {
     return ND >= 6 || ND < 0 || ND == kAccRuntimeND ? 6 : 8;
 }
 
-// Slice contributions at 4 consecutive elements, summed in rank order.
-template <int ND>
+// Slice contributions at 4 consecutive elements, summed in rank order
+// (GROUPED: in the order GroupSum fixes for hybrid sharding, groups of
+// `group` ranks first; the plain sum keeps the 8-slice kernel unspilled).
+template <int ND, bool GROUPED>
 __device__ __forceinline__ void accum_reduce4(const PtrTable& acc, const PtrTable& last,
-                                              int nd, float scale, int64_t i, float* g) {
+                                              int nd, int group, float scale, int64_t i,
+                                              float* g) {
     constexpr int B = ND > 0 ? ND : (ND < 0 ? -ND : 4);
     constexpr bool kGuard = ND <= 0;
     float s[4];
+    GroupSum<4> grouped;
     for (int q0 = 0; q0 < nd; q0 += B) {
         uint4 a[B];
         uint2 b[B];
@@ -62,30 +67,43 @@ __device__ __forceinline__ void accum_reduce4(const PtrTable& acc, const PtrTabl
                 const float f[4] = {bf16_lo(b[u].x), bf16_hi(b[u].x), bf16_lo(b[u].y),
                                     bf16_hi(b[u].y)};
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    t[k] = __fadd_rn(t[k], __fmul_rn(f[k], scale));
-                    s[k] = q0 + u == 0 ? t[k] : __fadd_rn(s[k], t[k]);
+                for (int k = 0; k < 4; ++k) t[k] = __fadd_rn(t[k], __fmul_rn(f[k], scale));
+                if constexpr (GROUPED) {
+                    if (q0 + u == 0) grouped.first(t);
+                    else grouped.add(t, group);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) s[k] = q0 + u == 0 ? t[k] : __fadd_rn(s[k], t[k]);
                 }
             }
         }
     }
+    if constexpr (GROUPED) grouped.result(s);
 #pragma unroll
     for (int k = 0; k < 4; ++k) g[k] = s[k];
 }
 
+template <bool GROUPED>
 __device__ __forceinline__ void accum_step_elem(const PtrTable& acc, const PtrTable& last,
                                                 int nd, float scale, int64_t j,
                                                 float* __restrict__ P, float* __restrict__ M,
                                                 float* __restrict__ V,
                                                 uint16_t* __restrict__ out,
                                                 const AdamScalars& c, const MeanOp& mo) {
+    GroupSum<1> grouped;
     float s = 0.0f;
     for (int q = 0; q < nd; ++q) {
         const float a = static_cast<const float*>(acc.p[q])[j];
         const float g = bf16_to_f32(static_cast<const uint16_t*>(last.p[q])[j]);
         const float t = __fadd_rn(a, __fmul_rn(g, scale));
-        s = q == 0 ? t : __fadd_rn(s, t);
+        if constexpr (GROUPED) {
+            if (q == 0) grouped.first(&t);
+            else grouped.add(&t, mo.group);
+        } else {
+            s = q == 0 ? t : __fadd_rn(s, t);
+        }
     }
+    if constexpr (GROUPED) grouped.result(&s);
     float p = P[j], m = M[j], v = V[j];
     adamw_elem(mean_of(s, mo), p, m, v, c);
     P[j] = p;
@@ -96,7 +114,7 @@ __device__ __forceinline__ void accum_step_elem(const PtrTable& acc, const PtrTa
 
 // Accumulator slices and state 16-byte aligned, bf16 slices and the output
 // 8-byte aligned: 4 elements per thread, the (< 4 element) tail by block 0.
-template <int ND>
+template <int ND, bool GROUPED>
 __global__ void __launch_bounds__(kAccThreads, acc_min_blocks<ND>())
     accum_rs_adamw_cast_vec4(PtrTable acc, PtrTable last, int nd, int64_t S, float scale,
                              float* __restrict__ P, float* __restrict__ M,
@@ -111,7 +129,7 @@ __global__ void __launch_bounds__(kAccThreads, acc_min_blocks<ND>())
         const uint4 m0 = ldcs16(M + 4 * i);
         const uint4 v0 = ldcs16(V + 4 * i);
         float g[4];
-        accum_reduce4<ND>(acc, last, nd, scale, i, g);
+        accum_reduce4<ND, GROUPED>(acc, last, nd, mo.group, scale, i, g);
         float p[4], m[4], v[4];
         unpack4f(p0, p);
         unpack4f(m0, m);
@@ -124,7 +142,8 @@ __global__ void __launch_bounds__(kAccThreads, acc_min_blocks<ND>())
         stcs8(out + 4 * i, make_uint2(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3])));
     }
     if (blockIdx.x == 0 && threadIdx.x < (S & 3))
-        accum_step_elem(acc, last, nd, scale, (nvec << 2) + threadIdx.x, P, M, V, out, c, mo);
+        accum_step_elem<GROUPED>(acc, last, nd, scale, (nvec << 2) + threadIdx.x, P, M, V, out,
+                                 c, mo);
 }
 
 // Any alignment: one element per thread per iteration.
@@ -137,18 +156,18 @@ __global__ void __launch_bounds__(kThreads)
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
     for (int64_t j = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; j < S;
          j += stride)
-        accum_step_elem(acc, last, nd, scale, j, P, M, V, out, c, mo);
+        accum_step_elem<true>(acc, last, nd, scale, j, P, M, V, out, c, mo);
 }
 
-template <int ND>
+template <int ND, bool GROUPED = false>
 cudaError_t go_accum(const PtrTable& acc, const PtrTable& last, int nd, int64_t S, float scale,
                      float* P, float* M, float* V, uint16_t* out, const AdamScalars& c,
                      const MeanOp& mo, cudaStream_t s) {
     const int64_t blocks = ((S >> 2) + kAccThreads - 1) / kAccThreads;
     const int64_t cap = (int64_t{1} << 31) - 1;
     const unsigned grid = static_cast<unsigned>(blocks < 1 ? 1 : (blocks > cap ? cap : blocks));
-    accum_rs_adamw_cast_vec4<ND><<<grid, kAccThreads, 0, s>>>(acc, last, nd, S, scale, P, M, V,
-                                                               out, c, mo);
+    accum_rs_adamw_cast_vec4<ND, GROUPED><<<grid, kAccThreads, 0, s>>>(acc, last, nd, S, scale,
+                                                                        P, M, V, out, c, mo);
     note_launch();
     return cudaGetLastError();
 }
@@ -159,6 +178,9 @@ cudaError_t launch_accum_rs_adamw_cast(const PtrTable& acc, const PtrTable& last
                                        int64_t S, float scale, float* master, float* m,
                                        float* v, uint16_t* out, const AdamScalars& c,
                                        const MeanOp& mo, bool vec, cudaStream_t stream) {
+    if (vec && mo.group != nd)  // hybrid sharding: grouped order, any N_d
+        return go_accum<kAccRuntimeND, true>(acc, last, nd, S, scale, master, m, v, out, c, mo,
+                                             stream);
     if (vec) {
         switch (nd) {
             case 1: return go_accum<1>(acc, last, nd, S, scale, master, m, v, out, c, mo, stream);

@@ -691,12 +691,13 @@ int fused_step(const void* const* grad_slices, int32_t grad_dtype, int32_t nd, i
 // The last micro-batch accumulated inside the fused step; the AdamW scalars
 // from `hp` on the host or from a device-resident step `state`.
 int accum_step(const float* const* acc_slices, const uint16_t* const* last_slices, int32_t nd,
-               int64_t S, float scale, float* master, float* m, float* v, uint16_t* out_bf16,
-               const shardstep_adamw_t* hp, const shardstep_adamw_state_t* state,
-               void* stream) {
+               int32_t shard_group, int64_t S, float scale, float* master, float* m, float* v,
+               uint16_t* out_bf16, const shardstep_adamw_t* hp,
+               const shardstep_adamw_state_t* state, void* stream) {
     if (nd < 1) return fail(SHARDSTEP_ERR_INVALID, "nd must be >= 1 (got %d)", nd);
     if (nd > SHARDSTEP_MAX_ND)
         return fail(SHARDSTEP_ERR_CAPACITY, "nd %d > %d", nd, SHARDSTEP_MAX_ND);
+    if (int rc = check_shard_group(nd, shard_group); rc != SHARDSTEP_OK) return rc;
     if (S < 0) return fail(SHARDSTEP_ERR_INVALID, "S must be >= 0");
     AdamScalars c{};
     if (int rc = adam_source(hp, state, &c); rc != SHARDSTEP_OK) return rc;
@@ -715,10 +716,13 @@ int accum_step(const float* const* acc_slices, const uint16_t* const* last_slice
     const bool vec = vec_a && vec_l && aligned(master, 16) && aligned(m, 16) &&
                      aligned(v, 16) && aligned(out_bf16, 8);
     cudaError_t e = launch_accum_rs_adamw_cast(acc, last, nd, S, scale, master, m, v, out_bf16,
-                                               c, mean_op(nd, nd), vec,
+                                               c, mean_op(nd, shard_group), vec,
                                                static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "fused accumulate + step kernel launch");
-    if (vec && compiled_nd(nd, {1, 2, 3, 4, 6, 8}))
+    if (vec && shard_group != nd)
+        note_kernel("accum_rs_adamw_cast_vec4<any N_d = %d, groups of %d> (register-staged)", nd,
+                    shard_group);
+    else if (vec && compiled_nd(nd, {1, 2, 3, 4, 6, 8}))
         note_kernel("accum_rs_adamw_cast_vec4<%d> (register-staged)", nd);
     else if (vec && (nd == 5 || nd == 7))
         note_kernel("accum_rs_adamw_cast_vec4<up to 8: %d> (register-staged)", nd);
@@ -740,24 +744,25 @@ int fsdp_rs_avg_adamw_cast(const void* const* grad_slices, int32_t grad_dtype, i
 }
 
 int fsdp_accumulate_rs_avg_adamw_cast(const float* const* acc_slices,
-                                      const uint16_t* const* last_slices, int32_t nd, int64_t S,
-                                      float scale, float* master, float* m, float* v,
-                                      uint16_t* out_bf16, const shardstep_adamw_t* hp,
-                                      void* stream) {
+                                      const uint16_t* const* last_slices, int32_t nd,
+                                      int32_t shard_group, int64_t S, float scale, float* master,
+                                      float* m, float* v, uint16_t* out_bf16,
+                                      const shardstep_adamw_t* hp, void* stream) {
     if (hp == nullptr) return fail(SHARDSTEP_ERR_INVALID, "hp is NULL");
-    return accum_step(acc_slices, last_slices, nd, S, scale, master, m, v, out_bf16, hp, nullptr,
-                      stream);
+    return accum_step(acc_slices, last_slices, nd, shard_group, S, scale, master, m, v, out_bf16,
+                      hp, nullptr, stream);
 }
 
 int fsdp_state_accumulate_rs_avg_adamw_cast(const float* const* acc_slices,
                                             const uint16_t* const* last_slices, int32_t nd,
-                                            int64_t S, float scale, float* master, float* m,
-                                            float* v, uint16_t* out_bf16,
+                                            int32_t shard_group, int64_t S, float scale,
+                                            float* master, float* m, float* v,
+                                            uint16_t* out_bf16,
                                             const shardstep_adamw_state_t* state,
                                             void* stream) {
     if (state == nullptr) return fail(SHARDSTEP_ERR_INVALID, "state is NULL");
-    return accum_step(acc_slices, last_slices, nd, S, scale, master, m, v, out_bf16, nullptr,
-                      state, stream);
+    return accum_step(acc_slices, last_slices, nd, shard_group, S, scale, master, m, v, out_bf16,
+                      nullptr, state, stream);
 }
 
 int fsdp_hybrid_rs_avg_adamw_cast(const void* const* grad_slices, int32_t grad_dtype, int32_t nd,

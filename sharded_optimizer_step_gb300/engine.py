@@ -78,12 +78,11 @@ class RankShardOptimizer:
         micro-batches 0..M-2 and ``last[q]`` is contribution q's bf16
         gradient of the last micro-batch (laid out like ``grad_in[q]``):
         the last accumulation (``scale`` = 1/M) runs inside the fused launch
-        and ``grad_in`` is left as it was.  Plain sharding only."""
-        if self.F != self.nd:
-            raise ValueError("the fused last-micro-batch step is for plain sharding")
+        and ``grad_in`` is left as it was."""
         self.t += 1
         fsdp_accumulate_rs_avg_adamw_cast(self.grad_in, last, scale, self.master, self.m, self.v,
-                                          self.params, self.hp, self.t, stream=stream)
+                                          self.params, self.hp, self.t, shard_group=self.F,
+                                          stream=stream)
 
     def begin_step(self):
         """Advance the step count for an update issued piece by piece with
@@ -114,13 +113,12 @@ class RankShardOptimizer:
     def step_with_last_micro_batch_on_device(self, last, scale: float, stream=None):
         """``step_with_last_micro_batch`` with the count advanced and the AdamW
         scalars derived on the device (see ``step_on_device``): capturable in
-        a CUDA graph together with the accumulate launches.  Plain sharding
-        only; needs ``device_step_state`` first."""
-        if self.F != self.nd:
-            raise ValueError("the fused last-micro-batch step is for plain sharding")
+        a CUDA graph together with the accumulate launches.  Needs
+        ``device_step_state`` first."""
         self.state.advance(stream=stream)
         fsdp_state_accumulate_rs_avg_adamw_cast(self.grad_in, last, scale, self.master, self.m,
-                                                self.v, self.params, self.state, stream=stream)
+                                                self.v, self.params, self.state,
+                                                shard_group=self.F, stream=stream)
 
     def gather_unit(self, u, peer_shards, full, stream=None):
         """All-gather unit u inside the rank's shard group: ``peer_shards[q]``

@@ -161,7 +161,7 @@ def test_accumulate_step_rejects_bad_arguments_before_launch():
     def call(acc, last, nd, S, *state, step=1):
         hp = ss.AdamW().at_step(step)
         return L.fsdp_accumulate_rs_avg_adamw_cast(
-            _capi.ptr_array(acc), _capi.ptr_array(last), nd, S, ctypes.c_float(0.25),
+            _capi.ptr_array(acc), _capi.ptr_array(last), nd, nd, S, ctypes.c_float(0.25),
             *[ctypes.c_void_p(a) for a in state], ctypes.byref(hp), None)
 
     assert call(acc, last, 0, S, *st) == _capi.ERR_INVALID
@@ -178,13 +178,18 @@ def test_accumulate_step_rejects_bad_arguments_before_launch():
     assert call(acc, last, 8, 0, *st) == _capi.OK                           # nothing to do
     sp = [ctypes.c_void_p(a) for a in st]
     assert L.fsdp_state_accumulate_rs_avg_adamw_cast(
-        _capi.ptr_array(acc), _capi.ptr_array(last), 8, S, ctypes.c_float(0.25), *sp, None,
+        _capi.ptr_array(acc), _capi.ptr_array(last), 8, 8, S, ctypes.c_float(0.25), *sp, None,
         None) == _capi.ERR_INVALID
     assert "state is NULL" in L.shardstep_last_error().decode()
     assert L.fsdp_state_accumulate_rs_avg_adamw_cast(
-        _capi.ptr_array(acc), _capi.ptr_array(last), 8, S, ctypes.c_float(0.25), *sp,
+        _capi.ptr_array(acc), _capi.ptr_array(last), 8, 8, S, ctypes.c_float(0.25), *sp,
         ctypes.c_void_p(A + 4), None) == _capi.ERR_INVALID
     assert "misaligned" in L.shardstep_last_error().decode()
+    hp = ss.AdamW().at_step(1)
+    assert L.fsdp_accumulate_rs_avg_adamw_cast(
+        _capi.ptr_array(acc), _capi.ptr_array(last), 8, 3, S, ctypes.c_float(0.25), *sp,
+        ctypes.byref(hp), None) == _capi.ERR_INVALID       # 3 does not divide 8
+    assert "sharding factor" in L.shardstep_last_error().decode()
 
 
 def test_other_entry_points_reject_bad_arguments():

@@ -62,8 +62,8 @@ def _state(seed, S):
     return p, m, v
 
 
-def _check(nd, S, M, step, shift):
-    seed = 31 * nd + S + M
+def _check(nd, S, M, step, shift, F=None):
+    seed = 31 * nd + S + M + (F or 0)
     micro = _micro(seed, nd, M, S)
     scale = np.float32(1.0 / M)
     p, m, v = _state(seed, S)
@@ -76,9 +76,13 @@ def _check(nd, S, M, step, shift):
             ss.fsdp_grad_accumulate(dev(micro[q][j]), acc, float(scale), j == 0)
         accs.append(acc)
     last = [dev(micro[q][M - 1], shift if q % 3 == 1 else 0) for q in range(nd)]
-    ss.fsdp_accumulate_rs_avg_adamw_cast(accs, last, float(scale), dp, dm, dv, out, HPC, step)
+    ss.fsdp_accumulate_rs_avg_adamw_cast(accs, last, float(scale), dp, dm, dv, out, HPC, step,
+                                         shard_group=F)
     contribs = [oracle.grad_accumulate(micro[q], scale) for q in range(nd)]
-    wp, wm, wv, wo = oracle.fsdp_shard_step(contribs, 0, S, p, m, v, HP, step)
+    if F is None or F == nd:
+        wp, wm, wv, wo = oracle.fsdp_shard_step(contribs, 0, S, p, m, v, HP, step)
+    else:
+        wp, wm, wv, wo = oracle.hybrid_shard_step(contribs, F, 0, S, p, m, v, HP, step)
     torch.cuda.synchronize()
     for name, got, want in (("master", host(dp), wp), ("m", host(dm), wm), ("v", host(dv), wv)):
         assert_f32(got, want, name)
@@ -94,6 +98,14 @@ def _check(nd, S, M, step, shift):
 @pytest.mark.parametrize("shift", [0, 1])
 def test_accumulate_step_matches_oracle(nd, S, shift):
     _check(nd, S, M=3, step=1 + nd % 3, shift=shift)
+
+
+@pytest.mark.parametrize("nd,F", [(16, 8), (8, 4), (6, 3), (8, 2), (4, 1), (9, 3)])
+@pytest.mark.parametrize("S", [13, 4099, 70001])
+def test_hybrid_accumulate_step_matches_oracle(nd, F, S):
+    """Hybrid sharding (sharding factor F): the contributions summed inside
+    each group of F ranks, then across the groups, as the hybrid step does."""
+    _check(nd, S, M=3, step=2, shift=0, F=F)
 
 
 @pytest.mark.parametrize("nd,S,M", [(8, 152 * 128 * 6 * 2 + 7, 4), (8, 1 << 18, 2),
@@ -144,6 +156,9 @@ def test_accumulate_step_names_its_kernel():
     assert ss.last_kernel() == "accum_rs_adamw_cast_vec4<6> (register-staged)"
     ss.fsdp_accumulate_rs_avg_adamw_cast(accs[:5], last[:5], 0.5, *st, HPC, 1)
     assert ss.last_kernel() == "accum_rs_adamw_cast_vec4<up to 8: 5> (register-staged)"
+    ss.fsdp_accumulate_rs_avg_adamw_cast(accs, last, 0.5, *st, HPC, 1, shard_group=4)
+    assert ss.last_kernel() == ("accum_rs_adamw_cast_vec4<any N_d = 8, groups of 4> "
+                                "(register-staged)")
     more = accs + accs[:1]
     ss.fsdp_accumulate_rs_avg_adamw_cast(more, last + last[:1], 0.5, *st, HPC, 1)
     assert ss.last_kernel() == "accum_rs_adamw_cast_vec4<any N_d = 9> (register-staged)"
