@@ -48,7 +48,7 @@ against facts the pages or mathematics fix (worked example, closed forms,
 library routines, brute force).  No function is left unpinned.
 """
 from .flat import (Layout, layout, flat_pack, shard_of, sharded_views, ag_unpack,
-                   unpack_views)
+                   unpack_views, element_source, rank_view_sources)
 from .numerics import (AdamWConfig, adamw_scalars, adamw, bf16_to_f32, f32_to_bf16,
                        grad_accumulate, rs_avg, fsdp_shard_step, hybrid_rs_avg,
                        hybrid_shard_step)
@@ -63,6 +63,7 @@ from .ledger import (state_bytes_per_gpu, comm_bytes_per_gpu, hybrid_state_bytes
 
 __all__ = [
     "Layout", "layout", "flat_pack", "shard_of", "sharded_views", "ag_unpack", "unpack_views",
+    "element_source", "rank_view_sources",
     "AdamWConfig", "adamw_scalars", "adamw", "bf16_to_f32", "f32_to_bf16", "grad_accumulate",
     "rs_avg", "fsdp_shard_step", "hybrid_rs_avg", "hybrid_shard_step", "bucket_plan",
     "bucket_allreduce_avg", "ddp_step", "state_bytes_per_gpu", "comm_bytes_per_gpu",

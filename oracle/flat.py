@@ -106,3 +106,42 @@ def unpack_views(full, lay: Layout, shapes=None):
             v = v.reshape(shapes[t])
         views.append(v)
     return views
+
+
+def element_source(lay: Layout, flat_idx):
+    """Where FlatParameter element f comes from: tensor t = the one whose range
+    [off_t, off_t + n_t) holds f, at row-major index k = f - off_t; t = -1
+    (and k = 0) for the zero padding [T, P).  The inverse of flat_pack,
+    element by element."""
+    flat_idx = np.asarray(flat_idx, dtype=np.int64)
+    t = np.full(flat_idx.size, -1, dtype=np.int64)
+    k = np.zeros(flat_idx.size, dtype=np.int64)
+    for ti, (off, n) in enumerate(zip(lay.offsets, lay.numels)):
+        sel = (flat_idx >= off) & (flat_idx < off + n)
+        t[sel] = ti
+        k[sel] = flat_idx[sel] - off
+    return t, k
+
+
+def rank_view_sources(layouts, r: int, idx):
+    """A rank that keeps its shard of every unit back to back (unit order):
+    for position i of that concatenation, the unit u, and the tensor t and
+    row-major index k it comes from (t = -1 in a unit's padding).  Unit u's
+    part is shard_of(flat_u, r), i.e. flat_u[r*S_u + j] for j < S_u."""
+    idx = np.asarray(idx, dtype=np.int64)
+    u_out = np.full(idx.size, -1, dtype=np.int64)
+    t_out = np.full(idx.size, -1, dtype=np.int64)
+    k_out = np.zeros(idx.size, dtype=np.int64)
+    start = 0
+    for u, lay in enumerate(layouts):
+        sel = np.nonzero((idx >= start) & (idx < start + lay.shard))[0]
+        if sel.size:
+            t, k = element_source(lay, r * lay.shard + (idx[sel] - start))
+            u_out[sel] = u
+            t_out[sel] = t
+            k_out[sel] = k
+        start += lay.shard
+    if (u_out < 0).any():
+        raise IndexError("position past the rank's shards")
+    return u_out, t_out, k_out
+

@@ -167,3 +167,24 @@ def test_comm_ledger_closed_forms():
     assert b("centralised_root") / 2 == 2 * (nd - 1) * psi
     with pytest.raises(ValueError):
         b("broadcast")
+
+
+def test_ddp_step_updates_with_the_bf16_rounded_mean():
+    """The all-reduce keeps bf16, so the replicated AdamW sees the mean rounded
+    to bf16, not the fp32 mean.  Two ranks with gradients 1 and 2^-8: the
+    fp32 mean 0.5 + 2^-9 lies half a bf16 ulp above 0.5, so it rounds (ties
+    to even) to exactly 0.5.  With beta1 = beta2 = 0, eps = 1, lr = 1, no
+    decay, p = 0 at step 1: m = g, v = g^2, bc1 = bc2 = 1 and the update is
+    g / (|g| + 1), so p = -(0.5 / 1.5) = -fl32(1/3) for the rounded mean,
+    while the fp32 mean would give -fl32(0.501953125 / 1.501953125)."""
+    from oracle.numerics import AdamWConfig
+    one, tiny = 0x3F80, 0x3B80                         # bf16 bits of 1.0 and 2^-8
+    assert oracle.bf16_to_f32(np.array([tiny], np.uint16))[0] == np.float32(2.0 ** -8)
+    hp = AdamWConfig(lr=1.0, beta1=0.0, beta2=0.0, eps=1.0, weight_decay=0.0)
+    z = np.zeros(1, np.float32)
+    avg, p, m, v, pb = oracle.ddp_step([np.array([one], np.uint16), np.array([tiny], np.uint16)],
+                                       [0, 1], z, z, z, hp, 1)
+    assert avg[0] == 0x3F00                            # bf16 0.5
+    assert m[0] == np.float32(0.5) and v[0] == np.float32(0.25)
+    assert p[0] == -np.float32(1.0 / 3.0)
+    assert p[0] != -np.float32(0.501953125 / 1.501953125)

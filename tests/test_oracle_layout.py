@@ -132,3 +132,55 @@ def test_layout_rejects_bad_arguments():
         oracle.layout([1, 2], 0)
     with pytest.raises(ValueError):
         oracle.layout([-1], 2)
+
+
+# ---------------------------------------- element sources (the inverse of pack)
+
+def _tagged(numels, u=0):
+    # tensor t's element k holds the value u * 10^6 + (t + 1) * 10^4 + k (exact in
+    # float64), so every element of a packed buffer names its source
+    return [(u * 10 ** 6 + (t + 1) * 10 ** 4 + np.arange(n)).astype(np.float64)
+            for t, n in enumerate(numels)]
+
+
+def test_element_source_inverts_flat_pack_by_brute_force():
+    for nd in range(1, 6):
+        for k in range(0, 4):
+            for numels in itertools.product(range(0, 6), repeat=k):
+                flat, lay = oracle.flat_pack(_tagged(numels), nd) if k else \
+                    (np.zeros(0), oracle.layout([], nd))
+                t, kk = oracle.element_source(lay, np.arange(lay.padded))
+                for f in range(lay.padded):
+                    if t[f] < 0:
+                        assert f >= lay.total and flat[f] == 0
+                    else:
+                        assert flat[f] == (t[f] + 1) * 10 ** 4 + kk[f]
+
+
+def test_element_source_on_the_worked_example():
+    # [W1(8) | W2(8) | W3(8)] on two ranks: element 12 (rank 1's first) is W2
+    # row 2 column 0, i.e. W2's element 4; element 23 is W3's last
+    lay = oracle.layout([8, 8, 8], 2)
+    t, k = oracle.element_source(lay, [0, 11, 12, 15, 16, 23])
+    assert list(t) == [0, 1, 1, 1, 2, 2]
+    assert list(k) == [0, 3, 4, 7, 0, 7]
+
+
+def test_rank_view_sources_match_the_concatenated_shards():
+    rnd = random.Random(5)
+    for _ in range(200):
+        nd = rnd.randint(1, 6)
+        units = [[rnd.randint(0, 9) for _ in range(rnd.randint(1, 4))]
+                 for _ in range(rnd.randint(1, 4))]
+        packed = [oracle.flat_pack(_tagged(n, u), nd) for u, n in enumerate(units)]
+        layouts = [lay for _, lay in packed]
+        for r in range(nd):
+            view = np.concatenate([oracle.shard_of(f, lay, r) for f, lay in packed])
+            u, t, k = oracle.rank_view_sources(layouts, r, np.arange(view.size))
+            for i in range(view.size):
+                if t[i] < 0:
+                    assert view[i] == 0
+                else:
+                    assert view[i] == u[i] * 10 ** 6 + (t[i] + 1) * 10 ** 4 + k[i]
+            with pytest.raises(IndexError):
+                oracle.rank_view_sources(layouts, r, [view.size])
