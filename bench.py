@@ -256,6 +256,24 @@ WORKLOADS = {
 LOSS_SCALE = 65536.0
 
 
+def fill_rank_view(opt, buf, stream_of):
+    """Seeded inputs of one of a rank's buffers, placed where the library's
+    FlatParameter layout puts each tensor's piece (``rank_pieces``, i.e.
+    fsdp_shard_pieces); the units' padding stays zero."""
+    import synth
+    synth.dev_fill_pieces(buf, opt.rank_pieces(), stream_of)
+
+
+def oracle_rank_values(w, r, idx, stream_of, dtype):
+    """CPU-baseline inputs: the values at positions idx of rank r's buffer,
+    each traced to its tensor element by the oracle's own layout."""
+    import oracle
+    import synth
+    lays = [oracle.layout(w.unit_numels(u), w.F) for u in range(len(w.units))]
+    u, t, k = oracle.rank_view_sources(lays, r, idx)
+    return synth.host_gather_sources(u, t, k, stream_of, dtype)
+
+
 def workload(args):
     from synth import workloads as W
     w = getattr(W, WORKLOADS[args.workload])()
@@ -294,11 +312,11 @@ def run_ours(args):
                              grad_dtype=torch.float16 if scaled else torch.bfloat16)
     scaler = ss.GradScaler(LOSS_SCALE, device=dev) if scaled else None
     S = opt.shard_total
-    W.dev_fill_rank_master(w, r, opt.master)
+    fill_rank_view(opt, opt.master, w.master_stream)
     for q in range(nd):
-        W.dev_fill_rank_grad(w, 1, r, q, 0, opt.grad_in[q])
+        fill_rank_view(opt, opt.grad_in[q], lambda u, k, q=q: w.grad_stream(1, q, 0, u, k))
     u = w.extra["ag_unit"]
-    Su, Pu = w.unit_shard(u), w.unit_padded(u)
+    Su, Pu = opt.layouts[u].shard, opt.layouts[u].padded
     peers = [torch.empty(Su, dtype=torch.bfloat16, device=dev) for _ in range(F)]
     for q in range(F):
         if q != r:
@@ -620,12 +638,14 @@ def _oracle_sample(w, r, n, step, rng_seed=0):
     """Inputs of a contiguous sample of n shard elements (plus the matching
     sample of the all-gather), generated on the host."""
     import numpy as np
-    from synth import workloads as W
+    import oracle
     import synth
-    start = (rng_seed * 7919 * n) % max(1, 842_301_952 - n)
+    total = sum(oracle.layout(w.unit_numels(u), w.F).shard for u in range(len(w.units)))
+    start = (rng_seed * 7919 * n) % max(1, total - n)
     idx = np.arange(start, start + n, dtype=np.int64)
-    contribs = [W.host_gather_rank_grad(w, step, r, q, 0, idx) for q in range(w.nd)]
-    p = W.host_gather_rank_master(w, r, idx)
+    contribs = [oracle_rank_values(w, r, idx, lambda u, k, q=q: w.grad_stream(step, q, 0, u, k),
+                                   "bf16") for q in range(w.nd)]
+    p = oracle_rank_values(w, r, idx, w.master_stream, "f32")
     u = w.extra["ag_unit"]
     n_ag = max(1, n // (w.F * 4))
     shards = [synth.host_fill(w.peer_shard_stream(step, q, u), 0, n_ag, "bf16") for q in range(w.F)]
@@ -742,11 +762,11 @@ def run_fsdp2(args):
              for _ in range(nd)]
     for q in range(nd):
         for t, g in enumerate(grads[q]):
-            synth.dev_fill(w.grad_stream(1, q, 0, 100 + t), g)
+            synth.dev_fill(w.grad_stream(1, q, 0, 100, t), g)
     rs_in = [torch.empty(nd * L, dtype=torch.bfloat16, device=dev) for _ in range(nd)]
     masters = [torch.empty(sh, dtype=torch.float32, device=dev) for sh in shapes]
     for t, mt in enumerate(masters):
-        synth.dev_fill(w.master_stream(100 + t), mt)
+        synth.dev_fill(w.master_stream(100, t), mt)
     master = ss.fsdp2_chunk_cat(masters, nd)
     del masters
     m = torch.zeros(nd * L, device=dev)
@@ -1130,9 +1150,9 @@ def run_ckpt(args):
     hp = ss.AdamW()
     old = [RankShardOptimizer(w.units, 8, r, hp, device="cuda:0") for r in range(8)]
     for o in old:
-        W.dev_fill_rank_master(w, o.rank, o.master)
+        fill_rank_view(o, o.master, w.master_stream)
         for q in range(8):
-            W.dev_fill_rank_grad(w, 1, o.rank, q, 0, o.grad_in[q])
+            fill_rank_view(o, o.grad_in[q], lambda u, k, q=q: w.grad_stream(1, q, 0, u, k))
         o.step()
     new = [RankShardOptimizer(w.units, 4, r, hp, device="cuda:0") for r in range(4)]
     torch.cuda.synchronize()
@@ -1250,11 +1270,10 @@ def _accum_oracle_sample(w, n, t):
     import numpy as np
     import oracle
     from oracle.numerics import AdamWConfig
-    from synth import workloads as W
     idx = np.arange(1_000_000, 1_000_000 + n, dtype=np.int64)
-    micro = [[W.host_gather_rank_grad(w, 1, 0, q, j, idx) for j in range(w.micro)]
-             for q in range(w.nd)]
-    p = W.host_gather_rank_master(w, 0, idx)
+    micro = [[oracle_rank_values(w, 0, idx, lambda u, k, q=q, j=j: w.grad_stream(1, q, j, u, k),
+                                 "bf16") for j in range(w.micro)] for q in range(w.nd)]
+    p = oracle_rank_values(w, 0, idx, w.master_stream, "f32")
     hp = AdamWConfig(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
     m = np.zeros(n, np.float32)
     v = np.zeros(n, np.float32)
@@ -1313,10 +1332,11 @@ def run_accum(args):
     micro = [torch.empty(nd * S, dtype=torch.bfloat16, device=dev) for _ in range(M)]
     for j in range(M):
         for q in range(nd):
-            W.dev_fill_rank_grad(w, 1, r, q, j, micro[j][q * S:(q + 1) * S])
-    W.dev_fill_rank_master(w, r, opt.master)
+            fill_rank_view(opt, micro[j][q * S:(q + 1) * S],
+                           lambda u, k, q=q, j=j: w.grad_stream(1, q, j, u, k))
+    fill_rank_view(opt, opt.master, w.master_stream)
     u = 0
-    Su, Pu = w.unit_shard(u), w.unit_padded(u)
+    Su, Pu = opt.layouts[u].shard, opt.layouts[u].padded
     peers = [torch.empty(Su, dtype=torch.bfloat16, device=dev) for _ in range(nd)]
     for q in range(1, nd):
         synth.dev_fill(w.peer_shard_stream(1, q, u), peers[q])
@@ -1501,9 +1521,10 @@ def _ddp_oracle_sample(w, numels, n_params, t):
     from oracle.numerics import AdamWConfig
     sel = numels[:n_params]
     total = sum(sel)
-    grads = [np.concatenate([synth.host_fill(w.grad_stream(1, q, 0, i), 0, n, "bf16")
+    grads = [np.concatenate([synth.host_fill(w.grad_stream(1, q, 0, 0, i), 0, n, "bf16")
                              for i, n in enumerate(sel)]) for q in range(w.nd)]
-    p = synth.host_fill(w.master_stream(0), 0, total, "f32")
+    p = np.concatenate([synth.host_fill(w.master_stream(0, i), 0, n, "f32")
+                        for i, n in enumerate(sel)])
     z = np.zeros(total, np.float32)
     hp = AdamWConfig(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
     bounds = [0]
@@ -1570,10 +1591,11 @@ def run_ddp(args):
     off, _, boff = plans[25]
     for q in range(nd):
         for i, n in enumerate(numels):
-            synth.dev_fill(w.grad_stream(1, q, 0, i), grads[q][off[i]:off[i] + n])
+            synth.dev_fill(w.grad_stream(1, q, 0, 0, i), grads[q][off[i]:off[i] + n])
     out = torch.empty(total, dtype=torch.bfloat16, device=dev)
     master = torch.empty(total, dtype=torch.float32, device=dev)
-    synth.dev_fill(w.master_stream(0), master)
+    for i, n in enumerate(numels):
+        synth.dev_fill(w.master_stream(0, i), master[off[i]:off[i] + n])
     mm = torch.zeros(total, device=dev)
     vv = torch.zeros(total, device=dev)
     pb = torch.empty(total, dtype=torch.bfloat16, device=dev)

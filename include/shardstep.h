@@ -114,6 +114,23 @@ int fsdp_layout(const int64_t* numels, int32_t n, int32_t nd, shardstep_layout_i
 int fsdp_flat_pack(const void* const* src, const int64_t* numels, int32_t n, int32_t nd,
                    int32_t dtype, void* flat, void* stream);
 
+/* fsdp_shard_pieces -- host only.
+ * Same source as fsdp_layout ([P1] "FSDP1：先打包，再切分": a shard may cut
+ * a tensor, and a rank may hold nothing of one).  For rank `rank`, per
+ * tensor t, where the piece of t that the rank holds sits on both sides:
+ *   shard_lo[t]   its first position in the rank's shard (0..S),
+ *   tensor_lo[t]  its first element within tensor t (row-major order),
+ *   count[t]      its length (0 when the rank holds nothing of t; then
+ *                 shard_lo and tensor_lo are 0),
+ * so shard_r[shard_lo[t] + k] = tensor_t[tensor_lo[t] + k] for k < count[t]:
+ * what a caller needs to fill a rank's shard from the original tensors, or
+ * to write it back, without forming the full FlatParameter.
+ *   numels[n]   host, as in fsdp_layout;  nd  N_d >= 1;  0 <= rank < nd.
+ *   shard_lo, tensor_lo, count   host out, n entries each.
+ * Errors: INVALID (as fsdp_layout, rank out of range, a NULL array). */
+int fsdp_shard_pieces(const int64_t* numels, int32_t n, int32_t nd, int32_t rank,
+                      int64_t* shard_lo, int64_t* tensor_lo, int64_t* count);
+
 /* fsdp_views -- host only.
  * The use_orig_params views of [P1] section "FSDP1：先打包，再切分": per tensor,
  * the address and element count of its piece inside a buffer laid out by
@@ -487,6 +504,40 @@ int ddp_bucket_allreduce_avg(const uint16_t* const* rank_grads, int32_t nd,
                              const int64_t* bucket_offsets, int32_t first, int32_t count,
                              uint16_t* out, void* stream);
 
+/* ddp_bucket_allreduce_avg_adamw_cast -- device, one launch.
+ * The same sources as ddp_bucket_allreduce_avg, with the replicated update
+ * that follows it in one pass ([P1] section "Naïve Data Parallelism": every
+ * rank averages the full gradient and runs the same optimizer step).  For
+ * every element k of buckets first..first+count-1 (one contiguous range):
+ *     h        = bf16((((G_0[k] + G_1[k]) + ...) + G_{N_d-1}[k]) / N_d)
+ *                (fp32 sum in rank order; the all-reduce keeps bf16)
+ *     mean_out[k] = h                      (when mean_out is not NULL)
+ *     master[k], m[k], v[k], params[k]     AdamW of fsdp_rs_avg_adamw_cast
+ *                with g = bf16->fp32(h), then params[k] = bf16(master[k])
+ * i.e. the bits of ddp_bucket_allreduce_avg followed by
+ * fsdp_rs_avg_adamw_cast at nd = 1 on its output, without writing the mean
+ * and reading it back (2 N_d + 26 bytes per element instead of
+ * 2 N_d + 2 + 28; + 2 when mean_out is kept).
+ *   rank_grads[nd]   host array of device pointers, as in
+ *                    ddp_bucket_allreduce_avg (bf16).
+ *   bucket_offsets   host, from ddp_bucket_plan; first, count as there.
+ *   mean_out         device bf16 or NULL (the averaged gradient is not kept).
+ *   master, m, v     device fp32, params device bf16: the replicated state,
+ *                    indexed like the rank buffers (bucketed flat order),
+ *                    updated in place over the buckets' range.
+ *   hp               AdamW hyper-parameters and step t >= 1.
+ * The outputs must not overlap one another or any gradient.  Any alignment
+ * is accepted (4-element accesses need the state 16-byte, the gradients,
+ * mean_out and params 8-byte aligned at the range's start).  Register-staged
+ * kernels only.
+ * Errors: INVALID (null pointer, decreasing offsets, step < 1, overlap),
+ * CAPACITY (nd > SHARDSTEP_MAX_ND), CUDA (launch refused). */
+int ddp_bucket_allreduce_avg_adamw_cast(const uint16_t* const* rank_grads, int32_t nd,
+                                        const int64_t* bucket_offsets, int32_t first,
+                                        int32_t count, uint16_t* mean_out, float* master,
+                                        float* m, float* v, uint16_t* params,
+                                        const shardstep_adamw_t* hp, void* stream);
+
 /* ---------------------------------------------- DDP bucket readiness
  * Host only.  [P3] section 4.2: a bucket is all-reduced as soon as every
  * gradient in it is ready, so the buckets' reductions overlap the rest of
@@ -674,11 +725,41 @@ int32_t shardstep_set_tma_stages(int32_t stages);
 
 /* Watchdog word of the current device: bit 0 = a consumer's wait for a
  * staged tile ran out, bit 1 = the producer's wait for a free stage ran out
- * (the launch then returned early and its results are incomplete).  0 means
- * every TMA-staged launch so far completed its waits.  Synchronous (copies
- * the word to *status); clear != 0 resets it afterwards.  Errors: INVALID
- * (NULL), CUDA. */
+ * (in either case the launch returned early and its results are
+ * incomplete), bit 2 = the producer's wait for its own copies in flight ran
+ * out before the block exited (never expected: those copies read validated
+ * device memory).  0 means every TMA-staged launch so far completed its
+ * waits.  Synchronous (copies the word to *status); clear != 0 resets it
+ * afterwards.  Errors: INVALID (NULL), CUDA. */
 int shardstep_device_status(uint32_t* status, int32_t clear);
+
+/* Sets how long a TMA-staged kernel's waits for a staged tile or a free
+ * stage may last before the kernel gives up (status bits 0 and 1), in ns,
+ * process-wide, read at each launch: 0 = the default of about two seconds.
+ * A control for tests that make a wait run out: limits below 1 ms poll
+ * without blocking and read the clock after every poll (slower, but such a
+ * wait runs out even when each blocking poll would have lasted until its
+ * copy landed).  The wait of a block for its own bulk copies before it
+ * exits keeps its fixed two-second limit, so no setting lets a block exit
+ * with a copy in flight.  Returns the previous limit, or INVALID for
+ * ns < 0. */
+int64_t shardstep_set_tma_wait_ns(int64_t ns);
+
+/* shardstep_check_mean_division -- device, one launch (self-check).
+ * Every reduce here ends with a division by N_d ([P3] section 2: the mean of
+ * the N_d local-mean gradients), computed without a divide instruction when
+ * N_d is known in advance: a multiply by the exact reciprocal for a power of
+ * two, else a multiply by RN(1/N_d) and one fma correction (Markstein).
+ * This call runs that division and IEEE fp32 division on all 2^32 fp32 bit
+ * patterns and counts the patterns whose results differ in any bit.
+ *   nd          1..SHARDSTEP_MAX_ND.
+ *   mismatches  device uint64, 8-byte aligned: the count is added to it
+ *               (the caller zeroes it first).
+ *   first_bad   device uint32: lowered to the smallest differing pattern
+ *               (the caller sets it to 0xFFFFFFFF first).
+ * Errors: INVALID (nd out of range, NULL, misaligned), CUDA. */
+int shardstep_check_mean_division(int32_t nd, uint64_t* mismatches, uint32_t* first_bad,
+                                  void* stream);
 
 /* Description of the last error on the calling thread ("" if none). */
 const char* shardstep_last_error(void);

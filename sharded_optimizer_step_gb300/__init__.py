@@ -27,6 +27,8 @@ __all__ = [
     "hybrid_comm_bytes", "Fsdp2Layout", "fsdp2_layout", "fsdp2_local_views", "fsdp2_chunk_cat",
     "fsdp2_all_gather_copy_out", "AdamWState", "fsdp_state_rs_avg_adamw_cast",
     "fsdp_accumulate_rs_avg_adamw_cast", "fsdp_state_accumulate_rs_avg_adamw_cast",
+    "ddp_bucket_allreduce_avg_adamw_cast", "set_tma_wait_ns", "check_mean_division",
+    "fsdp_shard_pieces",
 ]
 
 
@@ -98,6 +100,20 @@ def fsdp_layout(numels, nd: int) -> Layout:
     return Layout(list(int(x) for x in numels), nd, info.total, info.padded, info.shard,
                   list(off[:n]), [list(lo[r * n:(r + 1) * n]) for r in range(nd)],
                   [list(hi[r * n:(r + 1) * n]) for r in range(nd)])
+
+
+def fsdp_shard_pieces(numels, nd: int, rank: int):
+    """Per tensor of a unit, the piece that rank ``rank`` holds: a list of
+    (position in the rank's shard, first element within the tensor, length)
+    (length 0: the rank holds nothing of that tensor).  Host only."""
+    L = _capi.lib()
+    n = len(numels)
+    slo = (_capi.c_i64 * max(1, n))()
+    tlo = (_capi.c_i64 * max(1, n))()
+    cnt = (_capi.c_i64 * max(1, n))()
+    _capi.check("fsdp_shard_pieces", L.fsdp_shard_pieces(_capi.i64_array(numels), n, nd, rank,
+                                                         slo, tlo, cnt))
+    return [(int(slo[t]), int(tlo[t]), int(cnt[t])) for t in range(n)]
 
 
 def fsdp_flat_pack(tensors, nd: int, flat=None, stream=None):
@@ -559,6 +575,41 @@ def ddp_bucket_allreduce_avg(rank_grads, bucket_offsets, out, first: int = 0,
     return out
 
 
+def ddp_bucket_allreduce_avg_adamw_cast(rank_grads, bucket_offsets, master, m, v, params,
+                                        hp: AdamW, step: int, mean_out=None, first: int = 0,
+                                        count: int | None = None, stream=None):
+    """The bucket all-reduce average of buckets first..first+count-1 fused with
+    the replicated AdamW + bf16 cast of the same elements (one launch): the
+    bits of ``ddp_bucket_allreduce_avg`` followed by the fused step at
+    N_d = 1 on its output.  ``mean_out`` (optional) receives the bf16 mean."""
+    import torch
+    _need_cuda(*rank_grads, master, m, v, params, mean_out)
+    if any(g.dtype != torch.bfloat16 for g in rank_grads) or params.dtype != torch.bfloat16:
+        raise ValueError("bf16 gradients and parameters")
+    if any(t.dtype != torch.float32 for t in (master, m, v)):
+        raise ValueError("master / m / v must be fp32")
+    if mean_out is not None and mean_out.dtype != torch.bfloat16:
+        raise ValueError("mean_out must be bf16")
+    nb = len(bucket_offsets) - 1
+    if count is None:
+        count = nb - first
+    if first < 0 or count < 0 or first + count > nb:
+        raise ValueError("bucket range out of bounds")
+    total = bucket_offsets[first + count] if nb >= 0 else 0
+    bufs = [*rank_grads, master, m, v, params] + ([mean_out] if mean_out is not None else [])
+    if any(t.numel() < total for t in bufs):
+        raise ValueError("buffers shorter than the bucketed range")
+    hpc = hp.at_step(step)
+    _capi.check("ddp_bucket_allreduce_avg_adamw_cast",
+                _capi.lib().ddp_bucket_allreduce_avg_adamw_cast(
+                    _capi.ptr_array([g.data_ptr() for g in rank_grads]), len(rank_grads),
+                    _capi.i64_array(bucket_offsets), first, count,
+                    ctypes.c_void_p(mean_out.data_ptr() if mean_out is not None else None),
+                    ctypes.c_void_p(master.data_ptr()), ctypes.c_void_p(m.data_ptr()),
+                    ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(params.data_ptr()),
+                    ctypes.byref(hpc), _stream(stream, master.device)))
+
+
 class BucketNotReady(TimeoutError):
     """A bucket's wait ran out: `rank` never marked `param` ready."""
 
@@ -675,6 +726,33 @@ def device_status(clear: bool = False) -> int:
     _capi.check("shardstep_device_status",
                 _capi.lib().shardstep_device_status(ctypes.byref(st), int(bool(clear))))
     return st.value
+
+
+def set_tma_wait_ns(ns: int) -> int:
+    """How long a TMA-staged kernel's waits for a tile or a free stage may
+    last (ns; 0 = the default of about two seconds).  A test control: a wait
+    that runs out sets a bit of ``device_status``.  Returns the previous
+    limit."""
+    prev = _capi.lib().shardstep_set_tma_wait_ns(int(ns))
+    if prev < 0:
+        _capi.check("shardstep_set_tma_wait_ns", int(prev))
+    return int(prev)
+
+
+def check_mean_division(nd: int, device=None, stream=None):
+    """Runs the library's division by N_d and IEEE fp32 division on all 2^32
+    fp32 bit patterns on the GPU.  Returns (mismatches, smallest differing
+    pattern or None); synchronises the stream."""
+    import torch
+    dev = torch.device(device) if device is not None else torch.device("cuda")
+    count = torch.zeros(1, dtype=torch.int64, device=dev)
+    first = torch.full((1,), -1, dtype=torch.int32, device=dev)
+    _capi.check("shardstep_check_mean_division", _capi.lib().shardstep_check_mean_division(
+        int(nd), ctypes.c_void_p(count.data_ptr()), ctypes.c_void_p(first.data_ptr()),
+        _stream(stream, dev)))
+    n = int(count.item())
+    f = int(first.item()) & 0xFFFFFFFF
+    return n, (f if n else None)
 
 
 def hybrid_state_bytes(psi: float, shard_group: int, k: float = 12.0) -> float:

@@ -61,6 +61,7 @@ SIGNATURES = {
     "fsdp_layout": (c_i32, [P_i64, c_i32, c_i32, ctypes.POINTER(LayoutInfo), P_i64, P_i64, P_i64]),
     "fsdp_flat_pack": (c_i32, [P_vp, P_i64, c_i32, c_i32, c_i32, c_vp, c_vp]),
     "fsdp_views": (c_i32, [P_i64, c_i32, c_i32, c_i32, c_vp, c_i32, P_vp, P_i64]),
+    "fsdp_shard_pieces": (c_i32, [P_i64, c_i32, c_i32, c_i32, P_i64, P_i64, P_i64]),
     "fsdp_grad_accumulate": (c_i32, [c_vp, c_vp, c_i64, c_f32, c_i32, c_vp]),
     "fsdp_rs_avg_adamw_cast": (c_i32, [P_vp, c_i32, c_i32, c_i64, c_vp, c_vp, c_vp, c_vp,
                                        ctypes.POINTER(AdamWHP), c_vp]),
@@ -82,6 +83,9 @@ SIGNATURES = {
     "fsdp2_all_gather_copy_out": (c_i32, [P_vp, P_i64, P_i64, c_i32, c_i32, c_i32, P_vp, c_vp]),
     "ddp_bucket_plan": (c_i32, [P_i64, c_i32, c_i32, c_i64, P_i64, P_i32, P_i64, P_i32]),
     "ddp_bucket_allreduce_avg": (c_i32, [P_vp, c_i32, P_i64, c_i32, c_i32, c_vp, c_vp]),
+    "ddp_bucket_allreduce_avg_adamw_cast": (c_i32, [P_vp, c_i32, P_i64, c_i32, c_i32, c_vp, c_vp,
+                                                    c_vp, c_vp, c_vp, ctypes.POINTER(AdamWHP),
+                                                    c_vp]),
     "shardstep_state_bytes": (c_f64, [c_f64, c_i32, c_i32, c_f64]),
     "shardstep_comm_bytes": (c_f64, [c_f64, c_i32, c_i32, c_i32]),
     "shardstep_hybrid_state_bytes": (c_f64, [c_f64, c_i32, c_f64]),
@@ -103,6 +107,8 @@ SIGNATURES = {
     "shardstep_set_tma_stages": (c_i32, [c_i32]),
     "shardstep_set_dependent_launch": (c_i32, [c_i32]),
     "shardstep_device_status": (c_i32, [ctypes.POINTER(ctypes.c_uint32), c_i32]),
+    "shardstep_set_tma_wait_ns": (c_i64, [c_i64]),
+    "shardstep_check_mean_division": (c_i32, [c_i32, c_vp, c_vp, c_vp]),
     "shardstep_launch_count": (c_u64, []),
     "shardstep_last_kernel": (ctypes.c_char_p, []),
     "shardstep_adamw_state_init": (c_i32, [c_vp, ctypes.POINTER(AdamWHP), c_i64, c_vp]),

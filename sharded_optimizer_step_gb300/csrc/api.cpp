@@ -56,14 +56,14 @@ std::atomic<int> g_dependent_launch{1};
 //     12 the two were level; at 1..4 and 16 it was faster as well);
 //   bucket all-reduce: at N_d = 4 and 8 on buckets of at least 32M
 //     elements (one 400M bucket at N_d = 4: 6.9 vs 6.4 TB/s; at N_d = 8:
-//     7.05 vs 6.98), at every N_d > 3 without a compiled register kernel
-//     on every bucket (N_d = 7: 6.5 vs 5.9 TB/s on one bucket, 6.1 vs 5.8
-//     on 25 MiB buckets); never at N_d = 1..3 (N_d = 3 on the up-to-8
-//     register kernel: 4.6 vs 4.2 TB/s);
-//   non-finite check: at every N_d but 1, 2, 4 and 8, the counts the
-//     register kernel is compiled for (at N_d = 1 / 2 / 4 / 8: 5.0 vs 2.1,
-//     6.0 vs 3.2, 6.7 vs 5.7, 7.4 vs 7.3 TB/s), and 3 with 16-bit slices
-//     (up-to-8 form: 3.7 vs 3.3 TB/s);
+//     7.05 vs 6.98) and at N_d > 8; never at N_d = 1..3 and 5..7, where the
+//     register kernel is compiled with several vectors' loads in flight
+//     (200M elements in 25 MiB buckets, register / TMA-staged: N_d = 3
+//     6.1 / 3.7, 5 6.5 / 4.8, 6 6.5 / 5.4, 7 6.7 / 5.9 TB/s);
+//   non-finite check: with 16-bit slices at N_d > 8 only (N_d = 3 / 5 / 6
+//     / 7, 200M fp16 elements: 5.1 / 2.7, 6.4 / 4.1, 6.9 / 4.6, 6.9 / 5.1
+//     TB/s; at N_d = 1 / 2 / 4 / 8: 5.0 vs 2.1, 6.0 vs 3.2, 6.7 vs 5.7,
+//     7.4 vs 7.3), with fp32 slices at every N_d but 1, 2, 4 and 8;
 //   accumulation: never (7.0 vs 6.0 TB/s for the first micro-batch, 7.2 vs
 //     6.6 for the others).
 enum class TmaOp { kStep, kAllReduce, kAccumulate, kCheck };
@@ -82,12 +82,11 @@ bool use_tma(TmaOp op, int64_t n, int nd = 0, int grad_dtype = SHARDSTEP_DTYPE_B
     switch (op) {
         case TmaOp::kStep: return nd >= 3 && !register_step_kernel(nd, grad_dtype);
         case TmaOp::kAllReduce:
-            if (nd <= 3) return false;
             if (nd == 4 || nd == 8) return n >= (int64_t{32} << 20);
-            return true;
+            return nd > 8;
         case TmaOp::kCheck:
-            if (nd == 3) return grad_dtype == SHARDSTEP_DTYPE_F32;
-            return nd != 1 && nd != 2 && nd != 4 && nd != 8;
+            if (grad_dtype == SHARDSTEP_DTYPE_F32) return nd != 1 && nd != 2 && nd != 4 && nd != 8;
+            return nd > 8;
         default: return false;
     }
 }
@@ -132,11 +131,25 @@ int elem_size_of(int32_t dtype) {
     }
 }
 
+// RN(1/nd) in fp32, from integers: the significand is 2^k / nd rounded to
+// the nearest integer for the k that puts it in [2^23, 2^24).  A tie cannot
+// occur (2^(k+1) / nd is an integer only for a power of two, and then the
+// quotient is exact), so rounding half up is round to nearest.
+float reciprocal_rn(int nd) {
+    int k = 0;
+    while ((uint64_t{1} << k) / static_cast<uint64_t>(nd) < (uint64_t{1} << 23)) ++k;
+    const uint64_t num = uint64_t{1} << k;
+    const uint64_t q = num / static_cast<uint64_t>(nd);
+    const uint64_t rem = num % static_cast<uint64_t>(nd);
+    const uint64_t sig = q + (2 * rem >= static_cast<uint64_t>(nd) ? 1 : 0);
+    return std::ldexp(static_cast<float>(sig), -k);
+}
+
 MeanOp mean_op(int nd, int group) {
     MeanOp mo;
     mo.nd = static_cast<float>(nd);
     mo.pow2 = (nd & (nd - 1)) == 0;
-    mo.inv_nd = 1.0f / static_cast<float>(nd);  // exact when nd is a power of two
+    mo.inv_nd = reciprocal_rn(nd);  // exact when nd is a power of two
     mo.group = group;
     mo.inv_scale = 1.0f;
     mo.scaled = 0;
@@ -298,6 +311,27 @@ int32_t shardstep_set_tma_stages(int32_t stages) {
     return set_tma_stage_limit(stages);
 }
 
+int64_t shardstep_set_tma_wait_ns(int64_t ns) {
+    if (ns < 0) return fail(SHARDSTEP_ERR_INVALID, "the wait limit must be >= 0 (got %lld)",
+                            static_cast<long long>(ns));
+    return set_tma_wait_ns(ns);
+}
+
+int shardstep_check_mean_division(int32_t nd, uint64_t* mismatches, uint32_t* first_bad,
+                                  void* stream) {
+    if (nd < 1 || nd > SHARDSTEP_MAX_ND)
+        return fail(SHARDSTEP_ERR_INVALID, "nd must be 1..%d (got %d)", SHARDSTEP_MAX_ND, nd);
+    if (mismatches == nullptr || first_bad == nullptr)
+        return fail(SHARDSTEP_ERR_INVALID, "mismatches / first_bad is NULL");
+    if (!aligned(mismatches, 8) || !aligned(first_bad, 4))
+        return fail(SHARDSTEP_ERR_INVALID, "mismatches / first_bad misaligned");
+    cudaError_t e = launch_mean_division_check(
+        mean_op(nd, nd), reinterpret_cast<unsigned long long*>(mismatches), first_bad,
+        static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "division check kernel launch");
+    return ok();
+}
+
 int shardstep_device_status(uint32_t* status, int32_t clear) {
     if (status == nullptr) return fail(SHARDSTEP_ERR_INVALID, "status is NULL");
     unsigned int s = 0;
@@ -324,6 +358,34 @@ int fsdp_layout(const int64_t* numels, int32_t n, int32_t nd, shardstep_layout_i
             b = b < 0 ? 0 : (b > S ? S : b);
             if (lo) lo[static_cast<int64_t>(r) * n + t] = a;
             if (hi) hi[static_cast<int64_t>(r) * n + t] = b;
+        }
+    }
+    return ok();
+}
+
+int fsdp_shard_pieces(const int64_t* numels, int32_t n, int32_t nd, int32_t rank,
+                      int64_t* shard_lo, int64_t* tensor_lo, int64_t* count) {
+    shardstep_layout_info_t info;
+    std::vector<int64_t> off(n > 0 ? n : 0);
+    int rc = compute_layout(numels, n, nd, &info, off.data());
+    if (rc != SHARDSTEP_OK) return rc;
+    if (rank < 0 || rank >= nd)
+        return fail(SHARDSTEP_ERR_INVALID, "rank %d out of 0..%d", rank, nd - 1);
+    if (n > 0 && (shard_lo == nullptr || tensor_lo == nullptr || count == nullptr))
+        return fail(SHARDSTEP_ERR_INVALID, "shard_lo / tensor_lo / count is NULL");
+    const int64_t S = info.shard, r0 = static_cast<int64_t>(rank) * S;
+    for (int32_t t = 0; t < n; ++t) {
+        // the tensor's flat range [off, off + n_t) meets [r0, r0 + S)
+        const int64_t a = off[t] > r0 ? off[t] : r0;
+        const int64_t e = off[t] + numels[t] < r0 + S ? off[t] + numels[t] : r0 + S;
+        if (a < e) {
+            shard_lo[t] = a - r0;
+            tensor_lo[t] = a - off[t];
+            count[t] = e - a;
+        } else {
+            shard_lo[t] = 0;
+            tensor_lo[t] = 0;
+            count[t] = 0;
         }
     }
     return ok();
@@ -838,11 +900,9 @@ int fsdp_grad_unscale_check(const void* const* grad_slices, int32_t grad_dtype, 
     if (e != cudaSuccess) return cuda_fail(e, "non-finite check launch");
     if (tma)
         note_kernel("staged_stream<CheckOp<%s>> (TMA-staged)", dtype_name(grad_dtype));
-    else if (vec && compiled_nd(nd, {1, 2, 4, 8}))
+    else if (vec && (compiled_nd(nd, {1, 2, 4, 8}) ||
+                     (grad_dtype != SHARDSTEP_DTYPE_F32 && compiled_nd(nd, {3, 5, 6, 7}))))
         note_kernel("nonfinite_check_vec4<%d, %s> (register-staged)", nd, dtype_name(grad_dtype));
-    else if (vec && nd == 3 && grad_dtype != SHARDSTEP_DTYPE_F32)
-        note_kernel("nonfinite_check_vec4<up to 8: 3, %s> (register-staged)",
-                    dtype_name(grad_dtype));
     else if (vec)
         note_kernel("nonfinite_check_vec4<any N_d = %d, %s> (register-staged)", nd,
                     dtype_name(grad_dtype));
@@ -1144,16 +1204,77 @@ int ddp_bucket_allreduce_avg(const uint16_t* const* rank_grads, int32_t nd,
         if (e != cudaSuccess) return cuda_fail(e, "all-reduce kernel launch");
         if (tma)
             note_kernel("staged_stream<MeanOutOp> (TMA-staged)");
-        else if (vec && compiled_nd(nd, {1, 2, 4, 8}))
+        else if (vec && compiled_nd(nd, {1, 2, 3, 4, 5, 6, 7, 8}))
             note_kernel("allreduce_avg_vec4<%d> (register-staged)", nd);
-        else if (vec && nd == 3)
-            note_kernel("allreduce_avg_vec4<up to 8: 3> (register-staged)");
         else if (vec)
             note_kernel("allreduce_avg_vec4<any N_d = %d> (register-staged)", nd);
         else
             note_kernel("allreduce_avg_scalar");
         pdl = g_dependent_launch.load(std::memory_order_relaxed) != 0;
     }
+    return ok();
+}
+
+int ddp_bucket_allreduce_avg_adamw_cast(const uint16_t* const* rank_grads, int32_t nd,
+                                        const int64_t* bucket_offsets, int32_t first,
+                                        int32_t count, uint16_t* mean_out, float* master,
+                                        float* m, float* v, uint16_t* params,
+                                        const shardstep_adamw_t* hp, void* stream) {
+    if (nd < 1) return fail(SHARDSTEP_ERR_INVALID, "nd must be >= 1 (got %d)", nd);
+    if (nd > SHARDSTEP_MAX_ND)
+        return fail(SHARDSTEP_ERR_CAPACITY, "nd %d > %d", nd, SHARDSTEP_MAX_ND);
+    if (first < 0 || count < 0) return fail(SHARDSTEP_ERR_INVALID, "first / count negative");
+    AdamScalars c{};
+    if (int rc = adam_source(hp, nullptr, &c); rc != SHARDSTEP_OK) return rc;
+    if (count == 0) return ok();
+    if (bucket_offsets == nullptr || rank_grads == nullptr)
+        return fail(SHARDSTEP_ERR_INVALID, "bucket_offsets / rank_grads is NULL");
+    for (int32_t b = first; b < first + count; ++b)
+        if (bucket_offsets[b] < 0 || bucket_offsets[b + 1] < bucket_offsets[b])
+            return fail(SHARDSTEP_ERR_INVALID, "bucket offsets must be non-decreasing");
+    const int64_t a0 = bucket_offsets[first], n = bucket_offsets[first + count] - a0;
+    if (n == 0) return ok();
+    // the buckets first..first+count-1 are contiguous: one launch over them
+    Span outs[5];
+    if (int rc = check_step_outputs(n, master ? master + a0 : nullptr, m ? m + a0 : nullptr,
+                                    v ? v + a0 : nullptr, params ? params + a0 : nullptr, outs);
+        rc != SHARDSTEP_OK)
+        return rc;
+    int n_outs = 4;
+    if (mean_out != nullptr) {
+        if (!aligned(mean_out, 2))
+            return fail(SHARDSTEP_ERR_INVALID, "mean_out is not 2-byte aligned");
+        outs[4] = span(mean_out + a0, n * 2);
+        for (int a = 0; a < 4; ++a)
+            if (overlap(outs[4], outs[a]))
+                return fail(SHARDSTEP_ERR_INVALID, "mean_out overlaps output %d", a);
+        n_outs = 5;
+    }
+    std::vector<const void*> slices(nd);
+    for (int32_t q = 0; q < nd; ++q) {
+        if (rank_grads[q] == nullptr)
+            return fail(SHARDSTEP_ERR_INVALID, "rank_grads[%d] is NULL", q);
+        slices[q] = rank_grads[q] + a0;
+    }
+    PtrTable tab;
+    bool vec = false, tma = false;
+    int rc = take_slices(slices.data(), SHARDSTEP_DTYPE_BF16, nd, n, outs, n_outs, &tab, &vec,
+                         &tma);
+    if (rc != SHARDSTEP_OK) return rc;
+    vec = vec && aligned(master + a0, 16) && aligned(m + a0, 16) && aligned(v + a0, 16) &&
+          aligned(params + a0, 8) && (mean_out == nullptr || aligned(mean_out + a0, 8));
+    cudaError_t e = launch_ddp_allreduce_adamw_cast(
+        tab, nd, n, mean_out ? mean_out + a0 : nullptr, master + a0, m + a0, v + a0,
+        params + a0, c, mean_op(nd, nd), vec, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "fused all-reduce + AdamW kernel launch");
+    if (vec && (compiled_nd(nd, {1, 2, 3, 4, 6, 8, 12, 16})))
+        note_kernel("ddp_allreduce_adamw_cast_vec4<%d> (register-staged)", nd);
+    else if (vec && (nd == 5 || nd == 7))
+        note_kernel("ddp_allreduce_adamw_cast_vec4<up to 8: %d> (register-staged)", nd);
+    else if (vec)
+        note_kernel("ddp_allreduce_adamw_cast_vec4<any N_d = %d> (register-staged)", nd);
+    else
+        note_kernel("ddp_allreduce_adamw_cast_scalar");
     return ok();
 }
 

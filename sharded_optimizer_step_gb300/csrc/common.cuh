@@ -150,8 +150,33 @@ struct GroupSum {
     }
 };
 
+// x / N_d, correctly rounded (the same bits as IEEE division).  A power of
+// two multiplies by its exact reciprocal.  Any other N_d is divided with
+// Markstein's correction step (P. Markstein, "Computation of elementary
+// functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1),
+// 1990), the divisor being known in advance: with r = RN(1/N_d) from the
+// host, q0 = RN(x * r) is within one ulp of x / N_d, the residual
+// x - q0 * N_d is exact in one fma (N_d is a small integer, so it fits in a
+// few bits above q0's last place), and RN(q0 + residual * r) is the
+// correctly rounded quotient.  Those exactness arguments need q0 and the
+// residual well inside the normal range, so a sum whose biased exponent is
+// below kDivFastMinExp (zero, subnormals, |x| < 2^-63) or 255 (inf, NaN)
+// takes the IEEE division instead.  shardstep_check_mean_division compares
+// this with IEEE division on all 2^32 fp32 inputs, for every N_d.
+constexpr uint32_t kDivFastMinExp = 64u;
+__device__ __forceinline__ float div_nd(float x, const MeanOp& mo) {
+    if (mo.pow2) return __fmul_rn(x, mo.inv_nd);
+    const uint32_t ex = (__float_as_uint(x) >> 23) & 0xFFu;
+    if (ex >= kDivFastMinExp && ex != 0xFFu) {
+        const float q0 = __fmul_rn(x, mo.inv_nd);
+        const float res = __fmaf_rn(-q0, mo.nd, x);
+        return __fmaf_rn(res, mo.inv_nd, q0);
+    }
+    return __fdiv_rn(x, mo.nd);
+}
+
 __device__ __forceinline__ float mean_of(float sum, const MeanOp& mo) {
-    const float g = mo.pow2 ? __fmul_rn(sum, mo.inv_nd) : __fdiv_rn(sum, mo.nd);
+    const float g = div_nd(sum, mo);
     return mo.scaled ? __fmul_rn(g, mo.inv_scale) : g;
 }
 
@@ -161,6 +186,24 @@ __device__ __forceinline__ MeanOp resolve_scale(MeanOp mo) {
     if (mo.scaled) mo.inv_scale = __fdiv_rn(1.0f, __ldcg(mo.scale));
     return mo;
 }
+
+// For fp16 slices the scaler's check can be decided on the input bits alone.
+// A finite fp16 value is at most 65504 in magnitude, so the fp32 sum of at
+// most SHARDSTEP_MAX_ND = 64 of them (in any grouping) stays below 2^22, so
+// does the mean, and the mean times inv_scale stays finite while
+// |inv_scale| <= 2^100.  An inf or NaN input makes the sum inf or NaN, and
+// neither the division by N_d nor the multiplication by any inv_scale makes
+// it finite again (inf * 0 is NaN).  So when |inv_scale| <= 2^100 (false for
+// a NaN inv_scale) the unscaled mean is non-finite exactly where some slice
+// holds an inf or NaN, i.e. an all-ones exponent field: no conversion and
+// no arithmetic is needed.
+__device__ __forceinline__ bool f16_check_on_bits(const MeanOp& mo) {
+    return fabsf(mo.inv_scale) <= 0x1p100f;
+}
+__device__ __forceinline__ bool f16x2_nonfinite(uint32_t w) {
+    return ((w & 0x7C00u) == 0x7C00u) | ((w & 0x7C000000u) == 0x7C000000u);
+}
+__device__ __forceinline__ bool f16_nonfinite(uint16_t h) { return (h & 0x7C00u) == 0x7C00u; }
 
 // A gradient scaler's skip word: non-zero means this step changes nothing.
 __device__ __forceinline__ bool skip_step(const unsigned int* skip) {

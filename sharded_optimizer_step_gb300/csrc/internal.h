@@ -32,8 +32,9 @@ cudaError_t launch_adamw_state_advance(shardstep_adamw_state_t* state, double lr
 // How the reduce turns the N_d rank slices into a mean: the slices are summed
 // in groups of `group` consecutive ranks (group == N_d: one rank-order sum;
 // 1 < group < N_d: hybrid sharding, group sums first, then across groups),
-// then the total is multiplied by the exact reciprocal when N_d is a power of
-// two (identical to dividing) or divided by N_d.
+// then the total is divided by N_d, correctly rounded (div_nd: a multiply by
+// the exact reciprocal when N_d is a power of two, else a multiply by
+// inv_nd = RN(1/N_d) and one fma correction).
 // With `scaled` set, the mean is then multiplied by inv_scale, the gradient
 // scaler's 1/s, which each kernel computes at start from the device word
 // *scale (resolve_scale).
@@ -131,6 +132,9 @@ cudaError_t launch_rs_adamw_cast(const PtrTable& tab, int nd, int grad_type, int
 bool tma_step_fits(int nd, int grad_type);
 bool tma_reduce_fits(int nd, int grad_type);
 int set_tma_stage_limit(int stages);
+// The TMA-staged kernels' wait limit in ns (0: the default of two seconds);
+// read at each launch.  Returns the previous limit.
+int64_t set_tma_wait_ns(int64_t ns);
 cudaError_t launch_rs_adamw_cast_tma(const PtrTable& tab, int nd, int grad_type, int64_t S,
                                      float* master, float* m, float* v, uint16_t* out,
                                      const AdamScalars& c, const MeanOp& mo,
@@ -157,6 +161,18 @@ constexpr int64_t kTmaMinElements = 4096;
 
 cudaError_t launch_allreduce_avg(const PtrTable& tab, int nd, int64_t n, uint16_t* out,
                                  const MeanOp& mo, bool vec, bool pdl, cudaStream_t stream);
+// The DDP all-reduce average fused with the replicated AdamW + cast over n
+// bucketed elements (step.cu); mean_out may be null.  `vec`: state 16-byte,
+// gradients, mean_out and out 8-byte aligned.
+cudaError_t launch_ddp_allreduce_adamw_cast(const PtrTable& tab, int nd, int64_t n,
+                                            uint16_t* mean_out, float* master, float* m,
+                                            float* v, uint16_t* out, const AdamScalars& c,
+                                            const MeanOp& mo, bool vec, cudaStream_t stream);
+// Division self-check (step.cu): counts into *mismatches the fp32 patterns
+// for which the reduce's division by N_d differs from IEEE division and
+// lowers *first_bad to the smallest of them.
+cudaError_t launch_mean_division_check(const MeanOp& mo, unsigned long long* mismatches,
+                                       unsigned int* first_bad, cudaStream_t stream);
 // The copy launchers' `pdl`: launch as a programmatic dependent of the
 // previous kernel in the stream (only for a later launch of the same batch
 // of disjoint copies; every copy kernel waits for its predecessor before it

@@ -160,14 +160,21 @@ __device__ __forceinline__ void sum_loaded(const GradVec<GT>* gv, int group, flo
     acc.result(g);
 }
 
-// Kernels that read one, two or four slices per element move few bytes per
-// vector, so a thread loads light_u<ND>() vectors before summing any of
-// them.  On GB300 (200M elements) this took the fp16 check at N_d = 1 / 2 /
-// 4 from 1.4 / 2.5 / 6.1 to 5.0 / 6.0 / 6.7 TB/s and the all-reduce on
-// 25 MiB buckets from 4.7 / 5.2 / 6.0 to 5.8 / 6.3 / 6.6 TB/s.
+// The all-reduce and the check read 2 bytes per slice element, so with one
+// vector per thread in flight a thread has only 8 x N_d bytes outstanding:
+// at N_d < 8 too little to cover the latency of HBM.  A thread therefore
+// issues the loads of light_u<ND>() vectors before summing any of them (at
+// least 64 bytes in flight per thread).  On GB300 (200M elements) this took
+// the fp16 check at N_d = 1 / 2 / 4 from 1.4 / 2.5 / 6.1 to 5.0 / 6.0 / 6.7
+// TB/s and the all-reduce on 25 MiB buckets from 4.7 / 5.2 / 6.0 to 5.8 /
+// 6.3 / 6.6 TB/s.
 template <int ND>
 __host__ __device__ constexpr int light_u() {
-    return ND == 4 ? 2 : 4;
+    return ND <= 3 ? 4 : 2;
+}
+template <int ND>
+__host__ __device__ constexpr bool light_nd() {
+    return ND >= 1 && ND <= 7;
 }
 
 template <int GT>
@@ -252,6 +259,84 @@ __global__ void __launch_bounds__(kThreads)
         step_scalar<GT>(tab, nd, j, P, M, V, out, c, mo);
 }
 
+// ------------------------------------- DDP all-reduce avg + AdamW, fused
+
+// The replicated update of DDP in one pass over bucketed elements: the N_d
+// bf16 gradients summed in rank order and divided by N_d, the mean rounded
+// to bf16 once (the all-reduce keeps the gradient's dtype), optionally
+// stored, upcast, then AdamW and the bf16 cast -- the bits of the bucket
+// all-reduce followed by the fused step at N_d = 1 on its output.
+__device__ __forceinline__ void ddp_elem(float sum, float& p, float& m, float& v,
+                                         uint16_t* mean_out, int64_t j, const AdamScalars& c,
+                                         const MeanOp& mo) {
+    const uint16_t h = f32_to_bf16(mean_of(sum, mo));
+    if (mean_out != nullptr) mean_out[j] = h;
+    adamw_elem(bf16_to_f32(h), p, m, v, c);
+}
+
+template <int ND>
+__global__ void __launch_bounds__(kStepThreads, kStepMinBlocks)
+    ddp_allreduce_adamw_cast_vec4(PtrTable tab, int nd, int64_t n, uint16_t* __restrict__ mean_out,
+                                  float* __restrict__ P, float* __restrict__ M,
+                                  float* __restrict__ V, uint16_t* __restrict__ out,
+                                  AdamScalars c, MeanOp mo) {
+    c = resolve_adam(c);
+    const int64_t nvec = n >> 2;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kStepThreads;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kStepThreads + threadIdx.x; i < nvec;
+         i += stride) {
+        const uint4 p0 = ldcs16(P + 4 * i);
+        const uint4 m0 = ldcs16(M + 4 * i);
+        const uint4 v0 = ldcs16(V + 4 * i);
+        float g[4];
+        reduce4<ND, kGradBF16>(tab, nd, mo.group, i, g);
+        const uint2 h = make_uint2(pack_bf16x2(mean_of(g[0], mo), mean_of(g[1], mo)),
+                                   pack_bf16x2(mean_of(g[2], mo), mean_of(g[3], mo)));
+        if (mean_out != nullptr) stcs8(mean_out + 4 * i, h);
+        g[0] = bf16_lo(h.x);
+        g[1] = bf16_hi(h.x);
+        g[2] = bf16_lo(h.y);
+        g[3] = bf16_hi(h.y);
+        float p[4], m[4], v[4];
+        unpack4f(p0, p);
+        unpack4f(m0, m);
+        unpack4f(v0, v);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) adamw_elem(g[k], p[k], m[k], v[k], c);
+        stcs16(P + 4 * i, pack4f(p));
+        stcs16(M + 4 * i, pack4f(m));
+        stcs16(V + 4 * i, pack4f(v));
+        stcs8(out + 4 * i, make_uint2(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3])));
+    }
+    if (blockIdx.x == 0 && threadIdx.x < (n & 3)) {
+        const int64_t j = (nvec << 2) + threadIdx.x;
+        float p = P[j], m = M[j], v = V[j];
+        ddp_elem(reduce1<kGradBF16>(tab, nd, mo.group, j), p, m, v, mean_out, j, c, mo);
+        P[j] = p;
+        M[j] = m;
+        V[j] = v;
+        out[j] = f32_to_bf16(p);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads)
+    ddp_allreduce_adamw_cast_scalar(PtrTable tab, int nd, int64_t n,
+                                    uint16_t* __restrict__ mean_out, float* __restrict__ P,
+                                    float* __restrict__ M, float* __restrict__ V,
+                                    uint16_t* __restrict__ out, AdamScalars c, MeanOp mo) {
+    c = resolve_adam(c);
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    for (int64_t j = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; j < n;
+         j += stride) {
+        float p = P[j], m = M[j], v = V[j];
+        ddp_elem(reduce1<kGradBF16>(tab, nd, mo.group, j), p, m, v, mean_out, j, c, mo);
+        P[j] = p;
+        M[j] = m;
+        V[j] = v;
+        out[j] = f32_to_bf16(p);
+    }
+}
+
 // ------------------------------------------------ bucket all-reduce avg
 
 // Both all-reduce kernels may run as programmatic dependents of the previous
@@ -270,7 +355,7 @@ __global__ void __launch_bounds__(kStepThreads, kStepMinBlocks)
     const int64_t run = static_cast<int64_t>(kStepThreads) * vpt;
     for (int64_t b0 = static_cast<int64_t>(blockIdx.x) * run; b0 < nvec;
          b0 += static_cast<int64_t>(gridDim.x) * run) {
-        if constexpr (ND == 1 || ND == 2 || ND == 4) {
+        if constexpr (light_nd<ND>()) {
             constexpr int kLightU = light_u<ND>();
             for (int k = 0; k < vpt; k += kLightU) {
                 GradVec<kGradBF16> gv[kLightU][ND];
@@ -331,6 +416,56 @@ __device__ __forceinline__ bool not_finite(float x) {
     return (__float_as_uint(x) & 0x7F800000u) == 0x7F800000u;
 }
 
+// The fp16 check decided on the input bits (f16_check_on_bits): whether any
+// slice holds an inf or NaN in this thread's vectors, with the loads of
+// light_u<ND>() vectors (a batch of 8 slices at a time for any N_d) in
+// flight before any test.
+template <int ND>
+__device__ __forceinline__ bool f16_bits_scan(const PtrTable& tab, int nd, int64_t nvec,
+                                              int64_t b0, int vpt) {
+    bool bad = false;
+    if constexpr (light_nd<ND>()) {
+        constexpr int kLightU = light_u<ND>();
+        for (int k = 0; k < vpt; k += kLightU) {
+            GradVec<kGradF16> gv[kLightU][ND];
+#pragma unroll
+            for (int u = 0; u < kLightU; ++u) {
+                const int64_t i = b0 + static_cast<int64_t>(k + u) * kStepThreads + threadIdx.x;
+                if (k + u < vpt && i < nvec) {
+#pragma unroll
+                    for (int q = 0; q < ND; ++q) gv[u][q].load(tab.p[q], i);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < ND; ++q) gv[u][q].r = make_uint2(0u, 0u);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kLightU; ++u)
+#pragma unroll
+                for (int q = 0; q < ND; ++q)
+                    bad |= f16x2_nonfinite(gv[u][q].r.x) | f16x2_nonfinite(gv[u][q].r.y);
+        }
+    } else {
+        for (int k = 0; k < vpt; ++k) {
+            const int64_t i = b0 + static_cast<int64_t>(k) * kStepThreads + threadIdx.x;
+            if (i >= nvec) break;
+            const int n = ND == kRuntimeND ? nd : (ND < 0 ? nd : ND);
+            for (int q = 0; q < n; q += 8) {
+                GradVec<kGradF16> gv[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    if (q + u < n) gv[u].load(tab.p[q + u], i);
+                    else gv[u].r = make_uint2(0u, 0u);
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    bad |= f16x2_nonfinite(gv[u].r.x) | f16x2_nonfinite(gv[u].r.y);
+            }
+        }
+    }
+    return bad;
+}
+
 // Sets *found when any unscaled mean gradient is inf or NaN.  Reads the
 // slices only (2 B per fp16 slice element); one atomic per warp that saw one.
 template <int ND, int GT>
@@ -341,9 +476,22 @@ __global__ void __launch_bounds__(kStepThreads, kStepMinBlocks)
     bool bad = false;
     const int64_t nvec = S >> 2;
     const int64_t run = static_cast<int64_t>(kStepThreads) * vpt;
+    if constexpr (GT == kGradF16) {
+        if (f16_check_on_bits(mo)) {     // the same for the whole grid
+            for (int64_t b0 = static_cast<int64_t>(blockIdx.x) * run; b0 < nvec;
+                 b0 += static_cast<int64_t>(gridDim.x) * run)
+                bad |= f16_bits_scan<ND>(tab, nd, nvec, b0, vpt);
+            if (blockIdx.x == 0 && threadIdx.x < (S & 3))
+                for (int q = 0; q < nd; ++q)
+                    bad |= f16_nonfinite(static_cast<const uint16_t*>(
+                        tab.p[q])[(nvec << 2) + threadIdx.x]);
+            if (__any_sync(0xFFFFFFFFu, bad) && (threadIdx.x & 31) == 0) atomicOr(found, 1u);
+            return;
+        }
+    }
     for (int64_t b0 = static_cast<int64_t>(blockIdx.x) * run; b0 < nvec;
          b0 += static_cast<int64_t>(gridDim.x) * run) {
-        if constexpr (ND == 1 || ND == 2 || ND == 4) {
+        if constexpr (light_nd<ND>()) {
             constexpr int kLightU = light_u<ND>();
             for (int k = 0; k < vpt; k += kLightU) {
                 GradVec<GT> gv[kLightU][ND];
@@ -415,6 +563,35 @@ __global__ void scaler_update_kernel(float* scale, int* tracker, unsigned int* f
         }
     }
     *found = 0u;
+}
+
+// ------------------------------------------------- division self-check
+
+// Compares div_nd with IEEE division (__fdiv_rn) on every fp32 bit pattern:
+// counts the patterns whose results differ in any bit and keeps the
+// smallest such pattern.
+__global__ void __launch_bounds__(kThreads)
+    mean_division_check(MeanOp mo, unsigned long long* mismatches, unsigned int* first_bad) {
+    unsigned long long bad = 0;
+    unsigned int first = 0xFFFFFFFFu;
+    const uint64_t stride = static_cast<uint64_t>(gridDim.x) * kThreads;
+    for (uint64_t b = static_cast<uint64_t>(blockIdx.x) * kThreads + threadIdx.x;
+         b < (uint64_t{1} << 32); b += stride) {
+        const float x = __uint_as_float(static_cast<uint32_t>(b));
+        if (__float_as_uint(div_nd(x, mo)) != __float_as_uint(__fdiv_rn(x, mo.nd))) {
+            ++bad;
+            if (static_cast<uint32_t>(b) < first) first = static_cast<uint32_t>(b);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        bad += __shfl_xor_sync(0xFFFFFFFFu, bad, o);
+        first = min(first, __shfl_xor_sync(0xFFFFFFFFu, first, o));
+    }
+    if ((threadIdx.x & 31) == 0 && bad != 0) {
+        atomicAdd(mismatches, bad);
+        atomicMin(first_bad, first);
+    }
 }
 
 // --------------------------------------------------------------- launch
@@ -534,13 +711,24 @@ cudaError_t dispatch_check(const PtrTable& tab, int nd, int64_t S, const MeanOp&
         note_launch();
         return cudaGetLastError();
     }
+    // fp32 slices at N_d = 3..7 would hold too many registers of loads in
+    // flight: they take the loop over any N_d
     switch (nd) {
         case 1: return go_check<1, GT>(tab, nd, S, mo, found, s);
         case 2: return go_check<2, GT>(tab, nd, S, mo, found, s);
         case 3:
-            if constexpr (GT != kGradF32) return go_check<-8, GT>(tab, nd, S, mo, found, s);
+            if constexpr (GT != kGradF32) return go_check<3, GT>(tab, nd, S, mo, found, s);
             else return go_check<kRuntimeND, GT>(tab, nd, S, mo, found, s);
         case 4: return go_check<4, GT>(tab, nd, S, mo, found, s);
+        case 5:
+            if constexpr (GT != kGradF32) return go_check<5, GT>(tab, nd, S, mo, found, s);
+            else return go_check<kRuntimeND, GT>(tab, nd, S, mo, found, s);
+        case 6:
+            if constexpr (GT != kGradF32) return go_check<6, GT>(tab, nd, S, mo, found, s);
+            else return go_check<kRuntimeND, GT>(tab, nd, S, mo, found, s);
+        case 7:
+            if constexpr (GT != kGradF32) return go_check<7, GT>(tab, nd, S, mo, found, s);
+            else return go_check<kRuntimeND, GT>(tab, nd, S, mo, found, s);
         case 8: return go_check<8, GT>(tab, nd, S, mo, found, s);
         default: return go_check<kRuntimeND, GT>(tab, nd, S, mo, found, s);
     }
@@ -566,8 +754,11 @@ cudaError_t launch_allreduce_avg(const PtrTable& tab, int nd, int64_t n, uint16_
         switch (nd) {
             case 1: return go_ar<1>(tab, nd, n, out, mo, pdl, stream);
             case 2: return go_ar<2>(tab, nd, n, out, mo, pdl, stream);
-            case 3: return go_ar<-8>(tab, nd, n, out, mo, pdl, stream);
+            case 3: return go_ar<3>(tab, nd, n, out, mo, pdl, stream);
             case 4: return go_ar<4>(tab, nd, n, out, mo, pdl, stream);
+            case 5: return go_ar<5>(tab, nd, n, out, mo, pdl, stream);
+            case 6: return go_ar<6>(tab, nd, n, out, mo, pdl, stream);
+            case 7: return go_ar<7>(tab, nd, n, out, mo, pdl, stream);
             case 8: return go_ar<8>(tab, nd, n, out, mo, pdl, stream);
             default: return go_ar<kRuntimeND>(tab, nd, n, out, mo, pdl, stream);
         }
@@ -598,6 +789,47 @@ cudaError_t launch_nonfinite_check(const PtrTable& tab, int nd, int grad_type, i
 cudaError_t launch_scaler_update(float* scale, int* tracker, unsigned int* found, float growth,
                                  float backoff, int interval, cudaStream_t stream) {
     scaler_update_kernel<<<1, 32, 0, stream>>>(scale, tracker, found, growth, backoff, interval);
+    note_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_ddp_allreduce_adamw_cast(const PtrTable& tab, int nd, int64_t n,
+                                            uint16_t* mean_out, float* master, float* m,
+                                            float* v, uint16_t* out, const AdamScalars& c,
+                                            const MeanOp& mo, bool vec, cudaStream_t stream) {
+    if (!vec) {
+        const unsigned grid = grid_for(
+            reinterpret_cast<const void*>(ddp_allreduce_adamw_cast_scalar), n);
+        ddp_allreduce_adamw_cast_scalar<<<grid, kThreads, 0, stream>>>(tab, nd, n, mean_out,
+                                                                      master, m, v, out, c, mo);
+        note_launch();
+        return cudaGetLastError();
+    }
+    const unsigned grid = grid_one_pass(n >> 2);
+#define SHARDSTEP_DDP_GO(K)                                                                   \
+    ddp_allreduce_adamw_cast_vec4<K><<<grid, kStepThreads, 0, stream>>>(tab, nd, n, mean_out, \
+                                                                        master, m, v, out, c, mo)
+    switch (nd) {
+        case 1: SHARDSTEP_DDP_GO(1); break;
+        case 2: SHARDSTEP_DDP_GO(2); break;
+        case 3: SHARDSTEP_DDP_GO(3); break;
+        case 4: SHARDSTEP_DDP_GO(4); break;
+        case 5: case 7: SHARDSTEP_DDP_GO(-8); break;
+        case 6: SHARDSTEP_DDP_GO(6); break;
+        case 8: SHARDSTEP_DDP_GO(8); break;
+        case 12: SHARDSTEP_DDP_GO(12); break;
+        case 16: SHARDSTEP_DDP_GO(16); break;
+        default: SHARDSTEP_DDP_GO(kRuntimeND); break;
+    }
+#undef SHARDSTEP_DDP_GO
+    note_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_mean_division_check(const MeanOp& mo, unsigned long long* mismatches,
+                                       unsigned int* first_bad, cudaStream_t stream) {
+    const unsigned grid = static_cast<unsigned>(device_sms()) * 8u;
+    mean_division_check<<<grid, kThreads, 0, stream>>>(mo, mismatches, first_bad);
     note_launch();
     return cudaGetLastError();
 }

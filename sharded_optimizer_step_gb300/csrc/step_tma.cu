@@ -21,10 +21,17 @@
 // of 12 KB for an accumulation), at least 2 and at most 16, rounded down to
 // one of the instantiated counts 2, 3, 4, 6, 8, 12, 16.
 //
-// Every wait is bounded (about two seconds of %globaltimer).  A wait that
-// runs out sets a bit in the device status word (shardstep_device_status),
-// the producer then waits, again bounded, for the copies it already issued,
-// and the CTA returns.  Nothing here spins on another CTA or on the host.
+// Every wait is bounded (by default about two seconds of %globaltimer; a
+// process-wide setting passed to each launch, shardstep_set_tma_wait_ns).  A
+// wait that runs out sets a bit in the device status word
+// (shardstep_device_status) and the waiting warp returns.  No CTA exits
+// while a bulk copy it issued may still be writing its shared memory: before
+// it returns, on every path, the producer lane waits for the copies of the
+// last tiles it issued (the earlier ones were consumed, so they landed).
+// That drain waits on copies from validated, in-bounds global memory, which
+// always complete; its own limit (kDrainNs, two seconds) is fixed, so a short
+// watchdog setting never cuts it short.  Nothing here spins on another CTA
+// or on the host.
 #include <atomic>
 
 #include "common.cuh"
@@ -48,13 +55,15 @@ constexpr size_t kTargetInflight = 128 * 1024;
 constexpr int kConsumerWarps = 16;
 constexpr int kConsumers = kConsumerWarps * 32;   // 512: 4 elements each per tile
 constexpr int kTmaThreads = kConsumers + 32;      // + the producer warp
-constexpr unsigned long long kWaitNs = 2000000000ull;
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;
+constexpr unsigned long long kDrainNs = 2000000000ull;
 constexpr size_t kBarrierBytes = 2 * kMaxStages * sizeof(uint64_t);
 // Left for the kernels' static shared memory (the step scalars' broadcast).
 constexpr size_t kStaticSmemReserve = 1024;
 
 constexpr unsigned kStatusConsumerTimeout = 1u;
 constexpr unsigned kStatusProducerTimeout = 2u;
+constexpr unsigned kStatusDrainTimeout = 4u;
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -86,12 +95,36 @@ __device__ __forceinline__ unsigned long long now_ns() {
     asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
     return t;
 }
-// Waits for the phase of `parity` to complete; false after kWaitNs.
-__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity) {
+// Non-blocking test of the phase of `parity`.
+__device__ __forceinline__ bool mbar_test_now(uint64_t* b, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(smem_addr(b)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+// Limits below this are a test control: their waits poll without blocking
+// and read the clock after every poll, so that they run out even when each
+// blocking poll would have lasted until the copy landed.
+constexpr unsigned long long kShortWaitNs = 1000000ull;
+// Waits for the phase of `parity` to complete; false after limit_ns.  The
+// usual limit polls with try_wait, which suspends the thread until the
+// phase completes or a hardware time slice ends, and reads the clock every
+// 256 polls.
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity,
+                                          unsigned long long limit_ns) {
     const unsigned long long t0 = now_ns();
+    if (limit_ns < kShortWaitNs) {
+        while (!mbar_test_now(b, parity))
+            if (now_ns() - t0 > limit_ns) return false;
+        return true;
+    }
     for (uint32_t k = 1;; ++k) {
         if (mbar_test(b, parity)) return true;
-        if ((k & 255u) == 0 && now_ns() - t0 > kWaitNs) return false;
+        if ((k & 255u) == 0 && now_ns() - t0 > limit_ns) return false;
     }
 }
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -197,7 +230,8 @@ static_assert(kConsumers * 4 == kTile, "one group of 4 elements per consumer thr
 // the same kernel issued 24% more instructions and ran 1.4% slower (5.15 vs
 // 5.08 ms for the N_d = 8 step over 842M elements).
 template <class Op, int NST>
-__device__ __forceinline__ void staged_body(const Op& op, int64_t n) {
+__device__ __forceinline__ void staged_body(const Op& op, int64_t n,
+                                            unsigned long long wait_ns) {
     constexpr int nst = NST;
     if (op.skipped()) return;
     typename Op::State state = op.init();
@@ -226,7 +260,7 @@ __device__ __forceinline__ void staged_body(const Op& op, int64_t n) {
         uint32_t use = 0;
         bool ok = true;
         for (; j < my_tiles; ++j) {
-            if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1u)) {
+            if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1u, wait_ns)) {
                 ok = false;
                 break;
             }
@@ -239,13 +273,17 @@ __device__ __forceinline__ void staged_body(const Op& op, int64_t n) {
                 ++use;
             }
         }
-        if (!ok) {
-            atomicOr(&g_device_status, kStatusProducerTimeout);
-            // the copies already issued land in this CTA's shared memory:
-            // wait for them (bounded) before the CTA may exit
-            for (int64_t k = j > nst ? j - nst : 0; k < j; ++k)
-                mbar_wait(&full[k % nst], static_cast<uint32_t>(k / nst) & 1u);
-        }
+        if (!ok) atomicOr(&g_device_status, kStatusProducerTimeout);
+        // Tiles 0..j-1 were issued.  A stage was refilled only after its
+        // consumers released it, so every tile before the last nst has
+        // landed; the last nst (or fewer) land in this CTA's shared memory
+        // and are waited for here, whether or not the consumers are still
+        // there to see them, before the CTA may exit.
+        bool drained = true;
+        for (int64_t k = j > nst ? j - nst : 0; k < j; ++k)
+            drained = mbar_wait(&full[k % nst], static_cast<uint32_t>(k / nst) & 1u, kDrainNs) &&
+                      drained;
+        if (!drained) atomicOr(&g_device_status, kStatusDrainTimeout);
         return;
     }
 
@@ -256,7 +294,7 @@ __device__ __forceinline__ void staged_body(const Op& op, int64_t n) {
     int s = 0;
     uint32_t use = 0;
     for (int64_t j = 0; j < my_tiles; ++j) {
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[s], use & 1u))) {
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[s], use & 1u, wait_ns))) {
             if (lane == 0) atomicOr(&g_device_status, kStatusConsumerTimeout);
             return;
         }
@@ -280,9 +318,10 @@ __device__ __forceinline__ void staged_body(const Op& op, int64_t n) {
 // holds for whatever runs after the last launch.  Both are no-ops for an
 // ordinary launch.
 template <class Op, int NST>
-__global__ void __launch_bounds__(kTmaThreads, 1) staged_stream(const Op op, int64_t n) {
+__global__ void __launch_bounds__(kTmaThreads, 1)
+    staged_stream(const Op op, int64_t n, unsigned long long wait_ns) {
     pdl_trigger();
-    staged_body<Op, NST>(op, n);
+    staged_body<Op, NST>(op, n, wait_ns);
     pdl_wait();
 }
 
@@ -437,10 +476,14 @@ struct CheckOp {
     struct State {
         MeanOp mo;
         bool bad;
+        bool bits;   // fp16 slices decided on their bits (f16_check_on_bits)
     };
     static constexpr uint32_t gsz = grad_bytes<GT>();
     __device__ bool skipped() const { return false; }
-    __device__ State init() const { return State{resolve_scale(mo), false}; }
+    __device__ State init() const {
+        const MeanOp m = resolve_scale(mo);
+        return State{m, false, GT == kGradF16 && f16_check_on_bits(m)};
+    }
     __host__ __device__ uint32_t stage_bytes() const {
         return static_cast<uint32_t>(nd) * kTile * gsz;
     }
@@ -451,12 +494,24 @@ struct CheckOp {
                       n * gsz, bar);
     }
     __device__ void consume(const uint8_t* st, int64_t, int e, State& s) const {
+        if (GT == kGradF16 && s.bits) {
+            for (int q = 0; q < nd; ++q) {
+                const uint2 r = *reinterpret_cast<const uint2*>(st + q * (kTile * gsz) + e * gsz);
+                s.bad |= f16x2_nonfinite(r.x) | f16x2_nonfinite(r.y);
+            }
+            return;
+        }
         float g[4];
         reduce4_smem<GT>(st, nd, s.mo.group, e, g);
 #pragma unroll
         for (int k = 0; k < 4; ++k) s.bad |= not_finite(mean_of(g[k], s.mo));
     }
     __device__ void tail(int64_t j, State& s) const {
+        if (GT == kGradF16 && s.bits) {
+            for (int q = 0; q < nd; ++q)
+                s.bad |= f16_nonfinite(static_cast<const uint16_t*>(tab.p[q])[j]);
+            return;
+        }
         s.bad |= not_finite(mean_of(reduce1_global<GT>(tab, nd, s.mo.group, j), s.mo));
     }
     __device__ void finish(State& s, int lane) const {
@@ -467,6 +522,7 @@ struct CheckOp {
 // --------------------------------------------------------------- launch
 
 std::atomic<int> g_stage_limit{0};  // 0: about kTargetInflight bytes of stages
+std::atomic<unsigned long long> g_wait_ns{kDefaultWaitNs};
 
 // The stage counts instantiated; a launch takes the largest one not above
 // what it asks for.
@@ -503,11 +559,13 @@ cudaError_t launch_stages(const Op& op, int64_t n, cudaStream_t stream, bool pdl
     int64_t grid = device_sms();
     if (grid > ntiles) grid = ntiles;
     if (grid < 1) grid = 1;
+    const unsigned long long wait_ns = g_wait_ns.load(std::memory_order_relaxed);
     if (pdl) {
         e = launch_dependent(staged_stream<Op, NST>, dim3(static_cast<unsigned>(grid)),
-                             dim3(kTmaThreads), smem, stream, op, n);
+                             dim3(kTmaThreads), smem, stream, op, n, wait_ns);
     } else {
-        staged_stream<Op, NST><<<static_cast<unsigned>(grid), kTmaThreads, smem, stream>>>(op, n);
+        staged_stream<Op, NST><<<static_cast<unsigned>(grid), kTmaThreads, smem, stream>>>(
+            op, n, wait_ns);
         e = cudaGetLastError();
     }
     note_launch();
@@ -545,6 +603,11 @@ bool tma_reduce_fits(int nd, int grad_type) {
 }
 
 int set_tma_stage_limit(int stages) { return g_stage_limit.exchange(stages); }
+
+int64_t set_tma_wait_ns(int64_t ns) {
+    const unsigned long long v = ns == 0 ? kDefaultWaitNs : static_cast<unsigned long long>(ns);
+    return static_cast<int64_t>(g_wait_ns.exchange(v));
+}
 
 cudaError_t launch_rs_adamw_cast_tma(const PtrTable& tab, int nd, int grad_type, int64_t S,
                                      float* master, float* m, float* v, uint16_t* out,

@@ -17,6 +17,7 @@ import torch
 
 from . import (AdamW, AdamWState, fsdp_accumulate_rs_avg_adamw_cast, fsdp_ag_unpack,
                fsdp_hybrid_rs_avg_adamw_cast, fsdp_layout, fsdp_rs_avg_adamw_cast,
+               fsdp_shard_pieces,
                fsdp_state_accumulate_rs_avg_adamw_cast, fsdp_state_rs_avg_adamw_cast,
                fsdp_views)
 
@@ -59,6 +60,20 @@ class RankShardOptimizer:
     def unit_slice(self, buf, u):
         """This rank's piece of unit u inside a rank-shard buffer."""
         return buf[self.starts[u]:self.starts[u] + self.layouts[u].shard]
+
+    def rank_pieces(self):
+        """Where each original tensor's piece sits in this rank's buffers:
+        a list of (unit, tensor, position in the rank buffer, first element
+        within the tensor, length), one entry per piece the rank holds (the
+        library's FlatParameter layout).  Positions not covered are the
+        units' padding."""
+        out = []
+        for u, shapes in enumerate(self.unit_shapes):
+            pieces = fsdp_shard_pieces([_numel(s) for s in shapes], self.F, self.rank)
+            for t, (pos, tpos, cnt) in enumerate(pieces):
+                if cnt:
+                    out.append((u, t, self.starts[u] + pos, tpos, cnt))
+        return out
 
     def step(self, stream=None):
         """Reduce-scatter average + AdamW + bf16 cast over the whole rank shard

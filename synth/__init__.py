@@ -222,3 +222,34 @@ def dev_fill(st: Stream, tensor, start: int = 0) -> None:
         raise TypeError(tensor.dtype)
     if rc != 0:
         raise RuntimeError("synthetic fill kernel failed to launch")
+
+
+# ------------------------------------------------------- ranges of streams
+
+def dev_fill_pieces(tensor, pieces, stream_of) -> None:
+    """Fill ranges of a contiguous CUDA tensor from several streams:
+    ``pieces`` lists (u, t, pos, start, count), and tensor[pos:pos + count]
+    receives elements start..start+count-1 of ``stream_of(u, t)``.  Where the
+    ranges come from (a FlatParameter layout) is the caller's business;
+    positions no piece covers are left as they are."""
+    for u, t, pos, start, count in pieces:
+        if count:
+            dev_fill(stream_of(u, t), tensor[pos:pos + count], start)
+
+
+def host_gather_sources(units, tensors, index, stream_of, dtype: str) -> np.ndarray:
+    """Element index[i] of ``stream_of(units[i], tensors[i])`` for every i, as
+    uint16 (bf16 / fp16 bits) or float32; zero where tensors[i] < 0 (a
+    position that holds no tensor element, e.g. padding)."""
+    units = np.asarray(units, dtype=np.int64)
+    tensors = np.asarray(tensors, dtype=np.int64)
+    index = np.asarray(index, dtype=np.int64)
+    out = np.zeros(index.size, dtype=np.float32 if dtype == "f32" else np.uint16)
+    live = tensors >= 0
+    if live.any():
+        keys = np.unique(np.stack([units[live], tensors[live]], axis=1), axis=0)
+        for u, t in keys:
+            sel = np.nonzero(live & (units == u) & (tensors == t))[0]
+            out[sel] = host_gather(stream_of(int(u), int(t)), index[sel], dtype)
+    return out
+

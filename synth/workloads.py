@@ -1,15 +1,19 @@
 """Synthetic workloads: model-shaped FSDP units and the seeded streams their
 inputs come from.  Shapes only -- no weights, no data set.
 
-Each workload is a list of FSDP units (one FlatParameter each), the number of
-emulated data-parallel ranks N_d, micro-batches M and optimizer steps.  The
-inputs are:
-  * rank q's micro-batch j gradient of unit u at step t: bf16, approximately
-    N(0, grad_sigma), optionally with a fraction of elements scaled x100,
-    element index = position in the unit's flat (padded) buffer;
-  * the fp32 master weights of unit u: approximately N(0, master_sigma);
+Each workload is a list of FSDP units (one FlatParameter each) given as the
+shapes of their tensors, the number of emulated data-parallel ranks N_d,
+micro-batches M and optimizer steps.  Every input value is addressed by the
+tensor it belongs to and its row-major index within that tensor:
+  * rank q's micro-batch j gradient of tensor t of unit u at step t_s: bf16,
+    approximately N(0, grad_sigma), optionally with a fraction of elements
+    scaled x100;
+  * the fp32 master weights of tensor t of unit u: approximately
+    N(0, master_sigma);
   * moments start at zero.
-Padding positions (past the unit's last tensor) are zero in every input.
+Where an element sits in a FlatParameter, a shard or a rank's buffer (and
+the zero padding) is the business of the layout -- the library's on the GPU
+side, the oracle's on the CPU side -- never of this module.
 """
 from __future__ import annotations
 
@@ -52,37 +56,34 @@ class Workload:
             out.append(n)
         return out
 
-    def unit_total(self, u):
-        return sum(self.unit_numels(u))
-
-    def unit_padded(self, u):
-        T = self.unit_total(u)
-        return -(-T // self.F) * self.F
-
-    def unit_shard(self, u):
-        return self.unit_padded(u) // self.F
-
     @property
     def psi(self):
-        return sum(self.unit_total(u) for u in range(len(self.units)))
+        return sum(sum(self.unit_numels(u)) for u in range(len(self.units)))
 
     # ---------------------------------------------------------- streams
-    def grad_stream(self, step: int, rank: int, micro: int, unit: int):
-        return normal_stream(self.seed, (self.cfg_id, KIND_GRAD, step, rank, micro, unit),
+    def grad_stream(self, step: int, rank: int, micro: int, unit: int, tensor: int):
+        return normal_stream(self.seed, (self.cfg_id, KIND_GRAD, step, rank, micro, unit, tensor),
                              self.grad_sigma, self.outlier_p, self.outlier_scale)
 
-    def master_stream(self, unit: int):
-        return normal_stream(self.seed, (self.cfg_id, KIND_MASTER, 0, 0, 0, unit),
+    def master_stream(self, unit: int, tensor: int):
+        return normal_stream(self.seed, (self.cfg_id, KIND_MASTER, 0, 0, 0, unit, tensor),
                              self.master_sigma)
 
     def peer_shard_stream(self, step: int, rank: int, unit: int):
-        """bf16 parameter shard of another rank, for the all-gather input."""
+        """bf16 parameter shard of another rank (a flat buffer of the shard's
+        length), for the all-gather input."""
         return normal_stream(self.seed, (self.cfg_id, KIND_SHARD_BF16, step, rank, 0, unit),
                              self.master_sigma)
 
 
 def _llama_layer(h, ffn):
     return [(h, h)] * 4 + [(ffn, h), (ffn, h), (h, ffn), (h,), (h,)]
+
+
+def _gpt2_units():
+    h, f, v, ctx = 768, 3072, 50257, 1024
+    block = [(h, 3 * h), (3 * h,), (h, h), (h,), (h, f), (f,), (f, h), (h,), (h,), (h,), (h,), (h,)]
+    return [list(block) for _ in range(12)] + [[(v, h), (ctx, h), (h,), (h,)]]
 
 
 def unit_9m() -> Workload:
@@ -94,10 +95,14 @@ def unit_9m() -> Workload:
 def gpt2_small() -> Workload:
     """GPT-2 small shape: 12 block units (qkv, proj, fc, proj with biases and
     two LayerNorms) and one embedding unit (wte, wpe, ln_f; tied head)."""
-    h, f, v, ctx = 768, 3072, 50257, 1024
-    block = [(h, 3 * h), (3 * h,), (h, h), (h,), (h, f), (f,), (f, h), (h,), (h,), (h,), (h,), (h,)]
-    units = [list(block) for _ in range(12)] + [[(v, h), (ctx, h), (h,), (h,)]]
-    return Workload("gpt2_small_nd8", 2, units, nd=8, micro=1, steps=10)
+    return Workload("gpt2_small_nd8", 2, _gpt2_units(), nd=8, micro=1, steps=10)
+
+
+def gpt2_small_nd7() -> Workload:
+    """The GPT-2 small units over N_d = 7 ranks: every unit's length is not a
+    multiple of 7 (blocks of 7,087,872 elements, embedding unit of
+    39,385,344), so every unit carries padding."""
+    return Workload("gpt2_small_nd7", 7, _gpt2_units(), nd=7, micro=1, steps=3)
 
 
 def llama_1b() -> Workload:
@@ -141,84 +146,5 @@ def ddp_sweep() -> Workload:
                     extra={"caps_mib": [1, 4, 25, 64, 256]})
 
 
-ALL = {w().name: w for w in (unit_9m, gpt2_small, llama_1b, llama_7b_rank_view,
+ALL = {w().name: w for w in (unit_9m, gpt2_small, gpt2_small_nd7, llama_1b, llama_7b_rank_view,
                                llama_7b_hybrid_view, ddp_sweep)}
-
-
-# ------------------------------------------------- one rank's shard of all units
-# A rank keeps its shard of every unit back to back: shard index i of the
-# rank's concatenated shard belongs to unit u at local position i - start_u,
-# which is element r*S_u + (i - start_u) of that unit's flat buffer (r is the
-# shard index: the rank itself under full sharding, its position in the group
-# under hybrid sharding).
-
-def rank_shard_index(w: Workload):
-    """[(unit, start in the rank's concatenated shard, S_u)] and the total."""
-    out, pos = [], 0
-    for u in range(len(w.units)):
-        s = w.unit_shard(u)
-        out.append((u, pos, s))
-        pos += s
-    return out, pos
-
-
-def _split_by_unit(w: Workload, idx):
-    import numpy as np
-    parts, total = rank_shard_index(w)
-    idx = np.asarray(idx, dtype=np.int64)
-    for u, start, s in parts:
-        sel = np.nonzero((idx >= start) & (idx < start + s))[0]
-        if sel.size:
-            yield u, sel, idx[sel] - start
-
-
-def host_gather_rank_grad(w: Workload, step: int, rank: int, q: int, micro: int, idx, dtype="bf16"):
-    """Rank q's gradient at positions idx of rank `rank`'s concatenated shard
-    (zero on padding)."""
-    import numpy as np
-    from . import host_gather
-    out = np.zeros(len(idx), dtype=np.uint16 if dtype == "bf16" else np.float32)
-    for u, sel, local in _split_by_unit(w, idx):
-        flat = rank * w.unit_shard(u) + local
-        vals = host_gather(w.grad_stream(step, q, micro, u), flat, dtype)
-        vals[flat >= w.unit_total(u)] = 0
-        out[sel] = vals
-    return out
-
-
-def host_gather_rank_master(w: Workload, rank: int, idx):
-    import numpy as np
-    from . import host_gather
-    out = np.zeros(len(idx), dtype=np.float32)
-    for u, sel, local in _split_by_unit(w, idx):
-        flat = rank * w.unit_shard(u) + local
-        vals = host_gather(w.master_stream(u), flat, "f32")
-        vals[flat >= w.unit_total(u)] = 0
-        out[sel] = vals
-    return out
-
-
-def dev_fill_rank_grad(w: Workload, step: int, rank: int, q: int, micro: int, buf) -> None:
-    """Fill a CUDA bf16 tensor holding rank q's contribution to rank `rank`'s
-    concatenated shard (zero on padding)."""
-    from . import dev_fill
-    parts, total = rank_shard_index(w)
-    assert buf.numel() == total
-    for u, start, s in parts:
-        seg = buf[start:start + s]
-        dev_fill(w.grad_stream(step, q, micro, u), seg, rank * s)
-        T = w.unit_total(u)
-        if (rank + 1) * s > T:
-            seg[max(0, T - rank * s):].zero_()
-
-
-def dev_fill_rank_master(w: Workload, rank: int, buf) -> None:
-    from . import dev_fill
-    parts, total = rank_shard_index(w)
-    assert buf.numel() == total
-    for u, start, s in parts:
-        seg = buf[start:start + s]
-        dev_fill(w.master_stream(u), seg, rank * s)
-        T = w.unit_total(u)
-        if (rank + 1) * s > T:
-            seg[max(0, T - rank * s):].zero_()

@@ -337,3 +337,40 @@ def test_adamw_state_layout_and_validation():
     assert "state is NULL" in L.shardstep_last_error().decode()
     assert L.fsdp_state_rs_avg_adamw_cast(ptrs, 0, 4, 3, 16, None, None, None, None,
                                           ctypes.c_void_p(4096), None) < 0
+
+
+def test_shard_pieces_place_every_element_like_the_oracle_pack():
+    """fsdp_shard_pieces against the oracle's FlatParameter, by element
+    tracking: the piece of tensor t in rank r's shard holds exactly tensor t's
+    elements tensor_lo.., the pieces of a shard do not overlap, and what no
+    piece covers is the zero padding."""
+    rnd = random.Random(3)
+    for _ in range(300):
+        nd = rnd.randint(1, 7)
+        numels = [rnd.randint(0, 12) for _ in range(rnd.randint(0, 5))]
+        tensors = [(t + 1) * 1000.0 + np.arange(n, dtype=np.float64) for t, n in enumerate(numels)]
+        flat, lay = oracle.flat_pack(tensors, nd) if numels else (np.zeros(0), oracle.layout([], nd))
+        for r in range(nd):
+            shard = flat[r * lay.shard:(r + 1) * lay.shard]
+            covered = np.zeros(lay.shard, bool)
+            pieces = ss.fsdp_shard_pieces(numels, nd, r)
+            assert len(pieces) == len(numels)
+            for t, (slo, tlo, cnt) in enumerate(pieces):
+                if cnt == 0:
+                    assert (slo, tlo) == (0, 0)
+                    continue
+                assert np.array_equal(shard[slo:slo + cnt], tensors[t][tlo:tlo + cnt])
+                assert not covered[slo:slo + cnt].any()
+                covered[slo:slo + cnt] = True
+            assert not shard[~covered].any()
+            assert covered.sum() == max(0, min(lay.total, (r + 1) * lay.shard) - r * lay.shard)
+
+
+def test_shard_pieces_of_the_worked_example_and_bad_arguments():
+    # [P1] FSDP1 figure: three (4,2) weights on two ranks; rank 0 holds W1 and
+    # W2's first 4 elements, rank 1 the rest of W2 and all of W3
+    assert ss.fsdp_shard_pieces([8, 8, 8], 2, 0) == [(0, 0, 8), (8, 0, 4), (0, 0, 0)]
+    assert ss.fsdp_shard_pieces([8, 8, 8], 2, 1) == [(0, 0, 0), (0, 4, 4), (4, 0, 8)]
+    for nd, rank in ((2, 2), (2, -1), (0, 0)):
+        with pytest.raises(ss.ShardstepError):
+            ss.fsdp_shard_pieces([8, 8, 8], nd, rank)

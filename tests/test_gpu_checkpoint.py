@@ -12,6 +12,7 @@ from oracle import checkpoint as ock
 from sharded_optimizer_step_gb300 import checkpoint as ck
 from sharded_optimizer_step_gb300.engine import RankShardOptimizer
 from synth import workloads as W
+from tests._views import gpu_fill_rank
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -33,14 +34,11 @@ def _opts(w, nd, F=0):
 
 def _train(w, opts, steps):
     for o in opts:
-        w2 = W.Workload(w.name, w.cfg_id, w.units, nd=o.nd, shard_group=o.F if o.F != o.nd else 0)
-        W.dev_fill_rank_master(w2, o.rank, o.master)
+        gpu_fill_rank(o, o.master, w.master_stream)
     for t in range(1, steps + 1):
         for o in opts:
-            w2 = W.Workload(w.name, w.cfg_id, w.units, nd=o.nd,
-                            shard_group=o.F if o.F != o.nd else 0)
             for q in range(o.nd):
-                W.dev_fill_rank_grad(w2, t, o.rank, q, 0, o.grad_in[q])
+                gpu_fill_rank(o, o.grad_in[q], lambda u, k, q=q: w.grad_stream(t, q, 0, u, k))
             o.step()
     torch.cuda.synchronize()
 

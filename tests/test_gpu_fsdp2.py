@@ -142,12 +142,12 @@ def test_fsdp2_llama_layer_group_full_size():
     grads = [[torch.empty(s, dtype=torch.bfloat16, device=DEV) for s in shapes] for _ in range(nd)]
     for q in range(nd):
         for t, g in enumerate(grads[q]):
-            synth.dev_fill(w.grad_stream(1, q, 0, 100 + t), g)
+            synth.dev_fill(w.grad_stream(1, q, 0, 100, t), g)
     cc = [ss.fsdp2_chunk_cat(grads[q], nd) for q in range(nd)]
     rng = np.random.default_rng(5)
     masters = [torch.empty(s, dtype=torch.float32, device=DEV) for s in shapes]
     for t, mt in enumerate(masters):
-        synth.dev_fill(w.master_stream(100 + t), mt)
+        synth.dev_fill(w.master_stream(100, t), mt)
     local_master = ss.fsdp2_chunk_cat(masters, nd)
     outs = []
     for r in range(nd):
@@ -166,9 +166,9 @@ def test_fsdp2_llama_layer_group_full_size():
         row = int(np.prod(s[1:]))
         cols = np.unique(np.concatenate([rng.integers(0, row, 16), [0, row - 1]]))
         flat_idx = (rows[:, None] * row + cols[None, :]).reshape(-1)
-        gq = [synth.host_gather(w.grad_stream(1, q, 0, 100 + t), flat_idx, "bf16")
+        gq = [synth.host_gather(w.grad_stream(1, q, 0, 100, t), flat_idx, "bf16")
               for q in range(nd)]
-        p0 = synth.host_gather(w.master_stream(100 + t), flat_idx, "f32")
+        p0 = synth.host_gather(w.master_stream(100, t), flat_idx, "f32")
         z = np.zeros(flat_idx.size, np.float32)
         _, _, _, ob = oracle.fsdp_shard_step(gq, 0, flat_idx.size, p0, z, z, HP, 1)
         got = _host(params[t].reshape(-1)[torch.from_numpy(flat_idx).to(DEV)])

@@ -651,8 +651,8 @@ def test_auto_path_names_the_kernel_it_launched():
     """The automatic choice, as shardstep_last_kernel reports it: the
     register-staged fused kernel at N_d = 8 and its up-to-8 form at 7, the
     TMA-staged one at N_d = 9, TMA-staged whenever forced; the all-reduce
-    and the check on their register kernels at the compiled counts and at
-    3, on the TMA-staged ones at 5 and 6."""
+    and the check on their register kernels at N_d = 1..8 (16-bit slices),
+    on the TMA-staged ones above 8."""
     S = 8192
     master = torch.zeros(S, device=DEV)
     m = torch.zeros(S, device=DEV)
@@ -678,18 +678,21 @@ def test_auto_path_names_the_kernel_it_launched():
         ss.fsdp_grad_accumulate(g[0], acc, 0.25, True)
         assert ss.last_kernel() == "accumulate_vec8 (register-staged)"
         # the bucket all-reduce and the check by N_d
+        g = g + [torch.zeros(S, dtype=torch.bfloat16, device=DEV) for _ in range(2)]
         out16 = torch.empty(S, dtype=torch.bfloat16, device=DEV)
-        for nd, want in [(3, "allreduce_avg_vec4<up to 8: 3> (register-staged)"),
+        for nd, want in [(3, "allreduce_avg_vec4<3> (register-staged)"),
                          (8, "allreduce_avg_vec4<8> (register-staged)"),
-                         (6, "staged_stream<MeanOutOp> (TMA-staged)")]:
-            ss.ddp_bucket_allreduce_avg(g[:nd] if nd <= 8 else g, [0, S], out16)
+                         (6, "allreduce_avg_vec4<6> (register-staged)"),
+                         (10, "staged_stream<MeanOutOp> (TMA-staged)")]:
+            ss.ddp_bucket_allreduce_avg(g[:nd], [0, S], out16)
             assert ss.last_kernel() == want, nd
         h = [x.to(torch.float16) for x in g]
         sc = ss.GradScaler(1.0, device=DEV)
         for nd, want in [(1, "nonfinite_check_vec4<1, f16> (register-staged)"),
-                         (3, "nonfinite_check_vec4<up to 8: 3, f16> (register-staged)"),
+                         (3, "nonfinite_check_vec4<3, f16> (register-staged)"),
                          (8, "nonfinite_check_vec4<8, f16> (register-staged)"),
-                         (5, "staged_stream<CheckOp<f16>> (TMA-staged)")]:
+                         (5, "nonfinite_check_vec4<5, f16> (register-staged)"),
+                         (10, "staged_stream<CheckOp<f16>> (TMA-staged)")]:
             sc.check(h[:nd])
             assert ss.last_kernel() == want, nd
         torch.cuda.synchronize()

@@ -12,8 +12,10 @@ import sharded_optimizer_step_gb300 as ss
 import synth
 from oracle import scaler as osc
 from oracle.numerics import AdamWConfig
+from sharded_optimizer_step_gb300.engine import RankShardOptimizer
 from synth import workloads as W
 from tests._cmp import assert_bits
+from tests._views import gpu_fill_rank, oracle_rank_total, oracle_rank_values
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -158,17 +160,19 @@ def test_llama_7b_rank_view_fp16_scaled_full_size():
     w = W.llama_7b_rank_view()
     r = 0
     scale = 65536.0
-    S = W.rank_shard_index(w)[1]
-    master = torch.empty(S, dtype=torch.float32, device=DEV)
-    W.dev_fill_rank_master(w, r, master)
+    opt = RankShardOptimizer(w.units, w.nd, r, ss.AdamW(), device=DEV, grad_dtype=torch.float16)
+    S = opt.shard_total
+    assert S == oracle_rank_total(w)
+    master = opt.master
+    gpu_fill_rank(opt, master, w.master_stream)
     m = torch.zeros(S, device=DEV)
     v = torch.zeros(S, device=DEV)
     out = torch.zeros(S, dtype=torch.bfloat16, device=DEV)
-    grads = [torch.empty(S, dtype=torch.float16, device=DEV) for _ in range(w.nd)]
+    grads = opt.grad_in
     sc = ss.GradScaler(init_scale=scale, device=DEV)
     rng = np.random.default_rng(4)
     idx = np.unique(np.concatenate([rng.integers(0, S, 100_000), [0, S - 1, 12345]]))
-    p = W.host_gather_rank_master(w, r, idx)
+    p = oracle_rank_values(w, r, idx, w.master_stream, "f32")
     mm = np.zeros(idx.size, np.float32)
     vv = np.zeros(idx.size, np.float32)
     ob = np.zeros(idx.size, np.uint16)
@@ -225,3 +229,30 @@ def test_check_finds_one_planted_value_anywhere(where, stages, path):
     want = osc.found_inf([(h, "f16") for h in hs], nd, 0, S, np.float32(1.0 / 512.0))
     torch.cuda.synchronize()
     assert bool(int(sc.found_inf.item())) == want == (where is not None)
+
+
+@pytest.mark.parametrize("nd", [3, 8, 9])
+@pytest.mark.parametrize("scale,plant", [(2.0 ** -120, None), (2.0 ** -120, "inf"),
+                                         (float("nan"), None), (float("inf"), None),
+                                         (float("inf"), "inf"), (2.0 ** -100, None),
+                                         (2.0 ** -100, "nan"), (1.0, "nan")])
+def test_check_at_extreme_scales(nd, scale, plant, path):
+    """The fp16 check decides on the input bits only where that is exact
+    (|1/scale| <= 2^100); a tiny scale makes finite fp16 means overflow once
+    unscaled, a NaN scale makes every mean NaN, an infinite scale makes every
+    finite mean zero (and inf * 0 NaN).  All against the oracle."""
+    S = 128 * 8 * 4 * 9 + 4 * 3 + 2
+    hs = [synth.host_fill(synth.normal_stream(nd, (88, q), 1.0), 0, S, "f16") for q in range(nd)]
+    for h in hs:
+        h[1000] = 0x7AFF          # 57312, the same large value in every rank
+    if plant is not None:
+        hs[nd - 1][S - 1000] = 0x7C00 if plant == "inf" else 0x7E01
+    sc = ss.GradScaler(init_scale=1.0, device=DEV)
+    sc.scale.fill_(scale)
+    sc.check([_dev(h, "f16") for h in hs])
+    inv = np.float32(1.0) / np.float32(scale)
+    want = osc.found_inf([(h, "f16") for h in hs], nd, 0, S, inv)
+    torch.cuda.synchronize()
+    assert bool(int(sc.found_inf.item())) == want
+    if scale == 2.0 ** -120 or np.isnan(scale):
+        assert want                   # the shortcut's condition fails and the result shows it

@@ -1,10 +1,16 @@
-"""GPU parity on the five model-shaped workloads at full size.
+"""GPU parity on the model-shaped workloads at full size.
 
 The 9.4M-parameter unit (N_d = 4, M = 4) is compared element by element with
 the oracle.  The larger workloads run in full on the GPU and are checked on
 sampled outputs that the oracle computes one by one from the same seeded
 inputs (every step, every micro-batch, every rank), plus properties that hold
-at any size.  The Llama-7B rank view runs in the launch configuration the
+at any size.  The two sides lay the FlatParameters out independently: the
+GPU side packs each unit from its per-tensor inputs with ``fsdp_flat_pack``,
+takes the shards from ``fsdp_layout``, fills a rank's buffers at the places
+``fsdp_shard_pieces`` gives and reads the gathered tensors through
+``fsdp_views``; the oracle traces every sampled position back to its tensor
+element with its own layout.  GPT-2 small also runs at N_d = 7, where every
+unit is padded.  The Llama-7B rank view runs in the launch configuration the
 benchmark times: one fused launch over the rank's 842,301,952-element shard
 and one all-gather of a 202,383,360-parameter layer unit; so does the
 Llama-1B accumulation view (three accumulate launches over the 8
@@ -20,6 +26,7 @@ from oracle.numerics import AdamWConfig
 from sharded_optimizer_step_gb300.engine import RankShardOptimizer
 from synth import workloads as W
 from tests._cmp import assert_bf16, assert_bits, assert_f32
+from tests._views import gpu_fill_rank, oracle_rank_total, oracle_rank_values
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -52,6 +59,14 @@ def _sample(n, k, rng, extra=()):
     return np.array(sorted(idx), dtype=np.int64)
 
 
+def _gpu_pack(tensors, streams, nd, flat):
+    """Fill each device tensor of a unit from its stream and pack them with
+    the library into ``flat`` (its padding zeroed by the pack)."""
+    for x, st in zip(tensors, streams):
+        synth.dev_fill(st, x.view(-1))
+    ss.fsdp_flat_pack(tensors, nd, flat=flat)
+
+
 # --------------------------------------------------- 9.4M unit, every element
 
 def test_unit_9m_every_element():
@@ -61,12 +76,9 @@ def test_unit_9m_every_element():
     shapes = w.units[0]
     numels = w.unit_numels(0)
     # master weights: the unit's tensors packed into the fp32 FlatParameter
-    host_t, dev_t, off = [], [], 0
-    for n, s in zip(numels, shapes):
-        h = synth.host_fill(w.master_stream(0), off, n, "f32")
-        host_t.append(h.reshape(s))
-        dev_t.append(torch.from_numpy(h).to(DEV).view(s))
-        off += n
+    host_t = [synth.host_fill(w.master_stream(0, t), 0, n, "f32").reshape(s)
+              for t, (n, s) in enumerate(zip(numels, shapes))]
+    dev_t = [torch.from_numpy(h).to(DEV) for h in host_t]
     flat = ss.fsdp_flat_pack(dev_t, nd)
     want_flat, lay = oracle.flat_pack(host_t, nd)
     S, P = lay.shard, lay.padded
@@ -75,16 +87,18 @@ def test_unit_9m_every_element():
 
     accs, accs_h = [], []
     g = torch.empty(P, dtype=torch.bfloat16, device=DEV)
+    gt = [torch.empty(s, dtype=torch.bfloat16, device=DEV) for s in shapes]
     for q in range(nd):
         acc = torch.empty(P, dtype=torch.float32, device=DEV)
         micro_h = []
         for j in range(M):
-            st = w.grad_stream(1, q, j, 0)
-            synth.dev_fill(st, g)
-            micro_h.append(synth.host_fill(st, 0, P, "bf16"))
+            streams = [w.grad_stream(1, q, j, 0, t) for t in range(len(shapes))]
+            _gpu_pack(gt, streams, nd, g)
+            micro_h.append(oracle.flat_pack(
+                [synth.host_fill(st, 0, n, "bf16") for st, n in zip(streams, numels)], nd)[0])
             ss.fsdp_grad_accumulate(g, acc, float(np.float32(1.0 / M)), j == 0)
         torch.cuda.synchronize()
-        assert_bits(_host_bf16(g), micro_h[-1], "generator")
+        assert_bits(_host_bf16(g), micro_h[-1], "packed gradient")
         accs.append(acc)
         accs_h.append(oracle.grad_accumulate(micro_h, np.float32(1.0 / M)))
         assert_bits(acc.cpu().numpy(), accs_h[-1], f"accumulator rank {q}")
@@ -122,46 +136,54 @@ def test_unit_9m_every_element():
 # ------------------------------------- per-unit emulation of all N_d ranks
 
 def _run_all_ranks(w, sample_per_unit=1024, seed=0):
-    """Every rank of every unit, all steps; oracle on sampled shard positions.
-    Fused outputs land in per-rank shard buffers that the all-gather copies
-    into the unit's full flat buffer."""
+    """Every rank of every unit, all steps; oracle on sampled shard positions
+    (the last ones of every shard among them, so the padding of a padded
+    unit is sampled).  Each unit's inputs are packed on the GPU from its
+    per-tensor fills by the library; the fused outputs land in per-rank
+    shard buffers that the all-gather copies into the unit's full flat
+    buffer, whose tensor views are compared with the oracle."""
     hp, hpc = _hp(w)
     nd, M = w.nd, w.micro
     rng = np.random.default_rng(seed)
-    maxP = max(w.unit_padded(u) for u in range(len(w.units)))
+    glays = [ss.fsdp_layout(w.unit_numels(u), nd) for u in range(len(w.units))]
+    olays = [oracle.layout(w.unit_numels(u), nd) for u in range(len(w.units))]
+    maxP = max(g.padded for g in glays)
     g = torch.empty(maxP, dtype=torch.bfloat16, device=DEV)
     acc = [torch.empty(maxP, dtype=torch.float32 if M > 1 else torch.bfloat16, device=DEV)
            for _ in range(nd)]
     state = []
-    for u in range(len(w.units)):
-        S, P = w.unit_shard(u), w.unit_padded(u)
+    for u, shapes in enumerate(w.units):
+        glay, olay = glays[u], olays[u]
+        assert (glay.shard, glay.padded, glay.total) == (olay.shard, olay.padded, olay.total)
+        S, P = glay.shard, glay.padded
         master = torch.empty(P, dtype=torch.float32, device=DEV)
-        synth.dev_fill(w.master_stream(u), master)
-        if P > w.unit_total(u):
-            master[w.unit_total(u):].zero_()
+        mt = [torch.empty(s, dtype=torch.float32, device=DEV) for s in shapes]
+        _gpu_pack(mt, [w.master_stream(u, t) for t in range(len(shapes))], nd, master)
+        del mt
         ranks = []
         for r in range(nd):
             idx = _sample(S, sample_per_unit, rng)
-            flat_idx = r * S + idx
-            p0 = synth.host_gather(w.master_stream(u), flat_idx, "f32")
-            p0[flat_idx >= w.unit_total(u)] = 0
+            tt, kk = oracle.element_source(olay, r * olay.shard + idx)
+            p0 = synth.host_gather_sources(np.full(idx.size, u), tt, kk,
+                                           lambda uu, t: w.master_stream(uu, t), "f32")
             ranks.append(dict(master=master[r * S:(r + 1) * S], m=torch.zeros(S, device=DEV),
                               v=torch.zeros(S, device=DEV),
                               out=torch.empty(S, dtype=torch.bfloat16, device=DEV),
-                              idx=idx, p=p0, mm=np.zeros(idx.size, np.float32),
+                              idx=idx, tt=tt, kk=kk, p=p0, mm=np.zeros(idx.size, np.float32),
                               vv=np.zeros(idx.size, np.float32), ob=None))
         state.append(dict(S=S, P=P, ranks=ranks,
+                          gt=[torch.empty(s, dtype=torch.bfloat16, device=DEV) for s in shapes],
                           full=torch.empty(P, dtype=torch.bfloat16, device=DEV)))
 
     for t in range(1, w.steps + 1):
         for u, us in enumerate(state):
-            S, P, T = us["S"], us["P"], w.unit_total(u)
+            S, P = us["S"], us["P"]
+            nt = len(w.units[u])
             for q in range(nd):
                 for j in range(M):
                     dst = (g if M > 1 else acc[q])[:P]
-                    synth.dev_fill(w.grad_stream(t, q, j, u), dst)
-                    if P > T:
-                        dst[T:].zero_()
+                    _gpu_pack(us["gt"], [w.grad_stream(t, q, j, u, k) for k in range(nt)], nd,
+                              dst)
                     if M > 1:
                         ss.fsdp_grad_accumulate(dst, acc[q][:P], float(np.float32(1.0 / M)),
                                                 j == 0)
@@ -171,22 +193,22 @@ def _run_all_ranks(w, sample_per_unit=1024, seed=0):
             ss.fsdp_ag_unpack([rs["out"] for rs in us["ranks"]], us["full"])
             # oracle on the sampled positions of every rank
             for r, rs in enumerate(us["ranks"]):
-                flat_idx = r * S + rs["idx"]
+                uu = np.full(rs["idx"].size, u)
                 contribs = []
                 for q in range(nd):
-                    micro = []
-                    for j in range(M):
-                        gv = synth.host_gather(w.grad_stream(t, q, j, u), flat_idx, "bf16")
-                        gv[flat_idx >= T] = 0
-                        micro.append(gv)
+                    micro = [synth.host_gather_sources(
+                        uu, rs["tt"], rs["kk"],
+                        lambda a, b, q=q, j=j: w.grad_stream(t, q, j, a, b), "bf16")
+                        for j in range(M)]
                     contribs.append(oracle.grad_accumulate(micro, np.float32(1.0 / M))
                                     if M > 1 else micro[0])
                 rs["p"], rs["mm"], rs["vv"], rs["ob"] = oracle.fsdp_shard_step(
                     contribs, 0, rs["idx"].size, rs["p"], rs["mm"], rs["vv"], hp, t)
     torch.cuda.synchronize()
     for u, us in enumerate(state):
-        S = us["S"]
-        full_h = None
+        shapes = w.units[u]
+        views = ss.fsdp_views(us["full"], shapes, nd)
+        assert [tuple(x.shape) for x in views] == [tuple(s) for s in shapes]
         for r, rs in enumerate(us["ranks"]):
             it = torch.from_numpy(rs["idx"]).to(DEV)
             assert_f32(rs["master"][it].cpu().numpy(), rs["p"], f"unit {u} rank {r} master")
@@ -194,15 +216,28 @@ def _run_all_ranks(w, sample_per_unit=1024, seed=0):
             assert_bits(rs["m"][it].cpu().numpy(), rs["mm"], f"unit {u} rank {r} m")
             assert_bits(rs["v"][it].cpu().numpy(), rs["vv"], f"unit {u} rank {r} v")
             assert_bits(_host_bf16(rs["out"][it]), rs["ob"], f"unit {u} rank {r} bf16")
-            # the gathered buffer holds every rank's shard at its slot
-            assert torch.equal(us["full"][r * S:(r + 1) * S].view(torch.int16),
-                               rs["out"].view(torch.int16))
-            assert_bf16(_host_bf16(us["full"][r * S + it]), rs["ob"], "gathered")
-        del full_h
+            # the gathered tensors: each sampled element, found through the
+            # library's views, is the oracle's value of the tensor element
+            # the oracle's layout puts there
+            for k in np.unique(rs["tt"][rs["tt"] >= 0]):
+                sel = np.nonzero(rs["tt"] == k)[0]
+                got = _host_bf16(views[k].reshape(-1)[torch.from_numpy(rs["kk"][sel]).to(DEV)])
+                assert_bits(got, rs["ob"][sel], f"unit {u} rank {r} view {k}")
+            pad = np.nonzero(rs["tt"] < 0)[0]
+            assert not rs["ob"][pad].any() and not rs["p"][pad].any()
+        T = sum(w.unit_numels(u))
+        assert not us["full"][T:].view(torch.int16).any(), f"unit {u}: padding not zero"
 
 
 def test_gpt2_small_all_units_all_ranks():
     _run_all_ranks(W.gpt2_small(), sample_per_unit=512)
+
+
+def test_gpt2_small_nd7_every_unit_padded():
+    w = W.gpt2_small_nd7()
+    pads = [ss.fsdp_layout(w.unit_numels(u), w.nd) for u in range(len(w.units))]
+    assert [p.padded - p.total for p in pads] == [6] * 12 + [2]
+    _run_all_ranks(w, sample_per_unit=512)
 
 
 def test_llama_1b_all_units_all_ranks_with_accumulation_and_outliers():
@@ -216,22 +251,22 @@ def test_llama_7b_rank_view_as_benchmarked():
     hp, hpc = _hp(w)
     r = w.extra["rank"]
     opt = RankShardOptimizer(w.units, w.nd, r, hpc, device=DEV)
-    assert opt.shard_total == 842_301_952
-    W.dev_fill_rank_master(w, r, opt.master)
+    assert opt.shard_total == 842_301_952 == oracle_rank_total(w)
+    gpu_fill_rank(opt, opt.master, w.master_stream)
     rng = np.random.default_rng(7)
-    parts, total = W.rank_shard_index(w)
-    bounds = [s for _, s, _ in parts] + [s - 1 for _, s, _ in parts[1:]]
-    idx = _sample(total, 200_000, rng, extra=bounds)
-    p = W.host_gather_rank_master(w, r, idx)
+    bounds = opt.starts[1:] + [s - 1 for s in opt.starts[1:]]
+    idx = _sample(opt.shard_total, 200_000, rng, extra=bounds)
+    p = oracle_rank_values(w, r, idx, w.master_stream, "f32")
     m = np.zeros(idx.size, np.float32)
     v = np.zeros(idx.size, np.float32)
     for t in range(1, w.steps + 1):
         for q in range(w.nd):
-            W.dev_fill_rank_grad(w, t, r, q, 0, opt.grad_in[q])
+            gpu_fill_rank(opt, opt.grad_in[q], lambda u, k, q=q: w.grad_stream(t, q, 0, u, k))
         launches = ss.launch_count()
         opt.step()
         assert ss.launch_count() - launches == 1      # one fused launch over the shard
-        contribs = [W.host_gather_rank_grad(w, t, r, q, 0, idx) for q in range(w.nd)]
+        contribs = [oracle_rank_values(w, r, idx, lambda u, k, q=q: w.grad_stream(t, q, 0, u, k),
+                                       "bf16") for q in range(w.nd)]
         p, m, v, ob = oracle.fsdp_shard_step(contribs, 0, idx.size, p, m, v, hp, t)
     torch.cuda.synchronize()
     it = torch.from_numpy(idx).to(DEV)
@@ -243,7 +278,7 @@ def test_llama_7b_rank_view_as_benchmarked():
 
     # all-gather of one layer unit: the other ranks' shards are seeded inputs
     u = w.extra["ag_unit"]
-    S, P = w.unit_shard(u), w.unit_padded(u)
+    S, P = opt.layouts[u].shard, opt.layouts[u].padded
     assert P == 202_383_360
     peers = []
     for q in range(w.nd):
@@ -282,28 +317,29 @@ def test_llama_1b_rank_view_accumulation_as_benchmarked():
     opt.grad_in = [acc[q * S:(q + 1) * S] for q in range(nd)]
     micro = [torch.empty(nd * S, dtype=torch.bfloat16, device=DEV) for _ in range(M)]
     last = [micro[M - 1][q * S:(q + 1) * S] for q in range(nd)]
-    W.dev_fill_rank_master(w, r, opt.master)
+    gpu_fill_rank(opt, opt.master, w.master_stream)
     rng = np.random.default_rng(11)
-    parts, total = W.rank_shard_index(w)
-    assert total == S
-    bounds = [s for _, s, _ in parts] + [s - 1 for _, s, _ in parts[1:]]
+    assert oracle_rank_total(w) == S
+    bounds = opt.starts[1:] + [s - 1 for s in opt.starts[1:]]
     idx = _sample(S, 100_000, rng, extra=bounds)
-    p = W.host_gather_rank_master(w, r, idx)
+    p = oracle_rank_values(w, r, idx, w.master_stream, "f32")
     m = np.zeros(idx.size, np.float32)
     v = np.zeros(idx.size, np.float32)
     inv_m = np.float32(1.0 / M)
     for t in range(1, 4):
         for j in range(M):
             for q in range(nd):
-                W.dev_fill_rank_grad(w, t, r, q, j, micro[j][q * S:(q + 1) * S])
+                gpu_fill_rank(opt, micro[j][q * S:(q + 1) * S],
+                              lambda u, k, q=q, j=j: w.grad_stream(t, q, j, u, k))
         launches = ss.launch_count()
         for j in range(M - 1):
             ss.fsdp_grad_accumulate(micro[j], acc, float(inv_m), j == 0)
         opt.step_with_last_micro_batch(last, float(inv_m))
         assert ss.launch_count() - launches == M
         assert ss.last_kernel() == "accum_rs_adamw_cast_vec4<8> (register-staged)"
-        grads = [[W.host_gather_rank_grad(w, t, r, q, j, idx) for j in range(M)]
-                 for q in range(nd)]
+        grads = [[oracle_rank_values(w, r, idx,
+                                     lambda u, k, q=q, j=j: w.grad_stream(t, q, j, u, k), "bf16")
+                  for j in range(M)] for q in range(nd)]
         contribs = [oracle.grad_accumulate(grads[q], inv_m) for q in range(nd)]
         p, m, v, ob = oracle.fsdp_shard_step(contribs, 0, idx.size, p, m, v, hp, t)
     torch.cuda.synchronize()
@@ -331,7 +367,7 @@ def test_llama_7b_rank_view_every_kernel_and_the_graph_agree_everywhere():
     c = RankShardOptimizer(w.units, w.nd, r, hpc, device=DEV)
     b.grad_in = a.grad_in                 # one set of gradient buffers for all
     c.grad_in = a.grad_in
-    W.dev_fill_rank_master(w, r, a.master)
+    gpu_fill_rank(a, a.master, w.master_stream)
     b.master.copy_(a.master)
     c.master.copy_(a.master)
     c.device_step_state()
@@ -351,7 +387,7 @@ def test_llama_7b_rank_view_every_kernel_and_the_graph_agree_everywhere():
             c.step_on_device()
         for t in (1, 2):
             for q in range(w.nd):
-                W.dev_fill_rank_grad(w, t, r, q, 0, a.grad_in[q])
+                gpu_fill_rank(a, a.grad_in[q], lambda u, k, q=q: w.grad_stream(t, q, 0, u, k))
             ss.set_fused_path("auto")
             a.step()
             ss.set_fused_path("tma")
@@ -377,20 +413,21 @@ def test_llama_7b_hybrid_view_as_benchmarked():
     f = w.extra["rank"]
     opt = RankShardOptimizer(w.units, w.nd, f, hpc, device=DEV, shard_group=w.F)
     assert opt.shard_total == 842_301_952
-    W.dev_fill_rank_master(w, f, opt.master)
+    assert opt.shard_total == oracle_rank_total(w)
+    gpu_fill_rank(opt, opt.master, w.master_stream)
     rng = np.random.default_rng(11)
-    parts, total = W.rank_shard_index(w)
-    idx = _sample(total, 100_000, rng, extra=[s for _, s, _ in parts])
-    p = W.host_gather_rank_master(w, f, idx)
+    idx = _sample(opt.shard_total, 100_000, rng, extra=opt.starts)
+    p = oracle_rank_values(w, f, idx, w.master_stream, "f32")
     m = np.zeros(idx.size, np.float32)
     v = np.zeros(idx.size, np.float32)
     for t in (1, 2):
         for k in range(w.nd):
-            W.dev_fill_rank_grad(w, t, f, k, 0, opt.grad_in[k])
+            gpu_fill_rank(opt, opt.grad_in[k], lambda u, x, k=k: w.grad_stream(t, k, 0, u, x))
         launches = ss.launch_count()
         opt.step()
         assert ss.launch_count() - launches == 1
-        contribs = [W.host_gather_rank_grad(w, t, f, k, 0, idx) for k in range(w.nd)]
+        contribs = [oracle_rank_values(w, f, idx, lambda u, x, k=k: w.grad_stream(t, k, 0, u, x),
+                                       "bf16") for k in range(w.nd)]
         p, m, v, ob = oracle.hybrid_shard_step(contribs, w.F, 0, idx.size, p, m, v, hp, t)
     torch.cuda.synchronize()
     it = torch.from_numpy(idx).to(DEV)
@@ -400,7 +437,7 @@ def test_llama_7b_hybrid_view_as_benchmarked():
     assert_bits(_host_bf16(opt.params[it]), ob, "bf16")
     # all-gather inside the group of 8
     u = w.extra["ag_unit"]
-    S, P = w.unit_shard(u), w.unit_padded(u)
+    S, P = opt.layouts[u].shard, opt.layouts[u].padded
     peers = [torch.empty(S, dtype=torch.bfloat16, device=DEV) for _ in range(w.F)]
     for q in range(1, w.F):
         synth.dev_fill(w.peer_shard_stream(2, q, u), peers[q])
@@ -431,7 +468,7 @@ def test_ddp_bucket_sweep_full_size():
         # values do not depend on where the plan puts the parameter
         for q in range(nd):
             for i, n in enumerate(numels):
-                synth.dev_fill(w.grad_stream(1, q, 0, i), grads[q][off[i]:off[i] + n])
+                synth.dev_fill(w.grad_stream(1, q, 0, 0, i), grads[q][off[i]:off[i] + n])
         out = torch.empty(total, dtype=torch.bfloat16, device=DEV)
         before = ss.launch_count()
         ss.ddp_bucket_allreduce_avg(grads, boff, out)
@@ -441,7 +478,7 @@ def test_ddp_bucket_sweep_full_size():
         # oracle on sampled elements of sampled parameters
         for i in rng.choice(len(numels), size=12, replace=False):
             loc = _sample(numels[i], 512, rng)
-            gq = [synth.host_gather(w.grad_stream(1, q, 0, int(i)), loc, "bf16")
+            gq = [synth.host_gather(w.grad_stream(1, q, 0, 0, int(i)), loc, "bf16")
                   for q in range(nd)]
             want = oracle.bucket_allreduce_avg(gq, [0, loc.size])
             got = _host_bf16(out[off[i] + torch.from_numpy(loc).to(DEV)])
@@ -449,19 +486,29 @@ def test_ddp_bucket_sweep_full_size():
     ref = outs[25]
     for mib, o in outs.items():
         assert torch.equal(o.view(torch.int16), ref.view(torch.int16)), mib
-    # replicated AdamW over every parameter with the averaged gradient
+    # replicated AdamW over every parameter (registration order, the library's
+    # unsharded layout) with the averaged gradient
+    glay = ss.fsdp_layout(numels, 1)
     master = torch.empty(total, dtype=torch.float32, device=DEV)
-    synth.dev_fill(w.master_stream(0), master)
+    for i, n in enumerate(numels):
+        synth.dev_fill(w.master_stream(0, i), master[glay.offsets[i]:glay.offsets[i] + n])
     mm = torch.zeros(total, device=DEV)
     vv = torch.zeros(total, device=DEV)
     pb = torch.empty(total, dtype=torch.bfloat16, device=DEV)
     ss.fsdp_rs_avg_adamw_cast([ref], master, mm, vv, pb, hpc, 1)
+    # the oracle from the seeded inputs alone: each sampled position traced to
+    # its parameter element by the oracle's layout
     loc = _sample(total, 100_000, rng)
     it = torch.from_numpy(loc).to(DEV)
-    p0 = synth.host_gather(w.master_stream(0), loc, "f32")
+    tt, kk = oracle.element_source(oracle.layout(numels, 1), loc)
+    uu = np.zeros(loc.size, np.int64)
+    p0 = synth.host_gather_sources(uu, tt, kk, w.master_stream, "f32")
+    gq = [synth.host_gather_sources(uu, tt, kk, lambda u, i, q=q: w.grad_stream(1, q, 0, u, i),
+                                    "bf16") for q in range(nd)]
     z = np.zeros(loc.size, np.float32)
-    _, p1, m1, v1, pb1 = oracle.ddp_step([_host_bf16(ref[it])], [0, loc.size], p0, z, z, hp, 1)
+    avg, p1, m1, v1, pb1 = oracle.ddp_step(gq, [0, loc.size], p0, z, z, hp, 1)
     torch.cuda.synchronize()
+    assert_bits(_host_bf16(ref[it]), avg, "averaged gradient")
     assert_bits(master[it].cpu().numpy(), p1, "master")
     assert_bits(mm[it].cpu().numpy(), m1, "m")
     assert_bits(vv[it].cpu().numpy(), v1, "v")
