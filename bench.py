@@ -68,7 +68,8 @@ def parse():
     ap.add_argument("--e2e-streams", type=int, default=4)
     ap.add_argument("--workload", choices=sorted(WORKLOADS) + [FSDP2_WORKLOAD, CKPT_WORKLOAD,
                                                              ACCUM_WORKLOAD, DDP_WORKLOAD,
-                                                             RAGGED_WORKLOAD],
+                                                             RAGGED_WORKLOAD, UNIT9M_WORKLOAD,
+                                                             GPT2_WORKLOAD],
                     default="llama_7b_rank0_nd8",
                     help="the Llama-7B rank view under full sharding (the default line); the "
                          "other lines time the other steps of the path")
@@ -417,7 +418,6 @@ def run_ours(args):
     ms_per_step = total_ms_max / args.steps
     fused_avg = sum(fused_ms) / len(fused_ms)
     ag_avg = sum(ag_ms) / len(ag_ms)
-    peak, peak_kind = measured_peak()
     achieved = fused_bytes / (fused_avg / 1e3) / 1e9
     traffic_per_elem = (None if args.layers or args.kernel_path != "auto" or args.tma_stages
                         else profiled_traffic(args.workload))
@@ -483,15 +483,10 @@ def run_ours(args):
                         "ag_ms": round(ag_avg, 4),
                         "ag_gbs": round(ag_bytes / (ag_avg / 1e3) / 1e9, 1),
                         **pack},
-            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
-                         "unit": "GB/s", "frac": round(achieved / peak, 4),
-                         "peak_source": ("measured: MEASURED_PEAKS.json hbm_gbs (copy, burst)"
-                                         if peak_kind == "measured" else "fallback 6800 GB/s"),
-                         "kernel": f"{fused_kernel}, N_d = {nd}"
-                                   + (f", sharding factor {F}" if F != nd else ""),
-                         "algorithmic_bytes_per_launch": fused_bytes,
-                         "traffic": (None if traffic_per_elem is None
-                                     else round(traffic_per_elem * S))},
+            "roofline": _roofline(achieved, f"{fused_kernel}, N_d = {nd}"
+                                  + (f", sharding factor {F}" if F != nd else ""), fused_bytes,
+                                  None if traffic_per_elem is None
+                                  else round(traffic_per_elem * S)),
             "e2e": e2e,
             **({"e2e_note": "the end-to-end leg runs without --graph"} if args.graph else {}),
             "gpu_launches": launches,
@@ -823,7 +818,6 @@ def run_fsdp2(args):
     total_ms = allreduce_max(world, a.elapsed_time(b))
     ms = [[e[i].elapsed_time(e[i + 1]) for e in events] for i in range(3)]
     avg = [sum(x) / len(x) for x in ms]
-    peak, peak_kind = measured_peak()
     fused_launch = fused_b / nd
     achieved = fused_launch / (avg[1] / nd / 1e3) / 1e9
     value = allreduce_sum(world, step_b * args.steps) / (total_ms / 1e3) / 1e9
@@ -847,12 +841,8 @@ def run_fsdp2(args):
                         "fused_gbs": round(achieved, 1),
                         "copy_out_ms": round(avg[2], 4),
                         "copy_out_gbs": round(ag_b / (avg[2] / 1e3) / 1e9, 1)},
-            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
-                         "unit": "GB/s", "frac": round(achieved / peak, 4),
-                         "peak_source": ("measured: MEASURED_PEAKS.json hbm_gbs (copy, burst)"
-                                         if peak_kind == "measured" else "fallback 6800 GB/s"),
-                         "kernel": f"{fused_kernel} on one rank's local buffer",
-                         "algorithmic_bytes_per_launch": fused_launch, "traffic": None},
+            "roofline": _roofline(achieved, f"{fused_kernel} on one rank's local buffer",
+                                  fused_launch),
             "e2e": None, "gpu_launches": launches, "clocks": clk, "cpu_baseline": None,
         }))
 
@@ -1253,12 +1243,25 @@ def _traffic(workload_name, elements, args):
     return round(per * elements)
 
 
+# GB300 HBM3e nominal bandwidth (8 stacks, NVIDIA's published 7.9 TB/s per
+# GPU).  The roofline's `peak` is the measured copy bandwidth instead, so
+# `frac` can read a little above 1 for a read-heavy kernel; `frac_of_nominal`
+# puts the same bytes against the nominal figure.
+HBM_NOMINAL_GBS = 7900.0
+
+
 def _roofline(achieved, kernel, bytes_per_launch, traffic=None):
     peak, kind = measured_peak()
     return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4),
+            "frac_of": ("the measured copy bandwidth (MEASURED_PEAKS.json hbm_gbs: b.copy_ of "
+                        "1 Gi bf16, read + write bytes, burst)" if kind == "measured"
+                        else "the fallback 6800 GB/s"),
             "peak_source": ("measured: MEASURED_PEAKS.json hbm_gbs (copy, burst)"
                             if kind == "measured" else "fallback 6800 GB/s"),
+            "frac_of_nominal": round(achieved / HBM_NOMINAL_GBS, 4),
+            "nominal_gbs": HBM_NOMINAL_GBS,
+            "nominal_source": "GB300 HBM3e nominal 7.9 TB/s (NVIDIA specification)",
             "kernel": kernel, "algorithmic_bytes_per_launch": bytes_per_launch,
             "traffic": traffic}
 
@@ -1691,8 +1694,367 @@ def run_ddp(args):
     _finish_dist(world)
 
 
+# ------------------------------------- small configurations: the whole job
+
+UNIT9M_WORKLOAD = "unit_9m_nd4_m4"
+GPT2_WORKLOAD = "gpt2_small_nd8"
+SMALL_METRICS = {
+    UNIT9M_WORKLOAD: ("whole-job step HBM GB/s: 4 ranks x (3 micro-batch accumulations + fused "
+                      "last micro-batch rs_avg+AdamW+bf16 cast) + all-gather, one 9.4M-param "
+                      "unit, N_d=4, M=4"),
+    GPT2_WORKLOAD: ("whole-job step HBM GB/s: 8 rank-view fused rs_avg+AdamW+bf16 cast launches "
+                    "over 13 units + all-gather of one block unit, GPT-2 small, N_d=8"),
+}
+L2_FLUSH_BYTES = 256 << 20          # written between timed steps: twice the 129 MB L2
+
+
+class _SmallJob:
+    """The whole data-parallel job of a small configuration on one GPU: every
+    emulated rank's step, so that launch latency and the small arrays are what
+    is measured.  Inputs (gradients of every rank and micro-batch, fp32
+    master) are seeded, packed / placed by the library's layout and resident
+    before timing."""
+
+    def __init__(self, name, torch, ss, dev):
+        import synth
+        from synth import workloads as W
+        from sharded_optimizer_step_gb300.engine import RankShardOptimizer
+        self.name, self.torch, self.ss, self.dev = name, torch, ss, dev
+        w = self.w = W.unit_9m() if name == UNIT9M_WORKLOAD else W.gpt2_small()
+        self.hp = ss.AdamW(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
+        nd, M = w.nd, w.micro
+        bf16, f32 = torch.bfloat16, torch.float32
+        if name == UNIT9M_WORKLOAD:
+            shapes = w.units[0]
+            lay = self.lay = ss.fsdp_layout(w.unit_numels(0), nd)
+            S, P = lay.shard, lay.padded
+            tens = [torch.empty(s, dtype=bf16, device=dev) for s in shapes]
+            self.g = []
+            for q in range(nd):
+                row = []
+                for j in range(M):
+                    flat = torch.empty(P, dtype=bf16, device=dev)
+                    for t, x in enumerate(tens):
+                        synth.dev_fill(w.grad_stream(1, q, j, 0, t), x.view(-1))
+                    ss.fsdp_flat_pack(tens, nd, flat=flat)
+                    row.append(flat)
+                self.g.append(row)
+            mt = [torch.empty(s, dtype=f32, device=dev) for s in shapes]
+            for t, x in enumerate(mt):
+                synth.dev_fill(w.master_stream(0, t), x.view(-1))
+            self.master = ss.fsdp_flat_pack(mt, nd)
+            self.m = torch.zeros(P, dtype=f32, device=dev)
+            self.v = torch.zeros(P, dtype=f32, device=dev)
+            self.acc = [torch.empty(P, dtype=f32, device=dev) for _ in range(nd)]
+            self.outs = [torch.empty(S, dtype=bf16, device=dev) for _ in range(nd)]
+            self.full = torch.empty(P, dtype=bf16, device=dev)
+            self.S, self.P = S, P
+            acc_b = nd * (6 + 10 * (M - 2)) * P
+            fused_b = (6 * nd + 26) * P             # nd launches of S elements
+            self.parts = [("accumulate", acc_b), ("fused", fused_b), ("all-gather", 4 * P)]
+            self.shard_elements = P
+            self.h2d = nd * M * P * 2
+        else:
+            self.opts = [RankShardOptimizer(w.units, nd, r, self.hp, device=dev)
+                         for r in range(nd)]
+            for o in self.opts:
+                fill_rank_view(o, o.master, w.master_stream)
+                for q in range(nd):
+                    fill_rank_view(o, o.grad_in[q], lambda u, k, q=q: w.grad_stream(1, q, 0, u, k))
+            S = self.opts[0].shard_total
+            self.u = 0
+            Pu = self.opts[0].layouts[self.u].padded
+            self.full = torch.empty(Pu, dtype=bf16, device=dev)
+            self.S, self.P = S, Pu
+            self.parts = [("fused", (2 * nd + 26) * S * nd), ("all-gather", 4 * Pu)]
+            self.shard_elements = S * nd
+            self.h2d = nd * nd * S * 2
+        self.d2h = 2 * self.P
+        self.step_bytes = sum(b for _, b in self.parts)
+        self.state = None
+        self.t = 0
+
+    def device_state(self):
+        """Step count and AdamW scalars on the device, for graph capture."""
+        if self.name == UNIT9M_WORKLOAD:
+            self.state = self.ss.AdamWState(self.hp, self.t, device=self.dev)
+        else:
+            for o in self.opts:
+                o.device_step_state()
+
+    def run(self, ev=None, graph_form=False):
+        """One step of the whole job; ev: 4 events (start, after the
+        accumulation, after the fused steps, after the all-gather)."""
+        ss, w = self.ss, self.w
+        nd, M = w.nd, w.micro
+        if ev is not None:
+            ev[0].record()
+        if self.name == UNIT9M_WORKLOAD:
+            S = self.S
+            inv_m = float(1.0 / M)
+            for q in range(nd):
+                for j in range(M - 1):
+                    ss.fsdp_grad_accumulate(self.g[q][j], self.acc[q], inv_m, j == 0)
+            if ev is not None:
+                ev[1].record()
+            if graph_form:
+                self.state.advance()
+            else:
+                self.t += 1
+            for r in range(nd):
+                sl = slice(r * S, (r + 1) * S)
+                args = ([a[sl] for a in self.acc], [gq[M - 1][sl] for gq in self.g], inv_m,
+                        self.master[sl], self.m[sl], self.v[sl], self.outs[r])
+                if graph_form:
+                    ss.fsdp_state_accumulate_rs_avg_adamw_cast(*args, self.state)
+                else:
+                    ss.fsdp_accumulate_rs_avg_adamw_cast(*args, self.hp, self.t)
+            if ev is not None:
+                ev[2].record()
+            ss.fsdp_ag_unpack(self.outs, self.full)
+        else:
+            if ev is not None:
+                ev[1].record()
+            for o in self.opts:
+                if graph_form:
+                    o.step_on_device()
+                else:
+                    o.step()
+            if ev is not None:
+                ev[2].record()
+            u = self.u
+            peers = [o.unit_slice(o.params, u) for o in self.opts]
+            self.opts[0].gather_unit(u, peers, self.full)
+        if ev is not None:
+            ev[3].record()
+
+    def host_inputs(self):
+        """(device buffer, pinned host copy) of every gradient input: what an
+        end-to-end step brings in from the host."""
+        torch = self.torch
+        bufs = ([g for row in self.g for g in row] if self.name == UNIT9M_WORKLOAD
+                else [x for o in self.opts for x in o.grad_in])
+        return [(b, torch.empty(b.shape, dtype=b.dtype, pin_memory=True).copy_(b)) for b in bufs]
+
+
+def _small_oracle(w_name, budget_s):
+    """The oracle on the host: the whole step of the 9.4M unit (all ranks'
+    accumulations, fused steps, the all-gather), or a contiguous sample of
+    rank 0's GPT-2 view (fused step) plus the matching all-gather share.
+    Returns (GB/s of algorithmic bytes, sample description)."""
+    import numpy as np
+    import oracle
+    import synth
+    from oracle.numerics import AdamWConfig
+    from synth import workloads as W
+    if w_name == UNIT9M_WORKLOAD:
+        w = W.unit_9m()
+        nd, M = w.nd, w.micro
+        numels = w.unit_numels(0)
+        hp = AdamWConfig(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
+        g = [[oracle.flat_pack([synth.host_fill(w.grad_stream(1, q, j, 0, t), 0, n, "bf16")
+                                for t, n in enumerate(numels)], nd)[0] for j in range(M)]
+             for q in range(nd)]
+        p, lay = oracle.flat_pack([synth.host_fill(w.master_stream(0, t), 0, n, "f32")
+                                   for t, n in enumerate(numels)], nd)
+        S, P = lay.shard, lay.padded
+        step_b = nd * (6 + 10 * (M - 2)) * P + (6 * nd + 26) * P + 4 * P
+        total_t, total_b, reps = 0.0, 0, 0
+        while total_t < budget_s and reps < 20:
+            t0 = time.perf_counter()
+            accs = [oracle.grad_accumulate(g[q], np.float32(1.0 / M)) for q in range(nd)]
+            outs = []
+            for r in range(nd):
+                z = np.zeros(S, np.float32)
+                outs.append(oracle.fsdp_shard_step(accs, r, S, p[r * S:(r + 1) * S], z, z, hp,
+                                                   1)[3])
+            oracle.ag_unpack(outs, lay)
+            total_t += time.perf_counter() - t0
+            total_b += step_b
+            reps += 1
+        return total_b / total_t / 1e9, (f"{reps} x the whole step (4 ranks' accumulations of 4 "
+                                         f"micro-batches, 4 fused steps, the all-gather), numpy "
+                                         f"single-threaded")
+    w = W.gpt2_small()
+    n = 2_000_000
+    hp = AdamWConfig(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
+    idx = np.arange(n, dtype=np.int64)
+    contribs = [oracle_rank_values(w, 0, idx, lambda u, k, q=q: w.grad_stream(1, q, 0, u, k),
+                                   "bf16") for q in range(w.nd)]
+    p = oracle_rank_values(w, 0, idx, w.master_stream, "f32")
+    shards = [synth.host_fill(w.peer_shard_stream(1, q, 0), 0, n // 64, "bf16")
+              for q in range(w.nd)]
+    lay = oracle.layout([w.nd * (n // 64)], w.nd)
+    total_t, total_b, reps = 0.0, 0, 0
+    while total_t < budget_s and reps < 50:
+        z = np.zeros(n, np.float32)
+        t0 = time.perf_counter()
+        oracle.fsdp_shard_step(contribs, 0, n, p, z, z, hp, reps + 1)
+        oracle.ag_unpack(shards, lay)
+        total_t += time.perf_counter() - t0
+        total_b += (2 * w.nd + 26) * n + 4 * w.nd * (n // 64)
+        reps += 1
+    return total_b / total_t / 1e9, (f"{reps} x (fused step on the first {n} elements of rank "
+                                     f"0's view + all-gather of {w.nd * (n // 64)} bf16), numpy "
+                                     f"single-threaded")
+
+
+def run_small(args):
+    """Configurations 1 and 2 of the path: a 9.4M-parameter unit (N_d = 4,
+    M = 4) and the GPT-2 small model (N_d = 8), each as its whole job on one
+    GPU.  At these sizes (a step of 1.5 GB and 5.3 GB) launch latency is part
+    of the answer, so the line gives the eager step and, with --graph, the
+    same launches replayed from one CUDA graph.  L2 is flushed (256 MB
+    written) between timed steps, outside the timed events."""
+    world, rank, local = dist_env()
+    name = args.workload
+    metric = SMALL_METRICS[name]
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        value, sample = _small_oracle(name, max(1.0, args.cpu_seconds))
+        print(json.dumps({
+            "impl": "reference", "metric": metric, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": None,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "config": {"workload": name},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}))
+        return
+    init_dist(world)
+    import torch
+    torch.cuda.set_device(local)
+    import __graft_entry__
+    __graft_entry__.build()
+    _apply_stages(args)
+    import sharded_optimizer_step_gb300 as ss
+    dev = torch.device("cuda", local)
+    job = _SmallJob(name, torch, ss, dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    run = job.run
+    graph_launches = 0
+    if args.graph:
+        job.device_state()
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            job.run(graph_form=True)          # warm-up outside the capture
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        l0 = ss.launch_count()
+        with torch.cuda.graph(graph):
+            job.run(graph_form=True)
+        graph_launches = ss.launch_count() - l0
+
+        def run(ev=None):                     # noqa: F811 -- the replayed step
+            if ev is not None:
+                ev[0].record()
+                ev[1].record()
+                ev[2].record()
+            graph.replay()
+            if ev is not None:
+                ev[3].record()
+
+    def one_step(ev):
+        flush.zero_()                         # L2 holds nothing of the previous step
+        run(ev)
+
+    total_ms, events, clk, launches = _timed_loop(torch, stream, args, one_step, 4, world)
+    launches += graph_launches * args.steps
+    step_ms = [e[0].elapsed_time(e[3]) for e in events]
+    ms_per_step = allreduce_max(world, sum(step_ms) / len(step_ms))
+    value = allreduce_sum(world, job.step_bytes) / (ms_per_step / 1e3) / 1e9
+    parts = {}
+    if not args.graph:
+        for k, (pname, b) in enumerate(job.parts if name == UNIT9M_WORKLOAD
+                                       else [("accumulate", 0)] + job.parts):
+            if pname == "accumulate" and b == 0:
+                continue
+            ms = _avg_ms(events, k, k + 1)
+            parts[pname] = {"ms": round(ms, 4), "gbs": round(b / (ms / 1e3) / 1e9, 1)}
+    dom_name, dom_bytes = max(job.parts, key=lambda x: x[1])
+    if parts:
+        dom_ms = parts[dom_name]["ms"]
+        dom_kernel = ("accumulate_vec8 (register-staged)" if dom_name == "accumulate"
+                      else "rs_adamw_cast_vec4<8, bf16> (register-staged)")
+        n_launch = (job.w.nd * (job.w.micro - 1) if dom_name == "accumulate" else job.w.nd)
+        roof = _roofline(dom_bytes / (dom_ms / 1e3) / 1e9, f"{dom_kernel}, {n_launch} launches "
+                         f"per step ({dom_name})", dom_bytes // n_launch)
+    else:
+        roof = _roofline(job.step_bytes / (ms_per_step / 1e3) / 1e9,
+                         "the whole step replayed from one CUDA graph (per-kernel times not "
+                         "separable)", job.step_bytes)
+
+    # end to end: every gradient input copied in from pinned host memory and
+    # the gathered unit copied out, inside the timing, each step
+    e2e = None
+    if not args.no_e2e:
+        pairs = job.host_inputs()
+        host_out = torch.empty(job.full.shape, dtype=job.full.dtype, pin_memory=True)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        n_e2e = max(1, args.e2e_steps)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(n_e2e):
+            for d, h in pairs:
+                d.copy_(h, non_blocking=True)
+            run(None)
+            host_out.copy_(job.full, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = allreduce_max(world, a.elapsed_time(b) / n_e2e)
+        e2e = {"value": round(allreduce_sum(world, job.step_bytes) / (e2e_ms / 1e3) / 1e9, 1),
+               "unit": "GB/s", "h2d_bytes_per_step": job.h2d, "d2h_bytes_per_step": job.d2h,
+               "ms_per_step": round(e2e_ms, 4),
+               "path": "pinned host gradients copied in on the compute stream, then the step's "
+                       "C-ABI calls, then the gathered unit copied out; no overlap"}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        cv, sample = _small_oracle(name, args.cpu_seconds)
+        cpu = {"value": round(cv, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": sample}
+    if rank == 0:
+        print(json.dumps({
+            "metric": metric, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded counter-based generator on the device; no data set or "
+                    "weights)",
+            "config": {"workload": name, "graph": bool(args.graph), "psi": job.w.psi,
+                       "nd": job.w.nd, "micro_batches": job.w.micro,
+                       "units": len(job.w.units), "ranks_per_gpu": job.w.nd,
+                       "elements_updated_per_step": job.shard_elements,
+                       "bytes_per_step": job.step_bytes,
+                       "roofline_ms": round(job.step_bytes / measured_peak()[0] / 1e6, 4),
+                       "l2": "flushed between steps (256 MB written, outside the timed events)",
+                       "tma_stages": _stages_name(args)},
+            "params_per_s": round(job.shard_elements * world / (ms_per_step / 1e3), 1),
+            "kernels": parts,
+            "roofline": roof,
+            "e2e": e2e,
+            "gpu_launches": launches,
+            **({"gpu_launches_note": f"{graph_launches} kernels per replayed step, counted when "
+                                     f"the graph was captured"} if args.graph else {}),
+            "clocks": clk,
+            "cpu_baseline": cpu,
+        }))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 def main():
     args = parse()
+    if args.workload in SMALL_METRICS:
+        run_small(args)
+        return
     if args.workload == ACCUM_WORKLOAD:
         run_accum(args)
         return

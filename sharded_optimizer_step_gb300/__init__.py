@@ -75,6 +75,13 @@ def _dtype_code(t):
     raise TypeError(f"unsupported dtype {t.dtype} (bf16, fp16 or fp32)")
 
 
+def _group(shard_group, nd):
+    """The sharding factor passed to the C ABI: None means full sharding
+    (F = N_d); any other value goes through as given, so that the library
+    rejects 0, negative factors and factors that do not divide N_d."""
+    return nd if shard_group is None else int(shard_group)
+
+
 def _need_cuda(*tensors):
     for t in tensors:
         if t is None:
@@ -226,7 +233,7 @@ def _accum_ptrs(acc_slices, last_slices, shard_group, S, scale, master, m, v, ou
     nd = len(acc_slices)
     return (_capi.ptr_array([a.data_ptr() for a in acc_slices]),
             _capi.ptr_array([g.data_ptr() for g in last_slices]), nd,
-            int(shard_group) if shard_group else nd, S,
+            _group(shard_group, nd), S,
             ctypes.c_float(scale), ctypes.c_void_p(master.data_ptr()),
             ctypes.c_void_p(m.data_ptr()), ctypes.c_void_p(v.data_ptr()),
             ctypes.c_void_p(out_bf16.data_ptr()))
@@ -344,7 +351,8 @@ def fsdp_state_rs_avg_adamw_cast(grad_slices, master, m, v, out_bf16, state: Ada
         raise ValueError("out must be bf16 with S elements")
     _capi.check("fsdp_state_rs_avg_adamw_cast", _capi.lib().fsdp_state_rs_avg_adamw_cast(
         _capi.ptr_array([g.data_ptr() for g in grad_slices]), _dtype_code(grad_slices[0]),
-        len(grad_slices), shard_group or len(grad_slices), S, ctypes.c_void_p(master.data_ptr()),
+        len(grad_slices), _group(shard_group, len(grad_slices)), S,
+        ctypes.c_void_p(master.data_ptr()),
         ctypes.c_void_p(m.data_ptr()), ctypes.c_void_p(v.data_ptr()),
         ctypes.c_void_p(out_bf16.data_ptr()), ctypes.c_void_p(state.buf.data_ptr()),
         _stream(stream, master.device)))
@@ -375,7 +383,7 @@ class GradScaler:
         nd = len(grad_slices)
         _capi.check("fsdp_grad_unscale_check", _capi.lib().fsdp_grad_unscale_check(
             _capi.ptr_array([g.data_ptr() for g in grad_slices]), _dtype_code(grad_slices[0]),
-            nd, shard_group or nd, S, ctypes.c_void_p(self.scale.data_ptr()),
+            nd, _group(shard_group, nd), S, ctypes.c_void_p(self.scale.data_ptr()),
             ctypes.c_void_p(self.found_inf.data_ptr()), _stream(stream, grad_slices[0].device)))
 
     def step(self, grad_slices, master, m, v, out_bf16, hp: AdamW, step: int,
@@ -388,7 +396,7 @@ class GradScaler:
         hpc = hp.at_step(step)
         _capi.check("fsdp_scaled_rs_avg_adamw_cast", _capi.lib().fsdp_scaled_rs_avg_adamw_cast(
             _capi.ptr_array([g.data_ptr() for g in grad_slices]), _dtype_code(grad_slices[0]),
-            nd, shard_group or nd, S, ctypes.c_void_p(master.data_ptr()),
+            nd, _group(shard_group, nd), S, ctypes.c_void_p(master.data_ptr()),
             ctypes.c_void_p(m.data_ptr()), ctypes.c_void_p(v.data_ptr()),
             ctypes.c_void_p(out_bf16.data_ptr()), ctypes.byref(hpc),
             ctypes.c_void_p(self.scale.data_ptr()), ctypes.c_void_p(self.found_inf.data_ptr()),
@@ -406,7 +414,7 @@ class GradScaler:
         _capi.check("fsdp_state_scaled_rs_avg_adamw_cast",
                     _capi.lib().fsdp_state_scaled_rs_avg_adamw_cast(
                         _capi.ptr_array([g.data_ptr() for g in grad_slices]),
-                        _dtype_code(grad_slices[0]), nd, shard_group or nd, S,
+                        _dtype_code(grad_slices[0]), nd, _group(shard_group, nd), S,
                         ctypes.c_void_p(master.data_ptr()), ctypes.c_void_p(m.data_ptr()),
                         ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(out_bf16.data_ptr()),
                         ctypes.c_void_p(state.buf.data_ptr()),

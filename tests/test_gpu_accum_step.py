@@ -102,10 +102,67 @@ def test_accumulate_step_matches_oracle(nd, S, shift):
 
 @pytest.mark.parametrize("nd,F", [(16, 8), (8, 4), (6, 3), (8, 2), (4, 1), (9, 3)])
 @pytest.mark.parametrize("S", [13, 4099, 70001])
-def test_hybrid_accumulate_step_matches_oracle(nd, F, S):
+@pytest.mark.parametrize("shift", [0, 1])
+def test_hybrid_accumulate_step_matches_oracle(nd, F, S, shift):
     """Hybrid sharding (sharding factor F): the contributions summed inside
-    each group of F ranks, then across the groups, as the hybrid step does."""
-    _check(nd, S, M=3, step=2, shift=0, F=F)
+    each group of F ranks, then across the groups, as the hybrid step does;
+    with shift = 1 the slices are misaligned and the one-element kernel runs
+    the grouped sum."""
+    _check(nd, S, M=3, step=2, shift=shift, F=F)
+
+
+@pytest.mark.parametrize("nd,F,rank", [(8, 4, 3), (9, 3, 2), (16, 8, 7)])
+def test_engine_hybrid_last_micro_batch_in_a_cuda_graph(nd, F, rank):
+    """RankShardOptimizer with sharding factor F < N_d and a rank other than
+    0: step_with_last_micro_batch (host scalars) and its device-state form
+    captured once in a CUDA graph and replayed, over three steps of a small
+    model, against the oracle's accumulation and hybrid shard step."""
+    from sharded_optimizer_step_gb300.engine import RankShardOptimizer
+    units = [[(37, 29), (29,), (301,)], [(64, 64), (5,)]]
+    M, steps = 3, 3
+    a = RankShardOptimizer(units, nd, rank, HPC, device=DEV, grad_dtype=torch.float32,
+                           shard_group=F)
+    b = RankShardOptimizer(units, nd, rank, HPC, device=DEV, grad_dtype=torch.float32,
+                           shard_group=F)
+    S = a.shard_total
+    seed = 7 * nd + F + rank
+    p, _, _ = _state(seed, S)
+    a.master.copy_(torch.from_numpy(p))
+    b.master.copy_(torch.from_numpy(p))
+    last = [torch.empty(S, dtype=torch.bfloat16, device=DEV) for _ in range(nd)]
+    scale = np.float32(1.0 / M)
+    b.device_step_state()
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):          # a warm-up outside the capture, then undone
+        b.step_with_last_micro_batch_on_device(last, float(scale))
+    torch.cuda.current_stream().wait_stream(side)
+    b.master.copy_(torch.from_numpy(p))
+    b.m.zero_()
+    b.v.zero_()
+    b.state.init(0)
+    with torch.cuda.graph(graph):
+        b.step_with_last_micro_batch_on_device(last, float(scale))
+    wp, wm, wv = p, np.zeros(S, np.float32), np.zeros(S, np.float32)
+    for t in range(1, steps + 1):
+        micro = _micro(seed + t, nd, M, S)
+        for q in range(nd):
+            for j in range(M - 1):
+                ss.fsdp_grad_accumulate(dev(micro[q][j]), a.grad_in[q], float(scale), j == 0)
+            b.grad_in[q].copy_(a.grad_in[q])
+            last[q].copy_(dev(micro[q][M - 1]))
+        a.step_with_last_micro_batch(last, float(scale))
+        graph.replay()
+        contribs = [oracle.grad_accumulate(micro[q], scale) for q in range(nd)]
+        wp, wm, wv, wo = oracle.hybrid_shard_step(contribs, F, 0, S, wp, wm, wv, HP, t)
+    torch.cuda.synchronize()
+    assert b.state.step() == steps and a.t == steps
+    for o in (a, b):
+        assert_bits(host(o.master), wp, "master")
+        assert_bits(host(o.m), wm, "m")
+        assert_bits(host(o.v), wv, "v")
+        assert_bits(host(o.params), wo, "bf16")
 
 
 @pytest.mark.parametrize("nd,S,M", [(8, 152 * 128 * 6 * 2 + 7, 4), (8, 1 << 18, 2),
@@ -219,3 +276,21 @@ def test_accumulation_step_on_device_captured_in_a_cuda_graph():
             assert torch.equal(x.view(torch.int32), y.view(torch.int32)), t
         assert torch.equal(a.params.view(torch.int16), b.params.view(torch.int16)), t
     assert b.state.step() == 3
+
+
+def test_binding_passes_an_explicit_sharding_factor_through():
+    """Only None means full sharding in the binding; 0 or a factor that does
+    not divide N_d reaches the C ABI and is rejected there."""
+    S, nd = 64, 4
+    accs = [torch.zeros(S, device=DEV) for _ in range(nd)]
+    last = [torch.zeros(S, dtype=torch.bfloat16, device=DEV) for _ in range(nd)]
+    st = (torch.zeros(S, device=DEV), torch.zeros(S, device=DEV), torch.zeros(S, device=DEV),
+          torch.empty(S, dtype=torch.bfloat16, device=DEV))
+    for bad in (0, -2, 3):
+        with pytest.raises(ss.ShardstepError):
+            ss.fsdp_accumulate_rs_avg_adamw_cast(accs, last, 0.5, *st, HPC, 1, shard_group=bad)
+    sc = ss.GradScaler(1.0, device=DEV)
+    with pytest.raises(ss.ShardstepError):
+        sc.check([a.to(torch.float16) for a in accs], shard_group=0)
+    ss.fsdp_accumulate_rs_avg_adamw_cast(accs, last, 0.5, *st, HPC, 1, shard_group=None)
+    torch.cuda.synchronize()

@@ -143,3 +143,66 @@ def test_fsdp2_copies_write_only_their_buffers(path):
     ss.fsdp2_all_gather_copy_out(locals_, [o.t.view(s) for o, s in zip(outs, shapes)])
     for k, o in enumerate(outs):
         o.check(f"copy-out {k}")
+
+
+def _f32(n, seed, sigma=1e-3, shift=0):
+    h = synth.host_fill(synth.normal_stream(seed, (78, n), sigma), 0, n, "f32")
+    buf = torch.empty(n + shift + 8, dtype=torch.float32, device=DEV)
+    t = buf[shift:shift + n]
+    t.copy_(torch.from_numpy(h))
+    return t
+
+
+@pytest.mark.parametrize("nd,F", [(8, 8), (8, 4), (9, 3), (2, 2), (6, 2)])
+@pytest.mark.parametrize("S,shift", [(4099, 0), (2048 * 152 + 13, 0), (70001, 1), (13, 0)])
+@pytest.mark.parametrize("state", [False, True])
+def test_fused_last_micro_batch_writes_only_its_outputs(nd, F, S, shift, state, path):
+    """The last micro-batch accumulated inside the fused step, plain and
+    hybrid, host scalars and device step state: master / m / v / out inside
+    sentinel bands, and the accumulator and last-gradient slices (also in
+    bands) read, never written."""
+    acc = [Guarded(S, torch.float32, shift, _f32(S, 80 + q)) for q in range(nd)]
+    last = [Guarded(S, torch.bfloat16, shift, _bf16(S, 90 + q)) for q in range(nd)]
+    before = [a.t.clone() for a in acc] + [g.t.clone() for g in last]
+    master = Guarded(S, torch.float32, shift, torch.randn(S, device=DEV) * 0.02)
+    m = Guarded(S, torch.float32, shift, torch.zeros(S, device=DEV))
+    v = Guarded(S, torch.float32, shift, torch.zeros(S, device=DEV))
+    out = Guarded(S, torch.bfloat16, shift)
+    hp = ss.AdamW()
+    args = ([a.t for a in acc], [g.t for g in last], 0.25, master.t, m.t, v.t, out.t)
+    if state:
+        st = ss.AdamWState(hp, 0, device=DEV)
+        st.advance()
+        ss.fsdp_state_accumulate_rs_avg_adamw_cast(*args, st, shard_group=F)
+    else:
+        ss.fsdp_accumulate_rs_avg_adamw_cast(*args, hp, 1, shard_group=F)
+    for name, g in (("master", master), ("m", m), ("v", v), ("bf16", out)):
+        g.check(f"fused last micro-batch {name}")
+    for k, (g, b) in enumerate(zip(acc + last, before)):
+        g.check(f"input slice {k}")
+        assert torch.equal(g.t.view(torch.uint8), b.view(torch.uint8)), f"input slice {k} written"
+
+
+@pytest.mark.parametrize("nd", [1, 3, 8])
+@pytest.mark.parametrize("keep_mean", [False, True])
+def test_fused_ddp_step_writes_only_its_outputs(nd, keep_mean):
+    boff = [0, 4096, 4096 + 70003, 4096 + 70003 + 5, 4096 + 70003 + 5 + 40000]
+    total = boff[-1]
+    grads = [Guarded(total, torch.bfloat16, q % 2, _bf16(total, 100 + q)) for q in range(nd)]
+    before = [g.t.clone() for g in grads]
+    master = Guarded(total, torch.float32, 1, torch.randn(total, device=DEV) * 0.02)
+    m = Guarded(total, torch.float32, 1, torch.zeros(total, device=DEV))
+    v = Guarded(total, torch.float32, 1, torch.zeros(total, device=DEV))
+    pb = Guarded(total, torch.bfloat16, 1)
+    mean = Guarded(total, torch.bfloat16, 3) if keep_mean else None
+    ss.ddp_bucket_allreduce_avg_adamw_cast([g.t for g in grads], boff, master.t, m.t, v.t, pb.t,
+                                           ss.AdamW(), 1, mean_out=mean.t if mean else None)
+    # one bucket in the middle touches only its own range of every output
+    ss.ddp_bucket_allreduce_avg_adamw_cast([g.t for g in grads], boff, master.t, m.t, v.t, pb.t,
+                                           ss.AdamW(), 2, first=2, count=1)
+    for name, g in (("master", master), ("m", m), ("v", v), ("params", pb)) + \
+            ((("mean", mean),) if mean else ()):
+        g.check(f"fused DDP {name}")
+    for q, (g, b) in enumerate(zip(grads, before)):
+        g.check(f"gradient {q}")
+        assert torch.equal(g.t.view(torch.uint8), b.view(torch.uint8)), f"gradient {q} written"

@@ -5,7 +5,7 @@ element.  The oracle computes sampled outputs one by one from the same
 seeded inputs: the first and last elements, a band around element 2^31 (and
 around byte 2^32 of the fp32 arrays), and random positions; properties that
 hold at any size (the zero padding, the found-inf flag) cover the rest.
-About 40 GB of device memory at most, released after each test."""
+About 60 GB of device memory at most, released after each test."""
 import numpy as np
 import pytest
 import torch
@@ -174,3 +174,69 @@ def test_flat_pack_and_ag_unpack_past_2_31(path):
         idx = _sample(k, 3 + i)
         assert_bits(_bits16(_at(vw, idx)), synth.host_gather(_stream(6, i), idx, "bf16"),
                     f"tensor {i}")
+
+
+def test_fused_last_micro_batch_past_2_31(path):
+    """The last micro-batch accumulated inside the fused step over 2^31 + 13
+    elements: fp32 accumulators of micro-batches 0..M-2 and the last bf16
+    gradient per contribution; the accumulators are read, not written."""
+    nd, S, M = 2, BIG, 2
+    acc = [torch.empty(S, dtype=torch.float32, device=DEV) for _ in range(nd)]
+    last = [torch.empty(S, dtype=torch.bfloat16, device=DEV) for _ in range(nd)]
+    g = torch.empty(S, dtype=torch.bfloat16, device=DEV)
+    for q in range(nd):
+        synth.dev_fill(_stream(7, q, 0), g)
+        ss.fsdp_grad_accumulate(g, acc[q], 1.0 / M, True)
+        synth.dev_fill(_stream(7, q, 1), last[q])
+    del g
+    master = torch.empty(S, dtype=torch.float32, device=DEV)
+    synth.dev_fill(_stream(8, 0, sigma=0.02), master)
+    m = torch.zeros(S, dtype=torch.float32, device=DEV)
+    v = torch.zeros(S, dtype=torch.float32, device=DEV)
+    out = torch.empty(S, dtype=torch.bfloat16, device=DEV)
+    ss.fsdp_accumulate_rs_avg_adamw_cast(acc, last, 1.0 / M, master, m, v, out, HPC, 1)
+    idx = _sample(S, 4)
+    micro = [[synth.host_gather(_stream(7, q, j), idx, "bf16") for j in range(M)]
+             for q in range(nd)]
+    contribs = [oracle.grad_accumulate(micro[q], np.float32(1.0 / M)) for q in range(nd)]
+    z = np.zeros(idx.size, np.float32)
+    p, mh, vh, ob = oracle.fsdp_shard_step(contribs, 0, idx.size,
+                                           synth.host_gather(_stream(8, 0, sigma=0.02), idx, "f32"),
+                                           z, z, HP, 1)
+    torch.cuda.synchronize()
+    assert_bits(_at(master, idx).cpu().numpy(), p, "master")
+    assert_bits(_at(m, idx).cpu().numpy(), mh, "m")
+    assert_bits(_at(v, idx).cpu().numpy(), vh, "v")
+    assert_bits(_bits16(_at(out, idx)), ob, "bf16")
+    for q in range(nd):
+        assert_bits(_at(acc[q], idx).cpu().numpy(),
+                    oracle.grad_accumulate(micro[q][:1], np.float32(1.0 / M)), f"accumulator {q}")
+
+
+def test_fused_ddp_step_past_2_31(path):
+    nd, n = 2, BIG
+    grads = [torch.empty(n, dtype=torch.bfloat16, device=DEV) for _ in range(nd)]
+    for q in range(nd):
+        synth.dev_fill(_stream(9, q), grads[q])
+    master = torch.empty(n, dtype=torch.float32, device=DEV)
+    synth.dev_fill(_stream(10, 0, sigma=0.02), master)
+    m = torch.zeros(n, dtype=torch.float32, device=DEV)
+    v = torch.zeros(n, dtype=torch.float32, device=DEV)
+    pb = torch.empty(n, dtype=torch.bfloat16, device=DEV)
+    mean = torch.empty(n, dtype=torch.bfloat16, device=DEV)
+    # buckets split at 2^30 and 2^31 + 1, all in one call (one launch)
+    ss.ddp_bucket_allreduce_avg_adamw_cast(grads, [0, 1 << 30, (1 << 31) + 1, n], master, m, v,
+                                           pb, HPC, 1, mean_out=mean)
+    idx = _sample(n, 5)
+    contribs = [synth.host_gather(_stream(9, q), idx, "bf16") for q in range(nd)]
+    z = np.zeros(idx.size, np.float32)
+    avg, p, mh, vh, ob = oracle.ddp_step(contribs, [0, idx.size],
+                                         synth.host_gather(_stream(10, 0, sigma=0.02), idx, "f32"),
+                                         z, z, HP, 1)
+    torch.cuda.synchronize()
+    assert_bits(_bits16(_at(mean, idx)), avg, "mean")
+    assert_bits(_at(master, idx).cpu().numpy(), p, "master")
+    assert_bits(_at(m, idx).cpu().numpy(), mh, "m")
+    assert_bits(_at(v, idx).cpu().numpy(), vh, "v")
+    assert_bits(_bits16(_at(pb, idx)), ob, "params")
+
