@@ -75,6 +75,14 @@ def parse():
                          "other lines time the other steps of the path")
     ap.add_argument("--layers", type=int, default=0,
                     help="smaller case: only the first N layer units (for profiler captures)")
+    ap.add_argument("--nd", type=int, default=0,
+                    help="rank-view lines (default, hybrid, fp16) and the DDP line: another "
+                         "number of emulated ranks N_d (0: the workload's own), for kernel "
+                         "sweeps and profiler captures")
+    ap.add_argument("--shrink", type=int, default=1,
+                    help="FSDP2 and ragged lines: a smaller case of the same kernels, every "
+                         "parameter's first dimension (ragged: every tensor) divided by this "
+                         "(for profiler captures)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--tma-stages", type=int, default=0,
@@ -282,6 +290,11 @@ def workload(args):
         # a smaller case of the same kernel: the first N layer units only
         w.units = w.units[:args.layers]
         w.name = f"{w.name}_first{args.layers}layers"
+    if args.nd and args.nd != w.nd:
+        if w.shard_group and args.nd % w.shard_group:
+            raise SystemExit("--nd must be a multiple of the sharding factor")
+        w.nd = args.nd
+        w.name = f"{w.name}_nd{args.nd}"
     return w
 
 
@@ -419,8 +432,8 @@ def run_ours(args):
     fused_avg = sum(fused_ms) / len(fused_ms)
     ag_avg = sum(ag_ms) / len(ag_ms)
     achieved = fused_bytes / (fused_avg / 1e3) / 1e9
-    traffic_per_elem = (None if args.layers or args.kernel_path != "auto" or args.tma_stages
-                        else profiled_traffic(args.workload))
+    traffic_per_elem = (None if args.layers or args.nd or args.kernel_path != "auto"
+                        or args.tma_stages else profiled_traffic(args.workload))
 
     pack = _time_flat_pack(torch, ss, w, u, nd if F == nd else F, dev, stream)
 
@@ -446,9 +459,11 @@ def run_ours(args):
             e2e.pop("seconds")
             e2e["value"] = round(got_bytes / got_sec / 1e9, 1)
 
-    cpu = None
+    cpu = cpu_all = None
     if rank == 0 and not args.no_cpu:
-        cpu = cpu_baseline(w, r, budget_s=args.cpu_seconds)
+        sample = _oracle_sample(w, r, 4_000_000, 1)
+        cpu = cpu_baseline(w, r, budget_s=args.cpu_seconds, sample=sample)
+        cpu_all = cpu_baseline_all_cores(w, r, budget_s=args.cpu_seconds, sample=sample)
 
     if rank == 0:
         line = {
@@ -494,6 +509,7 @@ def run_ours(args):
                                      f"when the graphs were captured"} if args.graph else {}),
             "clocks": clk,
             "cpu_baseline": cpu,
+            "cpu_baseline_all_cores": cpu_all,
         }
         print(json.dumps(line))
     if world > 1:
@@ -671,8 +687,8 @@ def _time_oracle(w, contribs, p, shards, t):
     return dt, bytes_
 
 
-def cpu_baseline(w, r, budget_s=10.0, n=4_000_000):
-    contribs, p, shards = _oracle_sample(w, r, n, 1)
+def cpu_baseline(w, r, budget_s=10.0, n=4_000_000, sample=None):
+    contribs, p, shards = sample or _oracle_sample(w, r, n, 1)
     total_t, total_b, reps = 0.0, 0, 0
     while total_t < budget_s and reps < 50:
         dt, b = _time_oracle(w, contribs, p, shards, reps + 1)
@@ -683,6 +699,39 @@ def cpu_baseline(w, r, budget_s=10.0, n=4_000_000):
             "kind": "oracle",
             "sample": f"{reps} x (fused step on {n} contiguous shard elements of {w.name} "
                       f"+ all-gather of {shards[0].size * w.F} bf16), numpy single-threaded"}
+
+
+def cpu_baseline_all_cores(w, r, budget_s=10.0, n=4_000_000, sample=None):
+    """The same oracle (unchanged) on all host cores: the sample is cut into
+    one contiguous element range per thread and each thread runs the fused
+    step and its share of the all-gather on its range (numpy releases the
+    interpreter lock inside its array operations).  Labelled as such; the
+    single-threaded figure is the baseline of record."""
+    import concurrent.futures as cf
+    threads = max(1, os.cpu_count() or 1)
+    contribs, p, shards = sample or _oracle_sample(w, r, n, 1)
+    per = -(-n // threads)
+    ranges = [(a, min(n, a + per)) for a in range(0, n, per)]
+    s_per = -(-shards[0].size // threads)
+    pieces = [[s[a:a + s_per] for s in shards] for a in range(0, shards[0].size, s_per)]
+
+    def work(k, t):
+        a, e = ranges[k]
+        dt, b = _time_oracle(w, [c[a:e] for c in contribs], p[a:e].copy(),
+                             pieces[min(k, len(pieces) - 1)], t)
+        return b
+
+    total_t, total_b, reps = 0.0, 0, 0
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        while total_t < budget_s and reps < 50:
+            t0 = time.perf_counter()
+            total_b += sum(ex.map(lambda k: work(k, reps + 1), range(len(ranges))))
+            total_t += time.perf_counter() - t0
+            reps += 1
+    return {"value": round(total_b / total_t / 1e9, 4), "unit": "GB/s", "cores": threads,
+            "kind": "oracle, all cores (numpy, one thread per contiguous element range)",
+            "sample": f"{reps} x (fused step on {n} contiguous shard elements of {w.name} split "
+                      f"over {len(ranges)} threads + their all-gather shares)"}
 
 
 def run_reference(args):
@@ -748,6 +797,8 @@ def run_fsdp2(args):
     from synth import workloads as W
     w = W.llama_7b_rank_view()
     shapes = w.units[0]
+    if args.shrink > 1:           # a smaller case: every parameter's dim 0 divided
+        shapes = [(-(-sh[0] // args.shrink),) + tuple(sh[1:]) for sh in shapes]
     nd = w.nd
     dev = torch.device("cuda", local_rank)
     hp = ss.AdamW(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
@@ -828,7 +879,9 @@ def run_fsdp2(args):
             "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded counter-based generator on the device; no data set or weights)",
-            "config": {"workload": FSDP2_WORKLOAD, "tma_stages": _stages_name(args),
+            "config": {"workload": FSDP2_WORKLOAD + (f"_shrunk{args.shrink}x"
+                                                     if args.shrink > 1 else ""),
+                       "tma_stages": _stages_name(args),
                        "group": "one Llama-7B layer (9 parameters, "
                        "202,383,360 elements)", "nd": nd, "local_elements": L,
                        "step": "8 x chunk-cat of a rank's full bf16 gradients, 8 x fused step on "
@@ -852,14 +905,16 @@ def run_fsdp2(args):
 RAGGED_WORKLOAD = "llama_7b_layer_ragged_nd8"
 
 
-def _ragged_unit():
+def _ragged_unit(shrink=1):
     """The Llama-7B layer unit's 9 tensors, each one element longer, so that
     every tensor after the first starts at an odd element offset of the
-    FlatParameter and the 8 shard slots sit 4 bytes off 16-byte boundaries."""
+    FlatParameter and the 8 shard slots sit 4 bytes off 16-byte boundaries
+    (shrink > 1: every tensor's length divided by it first, for a smaller
+    case of the same copies)."""
     from synth import workloads as W
     w = W.llama_7b_rank_view()
     shapes = w.units[w.extra["ag_unit"]]
-    return w, [math.prod(sh) + 1 for sh in shapes]
+    return w, [math.prod(sh) // shrink + 1 for sh in shapes]
 
 
 def _ragged_oracle(numels, nd, scale, step):
@@ -884,7 +939,7 @@ def run_ragged(args):
     world, rank, local = dist_env()
     init_dist(world)
     nd = 8
-    w, numels = _ragged_unit()
+    w, numels = _ragged_unit(args.shrink)
     if args.impl == "reference":
         if rank == 0:
             tt, tb = 0.0, 0
@@ -967,7 +1022,9 @@ def run_ragged(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded counter-based generator on the device; no data set or weights)",
-        "config": {"workload": RAGGED_WORKLOAD, "tma_stages": _stages_name(args), "nd": nd,
+        "config": {"workload": RAGGED_WORKLOAD + (f"_shrunk{args.shrink}x" if args.shrink > 1
+                                                  else ""),
+                   "tma_stages": _stages_name(args), "nd": nd,
                    "tensors": len(numels), "elements": lay.total, "padded": lay.padded,
                    "shard": S, "byte_offsets_mod_16": offs,
                    "step": "flat_pack of the 9 tensors (1 call), all-gather of the 8 shards "
@@ -1238,7 +1295,7 @@ def _traffic(workload_name, elements, args):
     the profile's bytes per element (None for smaller cases, other kernel
     choices or a kernel changed since the capture)."""
     per = profiled_traffic(workload_name)
-    if per is None or args.layers or args.kernel_path != "auto" or args.tma_stages:
+    if per is None or args.layers or args.nd or args.kernel_path != "auto" or args.tma_stages:
         return None
     return round(per * elements)
 
@@ -1547,6 +1604,8 @@ def run_ddp(args):
     (all-reduce only)."""
     from synth import workloads as W
     w = W.ddp_sweep()
+    if args.nd:
+        w.nd = args.nd
     numels = w.unit_numels(0)
     if args.layers:
         numels = numels[:5 * args.layers]    # smaller case: the first N blocks' parameters
@@ -1644,6 +1703,31 @@ def run_ddp(args):
         cap_ms = a.elapsed_time(b) / reps
         by_cap[f"{mib}MiB"] = {"buckets": len(bo) - 1, "ms": round(cap_ms, 4),
                                "gbs": round(ar_bytes / (cap_ms / 1e3) / 1e9, 1)}
+    # the same step fused: the all-reduce of all buckets and the replicated
+    # AdamW + cast in one launch (ddp_bucket_allreduce_avg_adamw_cast), with
+    # and without the averaged gradient kept; back to back, same gradients
+    fused = {}
+    for keep in (False, True):
+        def fused_call():
+            t[0] += 1
+            ss.ddp_bucket_allreduce_avg_adamw_cast(grads, boff, master, mm, vv, pb, hp, t[0],
+                                                   mean_out=out if keep else None,
+                                                   stream=stream)
+        for _ in range(3):
+            fused_call()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            fused_call()
+        b.record(stream)
+        torch.cuda.synchronize()
+        f_ms = allreduce_max(world, a.elapsed_time(b) / args.steps)
+        f_bytes = (2 * nd + 26 + (2 if keep else 0)) * total
+        fused["keep_mean" if keep else "no_mean"] = {
+            "ms": round(f_ms, 4), "gbs": round(f_bytes / (f_ms / 1e3) / 1e9, 1),
+            "bytes": f_bytes, "time_vs_two_calls": round(f_ms / ms, 4),
+            "kernel": ss.last_kernel()}
     if rank != 0:
         _finish_dist(world)
         return
@@ -1666,7 +1750,7 @@ def run_ddp(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded counter-based generator on the device; no data set or weights)",
         "config": {"workload": DDP_WORKLOAD + (f"_first{args.layers}blocks" if args.layers
-                                               else ""),
+                                               else "") + (f"_nd{nd}" if nd != 8 else ""),
                    "tma_stages": _stages_name(args),
                    "dependent_launch": not args.no_dependent_launch,
                    "psi": total, "nd": nd, "cap_mib": 25,
@@ -1679,10 +1763,15 @@ def run_ddp(args):
         "kernels": {"allreduce_ms": round(ar_ms, 4), "allreduce_gbs": round(ar_gbs, 1),
                     "allreduce_frac": round(ar_gbs / measured_peak()[0], 4),
                     "adamw_ms": round(adam_ms, 4), "adamw_gbs": round(adam_gbs, 1),
-                    "allreduce_by_cap": by_cap},
+                    "allreduce_by_cap": by_cap,
+                    "fused_step": {**fused, "note": "ddp_bucket_allreduce_avg_adamw_cast over "
+                                   "the 25 MiB plan's buckets in one launch: the same bits as "
+                                   "the two calls timed above"}},
+        "roofline_fused": _roofline(fused["no_mean"]["gbs"], fused["no_mean"]["kernel"],
+                                    fused["no_mean"]["bytes"]),
         "roofline": _roofline(adam_gbs, f"{kernel_names['adamw']} at N_d = 1 (full AdamW)",
                               adam_bytes, _traffic(DDP_WORKLOAD, total, args)),
-        "roofline_allreduce": _roofline(ar_gbs, f"{kernel_names['allreduce']} at N_d = 8 "
+        "roofline_allreduce": _roofline(ar_gbs, f"{kernel_names['allreduce']} at N_d = {nd} "
                                                 f"({len(boff) - 1} launches, one per bucket; "
                                                 f"the last bucket's kernel named)", ar_bytes),
         "e2e": None, "e2e_note": "device-resident gradients; the end-to-end line is the "
