@@ -96,8 +96,10 @@ def parse():
                          "scalars on the device, the accumulate launches, the fused update "
                          "and the all-gather replayed from CUDA graphs captured once")
     ap.add_argument("--no-dependent-launch", action="store_true",
-                    help="launch every bucket of an all-reduce call, and every copy kernel "
-                         "of a pack / all-gather call, as an ordinary launch")
+                    help="launch every kernel as an ordinary launch (by default each call's "
+                         "first kernel is a programmatic dependent of the kernel before it, "
+                         "waiting for it before touching memory, and the later buckets / "
+                         "copies of a call overlap the previous one's drain)")
     ap.add_argument("--accum-two-pass", action="store_true",
                     help="accumulation line: accumulate every micro-batch with its own launch "
                          "and run the fused step on the accumulators (the last micro-batch "
@@ -473,6 +475,7 @@ def run_ours(args):
             "data": "synthetic (seeded counter-based generator on the device; no data set or weights)",
             "config": {"workload": w.name, "tma_stages": _stages_name(args),
                        "graph": bool(args.graph),
+                       "dependent_launch": not args.no_dependent_launch,
                        "model_shape": f"Llama-style 7B, {len(w.units)} FSDP units",
                        "psi": w.psi, "nd": nd, "shard_group": F, "rank": r,
                        "shard_elements": S,
@@ -2123,7 +2126,8 @@ def run_small(args):
                        "bytes_per_step": job.step_bytes,
                        "roofline_ms": round(job.step_bytes / measured_peak()[0] / 1e6, 4),
                        "l2": "flushed between steps (256 MB written, outside the timed events)",
-                       "tma_stages": _stages_name(args)},
+                       "tma_stages": _stages_name(args),
+                       "dependent_launch": not args.no_dependent_launch},
             "params_per_s": round(job.shard_elements * world / (ms_per_step / 1e3), 1),
             "kernels": parts,
             "roofline": roof,

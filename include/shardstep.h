@@ -704,15 +704,20 @@ int fsdp_reshard_plan(int64_t total, int32_t old_nd, int32_t new_nd, int32_t new
 #define SHARDSTEP_PATH_TMA 2
 int32_t shardstep_set_fused_path(int32_t path);
 
-/* Whether the second and later kernels of one call are launched as
- * programmatic dependents of the previous kernel of that call (they may
- * start while it drains; each still ends after it), process-wide: the
- * buckets of ddp_bucket_allreduce_avg and the copy kernels of
- * fsdp_flat_pack, fsdp_ag_unpack, fsdp2_chunk_cat and
- * fsdp2_all_gather_copy_out.  The first kernel of a call is always an
- * ordinary launch, so it waits for everything before it in the stream.
- * 1 (default) = yes, 0 = ordinary launches.  Results do not depend on it.
- * Returns the previous setting. */
+/* Whether kernels are launched as programmatic dependents of the kernel
+ * before them in the stream, process-wide.  The first kernel of a call (the
+ * fused steps, the accumulation, the step-state kernels, the first copy of
+ * a pack or all-gather) may then be scheduled while its predecessor drains,
+ * but waits for that predecessor to complete before it touches memory, so
+ * only the launch latency overlaps and stream order holds whatever the
+ * predecessor is; the second and later kernels of one call (the buckets of
+ * ddp_bucket_allreduce_avg, the copy kernels of fsdp_flat_pack,
+ * fsdp_ag_unpack, fsdp2_chunk_cat and fsdp2_all_gather_copy_out: disjoint
+ * work) start while the previous one drains and wait for it only before
+ * they end.  The first bucket of an all-reduce, the non-finite check and
+ * the TMA-staged kernels' first launches stay ordinary launches.  1
+ * (default) = yes, 0 = ordinary launches everywhere.  Results do not depend
+ * on it.  Returns the previous setting. */
 int32_t shardstep_set_dependent_launch(int32_t enable);
 
 /* Sets the shared-memory stages of each TMA-staged launch, process-wide:

@@ -120,6 +120,7 @@ __global__ void __launch_bounds__(kAccThreads, acc_min_blocks<ND>())
                              float* __restrict__ P, float* __restrict__ M,
                              float* __restrict__ V, uint16_t* __restrict__ out, AdamScalars c,
                              MeanOp mo) {
+    pdl_enter();
     c = resolve_adam(c);
     const int64_t nvec = S >> 2;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kAccThreads;
@@ -152,6 +153,7 @@ __global__ void __launch_bounds__(kThreads)
                                float* __restrict__ P, float* __restrict__ M,
                                float* __restrict__ V, uint16_t* __restrict__ out,
                                AdamScalars c, MeanOp mo) {
+    pdl_enter();
     c = resolve_adam(c);
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
     for (int64_t j = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; j < S;
@@ -166,10 +168,11 @@ cudaError_t go_accum(const PtrTable& acc, const PtrTable& last, int nd, int64_t 
     const int64_t blocks = ((S >> 2) + kAccThreads - 1) / kAccThreads;
     const int64_t cap = (int64_t{1} << 31) - 1;
     const unsigned grid = static_cast<unsigned>(blocks < 1 ? 1 : (blocks > cap ? cap : blocks));
-    accum_rs_adamw_cast_vec4<ND, GROUPED><<<grid, kAccThreads, 0, s>>>(acc, last, nd, S, scale,
-                                                                        P, M, V, out, c, mo);
+    const cudaError_t e = launch_after(accum_rs_adamw_cast_vec4<ND, GROUPED>, dim3(grid),
+                                       dim3(kAccThreads), 0, s, acc, last, nd, S, scale, P, M, V,
+                                       out, c, mo);
     note_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace
@@ -202,10 +205,12 @@ cudaError_t launch_accum_rs_adamw_cast(const PtrTable& acc, const PtrTable& last
                         resident_blocks(reinterpret_cast<const void*>(accum_rs_adamw_cast_scalar),
                                         kThreads);
     const int64_t g = want < cap ? want : cap;
-    accum_rs_adamw_cast_scalar<<<static_cast<unsigned>(g < 1 ? 1 : g), kThreads, 0, stream>>>(
-        acc, last, nd, S, scale, master, m, v, out, c, mo);
+    const cudaError_t e = launch_after(accum_rs_adamw_cast_scalar,
+                                       dim3(static_cast<unsigned>(g < 1 ? 1 : g)), dim3(kThreads),
+                                       0, stream, acc, last, nd, S, scale, master, m, v, out, c,
+                                       mo);
     note_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace shardstep

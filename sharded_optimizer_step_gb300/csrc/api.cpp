@@ -218,6 +218,8 @@ std::vector<OccEntry> g_occ;
 
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
+bool dependent_launches() { return g_dependent_launch.load(std::memory_order_relaxed) != 0; }
+
 // Error reporting for ckpt.cpp: the message is fmt with one string and one
 // integer argument (either may be unused).
 int ckpt_fail(int code, const char* fmt, const char* a, long long b) {
@@ -433,10 +435,12 @@ struct CopyBatcher {
     AlignedTable st;  // aligned destination, unaligned source (copy16_shift)
     cudaStream_t stream;
     int rc = SHARDSTEP_OK;
-    // whether this call has launched a kernel: the first launch waits for
-    // everything before it in the stream, the later ones (disjoint copies
-    // of the same call) go out as programmatic dependents of the previous
-    // unless dependent launches are switched off
+    // whether this call has launched a kernel.  With dependent launches on
+    // (the default) every launch goes out as a programmatic dependent of the
+    // kernel before it in the stream: the first one of the call waits for
+    // that unknown predecessor before it touches memory, the later ones
+    // (disjoint copies of the same call) only before they end, so that each
+    // overlaps the previous one's drain
     bool launched = false;
     const bool pdl_ok = g_dependent_launch.load(std::memory_order_relaxed) != 0;
     explicit CopyBatcher(cudaStream_t s) : stream(s) {
@@ -500,7 +504,7 @@ struct CopyBatcher {
     }
     void flush_vector() {
         if (t.n == 0 || rc != SHARDSTEP_OK) return;
-        cudaError_t e = launch_copy(t, launched && pdl_ok, stream);
+        cudaError_t e = launch_copy(t, pdl_ok, !launched, stream);
         if (e != cudaSuccess) rc = cuda_fail(e, "copy kernel launch");
         launched = true;
         t.n = 0;
@@ -508,9 +512,8 @@ struct CopyBatcher {
     }
     void flush_chunked(AlignedTable& tab) {
         if (tab.n == 0 || rc != SHARDSTEP_OK) return;
-        const bool pdl = launched && pdl_ok;
-        cudaError_t e = &tab == &bt ? launch_copy16(tab, pdl, stream)
-                                    : launch_copy16_shift(tab, pdl, stream);
+        cudaError_t e = &tab == &bt ? launch_copy16(tab, pdl_ok, !launched, stream)
+                                    : launch_copy16_shift(tab, pdl_ok, !launched, stream);
         if (e != cudaSuccess) rc = cuda_fail(e, "aligned copy kernel launch");
         launched = true;
         tab.n = 0;

@@ -77,6 +77,19 @@ __device__ __forceinline__ void pdl_trigger() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// The start of a kernel that may be launched as a programmatic dependent of
+// whatever kernel precedes it in the stream (the first kernel of a call, see
+// launch_after): it waits for the preceding grid to complete, with that
+// grid's memory visible, before it touches any memory, and only then lets
+// its own dependents be scheduled.  The order matters: a dependent that
+// waits only at its end (a later copy of the same call) starts its work as
+// soon as every block of this grid has triggered, so triggering before the
+// wait would let it read what the predecessor is still writing.  Only the
+// launch latency overlaps; for an ordinary launch both return at once.
+__device__ __forceinline__ void pdl_enter() {
+    pdl_wait();
+    pdl_trigger();
+}
 
 // ------------------------------------------------------------------- bf16
 

@@ -87,7 +87,8 @@ __device__ __forceinline__ void copy_vecs(const char* src, char* dst, int64_t v0
     }
 }
 
-__global__ void __launch_bounds__(kThreads) copy_segments(CopyTable t) {
+__global__ void __launch_bounds__(kThreads) copy_segments(CopyTable t, int wait_first) {
+    if (wait_first) pdl_wait();   // before the trigger: see pdl_enter
     pdl_trigger();
     int seg = 0;
     for (int64_t c = blockIdx.x; c < t.total_chunks; c += gridDim.x) {
@@ -119,7 +120,8 @@ __global__ void __launch_bounds__(kThreads) copy_segments(CopyTable t) {
     pdl_wait();
 }
 
-__global__ void __launch_bounds__(kThreads, 8) copy16(AlignedTable t) {
+__global__ void __launch_bounds__(kThreads, 8) copy16(AlignedTable t, int wait_first) {
+    if (wait_first) pdl_wait();   // before the trigger: see pdl_enter
     pdl_trigger();
     const int64_t c = blockIdx.x;
     int lo = 0, hi = t.n - 1;  // the range owning chunk c (chunk0 increasing)
@@ -161,7 +163,8 @@ __device__ __forceinline__ uint4 shift_pair(const uint4& a, const uint4& b, int 
                       __funnelshift_r(w2, w3, sh), __funnelshift_r(w3, w4, sh));
 }
 
-__global__ void __launch_bounds__(kThreads, 5) copy16_shift(AlignedTable t) {
+__global__ void __launch_bounds__(kThreads, 5) copy16_shift(AlignedTable t, int wait_first) {
+    if (wait_first) pdl_wait();   // before the trigger: see pdl_enter
     pdl_trigger();
     const int64_t c = blockIdx.x;
     int lo = 0, hi = t.n - 1;  // the range owning chunk c (chunk0 increasing)
@@ -216,6 +219,7 @@ template <bool FIRST>
 __global__ void __launch_bounds__(kThreads, 8)
     accumulate_vec8(const uint16_t* __restrict__ g, float* __restrict__ acc, int64_t n,
                     float scale) {
+    pdl_enter();
     const int64_t nvec = n >> 3;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < nvec;
@@ -244,6 +248,7 @@ template <bool FIRST>
 __global__ void __launch_bounds__(kThreads)
     accumulate_scalar(const uint16_t* __restrict__ g, float* __restrict__ acc, int64_t n,
                       float scale) {
+    pdl_enter();
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
     for (int64_t j = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; j < n;
          j += stride)
@@ -265,13 +270,14 @@ unsigned grid_one_pass(int64_t vectors) {
 }
 
 template <typename Table>
-cudaError_t launch_table(void (*kernel)(Table), unsigned grid, const Table& t, bool pdl,
-                         cudaStream_t stream) {
+cudaError_t launch_table(void (*kernel)(Table, int), unsigned grid, const Table& t, bool pdl,
+                         bool wait_first, cudaStream_t stream) {
     cudaError_t e;
     if (pdl) {
-        e = launch_dependent(kernel, dim3(grid), dim3(kThreads), 0, stream, t);
+        e = launch_dependent(kernel, dim3(grid), dim3(kThreads), 0, stream, t,
+                             wait_first ? 1 : 0);
     } else {
-        kernel<<<grid, kThreads, 0, stream>>>(t);
+        kernel<<<grid, kThreads, 0, stream>>>(t, 0);
         e = cudaGetLastError();
     }
     note_launch();
@@ -280,39 +286,35 @@ cudaError_t launch_table(void (*kernel)(Table), unsigned grid, const Table& t, b
 
 }  // namespace
 
-cudaError_t launch_copy(const CopyTable& t, bool pdl, cudaStream_t stream) {
+cudaError_t launch_copy(const CopyTable& t, bool pdl, bool wait_first, cudaStream_t stream) {
     const int64_t cap = static_cast<int64_t>(device_sms()) *
                         resident_blocks(reinterpret_cast<const void*>(copy_segments), kThreads);
     const int64_t g = t.total_chunks < cap ? t.total_chunks : cap;
-    return launch_table(copy_segments, static_cast<unsigned>(g < 1 ? 1 : g), t, pdl, stream);
+    return launch_table(copy_segments, static_cast<unsigned>(g < 1 ? 1 : g), t, pdl, wait_first,
+                        stream);
 }
 
-cudaError_t launch_copy16(const AlignedTable& t, bool pdl, cudaStream_t stream) {
-    return launch_table(copy16, static_cast<unsigned>(t.total_chunks), t, pdl, stream);
+cudaError_t launch_copy16(const AlignedTable& t, bool pdl, bool wait_first, cudaStream_t stream) {
+    return launch_table(copy16, static_cast<unsigned>(t.total_chunks), t, pdl, wait_first,
+                        stream);
 }
 
-cudaError_t launch_copy16_shift(const AlignedTable& t, bool pdl, cudaStream_t stream) {
-    return launch_table(copy16_shift, static_cast<unsigned>(t.total_chunks), t, pdl, stream);
+cudaError_t launch_copy16_shift(const AlignedTable& t, bool pdl, bool wait_first,
+                                cudaStream_t stream) {
+    return launch_table(copy16_shift, static_cast<unsigned>(t.total_chunks), t, pdl, wait_first,
+                        stream);
 }
 
 cudaError_t launch_accumulate(const uint16_t* g, float* acc, int64_t n, float scale, bool first,
                               bool vec, cudaStream_t stream) {
-    if (vec) {
-        const unsigned grid = grid_one_pass(n >> 3);
-        if (first)
-            accumulate_vec8<true><<<grid, kThreads, 0, stream>>>(g, acc, n, scale);
-        else
-            accumulate_vec8<false><<<grid, kThreads, 0, stream>>>(g, acc, n, scale);
-    } else if (first) {
-        accumulate_scalar<true><<<grid_for(reinterpret_cast<const void*>(accumulate_scalar<true>), n),
-                                  kThreads, 0, stream>>>(g, acc, n, scale);
-    } else {
-        accumulate_scalar<false><<<grid_for(reinterpret_cast<const void*>(accumulate_scalar<false>),
-                                            n),
-                                   kThreads, 0, stream>>>(g, acc, n, scale);
-    }
+    auto kernel = vec ? (first ? accumulate_vec8<true> : accumulate_vec8<false>)
+                      : (first ? accumulate_scalar<true> : accumulate_scalar<false>);
+    const unsigned grid = vec ? grid_one_pass(n >> 3)
+                              : grid_for(reinterpret_cast<const void*>(kernel), n);
+    const cudaError_t e = launch_after(kernel, dim3(grid), dim3(kThreads), 0, stream, g, acc, n,
+                                       scale);
     note_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace shardstep

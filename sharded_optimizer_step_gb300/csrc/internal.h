@@ -111,6 +111,30 @@ cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, si
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
 }
 
+// Whether kernels go out as programmatic dependent launches
+// (shardstep_set_dependent_launch; api.cpp).
+bool dependent_launches();
+
+// Launches `kernel` as a programmatic dependent of the previous kernel in the
+// stream when dependent launches are on, else as an ordinary launch.  The
+// kernel must begin with pdl_enter() (it waits for its predecessor before it
+// touches memory), so stream order holds whatever the predecessor is.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_after(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                         cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = dependent_launches() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // Launch bookkeeping (api.cpp).
 void note_launch();
 int device_sms();                                   // SMs of the current device (cached)
@@ -174,15 +198,19 @@ cudaError_t launch_ddp_allreduce_adamw_cast(const PtrTable& tab, int nd, int64_t
 cudaError_t launch_mean_division_check(const MeanOp& mo, unsigned long long* mismatches,
                                        unsigned int* first_bad, cudaStream_t stream);
 // The copy launchers' `pdl`: launch as a programmatic dependent of the
-// previous kernel in the stream (only for a later launch of the same batch
-// of disjoint copies; every copy kernel waits for its predecessor before it
-// ends, so the batch's last kernel completes after all of them).
-cudaError_t launch_copy(const CopyTable& t, bool pdl, cudaStream_t stream);
+// previous kernel in the stream.  `wait_first`: the kernel waits for that
+// predecessor before it touches memory (the first launch of a call, whose
+// predecessor is unknown); without it the kernel waits only before it ends
+// (a later launch of the same batch of disjoint copies, so that it overlaps
+// the previous one's drain; the batch's last kernel still completes after
+// all of them).
+cudaError_t launch_copy(const CopyTable& t, bool pdl, bool wait_first, cudaStream_t stream);
 // Aligned copy (copy.cu): one block per 16 KB chunk of 16-byte vectors.
-cudaError_t launch_copy16(const AlignedTable& t, bool pdl, cudaStream_t stream);
+cudaError_t launch_copy16(const AlignedTable& t, bool pdl, bool wait_first, cudaStream_t stream);
 // Realigning copy (copy.cu): like copy16, but every source starts 1..15
 // bytes past a 16-byte boundary (destinations and sizes 16-byte multiples).
-cudaError_t launch_copy16_shift(const AlignedTable& t, bool pdl, cudaStream_t stream);
+cudaError_t launch_copy16_shift(const AlignedTable& t, bool pdl, bool wait_first,
+                                cudaStream_t stream);
 cudaError_t launch_accumulate(const uint16_t* g, float* acc, int64_t n, float scale, bool first,
                               bool vec, cudaStream_t stream);
 // The last micro-batch's accumulation fused into the step (accum_step.cu):

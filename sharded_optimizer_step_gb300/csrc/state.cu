@@ -26,6 +26,7 @@ __device__ void derive_adam_scalars(float* out, double b1p, double b2p, double l
 __global__ void adamw_state_set_kernel(shardstep_adamw_state_t* st, int64_t step, double b1p,
                                        double b2p, double lr, double beta1, double beta2,
                                        double eps, double wd) {
+    pdl_enter();
     if (threadIdx.x != 0 || blockIdx.x != 0) return;
     st->step = step;
     st->beta1_pow = b1p;
@@ -42,6 +43,7 @@ __global__ void adamw_state_set_kernel(shardstep_adamw_state_t* st, int64_t step
 __global__ void adamw_state_advance_kernel(shardstep_adamw_state_t* st, double lr, double beta1,
                                            double beta2, double eps, double wd,
                                            const unsigned int* skip) {
+    pdl_enter();
     if (threadIdx.x != 0 || blockIdx.x != 0) return;
     if (skip_step(skip)) return;
     const double b1p = __dmul_rn(st->beta1_pow, beta1);
@@ -57,18 +59,19 @@ __global__ void adamw_state_advance_kernel(shardstep_adamw_state_t* st, double l
 cudaError_t launch_adamw_state_set(shardstep_adamw_state_t* state, int64_t step, double b1p,
                                    double b2p, double lr, double beta1, double beta2, double eps,
                                    double wd, cudaStream_t stream) {
-    adamw_state_set_kernel<<<1, 32, 0, stream>>>(state, step, b1p, b2p, lr, beta1, beta2, eps,
-                                                 wd);
+    const cudaError_t e = launch_after(adamw_state_set_kernel, dim3(1), dim3(32), 0, stream,
+                                       state, step, b1p, b2p, lr, beta1, beta2, eps, wd);
     note_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t launch_adamw_state_advance(shardstep_adamw_state_t* state, double lr, double beta1,
                                        double beta2, double eps, double wd,
                                        const unsigned int* skip, cudaStream_t stream) {
-    adamw_state_advance_kernel<<<1, 32, 0, stream>>>(state, lr, beta1, beta2, eps, wd, skip);
+    const cudaError_t e = launch_after(adamw_state_advance_kernel, dim3(1), dim3(32), 0, stream,
+                                       state, lr, beta1, beta2, eps, wd, skip);
     note_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace shardstep

@@ -215,6 +215,7 @@ __global__ void __launch_bounds__(kStepThreads, kStepMinBlocks)
     rs_adamw_cast_vec4(PtrTable tab, int nd, int64_t S, float* __restrict__ P,
                        float* __restrict__ M, float* __restrict__ V, uint16_t* __restrict__ out,
                        AdamScalars c, MeanOp mo, const unsigned int* skip) {
+    pdl_enter();
     if (skip_step(skip)) return;
     mo = resolve_scale(mo);
     c = resolve_adam(c);
@@ -250,6 +251,7 @@ __global__ void __launch_bounds__(kThreads)
                          float* __restrict__ M, float* __restrict__ V,
                          uint16_t* __restrict__ out, AdamScalars c, MeanOp mo,
                          const unsigned int* skip) {
+    pdl_enter();
     if (skip_step(skip)) return;
     c = resolve_adam(c);
     mo = resolve_scale(mo);
@@ -280,6 +282,7 @@ __global__ void __launch_bounds__(kStepThreads, kStepMinBlocks)
                                   float* __restrict__ P, float* __restrict__ M,
                                   float* __restrict__ V, uint16_t* __restrict__ out,
                                   AdamScalars c, MeanOp mo) {
+    pdl_enter();
     c = resolve_adam(c);
     const int64_t nvec = n >> 2;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kStepThreads;
@@ -324,6 +327,7 @@ __global__ void __launch_bounds__(kThreads)
                                     uint16_t* __restrict__ mean_out, float* __restrict__ P,
                                     float* __restrict__ M, float* __restrict__ V,
                                     uint16_t* __restrict__ out, AdamScalars c, MeanOp mo) {
+    pdl_enter();
     c = resolve_adam(c);
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
     for (int64_t j = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; j < n;
@@ -637,11 +641,12 @@ struct StepArgs {
 
 template <int ND, int GT>
 cudaError_t go_vec(const StepArgs& a, cudaStream_t s) {
-    auto k = rs_adamw_cast_vec4<ND, GT>;
     const unsigned grid = grid_one_pass(a.S >> 2);
-    k<<<grid, kStepThreads, 0, s>>>(a.tab, a.nd, a.S, a.P, a.M, a.V, a.out, a.c, a.mo, a.skip);
+    const cudaError_t e = launch_after(rs_adamw_cast_vec4<ND, GT>, dim3(grid), dim3(kStepThreads),
+                                       0, s, a.tab, a.nd, a.S, a.P, a.M, a.V, a.out, a.c, a.mo,
+                                       a.skip);
     note_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 template <int GT>
@@ -667,10 +672,10 @@ cudaError_t dispatch_vec(const StepArgs& a, cudaStream_t s) {
 template <int GT>
 cudaError_t go_scalar(const StepArgs& a, cudaStream_t s) {
     const unsigned grid = grid_for(reinterpret_cast<const void*>(rs_adamw_cast_scalar<GT>), a.S);
-    rs_adamw_cast_scalar<GT><<<grid, kThreads, 0, s>>>(a.tab, a.nd, a.S, a.P, a.M, a.V, a.out, a.c,
-                                                       a.mo, a.skip);
+    const cudaError_t e = launch_after(rs_adamw_cast_scalar<GT>, dim3(grid), dim3(kThreads), 0, s,
+                                       a.tab, a.nd, a.S, a.P, a.M, a.V, a.out, a.c, a.mo, a.skip);
     note_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 template <int ND>
@@ -800,15 +805,17 @@ cudaError_t launch_ddp_allreduce_adamw_cast(const PtrTable& tab, int nd, int64_t
     if (!vec) {
         const unsigned grid = grid_for(
             reinterpret_cast<const void*>(ddp_allreduce_adamw_cast_scalar), n);
-        ddp_allreduce_adamw_cast_scalar<<<grid, kThreads, 0, stream>>>(tab, nd, n, mean_out,
-                                                                      master, m, v, out, c, mo);
+        const cudaError_t e = launch_after(ddp_allreduce_adamw_cast_scalar, dim3(grid),
+                                           dim3(kThreads), 0, stream, tab, nd, n, mean_out,
+                                           master, m, v, out, c, mo);
         note_launch();
-        return cudaGetLastError();
+        return e;
     }
     const unsigned grid = grid_one_pass(n >> 2);
-#define SHARDSTEP_DDP_GO(K)                                                                   \
-    ddp_allreduce_adamw_cast_vec4<K><<<grid, kStepThreads, 0, stream>>>(tab, nd, n, mean_out, \
-                                                                        master, m, v, out, c, mo)
+    cudaError_t e = cudaSuccess;
+#define SHARDSTEP_DDP_GO(K)                                                                    \
+    e = launch_after(ddp_allreduce_adamw_cast_vec4<K>, dim3(grid), dim3(kStepThreads), 0, stream, \
+                     tab, nd, n, mean_out, master, m, v, out, c, mo)
     switch (nd) {
         case 1: SHARDSTEP_DDP_GO(1); break;
         case 2: SHARDSTEP_DDP_GO(2); break;
@@ -823,7 +830,7 @@ cudaError_t launch_ddp_allreduce_adamw_cast(const PtrTable& tab, int nd, int64_t
     }
 #undef SHARDSTEP_DDP_GO
     note_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t launch_mean_division_check(const MeanOp& mo, unsigned long long* mismatches,
