@@ -374,3 +374,46 @@ def test_shard_pieces_of_the_worked_example_and_bad_arguments():
     for nd, rank in ((2, 2), (2, -1), (0, 0)):
         with pytest.raises(ss.ShardstepError):
             ss.fsdp_shard_pieces([8, 8, 8], nd, rank)
+
+
+def test_new_entry_points_reject_bad_arguments_before_launch():
+    """The fused DDP step, the watchdog limit and the division self-check
+    validate everything on the host; nothing here reaches the GPU."""
+    L = _capi.lib()
+    A = 1 << 40
+    n = 4096
+    boff = _capi.i64_array([0, n])
+    grads = _capi.ptr_array([A, A + 2 * n])
+    master, m, v = (ctypes.c_void_p(A + (1 << 20) * k) for k in (1, 2, 3))
+    params = ctypes.c_void_p(A + (1 << 20) * 4)
+    hp = ss.AdamW().at_step(1)
+    call = L.ddp_bucket_allreduce_avg_adamw_cast
+    # params is gradient 1
+    assert call(grads, 2, boff, 0, 1, None, master, m, v, ctypes.c_void_p(A + 2 * n),
+                ctypes.byref(hp), None) == _capi.ERR_INVALID
+    # m is v
+    assert call(grads, 2, boff, 0, 1, None, master, v, v, params, ctypes.byref(hp),
+                None) == _capi.ERR_INVALID
+    # the mean is the parameters
+    assert call(grads, 2, boff, 0, 1, params, master, m, v, params, ctypes.byref(hp),
+                None) == _capi.ERR_INVALID
+    # decreasing bucket offsets, a null gradient, too many ranks, step 0
+    assert call(grads, 2, _capi.i64_array([0, n, 5]), 0, 2, None, master, m, v, params,
+                ctypes.byref(hp), None) == _capi.ERR_INVALID
+    assert call(_capi.ptr_array([A, 0]), 2, boff, 0, 1, None, master, m, v, params,
+                ctypes.byref(hp), None) == _capi.ERR_INVALID
+    assert call(grads, _capi.MAX_ND + 1, boff, 0, 1, None, master, m, v, params,
+                ctypes.byref(hp), None) == _capi.ERR_CAPACITY
+    hp0 = ss.AdamW().at_step(0)
+    assert call(grads, 2, boff, 0, 1, None, master, m, v, params, ctypes.byref(hp0),
+                None) == _capi.ERR_INVALID
+    # an empty range is accepted and launches nothing
+    assert call(grads, 2, _capi.i64_array([0, 0]), 0, 1, None, master, m, v, params,
+                ctypes.byref(hp), None) == _capi.OK
+    assert L.shardstep_set_tma_wait_ns(-5) == _capi.ERR_INVALID
+    check = L.shardstep_check_mean_division
+    for nd in (0, _capi.MAX_ND + 1):
+        assert check(nd, ctypes.c_void_p(A), ctypes.c_void_p(A + 8), None) == _capi.ERR_INVALID
+    assert check(3, None, ctypes.c_void_p(A + 8), None) == _capi.ERR_INVALID
+    assert check(3, ctypes.c_void_p(A + 4), ctypes.c_void_p(A + 8), None) == _capi.ERR_INVALID
+    assert b"misaligned" in L.shardstep_last_error()
