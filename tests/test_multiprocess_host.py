@@ -135,7 +135,8 @@ def test_sharded_step_across_two_processes_equals_the_emulation():
 
 @pytest.mark.parametrize("workload", ["llama_7b_rank0_nd8", "llama_1b_rank0_nd8_m4",
                                       "ddp_nd8_buckets", "llama_7b_layer_ragged_nd8",
-                                      "llama_7b_fsdp2_layer_nd8"])
+                                      "llama_7b_fsdp2_layer_nd8", "unit_9m_nd4_m4",
+                                      "gpt2_small_nd8"])
 def test_reference_arm_under_torchrun_prints_once(workload):
     """Launched the way the N > 1 runs are, the oracle arm runs on rank 0
     alone and prints one JSON line; the other rank exits 0."""
@@ -143,7 +144,7 @@ def test_reference_arm_under_torchrun_prints_once(workload):
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
            "--master-addr", "127.0.0.1", "--master-port", str(port), "bench.py",
            "--impl", "reference", "--workload", workload, "--gpus", "2",
-           "--steps", "1", "--warmup", "0"]
+           "--steps", "1", "--warmup", "0", "--cpu-seconds", "1"]
     r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
