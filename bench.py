@@ -1791,9 +1791,9 @@ def run_ddp(args):
 UNIT9M_WORKLOAD = "unit_9m_nd4_m4"
 GPT2_WORKLOAD = "gpt2_small_nd8"
 SMALL_METRICS = {
-    UNIT9M_WORKLOAD: ("whole-job step HBM GB/s: 4 ranks x (3 micro-batch accumulations + fused "
-                      "last micro-batch rs_avg+AdamW+bf16 cast) + all-gather, one 9.4M-param "
-                      "unit, N_d=4, M=4"),
+    UNIT9M_WORKLOAD: ("whole-job step HBM GB/s: 3 micro-batch accumulations of the 4 ranks' "
+                      "gradients + 4 fused last micro-batch rs_avg+AdamW+bf16 cast launches + "
+                      "all-gather, one 9.4M-param unit, N_d=4, M=4"),
     GPT2_WORKLOAD: ("whole-job step HBM GB/s: 8 rank-view fused rs_avg+AdamW+bf16 cast launches "
                     "over 13 units + all-gather of one block unit, GPT-2 small, N_d=8"),
 }
@@ -1820,24 +1820,25 @@ class _SmallJob:
             shapes = w.units[0]
             lay = self.lay = ss.fsdp_layout(w.unit_numels(0), nd)
             S, P = lay.shard, lay.padded
+            # micro-batch j's gradients of all N_d ranks side by side (rank q's
+            # packed unit at q*P), like the accumulators: one accumulate
+            # launch per micro-batch covers the whole job
             tens = [torch.empty(s, dtype=bf16, device=dev) for s in shapes]
             self.g = []
-            for q in range(nd):
-                row = []
-                for j in range(M):
-                    flat = torch.empty(P, dtype=bf16, device=dev)
+            for j in range(M):
+                flat = torch.empty(nd * P, dtype=bf16, device=dev)
+                for q in range(nd):
                     for t, x in enumerate(tens):
                         synth.dev_fill(w.grad_stream(1, q, j, 0, t), x.view(-1))
-                    ss.fsdp_flat_pack(tens, nd, flat=flat)
-                    row.append(flat)
-                self.g.append(row)
+                    ss.fsdp_flat_pack(tens, nd, flat=flat[q * P:(q + 1) * P])
+                self.g.append(flat)
             mt = [torch.empty(s, dtype=f32, device=dev) for s in shapes]
             for t, x in enumerate(mt):
                 synth.dev_fill(w.master_stream(0, t), x.view(-1))
             self.master = ss.fsdp_flat_pack(mt, nd)
             self.m = torch.zeros(P, dtype=f32, device=dev)
             self.v = torch.zeros(P, dtype=f32, device=dev)
-            self.acc = [torch.empty(P, dtype=f32, device=dev) for _ in range(nd)]
+            self.acc = torch.empty(nd * P, dtype=f32, device=dev)
             self.outs = [torch.empty(S, dtype=bf16, device=dev) for _ in range(nd)]
             self.full = torch.empty(P, dtype=bf16, device=dev)
             self.S, self.P = S, P
@@ -1882,11 +1883,10 @@ class _SmallJob:
         if ev is not None:
             ev[0].record()
         if self.name == UNIT9M_WORKLOAD:
-            S = self.S
+            S, P = self.S, self.P
             inv_m = float(1.0 / M)
-            for q in range(nd):
-                for j in range(M - 1):
-                    ss.fsdp_grad_accumulate(self.g[q][j], self.acc[q], inv_m, j == 0)
+            for j in range(M - 1):
+                ss.fsdp_grad_accumulate(self.g[j], self.acc, inv_m, j == 0)
             if ev is not None:
                 ev[1].record()
             if graph_form:
@@ -1895,8 +1895,9 @@ class _SmallJob:
                 self.t += 1
             for r in range(nd):
                 sl = slice(r * S, (r + 1) * S)
-                args = ([a[sl] for a in self.acc], [gq[M - 1][sl] for gq in self.g], inv_m,
-                        self.master[sl], self.m[sl], self.v[sl], self.outs[r])
+                args = ([self.acc[q * P + r * S:q * P + (r + 1) * S] for q in range(nd)],
+                        [self.g[M - 1][q * P + r * S:q * P + (r + 1) * S] for q in range(nd)],
+                        inv_m, self.master[sl], self.m[sl], self.v[sl], self.outs[r])
                 if graph_form:
                     ss.fsdp_state_accumulate_rs_avg_adamw_cast(*args, self.state)
                 else:
@@ -1924,7 +1925,7 @@ class _SmallJob:
         """(device buffer, pinned host copy) of every gradient input: what an
         end-to-end step brings in from the host."""
         torch = self.torch
-        bufs = ([g for row in self.g for g in row] if self.name == UNIT9M_WORKLOAD
+        bufs = (list(self.g) if self.name == UNIT9M_WORKLOAD
                 else [x for o in self.opts for x in o.grad_in])
         return [(b, torch.empty(b.shape, dtype=b.dtype, pin_memory=True).copy_(b)) for b in bufs]
 
@@ -2074,7 +2075,7 @@ def run_small(args):
         dom_ms = parts[dom_name]["ms"]
         dom_kernel = ("accumulate_vec8 (register-staged)" if dom_name == "accumulate"
                       else "rs_adamw_cast_vec4<8, bf16> (register-staged)")
-        n_launch = (job.w.nd * (job.w.micro - 1) if dom_name == "accumulate" else job.w.nd)
+        n_launch = job.w.micro - 1 if dom_name == "accumulate" else job.w.nd
         roof = _roofline(dom_bytes / (dom_ms / 1e3) / 1e9, f"{dom_kernel}, {n_launch} launches "
                          f"per step ({dom_name})", dom_bytes // n_launch)
     else:
