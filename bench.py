@@ -1786,7 +1786,7 @@ def run_ddp(args):
     _finish_dist(world)
 
 
-# ------------------------------------- small configurations: the whole job
+# ------------------------------------ small workloads: the whole job
 
 UNIT9M_WORKLOAD = "unit_9m_nd4_m4"
 GPT2_WORKLOAD = "gpt2_small_nd8"
@@ -1801,7 +1801,7 @@ L2_FLUSH_BYTES = 256 << 20          # written between timed steps: twice the 129
 
 
 class _SmallJob:
-    """The whole data-parallel job of a small configuration on one GPU: every
+    """The whole data-parallel job of a small workload on one GPU: every
     emulated rank's step, so that launch latency and the small arrays are what
     is measured.  Inputs (gradients of every rank and micro-batch, fp32
     master) are seeded, packed / placed by the library's layout and resident
@@ -1993,7 +1993,7 @@ def _small_oracle(w_name, budget_s):
 
 
 def run_small(args):
-    """Configurations 1 and 2 of the path: a 9.4M-parameter unit (N_d = 4,
+    """The two small model-shaped workloads: a 9.4M-parameter unit (N_d = 4,
     M = 4) and the GPT-2 small model (N_d = 8), each as its whole job on one
     GPU.  At these sizes (a step of 1.5 GB and 5.3 GB) launch latency is part
     of the answer, so the line gives the eager step and, with --graph, the
