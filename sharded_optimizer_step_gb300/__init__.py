@@ -722,9 +722,12 @@ def set_tma_stages(stages: int) -> int:
 
 
 def set_dependent_launch(enable: bool) -> bool:
-    """Whether later buckets of one all-reduce call are launched as
-    programmatic dependents of the previous bucket (default True).  Results
-    do not depend on it; returns the previous setting."""
+    """Whether kernels are launched as programmatic dependents of the kernel
+    before them in the stream (default True): each call's first kernel
+    waits for its predecessor before touching memory (only the launch
+    latency overlaps), later buckets / copies of one call overlap the
+    previous one's drain.  Results do not depend on it; returns the previous
+    setting."""
     return bool(_capi.lib().shardstep_set_dependent_launch(int(bool(enable))))
 
 

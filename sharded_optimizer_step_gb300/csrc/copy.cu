@@ -30,13 +30,16 @@
 // the destination to that alignment and the tail is copied byte-wise, both by
 // the lanes of the block that owns the segment's first / last chunk.
 //
-// One call's copies are disjoint and read nothing the call writes, so the
-// second and later launches of a call go out as programmatic dependents:
-// each copy kernel lets the next one be scheduled as soon as all of its own
-// blocks have started, and every block waits for the previous grid of the
-// call before it ends (both no-ops for an ordinary launch).  A call that
-// mixes congruent and realigned ranges, heads and tails then runs without
-// an idle gap between its kernels.
+// Every launch of a call goes out as a programmatic dependent of the kernel
+// before it (unless dependent launches are switched off).  The first one
+// (wait_first) waits for that unknown predecessor before it touches memory
+// and only then lets the next kernel be scheduled.  One call's copies are
+// disjoint and read nothing the call writes, so the second and later ones
+// let the next kernel be scheduled as soon as all of their own blocks have
+// started and wait for the previous grid of the call only before they end
+// (both no-ops for an ordinary launch): a call that mixes congruent and
+// realigned ranges, heads and tails runs without an idle gap between its
+// kernels.
 #include "common.cuh"
 
 namespace shardstep {
