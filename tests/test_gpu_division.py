@@ -8,8 +8,9 @@ for a power of two, else RN(1/N_d) and one fma correction); the first test
 runs that division and IEEE fp32 division on all 2^32 fp32 bit patterns for
 every N_d the library accepts and requires the same bits everywhere.  The
 others compare the bucket all-reduce and the gradient scaler's check at N_d =
-3, 5, 6 and 7 with the oracle, under every kernel choice, on buckets with
-ragged tails, unaligned starts and one planted non-finite value."""
+3, 5, 6 and 7 (and at 9..64, past the compiled counts) with the oracle,
+under every kernel choice, on buckets with ragged tails, unaligned starts
+and one planted non-finite value."""
 import numpy as np
 import pytest
 import torch
@@ -139,3 +140,30 @@ def test_fused_step_non_power_of_two_nd_matches_oracle(nd, path):
     assert_bits(m.cpu().numpy(), m1, "m")
     assert_bits(v.cpu().numpy(), v1, "v")
     assert_bits(out.cpu().numpy().view(np.uint16), o1, "bf16")
+
+
+@pytest.mark.parametrize("nd", [9, 16, 23, 33, 64])
+def test_light_kernels_at_large_nd_match_oracle(nd, path):
+    """Past N_d = 8 the all-reduce and the check take the TMA-staged kernel
+    where two stages fit (N_d <= 22 for 16-bit slices) and the register
+    kernel's loop over batches of 8 slices beyond: both against the oracle,
+    buckets with a ragged tail and an unaligned start, one planted inf."""
+    boff = [0, 2048 * 152 + 4099, 2048 * 152 + 4099 + 13, 2048 * 152 + 4099 + 13 + 70_001]
+    total = boff[-1]
+    gh = [synth.host_fill(synth.normal_stream(nd, (84, q), 1e-3), 0, total, "bf16")
+          for q in range(nd)]
+    out = torch.empty(total, dtype=torch.int16, device=DEV)
+    ss.ddp_bucket_allreduce_avg([_dev16(h).view(torch.bfloat16) for h in gh], boff,
+                                out.view(torch.bfloat16))
+    torch.cuda.synchronize()
+    assert_bits(out.cpu().numpy().view(np.uint16), oracle.bucket_allreduce_avg(gh, boff), "avg")
+    S = boff[1]
+    hs = [synth.host_fill(synth.normal_stream(nd, (85, q), 0.3), 0, S, "f16") for q in range(nd)]
+    for plant in (False, True):
+        if plant:
+            hs[nd // 2][S - 77] = 0x7C00
+        sc = ss.GradScaler(init_scale=64.0, device=DEV)
+        sc.check([_dev16(h).view(torch.float16) for h in hs])
+        want = osc.found_inf([(h, "f16") for h in hs], nd, 0, S, np.float32(1.0 / 64.0))
+        torch.cuda.synchronize()
+        assert bool(int(sc.found_inf.item())) == want == plant
