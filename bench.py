@@ -1792,8 +1792,9 @@ UNIT9M_WORKLOAD = "unit_9m_nd4_m4"
 GPT2_WORKLOAD = "gpt2_small_nd8"
 SMALL_METRICS = {
     UNIT9M_WORKLOAD: ("whole-job step HBM GB/s: 3 micro-batch accumulations of the 4 ranks' "
-                      "gradients + 4 fused last micro-batch rs_avg+AdamW+bf16 cast launches + "
-                      "all-gather, one 9.4M-param unit, N_d=4, M=4"),
+                      "gradients + the 4 ranks' fused last micro-batch rs_avg+AdamW+bf16 cast "
+                      "(one launch over their side-by-side shards) + all-gather, one "
+                      "9.4M-param unit, N_d=4, M=4"),
     GPT2_WORKLOAD: ("whole-job step HBM GB/s: 8 rank-view fused rs_avg+AdamW+bf16 cast launches "
                     "over 13 units + all-gather of one block unit, GPT-2 small, N_d=8"),
 }
@@ -1839,11 +1840,14 @@ class _SmallJob:
             self.m = torch.zeros(P, dtype=f32, device=dev)
             self.v = torch.zeros(P, dtype=f32, device=dev)
             self.acc = torch.empty(nd * P, dtype=f32, device=dev)
-            self.outs = [torch.empty(S, dtype=bf16, device=dev) for _ in range(nd)]
+            # the ranks' bf16 shards side by side (rank r's at r*S), as their
+            # fp32 state is: one fused launch updates every rank's shard
+            self.shards = torch.empty(P, dtype=bf16, device=dev)
+            self.outs = [self.shards[r * S:(r + 1) * S] for r in range(nd)]
             self.full = torch.empty(P, dtype=bf16, device=dev)
             self.S, self.P = S, P
             acc_b = nd * (6 + 10 * (M - 2)) * P
-            fused_b = (6 * nd + 26) * P             # nd launches of S elements
+            fused_b = (6 * nd + 26) * P             # every rank's shard: P elements
             self.parts = [("accumulate", acc_b), ("fused", fused_b), ("all-gather", 4 * P)]
             self.shard_elements = P
             self.h2d = nd * M * P * 2
@@ -1868,12 +1872,9 @@ class _SmallJob:
         self.t = 0
 
     def device_state(self):
-        """Step count and AdamW scalars on the device, for graph capture."""
-        if self.name == UNIT9M_WORKLOAD:
-            self.state = self.ss.AdamWState(self.hp, self.t, device=self.dev)
-        else:
-            for o in self.opts:
-                o.device_step_state()
+        """Step count and AdamW scalars on the device, for graph capture: one
+        state that every rank's launch reads (the ranks step in lockstep)."""
+        self.state = self.ss.AdamWState(self.hp, self.t, device=self.dev)
 
     def run(self, ev=None, graph_form=False):
         """One step of the whole job; ev: 4 events (start, after the
@@ -1893,25 +1894,30 @@ class _SmallJob:
                 self.state.advance()
             else:
                 self.t += 1
-            for r in range(nd):
-                sl = slice(r * S, (r + 1) * S)
-                args = ([self.acc[q * P + r * S:q * P + (r + 1) * S] for q in range(nd)],
-                        [self.g[M - 1][q * P + r * S:q * P + (r + 1) * S] for q in range(nd)],
-                        inv_m, self.master[sl], self.m[sl], self.v[sl], self.outs[r])
-                if graph_form:
-                    ss.fsdp_state_accumulate_rs_avg_adamw_cast(*args, self.state)
-                else:
-                    ss.fsdp_accumulate_rs_avg_adamw_cast(*args, self.hp, self.t)
+            # rank r's shard is positions r*S..(r+1)*S of the state; its N_d
+            # reduce inputs are the same positions of every rank's packed
+            # accumulator and last micro-batch, so one launch over P positions
+            # makes every rank's fused step with the same per-element sums
+            args = ([self.acc[q * P:(q + 1) * P] for q in range(nd)],
+                    [self.g[M - 1][q * P:(q + 1) * P] for q in range(nd)],
+                    inv_m, self.master, self.m, self.v, self.shards)
+            if graph_form:
+                ss.fsdp_state_accumulate_rs_avg_adamw_cast(*args, self.state)
+            else:
+                ss.fsdp_accumulate_rs_avg_adamw_cast(*args, self.hp, self.t)
             if ev is not None:
                 ev[2].record()
             ss.fsdp_ag_unpack(self.outs, self.full)
         else:
             if ev is not None:
                 ev[1].record()
-            for o in self.opts:
-                if graph_form:
-                    o.step_on_device()
-                else:
+            if graph_form:
+                self.state.advance()
+                for o in self.opts:
+                    ss.fsdp_state_rs_avg_adamw_cast(o.grad_in, o.master, o.m, o.v, o.params,
+                                                    self.state)
+            else:
+                for o in self.opts:
                     o.step()
             if ev is not None:
                 ev[2].record()

@@ -76,6 +76,51 @@ def test_fused_step_writes_only_its_outputs(nd, S, shift, path):
         g.check(f"fused step {name}")
 
 
+def _f16(n, seed, shift=0):
+    h = synth.host_fill(synth.normal_stream(seed, (78, n), 0.3), 0, n, "f16")
+    buf = torch.empty(n + shift + 8, dtype=torch.float16, device=DEV)
+    t = buf[shift:shift + n]
+    t.copy_(torch.from_numpy(h.view(np.int16)).view(torch.float16))
+    return t
+
+
+@pytest.mark.parametrize("variant", ["hybrid", "state", "scaled", "scaled_state"])
+@pytest.mark.parametrize("nd,F,S,shift", [(8, 4, 70001, 0), (8, 4, 70001, 1), (6, 3, 2048 * 152 + 13, 0),
+                                          (16, 8, 4099, 0), (4, 2, 13, 0)])
+def test_fused_step_variants_write_only_their_outputs(variant, nd, F, S, shift, path):
+    """The fused step's other instantiations (grouped reduce order, AdamW
+    scalars from the device state, fp16 gradients under loss scaling): the
+    same bands around master / m / v / out, and the scaler's words read,
+    not written, by the step."""
+    scaled = variant.startswith("scaled")
+    grads = ([_f16(S, 30 + q, shift) for q in range(nd)] if scaled
+             else [_bf16(S, 30 + q, shift=shift) for q in range(nd)])
+    master = Guarded(S, torch.float32, shift, torch.randn(S, device=DEV) * 0.02)
+    m = Guarded(S, torch.float32, shift, torch.zeros(S, device=DEV))
+    v = Guarded(S, torch.float32, shift, torch.zeros(S, device=DEV))
+    out = Guarded(S, torch.bfloat16, shift)
+    group = None if variant == "scaled" else F
+    hp = ss.AdamW()
+    st = ss.AdamWState(hp, 1, device=DEV)
+    if variant == "hybrid":
+        ss.fsdp_hybrid_rs_avg_adamw_cast(grads, F, master.t, m.t, v.t, out.t, hp, 1)
+    elif variant == "state":
+        ss.fsdp_state_rs_avg_adamw_cast(grads, master.t, m.t, v.t, out.t, st, shard_group=group)
+    else:
+        sc = ss.GradScaler(init_scale=1024.0, device=DEV)
+        sc.check(grads, shard_group=group)
+        words = (sc.scale.clone(), sc.found_inf.clone())
+        if variant == "scaled":
+            sc.step(grads, master.t, m.t, v.t, out.t, hp, 1)
+        else:
+            sc.step_state(grads, master.t, m.t, v.t, out.t, st, shard_group=group)
+        torch.cuda.synchronize()
+        assert torch.equal(sc.scale, words[0]) and torch.equal(sc.found_inf, words[1])
+        assert int(sc.found_inf.item()) == 0
+    for name, g in (("master", master), ("m", m), ("v", v), ("bf16", out)):
+        g.check(f"{variant} fused step {name}")
+
+
 @pytest.mark.parametrize("n,shift", [(4096 + 3, 0), (2048 * 152 * 2 + 7, 0), (10001, 1), (5, 0)])
 def test_accumulate_writes_only_the_accumulator(n, shift, path):
     acc = Guarded(n, torch.float32, shift)
