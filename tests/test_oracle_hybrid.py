@@ -86,6 +86,24 @@ def test_nested_order_differs_from_flat_order():
     assert oracle.rs_avg(c, 0, 1)[0] == np.float32(4194304.0)
 
 
+def test_group_sums_are_formed_inside_each_group_of_f():
+    # N_d = 4, F = 2: ranks k = g*F + j, so the groups are {0, 1} and {2, 3}
+    # ("PyTorch FSDP..." section 3.3: reduce inside a group, then across).
+    # By hand, with fp32 spacing 2 on [2^24, 2^25) and ties to even:
+    #   groups {0,1},{2,3}: (2^24 + 1 -> 2^24) + (3 + 2) = 2^24 + 5 -> 2^24 + 4;
+    #                       / 4 = 4194305
+    #   groups {0,2},{1,3} (ranks grouped across instead):
+    #                       (2^24 + 3 -> 2^24 + 4) + (1 + 2) = 2^24 + 7 -> 2^24 + 8;
+    #                       / 4 = 4194306
+    #   flat left fold:     ((2^24 + 1 -> 2^24) + 3 -> 2^24 + 4) + 2 = 2^24 + 6;
+    #                       / 4 = 4194305.5
+    c = [np.array([v], np.float32) for v in (2.0 ** 24, 1.0, 3.0, 2.0)]
+    assert oracle.hybrid_rs_avg(c, 2, 0, 1)[0] == np.float32(4194305.0)
+    assert oracle.rs_avg(c, 0, 1)[0] == np.float32(4194305.5)
+    # F = 1: every rank its own group, the groups summed in rank order = flat
+    assert oracle.hybrid_rs_avg(c, 1, 0, 1)[0] == np.float32(4194305.5)
+
+
 def test_hybrid_rejects_a_factor_that_does_not_divide():
     c = _bf16_contribs(6, 12, 0)
     with pytest.raises(ValueError):
