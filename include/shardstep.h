@@ -31,6 +31,11 @@
  *     multiply-adds, in the operation order each call states.
  *   - Every call is stateless and re-entrant; calls on different streams may
  *     run concurrently if their buffers do not overlap.
+ *   - A call with no element to process (S = 0, n = 0, a unit whose tensors
+ *     are all empty, no bucket or only empty buckets) launches nothing and
+ *     returns SHARDSTEP_OK once its scalar arguments (nd, the sharding
+ *     factor, the hyper-parameters or step state, the scaler's words) are
+ *     valid; its data pointers are not looked at and may be NULL.
  */
 #ifndef SHARDSTEP_H
 #define SHARDSTEP_H

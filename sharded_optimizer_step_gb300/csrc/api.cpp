@@ -1165,12 +1165,14 @@ int ddp_bucket_allreduce_avg(const uint16_t* const* rank_grads, int32_t nd,
         return fail(SHARDSTEP_ERR_CAPACITY, "nd %d > %d", nd, SHARDSTEP_MAX_ND);
     if (first < 0 || count < 0) return fail(SHARDSTEP_ERR_INVALID, "first / count negative");
     if (count == 0) return ok();
-    if (bucket_offsets == nullptr || rank_grads == nullptr || out == nullptr)
-        return fail(SHARDSTEP_ERR_INVALID, "bucket_offsets / rank_grads / out is NULL");
+    if (bucket_offsets == nullptr || rank_grads == nullptr)
+        return fail(SHARDSTEP_ERR_INVALID, "bucket_offsets / rank_grads is NULL");
     for (int32_t b = first; b < first + count; ++b)
         if (bucket_offsets[b] < 0 || bucket_offsets[b + 1] < bucket_offsets[b])
             return fail(SHARDSTEP_ERR_INVALID, "bucket offsets must be non-decreasing");
     const int64_t a0 = bucket_offsets[first], e0 = bucket_offsets[first + count];
+    if (e0 == a0) return ok();                 // every bucket of the range is empty
+    if (out == nullptr) return fail(SHARDSTEP_ERR_INVALID, "out is NULL");
     if (!aligned(out, 2)) return fail(SHARDSTEP_ERR_INVALID, "out is not 2-byte aligned");
     const Span os = span(out + a0, (e0 - a0) * 2);
     for (int32_t q = 0; q < nd; ++q) {

@@ -215,6 +215,39 @@ def test_other_entry_points_reject_bad_arguments():
         ss.fsdp_layout([3, -1], 2)
 
 
+def test_empty_calls_return_ok_with_null_data_pointers():
+    """A call with no element to process returns OK once its scalar
+    arguments are valid, whatever its data pointers (here NULL); with an
+    element to process, a NULL output is rejected.  None of these calls
+    reaches a launch."""
+    L = _capi.lib()
+    hp = ss.AdamW().at_step(1)
+    nul = ctypes.c_void_p(None)
+    nulls = _capi.ptr_array([0, 0, 0])
+    assert L.fsdp_rs_avg_adamw_cast(nulls, _capi.DTYPE_BF16, 3, 0, nul, nul, nul, nul,
+                                    ctypes.byref(hp), None) == _capi.OK
+    assert L.fsdp_ag_unpack(None, 3, 0, nul, None) == _capi.OK
+    assert L.fsdp_grad_accumulate(nul, nul, 0, ctypes.c_float(0.5), 1, None) == _capi.OK
+    assert L.fsdp_flat_pack(nulls, _capi.i64_array([0, 0]), 2, 4, _capi.DTYPE_F32, nul,
+                            None) == _capi.OK
+    empty = _capi.i64_array([0, 7, 7, 7])
+    assert L.ddp_bucket_allreduce_avg(nulls, 3, empty, 1, 2, nul, None) == _capi.OK
+    assert L.ddp_bucket_allreduce_avg(nulls, 3, empty, 0, 0, nul, None) == _capi.OK
+    assert L.ddp_bucket_allreduce_avg_adamw_cast(nulls, 3, empty, 1, 2, nul, nul, nul, nul, nul,
+                                                 ctypes.byref(hp), None) == _capi.OK
+    # an element to process: the NULL output is rejected
+    assert L.ddp_bucket_allreduce_avg(nulls, 3, empty, 0, 1, nul, None) == _capi.ERR_INVALID
+    assert L.fsdp_rs_avg_adamw_cast(nulls, _capi.DTYPE_BF16, 3, 5, nul, nul, nul, nul,
+                                    ctypes.byref(hp), None) == _capi.ERR_INVALID
+    # the scalar arguments are still checked on an empty call
+    assert L.fsdp_rs_avg_adamw_cast(nulls, _capi.DTYPE_BF16, 0, 0, nul, nul, nul, nul,
+                                    ctypes.byref(hp), None) == _capi.ERR_INVALID
+    assert L.fsdp_rs_avg_adamw_cast(nulls, _capi.DTYPE_BF16, 3, 0, nul, nul, nul, nul,
+                                    None, None) == _capi.ERR_INVALID
+    assert L.fsdp_grad_unscale_check(nulls, _capi.DTYPE_F16, 3, 3, 0, nul, nul,
+                                     None) == _capi.ERR_INVALID     # no scaler words
+
+
 def test_hybrid_ledger_matches_oracle():
     for psi in (7e9, 351e6):
         for nd, F in ((8, 1), (8, 2), (8, 4), (8, 8), (16, 8), (6, 3)):
