@@ -154,6 +154,22 @@ def test_memory_ledger_closed_forms():
     assert oracle.state_bytes_per_gpu(psi, 16, 3) == pytest.approx(16 * psi / 16)
 
 
+def test_comm_ledger_matches_printed_volumes():
+    """The per-GPU volumes the pages print (tests/golden/comm_volume.txt),
+    in bytes at 2 bytes per element or in elements, at several N_d (the
+    printed figures drop the (N_d - 1) / N_d factor, so they hold for any)."""
+    with open(os.path.join(GOLDEN, "comm_volume.txt")) as f:
+        rows = [ln.split() for ln in f if ln.strip() and not ln.startswith("#")]
+    assert len(rows) == 10
+    psi = 7e9
+    for name, kind, unit, value in rows:
+        for nd in (2, 8, 512):
+            got = oracle.comm_bytes_per_gpu(psi, nd, kind)
+            if unit == "elements":
+                got /= 2
+            assert got == float(value) * psi, (name, nd)
+
+
 def test_comm_ledger_closed_forms():
     psi, nd = 1e9, 8
     b = lambda kind: oracle.comm_bytes_per_gpu(psi, nd, kind)
