@@ -1363,11 +1363,15 @@ def _accum_bytes(nd, M, fused_last):
 def run_accum(args):
     """One rank's view of the Llama-style 1B model (17 units, N_d = 8) with
     M = 4 micro-batches: every one of the 8 contributions to this rank's
-    shard is accumulated in fp32 over the 4 bf16 micro-batch gradients
+    shard is accumulated in fp32 over the bf16 micro-batch gradients
     (acc = g*(1/M), then acc += g*(1/M); one launch per micro-batch over the
-    8 contributions side by side), then one fused step reads the 8 fp32
-    accumulators, then one layer unit is all-gathered.  The accumulate work
-    per step equals a real rank's (N_d shard slices = one full gradient)."""
+    8 contributions side by side).  By default micro-batches 0..M-2 are
+    accumulated so and the last one is added inside the fused step, which
+    reads the 8 fp32 accumulators and the 8 last bf16 gradients; with
+    --accum-two-pass all M are accumulated and the fused step reads the
+    accumulators only.  Then one layer unit is all-gathered.  The
+    accumulate work per step equals a real rank's (N_d shard slices = one
+    full gradient)."""
     world, rank, local = dist_env()
     if args.impl == "reference":
         return _accum_reference(args) if rank == 0 else None
