@@ -1,12 +1,17 @@
-"""The N > 1 path on CPU, with real processes and the gloo backend
-(world_size 2): the bench's control plane (barrier, max / sum over ranks,
-rank 0 alone printing), and the sharded step itself run across two
-processes -- each rank holds only its own gradient, receives the other
-rank's contribution to its shard through a collective, reduces it in rank
-order, updates its shard and all-gathers the bf16 parameters -- which must
-equal, bit for bit, the single-process emulation of N_d ranks that the
-library's kernels implement ("Infra: Data Parallel", FSDP sections: the
-reduce-scatter before the sharded update and the all-gather after it)."""
+"""The N > 1 path on CPU, with real processes and the gloo backend: the
+bench's control plane (barrier, max / sum over ranks, rank 0 alone
+printing), and the step itself run across processes, which must equal, bit
+for bit, the single-process emulation of N_d ranks that the library's
+kernels implement:
+- the sharded step on 2 ranks: each holds only its own gradient, receives
+  the other's contribution to its shard through a collective, reduces in
+  rank order, updates its shard and all-gathers the bf16 parameters
+  ("Infra: Data Parallel", FSDP sections);
+- hybrid sharding on 4 ranks with F = 2: a reduce-scatter inside each group,
+  an all-reduce of the shard across the groups and an all-gather inside the
+  group, over process groups of their own ("PyTorch FSDP..." section 3.3);
+- the DDP step on 2 ranks: the bucketed all-reduce to a bf16 mean and the
+  replicated AdamW ("4.1 数据并行详解" section 4.2)."""
 import json
 import os
 import socket
@@ -33,6 +38,29 @@ def _init(rank, world, port):
                       WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
     if ROOT not in sys.path:
         sys.path.insert(0, ROOT)
+
+
+def _collect(q, procs, world, timeout=180.0):
+    """Each rank's result, read before the processes are joined (a result
+    larger than a pipe's buffer blocks its sender until it is read); a rank
+    that dies or hangs fails the test instead of blocking it."""
+    import time
+    got, t0 = {}, time.monotonic()
+    while len(got) < world:
+        if q.empty():
+            if time.monotonic() - t0 > timeout or any(p.exitcode not in (None, 0) for p in procs):
+                for p in procs:
+                    if p.is_alive():
+                        p.kill()
+                raise AssertionError(f"ranks {sorted(set(range(world)) - set(got))} gave no result")
+            time.sleep(0.05)
+            continue
+        r, *rest = q.get()
+        got[r] = rest
+    for p in procs:
+        p.join(60)
+        assert p.exitcode == 0
+    return got
 
 
 def _control_plane(rank, world, port, q):
@@ -104,10 +132,7 @@ def test_sharded_step_across_two_processes_equals_the_emulation():
     procs = [ctx.Process(target=_sharded_step, args=(r, world, port, q)) for r in range(world)]
     for p in procs:
         p.start()
-    for p in procs:
-        p.join(120)
-        assert p.exitcode == 0
-    got = {r: rest for r, *rest in (q.get() for _ in range(world))}
+    got = _collect(q, procs, world)
     # one process emulating both ranks, as the GPU path does
     numels = [600, 7, 394]
     lay = oracle.layout(numels, world)
@@ -151,3 +176,155 @@ def test_reference_arm_under_torchrun_prints_once(workload):
     assert len(lines) == 1
     line = json.loads(lines[0])
     assert line["impl"] == "reference" and line["value"] > 0
+
+
+# ------------------------------------------- hybrid sharding, four processes
+
+def _bits32(a):
+    return torch.from_numpy(np.ascontiguousarray(a).astype(np.int32))
+
+
+def _hybrid_inputs(world, numels):
+    import oracle
+    import synth
+    lay = oracle.layout(numels, 2)                  # F = 2 shards of the unit
+    T, P = lay.total, lay.padded
+    grads = []
+    for k in range(world):
+        g = np.zeros(P, np.uint16)
+        g[:T] = synth.host_fill(synth.normal_stream(9, (71, k), 1e-3), 0, T, "bf16")
+        grads.append(g)
+    master = np.zeros(P, np.float32)
+    master[:T] = synth.host_fill(synth.normal_stream(9, (72,), 0.02), 0, T, "f32")
+    return lay, grads, master
+
+
+def _hybrid_step(rank, world, F, port, q):
+    """Rank (g, j) = g*F + j holds shard j of its replica: a reduce-scatter
+    inside its group of F ranks, an all-reduce of its shard across the R
+    groups, the mean over all N_d ranks, AdamW on shard j, the bf16 cast and
+    the all-gather inside the group ("PyTorch FSDP..." section 3.3: full
+    sharding inside groups, replication across them)."""
+    _init(rank, world, port)
+    import oracle
+    from oracle.numerics import AdamWConfig, bf16_to_f32
+    dist.init_process_group("gloo")
+    R = world // F
+    g_idx, j = divmod(rank, F)
+    # every rank creates every group, in the same order
+    intra = [dist.new_group([g * F + jj for jj in range(F)]) for g in range(R)]
+    inter = [dist.new_group([g * F + jj for g in range(R)]) for jj in range(F)]
+    lay, grads, master = _hybrid_inputs(world, [900, 13, 280])
+    S = lay.shard
+    mine = grads[rank]
+    # 1. reduce-scatter inside the group: the group's gradients, summed in order j
+    parts = [torch.empty(lay.padded, dtype=torch.int32) for _ in range(F)]
+    dist.all_gather(parts, _bits32(mine), group=intra[g_idx])
+    sl = [bf16_to_f32(p.numpy().astype(np.uint16)[j * S:(j + 1) * S]) for p in parts]
+    s = sl[0].copy()
+    for x in sl[1:]:
+        s = s + x
+    # 2. across the groups, summed in group order, then the mean over N_d
+    sums = [torch.empty(S, dtype=torch.float32) for _ in range(R)]
+    dist.all_gather(sums, torch.from_numpy(s), group=inter[j])
+    total = sums[0].numpy().copy()
+    for x in sums[1:]:
+        total = total + x.numpy()
+    mean = total / np.float32(world)
+    p = master[j * S:(j + 1) * S].copy()
+    z = np.zeros(S, np.float32)
+    p, m, v = oracle.adamw(p, z, z.copy(), mean, AdamWConfig(), 1)
+    ob = oracle.f32_to_bf16(p)
+    # 3. all-gather of the group's bf16 shards
+    shards = [torch.empty(S, dtype=torch.int32) for _ in range(F)]
+    dist.all_gather(shards, _bits32(ob), group=intra[g_idx])
+    full = np.concatenate([x.numpy().astype(np.uint16) for x in shards])
+    q.put((rank, p.tobytes(), m.tobytes(), v.tobytes(), full.tobytes()))
+    dist.destroy_process_group()
+
+
+def test_hybrid_step_across_four_processes_equals_the_emulation():
+    import oracle
+    from oracle.numerics import AdamWConfig
+    world, F = 4, 2
+    port = _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.SimpleQueue()
+    procs = [ctx.Process(target=_hybrid_step, args=(r, world, F, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    got = _collect(q, procs, world)
+    # the one-process emulation: hybrid_shard_step over all N_d contributions
+    lay, grads, master = _hybrid_inputs(world, [900, 13, 280])
+    S = lay.shard
+    obs = []
+    for f in range(F):
+        z = np.zeros(S, np.float32)
+        p, m, v, ob = oracle.hybrid_shard_step(grads, F, f, S, master[f * S:(f + 1) * S].copy(),
+                                               z, z.copy(), AdamWConfig(), 1)
+        obs.append(ob)
+        for g in range(world // F):         # every replica of shard f has the same bits
+            k = g * F + f
+            assert got[k][0] == p.tobytes() and got[k][1] == m.tobytes(), k
+            assert got[k][2] == v.tobytes(), k
+    full, _ = oracle.ag_unpack(obs, lay)
+    for k in range(world):
+        assert got[k][3] == full.tobytes(), k
+
+
+# ----------------------------------------------- DDP buckets, two processes
+
+def _ddp_inputs(world):
+    import oracle
+    import synth
+    numels = [3000, 1, 4096, 17, 2500, 0, 333]
+    _, _, boff = oracle.bucket_plan(numels, 2, 8192)
+    total = boff[-1]
+    grads = [synth.host_fill(synth.normal_stream(11, (81, k), 1e-3), 0, total, "bf16")
+             for k in range(world)]
+    master = synth.host_fill(synth.normal_stream(11, (82,), 0.02), 0, total, "f32")
+    return boff, grads, master
+
+
+def _ddp_step(rank, world, port, q):
+    """Each rank all-reduces its gradient bucket by bucket (gathered, summed in
+    rank order in fp32, divided by N_d, rounded to bf16: the all-reduce keeps
+    the gradient's dtype), then runs the same full AdamW and cast ("4.1 数据并行详解"
+    section 4.2; "Infra: Data Parallel", naive DP)."""
+    _init(rank, world, port)
+    import oracle
+    from oracle.numerics import AdamWConfig, bf16_to_f32
+    dist.init_process_group("gloo")
+    boff, grads, master = _ddp_inputs(world)
+    mine = grads[rank]
+    avg = np.zeros(boff[-1], np.uint16)
+    for a, e in zip(boff[:-1], boff[1:]):
+        parts = [torch.empty(e - a, dtype=torch.int32) for _ in range(world)]
+        dist.all_gather(parts, _bits32(mine[a:e]))
+        s = bf16_to_f32(parts[0].numpy().astype(np.uint16)).copy()
+        for x in parts[1:]:
+            s = s + bf16_to_f32(x.numpy().astype(np.uint16))
+        avg[a:e] = oracle.f32_to_bf16(s / np.float32(world))
+    z = np.zeros(boff[-1], np.float32)
+    p, m, v = oracle.adamw(master.copy(), z, z.copy(), bf16_to_f32(avg), AdamWConfig(), 1)
+    q.put((rank, avg.tobytes(), p.tobytes(), m.tobytes(), v.tobytes(),
+           oracle.f32_to_bf16(p).tobytes()))
+    dist.destroy_process_group()
+
+
+def test_ddp_step_across_two_processes_equals_the_emulation():
+    import oracle
+    from oracle.numerics import AdamWConfig
+    world = 2
+    port = _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.SimpleQueue()
+    procs = [ctx.Process(target=_ddp_step, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    got = _collect(q, procs, world)
+    boff, grads, master = _ddp_inputs(world)
+    z = np.zeros(boff[-1], np.float32)
+    want = oracle.ddp_step(grads, boff, master.copy(), z, z.copy(), AdamWConfig(), 1)
+    for r in range(world):
+        assert [bytes(x) for x in got[r]] == [np.ascontiguousarray(w).tobytes() for w in want], r
