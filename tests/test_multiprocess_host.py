@@ -11,7 +11,10 @@ kernels implement:
   an all-reduce of the shard across the groups and an all-gather inside the
   group, over process groups of their own ("PyTorch FSDP..." section 3.3);
 - the DDP step on 2 ranks: the bucketed all-reduce to a bf16 mean and the
-  replicated AdamW ("4.1 数据并行详解" section 4.2)."""
+  replicated AdamW ("4.1 数据并行详解" section 4.2);
+- FSDP2 per-parameter Shard(0) on 2 ranks: chunk-cat, the reduce-scatter,
+  AdamW on the padded local buffer, the all-gather copied out into the
+  full tensors ("Infra: Data Parallel", FSDP2 section)."""
 import json
 import os
 import socket
@@ -328,3 +331,77 @@ def test_ddp_step_across_two_processes_equals_the_emulation():
     want = oracle.ddp_step(grads, boff, master.copy(), z, z.copy(), AdamWConfig(), 1)
     for r in range(world):
         assert [bytes(x) for x in got[r]] == [np.ascontiguousarray(w).tobytes() for w in want], r
+
+
+# -------------------------------------------- FSDP2 Shard(0), two processes
+
+FSDP2_SHAPES = [(7, 5), (3,), (10, 2, 2), (1, 9)]     # uneven dim 0: padding rows
+
+
+def _fsdp2_inputs(world):
+    import synth
+    grads = [[synth.host_fill(synth.normal_stream(13, (91, k, t), 1e-3), 0, int(np.prod(s)),
+                              "bf16").reshape(s) for t, s in enumerate(FSDP2_SHAPES)]
+             for k in range(world)]
+    masters = [synth.host_fill(synth.normal_stream(13, (92, t), 0.02), 0, int(np.prod(s)),
+                               "f32").reshape(s) for t, s in enumerate(FSDP2_SHAPES)]
+    return grads, masters
+
+
+def _fsdp2_step(rank, world, port, q):
+    """FSDP2 per-parameter Shard(0) ("Infra: Data Parallel", FSDP2 section):
+    the rank's own gradients laid out rank-major with padding rows
+    (chunk-cat), the reduce-scatter of its piece (gathered, summed in rank
+    order), AdamW on its padded local buffer, then the all-gather of the
+    local buffers copied out into the full per-parameter tensors."""
+    _init(rank, world, port)
+    import oracle
+    from oracle.numerics import AdamWConfig
+    dist.init_process_group("gloo")
+    grads, masters = _fsdp2_inputs(world)
+    lay = oracle.fsdp2_layout(FSDP2_SHAPES, world)
+    L = lay.local
+    cc = oracle.chunk_cat(grads[rank], lay)
+    parts = [torch.empty(world * L, dtype=torch.int32) for _ in range(world)]
+    dist.all_gather(parts, _bits32(cc))
+    contribs = [x.numpy().astype(np.uint16) for x in parts]
+    p = oracle.local_buffer(masters, lay, rank)
+    z = np.zeros(L, np.float32)
+    p, m, v, ob = oracle.fsdp_shard_step(contribs, rank, L, p, z, z.copy(), AdamWConfig(), 1)
+    locs = [torch.empty(L, dtype=torch.int32) for _ in range(world)]
+    dist.all_gather(locs, _bits32(ob))
+    full = oracle.all_gather_copy_out([x.numpy().astype(np.uint16) for x in locs], lay)
+    q.put((rank, p.tobytes(), m.tobytes(), v.tobytes(), b"".join(x.tobytes() for x in full)))
+    dist.destroy_process_group()
+
+
+def test_fsdp2_step_across_two_processes_equals_the_emulation():
+    import oracle
+    from oracle.numerics import AdamWConfig
+    world = 2
+    port = _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.SimpleQueue()
+    procs = [ctx.Process(target=_fsdp2_step, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    got = _collect(q, procs, world)
+    grads, masters = _fsdp2_inputs(world)
+    lay = oracle.fsdp2_layout(FSDP2_SHAPES, world)
+    L = lay.local
+    cc = [oracle.chunk_cat(g, lay) for g in grads]
+    obs = []
+    for r in range(world):
+        z = np.zeros(L, np.float32)
+        p, m, v, ob = oracle.fsdp_shard_step(cc, r, L, oracle.local_buffer(masters, lay, r), z,
+                                             z.copy(), AdamWConfig(), 1)
+        assert got[r][:3] == [p.tobytes(), m.tobytes(), v.tobytes()], r
+        # the padding rows of the local buffer stay zero
+        for t in range(len(FSDP2_SHAPES)):
+            k = lay.rows_of(r, t) * lay.row[t]
+            seg = p[lay.offset[t]:lay.offset[t] + lay.chunk[t] * lay.row[t]]
+            assert not seg[k:].any(), (r, t)
+        obs.append(ob)
+    full = oracle.all_gather_copy_out(obs, lay)
+    for r in range(world):
+        assert got[r][3] == b"".join(x.tobytes() for x in full), r
