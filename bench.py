@@ -437,6 +437,18 @@ def run_ours(args):
     traffic_per_elem = (None if args.layers or args.nd or args.kernel_path != "auto"
                         or args.tma_stages else profiled_traffic(args.workload))
 
+    # the inter-rank bytes the step's emulated collectives stand for (ring
+    # model), from one more step issued call by call
+    torch.cuda.synchronize()
+    ss.comm_counter(reset=True)
+    if args.graph:
+        opt.step_on_device()
+        opt.gather_unit(u, peers, full)
+    else:
+        one_step()
+    torch.cuda.synchronize()
+    comm_step = ss.comm_counter(reset=True)
+
     pack = _time_flat_pack(torch, ss, w, u, nd if F == nd else F, dev, stream)
 
     # end to end through the public API: pinned host inputs copied in every
@@ -507,6 +519,13 @@ def run_ours(args):
                                   else round(traffic_per_elem * S)),
             "e2e": e2e,
             **({"e2e_note": "the end-to-end leg runs without --graph"} if args.graph else {}),
+            "emulated_comm": {
+                "bytes_per_step": round(comm_step),
+                "link_gbs_to_hide": round(comm_step / (ms_per_step / 1e3) / 1e9, 1),
+                "model": "bytes this rank would send per step if each emulated collective ran "
+                         "as a ring ((N_d-1)/N_d kept): the reduce-scatter into the fused step "
+                         "and the all-gather of one layer unit; link_gbs_to_hide = that over "
+                         "the measured step time"},
             "gpu_launches": launches,
             **({"gpu_launches_note": f"{graph_launches} kernels per replayed step, counted "
                                      f"when the graphs were captured"} if args.graph else {}),

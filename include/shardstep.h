@@ -778,6 +778,32 @@ const char* shardstep_last_error(void);
 /* Kernels this library has launched in this process (all threads). */
 uint64_t shardstep_launch_count(void);
 
+/* shardstep_comm_counter -- host only, thread-safe.
+ * The emulated collectives move no bytes between GPUs; this counter adds
+ * up, over the calls accepted in this process, the bytes their ranks would
+ * send if each collective ran as a ring, the model of [P1] ZeRO section and
+ * [P3] sections 5 and 8, with the (N_d - 1) / N_d factor kept.  Per call,
+ * summed over the shard positions it covers (es = bytes per element of the
+ * contributions the kernel reduces: 2 for bf16 / fp16, 4 for fp32 and for
+ * the fused last micro-batch, whose contributions are fp32 sums):
+ *   a fused step's reduce-scatter   (N_d - 1) * S * es; under hybrid
+ *                                   sharding (F - 1) * S * es inside the
+ *                                   group + 2 (R - 1) / R * S * es across
+ *                                   the R = N_d / F groups;
+ *   fsdp_ag_unpack                  (N_d - 1) * S * 2;
+ *   fsdp2_all_gather_copy_out       (N_d - 1) * local * es;
+ *   a bucket all-reduce (alone or   2 (N_d - 1) / N_d * 2 bytes per bucketed
+ *   fused with AdamW)               element;
+ *   fsdp_grad_unscale_check         2 (N_d - 1) / N_d * 4 (the found-inf
+ *                                   flags OR-ed over the ranks; the reduce
+ *                                   is the scaled step's).
+ * Packing, accumulation, chunk-cat, views and empty calls count 0.  One rank
+ * step of ZeRO-1/2 (a fused step over the rank's shard of every unit, then
+ * the all-gather of every unit) thus adds 4 (N_d - 1) / N_d * Psi bytes for
+ * Psi padded parameters, and a DDP step 4 (N_d - 1) / N_d * Psi.
+ * Returns the running total in bytes; reset != 0 sets it to 0 after reading. */
+double shardstep_comm_counter(int32_t reset);
+
 /* Name of the kernel that the calling thread's last successful streaming
  * call launched (fused steps, accumulation, non-finite check; for the bucket
  * all-reduce, the kernel of its last non-empty bucket), e.g.

@@ -21,7 +21,8 @@ from .build import build
 __all__ = [
     "build", "ShardstepError", "AdamW", "Layout", "fsdp_layout", "fsdp_flat_pack", "fsdp_views",
     "fsdp_grad_accumulate", "fsdp_rs_avg_adamw_cast", "fsdp_ag_unpack", "ddp_bucket_plan",
-    "ddp_bucket_allreduce_avg", "state_bytes", "comm_bytes", "launch_count", "last_kernel",
+    "ddp_bucket_allreduce_avg", "state_bytes", "comm_bytes", "comm_counter", "launch_count",
+    "last_kernel",
     "MAX_ND",
     "set_fused_path", "device_status", "fsdp_hybrid_rs_avg_adamw_cast", "hybrid_state_bytes",
     "hybrid_comm_bytes", "Fsdp2Layout", "fsdp2_layout", "fsdp2_local_views", "fsdp2_chunk_cat",
@@ -780,6 +781,13 @@ def hybrid_comm_bytes(psi: float, nd: int, shard_group: int, kind: str,
     if r < 0:
         raise ValueError("the sharding factor must divide N_d")
     return r
+
+
+def comm_counter(reset: bool = False) -> float:
+    """Bytes the emulated collectives of the calls so far would send between
+    ranks as rings (``shardstep_comm_counter``); ``reset`` zeroes it after
+    reading."""
+    return float(_capi.lib().shardstep_comm_counter(int(bool(reset))))
 
 
 def launch_count() -> int:

@@ -88,6 +88,7 @@ SIGNATURES = {
                                                     c_vp]),
     "shardstep_state_bytes": (c_f64, [c_f64, c_i32, c_i32, c_f64]),
     "shardstep_comm_bytes": (c_f64, [c_f64, c_i32, c_i32, c_i32]),
+    "shardstep_comm_counter": (c_f64, [c_i32]),
     "shardstep_hybrid_state_bytes": (c_f64, [c_f64, c_i32, c_f64]),
     "shardstep_hybrid_comm_bytes": (c_f64, [c_f64, c_i32, c_i32, c_i32, c_i32]),
     "shardstep_ckpt_save_rank": (c_i32, [ctypes.c_char_p, c_i32, c_i32, c_i64, P_i64, c_i32,

@@ -41,6 +41,30 @@ const char* dtype_name(int dtype) {
     return dtype == SHARDSTEP_DTYPE_F32 ? "f32" : dtype == SHARDSTEP_DTYPE_F16 ? "f16" : "bf16";
 }
 std::atomic<uint64_t> g_launches{0};
+
+// The inter-rank bytes the emulated collectives of the accepted calls stand
+// for (ring model; see shardstep_comm_counter in shardstep.h).
+std::mutex g_comm_mu;
+double g_comm_bytes = 0.0;
+void count_comm(double bytes) {
+    std::lock_guard<std::mutex> lock(g_comm_mu);
+    g_comm_bytes += bytes;
+}
+// The reduce of a fused step over S shard positions of es-byte
+// contributions: the reduce-scatter inside the group of `group` ranks, then,
+// under hybrid sharding, the ring all-reduce of the shard across the
+// nd / group groups.
+double reduce_comm_bytes(int32_t nd, int32_t group, int64_t S, int es) {
+    const double n = static_cast<double>(S) * es;
+    const int32_t R = nd / group;
+    double b = static_cast<double>(group - 1) * n;
+    if (R > 1) b += 2.0 * (R - 1) / R * n;
+    return b;
+}
+// One ring all-reduce of `bytes` over nd ranks: a reduce-scatter and an
+// all-gather, each sending (nd - 1) / nd of the buffer.
+double allreduce_comm_bytes(int32_t nd, double bytes) { return 2.0 * (nd - 1) / nd * bytes; }
+
 std::atomic<int> g_fused_path{SHARDSTEP_PATH_AUTO};
 std::atomic<int> g_dependent_launch{1};
 
@@ -295,6 +319,13 @@ const char* shardstep_last_error(void) { return g_error.c_str(); }
 const char* shardstep_last_kernel(void) { return g_last_kernel; }
 
 uint64_t shardstep_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+double shardstep_comm_counter(int32_t reset) {
+    std::lock_guard<std::mutex> lock(g_comm_mu);
+    const double b = g_comm_bytes;
+    if (reset != 0) g_comm_bytes = 0.0;
+    return b;
+}
 
 int32_t shardstep_set_fused_path(int32_t path) {
     if (path != SHARDSTEP_PATH_AUTO && path != SHARDSTEP_PATH_REGISTER &&
@@ -581,7 +612,9 @@ int fsdp_ag_unpack(const uint16_t* const* shards, int32_t nd, int64_t S, uint16_
         if (shards[q] != dst) cb.add(shards[q], dst, S * 2);
     }
     cb.flush();
-    return cb.rc == SHARDSTEP_OK ? ok() : cb.rc;
+    if (cb.rc != SHARDSTEP_OK) return cb.rc;
+    count_comm(static_cast<double>(nd - 1) * static_cast<double>(S) * 2.0);
+    return ok();
 }
 
 int fsdp_grad_accumulate(const uint16_t* g, float* acc, int64_t n, float scale, int32_t first,
@@ -750,6 +783,7 @@ int fused_step(const void* const* grad_slices, int32_t grad_dtype, int32_t nd, i
                     dtype_name(grad_dtype));
     else
         note_kernel("rs_adamw_cast_scalar<%s>", dtype_name(grad_dtype));
+    count_comm(reduce_comm_bytes(nd, group, S, elem_size_of(grad_dtype)));
     return ok();
 }
 
@@ -795,6 +829,8 @@ int accum_step(const float* const* acc_slices, const uint16_t* const* last_slice
         note_kernel("accum_rs_adamw_cast_vec4<any N_d = %d> (register-staged)", nd);
     else
         note_kernel("accum_rs_adamw_cast_scalar");
+    // the contributions reduced are the fp32 sums acc_q + g_q / M
+    count_comm(reduce_comm_bytes(nd, shard_group, S, 4));
     return ok();
 }
 
@@ -911,6 +947,8 @@ int fsdp_grad_unscale_check(const void* const* grad_slices, int32_t grad_dtype, 
                     dtype_name(grad_dtype));
     else
         note_kernel("nonfinite_check_scalar<%s>", dtype_name(grad_dtype));
+    // the reduce itself is the scaled step's; the ranks OR their flags
+    count_comm(allreduce_comm_bytes(nd, 4.0));
     return ok();
 }
 
@@ -1120,7 +1158,9 @@ int fsdp2_all_gather_copy_out(const void* const* local_bufs, const int64_t* dim0
                    have * es);
         }
     cb.flush();
-    return cb.rc == SHARDSTEP_OK ? ok() : cb.rc;
+    if (cb.rc != SHARDSTEP_OK) return cb.rc;
+    count_comm(static_cast<double>(nd - 1) * static_cast<double>(plan.local) * es);
+    return ok();
 }
 
 int ddp_bucket_plan(const int64_t* numels, int32_t n, int32_t elem_size, int64_t cap_bytes,
@@ -1217,6 +1257,7 @@ int ddp_bucket_allreduce_avg(const uint16_t* const* rank_grads, int32_t nd,
             note_kernel("allreduce_avg_scalar");
         pdl = g_dependent_launch.load(std::memory_order_relaxed) != 0;
     }
+    count_comm(allreduce_comm_bytes(nd, static_cast<double>(e0 - a0) * 2.0));
     return ok();
 }
 
@@ -1280,6 +1321,7 @@ int ddp_bucket_allreduce_avg_adamw_cast(const uint16_t* const* rank_grads, int32
         note_kernel("ddp_allreduce_adamw_cast_vec4<any N_d = %d> (register-staged)", nd);
     else
         note_kernel("ddp_allreduce_adamw_cast_scalar");
+    count_comm(allreduce_comm_bytes(nd, static_cast<double>(n) * 2.0));
     return ok();
 }
 

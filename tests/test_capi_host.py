@@ -248,6 +248,52 @@ def test_empty_calls_return_ok_with_null_data_pointers():
                                      None) == _capi.ERR_INVALID     # no scaler words
 
 
+def test_comm_counter_reads_and_resets():
+    """The counter of emulated inter-rank bytes: read, reset, and no count
+    for calls with nothing to process (they reach no collective)."""
+    L = _capi.lib()
+    ss.comm_counter(reset=True)
+    assert ss.comm_counter() == 0.0
+    hp = ss.AdamW().at_step(1)
+    nul = ctypes.c_void_p(None)
+    assert L.fsdp_rs_avg_adamw_cast(_capi.ptr_array([0, 0]), _capi.DTYPE_BF16, 2, 0, nul, nul,
+                                    nul, nul, ctypes.byref(hp), None) == _capi.OK
+    assert L.fsdp_ag_unpack(None, 8, 0, nul, None) == _capi.OK
+    assert L.ddp_bucket_allreduce_avg(_capi.ptr_array([0, 0]), 2, _capi.i64_array([0, 0]), 0, 1,
+                                      nul, None) == _capi.OK
+    # a rejected call counts nothing either
+    assert L.fsdp_ag_unpack(None, 8, 16, nul, None) == _capi.ERR_INVALID
+    assert ss.comm_counter(reset=True) == 0.0
+
+
+@pytest.mark.parametrize("nd,F", [(4, 4), (8, 8), (4, 2), (8, 1)])
+def test_rank_state_bytes_are_the_ledger_terms(nd, F):
+    """The per-rank state the optimizer allocates is the ZeRO ledger's terms
+    ("Infra: Data Parallel", ZeRO figure; "4.1 数据并行详解" section 7), with Psi
+    the padded parameter count: k Psi / F of fp32 master + m + v (k = 12) and
+    2 Psi / F of bf16 parameters; the reduced gradient shard (2 Psi / F) lives
+    only in the fused kernel's registers; the N_d contributions to the shard
+    that the emulated reduce-scatter reads add up to one full gradient, 2 Psi,
+    under full sharding (F = N_d)."""
+    from sharded_optimizer_step_gb300.engine import RankShardOptimizer
+    from synth import workloads as W
+    opt = RankShardOptimizer(W.unit_9m().units + [[(1000, 3), (7,)]], nd, 0, ss.AdamW(),
+                             device="cpu", shard_group=F)
+    psi = F * opt.shard_total
+    nbytes = lambda ts: sum(t.numel() * t.element_size() for t in ts)
+    optimizer = nbytes([opt.master, opt.m, opt.v])
+    params = nbytes([opt.params])
+    assert optimizer == 12 * psi / F and params == 2 * psi / F
+    assert ss.hybrid_state_bytes(psi, F) == optimizer + params + params   # + the gradient shard
+    if F == nd:
+        assert ss.state_bytes(psi, nd, 3) == optimizer + 2 * params
+    # N_d contributions of the rank's S = Psi / F positions: one full
+    # gradient (2 Psi) under full sharding, R = N_d / F of them under hybrid
+    assert nbytes(opt.grad_in) == nd * 2 * psi / F
+    if F == nd:
+        assert nbytes(opt.grad_in) == 2 * psi
+
+
 def test_hybrid_ledger_matches_oracle():
     for psi in (7e9, 351e6):
         for nd, F in ((8, 1), (8, 2), (8, 4), (8, 8), (16, 8), (6, 3)):
