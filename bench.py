@@ -472,6 +472,13 @@ def run_ours(args):
             e2e.pop("bytes")
             e2e.pop("seconds")
             e2e["value"] = round(got_bytes / got_sec / 1e9, 1)
+    elif not args.no_e2e and scaled and not args.graph:
+        # the check must see every contribution before any update, so the
+        # copies are not overlapped with the step here
+        e2e = _e2e_plain(torch, stream, opt.grad_in + [peers[q] for q in range(F) if q != r],
+                         [full], one_step, step_bytes, world, args.e2e_steps,
+                         "the 8 scaled fp16 contributions and the peers' shards in, the "
+                         "gathered layer unit out")
 
     cpu = cpu_all = None
     if rank == 0 and not args.no_cpu:
@@ -894,6 +901,19 @@ def run_fsdp2(args):
     fused_launch = fused_b / nd
     achieved = fused_launch / (avg[1] / nd / 1e3) / 1e9
     value = allreduce_sum(world, step_b * args.steps) / (total_ms / 1e3) / 1e9
+    e2e = None
+    if not args.no_e2e:
+        e2e = _e2e_plain(torch, stream, [g for gs in grads for g in gs], params,
+                         lambda: one_step(None), step_b, world, args.e2e_steps,
+                         "the 8 ranks' full bf16 gradients of the 9 parameters in, the 9 "
+                         "gathered bf16 parameters out")
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        cv, sec, n_el = _fsdp2_oracle(2)
+        cpu = {"value": round(cv, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"2 x (chunk-cat, 8 fused updates and the copy-out) of the layer group "
+                         f"with dimension 0 divided by 16 ({n_el} elements), numpy "
+                         f"single-threaded"}
     if rank == 0:
         print(json.dumps({
             "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
@@ -918,7 +938,7 @@ def run_fsdp2(args):
                         "copy_out_gbs": round(ag_b / (avg[2] / 1e3) / 1e9, 1)},
             "roofline": _roofline(achieved, f"{fused_kernel} on one rank's local buffer",
                                   fused_launch),
-            "e2e": None, "gpu_launches": launches, "clocks": clk, "cpu_baseline": None,
+            "e2e": e2e, "gpu_launches": launches, "clocks": clk, "cpu_baseline": cpu,
         }))
 
 
@@ -1023,6 +1043,11 @@ def run_ragged(args):
     pack_ms, ag_ms = _avg_ms(events, 0, 1), _avg_ms(events, 1, 2)
     ms = total_ms / args.steps
     all_bytes = allreduce_sum(world, step_bytes)
+    e2e = None
+    if not args.no_e2e:
+        e2e = _e2e_plain(torch, stream, tensors + shards, [flat, full], lambda: one_step(None),
+                         step_bytes, world, args.e2e_steps, "the unit's 9 bf16 tensors and the "
+                         "8 shards in, the packed unit and the gathered unit out")
     if rank != 0:
         _finish_dist(world)
         return
@@ -1059,56 +1084,64 @@ def run_ragged(args):
                               "offsets, copy16 for the congruent ones, copy_segments for "
                               "heads, tails and the zero pad", pack_bytes,
                               _traffic(RAGGED_WORKLOAD, lay.total, args)),
-        "e2e": None, "e2e_note": "device-resident tensors; the end-to-end line is the "
-                                 "default workload's",
+        "e2e": e2e,
         "gpu_launches": launches, "clocks": clk, "cpu_baseline": cpu}))
     _finish_dist(world)
 
 
-def run_fsdp2_reference(args):
+def _fsdp2_oracle(steps, warmup=0):
     """The oracle's FSDP2 group step (chunk-cat of every rank's gradients,
     the fused update of every rank's local buffer, all-gather copy-out) on
     the Llama-7B layer group with every dimension 0 divided by 16, numpy on
-    one core; rank 0 alone under torchrun."""
+    one core, timed over ``steps`` steps after ``warmup``.  Returns (GB/s of
+    the step's algorithmic bytes, seconds per step, elements)."""
     import numpy as np
     import oracle
     import synth
     from oracle.numerics import AdamWConfig
     from synth import workloads as W
+    w = W.llama_7b_rank_view()
+    shapes = [(max(1, sh[0] // 16),) + tuple(sh[1:]) for sh in w.units[0]]
+    nd = w.nd
+    lay = oracle.fsdp2_layout(shapes, nd)
+    hp = AdamWConfig(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
+    n = sum(math.prod(sh) for sh in shapes)
+    grads = [[synth.host_fill(synth.normal_stream(19, (86, q, k), 1e-3), 0, math.prod(sh),
+                              "bf16").reshape(sh) for k, sh in enumerate(shapes)]
+             for q in range(nd)]
+    master = oracle.chunk_cat([synth.host_fill(synth.normal_stream(19, (85, k), 0.02), 0,
+                                               math.prod(sh), "f32").reshape(sh)
+                               for k, sh in enumerate(shapes)], lay)
+    m = np.zeros_like(master)
+    v = np.zeros_like(master)
+    L = lay.local
+    cc_b, fused_b, ag_b = _fsdp2_bytes(shapes, nd, L)
+    tt = 0.0
+    for k in range(warmup + steps):
+        t0 = time.perf_counter()
+        rs_in = [oracle.chunk_cat(grads[q], lay) for q in range(nd)]
+        outs = []
+        for r in range(nd):
+            sl = slice(r * L, (r + 1) * L)
+            p1, m1, v1, o1 = oracle.fsdp_shard_step([x for x in rs_in], r, L, master[sl],
+                                                    m[sl], v[sl], hp, k + 1)
+            master[sl], m[sl], v[sl] = p1, m1, v1
+            outs.append(o1)
+        oracle.all_gather_copy_out(outs, lay)
+        if k >= warmup:
+            tt += time.perf_counter() - t0
+    return (cc_b + fused_b + ag_b) * steps / tt / 1e9, tt / steps, n
+
+
+def run_fsdp2_reference(args):
+    """The oracle arm of the FSDP2 line (``_fsdp2_oracle``); rank 0 alone
+    under torchrun."""
     world, rank, _ = dist_env()
     init_dist(world)
     if rank == 0:
-        w = W.llama_7b_rank_view()
-        shapes = [(max(1, sh[0] // 16),) + tuple(sh[1:]) for sh in w.units[0]]
-        nd = w.nd
-        lay = oracle.fsdp2_layout(shapes, nd)
-        hp = AdamWConfig(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
-        n = sum(math.prod(sh) for sh in shapes)
-        grads = [[synth.host_fill(synth.normal_stream(19, (86, q, k), 1e-3), 0, math.prod(sh),
-                                  "bf16").reshape(sh) for k, sh in enumerate(shapes)]
-                 for q in range(nd)]
-        master = oracle.chunk_cat([synth.host_fill(synth.normal_stream(19, (85, k), 0.02), 0,
-                                                   math.prod(sh), "f32").reshape(sh)
-                                   for k, sh in enumerate(shapes)], lay)
-        m = np.zeros_like(master)
-        v = np.zeros_like(master)
-        L = lay.local
-        cc_b, fused_b, ag_b = _fsdp2_bytes(shapes, nd, L)
-        tt = 0.0
-        for k in range(args.warmup + args.steps):
-            t0 = time.perf_counter()
-            rs_in = [oracle.chunk_cat(grads[q], lay) for q in range(nd)]
-            outs = []
-            for r in range(nd):
-                sl = slice(r * L, (r + 1) * L)
-                p1, m1, v1, o1 = oracle.fsdp_shard_step([x for x in rs_in], r, L, master[sl],
-                                                        m[sl], v[sl], hp, k + 1)
-                master[sl], m[sl], v[sl] = p1, m1, v1
-                outs.append(o1)
-            oracle.all_gather_copy_out(outs, lay)
-            if k >= args.warmup:
-                tt += time.perf_counter() - t0
-        val = (cc_b + fused_b + ag_b) * args.steps / tt / 1e9
+        nd = 8
+        val, sec, n = _fsdp2_oracle(args.steps, args.warmup)
+        tt = sec * args.steps
         print(json.dumps({
             "impl": "reference", "metric": METRIC, "value": round(val, 4), "unit": "GB/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -1129,60 +1162,66 @@ def run_fsdp2_reference(args):
 CKPT_WORKLOAD = "ckpt_gpt2_small_nd8_to_nd4"
 
 
-def run_ckpt_reference(args):
-    """The same checkpoint with numpy on the host: the 8 ranks' fp32 master /
-    m / v shards of every unit written with numpy.save, then the 4 new
-    ranks' shards read back and resharded by the oracle; rank 0 alone."""
+def _ckpt_oracle(steps, warmup=0):
+    """The checkpoint with numpy on the host: the 8 ranks' fp32 master / m / v
+    shards of every GPT-2-small unit written with numpy.save, then the 4 new
+    ranks' shards read back and resharded by the oracle; median seconds of
+    ``steps`` rounds after ``warmup``.  Returns (save s, load s, state bytes)."""
     import shutil
     import numpy as np
     import synth
     from oracle import checkpoint as oracle_ckpt
     from synth import workloads as W
+    w = W.gpt2_small()
+    totals = [sum(math.prod(sh) for sh in u) for u in w.units]
+    old_nd, new_nd = 8, 4
+    shards = {}                     # (rank, unit, kind) -> fp32 array
+    for u, T in enumerate(totals):
+        S = -(-T // old_nd)
+        for kind in range(3):
+            flat = np.zeros(S * old_nd, np.float32)
+            flat[:T] = synth.host_fill(synth.normal_stream(23, (84, u, kind), 0.02), 0, T, "f32")
+            for r in range(old_nd):
+                shards[(r, u, kind)] = flat[r * S:(r + 1) * S].copy()
+    state_bytes = sum(a.nbytes for a in shards.values())
+    root = tempfile.mkdtemp(prefix="shst_ckref_")
+    saves, loads = [], []
+    try:
+        for k in range(warmup + max(1, steps)):
+            d = os.path.join(root, f"step{k}")
+            os.makedirs(d)
+            t0 = time.perf_counter()
+            for (r, u, kind), a in shards.items():
+                np.save(os.path.join(d, f"{r}_{u}_{kind}.npy"), a)
+            t1 = time.perf_counter()
+            for u, T in enumerate(totals):
+                for kind in range(3):
+                    old = [np.load(os.path.join(d, f"{r}_{u}_{kind}.npy"))
+                           for r in range(old_nd)]
+                    for nr in range(new_nd):
+                        oracle_ckpt.reshard(old, T, new_nd, nr)
+            t2 = time.perf_counter()
+            if k >= warmup:
+                saves.append(t1 - t0)
+                loads.append(t2 - t1)
+            shutil.rmtree(d, ignore_errors=True)
+    finally:
+        shutil.rmtree(root, ignore_errors=True)
+    return statistics.median(saves), statistics.median(loads), state_bytes
+
+
+def run_ckpt_reference(args):
+    """The oracle arm of the checkpoint line (``_ckpt_oracle``); rank 0 alone."""
     world, rank, _ = dist_env()
     init_dist(world)
     if rank == 0:
-        w = W.gpt2_small()
-        totals = [sum(math.prod(sh) for sh in u) for u in w.units]
         old_nd, new_nd = 8, 4
-        shards = {}                     # (rank, unit, kind) -> fp32 array
-        for u, T in enumerate(totals):
-            S = -(-T // old_nd)
-            for kind in range(3):
-                flat = np.zeros(S * old_nd, np.float32)
-                flat[:T] = synth.host_fill(synth.normal_stream(23, (84, u, kind), 0.02), 0, T,
-                                           "f32")
-                for r in range(old_nd):
-                    shards[(r, u, kind)] = flat[r * S:(r + 1) * S].copy()
-        state_bytes = sum(a.nbytes for a in shards.values())
-        root = tempfile.mkdtemp(prefix="shst_ckref_")
-        saves, loads = [], []
-        try:
-            for k in range(args.warmup + max(1, args.steps)):
-                d = os.path.join(root, f"step{k}")
-                os.makedirs(d)
-                t0 = time.perf_counter()
-                for (r, u, kind), a in shards.items():
-                    np.save(os.path.join(d, f"{r}_{u}_{kind}.npy"), a)
-                t1 = time.perf_counter()
-                for u, T in enumerate(totals):
-                    for kind in range(3):
-                        old = [np.load(os.path.join(d, f"{r}_{u}_{kind}.npy"))
-                               for r in range(old_nd)]
-                        for nr in range(new_nd):
-                            oracle_ckpt.reshard(old, T, new_nd, nr)
-                t2 = time.perf_counter()
-                if k >= args.warmup:
-                    saves.append(t1 - t0)
-                    loads.append(t2 - t1)
-                shutil.rmtree(d, ignore_errors=True)
-        finally:
-            shutil.rmtree(root, ignore_errors=True)
-        sv, ld = statistics.median(saves), statistics.median(loads)
+        sv, ld, state_bytes = _ckpt_oracle(args.steps, args.warmup)
         val = state_bytes / sv / 1e9
         print(json.dumps({
             "impl": "reference",
             "metric": "sharded checkpoint save / load GB/s (fp32 master + moments)",
-            "value": round(val, 3), "unit": "GB/s", "n_gpus": world, "steps": len(saves),
+            "value": round(val, 3), "unit": "GB/s", "n_gpus": world, "steps": max(1, args.steps),
             "warmup": args.warmup, "ms_per_step": round(1e3 * (sv + ld), 1),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
@@ -1253,6 +1292,13 @@ def run_ckpt(args):
     finally:
         shutil.rmtree(root, ignore_errors=True)
     sv, ld = statistics.median(saves), statistics.median(loads)
+    cpu = None
+    if not args.no_cpu:
+        csv, cld, cbytes = _ckpt_oracle(1)
+        cpu = {"value": round(cbytes / csv / 1e9, 3), "unit": "GB/s", "cores": 1,
+               "kind": "oracle", "load_gbs": round(cbytes / cld / 1e9, 3),
+               "sample": "the whole optimizer state once: numpy.save per rank, unit and kind, "
+                         "then numpy.load + the oracle's reshard for the 4 new ranks"}
     print(json.dumps({
         "metric": "sharded checkpoint save / load GB/s (fp32 master + moments)",
         "value": round(state_bytes / sv / 1e9, 2), "unit": "GB/s", "n_gpus": 1,
@@ -1266,7 +1312,13 @@ def run_ckpt(args):
         "first_save_s": round(first[0], 3), "first_load_s": round(first[1], 3),
         "staging": "pinned host buffers per optimizer, pinned by the first save / load "
                    "(untimed, reported as first_*) and reused",
-        "roofline": None, "e2e": None, "gpu_launches": 0, "clocks": None, "cpu_baseline": None,
+        "roofline": None,
+        "e2e": {"value": round(state_bytes / sv / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": state_bytes, "d2h_bytes_per_step": state_bytes,
+                "note": "the line is itself end to end: the save copies the device state out "
+                        "and writes the files, the load reads them and copies the new ranks' "
+                        "state in, through the public checkpoint calls, timed on the host"},
+        "gpu_launches": 0, "clocks": None, "cpu_baseline": cpu,
         "note": "host-IO bound (device <-> pinned host copies and file reads / writes); "
                 "no GPU kernel runs"}))
 
@@ -1508,6 +1560,11 @@ def run_accum(args):
     acc_ms, fused_ms, ag_ms = _avg_ms(events, 0, 1), _avg_ms(events, 1, 2), _avg_ms(events, 2, 3)
     ms = total_ms / args.steps
     all_bytes = allreduce_sum(world, step_bytes)
+    e2e = None
+    if not args.no_e2e:
+        e2e = _e2e_plain(torch, stream, micro, [full], lambda: one_step(None), step_bytes, world,
+                         args.e2e_steps, f"the {M} micro-batches' bf16 gradients of the {nd} "
+                         f"contributions in, the gathered layer unit out")
     if rank != 0:
         _finish_dist(world)
         return
@@ -1556,8 +1613,7 @@ def run_accum(args):
                                        f"({n_acc} launches over {nd} x {S} elements)",
                               acc_bytes // n_acc, _traffic(ACCUM_WORKLOAD, nd * S, args)
                               if fused_last else None),
-        "e2e": None, "e2e_note": "device-resident micro-batch gradients; the end-to-end "
-                                 "line is the default workload's",
+        "e2e": e2e,
         "gpu_launches": launches, "clocks": clk, "cpu_baseline": cpu}))
     _finish_dist(world)
 
@@ -1754,6 +1810,11 @@ def run_ddp(args):
             "ms": round(f_ms, 4), "gbs": round(f_bytes / (f_ms / 1e3) / 1e9, 1),
             "bytes": f_bytes, "time_vs_two_calls": round(f_ms / ms, 4),
             "kernel": ss.last_kernel()}
+    e2e = None
+    if not args.no_e2e:
+        e2e = _e2e_plain(torch, stream, grads, [pb], lambda: one_step(None), step_bytes, world,
+                         args.e2e_steps, "the 8 ranks' bucketed bf16 gradients in, the "
+                         "bf16 parameters out")
     if rank != 0:
         _finish_dist(world)
         return
@@ -1800,13 +1861,59 @@ def run_ddp(args):
         "roofline_allreduce": _roofline(ar_gbs, f"{kernel_names['allreduce']} at N_d = {nd} "
                                                 f"({len(boff) - 1} launches, one per bucket; "
                                                 f"the last bucket's kernel named)", ar_bytes),
-        "e2e": None, "e2e_note": "device-resident gradients; the end-to-end line is the "
-                                 "default workload's",
+        "e2e": e2e,
         "note": "buckets after the first of the call are launched as programmatic dependents "
                 "of the previous bucket's kernel" if not args.no_dependent_launch else
                 "every bucket an ordinary launch",
         "gpu_launches": launches, "clocks": clk, "cpu_baseline": cpu}))
     _finish_dist(world)
+
+
+def _e2e_plain(torch, stream, inputs, outputs, step_fn, step_bytes, world, steps, what):
+    """End to end through the public calls with host buffers: every step
+    copies the step's inputs in from pinned host memory, issues the step's
+    calls and reads its outputs back, all on the compute stream, with no
+    overlap.  ``inputs`` / ``outputs`` are the device tensors the step reads
+    / produces; ``step_fn()`` issues the step.  Every rank takes part in the
+    same reductions, whatever happened; returns the line's ``e2e`` object
+    (GB/s of the step's algorithmic bytes)."""
+    failed, ms, h2d, d2h = "", 0.0, 0, 0
+    try:
+        pairs = [(d, torch.empty(d.shape, dtype=d.dtype, pin_memory=True)) for d in inputs]
+        for d, h in pairs:
+            h.copy_(d)
+        host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outputs]
+        h2d = sum(d.numel() * d.element_size() for d in inputs)
+        d2h = sum(o.numel() * o.element_size() for o in outputs)
+        n = max(1, steps)
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            for d, h in pairs:
+                d.copy_(h, non_blocking=True)
+            step_fn()
+            for o, h in zip(outputs, host_out):
+                h.copy_(o, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / n
+        del pairs, host_out
+    except RuntimeError as exc:          # e.g. the host cannot pin this much memory
+        failed = str(exc).splitlines()[0][:200]
+        torch.cuda.synchronize()
+    n_failed = allreduce_sum(world, 1.0 if failed else 0.0)
+    ms = allreduce_max(world, ms)
+    total = allreduce_sum(world, float(step_bytes))
+    if n_failed:
+        return {"value": None, "unit": "GB/s",
+                "unavailable": f"end-to-end leg failed on {int(n_failed)} rank(s): "
+                               f"{failed or 'another rank'}"}
+    return {"value": round(total / (ms / 1e3) / 1e9, 1), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4),
+            "path": f"{what}: pinned host inputs copied in, the step's C-ABI calls, the "
+                    f"outputs read back, every step on the compute stream, no overlap"}
 
 
 # ------------------------------------ small workloads: the whole job
@@ -1873,7 +1980,6 @@ class _SmallJob:
             fused_b = (6 * nd + 26) * P             # every rank's shard: P elements
             self.parts = [("accumulate", acc_b), ("fused", fused_b), ("all-gather", 4 * P)]
             self.shard_elements = P
-            self.h2d = nd * M * P * 2
         else:
             self.opts = [RankShardOptimizer(w.units, nd, r, self.hp, device=dev)
                          for r in range(nd)]
@@ -1888,8 +1994,6 @@ class _SmallJob:
             self.S, self.P = S, Pu
             self.parts = [("fused", (2 * nd + 26) * S * nd), ("all-gather", 4 * Pu)]
             self.shard_elements = S * nd
-            self.h2d = nd * nd * S * 2
-        self.d2h = 2 * self.P
         self.step_bytes = sum(b for _, b in self.parts)
         self.state = None
         self.t = 0
@@ -1950,13 +2054,11 @@ class _SmallJob:
         if ev is not None:
             ev[3].record()
 
-    def host_inputs(self):
-        """(device buffer, pinned host copy) of every gradient input: what an
-        end-to-end step brings in from the host."""
-        torch = self.torch
-        bufs = (list(self.g) if self.name == UNIT9M_WORKLOAD
+    def inputs(self):
+        """The device buffers of every gradient input: what an end-to-end step
+        brings in from the host."""
+        return (list(self.g) if self.name == UNIT9M_WORKLOAD
                 else [x for o in self.opts for x in o.grad_in])
-        return [(b, torch.empty(b.shape, dtype=b.dtype, pin_memory=True).copy_(b)) for b in bufs]
 
 
 def _small_oracle(w_name, budget_s):
@@ -2116,26 +2218,9 @@ def run_small(args):
     # the gathered unit copied out, inside the timing, each step
     e2e = None
     if not args.no_e2e:
-        pairs = job.host_inputs()
-        host_out = torch.empty(job.full.shape, dtype=job.full.dtype, pin_memory=True)
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        n_e2e = max(1, args.e2e_steps)
-        torch.cuda.synchronize()
-        a.record(stream)
-        for _ in range(n_e2e):
-            for d, h in pairs:
-                d.copy_(h, non_blocking=True)
-            run(None)
-            host_out.copy_(job.full, non_blocking=True)
-        b.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms = allreduce_max(world, a.elapsed_time(b) / n_e2e)
-        e2e = {"value": round(allreduce_sum(world, job.step_bytes) / (e2e_ms / 1e3) / 1e9, 1),
-               "unit": "GB/s", "h2d_bytes_per_step": job.h2d, "d2h_bytes_per_step": job.d2h,
-               "ms_per_step": round(e2e_ms, 4),
-               "path": "pinned host gradients copied in on the compute stream, then the step's "
-                       "C-ABI calls, then the gathered unit copied out; no overlap"}
+        e2e = _e2e_plain(torch, stream, job.inputs(), [job.full], lambda: run(None),
+                         job.step_bytes, world, args.e2e_steps,
+                         "every rank's gradients (every micro-batch) in, the gathered unit out")
 
     cpu = None
     if rank == 0 and not args.no_cpu:
