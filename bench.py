@@ -901,6 +901,30 @@ def run_fsdp2(args):
     fused_launch = fused_b / nd
     achieved = fused_launch / (avg[1] / nd / 1e3) / 1e9
     value = allreduce_sum(world, step_b * args.steps) / (total_ms / 1e3) / 1e9
+    # the same step without the chunk-cat copy: every rank's update read
+    # straight from the ranks' per-parameter gradients (same bits)
+    direct_b = fused_b + ag_b
+
+    def direct_step():
+        t_step[0] += 1
+        for r in range(nd):
+            sl = slice(r * L, (r + 1) * L)
+            ss.fsdp2_rs_avg_adamw_cast(grads, r, master[sl], m[sl], v[sl], out[sl], hp,
+                                       t_step[0])
+        ss.fsdp2_all_gather_copy_out([out[r * L:(r + 1) * L] for r in range(nd)], params)
+
+    for _ in range(3):
+        direct_step()
+    da = torch.cuda.Event(enable_timing=True)
+    db = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    da.record(stream)
+    for _ in range(args.steps):
+        direct_step()
+    db.record(stream)
+    torch.cuda.synchronize()
+    direct_ms = allreduce_max(world, da.elapsed_time(db) / args.steps)
+    direct_kernel = ss.last_kernel()
     e2e = None
     if not args.no_e2e:
         e2e = _e2e_plain(torch, stream, [g for gs in grads for g in gs], params,
@@ -935,7 +959,17 @@ def run_fsdp2(args):
                         "fused_ms_per_launch": round(avg[1] / nd, 4),
                         "fused_gbs": round(achieved, 1),
                         "copy_out_ms": round(avg[2], 4),
-                        "copy_out_gbs": round(ag_b / (avg[2] / 1e3) / 1e9, 1)},
+                        "copy_out_gbs": round(ag_b / (avg[2] / 1e3) / 1e9, 1),
+                        "step_without_chunk_cat": {
+                            "ms": round(direct_ms, 4),
+                            "gbs": round(direct_b / (direct_ms / 1e3) / 1e9, 1),
+                            "bytes": direct_b,
+                            "time_vs_chunk_cat_step": round(direct_ms / (total_ms / args.steps),
+                                                            4),
+                            "kernel": direct_kernel,
+                            "note": "fsdp2_rs_avg_adamw_cast per rank (one fused launch per "
+                                    "parameter, read straight from the ranks' gradients) + "
+                                    "the copy-out: the same bits as the chunk-cat step"}},
             "roofline": _roofline(achieved, f"{fused_kernel} on one rank's local buffer",
                                   fused_launch),
             "e2e": e2e, "gpu_launches": launches, "clocks": clk, "cpu_baseline": cpu,

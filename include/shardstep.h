@@ -469,6 +469,35 @@ int fsdp2_all_gather_copy_out(const void* const* local_bufs, const int64_t* dim0
                               const int64_t* row, int32_t n, int32_t nd, int32_t dtype,
                               void* const* params, void* stream);
 
+/* fsdp2_rs_avg_adamw_cast -- device; one fused launch per parameter the rank
+ * holds rows of, one small launch per parameter with padding rows.
+ * Rank `rank`'s FSDP2 optimizer step read straight from the ranks' full
+ * per-parameter gradients ([P1] FSDP2 section: a group's parameters are
+ * reduce-scattered together; the emulated reduce-scatter needs no
+ * contiguous send buffer, so the chunk-cat copy is skipped).  The same bits
+ * as fsdp2_chunk_cat of every rank's gradients followed by
+ * fsdp_rs_avg_adamw_cast over the N_d pieces at rank*local: at held rows
+ *     g = (grads[0][t][j] + grads[1][t][j] + ...) / N_d,
+ *     j = rank*c_t*row[t] + k   (rank order, fp32, as fsdp_rs_avg_adamw_cast)
+ * and at padding rows every contribution is +0, so AdamW runs on g = +0.
+ *   grads[nd*n]   host array of device pointers: grads[q*n + t] is rank q's
+ *                 full contiguous gradient of parameter t (dim0[t]*row[t]
+ *                 elements; NULL allowed for an empty parameter), all of
+ *                 grad_dtype (SHARDSTEP_DTYPE_BF16, _F16 or _F32).
+ *   dim0, row, n  the group's shapes, as in fsdp2_layout.
+ *   rank          0 <= rank < nd.
+ *   master, m, v  device fp32, the rank's padded local buffers (`local`
+ *                 elements, fsdp2_layout's offsets), updated in place.
+ *   out_bf16      device, `local` elements: the updated parameters in bf16.
+ *   hp            host, as in fsdp_rs_avg_adamw_cast.
+ * No gradient may overlap an output; the outputs must not overlap one
+ * another.  Errors: INVALID (dtype, nd, rank, NULL, alignment, overlap, bad
+ * shapes), CAPACITY (nd > SHARDSTEP_MAX_ND), CUDA. */
+int fsdp2_rs_avg_adamw_cast(const void* const* grads, int32_t grad_dtype, const int64_t* dim0,
+                            const int64_t* row, int32_t n, int32_t nd, int32_t rank,
+                            float* master, float* m, float* v, uint16_t* out_bf16,
+                            const shardstep_adamw_t* hp, void* stream);
+
 /* ---------------------------------------------------- DDP buckets */
 
 /* ddp_bucket_plan -- host only.

@@ -29,7 +29,7 @@ __all__ = [
     "fsdp2_all_gather_copy_out", "AdamWState", "fsdp_state_rs_avg_adamw_cast",
     "fsdp_accumulate_rs_avg_adamw_cast", "fsdp_state_accumulate_rs_avg_adamw_cast",
     "ddp_bucket_allreduce_avg_adamw_cast", "set_tma_wait_ns", "check_mean_division",
-    "fsdp_shard_pieces",
+    "fsdp_shard_pieces", "fsdp2_rs_avg_adamw_cast",
 ]
 
 
@@ -526,6 +526,42 @@ def fsdp2_chunk_cat(grads, nd: int, out=None, stream=None):
         len(grads), nd, _dtype_code(out), ctypes.c_void_p(out.data_ptr()),
         _stream(stream, out.device)))
     return out
+
+
+def fsdp2_rs_avg_adamw_cast(rank_grads, rank: int, master, m, v, out_bf16, hp: AdamW, step: int,
+                            stream=None):
+    """Rank ``rank``'s FSDP2 step read straight from every rank's full
+    per-parameter gradients (``rank_grads[q][t]``: rank q's gradient of
+    parameter t, global shape): the bits of ``fsdp2_chunk_cat`` of each
+    rank's gradients followed by ``fsdp_rs_avg_adamw_cast`` on the rank's
+    pieces, without the chunk-cat copy.  ``master`` / ``m`` / ``v`` /
+    ``out_bf16`` are the rank's padded local buffers."""
+    import torch
+    nd = len(rank_grads)
+    if nd == 0:
+        raise ValueError("need at least one rank")
+    shapes = [tuple(g.shape) for g in rank_grads[0]]
+    gd = rank_grads[0][0].dtype if shapes else torch.bfloat16
+    for gs in rank_grads:
+        _need_cuda(*gs)
+        if [tuple(g.shape) for g in gs] != shapes or any(g.dtype != gd for g in gs):
+            raise ValueError("every rank's gradients must have the same shapes and dtype")
+    _need_cuda(master, m, v, out_bf16)
+    L = fsdp2_layout(shapes, nd).local
+    for t in (master, m, v):
+        if t.dtype != torch.float32 or t.numel() != L:
+            raise ValueError(f"master / m / v must be fp32 with {L} elements")
+    if out_bf16.dtype != torch.bfloat16 or out_bf16.numel() != L:
+        raise ValueError(f"out must be bf16 with {L} elements")
+    d0, row = _dims(shapes)
+    hpc = hp.at_step(step)
+    code = _dtype_code(rank_grads[0][0]) if shapes else _capi.DTYPE_BF16
+    _capi.check("fsdp2_rs_avg_adamw_cast", _capi.lib().fsdp2_rs_avg_adamw_cast(
+        _capi.ptr_array([g.data_ptr() for gs in rank_grads for g in gs]), code,
+        _capi.i64_array(d0), _capi.i64_array(row), len(shapes), nd, int(rank),
+        ctypes.c_void_p(master.data_ptr()), ctypes.c_void_p(m.data_ptr()),
+        ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(out_bf16.data_ptr()), ctypes.byref(hpc),
+        _stream(stream, master.device)))
 
 
 def fsdp2_all_gather_copy_out(local_bufs, params, stream=None):

@@ -1163,6 +1163,71 @@ int fsdp2_all_gather_copy_out(const void* const* local_bufs, const int64_t* dim0
     return ok();
 }
 
+int fsdp2_rs_avg_adamw_cast(const void* const* grads, int32_t grad_dtype, const int64_t* dim0,
+                            const int64_t* row, int32_t n, int32_t nd, int32_t rank,
+                            float* master, float* m, float* v, uint16_t* out_bf16,
+                            const shardstep_adamw_t* hp, void* stream) {
+    const int es = elem_size_of(grad_dtype);
+    if (es == 0) return fail(SHARDSTEP_ERR_INVALID, "unknown grad dtype %d", grad_dtype);
+    if (nd > SHARDSTEP_MAX_ND)
+        return fail(SHARDSTEP_ERR_CAPACITY, "nd %d > %d", nd, SHARDSTEP_MAX_ND);
+    Fsdp2Plan plan;
+    int rc = fsdp2_plan(dim0, row, n, nd, &plan);
+    if (rc != SHARDSTEP_OK) return rc;
+    if (rank < 0 || rank >= nd) return fail(SHARDSTEP_ERR_INVALID, "rank %d not in [0, %d)", rank, nd);
+    AdamScalars c{};
+    if (int rc2 = adam_source(hp, nullptr, &c); rc2 != SHARDSTEP_OK) return rc2;
+    const int64_t L = plan.local;
+    if (L == 0) return ok();
+    Span outs[4];
+    if (int rc2 = check_step_outputs(L, master, m, v, out_bf16, outs); rc2 != SHARDSTEP_OK)
+        return rc2;
+    if (n > 0 && grads == nullptr) return fail(SHARDSTEP_ERR_INVALID, "grads is NULL");
+    // every gradient whole: present, aligned, and clear of the local buffers
+    for (int32_t q = 0; q < nd; ++q)
+        for (int32_t t = 0; t < n; ++t) {
+            const int64_t bytes = dim0[t] * row[t] * es;
+            if (bytes == 0) continue;
+            const void* g = grads[static_cast<int64_t>(q) * n + t];
+            if (g == nullptr) return fail(SHARDSTEP_ERR_INVALID, "grads[%d][%d] is NULL", q, t);
+            if (!aligned(g, es))
+                return fail(SHARDSTEP_ERR_INVALID, "grads[%d][%d] is not %d-byte aligned", q, t, es);
+            for (const Span& o : outs)
+                if (overlap(span(g, bytes), o))
+                    return fail(SHARDSTEP_ERR_INVALID, "grads[%d][%d] overlaps an output", q, t);
+        }
+    // per parameter: the fused step over the rank's rows, slice q = rank q's
+    // gradient from row rank * chunk; AdamW on a zero gradient over the
+    // padding rows
+    std::vector<const void*> slices(nd);
+    bool fused_launched = false, pad_launched = false;
+    for (int32_t t = 0; t < n; ++t) {
+        const int64_t off = plan.offset[t];
+        const int64_t have = rows_of(plan, dim0, rank, t) * row[t];
+        const int64_t pad = plan.chunk[t] * row[t] - have;
+        if (have > 0) {
+            const int64_t src = static_cast<int64_t>(rank) * plan.chunk[t] * row[t] * es;
+            for (int32_t q = 0; q < nd; ++q)
+                slices[q] = static_cast<const char*>(grads[static_cast<int64_t>(q) * n + t]) + src;
+            rc = fused_step(slices.data(), grad_dtype, nd, nd, have, master + off, m + off, v + off,
+                            out_bf16 + off, hp, stream);
+            if (rc != SHARDSTEP_OK) return rc;
+            fused_launched = true;
+        }
+        if (pad > 0) {
+            cudaError_t e = launch_adamw_zero_grad(pad, master + off + have, m + off + have,
+                                                   v + off + have, out_bf16 + off + have, c,
+                                                   static_cast<cudaStream_t>(stream));
+            if (e != cudaSuccess) return cuda_fail(e, "zero-gradient AdamW launch");
+            // the padding rows are in the reduce-scatter a real group sends
+            count_comm(reduce_comm_bytes(nd, nd, pad, es));
+            pad_launched = true;
+        }
+    }
+    if (pad_launched && !fused_launched) note_kernel("adamw_zero_grad");
+    return ok();
+}
+
 int ddp_bucket_plan(const int64_t* numels, int32_t n, int32_t elem_size, int64_t cap_bytes,
                     int64_t* param_offset, int32_t* bucket_of_param, int64_t* bucket_offsets,
                     int32_t* n_buckets) {

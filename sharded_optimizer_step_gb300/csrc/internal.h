@@ -185,6 +185,9 @@ constexpr int64_t kTmaMinElements = 4096;
 
 cudaError_t launch_allreduce_avg(const PtrTable& tab, int nd, int64_t n, uint16_t* out,
                                  const MeanOp& mo, bool vec, bool pdl, cudaStream_t stream);
+// AdamW with a zero gradient over n elements (FSDP2 padding rows).
+cudaError_t launch_adamw_zero_grad(int64_t n, float* master, float* m, float* v, uint16_t* out,
+                                   const AdamScalars& c, cudaStream_t stream);
 // The DDP all-reduce average fused with the replicated AdamW + cast over n
 // bucketed elements (step.cu); mean_out may be null.  `vec`: state 16-byte,
 // gradients, mean_out and out 8-byte aligned.

@@ -120,6 +120,20 @@ def test_fsdp2_step_counts_rs_plus_ag():
     ss.fsdp2_all_gather_copy_out([out] * nd, params)
     got = ss.comm_counter(reset=True)
     assert got == pytest.approx(ss.comm_bytes(nd * L, nd, "zero1", exact=True), rel=1e-12)
+    # the same step read straight from the gradients counts the same bytes,
+    # padding rows included
+    shapes2 = [(4099, 7), (13,), (1030, 3)]
+    L2 = ss.fsdp2_layout(shapes2, nd).local
+    g2 = [[torch.zeros(s, dtype=torch.bfloat16, device=DEV) for s in shapes2] for _ in range(nd)]
+    st2 = [torch.zeros(L2, device=DEV) for _ in range(3)]
+    out2 = torch.empty(L2, dtype=torch.bfloat16, device=DEV)
+    params2 = [torch.empty(s, dtype=torch.bfloat16, device=DEV) for s in shapes2]
+    torch.cuda.synchronize()
+    ss.comm_counter(reset=True)
+    ss.fsdp2_rs_avg_adamw_cast(g2, 0, *st2, out2, ss.AdamW(), 1)
+    ss.fsdp2_all_gather_copy_out([out2] * nd, params2)
+    got = ss.comm_counter(reset=True)
+    assert got == pytest.approx(ss.comm_bytes(nd * L2, nd, "zero1", exact=True), rel=1e-12)
 
 
 def test_fp32_contributions_and_the_scaler_flag():

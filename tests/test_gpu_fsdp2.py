@@ -174,3 +174,92 @@ def test_fsdp2_llama_layer_group_full_size():
         got = _host(params[t].reshape(-1)[torch.from_numpy(flat_idx).to(DEV)])
         assert_bits(got, ob, f"param {t}")
     del olay
+
+
+# ------------------------------------ the step read straight from the gradients
+
+def _f32_dev(h):
+    return torch.from_numpy(np.ascontiguousarray(h, dtype=np.float32)).to(DEV)
+
+
+@pytest.mark.parametrize("shapes", SHAPE_SETS, ids=lambda s: f"{len(s)}params")
+@pytest.mark.parametrize("nd", [1, 2, 3, 4, 8])
+@pytest.mark.parametrize("gdt", ["bf16", "f32"])
+def test_fsdp2_step_without_chunk_cat_matches_oracle(shapes, nd, gdt, path):
+    """fsdp2_rs_avg_adamw_cast on every rank, two steps, against the oracle's
+    chunk-cat + shard step.  The local state starts non-zero everywhere,
+    padding rows included, so that the padding rows' update (AdamW on a
+    zero gradient) is checked too."""
+    lay = oracle.fsdp2_layout(shapes, nd)
+    L = lay.local
+    state = []
+    for r in range(nd):
+        p = synth.host_fill(synth.normal_stream(5, (88, r), 0.02), 0, L, "f32")
+        m0 = synth.host_fill(synth.normal_stream(5, (87, r), 1e-4), 0, L, "f32")
+        v0 = np.abs(synth.host_fill(synth.normal_stream(5, (86, r), 1e-6), 0, L, "f32"))
+        state.append(dict(p=p, m=m0, v=v0, dp=_f32_dev(p), dm=_f32_dev(m0), dv=_f32_dev(v0),
+                          out=torch.empty(L, dtype=torch.bfloat16, device=DEV)))
+    for t in (1, 2):
+        grads_h = [_tensors(shapes, 300 * t + q, gdt) for q in range(nd)]
+        grads = [[_dev(x.reshape(-1)).view(x.shape) for x in g] for g in grads_h]
+        cc_h = [oracle.chunk_cat(g, lay) for g in grads_h]
+        for r, st in enumerate(state):
+            ss.fsdp2_rs_avg_adamw_cast(grads, r, st["dp"], st["dm"], st["dv"], st["out"], HPC, t)
+            st["p"], st["m"], st["v"], st["ob"] = oracle.fsdp_shard_step(
+                cc_h, r, L, st["p"], st["m"], st["v"], HP, t)
+        torch.cuda.synchronize()
+        for r, st in enumerate(state):
+            assert_bits(_host(st["dp"]), st["p"], f"step {t} rank {r} master")
+            assert_bits(_host(st["dm"]), st["m"], f"step {t} rank {r} m")
+            assert_bits(_host(st["dv"]), st["v"], f"step {t} rank {r} v")
+            assert_bits(_host(st["out"]), st["ob"], f"step {t} rank {r} bf16")
+
+
+def test_fsdp2_step_without_chunk_cat_equals_the_chunk_cat_path():
+    """On the GPU both compositions give the same bits on one Llama-7B layer
+    group at 8 ranks (a rank's 9 parameters, 25.3M local elements), and the
+    call launches one kernel per parameter."""
+    w = W.llama_7b_rank_view()
+    shapes = w.units[0]
+    nd, r = 8, 3
+    lay = ss.fsdp2_layout(shapes, nd)
+    L = lay.local
+    grads = [[torch.empty(s, dtype=torch.bfloat16, device=DEV) for s in shapes] for _ in range(nd)]
+    for q in range(nd):
+        for k, g in enumerate(grads[q]):
+            synth.dev_fill(w.grad_stream(1, q, 0, 0, k), g)
+    p0 = torch.empty(L, device=DEV)
+    synth.dev_fill(synth.normal_stream(7, (85,), 0.02), p0)
+    a = [p0.clone(), torch.zeros(L, device=DEV), torch.zeros(L, device=DEV),
+         torch.empty(L, dtype=torch.bfloat16, device=DEV)]
+    b = [p0.clone(), torch.zeros(L, device=DEV), torch.zeros(L, device=DEV),
+         torch.empty(L, dtype=torch.bfloat16, device=DEV)]
+    cc = [ss.fsdp2_chunk_cat(grads[q], nd) for q in range(nd)]
+    ss.fsdp_rs_avg_adamw_cast([c[r * L:(r + 1) * L] for c in cc], *a, HPC, 1)
+    torch.cuda.synchronize()
+    before = ss.launch_count()
+    ss.fsdp2_rs_avg_adamw_cast(grads, r, *b, HPC, 1)
+    torch.cuda.synchronize()
+    assert ss.launch_count() - before == len(shapes)
+    for x, y, name in zip(a, b, ("master", "m", "v", "bf16")):
+        assert torch.equal(x.view(torch.uint8), y.view(torch.uint8)), name
+
+
+def test_fsdp2_step_without_chunk_cat_rejects_bad_arguments():
+    shapes = [(5, 3), (2,)]
+    nd = 2
+    L = ss.fsdp2_layout(shapes, nd).local
+    grads = [[torch.zeros(s, dtype=torch.bfloat16, device=DEV) for s in shapes]
+             for _ in range(nd)]
+    st = [torch.zeros(L, device=DEV) for _ in range(3)]
+    out = torch.empty(L, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(ss.ShardstepError):
+        ss.fsdp2_rs_avg_adamw_cast(grads, 2, *st, out, HPC, 1)          # rank out of range
+    with pytest.raises(ValueError):
+        ss.fsdp2_rs_avg_adamw_cast(grads, 0, *st, out[:-1], HPC, 1)     # wrong local length
+    # a gradient that overlaps the local state
+    big = torch.zeros(4 * L + 64, device=DEV)
+    with pytest.raises(ss.ShardstepError):
+        ss.fsdp2_rs_avg_adamw_cast([[big[:15].view(5, 3), torch.zeros(2, device=DEV)]] * nd, 0,
+                                   big[:L], big[L:2 * L], big[2 * L:3 * L],
+                                   torch.empty(L, dtype=torch.bfloat16, device=DEV), HPC, 1)

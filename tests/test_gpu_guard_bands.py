@@ -251,3 +251,28 @@ def test_fused_ddp_step_writes_only_its_outputs(nd, keep_mean):
     for q, (g, b) in enumerate(zip(grads, before)):
         g.check(f"gradient {q}")
         assert torch.equal(g.t.view(torch.uint8), b.view(torch.uint8)), f"gradient {q} written"
+
+
+@pytest.mark.parametrize("nd", [1, 3, 8])
+def test_fsdp2_step_without_chunk_cat_writes_only_its_outputs(nd, path):
+    """The FSDP2 step read straight from the gradients (uneven dim 0, so
+    padding rows get their own launch): master / m / v / out inside bands,
+    the gradients (also in bands) read, never written."""
+    shapes = [(1023, 130), (7,), (300, 512), (5, 3)]
+    L = ss.fsdp2_layout(shapes, nd).local
+    grads = [[Guarded(int(np.prod(s)), torch.bfloat16, (q + k) % 3,
+                      _bf16(int(np.prod(s)), 200 + 10 * q + k)) for k, s in enumerate(shapes)]
+             for q in range(nd)]
+    before = [g.t.clone() for gs in grads for g in gs]
+    outs = [Guarded(L, torch.float32, 1, torch.randn(L, device=DEV) * 0.02),
+            Guarded(L, torch.float32, 1, torch.zeros(L, device=DEV)),
+            Guarded(L, torch.float32, 1, torch.zeros(L, device=DEV)),
+            Guarded(L, torch.bfloat16, 3)]
+    for r in range(nd):
+        ss.fsdp2_rs_avg_adamw_cast([[g.t.view(s) for g, s in zip(gs, shapes)] for gs in grads], r,
+                                   *[o.t for o in outs], ss.AdamW(), 1)
+        for name, o in zip(("master", "m", "v", "bf16"), outs):
+            o.check(f"FSDP2 step rank {r} {name}")
+    for k, (g, b) in enumerate(zip([g for gs in grads for g in gs], before)):
+        g.check(f"gradient {k}")
+        assert torch.equal(g.t.view(torch.uint8), b.view(torch.uint8)), f"gradient {k} written"

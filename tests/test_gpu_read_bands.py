@@ -194,3 +194,27 @@ def test_copies_read_only_their_sources(path):
         return _bytes(flat, full, cc, *outs)
 
     _same_for_every_poison(run)
+
+
+@pytest.mark.parametrize("nd", [1, 3, 8])
+def test_fsdp2_step_without_chunk_cat_reads_only_its_inputs(nd, path):
+    shapes = [(1023, 130), (7,), (300, 512), (5, 3)]
+    L = ss.fsdp2_layout(shapes, nd).local
+    gh = [[_host("bf16", int(np.prod(s)), 140 + 10 * q + k, 1e-3) for k, s in enumerate(shapes)]
+          for q in range(nd)]
+    ph = _host("f32", L, 150, 0.02)
+
+    def run(poison):
+        grads = [[_poisoned(h, "bf16", (q + k) % 3, poison).view(s)
+                  for k, (h, s) in enumerate(zip(gs, shapes))] for q, gs in enumerate(gh)]
+        res = []
+        for r in range(nd):
+            p = _poisoned(ph, "f32", 1, poison)
+            m = _poisoned(np.zeros(L, np.float32), "f32", 1, poison)
+            v = _poisoned(np.zeros(L, np.float32), "f32", 1, poison)
+            out = torch.empty(L, dtype=torch.bfloat16, device=DEV)
+            ss.fsdp2_rs_avg_adamw_cast(grads, r, p, m, v, out, ss.AdamW(), 1)
+            res += _bytes(p, m, v, out)
+        return res
+
+    _same_for_every_poison(run)
