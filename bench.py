@@ -967,9 +967,10 @@ def run_fsdp2(args):
                             "time_vs_chunk_cat_step": round(direct_ms / (total_ms / args.steps),
                                                             4),
                             "kernel": direct_kernel,
-                            "note": "fsdp2_rs_avg_adamw_cast per rank (one fused launch per "
-                                    "parameter, read straight from the ranks' gradients) + "
-                                    "the copy-out: the same bits as the chunk-cat step"}},
+                            "note": "fsdp2_rs_avg_adamw_cast per rank (one launch over all "
+                                    "its parameters, read straight from the ranks' "
+                                    "gradients) + the copy-out: the same bits as the "
+                                    "chunk-cat step"}},
             "roofline": _roofline(achieved, f"{fused_kernel} on one rank's local buffer",
                                   fused_launch),
             "e2e": e2e, "gpu_launches": launches, "clocks": clk, "cpu_baseline": cpu,

@@ -14,7 +14,8 @@ INCLUDE = os.path.join(ROOT, "include")
 OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libshardstep.so")
 
-SOURCES = ["step.cu", "step_tma.cu", "copy.cu", "accum_step.cu", "state.cu", "api.cpp", "ckpt.cpp", "ready.cpp"]
+SOURCES = ["step.cu", "step_tma.cu", "copy.cu", "accum_step.cu", "fsdp2_step.cu", "state.cu",
+           "api.cpp", "ckpt.cpp", "ready.cpp"]
 HEADERS = ["common.cuh", "internal.h"]
 ARCH = "103a"
 

@@ -1196,9 +1196,41 @@ int fsdp2_rs_avg_adamw_cast(const void* const* grads, int32_t grad_dtype, const 
                 if (overlap(span(g, bytes), o))
                     return fail(SHARDSTEP_ERR_INVALID, "grads[%d][%d] overlaps an output", q, t);
         }
-    // per parameter: the fused step over the rank's rows, slice q = rank q's
-    // gradient from row rank * chunk; AdamW on a zero gradient over the
-    // padding rows
+    // Segments: per parameter, the rank's rows (slice q = rank q's gradient
+    // from row rank * chunk) and its padding rows (every contribution +0).
+    // Aligned ones go into tables of one launch each (rs_adamw_cast_segs);
+    // the others, and every one when the TMA path is forced, take the fused
+    // step per parameter and the zero-gradient AdamW per padding run.
+    const bool segs_ok = g_fused_path.load(std::memory_order_relaxed) != SHARDSTEP_PATH_TMA &&
+                         aligned(master, 16) && aligned(m, 16) && aligned(v, 16) &&
+                         aligned(out_bf16, 8);
+    const uintptr_t slice_align = grad_dtype == SHARDSTEP_DTYPE_F32 ? 16 : 8;
+    const MeanOp mo = mean_op(nd, nd);
+    SegTable st{};
+    st.ns = 0;
+    st.b0[0] = 0;
+    int tables = 0;
+    auto flush = [&]() -> int {
+        if (st.ns == 0) return SHARDSTEP_OK;
+        cudaError_t e = launch_rs_adamw_cast_segs(st, nd, grad_dtype, master, m, v, out_bf16, c,
+                                                  mo, static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(e, "FSDP2 step launch");
+        ++tables;
+        st.ns = 0;
+        st.b0[0] = 0;
+        return SHARDSTEP_OK;
+    };
+    auto add_seg = [&](int64_t lo, int64_t cnt, const void* const* p) -> int {
+        if (st.ns == kSegMax || (st.ns + 1) * nd > kSegPtrMax)
+            if (int r = flush(); r != SHARDSTEP_OK) return r;
+        const int k = st.ns;
+        st.lo[k] = lo;
+        st.n[k] = cnt;
+        for (int32_t q = 0; q < nd; ++q) st.p[k * nd + q] = p != nullptr ? p[q] : nullptr;
+        st.b0[k + 1] = st.b0[k] + seg_blocks(cnt);
+        st.ns = k + 1;
+        return SHARDSTEP_OK;
+    };
     std::vector<const void*> slices(nd);
     bool fused_launched = false, pad_launched = false;
     for (int32_t t = 0; t < n; ++t) {
@@ -1207,24 +1239,41 @@ int fsdp2_rs_avg_adamw_cast(const void* const* grads, int32_t grad_dtype, const 
         const int64_t pad = plan.chunk[t] * row[t] - have;
         if (have > 0) {
             const int64_t src = static_cast<int64_t>(rank) * plan.chunk[t] * row[t] * es;
-            for (int32_t q = 0; q < nd; ++q)
+            bool vec = segs_ok && off % 4 == 0;
+            for (int32_t q = 0; q < nd; ++q) {
                 slices[q] = static_cast<const char*>(grads[static_cast<int64_t>(q) * n + t]) + src;
-            rc = fused_step(slices.data(), grad_dtype, nd, nd, have, master + off, m + off, v + off,
-                            out_bf16 + off, hp, stream);
-            if (rc != SHARDSTEP_OK) return rc;
-            fused_launched = true;
+                vec = vec && aligned(slices[q], slice_align);
+            }
+            if (vec) {
+                if (int r = add_seg(off, have, slices.data()); r != SHARDSTEP_OK) return r;
+                count_comm(reduce_comm_bytes(nd, nd, have, es));
+            } else {
+                rc = fused_step(slices.data(), grad_dtype, nd, nd, have, master + off, m + off,
+                                v + off, out_bf16 + off, hp, stream);
+                if (rc != SHARDSTEP_OK) return rc;
+                fused_launched = true;
+            }
         }
         if (pad > 0) {
-            cudaError_t e = launch_adamw_zero_grad(pad, master + off + have, m + off + have,
-                                                   v + off + have, out_bf16 + off + have, c,
-                                                   static_cast<cudaStream_t>(stream));
-            if (e != cudaSuccess) return cuda_fail(e, "zero-gradient AdamW launch");
             // the padding rows are in the reduce-scatter a real group sends
             count_comm(reduce_comm_bytes(nd, nd, pad, es));
-            pad_launched = true;
+            if (segs_ok && (off + have) % 4 == 0) {
+                if (int r = add_seg(off + have, pad, nullptr); r != SHARDSTEP_OK) return r;
+            } else {
+                cudaError_t e = launch_adamw_zero_grad(pad, master + off + have, m + off + have,
+                                                       v + off + have, out_bf16 + off + have, c,
+                                                       static_cast<cudaStream_t>(stream));
+                if (e != cudaSuccess) return cuda_fail(e, "zero-gradient AdamW launch");
+                pad_launched = true;
+            }
         }
     }
-    if (pad_launched && !fused_launched) note_kernel("adamw_zero_grad");
+    if (int r = flush(); r != SHARDSTEP_OK) return r;
+    if (tables > 0)
+        note_kernel("rs_adamw_cast_segs<%d, %s> (register-staged, %d launch%s)", nd,
+                    dtype_name(grad_dtype), tables, tables > 1 ? "es" : "");
+    else if (pad_launched && !fused_launched)
+        note_kernel("adamw_zero_grad");
     return ok();
 }
 

@@ -185,6 +185,27 @@ constexpr int64_t kTmaMinElements = 4096;
 
 cudaError_t launch_allreduce_avg(const PtrTable& tab, int nd, int64_t n, uint16_t* out,
                                  const MeanOp& mo, bool vec, bool pdl, cudaStream_t stream);
+// The segments of one FSDP2 step launch (launch_rs_adamw_cast_segs): segment
+// s covers local elements [lo[s], lo[s] + n[s]) and reads the N_d slices
+// p[s * nd + q] (p[s * nd] == nullptr: padding rows, every contribution +0);
+// b0[s] is its first block, b0[ns] the launch's block count.
+constexpr int kSegMax = 16;
+constexpr int kSegPtrMax = 128;
+struct SegTable {
+    const void* p[kSegPtrMax];
+    int64_t lo[kSegMax];
+    int64_t n[kSegMax];
+    int64_t b0[kSegMax + 1];
+    int ns;
+};
+// Blocks one segment of n elements takes in launch_rs_adamw_cast_segs.
+int64_t seg_blocks(int64_t n);
+// One launch over the table's segments: the fused step's reduce (rank
+// order), mean, AdamW and cast; every segment 16-byte aligned in the state
+// and 8-byte (16-bit slices) or 16-byte (fp32 slices) in its slices.
+cudaError_t launch_rs_adamw_cast_segs(const SegTable& st, int nd, int grad_type, float* master,
+                                      float* m, float* v, uint16_t* out, const AdamScalars& c,
+                                      const MeanOp& mo, cudaStream_t stream);
 // AdamW with a zero gradient over n elements (FSDP2 padding rows).
 cudaError_t launch_adamw_zero_grad(int64_t n, float* master, float* m, float* v, uint16_t* out,
                                    const AdamScalars& c, cudaStream_t stream);

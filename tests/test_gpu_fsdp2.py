@@ -183,7 +183,7 @@ def _f32_dev(h):
 
 
 @pytest.mark.parametrize("shapes", SHAPE_SETS, ids=lambda s: f"{len(s)}params")
-@pytest.mark.parametrize("nd", [1, 2, 3, 4, 8])
+@pytest.mark.parametrize("nd", [1, 2, 3, 4, 8, 12, 16])
 @pytest.mark.parametrize("gdt", ["bf16", "f32"])
 def test_fsdp2_step_without_chunk_cat_matches_oracle(shapes, nd, gdt, path):
     """fsdp2_rs_avg_adamw_cast on every rank, two steps, against the oracle's
@@ -218,7 +218,7 @@ def test_fsdp2_step_without_chunk_cat_matches_oracle(shapes, nd, gdt, path):
 def test_fsdp2_step_without_chunk_cat_equals_the_chunk_cat_path():
     """On the GPU both compositions give the same bits on one Llama-7B layer
     group at 8 ranks (a rank's 9 parameters, 25.3M local elements), and the
-    call launches one kernel per parameter."""
+    call launches one kernel for all 9 parameters."""
     w = W.llama_7b_rank_view()
     shapes = w.units[0]
     nd, r = 8, 3
@@ -240,7 +240,8 @@ def test_fsdp2_step_without_chunk_cat_equals_the_chunk_cat_path():
     before = ss.launch_count()
     ss.fsdp2_rs_avg_adamw_cast(grads, r, *b, HPC, 1)
     torch.cuda.synchronize()
-    assert ss.launch_count() - before == len(shapes)
+    assert ss.launch_count() - before == 1
+    assert ss.last_kernel().startswith("rs_adamw_cast_segs<8, bf16>")
     for x, y, name in zip(a, b, ("master", "m", "v", "bf16")):
         assert torch.equal(x.view(torch.uint8), y.view(torch.uint8)), name
 
