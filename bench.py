@@ -904,13 +904,13 @@ def run_fsdp2(args):
     # the same step without the chunk-cat copy: every rank's update read
     # straight from the ranks' per-parameter gradients (same bits)
     direct_b = fused_b + ag_b
+    fsdp2_step = ss.Fsdp2Step(grads)       # the gradient buffers checked once
 
     def direct_step():
         t_step[0] += 1
         for r in range(nd):
             sl = slice(r * L, (r + 1) * L)
-            ss.fsdp2_rs_avg_adamw_cast(grads, r, master[sl], m[sl], v[sl], out[sl], hp,
-                                       t_step[0])
+            fsdp2_step(r, master[sl], m[sl], v[sl], out[sl], hp, t_step[0])
         ss.fsdp2_all_gather_copy_out([out[r * L:(r + 1) * L] for r in range(nd)], params)
 
     for _ in range(3):
@@ -967,9 +967,9 @@ def run_fsdp2(args):
                             "time_vs_chunk_cat_step": round(direct_ms / (total_ms / args.steps),
                                                             4),
                             "kernel": direct_kernel,
-                            "note": "fsdp2_rs_avg_adamw_cast per rank (one launch over all "
-                                    "its parameters, read straight from the ranks' "
-                                    "gradients) + the copy-out: the same bits as the "
+                            "note": "fsdp2_rs_avg_adamw_cast per rank through Fsdp2Step (one "
+                                    "launch over all its parameters, read straight from the "
+                                    "ranks' gradients) + the copy-out: the same bits as the "
                                     "chunk-cat step"}},
             "roofline": _roofline(achieved, f"{fused_kernel} on one rank's local buffer",
                                   fused_launch),

@@ -29,7 +29,7 @@ __all__ = [
     "fsdp2_all_gather_copy_out", "AdamWState", "fsdp_state_rs_avg_adamw_cast",
     "fsdp_accumulate_rs_avg_adamw_cast", "fsdp_state_accumulate_rs_avg_adamw_cast",
     "ddp_bucket_allreduce_avg_adamw_cast", "set_tma_wait_ns", "check_mean_division",
-    "fsdp_shard_pieces", "fsdp2_rs_avg_adamw_cast",
+    "fsdp_shard_pieces", "fsdp2_rs_avg_adamw_cast", "Fsdp2Step",
 ]
 
 
@@ -535,33 +535,53 @@ def fsdp2_rs_avg_adamw_cast(rank_grads, rank: int, master, m, v, out_bf16, hp: A
     parameter t, global shape): the bits of ``fsdp2_chunk_cat`` of each
     rank's gradients followed by ``fsdp_rs_avg_adamw_cast`` on the rank's
     pieces, without the chunk-cat copy.  ``master`` / ``m`` / ``v`` /
-    ``out_bf16`` are the rank's padded local buffers."""
-    import torch
-    nd = len(rank_grads)
-    if nd == 0:
-        raise ValueError("need at least one rank")
-    shapes = [tuple(g.shape) for g in rank_grads[0]]
-    gd = rank_grads[0][0].dtype if shapes else torch.bfloat16
-    for gs in rank_grads:
-        _need_cuda(*gs)
-        if [tuple(g.shape) for g in gs] != shapes or any(g.dtype != gd for g in gs):
-            raise ValueError("every rank's gradients must have the same shapes and dtype")
-    _need_cuda(master, m, v, out_bf16)
-    L = fsdp2_layout(shapes, nd).local
-    for t in (master, m, v):
-        if t.dtype != torch.float32 or t.numel() != L:
-            raise ValueError(f"master / m / v must be fp32 with {L} elements")
-    if out_bf16.dtype != torch.bfloat16 or out_bf16.numel() != L:
-        raise ValueError(f"out must be bf16 with {L} elements")
-    d0, row = _dims(shapes)
-    hpc = hp.at_step(step)
-    code = _dtype_code(rank_grads[0][0]) if shapes else _capi.DTYPE_BF16
-    _capi.check("fsdp2_rs_avg_adamw_cast", _capi.lib().fsdp2_rs_avg_adamw_cast(
-        _capi.ptr_array([g.data_ptr() for gs in rank_grads for g in gs]), code,
-        _capi.i64_array(d0), _capi.i64_array(row), len(shapes), nd, int(rank),
-        ctypes.c_void_p(master.data_ptr()), ctypes.c_void_p(m.data_ptr()),
-        ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(out_bf16.data_ptr()), ctypes.byref(hpc),
-        _stream(stream, master.device)))
+    ``out_bf16`` are the rank's padded local buffers.  For repeated steps
+    over the same gradient buffers, ``Fsdp2Step`` checks them once."""
+    Fsdp2Step(rank_grads)(rank, master, m, v, out_bf16, hp, step, stream)
+
+
+class Fsdp2Step:
+    """``fsdp2_rs_avg_adamw_cast`` over one group's gradient buffers, checked
+    once: the ranks' per-parameter gradient tensors (``rank_grads[q][t]``)
+    are validated and their device pointers, shapes and the local length
+    taken when the object is made, and it keeps the tensors alive.  Each
+    call then checks only the rank's four local buffers before the C call
+    (which checks every pointer again), so a step of many small parameters
+    costs little host time."""
+
+    def __init__(self, rank_grads):
+        import torch
+        self.nd = len(rank_grads)
+        if self.nd == 0:
+            raise ValueError("need at least one rank")
+        self.shapes = [tuple(g.shape) for g in rank_grads[0]]
+        dt = rank_grads[0][0].dtype if self.shapes else torch.bfloat16
+        for gs in rank_grads:
+            _need_cuda(*gs)
+            if [tuple(g.shape) for g in gs] != self.shapes or any(g.dtype != dt for g in gs):
+                raise ValueError("every rank's gradients must have the same shapes and dtype")
+        self._keep = [list(gs) for gs in rank_grads]
+        self.local = fsdp2_layout(self.shapes, self.nd).local
+        d0, row = _dims(self.shapes)
+        self._d0, self._row = _capi.i64_array(d0), _capi.i64_array(row)
+        self._ptrs = _capi.ptr_array([g.data_ptr() for gs in rank_grads for g in gs])
+        self._code = _dtype_code(rank_grads[0][0]) if self.shapes else _capi.DTYPE_BF16
+
+    def __call__(self, rank: int, master, m, v, out_bf16, hp: AdamW, step: int, stream=None):
+        import torch
+        L = self.local
+        for t in (master, m, v):
+            if not t.is_cuda or t.dtype != torch.float32 or t.numel() != L or not t.is_contiguous():
+                raise ValueError(f"master / m / v must be contiguous CUDA fp32 with {L} elements")
+        if (not out_bf16.is_cuda or out_bf16.dtype != torch.bfloat16 or out_bf16.numel() != L
+                or not out_bf16.is_contiguous()):
+            raise ValueError(f"out must be contiguous CUDA bf16 with {L} elements")
+        hpc = hp.at_step(step)
+        _capi.check("fsdp2_rs_avg_adamw_cast", _capi.lib().fsdp2_rs_avg_adamw_cast(
+            self._ptrs, self._code, self._d0, self._row, len(self.shapes), self.nd, int(rank),
+            ctypes.c_void_p(master.data_ptr()), ctypes.c_void_p(m.data_ptr()),
+            ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(out_bf16.data_ptr()),
+            ctypes.byref(hpc), _stream(stream, master.device)))
 
 
 def fsdp2_all_gather_copy_out(local_bufs, params, stream=None):

@@ -264,3 +264,32 @@ def test_fsdp2_step_without_chunk_cat_rejects_bad_arguments():
         ss.fsdp2_rs_avg_adamw_cast([[big[:15].view(5, 3), torch.zeros(2, device=DEV)]] * nd, 0,
                                    big[:L], big[L:2 * L], big[2 * L:3 * L],
                                    torch.empty(L, dtype=torch.bfloat16, device=DEV), HPC, 1)
+
+
+def test_fsdp2_step_object_gives_the_same_bits_and_checks_its_buffers():
+    """Fsdp2Step (gradient buffers checked once) equals the function form,
+    step after step, and still rejects local buffers of the wrong kind."""
+    shapes = SHAPE_SETS[2]
+    nd = 4
+    L = ss.fsdp2_layout(shapes, nd).local
+    grads = [[_dev(x.reshape(-1)).view(x.shape) for x in _tensors(shapes, 400 + q, "bf16")]
+             for q in range(nd)]
+    p0 = _f32_dev(synth.host_fill(synth.normal_stream(9, (84,), 0.02), 0, L, "f32"))
+    a = [p0.clone(), torch.zeros(L, device=DEV), torch.zeros(L, device=DEV),
+         torch.empty(L, dtype=torch.bfloat16, device=DEV)]
+    b = [p0.clone(), torch.zeros(L, device=DEV), torch.zeros(L, device=DEV),
+         torch.empty(L, dtype=torch.bfloat16, device=DEV)]
+    step = ss.Fsdp2Step(grads)
+    assert step.local == L
+    for t in (1, 2, 3):
+        ss.fsdp2_rs_avg_adamw_cast(grads, 2, *a, HPC, t)
+        step(2, *b, HPC, t)
+    torch.cuda.synchronize()
+    for x, y in zip(a, b):
+        assert torch.equal(x.view(torch.uint8), y.view(torch.uint8))
+    with pytest.raises(ValueError):
+        step(0, b[0][:-1], b[1], b[2], b[3], HPC, 1)
+    with pytest.raises(ValueError):
+        step(0, b[0], b[1], b[2], b[0], HPC, 1)        # fp32 where bf16 goes
+    with pytest.raises(ValueError):
+        ss.Fsdp2Step([grads[0], grads[1][:-1]])         # ranks disagree on the parameters
