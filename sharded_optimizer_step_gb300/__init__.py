@@ -545,9 +545,9 @@ class Fsdp2Step:
     once: the ranks' per-parameter gradient tensors (``rank_grads[q][t]``)
     are validated and their device pointers, shapes and the local length
     taken when the object is made, and it keeps the tensors alive.  Each
-    call then checks only the rank's four local buffers before the C call
-    (which checks every pointer again), so a step of many small parameters
-    costs little host time."""
+    call then checks only that no gradient's storage has moved and the
+    rank's four local buffers before the C call (which checks every pointer
+    again), so a step of many small parameters costs little host time."""
 
     def __init__(self, rank_grads):
         import torch
@@ -560,11 +560,12 @@ class Fsdp2Step:
             _need_cuda(*gs)
             if [tuple(g.shape) for g in gs] != self.shapes or any(g.dtype != dt for g in gs):
                 raise ValueError("every rank's gradients must have the same shapes and dtype")
-        self._keep = [list(gs) for gs in rank_grads]
+        self._keep = [g for gs in rank_grads for g in gs]
+        self._addrs = [g.data_ptr() for g in self._keep]
         self.local = fsdp2_layout(self.shapes, self.nd).local
         d0, row = _dims(self.shapes)
         self._d0, self._row = _capi.i64_array(d0), _capi.i64_array(row)
-        self._ptrs = _capi.ptr_array([g.data_ptr() for gs in rank_grads for g in gs])
+        self._ptrs = _capi.ptr_array(self._addrs)
         self._code = _dtype_code(rank_grads[0][0]) if self.shapes else _capi.DTYPE_BF16
 
     def __call__(self, rank: int, master, m, v, out_bf16, hp: AdamW, step: int, stream=None):
@@ -576,6 +577,10 @@ class Fsdp2Step:
         if (not out_bf16.is_cuda or out_bf16.dtype != torch.bfloat16 or out_bf16.numel() != L
                 or not out_bf16.is_contiguous()):
             raise ValueError(f"out must be contiguous CUDA bf16 with {L} elements")
+        # a gradient whose storage moved (an in-place resize) would leave a
+        # stale pointer in the table
+        if any(g.data_ptr() != a for g, a in zip(self._keep, self._addrs)):
+            raise ValueError("a gradient buffer moved since this Fsdp2Step was made")
         hpc = hp.at_step(step)
         _capi.check("fsdp2_rs_avg_adamw_cast", _capi.lib().fsdp2_rs_avg_adamw_cast(
             self._ptrs, self._code, self._d0, self._row, len(self.shapes), self.nd, int(rank),

@@ -293,3 +293,9 @@ def test_fsdp2_step_object_gives_the_same_bits_and_checks_its_buffers():
         step(0, b[0], b[1], b[2], b[0], HPC, 1)        # fp32 where bf16 goes
     with pytest.raises(ValueError):
         ss.Fsdp2Step([grads[0], grads[1][:-1]])         # ranks disagree on the parameters
+    # a gradient's storage moved by an in-place resize: refused, not read
+    g = torch.zeros(shapes[0], dtype=torch.bfloat16, device=DEV)
+    moved = ss.Fsdp2Step([[g] + grads[q][1:] for q in range(nd)])
+    g.resize_(4096, 4096)
+    with pytest.raises(ValueError):
+        moved(0, *b, HPC, 1)
