@@ -160,6 +160,28 @@ __global__ void __launch_bounds__(kSegThreads, kSegMinBlocks)
     }
 }
 
+// AdamW on a zero gradient over n elements: padding rows the segment kernel
+// does not take (a start that is not 16-byte aligned).  Every rank's
+// reduce-scatter contribution there is +0, so their rank-order sum and its
+// mean are +0 whatever N_d is: the fused step's update of those positions,
+// without reading the zeros.
+__global__ void __launch_bounds__(kSegThreads)
+    adamw_zero_grad(int64_t n, float* __restrict__ P, float* __restrict__ M,
+                    float* __restrict__ V, uint16_t* __restrict__ out, AdamScalars c) {
+    pdl_enter();
+    c = resolve_adam(c);
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kSegThreads;
+    for (int64_t j = static_cast<int64_t>(blockIdx.x) * kSegThreads + threadIdx.x; j < n;
+         j += stride) {
+        float p = P[j], m = M[j], v = V[j];
+        adamw_elem(0.0f, p, m, v, c);
+        P[j] = p;
+        M[j] = m;
+        V[j] = v;
+        out[j] = f32_to_bf16(p);
+    }
+}
+
 template <int ND, int GT>
 cudaError_t go_segs(const SegTable& st, int nd, float* P, float* M, float* V, uint16_t* out,
                     const AdamScalars& c, const MeanOp& mo, cudaStream_t s) {
@@ -198,6 +220,17 @@ cudaError_t dispatch_segs(const SegTable& st, int nd, float* P, float* M, float*
 int64_t seg_blocks(int64_t n) {
     const int64_t slots = (n + 3) / 4;     // 4-element vectors, the last one partial
     return (slots + kSegThreads - 1) / kSegThreads;
+}
+
+cudaError_t launch_adamw_zero_grad(int64_t n, float* master, float* m, float* v, uint16_t* out,
+                                   const AdamScalars& c, cudaStream_t stream) {
+    // one pass (the loop strides only past 2^31 - 1 blocks)
+    int64_t blocks = (n + kSegThreads - 1) / kSegThreads;
+    if (blocks > (int64_t{1} << 31) - 1) blocks = (int64_t{1} << 31) - 1;
+    const cudaError_t e = launch_after(adamw_zero_grad, dim3(static_cast<unsigned>(blocks)),
+                                       dim3(kSegThreads), 0, stream, n, master, m, v, out, c);
+    note_launch();
+    return e;
 }
 
 cudaError_t launch_rs_adamw_cast_segs(const SegTable& st, int nd, int grad_type, float* master,

@@ -261,27 +261,6 @@ __global__ void __launch_bounds__(kThreads)
         step_scalar<GT>(tab, nd, j, P, M, V, out, c, mo);
 }
 
-// AdamW on a zero gradient: the padding rows of an FSDP2 local buffer.  Every
-// rank's reduce-scatter contribution there is +0, so their rank-order sum
-// and its mean are +0 whatever N_d is, and this is the fused step's update
-// of those positions, without reading the zeros.
-__global__ void __launch_bounds__(kThreads)
-    adamw_zero_grad(int64_t n, float* __restrict__ P, float* __restrict__ M,
-                    float* __restrict__ V, uint16_t* __restrict__ out, AdamScalars c) {
-    pdl_enter();
-    c = resolve_adam(c);
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
-    for (int64_t j = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; j < n;
-         j += stride) {
-        float p = P[j], m = M[j], v = V[j];
-        adamw_elem(0.0f, p, m, v, c);
-        P[j] = p;
-        M[j] = m;
-        V[j] = v;
-        out[j] = f32_to_bf16(p);
-    }
-}
-
 // ------------------------------------- DDP all-reduce avg + AdamW, fused
 
 // The replicated update of DDP in one pass over bucketed elements: the N_d
@@ -772,15 +751,6 @@ cudaError_t launch_rs_adamw_cast(const PtrTable& tab, int nd, int grad_type, int
         case kGradF16: return vec ? dispatch_vec<kGradF16>(a, stream) : go_scalar<kGradF16>(a, stream);
         default: return vec ? dispatch_vec<kGradBF16>(a, stream) : go_scalar<kGradBF16>(a, stream);
     }
-}
-
-cudaError_t launch_adamw_zero_grad(int64_t n, float* master, float* m, float* v, uint16_t* out,
-                                   const AdamScalars& c, cudaStream_t stream) {
-    const unsigned grid = grid_for(reinterpret_cast<const void*>(adamw_zero_grad), n);
-    const cudaError_t e = launch_after(adamw_zero_grad, dim3(grid), dim3(kThreads), 0, stream, n,
-                                       master, m, v, out, c);
-    note_launch();
-    return e;
 }
 
 cudaError_t launch_allreduce_avg(const PtrTable& tab, int nd, int64_t n, uint16_t* out,

@@ -496,3 +496,13 @@ def test_new_entry_points_reject_bad_arguments_before_launch():
     assert check(3, None, ctypes.c_void_p(A + 8), None) == _capi.ERR_INVALID
     assert check(3, ctypes.c_void_p(A + 4), ctypes.c_void_p(A + 8), None) == _capi.ERR_INVALID
     assert b"misaligned" in L.shardstep_last_error()
+
+
+def test_every_profiled_kernel_matches_its_counters():
+    """bench.py reports roofline.traffic only while the source of the kernel
+    a profile's DRAM counters were taken on is unchanged (a hash of its code
+    without comments); every line with a profile must still have its
+    counters, so a kernel change without a new capture is caught here."""
+    import bench
+    stale = [w for w in bench.PROFILES if bench.profiled_traffic(w) is None]
+    assert not stale, f"profiles whose kernel source changed since the capture: {stale}"
