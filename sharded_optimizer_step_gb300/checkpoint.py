@@ -57,9 +57,17 @@ def _states(opt):
     return (opt.master, opt.m, opt.v)
 
 
+def _step_count(opt) -> int:
+    """The optimizer's step count: the device step state's when it has one
+    (``step_on_device`` advances that one only; reading it synchronises),
+    else the host count."""
+    state = getattr(opt, "state", None)
+    return state.step() if state is not None else opt.t
+
+
 def save_rank(directory: str, opt) -> str:
-    """Write ``opt``'s shard state to ``directory`` (rank = opt.rank of opt.F
-    shards).  Synchronises with the device."""
+    """Write ``opt``'s shard state and step count to ``directory`` (rank =
+    opt.rank of opt.F shards).  Synchronises with the device."""
     import torch
     os.makedirs(directory, exist_ok=True)
     host = _staging(opt)
@@ -75,7 +83,8 @@ def save_rank(directory: str, opt) -> str:
             k += 1
     path = rank_file(directory, opt.rank)
     _capi.check("shardstep_ckpt_save_rank", _capi.lib().shardstep_ckpt_save_rank(
-        path.encode(), opt.F, opt.rank, opt.t, _capi.i64_array([l.total for l in opt.layouts]),
+        path.encode(), opt.F, opt.rank, _step_count(opt),
+        _capi.i64_array([l.total for l in opt.layouts]),
         n_units, secs, k))
     return path
 
@@ -118,8 +127,9 @@ def plan(total: int, old_nd: int, new_nd: int, new_rank: int):
 
 
 def load_rank(directory: str, opt) -> None:
-    """Fill ``opt``'s master / m / v (and step count) from a checkpoint saved
-    under any rank count; padding positions of the new layout are zero."""
+    """Fill ``opt``'s master / m / v and step count (the host count, and the
+    device step state's when it has one) from a checkpoint saved under any
+    rank count; padding positions of the new layout are zero."""
     import torch
     old_nd, step, totals = info(directory)
     mine = [l.total for l in opt.layouts]
@@ -140,8 +150,11 @@ def load_rank(directory: str, opt) -> None:
                     path, u, kind, off * 4, count * 4, ctypes.c_void_p(dst)))
     for buf, h in zip(_states(opt), host):
         buf.copy_(h, non_blocking=True)
-    torch.cuda.synchronize(opt.master.device)
     opt.t = step
+    state = getattr(opt, "state", None)
+    if state is not None:                 # the device step state continues from here too
+        state.init(step)
+    torch.cuda.synchronize(opt.master.device)
 
 
 def load(directory: str, opts, threads: int = 8) -> None:

@@ -56,6 +56,7 @@ class RankShardOptimizer:
         self.params = torch.zeros(pos, dtype=torch.bfloat16, device=dev)
         self.grad_in = [torch.zeros(pos, dtype=grad_dtype, device=dev) for _ in range(nd)]
         self.t = 0
+        self.state = None                 # the device step state, once made
 
     def unit_slice(self, buf, u):
         """This rank's piece of unit u inside a rank-shard buffer."""

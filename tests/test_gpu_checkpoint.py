@@ -120,3 +120,42 @@ def test_reload_through_used_staging_restores_padding(tmp_path):
                 assert got.tobytes() == want.tobytes(), (o.rank, u, name)
     for o in new:
         ck.release_staging(o)
+
+
+def test_device_step_state_is_saved_and_restored(tmp_path):
+    """Steps taken on the device step state (the host count does not move)
+    are saved with the device count; a load into optimizers that also keep
+    their count on the device restores it there, and the next replayed-style
+    step continues with the bits of uninterrupted training."""
+    w = W.gpt2_small_nd7()
+    w.units = w.units[:2]
+    nd = 4
+    a = _opts(w, nd)
+    for o in a:
+        gpu_fill_rank(o, o.master, w.master_stream)
+        for q in range(nd):
+            gpu_fill_rank(o, o.grad_in[q], lambda u, k, q=q: w.grad_stream(1, q, 0, u, k))
+        o.device_step_state()
+    for _ in range(3):
+        for o in a:
+            o.step_on_device()
+    torch.cuda.synchronize()
+    assert all(o.t == 0 and o.state.step() == 3 for o in a)
+    ck.save(str(tmp_path / "ck"), a)
+    assert ck.info(str(tmp_path / "ck"))[1] == 3
+    b = _opts(w, nd)
+    for o in b:
+        o.device_step_state()              # at step 0, until the load
+        for q in range(nd):
+            o.grad_in[q].copy_(a[o.rank].grad_in[q])
+    ck.load(str(tmp_path / "ck"), b)
+    assert all(o.t == 3 and o.state.step() == 3 for o in b)
+    for o, p in zip(a, b):
+        o.step_on_device()
+        p.step_on_device()
+    torch.cuda.synchronize()
+    for o, p in zip(a, b):
+        for name in ("master", "m", "v", "params"):
+            x, y = getattr(o, name), getattr(p, name)
+            assert torch.equal(x.view(torch.uint8), y.view(torch.uint8)), name
+        assert o.state.step() == p.state.step() == 4
