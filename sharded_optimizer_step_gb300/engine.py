@@ -58,6 +58,17 @@ class RankShardOptimizer:
         self.t = 0
         self.state = None                 # the device step state, once made
 
+    def _next_host_step(self):
+        """Advance the count for a host-scalar step.  When the count is also
+        kept on the device (``device_step_state``), the device count is the
+        current one (reading it synchronises) and the device state moves to
+        the new count too, so the two forms of step can be mixed."""
+        if self.state is not None:
+            self.t = self.state.step()
+        self.t += 1
+        if self.state is not None:
+            self.state.init(self.t)
+
     def unit_slice(self, buf, u):
         """This rank's piece of unit u inside a rank-shard buffer."""
         return buf[self.starts[u]:self.starts[u] + self.layouts[u].shard]
@@ -79,7 +90,7 @@ class RankShardOptimizer:
     def step(self, stream=None):
         """Reduce-scatter average + AdamW + bf16 cast over the whole rank shard
         (one launch)."""
-        self.t += 1
+        self._next_host_step()
         self._update(self.grad_in, self.master, self.m, self.v, self.params, stream)
 
     def _update(self, grads, master, m, v, params, stream):
@@ -95,7 +106,7 @@ class RankShardOptimizer:
         gradient of the last micro-batch (laid out like ``grad_in[q]``):
         the last accumulation (``scale`` = 1/M) runs inside the fused launch
         and ``grad_in`` is left as it was."""
-        self.t += 1
+        self._next_host_step()
         fsdp_accumulate_rs_avg_adamw_cast(self.grad_in, last, scale, self.master, self.m, self.v,
                                           self.params, self.hp, self.t, shard_group=self.F,
                                           stream=stream)
@@ -103,7 +114,7 @@ class RankShardOptimizer:
     def begin_step(self):
         """Advance the step count for an update issued piece by piece with
         ``update_range`` (e.g. overlapped with the arrival of the gradients)."""
-        self.t += 1
+        self._next_host_step()
 
     def update_range(self, a: int, b: int, stream=None):
         """The fused update of shard positions [a, b) at the current step count."""

@@ -330,3 +330,32 @@ def test_state_at_a_late_step():
     torch.cuda.synchronize()
     a.assert_equal(b, "late step")
     assert st.step() == 10 ** 6 + 1
+
+
+def test_engine_mixes_host_and_device_steps():
+    """RankShardOptimizer with its count on the device: device steps, then a
+    host-scalar step (which takes the device count and moves it on), then a
+    device step again give the bits of four host-scalar steps, and both
+    counts agree at 4."""
+    from sharded_optimizer_step_gb300.engine import RankShardOptimizer
+    units = [[(300, 7), (5,)], [(1000,)]]
+    nd = 3
+    a = RankShardOptimizer(units, nd, 1, HP, device=DEV)
+    b = RankShardOptimizer(units, nd, 1, HP, device=DEV)
+    for o in (a, b):
+        torch.manual_seed(3)
+        o.master.copy_(torch.randn(o.shard_total, device=DEV) * 0.02)
+        for q in range(nd):
+            o.grad_in[q].copy_((torch.randn(o.shard_total, device=DEV) * 1e-3).to(torch.bfloat16))
+    for _ in range(4):
+        a.step()
+    b.device_step_state()
+    b.step_on_device()
+    b.step_on_device()
+    b.step()
+    b.step_on_device()
+    torch.cuda.synchronize()
+    assert a.t == 4 and b.state.step() == 4 and b.t == 3
+    for name in ("master", "m", "v", "params"):
+        x, y = getattr(a, name), getattr(b, name)
+        assert torch.equal(x.view(torch.uint8), y.view(torch.uint8)), name
