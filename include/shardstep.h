@@ -598,8 +598,12 @@ int64_t ddp_ready_bytes(int32_t n_params, int32_t n_buckets, int32_t nd);
 int ddp_ready_init(void* table, int64_t table_bytes, const int32_t* bucket_of_param,
                    int32_t n_params, int32_t n_buckets, int32_t nd);
 
-/* Rank `rank` has the gradient of parameter `param`.  *bucket_done (may be
- * NULL) receives the bucket this mark completed on all ranks, else -1.
+/* Rank `rank` has the gradient of parameter `param` in device memory: mark
+ * only after the writes that produced it have completed (the bucket's
+ * all-reduce may be launched on another stream as soon as this mark
+ * completes the bucket; the table orders host threads, not device work).
+ * *bucket_done (may be NULL) receives the bucket this mark completed on all
+ * ranks, else -1.
  * Errors: INVALID (uninitialised table, out of range, marked twice). */
 int ddp_ready_mark(void* table, int32_t rank, int32_t param, int32_t* bucket_done);
 

@@ -708,8 +708,11 @@ class BucketReadiness:
                                                        n_buckets, nd))
 
     def mark(self, rank: int, param: int):
-        """Rank `rank` has param's gradient; returns the bucket this completed
-        on every rank, or None."""
+        """Rank `rank` has param's gradient in device memory; returns the
+        bucket this completed on every rank, or None.  Mark only once the
+        gradient's writes have completed (e.g. after synchronising the
+        stream that produced it): the bucket's all-reduce may be launched on
+        another stream as soon as the mark completes the bucket."""
         done = _capi.c_i32(-1)
         _capi.check("ddp_ready_mark", _capi.lib().ddp_ready_mark(self._ptr, rank, param,
                                                                  ctypes.byref(done)))
