@@ -182,9 +182,22 @@ def _f32_dev(h):
     return torch.from_numpy(np.ascontiguousarray(h, dtype=np.float32)).to(DEV)
 
 
+def _dev_grad(h, gdt):
+    if gdt == "f16":
+        return torch.from_numpy(np.ascontiguousarray(h).view(np.int16)).to(DEV).view(
+            torch.float16)
+    return _dev(h)
+
+
+def _oracle_contribs(cc, gdt):
+    """fp16 contributions widened to fp32 (exact) for the oracle's shard step,
+    which reads bf16 bits or fp32 values."""
+    return [oracle.f16_to_f32(c) for c in cc] if gdt == "f16" else cc
+
+
 @pytest.mark.parametrize("shapes", SHAPE_SETS, ids=lambda s: f"{len(s)}params")
 @pytest.mark.parametrize("nd", [1, 2, 3, 4, 8, 12, 16])
-@pytest.mark.parametrize("gdt", ["bf16", "f32"])
+@pytest.mark.parametrize("gdt", ["bf16", "f32", "f16"])
 def test_fsdp2_step_without_chunk_cat_matches_oracle(shapes, nd, gdt, path):
     """fsdp2_rs_avg_adamw_cast on every rank, two steps, against the oracle's
     chunk-cat + shard step.  The local state starts non-zero everywhere,
@@ -201,8 +214,8 @@ def test_fsdp2_step_without_chunk_cat_matches_oracle(shapes, nd, gdt, path):
                           out=torch.empty(L, dtype=torch.bfloat16, device=DEV)))
     for t in (1, 2):
         grads_h = [_tensors(shapes, 300 * t + q, gdt) for q in range(nd)]
-        grads = [[_dev(x.reshape(-1)).view(x.shape) for x in g] for g in grads_h]
-        cc_h = [oracle.chunk_cat(g, lay) for g in grads_h]
+        grads = [[_dev_grad(x.reshape(-1), gdt).view(x.shape) for x in g] for g in grads_h]
+        cc_h = _oracle_contribs([oracle.chunk_cat(g, lay) for g in grads_h], gdt)
         for r, st in enumerate(state):
             ss.fsdp2_rs_avg_adamw_cast(grads, r, st["dp"], st["dm"], st["dv"], st["out"], HPC, t)
             st["p"], st["m"], st["v"], st["ob"] = oracle.fsdp_shard_step(
