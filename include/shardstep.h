@@ -498,6 +498,17 @@ int fsdp2_rs_avg_adamw_cast(const void* const* grads, int32_t grad_dtype, const 
                             float* master, float* m, float* v, uint16_t* out_bf16,
                             const shardstep_adamw_t* hp, void* stream);
 
+/* fsdp2_state_rs_avg_adamw_cast -- device; fsdp2_rs_avg_adamw_cast with the
+ * AdamW scalars read on the device from `state` (at a step >= 1; see
+ * shardstep_adamw_state_t), so that the FSDP2 step of every rank can be
+ * captured in a CUDA graph with shardstep_adamw_state_advance before it.
+ * Same bits as the host-scalar call at the state's step. */
+int fsdp2_state_rs_avg_adamw_cast(const void* const* grads, int32_t grad_dtype,
+                                  const int64_t* dim0, const int64_t* row, int32_t n, int32_t nd,
+                                  int32_t rank, float* master, float* m, float* v,
+                                  uint16_t* out_bf16, const shardstep_adamw_state_t* state,
+                                  void* stream);
+
 /* ---------------------------------------------------- DDP buckets */
 
 /* ddp_bucket_plan -- host only.

@@ -568,7 +568,7 @@ class Fsdp2Step:
         self._ptrs = _capi.ptr_array(self._addrs)
         self._code = _dtype_code(rank_grads[0][0]) if self.shapes else _capi.DTYPE_BF16
 
-    def __call__(self, rank: int, master, m, v, out_bf16, hp: AdamW, step: int, stream=None):
+    def _check(self, master, m, v, out_bf16):
         import torch
         L = self.local
         for t in (master, m, v):
@@ -581,12 +581,28 @@ class Fsdp2Step:
         # stale pointer in the table
         if any(g.data_ptr() != a for g, a in zip(self._keep, self._addrs)):
             raise ValueError("a gradient buffer moved since this Fsdp2Step was made")
+
+    def __call__(self, rank: int, master, m, v, out_bf16, hp: AdamW, step: int, stream=None):
+        """Rank ``rank``'s step at step count ``step`` (host scalars)."""
+        self._check(master, m, v, out_bf16)
         hpc = hp.at_step(step)
         _capi.check("fsdp2_rs_avg_adamw_cast", _capi.lib().fsdp2_rs_avg_adamw_cast(
             self._ptrs, self._code, self._d0, self._row, len(self.shapes), self.nd, int(rank),
             ctypes.c_void_p(master.data_ptr()), ctypes.c_void_p(m.data_ptr()),
             ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(out_bf16.data_ptr()),
             ctypes.byref(hpc), _stream(stream, master.device)))
+
+    def step_state(self, rank: int, master, m, v, out_bf16, state: AdamWState, stream=None):
+        """Rank ``rank``'s step with the AdamW scalars read on the device from
+        ``state`` (an ``AdamWState`` at a step >= 1): with ``state.advance()``
+        before the ranks' calls, a step a CUDA graph can capture."""
+        self._check(master, m, v, out_bf16)
+        _need_cuda(state.buf)
+        _capi.check("fsdp2_state_rs_avg_adamw_cast", _capi.lib().fsdp2_state_rs_avg_adamw_cast(
+            self._ptrs, self._code, self._d0, self._row, len(self.shapes), self.nd, int(rank),
+            ctypes.c_void_p(master.data_ptr()), ctypes.c_void_p(m.data_ptr()),
+            ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(out_bf16.data_ptr()),
+            ctypes.c_void_p(state.buf.data_ptr()), _stream(stream, master.device)))
 
 
 def fsdp2_all_gather_copy_out(local_bufs, params, stream=None):

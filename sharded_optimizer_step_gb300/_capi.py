@@ -81,6 +81,8 @@ SIGNATURES = {
     "fsdp2_local_views": (c_i32, [P_i64, P_i64, c_i32, c_i32, c_i32, c_vp, c_i32, P_vp, P_i64]),
     "fsdp2_rs_avg_adamw_cast": (c_i32, [P_vp, c_i32, P_i64, P_i64, c_i32, c_i32, c_i32, c_vp,
                                         c_vp, c_vp, c_vp, ctypes.POINTER(AdamWHP), c_vp]),
+    "fsdp2_state_rs_avg_adamw_cast": (c_i32, [P_vp, c_i32, P_i64, P_i64, c_i32, c_i32, c_i32,
+                                              c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
     "fsdp2_chunk_cat": (c_i32, [P_vp, P_i64, P_i64, c_i32, c_i32, c_i32, c_vp, c_vp]),
     "fsdp2_all_gather_copy_out": (c_i32, [P_vp, P_i64, P_i64, c_i32, c_i32, c_i32, P_vp, c_vp]),
     "ddp_bucket_plan": (c_i32, [P_i64, c_i32, c_i32, c_i64, P_i64, P_i32, P_i64, P_i32]),

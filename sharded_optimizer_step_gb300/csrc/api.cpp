@@ -1163,10 +1163,14 @@ int fsdp2_all_gather_copy_out(const void* const* local_bufs, const int64_t* dim0
     return ok();
 }
 
-int fsdp2_rs_avg_adamw_cast(const void* const* grads, int32_t grad_dtype, const int64_t* dim0,
-                            const int64_t* row, int32_t n, int32_t nd, int32_t rank,
-                            float* master, float* m, float* v, uint16_t* out_bf16,
-                            const shardstep_adamw_t* hp, void* stream) {
+namespace {
+
+// The FSDP2 step of one rank; the AdamW scalars from `hp` on the host or
+// from a device-resident step `state`.
+int fsdp2_step(const void* const* grads, int32_t grad_dtype, const int64_t* dim0,
+               const int64_t* row, int32_t n, int32_t nd, int32_t rank, float* master, float* m,
+               float* v, uint16_t* out_bf16, const shardstep_adamw_t* hp,
+               const shardstep_adamw_state_t* state, void* stream) {
     const int es = elem_size_of(grad_dtype);
     if (es == 0) return fail(SHARDSTEP_ERR_INVALID, "unknown grad dtype %d", grad_dtype);
     if (nd > SHARDSTEP_MAX_ND)
@@ -1176,7 +1180,7 @@ int fsdp2_rs_avg_adamw_cast(const void* const* grads, int32_t grad_dtype, const 
     if (rc != SHARDSTEP_OK) return rc;
     if (rank < 0 || rank >= nd) return fail(SHARDSTEP_ERR_INVALID, "rank %d not in [0, %d)", rank, nd);
     AdamScalars c{};
-    if (int rc2 = adam_source(hp, nullptr, &c); rc2 != SHARDSTEP_OK) return rc2;
+    if (int rc2 = adam_source(hp, state, &c); rc2 != SHARDSTEP_OK) return rc2;
     const int64_t L = plan.local;
     if (L == 0) return ok();
     Span outs[4];
@@ -1249,7 +1253,7 @@ int fsdp2_rs_avg_adamw_cast(const void* const* grads, int32_t grad_dtype, const 
                 count_comm(reduce_comm_bytes(nd, nd, have, es));
             } else {
                 rc = fused_step(slices.data(), grad_dtype, nd, nd, have, master + off, m + off,
-                                v + off, out_bf16 + off, hp, stream);
+                                v + off, out_bf16 + off, hp, stream, nullptr, nullptr, state);
                 if (rc != SHARDSTEP_OK) return rc;
                 fused_launched = true;
             }
@@ -1275,6 +1279,27 @@ int fsdp2_rs_avg_adamw_cast(const void* const* grads, int32_t grad_dtype, const 
     else if (pad_launched && !fused_launched)
         note_kernel("adamw_zero_grad");
     return ok();
+}
+
+}  // namespace
+
+int fsdp2_rs_avg_adamw_cast(const void* const* grads, int32_t grad_dtype, const int64_t* dim0,
+                            const int64_t* row, int32_t n, int32_t nd, int32_t rank,
+                            float* master, float* m, float* v, uint16_t* out_bf16,
+                            const shardstep_adamw_t* hp, void* stream) {
+    if (hp == nullptr) return fail(SHARDSTEP_ERR_INVALID, "hp is NULL");
+    return fsdp2_step(grads, grad_dtype, dim0, row, n, nd, rank, master, m, v, out_bf16, hp,
+                      nullptr, stream);
+}
+
+int fsdp2_state_rs_avg_adamw_cast(const void* const* grads, int32_t grad_dtype,
+                                  const int64_t* dim0, const int64_t* row, int32_t n, int32_t nd,
+                                  int32_t rank, float* master, float* m, float* v,
+                                  uint16_t* out_bf16, const shardstep_adamw_state_t* state,
+                                  void* stream) {
+    if (state == nullptr) return fail(SHARDSTEP_ERR_INVALID, "state is NULL");
+    return fsdp2_step(grads, grad_dtype, dim0, row, n, nd, rank, master, m, v, out_bf16, nullptr,
+                      state, stream);
 }
 
 int ddp_bucket_plan(const int64_t* numels, int32_t n, int32_t elem_size, int64_t cap_bytes,

@@ -312,3 +312,49 @@ def test_fsdp2_step_object_gives_the_same_bits_and_checks_its_buffers():
     g.resize_(4096, 4096)
     with pytest.raises(ValueError):
         moved(0, *b, HPC, 1)
+
+
+@pytest.mark.parametrize("nd", [3, 8])
+def test_fsdp2_step_replayed_from_a_cuda_graph(nd):
+    """The whole FSDP2 step -- the step count advanced on the device, every
+    rank's step read straight from the gradients, the copy-out -- captured
+    once and replayed three times gives the bits of three host-scalar steps
+    (steps 1, 2, 3), padding rows included."""
+    shapes = SHAPE_SETS[4]                     # uneven dim 0: padding rows
+    L = ss.fsdp2_layout(shapes, nd).local
+    grads = [[_dev(x.reshape(-1)).view(x.shape) for x in _tensors(shapes, 500 + q, "bf16")]
+             for q in range(nd)]
+    step = ss.Fsdp2Step(grads)
+
+    def fresh():
+        bufs = []
+        for r in range(nd):
+            p = _f32_dev(synth.host_fill(synth.normal_stream(9, (83, r), 0.02), 0, L, "f32"))
+            bufs.append([p, torch.zeros(L, device=DEV), torch.zeros(L, device=DEV),
+                         torch.empty(L, dtype=torch.bfloat16, device=DEV)])
+        return bufs
+
+    a, b = fresh(), fresh()
+    pa = [torch.empty(s, dtype=torch.bfloat16, device=DEV) for s in shapes]
+    pb = [torch.empty(s, dtype=torch.bfloat16, device=DEV) for s in shapes]
+    for t in (1, 2, 3):
+        for r in range(nd):
+            step(r, *a[r], HPC, t)
+        ss.fsdp2_all_gather_copy_out([x[3] for x in a], pa)
+    state = ss.AdamWState(HPC, 0, device=DEV)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        state.advance()
+        for r in range(nd):
+            step.step_state(r, *b[r], state)
+        ss.fsdp2_all_gather_copy_out([x[3] for x in b], pb)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert state.step() == 3
+    for r in range(nd):
+        for x, y in zip(a[r], b[r]):
+            assert torch.equal(x.view(torch.uint8), y.view(torch.uint8)), r
+    for x, y in zip(pa, pb):
+        assert torch.equal(x.view(torch.uint8), y.view(torch.uint8))
