@@ -59,13 +59,21 @@ PROFILES = {
 
 def parse():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--e2e-steps", type=int, default=5)
-    ap.add_argument("--e2e-chunks", type=int, default=8)
-    ap.add_argument("--e2e-streams", type=int, default=4)
+    ap.add_argument("--gpus", type=int, default=1,
+                    help="GPUs of this node, one process each under torchrun (one replica "
+                         "of the line per GPU)")
+    ap.add_argument("--steps", type=int, default=200, help="timed steps")
+    ap.add_argument("--warmup", type=int, default=5, help="untimed steps before the timing")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours",
+                    help="ours: the library on the GPU; reference: the CPU oracle on a "
+                         "bounded sample of the same workload")
+    ap.add_argument("--e2e-steps", type=int, default=5,
+                    help="steps of the end-to-end leg (host buffers in and out)")
+    ap.add_argument("--e2e-chunks", type=int, default=8,
+                    help="default line's end-to-end leg: chunks of the shard whose copies "
+                         "overlap the previous chunk's update")
+    ap.add_argument("--e2e-streams", type=int, default=4,
+                    help="default line's end-to-end leg: copy streams")
     ap.add_argument("--workload", choices=sorted(WORKLOADS) + [FSDP2_WORKLOAD, CKPT_WORKLOAD,
                                                              ACCUM_WORKLOAD, DDP_WORKLOAD,
                                                              RAGGED_WORKLOAD, UNIT9M_WORKLOAD,
@@ -92,9 +100,10 @@ def parse():
                     help="streaming kernels: TMA-staged where they measured faster (auto), "
                          "register-staged only, or TMA-staged wherever the arguments allow")
     ap.add_argument("--graph", action="store_true",
-                    help="default / hybrid / accumulation lines: the step count and AdamW "
-                         "scalars on the device, the accumulate launches, the fused update "
-                         "and the all-gather replayed from CUDA graphs captured once")
+                    help="default / hybrid / accumulation lines and the two whole-job "
+                         "lines: the step count and AdamW scalars on the device, the "
+                         "accumulate launches, the fused update and the all-gather replayed "
+                         "from CUDA graphs captured once")
     ap.add_argument("--no-dependent-launch", action="store_true",
                     help="launch every kernel as an ordinary launch (by default each call's "
                          "first kernel is a programmatic dependent of the kernel before it, "
@@ -104,8 +113,9 @@ def parse():
                     help="accumulation line: accumulate every micro-batch with its own launch "
                          "and run the fused step on the accumulators (the last micro-batch "
                          "is otherwise accumulated inside the fused step)")
-    ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg")
+    ap.add_argument("--no-cpu", action="store_true",
+                    help="skip the CPU oracle baseline beside the line")
     return ap.parse_args()
 
 
