@@ -358,3 +358,32 @@ def test_fsdp2_step_replayed_from_a_cuda_graph(nd):
             assert torch.equal(x.view(torch.uint8), y.view(torch.uint8)), r
     for x, y in zip(pa, pb):
         assert torch.equal(x.view(torch.uint8), y.view(torch.uint8))
+
+
+@pytest.mark.parametrize("nd", [33, 64])
+@pytest.mark.parametrize("gdt", ["bf16", "f32"])
+def test_fsdp2_step_without_chunk_cat_at_large_nd(nd, gdt):
+    """Past the compiled counts (the kernel's loop over batches of slices) and
+    with the 128-pointer table holding only 3 or 2 segments (a rank's
+    segments split over several launches), against the oracle."""
+    shapes = SHAPE_SETS[3]                     # 12 parameters: 24 segments at most
+    lay = oracle.fsdp2_layout(shapes, nd)
+    L = lay.local
+    grads_h = [_tensors(shapes, 600 + q, gdt) for q in range(nd)]
+    grads = [[_dev(x.reshape(-1)).view(x.shape) for x in g] for g in grads_h]
+    cc_h = [oracle.chunk_cat(g, lay) for g in grads_h]
+    step = ss.Fsdp2Step(grads)
+    for r in (0, 1, nd // 2, nd - 1):
+        p = synth.host_fill(synth.normal_stream(9, (82, r), 0.02), 0, L, "f32")
+        dp, dm, dv = _f32_dev(p), torch.zeros(L, device=DEV), torch.zeros(L, device=DEV)
+        out = torch.empty(L, dtype=torch.bfloat16, device=DEV)
+        before = ss.launch_count()
+        step(r, dp, dm, dv, out, HPC, 1)
+        torch.cuda.synchronize()
+        assert ss.launch_count() - before >= 2      # the table filled at least once
+        z = np.zeros(L, np.float32)
+        p1, m1, v1, o1 = oracle.fsdp_shard_step(cc_h, r, L, p, z, z, HP, 1)
+        assert_bits(_host(dp), p1, f"rank {r} master")
+        assert_bits(_host(dm), m1, f"rank {r} m")
+        assert_bits(_host(dv), v1, f"rank {r} v")
+        assert_bits(_host(out), o1, f"rank {r} bf16")
