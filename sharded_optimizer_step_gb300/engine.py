@@ -15,7 +15,8 @@ from __future__ import annotations
 
 import torch
 
-from . import (AdamW, AdamWState, fsdp_accumulate_rs_avg_adamw_cast, fsdp_ag_unpack,
+from . import (AdamW, AdamWState, Fsdp2Step, fsdp2_all_gather_copy_out, fsdp2_layout,
+               fsdp2_local_views, fsdp_accumulate_rs_avg_adamw_cast, fsdp_ag_unpack,
                fsdp_hybrid_rs_avg_adamw_cast, fsdp_layout, fsdp_rs_avg_adamw_cast,
                fsdp_shard_pieces,
                fsdp_state_accumulate_rs_avg_adamw_cast, fsdp_state_rs_avg_adamw_cast,
@@ -156,3 +157,68 @@ class RankShardOptimizer:
         shards[self.rank] = self.unit_slice(self.params, u)
         fsdp_ag_unpack(shards, full, stream=stream)
         return fsdp_views(full, self.unit_shapes[u], self.F)
+
+
+class Fsdp2RankOptimizer:
+    """One rank's optimizer over an FSDP2 group (per-parameter Shard(0)): the
+    rank's padded local buffers -- fp32 master, m, v and the bf16 parameter
+    rows, ``local`` elements laid out as fsdp2_layout gives -- and the step
+    read straight from every rank's per-parameter gradients (``Fsdp2Step``,
+    no chunk-cat copy).  ``rank_grads[q][t]`` is rank q's gradient of
+    parameter t (global shape), kept and checked once.  ``gather`` copies the
+    ranks' bf16 rows out into the full parameters; ``local_views`` are the
+    rank's DTensor.to_local() views of a local buffer."""
+
+    def __init__(self, rank_grads, rank: int, hp: AdamW, device="cuda"):
+        self._step = Fsdp2Step(rank_grads)
+        self.nd, self.rank, self.hp = self._step.nd, rank, hp
+        if not 0 <= rank < self.nd:
+            raise ValueError("rank out of range")
+        self.shapes = self._step.shapes
+        self.layout = fsdp2_layout(self.shapes, self.nd)
+        L = self._step.local
+        dev = torch.device(device)
+        self.master = torch.zeros(L, dtype=torch.float32, device=dev)
+        self.m = torch.zeros(L, dtype=torch.float32, device=dev)
+        self.v = torch.zeros(L, dtype=torch.float32, device=dev)
+        self.params = torch.zeros(L, dtype=torch.bfloat16, device=dev)
+        self.t = 0
+        self.state = None                 # the device step state, once made
+
+    def local_views(self, buf):
+        """The rank's rows of every parameter inside ``buf`` (one of its local
+        buffers), shaped (rows, trailing dims)."""
+        return fsdp2_local_views(buf, self.shapes, self.nd, self.rank)
+
+    def step(self, stream=None):
+        """The rank's step with host scalars (the count advanced on the host;
+        with a device step state, from and into the device count)."""
+        if self.state is not None:
+            self.t = self.state.step()
+        self.t += 1
+        if self.state is not None:
+            self.state.init(self.t)
+        self._step(self.rank, self.master, self.m, self.v, self.params, self.hp, self.t,
+                   stream=stream)
+
+    def device_step_state(self) -> AdamWState:
+        """Moves the step count to the device for ``step_on_device``."""
+        self.state = AdamWState(self.hp, self.t, device=self.master.device)
+        return self.state
+
+    def step_on_device(self, stream=None):
+        """The count advanced and the AdamW scalars derived on the device: the
+        same launches every call, so a CUDA graph can capture it."""
+        self.state.advance(stream=stream)
+        self._step.step_state(self.rank, self.master, self.m, self.v, self.params, self.state,
+                              stream=stream)
+
+    def gather(self, peer_params, params, stream=None):
+        """All-gather: ``peer_params[q]`` is rank q's bf16 local buffer (this
+        rank's own entry is ignored and taken from ``params`` of this
+        optimizer); ``params`` are the full parameter tensors (global shapes)
+        written in place."""
+        bufs = list(peer_params)
+        bufs[self.rank] = self.params
+        fsdp2_all_gather_copy_out(bufs, params, stream=stream)
+        return params

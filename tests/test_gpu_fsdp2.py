@@ -387,3 +387,45 @@ def test_fsdp2_step_without_chunk_cat_at_large_nd(nd, gdt):
         assert_bits(_host(dm), m1, f"rank {r} m")
         assert_bits(_host(dv), v1, f"rank {r} v")
         assert_bits(_host(out), o1, f"rank {r} bf16")
+
+
+def test_fsdp2_rank_optimizer_steps_and_gathers_like_the_oracle():
+    """Fsdp2RankOptimizer: every rank's local state, two host-scalar steps and
+    a third on the device step state, then the gather into the full
+    parameters, against the oracle; the local views have DTensor's local
+    shapes."""
+    from sharded_optimizer_step_gb300.engine import Fsdp2RankOptimizer
+    shapes, nd = SHAPE_SETS[2], 4
+    lay = oracle.fsdp2_layout(shapes, nd)
+    masters = [synth.host_fill(synth.normal_stream(11, (81, t), 0.02), 0, int(np.prod(s)),
+                               "f32").reshape(s) for t, s in enumerate(shapes)]
+    grads_h = [_tensors(shapes, 700 + q, "bf16") for q in range(nd)]
+    grads = [[_dev(x.reshape(-1)).view(x.shape) for x in g] for g in grads_h]
+    opts = [Fsdp2RankOptimizer(grads, r, HPC, device=DEV) for r in range(nd)]
+    want = []
+    for r, o in enumerate(opts):
+        p = oracle.local_buffer(masters, lay, r)
+        o.master.copy_(_f32_dev(p))
+        views = o.local_views(o.master)
+        assert [tuple(x.shape) for x in views] == \
+            [tuple(x.shape) for x in oracle.local_shards(masters, lay, r)]
+        want.append([p, np.zeros(lay.local, np.float32), np.zeros(lay.local, np.float32), None])
+    cc = [oracle.chunk_cat(g, lay) for g in grads_h]
+    for t in (1, 2, 3):
+        for r, o in enumerate(opts):
+            if t < 3:
+                o.step()
+            else:
+                o.device_step_state()
+                o.step_on_device()
+            want[r][0], want[r][1], want[r][2], want[r][3] = oracle.fsdp_shard_step(
+                cc, r, lay.local, want[r][0], want[r][1], want[r][2], HP, t)
+    params = [torch.empty(s, dtype=torch.bfloat16, device=DEV) for s in shapes]
+    opts[0].gather([o.params for o in opts], params)
+    torch.cuda.synchronize()
+    for r, o in enumerate(opts):
+        assert o.state.step() == 3
+        assert_bits(_host(o.master), want[r][0], f"rank {r} master")
+        assert_bits(_host(o.params), want[r][3], f"rank {r} bf16")
+    for got, w in zip(params, oracle.all_gather_copy_out([x[3] for x in want], lay)):
+        assert_bits(_host(got).reshape(-1), w.reshape(-1), "gathered parameter")
