@@ -43,6 +43,8 @@ REGISTER_SOURCES = ["sharded_optimizer_step_gb300/csrc/step.cu",
                     "sharded_optimizer_step_gb300/csrc/common.cuh"]
 COPY_SOURCES = ["sharded_optimizer_step_gb300/csrc/copy.cu",
                 "sharded_optimizer_step_gb300/csrc/common.cuh"]
+FSDP2_SOURCES = ["sharded_optimizer_step_gb300/csrc/fsdp2_step.cu",
+                 "sharded_optimizer_step_gb300/csrc/common.cuh"]
 # per bench line: the ncu summary of its dominant kernel (DRAM bytes per
 # element, recorded with the hash of the sources that kernel is built from)
 PROFILES = {
@@ -54,6 +56,7 @@ PROFILES = {
                               COPY_SOURCES + ["sharded_optimizer_step_gb300/csrc/accum_step.cu"]),
     "ddp_nd8_buckets": ("ddp_buckets_nd8_adamw.md", REGISTER_SOURCES),
     "llama_7b_layer_ragged_nd8": ("pack_gather_llama7b_layer_ragged.md", COPY_SOURCES),
+    "llama_7b_fsdp2_layer_nd8": ("fsdp2_llama7b_layer_group.md", FSDP2_SOURCES),
 }
 
 
@@ -109,6 +112,11 @@ def parse():
                          "first kernel is a programmatic dependent of the kernel before it, "
                          "waiting for it before touching memory, and the later buckets / "
                          "copies of a call overlap the previous one's drain)")
+    ap.add_argument("--fsdp2-chunk-cat", action="store_true",
+                    help="FSDP2 line: time the step through the chunk-cat (the reduce-scatter "
+                         "input a collective needs) and the fused step on its pieces; by "
+                         "default the step is read straight from the gradients (same bits) "
+                         "and the chunk-cat path is timed beside it")
     ap.add_argument("--accum-two-pass", action="store_true",
                     help="accumulation line: accumulate every micro-batch with its own launch "
                          "and run the fused step on the accumulators (the last micro-batch "
@@ -871,10 +879,12 @@ def run_fsdp2(args):
     params = [torch.empty(sh, dtype=torch.bfloat16, device=dev) for sh in shapes]
     stream = torch.cuda.current_stream(dev)
     cc_b, fused_b, ag_b = _fsdp2_bytes(shapes, nd, L)
-    step_b = cc_b + fused_b + ag_b
     t_step = [0]
+    fsdp2_step = ss.Fsdp2Step(grads)       # the gradient buffers checked once
 
-    def one_step(ev=None):
+    def chunk_cat_step(ev=None):
+        """chunk-cat of every rank's gradients, the fused step per rank on the
+        pieces, the copy-out"""
         t_step[0] += 1
         if ev is not None:
             ev[0].record(stream)
@@ -891,6 +901,28 @@ def run_fsdp2(args):
         ss.fsdp2_all_gather_copy_out([out[r * L:(r + 1) * L] for r in range(nd)], params)
         if ev is not None:
             ev[3].record(stream)
+
+    def direct_step(ev=None):
+        """every rank's step read straight from the ranks' gradients (the same
+        bits, no chunk-cat copy), the copy-out"""
+        t_step[0] += 1
+        if ev is not None:
+            ev[0].record(stream)
+            ev[1].record(stream)
+        for r in range(nd):
+            sl = slice(r * L, (r + 1) * L)
+            fsdp2_step(r, master[sl], m[sl], v[sl], out[sl], hp, t_step[0])
+        if ev is not None:
+            ev[2].record(stream)
+        ss.fsdp2_all_gather_copy_out([out[r * L:(r + 1) * L] for r in range(nd)], params)
+        if ev is not None:
+            ev[3].record(stream)
+
+    direct = not args.fsdp2_chunk_cat
+    one_step, other_step = ((direct_step, chunk_cat_step) if direct
+                            else (chunk_cat_step, direct_step))
+    step_b = fused_b + ag_b + (0 if direct else cc_b)
+    other_b = fused_b + ag_b + (cc_b if direct else 0)
 
     clocks = ClockSampler(smi_index(local_rank))
     clocks.start()
@@ -922,30 +954,19 @@ def run_fsdp2(args):
     fused_launch = fused_b / nd
     achieved = fused_launch / (avg[1] / nd / 1e3) / 1e9
     value = allreduce_sum(world, step_b * args.steps) / (total_ms / 1e3) / 1e9
-    # the same step without the chunk-cat copy: every rank's update read
-    # straight from the ranks' per-parameter gradients (same bits)
-    direct_b = fused_b + ag_b
-    fsdp2_step = ss.Fsdp2Step(grads)       # the gradient buffers checked once
-
-    def direct_step():
-        t_step[0] += 1
-        for r in range(nd):
-            sl = slice(r * L, (r + 1) * L)
-            fsdp2_step(r, master[sl], m[sl], v[sl], out[sl], hp, t_step[0])
-        ss.fsdp2_all_gather_copy_out([out[r * L:(r + 1) * L] for r in range(nd)], params)
-
+    # the other composition of the same step, timed beside it (same bits)
     for _ in range(3):
-        direct_step()
+        other_step()
     da = torch.cuda.Event(enable_timing=True)
     db = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     da.record(stream)
     for _ in range(args.steps):
-        direct_step()
+        other_step()
     db.record(stream)
     torch.cuda.synchronize()
-    direct_ms = allreduce_max(world, da.elapsed_time(db) / args.steps)
-    direct_kernel = ss.last_kernel()
+    other_ms = allreduce_max(world, da.elapsed_time(db) / args.steps)
+    other_kernel = ss.last_kernel()
     e2e = None
     if not args.no_e2e:
         e2e = _e2e_plain(torch, stream, [g for gs in grads for g in gs], params,
@@ -954,12 +975,30 @@ def run_fsdp2(args):
                          "gathered bf16 parameters out")
     cpu = None
     if rank == 0 and not args.no_cpu:
-        cv, sec, n_el = _fsdp2_oracle(2)
+        cv, sec, n_el = _fsdp2_oracle(2, 0, not direct)
         cpu = {"value": round(cv, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                "sample": f"2 x (chunk-cat, 8 fused updates and the copy-out) of the layer group "
                          f"with dimension 0 divided by 16 ({n_el} elements), numpy "
                          f"single-threaded"}
     if rank == 0:
+        steps_text = {
+            True: "8 x the rank's step read straight from the ranks' per-parameter gradients "
+                  "(Fsdp2Step: one launch over its 9 parameters, no chunk-cat copy), all-gather "
+                  "copy-out into the 9 full parameters",
+            False: "8 x chunk-cat of a rank's full bf16 gradients, 8 x fused step on the padded "
+                   "local buffers, all-gather copy-out into the 9 full parameters"}
+        kernels = {"fused_ms_per_launch": round(avg[1] / nd, 4),
+                   "fused_gbs": round(achieved, 1),
+                   "copy_out_ms": round(avg[2], 4),
+                   "copy_out_gbs": round(ag_b / (avg[2] / 1e3) / 1e9, 1)}
+        if not direct:
+            kernels = {"chunk_cat_ms": round(avg[0], 4),
+                       "chunk_cat_gbs": round(cc_b / (avg[0] / 1e3) / 1e9, 1), **kernels}
+        kernels["with_chunk_cat" if direct else "without_chunk_cat"] = {
+            "step": steps_text[not direct], "ms": round(other_ms, 4),
+            "gbs": round(other_b / (other_ms / 1e3) / 1e9, 1), "bytes": other_b,
+            "time_vs_this_line": round(other_ms / (total_ms / args.steps), 4),
+            "kernel": other_kernel, "note": "the same bits as the line's step"}
         print(json.dumps({
             "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
@@ -971,29 +1010,12 @@ def run_fsdp2(args):
                        "tma_stages": _stages_name(args),
                        "group": "one Llama-7B layer (9 parameters, "
                        "202,383,360 elements)", "nd": nd, "local_elements": L,
-                       "step": "8 x chunk-cat of a rank's full bf16 gradients, 8 x fused step on "
-                               "the padded local buffers, all-gather copy-out into the 9 full "
-                               "parameters", "bytes_per_step": step_b,
+                       "step": steps_text[direct], "bytes_per_step": step_b,
                        "l2": f"no flush: each step streams {step_b / 1e9:.1f} GB vs a 129 MB L2"},
-            "kernels": {"chunk_cat_ms": round(avg[0], 4),
-                        "chunk_cat_gbs": round(cc_b / (avg[0] / 1e3) / 1e9, 1),
-                        "fused_ms_per_launch": round(avg[1] / nd, 4),
-                        "fused_gbs": round(achieved, 1),
-                        "copy_out_ms": round(avg[2], 4),
-                        "copy_out_gbs": round(ag_b / (avg[2] / 1e3) / 1e9, 1),
-                        "step_without_chunk_cat": {
-                            "ms": round(direct_ms, 4),
-                            "gbs": round(direct_b / (direct_ms / 1e3) / 1e9, 1),
-                            "bytes": direct_b,
-                            "time_vs_chunk_cat_step": round(direct_ms / (total_ms / args.steps),
-                                                            4),
-                            "kernel": direct_kernel,
-                            "note": "fsdp2_rs_avg_adamw_cast per rank through Fsdp2Step (one "
-                                    "launch over all its parameters, read straight from the "
-                                    "ranks' gradients) + the copy-out: the same bits as the "
-                                    "chunk-cat step"}},
-            "roofline": _roofline(achieved, f"{fused_kernel} on one rank's local buffer",
-                                  fused_launch),
+            "kernels": kernels,
+            "roofline": _roofline(achieved, f"{fused_kernel}, one rank's local buffer",
+                                  fused_launch,
+                                  _traffic(FSDP2_WORKLOAD, L, args) if direct else None),
             "e2e": e2e, "gpu_launches": launches, "clocks": clk, "cpu_baseline": cpu,
         }))
 
@@ -1145,12 +1167,13 @@ def run_ragged(args):
     _finish_dist(world)
 
 
-def _fsdp2_oracle(steps, warmup=0):
+def _fsdp2_oracle(steps, warmup=0, with_chunk_cat=False):
     """The oracle's FSDP2 group step (chunk-cat of every rank's gradients,
     the fused update of every rank's local buffer, all-gather copy-out) on
     the Llama-7B layer group with every dimension 0 divided by 16, numpy on
     one core, timed over ``steps`` steps after ``warmup``.  Returns (GB/s of
-    the step's algorithmic bytes, seconds per step, elements)."""
+    the step's algorithmic bytes, seconds per step, elements); the bytes are
+    the bench line's: the chunk-cat's only when the line times it."""
     import numpy as np
     import oracle
     import synth
@@ -1186,7 +1209,8 @@ def _fsdp2_oracle(steps, warmup=0):
         oracle.all_gather_copy_out(outs, lay)
         if k >= warmup:
             tt += time.perf_counter() - t0
-    return (cc_b + fused_b + ag_b) * steps / tt / 1e9, tt / steps, n
+    step_b = fused_b + ag_b + (cc_b if with_chunk_cat else 0)
+    return step_b * steps / tt / 1e9, tt / steps, n
 
 
 def run_fsdp2_reference(args):
@@ -1196,7 +1220,7 @@ def run_fsdp2_reference(args):
     init_dist(world)
     if rank == 0:
         nd = 8
-        val, sec, n = _fsdp2_oracle(args.steps, args.warmup)
+        val, sec, n = _fsdp2_oracle(args.steps, args.warmup, args.fsdp2_chunk_cat)
         tt = sec * args.steps
         print(json.dumps({
             "impl": "reference", "metric": METRIC, "value": round(val, 4), "unit": "GB/s",
@@ -1425,7 +1449,8 @@ def _traffic(workload_name, elements, args):
     the profile's bytes per element (None for smaller cases, other kernel
     choices or a kernel changed since the capture)."""
     per = profiled_traffic(workload_name)
-    if per is None or args.layers or args.nd or args.kernel_path != "auto" or args.tma_stages:
+    if (per is None or args.layers or args.nd or args.kernel_path != "auto" or args.tma_stages
+            or getattr(args, "shrink", 1) > 1):
         return None
     return round(per * elements)
 
