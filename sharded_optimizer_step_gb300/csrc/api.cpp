@@ -74,10 +74,14 @@ std::atomic<int> g_dependent_launch{1};
 // register-staged kernel of the same operation --
 //   fused step: only at N_d = 9..11, 13..15 (the register kernel's loop
 //     over any N_d there: 5.7 vs 6.7 TB/s at N_d = 9), N_d > 16, and 5, 7,
-//     12 or 16 fp32 slices, whose register kernels would spill (at N_d = 8
-//     the register kernel moved 7.13 vs 6.88 TB/s; at 6, compiled, 6.8 vs
-//     6.3; at 5 and 7 on the up-to-8 kernel 6.6 vs 6.2 and 6.7 vs 6.5; at
-//     12 the two were level; at 1..4 and 16 it was faster as well);
+//     12 or 16 fp32 slices, which the compiled register kernels do not
+//     take because they would spill (at 12 and 16 fp32 slices two stages
+//     do not fit either, and the register kernel's loop over any N_d
+//     runs: 7.22 TB/s at 16, against 6.57 for the spilling compiled form).
+//     Elsewhere the register kernel won: at N_d = 8 7.13 vs 6.88 TB/s; at
+//     6, compiled, 6.8 vs 6.3; at 5 and 7 on the up-to-8 kernel 6.6 vs 6.2
+//     and 6.7 vs 6.5; at 12 the two were level; at 1..4 and 16 (16-bit
+//     slices) it was faster as well;
 //   bucket all-reduce: at N_d = 4 and 8 on buckets of at least 32M
 //     elements (one 400M bucket at N_d = 4: 6.9 vs 6.4 TB/s; at N_d = 8:
 //     7.05 vs 6.98) and at N_d > 8; never at N_d = 1..3 and 5..7, where the
@@ -745,11 +749,11 @@ int fused_step(const void* const* grad_slices, int32_t grad_dtype, int32_t nd, i
         return fail(SHARDSTEP_ERR_CAPACITY, "nd %d > %d", nd, SHARDSTEP_MAX_ND);
     if (S < 0) return fail(SHARDSTEP_ERR_INVALID, "S must be >= 0");
     AdamScalars c{};
-    if (int rc = adam_source(hp, state, &c); rc != SHARDSTEP_OK) return rc;
+    if (int rc2 = adam_source(hp, state, &c); rc2 != SHARDSTEP_OK) return rc2;
     if (S == 0) return ok();
     Span outs[4];
-    if (int rc = check_step_outputs(S, master, m, v, out_bf16, outs); rc != SHARDSTEP_OK)
-        return rc;
+    if (int rc2 = check_step_outputs(S, master, m, v, out_bf16, outs); rc2 != SHARDSTEP_OK)
+        return rc2;
     // vector path: 4 elements per access -> 16-byte state, 8-byte 16-bit
     // (16-byte fp32) gradient slices, 8-byte bf16 output
     PtrTable tab;
@@ -772,8 +776,8 @@ int fused_step(const void* const* grad_slices, int32_t grad_dtype, int32_t nd, i
     if (e != cudaSuccess) return cuda_fail(e, "fused step kernel launch");
     if (tma)
         note_kernel("staged_stream<AdamOp<%s>> (TMA-staged)", dtype_name(grad_dtype));
-    else if (vec && (compiled_nd(nd, {1, 2, 3, 4, 6, 8, 16}) ||
-                     (nd == 12 && grad_dtype != SHARDSTEP_DTYPE_F32)))
+    else if (vec && (compiled_nd(nd, {1, 2, 3, 4, 6, 8}) ||
+                     ((nd == 12 || nd == 16) && grad_dtype != SHARDSTEP_DTYPE_F32)))
         note_kernel("rs_adamw_cast_vec4<%d, %s> (register-staged)", nd, dtype_name(grad_dtype));
     else if (vec && (nd == 5 || nd == 7) && grad_dtype != SHARDSTEP_DTYPE_F32)
         note_kernel("rs_adamw_cast_vec4<up to 8: %d, %s> (register-staged)", nd,

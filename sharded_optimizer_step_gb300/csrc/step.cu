@@ -661,10 +661,12 @@ cudaError_t dispatch_vec(const StepArgs& a, cudaStream_t s) {
             else return go_vec<kRuntimeND, GT>(a, s);
         case 6: return go_vec<6, GT>(a, s);
         case 8: return go_vec<8, GT>(a, s);
-        case 12:  // 12 fp32 slices would spill at 64 registers: the loop instead
+        case 12:  // 12 or 16 fp32 slices would spill at 64 registers: the loop instead
             if constexpr (GT != kGradF32) return go_vec<12, GT>(a, s);
             else return go_vec<kRuntimeND, GT>(a, s);
-        case 16: return go_vec<16, GT>(a, s);
+        case 16:
+            if constexpr (GT != kGradF32) return go_vec<16, GT>(a, s);
+            else return go_vec<kRuntimeND, GT>(a, s);
         default: return go_vec<kRuntimeND, GT>(a, s);
     }
 }
