@@ -72,16 +72,15 @@ std::atomic<int> g_dependent_launch{1};
 // still checks alignment and the stage size).  PATH_REGISTER: never;
 // PATH_TMA: always; PATH_AUTO: where it measured faster on GB300 against the
 // register-staged kernel of the same operation --
-//   fused step: only at N_d = 9..11, 13..15 (the register kernel's loop
-//     over any N_d there: 5.7 vs 6.7 TB/s at N_d = 9), N_d > 16, and 5, 7,
-//     12 or 16 fp32 slices, which the compiled register kernels do not
-//     take because they would spill (at 12 and 16 fp32 slices two stages
-//     do not fit either, and the register kernel's loop over any N_d
-//     runs: 7.22 TB/s at 16, against 6.57 for the spilling compiled form).
-//     Elsewhere the register kernel won: at N_d = 8 7.13 vs 6.88 TB/s; at
-//     6, compiled, 6.8 vs 6.3; at 5 and 7 on the up-to-8 kernel 6.6 vs 6.2
-//     and 6.7 vs 6.5; at 12 the two were level; at 1..4 and 16 (16-bit
-//     slices) it was faster as well;
+//   fused step: only at N_d > 16 and with fp32 slices at N_d = 5, 7 and
+//     9..16, which the compiled register kernels do not take because they
+//     would spill (where two stages do not fit, at 12..16 fp32 slices, the
+//     register kernel's loop over any N_d runs: 7.22 TB/s at 16, against
+//     6.57 for a spilling compiled form).  Elsewhere the register kernel
+//     won: at N_d = 8 7.13 vs 6.88 TB/s; at 6, compiled, 6.8 vs 6.3; at 5
+//     and 7 on the up-to-8 kernel 6.6 vs 6.2 and 6.7 vs 6.5; compiled for
+//     9..16 16-bit slices 7.15-7.35 vs 6.80-7.15 (50M elements, the same
+//     buffers in one process); at 1..4 it was faster as well;
 //   bucket all-reduce: at N_d = 4 and 8 on buckets of at least 32M
 //     elements (one 400M bucket at N_d = 4: 6.9 vs 6.4 TB/s; at N_d = 8:
 //     7.05 vs 6.98) and at N_d > 8; never at N_d = 1..3 and 5..7, where the
@@ -98,7 +97,8 @@ enum class TmaOp { kStep, kAllReduce, kAccumulate, kCheck };
 bool register_step_kernel(int nd, int grad_dtype) {
     switch (nd) {
         case 1: case 2: case 3: case 4: case 6: case 8: return true;
-        case 5: case 7: case 12: case 16: return grad_dtype != SHARDSTEP_DTYPE_F32;
+        case 5: case 7: case 9: case 10: case 11: case 12: case 13: case 14: case 15:
+        case 16: return grad_dtype != SHARDSTEP_DTYPE_F32;
         default: return false;
     }
 }
@@ -777,7 +777,7 @@ int fused_step(const void* const* grad_slices, int32_t grad_dtype, int32_t nd, i
     if (tma)
         note_kernel("staged_stream<AdamOp<%s>> (TMA-staged)", dtype_name(grad_dtype));
     else if (vec && (compiled_nd(nd, {1, 2, 3, 4, 6, 8}) ||
-                     ((nd == 12 || nd == 16) && grad_dtype != SHARDSTEP_DTYPE_F32)))
+                     (nd >= 9 && nd <= 16 && grad_dtype != SHARDSTEP_DTYPE_F32)))
         note_kernel("rs_adamw_cast_vec4<%d, %s> (register-staged)", nd, dtype_name(grad_dtype));
     else if (vec && (nd == 5 || nd == 7) && grad_dtype != SHARDSTEP_DTYPE_F32)
         note_kernel("rs_adamw_cast_vec4<up to 8: %d, %s> (register-staged)", nd,

@@ -166,9 +166,11 @@ def test_hybrid_step_matches_oracle(nd, F, gdt, S, shift, path):
                                       (12, 4, "bf16"), (12, 3, "f32"), (64, 16, "bf16"),
                                       (5, 1, "bf16"), (7, 7, "f32"), (5, 5, "f32")])
 def test_fused_step_any_nd_matches_oracle(nd, F, gdt, path):
-    """N_d without a compiled register kernel: the slices are loaded in
-    batches (8 16-bit or 4 fp32 slices), the last batch partial, and with
-    hybrid sharding the groups of F cross the batch boundaries."""
+    """N_d without a compiled register kernel (24, 64, and fp32 slices
+    above 4 but 6 and 8): the slices are loaded in batches (8 16-bit or 4
+    fp32 slices), the last batch partial, and with hybrid sharding the
+    groups of F cross the batch boundaries; with 16-bit slices at 6, 7, 12
+    and 13, the compiled and up-to-8 forms."""
     S = 6151
     seed = 77 * nd + F
     f = (S + F - 1) % F
@@ -191,6 +193,38 @@ def test_fused_step_any_nd_matches_oracle(nd, F, gdt, path):
     assert_bits(host_f32(dm), m, "m")
     assert_bits(host_f32(dv), v, "v")
     assert_bits(host_bf16(out), ob, "bf16")
+
+
+@pytest.mark.parametrize("nd,F", [(9, 9), (10, 10), (11, 11), (13, 13), (14, 14), (15, 15),
+                                  (10, 5), (14, 7), (15, 3), (9, 3)])
+@pytest.mark.parametrize("S,shift", [(4099, 0), (152 * 512 + 13, 1)])
+def test_fused_step_compiled_9_to_15_matches_oracle(nd, F, S, shift, path):
+    """16-bit slices at N_d = 9..11 and 13..15: the register kernel compiled
+    for each count, all N_d loads in flight; plain rank order and grouped
+    (hybrid) order; ragged shards over many blocks, misaligned slices."""
+    seed = 131 * nd + F + S
+    f = (S + F - 1) % F
+    p = synth.host_fill(synth.normal_stream(seed, (95, 2), 0.02), 0, S, "f32")
+    m = synth.host_fill(synth.normal_stream(seed, (95, 3), 1e-4), 0, S, "f32")
+    v = np.abs(synth.host_fill(synth.normal_stream(seed, (95, 4), 1e-7), 0, S, "f32"))
+    dp, dm, dv = dev_f32(p, shift), dev_f32(m, shift), dev_f32(v, shift)
+    out = torch.empty(S + 1, dtype=torch.bfloat16, device=DEV)[shift:shift + S]
+    contribs = _grads(seed, nd, F * S, "bf16", 1)
+    slices = [dev_bf16(c[f * S:(f + 1) * S], shift if q % 3 == 1 else 0)
+              for q, c in enumerate(contribs)]
+    if F == nd:
+        ss.fsdp_rs_avg_adamw_cast(slices, dp, dm, dv, out, HPC, 2)
+        p, m, v, ob = oracle.fsdp_shard_step(contribs, f, S, p, m, v, HP, 2)
+    else:
+        ss.fsdp_hybrid_rs_avg_adamw_cast(slices, F, dp, dm, dv, out, HPC, 2)
+        p, m, v, ob = oracle.hybrid_shard_step(contribs, F, f, S, p, m, v, HP, 2)
+    torch.cuda.synchronize()
+    assert_bits(host_f32(dp), p, "master")
+    assert_bits(host_f32(dm), m, "m")
+    assert_bits(host_f32(dv), v, "v")
+    assert_bits(host_bf16(out), ob, "bf16")
+    if path != "tma" and shift == 0:
+        assert ss.last_kernel().startswith(f"rs_adamw_cast_vec4<{nd}, bf16>"), ss.last_kernel()
 
 
 def test_hybrid_group_order_is_not_the_flat_order(path):
@@ -649,8 +683,9 @@ def test_bucket_allreduce_dependent_launches_keep_stream_order(dependent, path):
 
 def test_auto_path_names_the_kernel_it_launched():
     """The automatic choice, as shardstep_last_kernel reports it: the
-    register-staged fused kernel at N_d = 8 and its up-to-8 form at 7, the
-    TMA-staged one at N_d = 9, TMA-staged whenever forced; the all-reduce
+    register-staged fused kernel at N_d = 8, 9 and 15 and its up-to-8 form
+    at 7; the TMA-staged one at N_d = 17 and with 9 fp32 slices, the loop
+    over any N_d with 16 fp32 slices; TMA-staged whenever forced; the all-reduce
     and the check on their register kernels at N_d = 1..8 (16-bit slices),
     on the TMA-staged ones above 8."""
     S = 8192
@@ -660,12 +695,18 @@ def test_auto_path_names_the_kernel_it_launched():
     out = torch.empty(S, dtype=torch.bfloat16, device=DEV)
     prev = ss.set_fused_path("auto")
     try:
-        for nd, want in [(8, "rs_adamw_cast_vec4<8, bf16> (register-staged)"),
-                         (7, "rs_adamw_cast_vec4<up to 8: 7, bf16> (register-staged)"),
-                         (9, "staged_stream<AdamOp<bf16>> (TMA-staged)")]:
-            g = [torch.zeros(S, dtype=torch.bfloat16, device=DEV) for _ in range(nd)]
+        for nd, dt, want in [
+                (8, torch.bfloat16, "rs_adamw_cast_vec4<8, bf16> (register-staged)"),
+                (7, torch.bfloat16, "rs_adamw_cast_vec4<up to 8: 7, bf16> (register-staged)"),
+                (9, torch.bfloat16, "rs_adamw_cast_vec4<9, bf16> (register-staged)"),
+                (15, torch.bfloat16, "rs_adamw_cast_vec4<15, bf16> (register-staged)"),
+                (17, torch.bfloat16, "staged_stream<AdamOp<bf16>> (TMA-staged)"),
+                (9, torch.float32, "staged_stream<AdamOp<f32>> (TMA-staged)"),
+                (16, torch.float32,
+                 "rs_adamw_cast_vec4<any N_d = 16, f32> (register-staged)")]:
+            g = [torch.zeros(S, dtype=dt, device=DEV) for _ in range(nd)]
             ss.fsdp_rs_avg_adamw_cast(g, master, m, v, out, HPC, 1)
-            assert ss.last_kernel() == want
+            assert ss.last_kernel() == want, (nd, dt)
         g = [torch.zeros(S, dtype=torch.bfloat16, device=DEV) for _ in range(8)]
         ss.set_fused_path("tma")
         ss.fsdp_rs_avg_adamw_cast(g, master, m, v, out, HPC, 1)

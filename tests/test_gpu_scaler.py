@@ -71,7 +71,7 @@ def test_device_fill_matches_host_fill_for_fp16():
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16", "f32"])
 @pytest.mark.parametrize("nd,F", [(8, 8), (4, 4), (8, 2), (3, 3), (1, 1), (2, 2), (6, 3),
-                                  (16, 16), (64, 8)])
+                                  (11, 11), (14, 7), (16, 16), (64, 8)])
 @pytest.mark.parametrize("S,shift", [(6151, 0), (4099, 1), (13, 0)])
 def test_scaled_steps_match_oracle(dtype, nd, F, S, shift, path):
     scale = 1024.0
