@@ -83,11 +83,15 @@ std::atomic<int> g_dependent_launch{1};
 //     buffers in one process); at 1..4 it was faster as well;
 //   bucket all-reduce: at N_d = 4 and 8 on buckets of at least 32M
 //     elements (one 400M bucket at N_d = 4: 6.9 vs 6.4 TB/s; at N_d = 8:
-//     7.05 vs 6.98) and at N_d > 8; never at N_d = 1..3 and 5..7, where the
+//     7.05 vs 6.98) and at N_d > 16; never at N_d = 1..3 and 5..7, where the
 //     register kernel is compiled with several vectors' loads in flight
 //     (200M elements in 25 MiB buckets, register / TMA-staged: N_d = 3
-//     6.1 / 3.7, 5 6.5 / 4.8, 6 6.5 / 5.4, 7 6.7 / 5.9 TB/s);
-//   non-finite check: with 16-bit slices at N_d > 8 only (N_d = 3 / 5 / 6
+//     6.1 / 3.7, 5 6.5 / 4.8, 6 6.5 / 5.4, 7 6.7 / 5.9 TB/s), nor at
+//     9..16, where it is compiled for each count (50M elements in 25 MiB
+//     buckets, same buffers: 6.8-7.0 vs 5.7-6.8 TB/s, the widest gap at
+//     11..14);
+//   non-finite check: with 16-bit slices at N_d > 16 only (at 9..16,
+//     compiled for each count, 7.1-7.4 vs 6.1-6.9 TB/s; N_d = 3 / 5 / 6
 //     / 7, 200M fp16 elements: 5.1 / 2.7, 6.4 / 4.1, 6.9 / 4.6, 6.9 / 5.1
 //     TB/s; at N_d = 1 / 2 / 4 / 8: 5.0 vs 2.1, 6.0 vs 3.2, 6.7 vs 5.7,
 //     7.4 vs 7.3), with fp32 slices at every N_d but 1, 2, 4 and 8;
@@ -111,10 +115,10 @@ bool use_tma(TmaOp op, int64_t n, int nd = 0, int grad_dtype = SHARDSTEP_DTYPE_B
         case TmaOp::kStep: return nd >= 3 && !register_step_kernel(nd, grad_dtype);
         case TmaOp::kAllReduce:
             if (nd == 4 || nd == 8) return n >= (int64_t{32} << 20);
-            return nd > 8;
+            return nd > 16;
         case TmaOp::kCheck:
             if (grad_dtype == SHARDSTEP_DTYPE_F32) return nd != 1 && nd != 2 && nd != 4 && nd != 8;
-            return nd > 8;
+            return nd > 16;
         default: return false;
     }
 }
@@ -944,7 +948,7 @@ int fsdp_grad_unscale_check(const void* const* grad_slices, int32_t grad_dtype, 
     if (tma)
         note_kernel("staged_stream<CheckOp<%s>> (TMA-staged)", dtype_name(grad_dtype));
     else if (vec && (compiled_nd(nd, {1, 2, 4, 8}) ||
-                     (grad_dtype != SHARDSTEP_DTYPE_F32 && compiled_nd(nd, {3, 5, 6, 7}))))
+                     (grad_dtype != SHARDSTEP_DTYPE_F32 && nd >= 3 && nd <= 16)))
         note_kernel("nonfinite_check_vec4<%d, %s> (register-staged)", nd, dtype_name(grad_dtype));
     else if (vec)
         note_kernel("nonfinite_check_vec4<any N_d = %d, %s> (register-staged)", nd,
@@ -1392,7 +1396,7 @@ int ddp_bucket_allreduce_avg(const uint16_t* const* rank_grads, int32_t nd,
         if (e != cudaSuccess) return cuda_fail(e, "all-reduce kernel launch");
         if (tma)
             note_kernel("staged_stream<MeanOutOp> (TMA-staged)");
-        else if (vec && compiled_nd(nd, {1, 2, 3, 4, 5, 6, 7, 8}))
+        else if (vec && nd >= 1 && nd <= 16)
             note_kernel("allreduce_avg_vec4<%d> (register-staged)", nd);
         else if (vec)
             note_kernel("allreduce_avg_vec4<any N_d = %d> (register-staged)", nd);

@@ -532,7 +532,7 @@ def test_grad_accumulate_matches_oracle(n, shift):
 
 # ---------------------------------------------------------------- buckets
 
-@pytest.mark.parametrize("nd", [2, 3, 8])
+@pytest.mark.parametrize("nd", [2, 3, 8, 9, 10, 11, 12, 13, 14, 15, 16, 17])
 @pytest.mark.parametrize("cap", [64, 5000, 1 << 22])
 def test_ddp_bucketed_step_matches_oracle(nd, cap):
     numels = [768, 3, 768 * 30, 5, 4096 * 3, 768, 1, 2000]
@@ -686,8 +686,8 @@ def test_auto_path_names_the_kernel_it_launched():
     register-staged fused kernel at N_d = 8, 9 and 15 and its up-to-8 form
     at 7; the TMA-staged one at N_d = 17 and with 9 fp32 slices, the loop
     over any N_d with 16 fp32 slices; TMA-staged whenever forced; the all-reduce
-    and the check on their register kernels at N_d = 1..8 (16-bit slices),
-    on the TMA-staged ones above 8."""
+    and the check on their register kernels at N_d = 1..16 (16-bit slices),
+    on the TMA-staged ones above 16."""
     S = 8192
     master = torch.zeros(S, device=DEV)
     m = torch.zeros(S, device=DEV)
@@ -719,12 +719,14 @@ def test_auto_path_names_the_kernel_it_launched():
         ss.fsdp_grad_accumulate(g[0], acc, 0.25, True)
         assert ss.last_kernel() == "accumulate_vec8 (register-staged)"
         # the bucket all-reduce and the check by N_d
-        g = g + [torch.zeros(S, dtype=torch.bfloat16, device=DEV) for _ in range(2)]
+        g = g + [torch.zeros(S, dtype=torch.bfloat16, device=DEV) for _ in range(9)]
         out16 = torch.empty(S, dtype=torch.bfloat16, device=DEV)
         for nd, want in [(3, "allreduce_avg_vec4<3> (register-staged)"),
                          (8, "allreduce_avg_vec4<8> (register-staged)"),
                          (6, "allreduce_avg_vec4<6> (register-staged)"),
-                         (10, "staged_stream<MeanOutOp> (TMA-staged)")]:
+                         (10, "allreduce_avg_vec4<10> (register-staged)"),
+                         (16, "allreduce_avg_vec4<16> (register-staged)"),
+                         (17, "staged_stream<MeanOutOp> (TMA-staged)")]:
             ss.ddp_bucket_allreduce_avg(g[:nd], [0, S], out16)
             assert ss.last_kernel() == want, nd
         h = [x.to(torch.float16) for x in g]
@@ -733,7 +735,9 @@ def test_auto_path_names_the_kernel_it_launched():
                          (3, "nonfinite_check_vec4<3, f16> (register-staged)"),
                          (8, "nonfinite_check_vec4<8, f16> (register-staged)"),
                          (5, "nonfinite_check_vec4<5, f16> (register-staged)"),
-                         (10, "staged_stream<CheckOp<f16>> (TMA-staged)")]:
+                         (10, "nonfinite_check_vec4<10, f16> (register-staged)"),
+                         (16, "nonfinite_check_vec4<16, f16> (register-staged)"),
+                         (17, "staged_stream<CheckOp<f16>> (TMA-staged)")]:
             sc.check(h[:nd])
             assert ss.last_kernel() == want, nd
         torch.cuda.synchronize()
