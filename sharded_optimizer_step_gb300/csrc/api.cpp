@@ -1281,9 +1281,13 @@ int fsdp2_step(const void* const* grads, int32_t grad_dtype, const int64_t* dim0
         }
     }
     if (int r = flush(); r != SHARDSTEP_OK) return r;
+    // compiled for 1..8 slices and 9..16 16-bit slices; the loop over any
+    // N_d otherwise
+    const bool compiled = nd <= 8 || (nd <= 16 && grad_dtype != SHARDSTEP_DTYPE_F32);
     if (tables > 0)
-        note_kernel("rs_adamw_cast_segs<%d, %s> (register-staged, %d launch%s)", nd,
-                    dtype_name(grad_dtype), tables, tables > 1 ? "es" : "");
+        note_kernel("rs_adamw_cast_segs<%s%d, %s> (register-staged, %d launch%s)",
+                    compiled ? "" : "any N_d = ", nd, dtype_name(grad_dtype), tables,
+                    tables > 1 ? "es" : "");
     else if (pad_launched && !fused_launched)
         note_kernel("adamw_zero_grad");
     return ok();

@@ -205,14 +205,24 @@ cudaError_t dispatch_segs(const SegTable& st, int nd, float* P, float* M, float*
         case 6: return go_segs<6, GT>(st, nd, P, M, V, out, c, mo, s);
         case 7: return go_segs<7, GT>(st, nd, P, M, V, out, c, mo, s);
         case 8: return go_segs<8, GT>(st, nd, P, M, V, out, c, mo, s);
-        case 12:  // 12 or 16 fp32 slices would spill at 64 registers: the loop instead
-            if constexpr (GT != kGradF32) return go_segs<12, GT>(st, nd, P, M, V, out, c, mo, s);
-            else return go_segs<kAnyND, GT>(st, nd, P, M, V, out, c, mo, s);
-        case 16:
-            if constexpr (GT != kGradF32) return go_segs<16, GT>(st, nd, P, M, V, out, c, mo, s);
-            else return go_segs<kAnyND, GT>(st, nd, P, M, V, out, c, mo, s);
-        default: return go_segs<kAnyND, GT>(st, nd, P, M, V, out, c, mo, s);
+        default: break;
     }
+    // 9..16 16-bit slices compiled for their count too (all loads in
+    // flight); as many fp32 slices would spill at 64 registers: the loop
+    if constexpr (GT != kGradF32) {
+        switch (nd) {
+            case 9: return go_segs<9, GT>(st, nd, P, M, V, out, c, mo, s);
+            case 10: return go_segs<10, GT>(st, nd, P, M, V, out, c, mo, s);
+            case 11: return go_segs<11, GT>(st, nd, P, M, V, out, c, mo, s);
+            case 12: return go_segs<12, GT>(st, nd, P, M, V, out, c, mo, s);
+            case 13: return go_segs<13, GT>(st, nd, P, M, V, out, c, mo, s);
+            case 14: return go_segs<14, GT>(st, nd, P, M, V, out, c, mo, s);
+            case 15: return go_segs<15, GT>(st, nd, P, M, V, out, c, mo, s);
+            case 16: return go_segs<16, GT>(st, nd, P, M, V, out, c, mo, s);
+            default: break;
+        }
+    }
+    return go_segs<kAnyND, GT>(st, nd, P, M, V, out, c, mo, s);
 }
 
 }  // namespace

@@ -195,9 +195,15 @@ def _oracle_contribs(cc, gdt):
     return [oracle.f16_to_f32(c) for c in cc] if gdt == "f16" else cc
 
 
+# every compiled count with every slice type, and the 16-bit counts 9..15
+# (compiled for 16-bit slices only)
+ND_GDT = ([(nd, g) for nd in (1, 2, 3, 4, 8, 12, 16) for g in ("bf16", "f32", "f16")] +
+          [(9, "bf16"), (10, "f16"), (11, "bf16"), (13, "f16"), (14, "bf16"), (15, "bf16"),
+           (11, "f32")])
+
+
 @pytest.mark.parametrize("shapes", SHAPE_SETS, ids=lambda s: f"{len(s)}params")
-@pytest.mark.parametrize("nd", [1, 2, 3, 4, 8, 12, 16])
-@pytest.mark.parametrize("gdt", ["bf16", "f32", "f16"])
+@pytest.mark.parametrize("nd,gdt", ND_GDT)
 def test_fsdp2_step_without_chunk_cat_matches_oracle(shapes, nd, gdt, path):
     """fsdp2_rs_avg_adamw_cast on every rank, two steps, against the oracle's
     chunk-cat + shard step.  The local state starts non-zero everywhere,
