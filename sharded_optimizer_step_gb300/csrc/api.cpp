@@ -1464,7 +1464,7 @@ int ddp_bucket_allreduce_avg_adamw_cast(const uint16_t* const* rank_grads, int32
         tab, nd, n, mean_out ? mean_out + a0 : nullptr, master + a0, m + a0, v + a0,
         params + a0, c, mean_op(nd, nd), vec, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "fused all-reduce + AdamW kernel launch");
-    if (vec && (compiled_nd(nd, {1, 2, 3, 4, 6, 8, 12, 16})))
+    if (vec && (compiled_nd(nd, {1, 2, 3, 4, 6, 8}) || (nd >= 9 && nd <= 16)))
         note_kernel("ddp_allreduce_adamw_cast_vec4<%d> (register-staged)", nd);
     else if (vec && (nd == 5 || nd == 7))
         note_kernel("ddp_allreduce_adamw_cast_vec4<up to 8: %d> (register-staged)", nd);

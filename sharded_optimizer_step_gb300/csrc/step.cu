@@ -862,7 +862,13 @@ cudaError_t launch_ddp_allreduce_adamw_cast(const PtrTable& tab, int nd, int64_t
         case 5: case 7: SHARDSTEP_DDP_GO(-8); break;
         case 6: SHARDSTEP_DDP_GO(6); break;
         case 8: SHARDSTEP_DDP_GO(8); break;
+        case 9: SHARDSTEP_DDP_GO(9); break;
+        case 10: SHARDSTEP_DDP_GO(10); break;
+        case 11: SHARDSTEP_DDP_GO(11); break;
         case 12: SHARDSTEP_DDP_GO(12); break;
+        case 13: SHARDSTEP_DDP_GO(13); break;
+        case 14: SHARDSTEP_DDP_GO(14); break;
+        case 15: SHARDSTEP_DDP_GO(15); break;
         case 16: SHARDSTEP_DDP_GO(16); break;
         default: SHARDSTEP_DDP_GO(kRuntimeND); break;
     }

@@ -54,7 +54,7 @@ def _h16(t):
 NUMELS = [768, 3, 768 * 30, 5, 4096 * 3, 768, 1, 2000, 70_001]
 
 
-@pytest.mark.parametrize("nd", [1, 2, 3, 5, 8, 13, 16, 64])
+@pytest.mark.parametrize("nd", [1, 2, 3, 5, 8, 9, 11, 13, 16, 64])
 @pytest.mark.parametrize("cap", [64, 5000, 1 << 22])
 @pytest.mark.parametrize("keep_mean", [True, False])
 @pytest.mark.parametrize("shift", [0, 1])
