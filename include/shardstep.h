@@ -738,12 +738,12 @@ int fsdp_reshard_plan(int64_t total, int32_t old_nd, int32_t new_nd, int32_t new
  * allow it (every source 16-byte aligned, at least 4096 elements, two stages
  * in shared memory); _REGISTER uses only the register-staged kernels;
  * _AUTO (default) uses the TMA-staged kernels where they measured faster:
- * the fused steps at N_d = 9..11, 13..15 and above 16 (and at 5, 7, 12 and
- * 16 with fp32 slices), the bucket all-reduce at N_d = 4 and 8 on buckets
- * of at least 32M elements and above N_d = 8 on every bucket, the check
- * above N_d = 8 (with fp32 slices at every N_d but 1, 2, 4 and 8), the
- * accumulation never; the fused DDP step and the fused last micro-batch
- * are register-staged only.  The copies (flat_pack, ag_unpack, FSDP2 chunk-cat /
+ * the fused steps above N_d = 16 and with fp32 slices at 5, 7 and 9..11
+ * (where two stages fit), the bucket all-reduce at N_d = 4 and 8 on
+ * buckets of at least 32M elements and above N_d = 16 on every bucket, the
+ * check above N_d = 16 (with fp32 slices at every N_d but 1, 2, 4 and 8),
+ * the accumulation never; the fused DDP step, the fused last micro-batch
+ * and the FSDP2 step without the chunk-cat are register-staged only.  The copies (flat_pack, ag_unpack, FSDP2 chunk-cat /
  * copy-out) send the body of every range between its first and last 16-byte
  * boundary of the destination to a 16-byte vector copy (realigning the
  * source when it is not congruent) except under _REGISTER, which keeps them
