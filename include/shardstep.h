@@ -674,12 +674,15 @@ double shardstep_hybrid_comm_bytes(double psi, int32_t nd, int32_t shard_group, 
  * loading; optimizer state is saved with the weights).  Host only: the
  * caller stages device state through host memory.
  *
- * A rank file holds a 64-byte header (magic "SHSTCKPT", version 1, nd, rank,
- * section count, step), the element count T_u of every unit's
- * FlatParameter, a section table and the sections, each at a 4096-byte
- * aligned offset with an FNV-1a checksum (64-bit, over little-endian 64-bit
- * words, a trailing partial word zero-padded).  It is written to
- * "<path>.tmp" and renamed into place. */
+ * A rank file holds a 64-byte header (magic "SHSTCKPT", version 2, nd, rank,
+ * section count, step, the tables' checksum), the element count T_u of
+ * every unit's FlatParameter, a section table and the sections, each at a
+ * 4096-byte aligned offset with its checksum.  Checksums are FNV-1a
+ * (64-bit) over little-endian 64-bit words, a trailing partial word
+ * zero-padded: the tables' one chain; a section's four chains, word j in
+ * chain j mod 4, whose four values are then folded in chain order by one
+ * more chain (version 1 files, whose sections have one chain, are read and
+ * verified too).  It is written to "<path>.tmp" and renamed into place. */
 typedef struct {
     int32_t unit;     /* unit index, 0 <= unit < n_units        */
     int32_t kind;     /* caller's tag, e.g. 0 master, 1 m, 2 v  */

@@ -131,3 +131,103 @@ def test_bad_arguments_are_refused(tmp_path):
     pieces = (_capi.CkptPiece * 1)()
     assert L.fsdp_reshard_plan(100, 8, 1, 0, pieces, 1, ctypes.byref(n)) == _capi.ERR_CAPACITY
     assert n.value == 8
+
+
+# ---- the rank-file format, restated here from its description: header of 64
+# bytes, unit totals, section table (unit, kind, bytes, offset, checksum),
+# sections at 4096-byte aligned offsets; FNV-1a over little-endian 64-bit words
+
+_BASIS, _PRIME, _MASK = 14695981039346656037, 1099511628211, (1 << 64) - 1
+
+
+def _words(data: bytes):
+    data = data + b"\0" * (-len(data) % 8)
+    return np.frombuffer(data, "<u8").tolist()
+
+
+def _fnv_chain(words, h=_BASIS):
+    for w in words:
+        h = ((h ^ w) * _PRIME) & _MASK
+    return h
+
+
+def _four_lane(data: bytes):
+    w = _words(data)
+    lanes = [_fnv_chain(w[k::4]) for k in range(4)]
+    return _fnv_chain(lanes)
+
+
+def _section_table(raw: bytes):
+    import struct
+    magic, version, hb, nd, rank, n_units, n_sec, step = struct.unpack_from("<8sIIiiiiq", raw, 0)
+    off = 64 + 8 * n_units
+    return version, [struct.unpack_from("<iiqqQ", raw, off + 32 * s) for s in range(n_sec)]
+
+
+def test_section_checksums_are_four_interleaved_fnv1a_chains(tmp_path):
+    # sizes whose word counts end on every chain, and a trailing partial word
+    totals = [1000, 1, 777, 4096, 13]
+    _save(str(tmp_path), totals, 3, step=2, seed=4)
+    for r in range(3):
+        raw = open(ck.rank_file(str(tmp_path), r), "rb").read()
+        version, table = _section_table(raw)
+        assert version == 2
+        for unit, kind, nbytes, offset, checksum in table:
+            data = raw[offset:offset + nbytes]
+            assert checksum == _four_lane(data), (r, unit, kind)
+            if nbytes > 8:
+                assert checksum != _fnv_chain(_words(data))
+
+
+def _version1_file(path, totals, nd, rank, step, sections):
+    """A rank file of the first format version (every checksum one chain)."""
+    import struct
+    n_u, n_s = len(totals), len(sections)
+    off = -(-(64 + 8 * n_u + 32 * n_s) // 4096) * 4096
+    table, body = [], b""
+    for unit, kind, data in sections:
+        table.append((unit, kind, len(data), off, _fnv_chain(_words(data))))
+        off = -(-(off + len(data)) // 4096) * 4096
+    totals_b = struct.pack(f"<{n_u}q", *totals)
+    table_b = b"".join(struct.pack("<iiqqQ", *e) for e in table)
+    tsum = _fnv_chain(_words(table_b), _fnv_chain(_words(totals_b)))
+    raw = bytearray(struct.pack("<8sIIiiiiqQ16s", b"SHSTCKPT", 1, 64, nd, rank, n_u, n_s, step,
+                                tsum, b"\0" * 16) + totals_b + table_b)
+    for (unit, kind, data), e in zip(sections, table):
+        raw += b"\0" * (e[3] - len(raw)) + data
+    open(path, "wb").write(bytes(raw))
+
+
+def test_version1_files_are_still_read_and_verified(tmp_path):
+    rng = np.random.default_rng(9)
+    totals = [10, 21]
+    secs = [(0, 0, rng.standard_normal(10).astype(np.float32).tobytes()),
+            (1, 0, rng.standard_normal(11).astype(np.float32).tobytes())]
+    path = ck.rank_file(str(tmp_path), 0)
+    _version1_file(path, totals, 2, 0, 5, secs)
+    nd, step, saved = ck.info(str(tmp_path))
+    assert (nd, step, saved) == (2, 5, totals)
+    L = _capi.lib()
+    assert L.shardstep_ckpt_verify(path.encode()) == _capi.OK
+    got = np.empty(11, np.float32)
+    assert L.shardstep_ckpt_read(path.encode(), 1, 0, 0, got.nbytes,
+                                 got.ctypes.data_as(ctypes.c_void_p)) == _capi.OK
+    assert got.tobytes() == secs[1][2]
+    raw = bytearray(open(path, "rb").read())
+    raw[-3] ^= 0x40
+    open(path, "wb").write(bytes(raw))
+    assert L.shardstep_ckpt_verify(path.encode()) == _capi.ERR_IO
+
+
+def test_four_lane_checksum_across_read_chunks(tmp_path):
+    """A section longer than the 4 MB pieces verify reads it in, with a
+    partial last piece: the chains continue across the pieces."""
+    totals = [2_100_003]
+    _save(str(tmp_path), totals, 1, step=1, seed=11)
+    path = ck.rank_file(str(tmp_path), 0)
+    raw = open(path, "rb").read()
+    _, table = _section_table(raw)
+    unit, kind, nbytes, offset, checksum = table[0]
+    assert nbytes > 2 * (1 << 22)
+    assert checksum == _four_lane(raw[offset:offset + nbytes])
+    assert _capi.lib().shardstep_ckpt_verify(path.encode()) == _capi.OK
