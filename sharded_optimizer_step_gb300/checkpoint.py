@@ -126,19 +126,17 @@ def plan(total: int, old_nd: int, new_nd: int, new_rank: int):
     return [(p.old_rank, p.old_offset, p.new_offset, p.count) for p in pieces[:n.value]]
 
 
-def load_rank(directory: str, opt) -> None:
-    """Fill ``opt``'s master / m / v and step count (the host count, and the
-    device step state's when it has one) from a checkpoint saved under any
-    rank count; padding positions of the new layout are zero."""
-    import torch
-    old_nd, step, totals = info(directory)
-    mine = [l.total for l in opt.layouts]
-    if totals != mine:
-        raise ValueError("checkpoint units do not match the optimizer's units")
-    L = _capi.lib()
+_READ_PIECE = 16 << 20   # bytes per read task, so that the pool stays balanced
+
+
+def _read_tasks(directory: str, opt, old_nd: int):
+    """The reads that fill ``opt``'s pinned staging from the saved rank
+    files: (path, unit, kind, byte offset in the section, bytes, destination
+    address), at most _READ_PIECE bytes each.  Zeroes the padding positions
+    of the new layout (no piece covers them) on the way."""
     host = _staging(opt)
+    tasks = []
     for u, lay in enumerate(opt.layouts):
-        # positions past the unit's total are padding: no piece covers them
         covered = max(0, min(lay.shard, lay.total - opt.rank * lay.shard))
         for h in host:
             h[opt.starts[u] + covered:opt.starts[u] + lay.shard].zero_()
@@ -146,18 +144,61 @@ def load_rank(directory: str, opt) -> None:
             path = rank_file(directory, q).encode()
             for kind, h in zip(_KINDS, host):
                 dst = h.data_ptr() + (opt.starts[u] + new_off) * 4
-                _capi.check("shardstep_ckpt_read", L.shardstep_ckpt_read(
-                    path, u, kind, off * 4, count * 4, ctypes.c_void_p(dst)))
-    for buf, h in zip(_states(opt), host):
+                for b0 in range(0, count * 4, _READ_PIECE):
+                    n = min(_READ_PIECE, count * 4 - b0)
+                    tasks.append((path, u, kind, off * 4 + b0, n, dst + b0))
+    return tasks
+
+
+def _run_read(task) -> None:
+    path, u, kind, off, n, dst = task
+    _capi.check("shardstep_ckpt_read", _capi.lib().shardstep_ckpt_read(
+        path, u, kind, off, n, ctypes.c_void_p(dst)))
+
+
+def _finish_load(opt, step: int) -> None:
+    """Staging -> device (queued; the caller synchronises), and the step
+    count (host and device)."""
+    for buf, h in zip(_states(opt), _staging(opt)):
         buf.copy_(h, non_blocking=True)
     opt.t = step
     state = getattr(opt, "state", None)
     if state is not None:                 # the device step state continues from here too
         state.init(step)
+
+
+def _check_units(opt, totals) -> None:
+    if totals != [l.total for l in opt.layouts]:
+        raise ValueError("checkpoint units do not match the optimizer's units")
+
+
+def load_rank(directory: str, opt) -> None:
+    """Fill ``opt``'s master / m / v and step count (the host count, and the
+    device step state's when it has one) from a checkpoint saved under any
+    rank count; padding positions of the new layout are zero."""
+    old_nd, step, totals = info(directory)
+    _check_units(opt, totals)
+    import torch
+    for t in _read_tasks(directory, opt, old_nd):
+        _run_read(t)
+    _finish_load(opt, step)
     torch.cuda.synchronize(opt.master.device)
 
 
-def load(directory: str, opts, threads: int = 8) -> None:
-    """Load every optimizer (one per rank of the new layout), in parallel."""
-    with ThreadPoolExecutor(max(1, min(threads, len(opts)))) as ex:
-        list(ex.map(lambda o: load_rank(directory, o), opts))
+def load(directory: str, opts, threads: int | None = None) -> None:
+    """Load every optimizer (one per rank of the new layout): every rank's
+    reads from the saved files go to one pool of ``threads`` workers (default:
+    the host's cores; the native reads release the interpreter lock), then
+    each rank's state is copied to its device."""
+    old_nd, step, totals = info(directory)
+    for o in opts:
+        _check_units(o, totals)
+    tasks = [t for o in opts for t in _read_tasks(directory, o, old_nd)]
+    workers = max(1, threads or os.cpu_count() or 1)
+    import torch
+    with ThreadPoolExecutor(workers) as ex:
+        list(ex.map(_run_read, tasks))
+    for o in opts:
+        _finish_load(o, step)
+    for dev in {o.master.device for o in opts}:
+        torch.cuda.synchronize(dev)
