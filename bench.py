@@ -87,7 +87,8 @@ def parse():
     ap.add_argument("--layers", type=int, default=0,
                     help="smaller case: only the first N layer units (for profiler captures)")
     ap.add_argument("--nd", type=int, default=0,
-                    help="rank-view lines (default, hybrid, fp16) and the DDP line: another "
+                    help="rank-view lines (default, hybrid, fp16), the DDP and the FSDP2 "
+                         "lines: another "
                          "number of emulated ranks N_d (0: the workload's own), for kernel "
                          "sweeps and profiler captures")
     ap.add_argument("--shrink", type=int, default=1,
@@ -857,7 +858,7 @@ def run_fsdp2(args):
     shapes = w.units[0]
     if args.shrink > 1:           # a smaller case: every parameter's dim 0 divided
         shapes = [(-(-sh[0] // args.shrink),) + tuple(sh[1:]) for sh in shapes]
-    nd = w.nd
+    nd = args.nd or w.nd
     dev = torch.device("cuda", local_rank)
     hp = ss.AdamW(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
     lay = ss.fsdp2_layout(shapes, nd)
@@ -1006,7 +1007,8 @@ def run_fsdp2(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded counter-based generator on the device; no data set or weights)",
             "config": {"workload": FSDP2_WORKLOAD + (f"_shrunk{args.shrink}x"
-                                                     if args.shrink > 1 else ""),
+                                                     if args.shrink > 1 else "") +
+                                    (f"_nd{nd}" if args.nd else ""),
                        "tma_stages": _stages_name(args),
                        "group": "one Llama-7B layer (9 parameters, "
                        "202,383,360 elements)", "nd": nd, "local_elements": L,
