@@ -1222,6 +1222,7 @@ int fsdp2_step(const void* const* grads, int32_t grad_dtype, const int64_t* dim0
     st.ns = 0;
     st.b0[0] = 0;
     int tables = 0;
+    int np = 0;  // slice pointers used in the current table
     auto flush = [&]() -> int {
         if (st.ns == 0) return SHARDSTEP_OK;
         cudaError_t e = launch_rs_adamw_cast_segs(st, nd, grad_dtype, master, m, v, out_bf16, c,
@@ -1230,15 +1231,22 @@ int fsdp2_step(const void* const* grads, int32_t grad_dtype, const int64_t* dim0
         ++tables;
         st.ns = 0;
         st.b0[0] = 0;
+        np = 0;
         return SHARDSTEP_OK;
     };
+    // p == nullptr: padding rows, which take no slice pointers
     auto add_seg = [&](int64_t lo, int64_t cnt, const void* const* p) -> int {
-        if (st.ns == kSegMax || (st.ns + 1) * nd > kSegPtrMax)
+        if (st.ns == kSegMax || (p != nullptr && np + nd > kSegPtrMax))
             if (int r = flush(); r != SHARDSTEP_OK) return r;
         const int k = st.ns;
         st.lo[k] = lo;
         st.n[k] = cnt;
-        for (int32_t q = 0; q < nd; ++q) st.p[k * nd + q] = p != nullptr ? p[q] : nullptr;
+        st.po[k] = -1;
+        if (p != nullptr) {
+            st.po[k] = np;
+            for (int32_t q = 0; q < nd; ++q) st.p[np + q] = p[q];
+            np += nd;
+        }
         st.b0[k + 1] = st.b0[k] + seg_blocks(cnt);
         st.ns = k + 1;
         return SHARDSTEP_OK;

@@ -5,7 +5,8 @@
 // rows the rank holds (N_d gradient slices, one per rank, each starting at
 // row rank * chunk of that rank's gradient), then its padding rows (every
 // contribution +0).  The host packs up to kSegMax segments (and at most
-// kSegPtrMax slice pointers) into one SegTable, passed as a __grid_constant__
+// kSegPtrMax slice pointers; padding rows take none) into one SegTable,
+// passed as a __grid_constant__
 // parameter so that a block can index its segment's pointers without a local
 // copy of the table.  Each block serves one segment: 128 threads, one
 // 4-element vector per thread, every load issued before any arithmetic, and
@@ -124,8 +125,8 @@ __global__ void __launch_bounds__(kSegThreads, kSegMinBlocks)
     const int64_t n = st.n[s];
     const int64_t nvec = n >> 2;
     const int64_t i = (static_cast<int64_t>(blockIdx.x) - st.b0[s]) * kSegThreads + threadIdx.x;
-    const void* const* p = st.p + static_cast<int64_t>(s) * nd;
-    const bool zero = p[0] == nullptr;     // padding rows: every contribution is +0
+    const bool zero = st.po[s] < 0;        // padding rows: every contribution is +0
+    const void* const* p = st.p + (zero ? 0 : st.po[s]);
     float* Ps = P + st.lo[s];
     float* Ms = M + st.lo[s];
     float* Vs = V + st.lo[s];

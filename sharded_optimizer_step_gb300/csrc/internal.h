@@ -187,15 +187,17 @@ cudaError_t launch_allreduce_avg(const PtrTable& tab, int nd, int64_t n, uint16_
                                  const MeanOp& mo, bool vec, bool pdl, cudaStream_t stream);
 // The segments of one FSDP2 step launch (launch_rs_adamw_cast_segs): segment
 // s covers local elements [lo[s], lo[s] + n[s]) and reads the N_d slices
-// p[s * nd + q] (p[s * nd] == nullptr: padding rows, every contribution +0);
-// b0[s] is its first block, b0[ns] the launch's block count.
-constexpr int kSegMax = 16;
-constexpr int kSegPtrMax = 128;
+// p[po[s] + q] (po[s] < 0: padding rows, every contribution +0, no
+// pointers); b0[s] is its first block, b0[ns] the launch's block count.
+// About 2.9 KB as a kernel parameter.
+constexpr int kSegMax = 32;
+constexpr int kSegPtrMax = 256;
 struct SegTable {
     const void* p[kSegPtrMax];
     int64_t lo[kSegMax];
     int64_t n[kSegMax];
     int64_t b0[kSegMax + 1];
+    int32_t po[kSegMax];
     int ns;
 };
 // Blocks one segment of n elements takes in launch_rs_adamw_cast_segs.
