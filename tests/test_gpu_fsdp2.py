@@ -234,13 +234,17 @@ def test_fsdp2_step_without_chunk_cat_matches_oracle(shapes, nd, gdt, path):
             assert_bits(_host(st["out"]), st["ob"], f"step {t} rank {r} bf16")
 
 
-def test_fsdp2_step_without_chunk_cat_equals_the_chunk_cat_path():
+@pytest.mark.parametrize("nd", [8, 12])
+def test_fsdp2_step_without_chunk_cat_equals_the_chunk_cat_path(nd):
     """On the GPU both compositions give the same bits on one Llama-7B layer
-    group at 8 ranks (a rank's 9 parameters, 25.3M local elements), and the
-    call launches one kernel for all 9 parameters."""
+    group at 8 ranks (a rank's 9 parameters, 25.3M local elements) and at
+    12 (every parameter with padding rows: 18 segments).  One segment table
+    holds them all; at 8 ranks that is the only launch, at 12 the rows that
+    start 2 elements off a 16-byte boundary (after a norm vector's
+    342-element chunk) take the per-parameter fallback."""
     w = W.llama_7b_rank_view()
     shapes = w.units[0]
-    nd, r = 8, 3
+    r = 3
     lay = ss.fsdp2_layout(shapes, nd)
     L = lay.local
     grads = [[torch.empty(s, dtype=torch.bfloat16, device=DEV) for s in shapes] for _ in range(nd)]
@@ -259,8 +263,9 @@ def test_fsdp2_step_without_chunk_cat_equals_the_chunk_cat_path():
     before = ss.launch_count()
     ss.fsdp2_rs_avg_adamw_cast(grads, r, *b, HPC, 1)
     torch.cuda.synchronize()
-    assert ss.launch_count() - before == 1
-    assert ss.last_kernel().startswith("rs_adamw_cast_segs<8, bf16>")
+    if nd == 8:
+        assert ss.launch_count() - before == 1
+    assert ss.last_kernel() == f"rs_adamw_cast_segs<{nd}, bf16> (register-staged, 1 launch)"
     for x, y, name in zip(a, b, ("master", "m", "v", "bf16")):
         assert torch.equal(x.view(torch.uint8), y.view(torch.uint8)), name
 
