@@ -2,7 +2,8 @@
 with element counts up to 2^40 and N_d up to 64 where the oracle's planner
 is arithmetic (the FlatParameter layout, the FSDP2 layout, the DDP bucket
 plan), and on random small units for the checkpoint reshard plan, whose
-oracle walks every element.  CPU only."""
+oracle walks every element; the memory and communication ledgers, plain and
+hybrid, on random Psi up to 2^44.  CPU only."""
 import pytest
 
 import oracle
@@ -65,3 +66,31 @@ def test_ddp_bucket_plan(numels, es, cap):
 def test_reshard_plan(total, old_nd, new_nd, data):
     rank = data.draw(st.integers(0, new_nd - 1))
     assert ck.plan(total, old_nd, new_nd, rank) == ock.plan(total, old_nd, new_nd, rank)
+
+
+PSI = st.one_of(st.integers(1, 1 << 20), st.integers(1, 1 << 44)).map(float)
+
+
+@settings(max_examples=300, deadline=None)
+@given(psi=PSI, nd=ND, stage=st.integers(0, 3),
+       kind=st.sampled_from(["reduce_scatter", "all_gather", "all_reduce", "zero1", "zero2",
+                             "zero3"]),
+       exact=st.booleans())
+def test_memory_and_communication_ledger(psi, nd, stage, kind, exact):
+    assert ss.state_bytes(psi, nd, stage) == pytest.approx(
+        oracle.state_bytes_per_gpu(psi, nd, stage), rel=1e-15)
+    assert ss.comm_bytes(psi, nd, kind, exact) == pytest.approx(
+        oracle.comm_bytes_per_gpu(psi, nd, kind, exact), rel=1e-15)
+
+
+@settings(max_examples=300, deadline=None)
+@given(psi=PSI, groups=st.integers(1, 16), F=st.integers(1, 16),
+       kind=st.sampled_from(["intra", "inter"]), exact=st.booleans())
+def test_hybrid_ledger(psi, groups, F, kind, exact):
+    nd = groups * F
+    if nd > ss.MAX_ND:
+        return
+    assert ss.hybrid_state_bytes(psi, F) == pytest.approx(
+        oracle.hybrid_state_bytes_per_gpu(psi, F), rel=1e-15)
+    assert ss.hybrid_comm_bytes(psi, nd, F, kind, exact) == pytest.approx(
+        oracle.hybrid_comm_bytes_per_gpu(psi, nd, F, kind, exact), rel=1e-15, abs=0)
